@@ -1,0 +1,538 @@
+/*
+ * oracle.c -- plain CPU oracle for tile-based rasterization of projected 2D
+ * Gaussian splats.  TEST INFRASTRUCTURE ONLY: used by tests/, the smoke check
+ * and the benchmark's CPU-baseline leg; never by the product path.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fPIC -shared oracle.c -lm
+ * (-ffp-contract=off matters: the float32 binning below must round after
+ * every operation, exactly as written.)
+ *
+ * The pages (see oracle.h) fix the model's names and shapes but print no
+ * equation.  The readings taken here, each the plainest one consistent with
+ * front-to-back alpha compositing of 2D Gaussians in 16x16 tiles:
+ *   R1 pixel (x, y) is sampled at its centre (x + 0.5, y + 0.5);
+ *   R2 conic (a, b, c) is the inverse covariance [[a, b], [b, c]];
+ *      sigma = (a dx^2 + c dy^2) / 2 + b dx dy,  G = exp(-sigma),  d = p - mean;
+ *   R3 alpha = min(0.99, opacity * G); a splat is skipped at a pixel when
+ *      alpha < 1/255;
+ *   R4 T starts at 1; for each unskipped splat in list order T' = T (1 - alpha);
+ *      if T' < 1e-4 the pixel stops before blending it, else C += rgb alpha T
+ *      and T = T';
+ *   R5 image = C + T_final * bg;
+ *   R6 last_contrib = 1 + list position of the last blended splat (0: none);
+ *   R7 binning: a splat touches the tiles of the AABB of the ellipse where
+ *      alpha >= 1/255 is possible, {d : d^T conic d <= 2 ln(255 o)}, whose
+ *      half widths are sqrt(k c / det), sqrt(k a / det);
+ *   R8 a splat is culled (no pairs) unless every input is finite, depth > 0,
+ *      a > 0, c > 0, det = ac - b^2 > 0, and 1/255 <= opacity (255 o finite);
+ *   R9 pair key = tile << 32 | float bits of depth; list order is (tile,
+ *      depth, splat index) ascending;
+ *   R10 backward: the exact partial derivatives of L = sum dL/dimage * image
+ *      with respect to the stored mean, conic (a, b, c as stored, so db is
+ *      the full partial of the off-diagonal entry), opacity and rgb; through
+ *      the 0.99 clamp the alpha derivative is 0;
+ *   R11 accumulated weight of a splat = sum over pixels of alpha T (the sum;
+ *      an average is the caller's division);
+ *   R12 median depth = depth of the last blended splat whose T before
+ *      blending was > 0.5 (0 when none was blended).
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ALPHA_MIN (1.0 / 255.0)
+#define ALPHA_MAX 0.99
+#define T_EPS 1e-4
+#define MAX_AMB 8
+
+/* Margins of the binning ellipse (R7): k is widened by a relative and an
+ * absolute 2^-10 so that float32 rounding of ln, products and square roots
+ * can never shrink the covered set. */
+#define K_REL (1.0f + 1.0f / 1024.0f)
+#define K_ABS (1.0f / 1024.0f)
+
+/* Unit roundoff of float32: the error model of the GPU's float evaluation
+ * that decides which pixels are knife edges. */
+#define U32 (1.0 / 16777216.0)
+
+void orc_constants(double out[4])
+{
+    out[0] = ALPHA_MIN;
+    out[1] = ALPHA_MAX;
+    out[2] = T_EPS;
+    out[3] = ORC_TILE;
+}
+
+/* ln(x) for a positive, finite, normal float32, in float32 arithmetic:
+ * x = m 2^e with m in [1, 2), ln x = e ln2 + 2 atanh(t), t = (m - 1)/(m + 1)
+ * in [0, 1/3), and atanh(t) = t (1 + t^2/3 + t^4/5 + ... + t^14/15) by
+ * Horner.  The truncated tail is below 2e-9; every operation is one IEEE
+ * rounding, so the result is reproducible anywhere IEEE float32 is. */
+float orc_ln(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    const int e = (int)((u >> 23) & 0xffu) - 127;
+    const uint32_t mu = (u & 0x007fffffu) | 0x3f800000u;
+    float m;
+    memcpy(&m, &mu, 4);
+    const float t = (m - 1.0f) / (m + 1.0f);
+    const float t2 = t * t;
+    float p = 1.0f / 15.0f;
+    p = p * t2 + 1.0f / 13.0f;
+    p = p * t2 + 1.0f / 11.0f;
+    p = p * t2 + 1.0f / 9.0f;
+    p = p * t2 + 1.0f / 7.0f;
+    p = p * t2 + 1.0f / 5.0f;
+    p = p * t2 + 1.0f / 3.0f;
+    p = p * t2 + 1.0f;
+    const float lnm = 2.0f * (t * p);
+    return (float)e * 0.69314718055994531f + lnm;
+}
+
+int orc_splat_rect(const orc_splats_f *s, int64_t i, int32_t W, int32_t H, int32_t r[4])
+{
+    const float mx = s->mean2d[2 * i], my = s->mean2d[2 * i + 1];
+    const float a = s->conic[3 * i], b = s->conic[3 * i + 1], c = s->conic[3 * i + 2];
+    const float o = s->opacity[i], d = s->depth[i];
+    const float *col = s->rgb + 3 * i;
+    if (!isfinite(mx) || !isfinite(my) || !isfinite(a) || !isfinite(b) || !isfinite(c) ||
+        !isfinite(o) || !isfinite(d) || !isfinite(col[0]) || !isfinite(col[1]) ||
+        !isfinite(col[2]))
+        return -1;
+    if (!(d > 0.0f) || !(a > 0.0f) || !(c > 0.0f))
+        return -1;
+    const float det = a * c - b * b;
+    if (!(det > 0.0f))
+        return -1;
+    if (!(o >= (float)ALPHA_MIN))
+        return -1;
+    const float x = 255.0f * o;
+    if (isinf(x))
+        return -1;
+    float k = 2.0f * orc_ln(x);
+    k = k * K_REL + K_ABS;
+    const float rx = sqrtf(k * c / det);
+    const float ry = sqrtf(k * a / det);
+    if (rx != rx || ry != ry)
+        return -1;
+    const int32_t tiles_x = (W + ORC_TILE - 1) / ORC_TILE;
+    const int32_t tiles_y = (H + ORC_TILE - 1) / ORC_TILE;
+    float x0 = floorf((mx - rx) * 0.0625f), x1 = floorf((mx + rx) * 0.0625f);
+    float y0 = floorf((my - ry) * 0.0625f), y1 = floorf((my + ry) * 0.0625f);
+    x0 = fmaxf(x0, 0.0f);
+    y0 = fmaxf(y0, 0.0f);
+    x1 = fminf(x1, (float)(tiles_x - 1));
+    y1 = fminf(y1, (float)(tiles_y - 1));
+    if (x0 > x1 || y0 > y1)
+        return 0;
+    r[0] = (int32_t)x0;
+    r[1] = (int32_t)y0;
+    r[2] = (int32_t)x1;
+    r[3] = (int32_t)y1;
+    return 1;
+}
+
+int64_t orc_bin(const orc_splats_f *s, int32_t W, int32_t H, uint64_t *keys, uint32_t *vals,
+                int64_t capacity, int64_t *culled)
+{
+    const int32_t tiles_x = (W + ORC_TILE - 1) / ORC_TILE;
+    int64_t count = 0, nculled = 0;
+    for (int64_t i = 0; i < s->n; ++i) {
+        int32_t r[4];
+        const int v = orc_splat_rect(s, i, W, H, r);
+        if (v < 0) {
+            ++nculled;
+            continue;
+        }
+        if (v == 0)
+            continue;
+        uint32_t dbits;
+        memcpy(&dbits, &s->depth[i], 4);
+        for (int32_t ty = r[1]; ty <= r[3]; ++ty)
+            for (int32_t tx = r[0]; tx <= r[2]; ++tx) {
+                if (count < capacity) {
+                    const uint64_t tile = (uint64_t)ty * (uint64_t)tiles_x + (uint64_t)tx;
+                    keys[count] = (tile << 32) | dbits;
+                    vals[count] = (uint32_t)i;
+                }
+                ++count;
+            }
+    }
+    if (culled)
+        *culled = nculled;
+    return count;
+}
+
+typedef struct {
+    uint64_t key;
+    uint32_t val;
+} pair_t;
+
+static int cmp_pair(const void *pa, const void *pb)
+{
+    const pair_t *a = pa, *b = pb;
+    if (a->key != b->key)
+        return a->key < b->key ? -1 : 1;
+    if (a->val != b->val)
+        return a->val < b->val ? -1 : 1;
+    return 0;
+}
+
+/* Order of R9: ascending (key, splat index) with the C library's qsort. */
+void orc_sort(uint64_t *keys, uint32_t *vals, int64_t n)
+{
+    if (n <= 0)
+        return;
+    pair_t *p = malloc((size_t)n * sizeof(pair_t));
+    for (int64_t i = 0; i < n; ++i) {
+        p[i].key = keys[i];
+        p[i].val = vals[i];
+    }
+    qsort(p, (size_t)n, sizeof(pair_t), cmp_pair);
+    for (int64_t i = 0; i < n; ++i) {
+        keys[i] = p[i].key;
+        vals[i] = p[i].val;
+    }
+    free(p);
+}
+
+/* CSR ranges: offs[t] = number of pairs whose tile is < t. */
+int orc_offsets(const uint64_t *keys, int64_t n, int32_t n_tiles, uint32_t *offs)
+{
+    memset(offs, 0, sizeof(uint32_t) * ((size_t)n_tiles + 1));
+    for (int64_t i = 0; i < n; ++i) {
+        const uint64_t t = keys[i] >> 32;
+        if (t >= (uint64_t)n_tiles)
+            return -1;
+        offs[t + 1] += 1;
+    }
+    for (int32_t t = 0; t < n_tiles; ++t)
+        offs[t + 1] += offs[t];
+    return 0;
+}
+
+/* ---------------------------------------------------------------- forward */
+
+typedef struct {
+    int64_t pos;       /* position in the tile's list */
+    double alpha, G;
+    double T;          /* transmittance before blending */
+    double mrel;       /* relative error bound of a float32 alpha here */
+    int clamped;
+} blend_rec;
+
+typedef struct {
+    blend_rec *rec;
+    int64_t n;
+    double C[3];
+    double T;          /* T_final */
+    double relT;       /* relative error bound of a float32 product for T */
+    double median;
+    uint32_t last;
+    int n_amb;
+    int64_t amb_pos[MAX_AMB];
+    int amb_kind[MAX_AMB];
+} pix_run;
+
+/* Relative error bound of alpha evaluated in float32 (dx, dy rounded, three
+ * products summed, exp): 32 u times the sum of the magnitudes of sigma's
+ * terms, plus 2^-19 for the exponential.  A decision whose margin is inside
+ * this bound may be taken either way by a float32 evaluation: a knife edge. */
+static double alpha_margin(double a, double b, double c, double dx, double dy)
+{
+    const double terms = 0.5 * fabs(a) * dx * dx + 0.5 * fabs(c) * dy * dy + fabs(b * dx * dy);
+    return 32.0 * U32 * (terms + 1.0) + 1.0 / 524288.0;
+}
+
+static void note_amb(pix_run *r, int64_t pos, int kind)
+{
+    if (r->n_amb < MAX_AMB) {
+        r->amb_pos[r->n_amb] = pos;
+        r->amb_kind[r->n_amb] = kind;
+    }
+    r->n_amb++;
+}
+
+/* Composite one pixel front to back over a tile's list (R1-R6, R12).  When
+ * flip_pos >= 0 the decision of kind flip_kind at that list position is taken
+ * the other way, giving an alternative outcome of a knife-edge pixel. */
+static void run_pixel(const orc_splats_d *s, const uint32_t *list, int64_t len, double px,
+                      double py, int64_t flip_pos, int flip_kind, pix_run *r)
+{
+    r->n = 0;
+    r->C[0] = r->C[1] = r->C[2] = 0.0;
+    r->T = 1.0;
+    r->relT = 0.0;
+    r->median = 0.0;
+    r->last = 0;
+    r->n_amb = 0;
+    for (int64_t k = 0; k < len; ++k) {
+        const int64_t i = list[k];
+        const double a = s->conic[3 * i], b = s->conic[3 * i + 1], c = s->conic[3 * i + 2];
+        const double dx = px - s->mean2d[2 * i], dy = py - s->mean2d[2 * i + 1];
+        const double sigma = 0.5 * (a * dx * dx + c * dy * dy) + b * dx * dy;
+        const double G = exp(-sigma);
+        const double oG = s->opacity[i] * G;
+        const double mrel = alpha_margin(a, b, c, dx, dy);
+
+        int clamped = oG > ALPHA_MAX;
+        if (fabs(oG - ALPHA_MAX) <= mrel * ALPHA_MAX)
+            note_amb(r, k, ORC_AMB_CLAMP);
+        if (k == flip_pos && flip_kind == ORC_AMB_CLAMP)
+            clamped = !clamped;
+        const double alpha = clamped ? ALPHA_MAX : oG;
+
+        int skip = alpha < ALPHA_MIN;
+        if (fabs(alpha - ALPHA_MIN) <= mrel * alpha)
+            note_amb(r, k, ORC_AMB_ALPHA);
+        if (k == flip_pos && flip_kind == ORC_AMB_ALPHA)
+            skip = !skip;
+        if (skip)
+            continue;
+
+        const double Tn = r->T * (1.0 - alpha);
+        const double rel_om = (alpha * mrel + U32) / (1.0 - alpha);
+        int stop = Tn < T_EPS;
+        if (fabs(Tn - T_EPS) <= 4.0 * (r->relT + rel_om + U32) * Tn)
+            note_amb(r, k, ORC_AMB_TERM);
+        if (k == flip_pos && flip_kind == ORC_AMB_TERM)
+            stop = !stop;
+        if (stop)
+            break;
+
+        int med = r->T > 0.5;
+        if (fabs(r->T - 0.5) <= 4.0 * (r->relT + U32) * r->T)
+            note_amb(r, k, ORC_AMB_MEDIAN);
+        if (k == flip_pos && flip_kind == ORC_AMB_MEDIAN)
+            med = !med;
+        if (med)
+            r->median = s->depth[i];
+
+        const double w = alpha * r->T;
+        for (int ch = 0; ch < 3; ++ch)
+            r->C[ch] += s->rgb[3 * i + ch] * w;
+        blend_rec *e = &r->rec[r->n++];
+        e->pos = k;
+        e->alpha = alpha;
+        e->G = G;
+        e->T = r->T;
+        e->mrel = mrel;
+        e->clamped = clamped;
+        r->T = Tn;
+        r->relT += rel_om + U32;
+        r->last = (uint32_t)(k + 1);
+    }
+}
+
+static int64_t max_list(const orc_frame *f, int32_t n_tiles)
+{
+    int64_t m = 1;
+    for (int32_t t = 0; t < n_tiles; ++t) {
+        const int64_t len = (int64_t)f->offs[t + 1] - (int64_t)f->offs[t];
+        if (len > m)
+            m = len;
+    }
+    return m;
+}
+
+int64_t orc_forward(const orc_splats_d *s, const orc_frame *f, orc_fwd_out *out,
+                    orc_alt *alts, int64_t alt_capacity)
+{
+    const int32_t W = f->W, H = f->H;
+    const int32_t tiles_x = (W + ORC_TILE - 1) / ORC_TILE;
+    const int32_t tiles_y = (H + ORC_TILE - 1) / ORC_TILE;
+    const int64_t HW = (int64_t)W * H;
+    const int64_t mlen = max_list(f, tiles_x * tiles_y);
+    pix_run r, r2;
+    r.rec = malloc(sizeof(blend_rec) * (size_t)mlen);
+    r2.rec = malloc(sizeof(blend_rec) * (size_t)mlen);
+    int64_t n_alt = 0;
+    for (int32_t ty = 0; ty < tiles_y; ++ty)
+        for (int32_t tx = 0; tx < tiles_x; ++tx) {
+            const int32_t t = ty * tiles_x + tx;
+            if (f->tile_mask && !f->tile_mask[t])
+                continue;
+            const uint32_t *list = f->vals + f->offs[t];
+            const int64_t len = (int64_t)f->offs[t + 1] - (int64_t)f->offs[t];
+            for (int32_t y = ty * ORC_TILE; y < (ty + 1) * ORC_TILE && y < H; ++y)
+                for (int32_t x = tx * ORC_TILE; x < (tx + 1) * ORC_TILE && x < W; ++x) {
+                    const int64_t p = (int64_t)y * W + x;
+                    run_pixel(s, list, len, x + 0.5, y + 0.5, -1, 0, &r);
+                    if (out->image)
+                        for (int ch = 0; ch < 3; ++ch)
+                            out->image[ch * HW + p] = r.C[ch] + r.T * f->bg[ch];
+                    if (out->T_final)
+                        out->T_final[p] = r.T;
+                    if (out->last)
+                        out->last[p] = r.last;
+                    if (out->median)
+                        out->median[p] = r.median;
+                    if (out->n_amb)
+                        out->n_amb[p] = (uint8_t)(r.n_amb > 255 ? 255 : r.n_amb);
+                    const int na = r.n_amb < MAX_AMB ? r.n_amb : MAX_AMB;
+                    for (int j = 0; j < na; ++j) {
+                        if (alts && n_alt < alt_capacity) {
+                            run_pixel(s, list, len, x + 0.5, y + 0.5, r.amb_pos[j],
+                                      r.amb_kind[j], &r2);
+                            orc_alt *e = &alts[n_alt];
+                            e->pixel = (int32_t)p;
+                            e->kind = r.amb_kind[j];
+                            e->list_pos = (int32_t)r.amb_pos[j];
+                            e->last = r2.last;
+                            for (int ch = 0; ch < 3; ++ch)
+                                e->image[ch] = r2.C[ch] + r2.T * f->bg[ch];
+                            e->T_final = r2.T;
+                            e->median = r2.median;
+                        }
+                        ++n_alt;
+                    }
+                }
+        }
+    free(r.rec);
+    free(r2.rec);
+    return n_alt;
+}
+
+/* --------------------------------------------------------------- backward */
+
+enum { F_MX, F_MY, F_A, F_B, F_C, F_O, F_R, F_G, F_BL, F_W, NF };
+
+/* Gradient contributions of one pixel by the plain definition (R10, R11):
+ * with T_k the transmittance before blended splat k, w_k = alpha_k T_k and
+ * S_k = sum over later blended splats j of rgb_j w_j,
+ *   dL/drgb_k   = g w_k
+ *   dL/dalpha_k = sum_ch g_ch (rgb_k,ch T_k - (S_k,ch + T_final bg_ch) / (1 - alpha_k))
+ *   dL/dsigma_k = -alpha_k dL/dalpha_k         (d alpha / d sigma = -o G)
+ *   dL/do_k     = G_k dL/dalpha_k
+ *   dL/dmean    = dL/dsigma * (-(a dx + b dy), -(b dx + c dy))
+ *   dL/d(a,b,c) = dL/dsigma * (dx^2 / 2, dx dy, dy^2 / 2)
+ * written to out[k][F_*]; out[k][F_W] = w_k. */
+static void pixel_backward(const orc_splats_d *s, const uint32_t *list, const pix_run *r,
+                           double px, double py, const double g[3], const double bg[3],
+                           double *out)
+{
+    double S[3] = {0.0, 0.0, 0.0};
+    for (int64_t k = r->n - 1; k >= 0; --k) {
+        const blend_rec *e = &r->rec[k];
+        const int64_t i = list[e->pos];
+        const double *col = s->rgb + 3 * i;
+        const double w = e->alpha * e->T;
+        double dL_dalpha = 0.0;
+        for (int ch = 0; ch < 3; ++ch)
+            dL_dalpha += g[ch] * (col[ch] * e->T - (S[ch] + r->T * bg[ch]) / (1.0 - e->alpha));
+        double *o = out + NF * k;
+        for (int ch = 0; ch < 3; ++ch)
+            o[F_R + ch] = g[ch] * w;
+        o[F_W] = w;
+        if (!e->clamped) {
+            const double a = s->conic[3 * i], b = s->conic[3 * i + 1], c = s->conic[3 * i + 2];
+            const double dx = px - s->mean2d[2 * i], dy = py - s->mean2d[2 * i + 1];
+            const double dL_dsigma = -e->alpha * dL_dalpha;
+            o[F_MX] = dL_dsigma * -(a * dx + b * dy);
+            o[F_MY] = dL_dsigma * -(b * dx + c * dy);
+            o[F_A] = dL_dsigma * 0.5 * dx * dx;
+            o[F_B] = dL_dsigma * dx * dy;
+            o[F_C] = dL_dsigma * 0.5 * dy * dy;
+            o[F_O] = dL_dalpha * e->G;
+        } else {
+            for (int q = F_MX; q <= F_O; ++q)
+                o[q] = 0.0;
+        }
+        for (int ch = 0; ch < 3; ++ch)
+            S[ch] += col[ch] * w;
+    }
+}
+
+static void add_fields(orc_grads *gr, int64_t i, const double *v, int absval)
+{
+#define ACC(dst, x) ((dst) += absval ? fabs(x) : (x))
+    ACC(gr->dmean2d[2 * i], v[F_MX]);
+    ACC(gr->dmean2d[2 * i + 1], v[F_MY]);
+    ACC(gr->dconic[3 * i], v[F_A]);
+    ACC(gr->dconic[3 * i + 1], v[F_B]);
+    ACC(gr->dconic[3 * i + 2], v[F_C]);
+    ACC(gr->dopacity[i], v[F_O]);
+    ACC(gr->drgb[3 * i], v[F_R]);
+    ACC(gr->drgb[3 * i + 1], v[F_G]);
+    ACC(gr->drgb[3 * i + 2], v[F_BL]);
+    if (gr->accum)
+        ACC(gr->accum[i], v[F_W]);
+#undef ACC
+}
+
+/* Accumulates (+=) into grads; the caller zeroes them.  slack (may be NULL)
+ * receives, per splat and field, the sum over knife-edge decisions of
+ * |alternative - normal| contribution.  accum_err (may be NULL) receives a
+ * bound on the error of a float32 evaluation of the accumulated weight:
+ * per blended pixel w (2 relT + mrel + 4 u (n + 2)) + 2^-32. */
+int orc_backward(const orc_splats_d *s, const orc_frame *f, const double *dL_dimage,
+                 orc_grads *grads, orc_grads *slack, double *accum_err)
+{
+    const int32_t W = f->W, H = f->H;
+    const int32_t tiles_x = (W + ORC_TILE - 1) / ORC_TILE;
+    const int32_t tiles_y = (H + ORC_TILE - 1) / ORC_TILE;
+    const int64_t HW = (int64_t)W * H;
+    const int64_t mlen = max_list(f, tiles_x * tiles_y);
+    pix_run r, r2;
+    r.rec = malloc(sizeof(blend_rec) * (size_t)mlen);
+    r2.rec = malloc(sizeof(blend_rec) * (size_t)mlen);
+    double *c1 = malloc(sizeof(double) * NF * (size_t)mlen);
+    double *c2 = malloc(sizeof(double) * NF * (size_t)mlen);
+    double *byp1 = calloc((size_t)mlen * NF, sizeof(double));
+    double *byp2 = calloc((size_t)mlen * NF, sizeof(double));
+    for (int32_t ty = 0; ty < tiles_y; ++ty)
+        for (int32_t tx = 0; tx < tiles_x; ++tx) {
+            const int32_t t = ty * tiles_x + tx;
+            if (f->tile_mask && !f->tile_mask[t])
+                continue;
+            const uint32_t *list = f->vals + f->offs[t];
+            const int64_t len = (int64_t)f->offs[t + 1] - (int64_t)f->offs[t];
+            for (int32_t y = ty * ORC_TILE; y < (ty + 1) * ORC_TILE && y < H; ++y)
+                for (int32_t x = tx * ORC_TILE; x < (tx + 1) * ORC_TILE && x < W; ++x) {
+                    const int64_t p = (int64_t)y * W + x;
+                    const double g[3] = {dL_dimage[p], dL_dimage[HW + p], dL_dimage[2 * HW + p]};
+                    const double px = x + 0.5, py = y + 0.5;
+                    run_pixel(s, list, len, px, py, -1, 0, &r);
+                    pixel_backward(s, list, &r, px, py, g, f->bg, c1);
+                    for (int64_t k = 0; k < r.n; ++k) {
+                        const int64_t i = list[r.rec[k].pos];
+                        add_fields(grads, i, c1 + NF * k, 0);
+                        if (accum_err) {
+                            const double relw = 2.0 * r.relT + r.rec[k].mrel +
+                                                4.0 * U32 * (double)(r.n + 2);
+                            accum_err[i] += c1[NF * k + F_W] * relw + 1.0 / 4294967296.0;
+                        }
+                    }
+                    if (!slack || r.n_amb == 0)
+                        continue;
+                    /* Contributions by list position, normal vs each alternative. */
+                    const int na = r.n_amb < MAX_AMB ? r.n_amb : MAX_AMB;
+                    for (int j = 0; j < na; ++j) {
+                        run_pixel(s, list, len, px, py, r.amb_pos[j], r.amb_kind[j], &r2);
+                        pixel_backward(s, list, &r2, px, py, g, f->bg, c2);
+                        memset(byp1, 0, sizeof(double) * NF * (size_t)len);
+                        memset(byp2, 0, sizeof(double) * NF * (size_t)len);
+                        for (int64_t k = 0; k < r.n; ++k)
+                            memcpy(byp1 + NF * r.rec[k].pos, c1 + NF * k, sizeof(double) * NF);
+                        for (int64_t k = 0; k < r2.n; ++k)
+                            memcpy(byp2 + NF * r2.rec[k].pos, c2 + NF * k, sizeof(double) * NF);
+                        for (int64_t q = 0; q < len; ++q) {
+                            double d[NF];
+                            for (int fld = 0; fld < NF; ++fld)
+                                d[fld] = byp2[NF * q + fld] - byp1[NF * q + fld];
+                            add_fields(slack, list[q], d, 1);
+                        }
+                    }
+                }
+        }
+    free(r.rec);
+    free(r2.rec);
+    free(c1);
+    free(c2);
+    free(byp1);
+    free(byp2);
+    return 0;
+}
