@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Benchmark of the splat rasterization path on the 2M-splat, 1237x822 workload.
+
+One step = the whole path over one scene: tile binning, pair count (one
+host read), onesweep sort + tile ranges, forward, backward.  Prints one JSON
+line (rank 0).  Under torchrun each rank runs an independent replica (the path
+does not shard across GPUs here); value = all ranks' candidate splat-pixel
+pairs / the slowest rank's time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (test infrastructure) on the host
+cores, on a bounded sample of the same workload, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "rasterize_bwd ms/call and splat-pixel pairs/s at 2M splats 1237×822; % roofline"
+UNIT = "splat-px pairs/s"
+WORKLOAD = 4
+L2_FLUSH_BYTES = 256 << 20
+BWD_SOURCES = ("gaussian_splatting_differentiable_gb300/csrc/ss_bwd.cu",
+               "gaussian_splatting_differentiable_gb300/csrc/ss_device.cuh")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def candidate_pairs(offs: np.ndarray, W: int, H: int) -> int:
+    """sum over tiles of (pairs of the tile) x (pixels of the tile inside the image)."""
+    tx, ty = (W + 15) // 16, (H + 15) // 16
+    per = np.diff(offs.astype(np.int64)).reshape(ty, tx)
+    wx = np.minimum(16, W - 16 * np.arange(tx))
+    wy = np.minimum(16, H - 16 * np.arange(ty))
+    return int((per * wy[:, None] * wx[None, :]).sum())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [r for (t, r) in self.rows if self.t0 is not None and self.t0 - 0.06 <= t <= (self.t1 or t) + 0.06]
+        if not rows:
+            rows = [r for (_, r) in self.rows]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[2]))
+                mx.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names, r[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(scene, n_tiles: int, seed: int = 0):
+    """Time the oracle: full binning and sort, forward + backward on n_tiles
+    random tiles; returns (seconds extrapolated to the whole step, details)."""
+    import oracle
+    t0 = time.perf_counter()
+    keys, vals, count, _ = oracle.bin_tiles(scene)
+    t1 = time.perf_counter()
+    keys, vals = oracle.sort_pairs(keys, vals)
+    tx, ty = oracle.tiles_xy(scene.W, scene.H)
+    offs = oracle.offsets(keys, tx * ty)
+    t2 = time.perf_counter()
+    rng = np.random.default_rng(seed)
+    mask = np.zeros(tx * ty, np.uint8)
+    mask[rng.choice(tx * ty, n_tiles, replace=False)] = 1
+    t3 = time.perf_counter()
+    oracle.forward(scene, vals, offs, tile_mask=mask)
+    oracle.backward(scene, vals, offs, tile_mask=mask, slack=False)
+    t4 = time.perf_counter()
+    full = candidate_pairs(offs, scene.W, scene.H)
+    per = np.diff(offs.astype(np.int64))
+    wx = np.minimum(16, scene.W - 16 * (np.arange(tx * ty) % tx))
+    wy = np.minimum(16, scene.H - 16 * (np.arange(tx * ty) // tx))
+    sample = int((per * wx * wy)[mask.astype(bool)].sum())
+    t_step = (t1 - t0) + (t2 - t1) + (t4 - t3) * full / max(sample, 1)
+    return t_step, {"bin_s": t1 - t0, "sort_s": t2 - t1, "raster_sample_s": t4 - t3,
+                    "sample_candidates": sample, "full_candidates": full, "measured_s": t4 - t0}
+
+
+def run_reference(args, rank: int):
+    import synth
+    if rank != 0:
+        return
+    scene = synth.make_scene(args.workload)
+    n_tiles = 6
+    times, det = [], None
+    for k in range(args.warmup + args.steps):
+        t, det = oracle_sample(scene, n_tiles, seed=k)
+        if k >= args.warmup:
+            times.append(t)
+    t = statistics.mean(times)
+    value = det["full_candidates"] / t
+    sample = ("per step: full binning and sort of the %d-splat scene, forward+backward on %d "
+              "random 16x16 tiles (%d candidate pairs), raster time scaled to all %d candidate "
+              "pairs" % (scene.n, n_tiles, det["sample_candidates"], det["full_candidates"]))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": synth.WORKLOADS[args.workload].name, "W": scene.W, "H": scene.H,
+                       "splats": scene.n},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def source_sha(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        rec = json.load(open(p)).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha") != source_sha(BWD_SOURCES):
+        return None
+    return rec.get("dram_bytes_per_launch_full")
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return {}
+
+
+def run_ours(args, rank: int, world: int, dist):
+    import torch
+    try:
+        import gaussian_splatting_differentiable_gb300 as ss
+    except ImportError:
+        import __graft_entry__
+        __graft_entry__.build()
+        import gaussian_splatting_differentiable_gb300 as ss
+    import synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    scene = synth.make_scene(args.workload)
+    wl = synth.WORKLOADS[args.workload]
+    flags = (ss.SS_ACCUM_WEIGHT if scene.accum_weight else 0) | \
+        (ss.SS_MEDIAN_DEPTH if scene.median_depth else 0)
+    sp = ss.Splats.from_numpy(scene, dev)
+    dL = torch.from_numpy(scene.dL_dimage).to(dev).contiguous()
+    r = ss.Rasterizer(scene.W, scene.H, scene.n, int(2.5 * scene.n), flags, bg=scene.bg,
+                      device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(args.warmup):
+        r.step(sp, dL)
+    torch.cuda.synchronize()
+    assert ss.ss_sort_status(r.workspace) == ss.SS_OK
+    offs = r.tile_offsets.cpu().numpy().view(np.uint32)
+    cand = candidate_pairs(offs, scene.W, scene.H)
+    active = int(r.last_contrib.sum().item())
+    P = r.n_pairs
+
+    # --- device-resident timed region
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    ss.ss_profile_collect()
+    ss.ss_profile_enable(True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(float(k))           # > L2: every step starts cold
+        ev[k][0].record(stream)
+        r.step(sp, dL)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    if dist:
+        dist.barrier()
+    clocks.mark(False)
+    ss.ss_profile_enable(False)
+    prof = ss.ss_profile_collect()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(step_ms)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * cand / (ms * 1e-3)
+    launches = sum(c for (c, _, _, _) in prof.values())
+
+    kernels = {k: {"launches": c, "ms_per_call": tot / c, "ms_total": tot, "min_ms": mn,
+                   "max_ms": mx} for k, (c, tot, mn, mx) in prof.items()}
+    stages = {
+        "tile isect (bin+sort)": sum(v["ms_total"] for k, v in kernels.items()
+                                     if k.startswith(("k_emit", "k_sort"))) / args.steps,
+        "raster fwd": kernels.get("k_raster_fwd", {}).get("ms_total", 0.0) / args.steps,
+        "raster bwd": sum(v["ms_total"] for k, v in kernels.items()
+                          if k in ("k_bwd_zero", "k_raster_bwd", "k_accum_final")) / args.steps,
+    }
+    k_total = sum(v["ms_total"] for v in kernels.values())
+    dom = max(kernels, key=lambda k: kernels[k]["ms_total"])
+    for v in kernels.values():
+        v["share"] = v["ms_total"] / k_total
+
+    # --- roofline of the backward kernel (and of the dominant kernel)
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs")
+    hbm_src = "measured" if hbm else "fallback"
+    hbm = hbm or 6800.0
+    HW = scene.W * scene.H
+    bwd_bytes = 40 * P + 20 * HW + (36 + (8 if scene.accum_weight else 0)) * scene.n
+    bwd_ms = kernels["k_raster_bwd"]["ms_per_call"]
+    achieved = bwd_bytes / (bwd_ms * 1e-3) / 1e9
+    # L2 atomic throughput: distinct-address float reductions
+    probe = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ss.ss_probe_red_f32(probe, 1)
+    torch.cuda.synchronize()
+    rounds = 4
+    e0.record(stream)
+    ss.ss_probe_red_f32(probe, rounds)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    red_rate = probe.numel() * rounds / (e0.elapsed_time(e1) * 1e-3)
+    del probe
+    n_atomics = (10 if scene.accum_weight else 9) * P
+    t_atom = n_atomics / red_rate
+    t_hbm = bwd_bytes / (hbm * 1e9)
+    roofline = {"kernel": "k_raster_bwd", "bound": "hbm", "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": achieved / hbm, "traffic": recorded_traffic("k_raster_bwd"),
+                "peak_source": hbm_src + " (MEASURED_PEAKS.json hbm_gbs, copy test)",
+                "algorithmic_bytes": bwd_bytes,
+                "bytes_model": "40 B/pair (index + 36 B splat gather) + 20 B/pixel "
+                               "(dL 12, T 4, last 4) + %d B/splat (gradients%s)" % (
+                                   36 + (8 if scene.accum_weight else 0),
+                                   " + 8 B fixed-point weight" if scene.accum_weight else "")}
+    roofline_atomic = {"kernel": "k_raster_bwd", "bound": "l2_atomic",
+                       "achieved": n_atomics / (bwd_ms * 1e-3), "peak": red_rate, "unit": "atomic/s",
+                       "frac": (n_atomics / (bwd_ms * 1e-3)) / red_rate,
+                       "count_model": "%d per (splat, tile) pair = method minimum" % (
+                           10 if scene.accum_weight else 9),
+                       "peak_source": "measured here: red.global.add.f32, 64M distinct addresses"}
+    hbm_atomic_frac = max(t_hbm, t_atom) / (bwd_ms * 1e-3)
+
+    # --- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: torch.from_numpy(getattr(scene, k)).pin_memory()
+                   for k in ("mean2d", "conic", "opacity", "rgb", "depth")}
+        host_dL = torch.from_numpy(scene.dL_dimage).pin_memory()
+        dev_in = ss.Splats(**{k: torch.empty_like(v, device=dev) for k, v in host_in.items()})
+        dev_dL = torch.empty_like(host_dL, device=dev)
+        outs = [r.image, *r.grads.values()] + ([r.accum_weight] if r.accum_weight is not None else [])
+        host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        bi = sum(v.numel() * v.element_size() for v in host_in.values()) + \
+            host_dL.numel() * host_dL.element_size()
+        bo = sum(o.numel() * o.element_size() for o in host_out)
+        n_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            for k, v in host_in.items():
+                getattr(dev_in, k).copy_(v, non_blocking=True)
+            dev_dL.copy_(host_dL, non_blocking=True)
+            r.step(dev_in, dev_dL)
+            for h, o in zip(host_out, outs):
+                h.copy_(o, non_blocking=True)
+            torch.cuda.synchronize()
+        e2e_step()
+        e2e_ms = []
+        for _ in range(n_e2e):
+            flush.fill_(0.0)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e2e_step()
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+        em = statistics.mean(e2e_ms)
+        if dist:
+            t = torch.tensor([em], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            em = float(t.item())
+        e2e = {"value": world * cand / (em * 1e-3), "unit": UNIT, "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo, "ms_per_step": em, "steps": n_e2e,
+               "how": "pinned host inputs -> device, bin/count/sort/fwd/bwd, gradients + image + "
+                      "weights -> pinned host, synchronize; wall clock"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_tiles = 12
+        t_step, det = oracle_sample(scene, n_tiles)
+        cpu = {"value": det["full_candidates"] / t_step, "unit": UNIT, "cores": 1,
+               "kind": "oracle",
+               "sample": "full binning + sort of the scene, forward+backward on %d random tiles "
+                         "(%d of %d candidate pairs) scaled to the whole step; %.1f s measured" % (
+                             n_tiles, det["sample_candidates"], det["full_candidates"],
+                             det["measured_s"])}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "W": scene.W, "H": scene.H, "splats": scene.n,
+                   "pairs": P, "candidate_splat_px": cand, "blended_px_splat": active,
+                   "flags": {"accum_weight": scene.accum_weight, "median_depth": scene.median_depth},
+                   "l2": "256 MB buffer written between timed steps (L2 is 129 MB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "rasterize_bwd_ms_per_call": bwd_ms,
+        "rasterize_bwd_pairs_per_s": cand / (bwd_ms * 1e-3),
+        "stages_ms_per_step": stages,
+        "kernels": kernels, "dominant_kernel": dom,
+        "roofline": roofline, "roofline_atomic": roofline_atomic,
+        "bwd_hbm_atomic_roofline_frac": hbm_atomic_frac,
+        "l2_red_f32_per_s": red_rate,
+        "gpu_launches": launches,
+        "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+        "wall_ms_per_step": (wall1 - wall0) * 1e3 / args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist = tdist
+    try:
+        run_ours(args, rank, world, dist)
+    finally:
+        if dist:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

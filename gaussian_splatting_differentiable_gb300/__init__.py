@@ -1,0 +1,253 @@
+"""Tile-based differentiable rasterization of projected 2D Gaussian splats on GB300.
+
+The compute path is libss.so (hand-written CUDA for sm_103a behind the C ABI
+of include/ss.h).  This module is its thin Python binding: each ss_* function
+here has the C function's name and arguments and only marshals torch tensors
+(device memory) and streams into pointers.  PyTorch provides memory and
+streams; every step of the path runs in the library's kernels.  There is no
+fallback: importing this package without the built library raises
+ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+
+import torch
+
+from . import _lib
+from ._lib import (SS_ACCUM_WEIGHT, SS_ERR_CAPACITY, SS_MEDIAN_DEPTH, SS_OK,  # noqa: F401
+                   STATUS_NAMES, SsGrads, SsSplats)
+
+_L = _lib.load()
+TILE = 16
+
+
+class SSError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = _L.ss_last_error().decode(errors="replace")
+        super().__init__("%s: %s: %s" % (where, STATUS_NAMES.get(status, status), msg))
+        self.status = status
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int, where: str):
+    if st != SS_OK:
+        raise SSError(st, where)
+
+
+def _f32_host3(bg):
+    if bg is None:
+        return None
+    return (ctypes.c_float * 3)(*[float(x) for x in bg])
+
+
+@dataclasses.dataclass
+class Splats:
+    """Device SoA splats (float32, contiguous): mean2d [n,2], conic [n,3],
+    opacity [n], rgb [n,3], depth [n]."""
+    mean2d: torch.Tensor
+    conic: torch.Tensor
+    opacity: torch.Tensor
+    rgb: torch.Tensor
+    depth: torch.Tensor
+
+    @property
+    def n(self) -> int:
+        return int(self.opacity.shape[0])
+
+    def c(self) -> SsSplats:
+        for k in ("mean2d", "conic", "opacity", "rgb", "depth"):
+            t = getattr(self, k)
+            if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+                raise ValueError("Splats.%s must be a contiguous float32 CUDA tensor" % k)
+        return SsSplats(_ptr(self.mean2d), _ptr(self.conic), _ptr(self.opacity), _ptr(self.rgb),
+                        _ptr(self.depth), self.n)
+
+    @staticmethod
+    def from_numpy(scene, device="cuda") -> "Splats":
+        f = lambda a: torch.from_numpy(a).to(device=device, dtype=torch.float32).contiguous()  # noqa
+        return Splats(f(scene.mean2d), f(scene.conic), f(scene.opacity), f(scene.rgb),
+                      f(scene.depth))
+
+
+# ------------------------------------------------------------------ C ABI
+
+def ss_abi_version() -> int:
+    return int(_L.ss_abi_version())
+
+
+def ss_constants() -> dict:
+    buf = (ctypes.c_float * 4)()
+    _L.ss_constants(buf)
+    return {"alpha_min": buf[0], "alpha_max": buf[1], "T_eps": buf[2], "tile": int(buf[3])}
+
+
+def ss_last_error() -> str:
+    return _L.ss_last_error().decode(errors="replace")
+
+
+def ss_workspace_bytes(n_splats: int, n_pairs: int, W: int, H: int) -> int:
+    return int(_L.ss_workspace_bytes(n_splats, n_pairs, W, H))
+
+
+def ss_bin_tiles(splats: Splats, W: int, H: int, keys, vals, capacity: int, counters,
+                 stream=None) -> None:
+    s = splats.c()
+    _check(_L.ss_bin_tiles(ctypes.byref(s), W, H, _ptr(keys), _ptr(vals), capacity,
+                           _ptr(counters), _stream(stream)), "ss_bin_tiles")
+
+
+def ss_pair_count(counters, capacity: int, stream=None):
+    """(status, pairs needed, culled); status is SS_OK or SS_ERR_CAPACITY."""
+    pairs, culled = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = _L.ss_pair_count(_ptr(counters), capacity, ctypes.byref(pairs), ctypes.byref(culled),
+                          _stream(stream))
+    if st not in (SS_OK, SS_ERR_CAPACITY):
+        raise SSError(st, "ss_pair_count")
+    return st, pairs.value, culled.value
+
+
+def ss_sort_pairs(keys, vals, n_pairs: int, W: int, H: int, tile_offsets, workspace,
+                  stream=None) -> None:
+    _check(_L.ss_sort_pairs(_ptr(keys), _ptr(vals), n_pairs, W, H, _ptr(tile_offsets),
+                            _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            _stream(stream)), "ss_sort_pairs")
+
+
+def ss_sort_status(workspace, stream=None) -> int:
+    return int(_L.ss_sort_status(_ptr(workspace), _stream(stream)))
+
+
+def ss_raster_fwd(splats: Splats, vals, tile_offsets, W: int, H: int, bg, flags: int, image,
+                  T_final, last_contrib, median_depth=None, stream=None) -> None:
+    s = splats.c()
+    _check(_L.ss_raster_fwd(ctypes.byref(s), _ptr(vals), _ptr(tile_offsets), W, H,
+                            _f32_host3(bg), flags, _ptr(image), _ptr(T_final),
+                            _ptr(last_contrib), _ptr(median_depth), _stream(stream)),
+           "ss_raster_fwd")
+
+
+def ss_raster_bwd(splats: Splats, vals, tile_offsets, W: int, H: int, bg, flags: int, T_final,
+                  last_contrib, dL_dimage, grads: dict, accum_weight, workspace,
+                  stream=None) -> None:
+    s = splats.c()
+    g = SsGrads(_ptr(grads["dmean2d"]), _ptr(grads["dconic"]), _ptr(grads["dopacity"]),
+                _ptr(grads["drgb"]))
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_L.ss_raster_bwd(ctypes.byref(s), _ptr(vals), _ptr(tile_offsets), W, H,
+                            _f32_host3(bg), flags, _ptr(T_final), _ptr(last_contrib),
+                            _ptr(dL_dimage), ctypes.byref(g), _ptr(accum_weight),
+                            _ptr(workspace), nbytes, _stream(stream)), "ss_raster_bwd")
+
+
+def ss_profile_enable(on: bool) -> None:
+    _L.ss_profile_enable(1 if on else 0)
+
+
+def ss_profile_collect() -> dict:
+    """{kernel name: (launches, total_ms, min_ms, max_ms)} since the last collect."""
+    n = _L.ss_profile_collect(None, 0)
+    buf = ctypes.create_string_buffer(int(n) + 1)
+    _L.ss_profile_collect(buf, len(buf))
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, cnt, tot, mn, mx = line.split()
+        out[name] = (int(cnt), float(tot), float(mn), float(mx))
+    return out
+
+
+def ss_probe_red_f32(buf, rounds: int, stream=None) -> None:
+    _check(_L.ss_probe_red_f32(_ptr(buf), buf.numel(), rounds, _stream(stream)),
+           "ss_probe_red_f32")
+
+
+# ------------------------------------------------------------------ whole path
+
+class Rasterizer:
+    """Buffers for one image size and splat count, reused across calls, and
+    the call sequence bin -> pair count -> sort -> forward / backward.
+
+    Pair buffers grow (once) when the binning reports more pairs than their
+    capacity; nothing else is allocated after construction."""
+
+    def __init__(self, W: int, H: int, n_splats: int, pair_capacity: int, flags: int = 0,
+                 bg=None, device="cuda"):
+        self.W, self.H, self.n, self.flags = W, H, n_splats, flags
+        self.bg = None if bg is None else [float(x) for x in bg]
+        self.device = torch.device(device)
+        self.tiles = ((W + TILE - 1) // TILE) * ((H + TILE - 1) // TILE)
+        d = self.device
+        self.counters = torch.zeros(2, dtype=torch.int64, device=d)
+        self.tile_offsets = torch.zeros(self.tiles + 1, dtype=torch.int32, device=d)
+        self._alloc_pairs(max(int(pair_capacity), 1))
+        self.image = torch.empty(3, H, W, dtype=torch.float32, device=d)
+        self.T_final = torch.empty(H, W, dtype=torch.float32, device=d)
+        self.last_contrib = torch.empty(H, W, dtype=torch.int32, device=d)
+        self.median_depth = (torch.empty(H, W, dtype=torch.float32, device=d)
+                             if flags & SS_MEDIAN_DEPTH else None)
+        self.grads = {"dmean2d": torch.empty(n_splats, 2, dtype=torch.float32, device=d),
+                      "dconic": torch.empty(n_splats, 3, dtype=torch.float32, device=d),
+                      "dopacity": torch.empty(n_splats, dtype=torch.float32, device=d),
+                      "drgb": torch.empty(n_splats, 3, dtype=torch.float32, device=d)}
+        self.accum_weight = (torch.empty(n_splats, dtype=torch.float32, device=d)
+                             if flags & SS_ACCUM_WEIGHT else None)
+        self.n_pairs = 0
+        self.culled = 0
+
+    def _alloc_pairs(self, cap: int):
+        d = self.device
+        self.capacity = cap
+        self.keys = torch.empty(cap, dtype=torch.int64, device=d)
+        self.vals = torch.empty(cap, dtype=torch.int32, device=d)
+        ws = ss_workspace_bytes(self.n, cap, self.W, self.H)
+        if ws == 0:
+            raise ValueError("sizes out of range")
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=d)
+
+    def bin_and_sort(self, splats: Splats, stream=None) -> int:
+        """Tile lists of `splats`; returns the number of pairs (one host sync)."""
+        ss_bin_tiles(splats, self.W, self.H, self.keys, self.vals, self.capacity, self.counters,
+                     stream)
+        st, pairs, culled = ss_pair_count(self.counters, self.capacity, stream)
+        if st == SS_ERR_CAPACITY:
+            self._alloc_pairs(int(pairs * 1.25) + 1024)
+            ss_bin_tiles(splats, self.W, self.H, self.keys, self.vals, self.capacity,
+                         self.counters, stream)
+            st, pairs, culled = ss_pair_count(self.counters, self.capacity, stream)
+            _check(st, "ss_pair_count")
+        self.n_pairs, self.culled = pairs, culled
+        ss_sort_pairs(self.keys, self.vals, pairs, self.W, self.H, self.tile_offsets,
+                      self.workspace, stream)
+        return pairs
+
+    def forward(self, splats: Splats, stream=None) -> None:
+        ss_raster_fwd(splats, self.vals, self.tile_offsets, self.W, self.H, self.bg, self.flags,
+                      self.image, self.T_final, self.last_contrib, self.median_depth, stream)
+
+    def backward(self, splats: Splats, dL_dimage: torch.Tensor, stream=None) -> None:
+        ss_raster_bwd(splats, self.vals, self.tile_offsets, self.W, self.H, self.bg, self.flags,
+                      self.T_final, self.last_contrib, dL_dimage, self.grads, self.accum_weight,
+                      self.workspace, stream)
+
+    def step(self, splats: Splats, dL_dimage: torch.Tensor, stream=None) -> int:
+        """One pass of the whole path: bin, sort, forward, backward."""
+        n = self.bin_and_sort(splats, stream)
+        self.forward(splats, stream)
+        self.backward(splats, dL_dimage, stream)
+        return n

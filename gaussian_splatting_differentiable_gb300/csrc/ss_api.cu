@@ -1,0 +1,147 @@
+// Shared pieces of the C ABI: error strings, constants, workspace sizing,
+// the pair-count read-back, the sort status read-back and the atomic probe.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "ss_device.cuh"
+#include "ss_internal.h"
+#include "ss_profile.h"
+
+namespace ss {
+
+static thread_local char g_err[512];
+
+ss_status fail(ss_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+void clear_error() { g_err[0] = 0; }
+
+ss_status check_cuda(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return SS_OK;
+    return fail(SS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+ss_status check_launch(const char *what) { return check_cuda(cudaGetLastError(), what); }
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H) {
+    WsLayout L{};
+    const int64_t tiles = int64_t(tiles_x(W)) * tiles_y(H);
+    L.ndig = sort_digits(tiles);
+    L.nparts = (n_pairs + kSortPart - 1) / kSortPart;
+    size_t off = 0;
+    L.status_word = off;
+    off += 256;
+    L.hist = off;
+    off = align256(off + size_t(L.ndig) * 256 * 4);
+    L.gofs = off;
+    off = align256(off + size_t(L.ndig) * 256 * 4);
+    L.tickets = off;
+    off = align256(off + 8 * 4);
+    L.lookback = off;
+    off = align256(off + size_t(L.ndig) * size_t(L.nparts) * 256 * 8);
+    L.zero_end = off;
+    L.alt_keys = off;
+    off = align256(off + size_t(n_pairs) * 8);
+    L.alt_vals = off;
+    off = align256(off + size_t(n_pairs) * 4);
+    L.sort_end = off;
+    L.accum = 256;  // after the status word; the sort's regions are dead by then
+    L.bwd_end = align256(L.accum + size_t(n_splats) * 8);
+    L.total = L.sort_end > L.bwd_end ? L.sort_end : L.bwd_end;
+    return L;
+}
+
+// Measurement probe: rounds of red.global.add.f32, consecutive threads on
+// consecutive addresses, grid-stride over n.
+__global__ void k_probe_red(float *buf, int64_t n, int32_t rounds) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int32_t r = 0; r < rounds; ++r)
+        for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+            atomicAdd(buf + i, 1.0f);
+}
+
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" {
+
+int32_t ss_abi_version(void) { return 1; }
+
+void ss_constants(float out[4]) {
+    out[0] = kAlphaMin;
+    out[1] = kAlphaMax;
+    out[2] = kTEps;
+    out[3] = float(kTile);
+}
+
+const char *ss_last_error(void) { return g_err; }
+
+size_t ss_workspace_bytes(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H) {
+    if (n_splats < 0 || n_pairs < 0 || n_pairs > int64_t(0xffffffffu) || W < 1 || H < 1 ||
+        W > kMaxSide || H > kMaxSide)
+        return 0;
+    return ws_layout(n_splats, n_pairs, W, H).total;
+}
+
+ss_status ss_pair_count(const uint64_t *d_counters, int64_t capacity, int64_t *h_pairs,
+                        int64_t *h_culled, ss_stream_t stream) {
+    clear_error();
+    if (!d_counters) return fail(SS_ERR_INVALID_ARG, "ss_pair_count: d_counters is NULL");
+    if (capacity < 0) return fail(SS_ERR_INVALID_ARG, "ss_pair_count: capacity < 0");
+    unsigned long long h[2] = {0, 0};
+    ss_status st = check_cuda(
+        cudaMemcpyAsync(h, d_counters, sizeof h, cudaMemcpyDeviceToHost, (cudaStream_t)stream),
+        "ss_pair_count: cudaMemcpyAsync");
+    if (st != SS_OK) return st;
+    st = check_cuda(cudaStreamSynchronize((cudaStream_t)stream), "ss_pair_count: synchronize");
+    if (st != SS_OK) return st;
+    if (h_pairs) *h_pairs = int64_t(h[0]);
+    if (h_culled) *h_culled = int64_t(h[1]);
+    if (int64_t(h[0]) > capacity)
+        return fail(SS_ERR_CAPACITY, "ss_pair_count: %lld pairs needed, capacity %lld",
+                    (long long)h[0], (long long)capacity);
+    return SS_OK;
+}
+
+ss_status ss_sort_status(const void *workspace, ss_stream_t stream) {
+    clear_error();
+    if (!workspace) return fail(SS_ERR_INVALID_ARG, "ss_sort_status: workspace is NULL");
+    uint32_t word = 0;
+    ss_status st = check_cuda(cudaMemcpyAsync(&word, workspace, 4, cudaMemcpyDeviceToHost,
+                                              (cudaStream_t)stream),
+                              "ss_sort_status: cudaMemcpyAsync");
+    if (st != SS_OK) return st;
+    st = check_cuda(cudaStreamSynchronize((cudaStream_t)stream), "ss_sort_status: synchronize");
+    if (st != SS_OK) return st;
+    if (word & kDevErrTimeout)
+        return fail(SS_ERR_TIMEOUT, "ss_sort_pairs: a look-back wait gave up (status 0x%x)", word);
+    if (word & kDevErrKeyRange)
+        return fail(SS_ERR_DEVICE, "ss_sort_pairs: a key's tile id is >= the tile count (status 0x%x)",
+                    word);
+    return SS_OK;
+}
+
+ss_status ss_probe_red_f32(float *buf, int64_t n, int32_t rounds, ss_stream_t stream) {
+    clear_error();
+    if (!buf || n < 1 || rounds < 0)
+        return fail(SS_ERR_INVALID_ARG, "ss_probe_red_f32: bad buffer, size or rounds");
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (n + 255) / 256;
+    const int grid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+    SS_LAUNCH("k_probe_red", (cudaStream_t)stream,
+              k_probe_red<<<grid, 256, 0, (cudaStream_t)stream>>>(buf, n, rounds));
+    return check_launch("ss_probe_red_f32");
+}
+
+}  // extern "C"

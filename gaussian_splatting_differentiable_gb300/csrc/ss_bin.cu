@@ -1,0 +1,95 @@
+// Tile binning ("Phase 5 step 30b -- kernel-by-kernel timing", emit_pairs:
+// tile id computation plus an atomic counter update).
+//
+// One thread per splat computes its tile rectangle; the warp sums its pair
+// counts with shuffles and lane 31 takes the warp's slots with a single
+// 64-bit atomic add, so the global counter sees one atomic per warp rather
+// than one per splat.  Each lane then writes its pairs into its slots.
+#include "ss_device.cuh"
+#include "ss_internal.h"
+#include "ss_profile.h"
+
+namespace ss {
+
+struct BinParams {
+    SplatPtrs s;
+    int32_t tiles_x, tiles_y;
+    uint64_t *keys;
+    uint32_t *vals;
+    int64_t capacity;
+    unsigned long long *counters;  // [0] pairs, [1] culled
+};
+
+__global__ void __launch_bounds__(256) k_emit_pairs(BinParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    int x0 = 0, y0 = 0, x1 = -1, y1 = -1, st = 0;
+    uint32_t dbits = 0;
+    if (i < p.s.n) st = splat_tile_rect(p.s, i, p.tiles_x, p.tiles_y, x0, y0, x1, y1, dbits);
+    const uint32_t cnt = st > 0 ? uint32_t(x1 - x0 + 1) * uint32_t(y1 - y0 + 1) : 0u;
+
+    uint32_t inc = cnt;  // warp inclusive scan of pair counts
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, inc, 31);
+    unsigned long long base = 0;
+    if (lane == 31 && total) base = atomicAdd(p.counters, (unsigned long long)total);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    const uint32_t culled = __ballot_sync(0xffffffffu, st < 0);
+    if (lane == 0 && culled) atomicAdd(p.counters + 1, (unsigned long long)__popc(culled));
+    if (!cnt) return;
+
+    unsigned long long pos = base + (inc - cnt);
+    const unsigned long long cap = (unsigned long long)p.capacity;
+    for (int ty = y0; ty <= y1; ++ty) {
+        const uint64_t row = uint64_t(ty) * uint64_t(p.tiles_x);
+        for (int tx = x0; tx <= x1; ++tx, ++pos) {
+            if (pos < cap) {
+                p.keys[pos] = ((row + uint64_t(tx)) << 32) | dbits;
+                p.vals[pos] = uint32_t(i);
+            }
+        }
+    }
+}
+
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" ss_status ss_bin_tiles(const ss_splats *splats, int32_t W, int32_t H, uint64_t *keys,
+                                  uint32_t *vals, int64_t capacity, uint64_t *d_counters,
+                                  ss_stream_t stream) {
+    clear_error();
+    if (!splats) return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: splats is NULL");
+    if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
+        return fail(SS_ERR_UNSUPPORTED, "ss_bin_tiles: image %dx%d outside 1..%d", W, H, kMaxSide);
+    if (splats->n < 0) return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: n < 0");
+    if (splats->n > 0 && (!splats->mean2d || !splats->conic || !splats->opacity || !splats->rgb ||
+                          !splats->depth))
+        return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: a splat array is NULL");
+    if (capacity < 0) return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: capacity < 0");
+    if (capacity > 0 && (!keys || !vals))
+        return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: keys/vals NULL with capacity > 0");
+    if (!d_counters) return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: d_counters is NULL");
+    if ((reinterpret_cast<uintptr_t>(d_counters) & 7) || (reinterpret_cast<uintptr_t>(keys) & 7) ||
+        (splats->n > 0 && (reinterpret_cast<uintptr_t>(splats->mean2d) & 7)))
+        return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: keys, counters and mean2d need 8-byte alignment");
+    cudaStream_t st = (cudaStream_t)stream;
+    ss_status s = check_cuda(cudaMemsetAsync(d_counters, 0, 16, st), "ss_bin_tiles: memset");
+    if (s != SS_OK || splats->n == 0) return s;
+    BinParams p{};
+    p.s = SplatPtrs{splats->mean2d, splats->conic, splats->opacity, splats->rgb, splats->depth,
+                    splats->n};
+    p.tiles_x = tiles_x(W);
+    p.tiles_y = tiles_y(H);
+    p.keys = keys;
+    p.vals = vals;
+    p.capacity = capacity;
+    p.counters = reinterpret_cast<unsigned long long *>(d_counters);
+    const int grid = int((int64_t(splats->n) + 255) / 256);
+    SS_LAUNCH("k_emit_pairs", st, k_emit_pairs<<<grid, 256, 0, st>>>(p));
+    return check_launch("ss_bin_tiles: k_emit_pairs");
+}

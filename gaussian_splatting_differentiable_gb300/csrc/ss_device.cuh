@@ -1,0 +1,172 @@
+// Device functions shared by the binning, forward and backward kernels.
+//
+// The forward and backward kernels must take the same per-(pixel, splat)
+// decision "is this splat blended here", or the backward replay would walk a
+// different list than the forward composited.  Both therefore stage splats
+// and evaluate the Gaussian exponent through the functions below, written
+// with explicit round-to-nearest intrinsics so that the compiler cannot
+// contract or reassociate them differently in the two kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace ss {
+
+constexpr float kAlphaMin = 1.0f / 255.0f;  // skip threshold on alpha
+constexpr float kAlphaMax = 0.99f;          // alpha cap
+constexpr float kTEps = 1e-4f;              // transmittance floor
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+
+// Binning ellipse margins: k widened by 2^-10 relative and absolute.
+constexpr float kKRel = 1.0f + 1.0f / 1024.0f;
+constexpr float kKAbs = 1.0f / 1024.0f;
+
+struct SplatPtrs {
+    const float *mean2d, *conic, *opacity, *rgb, *depth;
+    int32_t n;
+};
+
+// 2^x, the hardware approximation (relative error about 2^-22 on [-8, 0]).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ln(x) for positive, finite, normal float32 x: x = m 2^e, m in [1, 2),
+// ln x = e ln 2 + 2 atanh(t), t = (m - 1) / (m + 1), atanh by its Taylor
+// series to t^15 (Horner).  Only IEEE-rounded + - * /, so the value is the
+// same bits on any IEEE float32 machine: the binning must agree bit for bit
+// with an independent CPU evaluation.
+__device__ __forceinline__ float ln_series(float x) {
+    const uint32_t u = __float_as_uint(x);
+    const int e = int((u >> 23) & 0xffu) - 127;
+    const float m = __uint_as_float((u & 0x007fffffu) | 0x3f800000u);
+    const float t = __fdiv_rn(__fsub_rn(m, 1.0f), __fadd_rn(m, 1.0f));
+    const float t2 = __fmul_rn(t, t);
+    float p = 1.0f / 15.0f;
+    p = __fadd_rn(__fmul_rn(p, t2), 1.0f / 13.0f);
+    p = __fadd_rn(__fmul_rn(p, t2), 1.0f / 11.0f);
+    p = __fadd_rn(__fmul_rn(p, t2), 1.0f / 9.0f);
+    p = __fadd_rn(__fmul_rn(p, t2), 1.0f / 7.0f);
+    p = __fadd_rn(__fmul_rn(p, t2), 1.0f / 5.0f);
+    p = __fadd_rn(__fmul_rn(p, t2), 1.0f / 3.0f);
+    p = __fadd_rn(__fmul_rn(p, t2), 1.0f);
+    const float lnm = __fmul_rn(2.0f, __fmul_rn(t, p));
+    return __fadd_rn(__fmul_rn(__int2float_rn(e), kLn2), lnm);
+}
+
+// Tile rectangle of splat i (inclusive tile coordinates).  Returns -1 if the
+// splat is culled (non-finite input, depth <= 0, conic not positive
+// definite, opacity < 1/255), 0 if it touches no tile of the image, else 1.
+// The rectangle is the axis-aligned box of the ellipse where alpha >= 1/255
+// is possible: {d : d^T Q d <= k}, k = 2 ln(255 o), half widths
+// sqrt(k c / det) and sqrt(k a / det), Q = [[a, b], [b, c]].
+__device__ __forceinline__ int splat_tile_rect(const SplatPtrs &s, int64_t i, int32_t tiles_x,
+                                               int32_t tiles_y, int &x0, int &y0, int &x1,
+                                               int &y1, uint32_t &depth_bits) {
+    const float2 mu = reinterpret_cast<const float2 *>(s.mean2d)[i];
+    const float a = s.conic[3 * i], b = s.conic[3 * i + 1], c = s.conic[3 * i + 2];
+    const float o = s.opacity[i], d = s.depth[i];
+    const float r = s.rgb[3 * i], g = s.rgb[3 * i + 1], bl = s.rgb[3 * i + 2];
+    if (!isfinite(mu.x) || !isfinite(mu.y) || !isfinite(a) || !isfinite(b) || !isfinite(c) ||
+        !isfinite(o) || !isfinite(d) || !isfinite(r) || !isfinite(g) || !isfinite(bl))
+        return -1;
+    if (!(d > 0.0f) || !(a > 0.0f) || !(c > 0.0f)) return -1;
+    const float det = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, b));
+    if (!(det > 0.0f)) return -1;
+    if (!(o >= kAlphaMin)) return -1;
+    const float x = __fmul_rn(255.0f, o);
+    if (isinf(x)) return -1;
+    float k = __fmul_rn(2.0f, ln_series(x));
+    k = __fadd_rn(__fmul_rn(k, kKRel), kKAbs);
+    const float rx = __fsqrt_rn(__fdiv_rn(__fmul_rn(k, c), det));
+    const float ry = __fsqrt_rn(__fdiv_rn(__fmul_rn(k, a), det));
+    if (rx != rx || ry != ry) return -1;
+    float fx0 = floorf(__fmul_rn(__fsub_rn(mu.x, rx), 0.0625f));
+    float fx1 = floorf(__fmul_rn(__fadd_rn(mu.x, rx), 0.0625f));
+    float fy0 = floorf(__fmul_rn(__fsub_rn(mu.y, ry), 0.0625f));
+    float fy1 = floorf(__fmul_rn(__fadd_rn(mu.y, ry), 0.0625f));
+    fx0 = fmaxf(fx0, 0.0f);
+    fy0 = fmaxf(fy0, 0.0f);
+    fx1 = fminf(fx1, float(tiles_x - 1));
+    fy1 = fminf(fy1, float(tiles_y - 1));
+    depth_bits = __float_as_uint(d);
+    if (fx0 > fx1 || fy0 > fy1) return 0;
+    x0 = int(fx0);
+    y0 = int(fy0);
+    x1 = int(fx1);
+    y1 = int(fy1);
+    return 1;
+}
+
+// A splat as the rasterizers keep it in shared memory.  The exponent is
+// handled in base 2: e2 = -sigma log2(e) = A dx^2 + B dx dy + C dy^2 with
+// A = -a log2(e) / 2, B = -b log2(e), C = -c log2(e) / 2; the splat is
+// skipped at a pixel iff e2 < thr = -log2(255 o)  (alpha < 1/255).
+struct __align__(16) SplatGeo {
+    float mx, my, A, B;
+};
+struct __align__(8) SplatGeo2 {
+    float C, thr;
+};
+struct __align__(16) SplatCol {
+    float o, r, g, b;
+};
+// Conservative box of pixel centres where e2 >= thr can hold (the alpha
+// ellipse's bounding box grown by 0.4 % + 0.01 px); used only to skip work.
+struct __align__(16) SplatBox {
+    float x0, x1, y0, y1;
+};
+
+__device__ __forceinline__ void stage_splat(const SplatPtrs &s, uint32_t idx, SplatGeo &geo,
+                                            SplatGeo2 &geo2, SplatCol &col, SplatBox &box,
+                                            float *depth) {
+    if (idx >= uint32_t(s.n)) {  // not a splat: never blended
+        geo = SplatGeo{0.f, 0.f, 0.f, 0.f};
+        geo2 = SplatGeo2{0.f, __int_as_float(0x7f800000)};
+        col = SplatCol{0.f, 0.f, 0.f, 0.f};
+        box = SplatBox{1.f, -1.f, 1.f, -1.f};
+        if (depth) *depth = 0.f;
+        return;
+    }
+    const float2 mu = reinterpret_cast<const float2 *>(s.mean2d)[idx];
+    const float a = s.conic[3 * idx], b = s.conic[3 * idx + 1], c = s.conic[3 * idx + 2];
+    const float o = s.opacity[idx];
+    geo = SplatGeo{mu.x, mu.y, __fmul_rn(-0.5f * kLog2e, a), __fmul_rn(-kLog2e, b)};
+    geo2 = SplatGeo2{__fmul_rn(-0.5f * kLog2e, c), -log2f(__fmul_rn(255.0f, o))};
+    col = SplatCol{o, s.rgb[3 * idx], s.rgb[3 * idx + 1], s.rgb[3 * idx + 2]};
+    const float k = 2.0f * fmaxf(__logf(255.0f * o), 0.0f);
+    const float det = a * c - b * b;
+    const float rx = sqrtf(k * c / det) * 1.004f + 0.01f;
+    const float ry = sqrtf(k * a / det) * 1.004f + 0.01f;
+    box = SplatBox{mu.x - rx, mu.x + rx, mu.y - ry, mu.y + ry};
+    if (depth) *depth = s.depth[idx];
+}
+
+// Base-2 exponent of the splat's Gaussian at pixel centre (px, py); also
+// returns d = pixel - mean.  Identical operations in forward and backward.
+__device__ __forceinline__ float eval_e2(const SplatGeo &g, float C, float px, float py,
+                                         float &dx, float &dy) {
+    dx = __fsub_rn(px, g.mx);
+    dy = __fsub_rn(py, g.my);
+    const float t = __fmaf_rn(g.A, dx, __fmul_rn(g.B, dy));
+    return __fmaf_rn(dx, t, __fmul_rn(__fmul_rn(C, dy), dy));
+}
+
+// alpha = min(0.99, o 2^e2), and the unclamped o G.
+__device__ __forceinline__ float eval_alpha(float o, float G, float &oG) {
+    oG = __fmul_rn(o, G);
+    return fminf(kAlphaMax, oG);
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+}  // namespace ss

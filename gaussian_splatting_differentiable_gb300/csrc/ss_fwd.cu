@@ -1,0 +1,164 @@
+// Forward rasterization ("Phase 5 step 30b -- kernel-by-kernel timing",
+// rasterize_f32; "从 8.6 KB 到 4.2 KB ...", raster fwd).
+//
+// One 256-thread CTA per 16x16 tile, one thread per pixel; warp w covers the
+// 8x4 pixel block (8 (w & 1), 4 (w >> 1)) of the tile.  The tile's list is
+// walked front to back in batches of 256 splats: every thread stages one
+// splat of the batch into shared memory (gathered by index from the SoA
+// inputs, which stay resident in L2), then each warp compacts the batch to
+// the splats whose conservative box reaches its 8x4 block, and each pixel
+// composites that short list.  A pixel stops at the first splat whose blend
+// would take T below 1e-4; the CTA stops staging once all its pixels have.
+// The median-depth output is a template variant, so the default variant
+// carries neither its shared array nor its registers.
+#include "ss_device.cuh"
+#include "ss_internal.h"
+#include "ss_profile.h"
+
+namespace ss {
+
+struct FwdParams {
+    SplatPtrs s;
+    const uint32_t *vals;
+    const uint32_t *offs;
+    int32_t W, H, tiles_x;
+    float bg[3];
+    float *image;
+    float *T_final;
+    uint32_t *last;
+    float *median;
+};
+
+template <bool MEDIAN>
+__global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
+    __shared__ SplatGeo s_geo[256];
+    __shared__ SplatGeo2 s_geo2[256];
+    __shared__ SplatCol s_col[256];
+    __shared__ SplatBox s_box[256];
+    __shared__ float s_depth[MEDIAN ? 256 : 1];
+    __shared__ uint8_t s_list[8][256];
+
+    const int tile = blockIdx.x;
+    const int tx = tile % p.tiles_x, ty = tile / p.tiles_x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bx = tx * kTile + ((warp & 1) << 3), by = ty * kTile + ((warp >> 1) << 2);
+    const int x = bx + (lane & 7), y = by + (lane >> 3);
+    const bool inside = x < p.W && y < p.H;
+    const float px = float(x) + 0.5f, py = float(y) + 0.5f;
+    const float wx0 = float(bx) + 0.5f, wx1 = wx0 + 7.0f;
+    const float wy0 = float(by) + 0.5f, wy1 = wy0 + 3.0f;
+    const uint32_t start = p.offs[tile], end = p.offs[tile + 1];
+    const uint32_t lt = lanemask_lt();
+
+    float T = 1.0f, cr = 0.0f, cg = 0.0f, cb = 0.0f, med = 0.0f;
+    uint32_t last = 0;
+    bool done = !inside;
+
+    for (uint32_t base = start; base < end; base += 256) {
+        if (__syncthreads_count(!done) == 0) break;
+        const int nb = int(min(256u, end - base));
+        if (int(threadIdx.x) < nb) {
+            const uint32_t idx = p.vals[base + threadIdx.x];
+            stage_splat(p.s, idx, s_geo[threadIdx.x], s_geo2[threadIdx.x], s_col[threadIdx.x],
+                        s_box[threadIdx.x], MEDIAN ? &s_depth[threadIdx.x] : nullptr);
+        }
+        __syncthreads();
+        if (!__any_sync(0xffffffffu, !done)) continue;
+        int cnt = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int j = q * 32 + lane;
+            bool hit = false;
+            if (j < nb) {
+                const SplatBox b = s_box[j];
+                hit = b.x0 <= wx1 && b.x1 >= wx0 && b.y0 <= wy1 && b.y1 >= wy0;
+            }
+            const uint32_t m = __ballot_sync(0xffffffffu, hit);
+            if (hit) s_list[warp][cnt + __popc(m & lt)] = uint8_t(j);
+            cnt += __popc(m);
+        }
+        __syncwarp();
+        if (done) continue;
+        for (int q = 0; q < cnt; ++q) {
+            const int j = s_list[warp][q];
+            const SplatGeo g = s_geo[j];
+            const SplatGeo2 g2 = s_geo2[j];
+            float dx, dy;
+            const float e2 = eval_e2(g, g2.C, px, py, dx, dy);
+            if (!(e2 >= g2.thr)) continue;  // skipped (alpha < 1/255); NaN-safe
+            const SplatCol c = s_col[j];
+            float oG;
+            const float alpha = eval_alpha(c.o, ex2_approx(e2), oG);
+            const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
+            if (Tn < kTEps) {
+                done = true;
+                break;
+            }
+            const float w = alpha * T;
+            cr = fmaf(c.r, w, cr);
+            cg = fmaf(c.g, w, cg);
+            cb = fmaf(c.b, w, cb);
+            if (MEDIAN && T > 0.5f) med = s_depth[j];
+            T = Tn;
+            last = base - start + uint32_t(j) + 1u;
+        }
+    }
+    if (inside) {
+        const size_t HW = size_t(p.W) * p.H, pix = size_t(y) * p.W + x;
+        p.image[pix] = fmaf(T, p.bg[0], cr);
+        p.image[HW + pix] = fmaf(T, p.bg[1], cg);
+        p.image[2 * HW + pix] = fmaf(T, p.bg[2], cb);
+        p.T_final[pix] = T;
+        p.last[pix] = last;
+        if (MEDIAN) p.median[pix] = med;
+    }
+}
+
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" ss_status ss_raster_fwd(const ss_splats *splats, const uint32_t *vals,
+                                   const uint32_t *tile_offsets, int32_t W, int32_t H,
+                                   const float *bg, uint32_t flags, float *image, float *T_final,
+                                   uint32_t *last_contrib, float *median_depth,
+                                   ss_stream_t stream) {
+    clear_error();
+    if (!splats) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: splats is NULL");
+    if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
+        return fail(SS_ERR_UNSUPPORTED, "ss_raster_fwd: image %dx%d outside 1..%d", W, H, kMaxSide);
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: unknown flag bits 0x%x", flags);
+    if (splats->n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: n < 0");
+    if (splats->n > 0 && (!splats->mean2d || !splats->conic || !splats->opacity || !splats->rgb ||
+                          !splats->depth))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: a splat array is NULL");
+    if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: vals/offsets NULL");
+    if (!image || !T_final || !last_contrib)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: an output is NULL");
+    const bool median = flags & SS_MEDIAN_DEPTH;
+    if (median && !median_depth)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: SS_MEDIAN_DEPTH set but median_depth NULL");
+    if (splats->n > 0 && (reinterpret_cast<uintptr_t>(splats->mean2d) & 7))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: mean2d not 8-byte aligned");
+    FwdParams p{};
+    p.s = SplatPtrs{splats->mean2d, splats->conic, splats->opacity, splats->rgb, splats->depth,
+                    splats->n};
+    p.vals = vals;
+    p.offs = tile_offsets;
+    p.W = W;
+    p.H = H;
+    p.tiles_x = tiles_x(W);
+    for (int c = 0; c < 3; ++c) p.bg[c] = bg ? bg[c] : 0.0f;
+    p.image = image;
+    p.T_final = T_final;
+    p.last = last_contrib;
+    p.median = median_depth;
+    const int grid = tiles_x(W) * tiles_y(H);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (median)
+        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<true><<<grid, 256, 0, st>>>(p));
+    else
+        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<false><<<grid, 256, 0, st>>>(p));
+    return check_launch("ss_raster_fwd");
+}

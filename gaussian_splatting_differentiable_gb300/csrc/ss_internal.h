@@ -1,0 +1,63 @@
+// Host-side internals of libss.so: error reporting, size limits, workspace
+// layout.  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "ss.h"
+
+namespace ss {
+
+constexpr int kTile = 16;
+constexpr int32_t kMaxSide = 32768;
+constexpr int kSortThreads = 256;
+constexpr int kSortKeysPerThread = 16;
+constexpr int kSortPart = kSortThreads * kSortKeysPerThread;  // keys per onesweep partition
+
+// Records `st` and a printf-style message as this thread's last error.
+ss_status fail(ss_status st, const char *fmt, ...);
+// Clears this thread's last error (start of every ABI call).
+void clear_error();
+// SS_OK, or SS_ERR_CUDA with the pending launch error's text.
+ss_status check_launch(const char *what);
+// SS_ERR_CUDA with the text of `e` if e != cudaSuccess.
+ss_status check_cuda(cudaError_t e, const char *what);
+
+inline int32_t tiles_x(int32_t W) { return (W + kTile - 1) / kTile; }
+inline int32_t tiles_y(int32_t H) { return (H + kTile - 1) / kTile; }
+
+// Number of 8-bit digits in a (tile << 32 | depth bits) key for `tiles` tiles.
+inline int sort_digits(int64_t tiles) {
+    int tile_bits = 0;
+    while (tile_bits < 32 && (int64_t(1) << tile_bits) < tiles) ++tile_bits;
+    return (32 + tile_bits + 7) / 8;
+}
+
+// Workspace layout.  The first 256 bytes hold the device status word of the
+// last sort; the rest is shared by ss_sort_pairs and ss_raster_bwd.
+struct WsLayout {
+    size_t status_word;   // uint32, offset 0
+    size_t hist;          // uint32 [ndig][256] digit counts
+    size_t gofs;          // uint32 [ndig][256] exclusive digit starts
+    size_t tickets;       // uint32 [8] partition tickets per pass
+    size_t lookback;      // uint64 [ndig][nparts][256] onesweep look-back words
+    size_t zero_end;      // [0, zero_end) is cleared before each sort
+    size_t alt_keys;      // uint64 [n_pairs] ping-pong buffer
+    size_t alt_vals;      // uint32 [n_pairs]
+    size_t sort_end;
+    size_t accum;         // uint64 [n_splats] backward 32.32 fixed-point accumulator
+    size_t bwd_end;
+    size_t total;
+    int ndig;
+    int64_t nparts;
+};
+
+WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H);
+
+// Device status bits written by the sort kernels.
+enum : uint32_t { kDevErrTimeout = 1u, kDevErrKeyRange = 2u };
+
+}  // namespace ss

@@ -1,0 +1,348 @@
+// Sort of the (tile << 32 | depth bits, splat index) pairs and per-tile
+// ranges ("Phase 5 step 30b -- kernel-by-kernel timing": radix_hist,
+// radix_scatter -- 16 passes there -- and extract_offsets).
+//
+// Here an LSD radix sort in the onesweep style (Adinets & Merrill, "Onesweep:
+// A Faster Least Significant Digit Radix Sort for GPUs", 2022):
+//   k_sort_hist   one read of all keys builds the histograms of every 8-bit
+//                 digit at once;
+//   k_sort_scan   exclusive scan of each digit's histogram;
+//   k_sort_pass   one launch per digit: each CTA takes the next partition of
+//                 4096 keys by an atomic ticket (so a CTA only ever waits on
+//                 CTAs that are already running), ranks its keys with warp
+//                 match + per-warp histograms (stable), publishes its digit
+//                 counts, and finds its global offsets by decoupled look-back
+//                 over earlier partitions; every wait is bounded and reports
+//                 a timeout through the workspace status word instead of
+//                 spinning forever;
+//   k_sort_final  equal keys (same tile, same depth) come out in emission
+//                 order, which the atomic counter of the binning makes
+//                 arbitrary: each run of equal keys is re-sorted by splat
+//                 index, and the tile boundaries give the CSR offsets.
+// Only 32 + ceil(log2 tiles) key bits are sorted.
+#include "ss_device.cuh"
+#include "ss_internal.h"
+#include "ss_profile.h"
+
+namespace ss {
+
+constexpr uint64_t kFlagAgg = 1ull << 62;
+constexpr uint64_t kFlagInc = 2ull << 62;
+constexpr uint64_t kValMask = (1ull << 62) - 1;
+constexpr uint32_t kSpinLimit = 1u << 21;  // x ~100 ns backoff: about 0.2 s per wait
+
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint64_t *p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Exclusive scan of one value per thread over a 256-thread block.
+__device__ __forceinline__ uint32_t block_excl_scan256(uint32_t v, uint32_t *s_warp,
+                                                       uint32_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    uint32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t t = s_warp[w];
+        before += w < warp ? t : 0u;
+        all += t;
+    }
+    __syncthreads();
+    if (total) *total = all;
+    return before + inc - v;
+}
+
+__global__ void __launch_bounds__(256) k_sort_hist(const uint64_t *__restrict__ keys, int64_t n,
+                                                   int ndig, uint32_t *__restrict__ hist) {
+    __shared__ uint32_t s_h[8][256];
+    for (int k = threadIdx.x; k < 8 * 256; k += 256) (&s_h[0][0])[k] = 0;
+    __syncthreads();
+    const int64_t stride = int64_t(gridDim.x) * 256;
+    for (int64_t i = int64_t(blockIdx.x) * 256 + threadIdx.x; i < n; i += stride) {
+        const uint64_t k = keys[i];
+        for (int d = 0; d < ndig; ++d) atomicAdd(&s_h[d][(k >> (8 * d)) & 255u], 1u);
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < ndig * 256; k += 256) {
+        const uint32_t v = (&s_h[0][0])[k];
+        if (v) atomicAdd(hist + k, v);
+    }
+}
+
+__global__ void __launch_bounds__(256) k_sort_scan(const uint32_t *__restrict__ hist,
+                                                   uint32_t *__restrict__ gofs) {
+    __shared__ uint32_t s_warp[8];
+    const int d = blockIdx.x;
+    gofs[d * 256 + threadIdx.x] = block_excl_scan256(hist[d * 256 + threadIdx.x], s_warp, nullptr);
+}
+
+struct PassParams {
+    const uint64_t *kin;
+    const uint32_t *vin;
+    uint64_t *kout;
+    uint32_t *vout;
+    int64_t n;
+    int shift;
+    const uint32_t *gofs;  // [256] exclusive starts of this digit
+    uint64_t *lookback;    // [nparts][256]
+    uint32_t *ticket;
+    uint32_t *err;
+};
+
+__global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
+    constexpr int KPT = kSortKeysPerThread;
+    __shared__ uint32_t s_whist[8][256];  // per-warp digit counts, then warp-exclusive offsets
+    __shared__ uint32_t s_lstart[256];    // digit start within the partition
+    __shared__ uint32_t s_gbase[256];     // global start of the partition's keys of each digit
+    __shared__ uint32_t s_warp[8];
+    __shared__ uint32_t s_part;
+    extern __shared__ __align__(16) unsigned char s_dyn[];
+    uint64_t *s_keys = reinterpret_cast<uint64_t *>(s_dyn);
+    uint32_t *s_vals = reinterpret_cast<uint32_t *>(s_dyn + kSortPart * 8);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_part = atomicAdd(p.ticket, 1u);
+    for (int k = tid; k < 8 * 256; k += 256) (&s_whist[0][0])[k] = 0;
+    __syncthreads();
+    const int64_t part = s_part;
+    const int64_t base = part * kSortPart;
+    const int64_t wbase = base + warp * (KPT * 32);
+
+    uint64_t key[KPT];
+    uint32_t val[KPT];
+    uint32_t rank[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int64_t idx = wbase + j * 32 + lane;
+        const bool ok = idx < p.n;
+        key[j] = ok ? p.kin[idx] : ~0ull;
+        val[j] = ok ? p.vin[idx] : 0u;
+    }
+    // Stable rank within the warp: keys in order (j, lane).
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int64_t idx = wbase + j * 32 + lane;
+        const bool ok = idx < p.n;
+        const uint32_t dig = ok ? uint32_t(key[j] >> p.shift) & 255u : 256u + lane;
+        const uint32_t peers = __match_any_sync(0xffffffffu, dig);
+        const uint32_t before = __popc(peers & lt);
+        uint32_t cur = 0;
+        if (ok) cur = s_whist[warp][dig];
+        rank[j] = cur + before;
+        __syncwarp();
+        if (ok && before == 0) s_whist[warp][dig] = cur + __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // Per digit (thread = digit): warp-exclusive offsets and partition total.
+    const int d = tid;
+    uint32_t total = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t c = s_whist[w][d];
+        s_whist[w][d] = total;
+        total += c;
+    }
+    uint64_t *my = p.lookback + part * 256 + d;
+    st_relaxed(my, (part == 0 ? kFlagInc : kFlagAgg) | uint64_t(total));
+
+    s_lstart[d] = block_excl_scan256(total, s_warp, nullptr);
+
+    // Decoupled look-back: sum the counts of digit d in earlier partitions.
+    uint64_t excl = 0;
+    if (part > 0) {
+        int64_t q = part - 1;
+        uint32_t spins = 0;
+        while (true) {
+            const uint64_t s = ld_relaxed(p.lookback + q * 256 + d);
+            const uint64_t flag = s & ~kValMask;
+            if (flag == 0) {
+                if (++spins > kSpinLimit) {
+                    atomicOr(p.err, kDevErrTimeout);
+                    break;
+                }
+                if (spins > 32) __nanosleep(100);
+                continue;
+            }
+            excl += s & kValMask;
+            if (flag == kFlagInc || q == 0) break;
+            --q;
+            spins = 0;
+        }
+        st_relaxed(my, kFlagInc | (excl + total));
+    }
+    s_gbase[d] = p.gofs[d] + uint32_t(excl);
+    __syncthreads();
+
+    // Scatter into shared memory in (digit, rank) order, then out.
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int64_t idx = wbase + j * 32 + lane;
+        if (idx < p.n) {
+            const uint32_t dig = uint32_t(key[j] >> p.shift) & 255u;
+            const uint32_t pos = s_lstart[dig] + s_whist[warp][dig] + rank[j];
+            s_keys[pos] = key[j];
+            s_vals[pos] = val[j];
+        }
+    }
+    __syncthreads();
+    const int64_t left = p.n - base;
+    const int cnt = int(left < kSortPart ? left : kSortPart);
+    for (int i = tid; i < cnt; i += 256) {
+        const uint64_t k = s_keys[i];
+        const uint32_t dig = uint32_t(k >> p.shift) & 255u;
+        const uint32_t g = s_gbase[dig] + uint32_t(i) - s_lstart[dig];
+        p.kout[g] = k;
+        p.vout[g] = s_vals[i];
+    }
+}
+
+// Ties and offsets.  For element i of the sorted keys:
+//  - tile boundaries: offs[t] = i for every tile t in (tile(i-1), tile(i)],
+//    and offs[t] = n for t > tile(n-1);
+//  - a run of equal keys starting at i is re-sorted by value (insertion sort
+//    by the run's first thread; runs are a few elements);
+//  - when src != dst the element is copied (run members by the run head).
+__global__ void __launch_bounds__(256) k_sort_final(const uint64_t *__restrict__ sk,
+                                                    uint32_t *sv, uint64_t *dk, uint32_t *dv,
+                                                    int64_t n, int64_t tiles, uint32_t *offs,
+                                                    uint32_t *err) {
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const uint64_t key = sk[i];
+    int64_t t = int64_t(key >> 32);
+    if (t >= tiles) {
+        atomicOr(err, kDevErrKeyRange);
+        t = tiles;
+    }
+    int64_t tp = -1;
+    if (i > 0) {
+        tp = int64_t(sk[i - 1] >> 32);
+        if (tp > tiles) tp = tiles;
+    }
+    for (int64_t u = tp + 1; u <= t; ++u) offs[u] = uint32_t(i);
+    if (i == n - 1)
+        for (int64_t u = t + 1; u <= tiles; ++u) offs[u] = uint32_t(n);
+
+    const bool copy = sk != dk;
+    const bool member = i > 0 && sk[i - 1] == key;
+    if (member) return;
+    const bool head = i + 1 < n && sk[i + 1] == key;
+    if (!head) {
+        if (copy) {
+            dk[i] = key;
+            dv[i] = sv[i];
+        }
+        return;
+    }
+    int64_t e = i + 1;
+    while (e < n && sk[e] == key) ++e;
+    // insertion sort of sv[i..e) by value, written to dv[i..e)
+    for (int64_t a = i; a < e; ++a) {
+        const uint32_t v = sv[a];
+        int64_t b = a;
+        while (b > i && dv[b - 1] > v) {
+            dv[b] = dv[b - 1];
+            --b;
+        }
+        dv[b] = v;
+        if (copy) dk[a] = key;
+    }
+}
+
+static int g_attr_set[64];
+
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" ss_status ss_sort_pairs(uint64_t *keys, uint32_t *vals, int64_t n_pairs, int32_t W,
+                                   int32_t H, uint32_t *tile_offsets, void *workspace,
+                                   size_t workspace_bytes, ss_stream_t stream) {
+    clear_error();
+    if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
+        return fail(SS_ERR_UNSUPPORTED, "ss_sort_pairs: image %dx%d outside 1..%d", W, H, kMaxSide);
+    if (n_pairs < 0) return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: n_pairs < 0");
+    if (n_pairs > int64_t(0xffffffffu))
+        return fail(SS_ERR_UNSUPPORTED, "ss_sort_pairs: n_pairs %lld >= 2^32", (long long)n_pairs);
+    if (!tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: tile_offsets is NULL");
+    if (n_pairs > 0 && (!keys || !vals))
+        return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: keys/vals NULL");
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: workspace NULL or not 256-byte aligned");
+    if (reinterpret_cast<uintptr_t>(keys) & 7)
+        return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: keys not 8-byte aligned");
+    const WsLayout L = ws_layout(0, n_pairs, W, H);
+    if (workspace_bytes < L.sort_end)
+        return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: workspace %zu bytes < %zu needed",
+                    workspace_bytes, L.sort_end);
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t tiles = int64_t(tiles_x(W)) * tiles_y(H);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws + L.status_word);
+    ss_status s = check_cuda(cudaMemsetAsync(ws, 0, L.zero_end, st), "ss_sort_pairs: memset");
+    if (s != SS_OK) return s;
+    if (n_pairs == 0)
+        return check_cuda(cudaMemsetAsync(tile_offsets, 0, size_t(tiles + 1) * 4, st),
+                          "ss_sort_pairs: memset offsets");
+
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int dyn = kSortPart * 12;
+    if (dev < 64 && !g_attr_set[dev]) {
+        s = check_cuda(cudaFuncSetAttribute(k_sort_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            dyn),
+                       "ss_sort_pairs: cudaFuncSetAttribute");
+        if (s != SS_OK) return s;
+        g_attr_set[dev] = 1;
+    }
+
+    uint32_t *hist = reinterpret_cast<uint32_t *>(ws + L.hist);
+    uint32_t *gofs = reinterpret_cast<uint32_t *>(ws + L.gofs);
+    uint32_t *tickets = reinterpret_cast<uint32_t *>(ws + L.tickets);
+    uint64_t *lookback = reinterpret_cast<uint64_t *>(ws + L.lookback);
+    uint64_t *ak = reinterpret_cast<uint64_t *>(ws + L.alt_keys);
+    uint32_t *av = reinterpret_cast<uint32_t *>(ws + L.alt_vals);
+
+    const int64_t blocks = (n_pairs + 255) / 256;
+    const int hgrid = int(blocks < int64_t(sms) * 4 ? blocks : int64_t(sms) * 4);
+    SS_LAUNCH("k_sort_hist", st, k_sort_hist<<<hgrid, 256, 0, st>>>(keys, n_pairs, L.ndig, hist));
+    SS_LAUNCH("k_sort_scan", st, k_sort_scan<<<L.ndig, 256, 0, st>>>(hist, gofs));
+    uint64_t *bk[2] = {keys, ak};
+    uint32_t *bv[2] = {vals, av};
+    for (int d = 0; d < L.ndig; ++d) {
+        PassParams p{};
+        p.kin = bk[d & 1];
+        p.vin = bv[d & 1];
+        p.kout = bk[(d + 1) & 1];
+        p.vout = bv[(d + 1) & 1];
+        p.n = n_pairs;
+        p.shift = 8 * d;
+        p.gofs = gofs + 256 * d;
+        p.lookback = lookback + size_t(d) * size_t(L.nparts) * 256;
+        p.ticket = tickets + d;
+        p.err = err;
+        SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<int(L.nparts), 256, dyn, st>>>(p));
+    }
+    const int r = L.ndig & 1;
+    SS_LAUNCH("k_sort_final", st,
+              k_sort_final<<<int(blocks), 256, 0, st>>>(bk[r], bv[r], keys, vals, n_pairs, tiles,
+                                                        tile_offsets, err));
+    return check_launch("ss_sort_pairs");
+}

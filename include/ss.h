@@ -1,0 +1,230 @@
+/*
+ * ss.h -- C ABI of libss.so, a GB300 (sm_103a) implementation of tile-based
+ * differentiable rasterization of projected 2D Gaussian splats.
+ *
+ * The path has the kernels the pages time one after another in a training
+ * step ("Phase 5 step 30b -- kernel-by-kernel timing", measurement table:
+ * emit_pairs, radix_hist / radix_scatter, extract_offsets, rasterize_f32,
+ * rasterize_backwards) and that the Spirula Studio write-up benchmarks as
+ * "tile isect", "raster fwd" and "raster bwd" ("从 8.6 KB 到 4.2 KB ...",
+ * section 亲手验证):
+ *
+ *   ss_bin_tiles   tile binning: one (key, value) pair per (splat, touched tile)
+ *   ss_pair_count  the one device-to-host read: how many pairs were emitted
+ *   ss_sort_pairs  radix sort of the pairs by (tile, depth) + per-tile ranges
+ *   ss_raster_fwd  front-to-back compositing per pixel
+ *   ss_raster_bwd  back-to-front gradient of the 9 per-splat fields
+ *
+ * Conventions (every function):
+ *   - Memory: the caller owns all memory.  Every pointer is a DEVICE pointer
+ *     unless its name starts with h_ or the comment says host.  The library
+ *     allocates nothing and keeps no state except a per-thread error string.
+ *   - Streams: work is enqueued on `stream` (NULL = the legacy default stream)
+ *     and returns before it runs, except ss_pair_count and ss_sort_status,
+ *     which synchronize `stream`.
+ *   - Errors: argument errors are found on the host before anything is
+ *     enqueued and return SS_ERR_INVALID_ARG / SS_ERR_UNSUPPORTED with a
+ *     message in ss_last_error(); a failed CUDA launch returns SS_ERR_CUDA.
+ *     Nothing traps or asserts on the device.
+ *   - Tiles are 16x16 pixels, tile id = ty * ceil(W/16) + tx, in row-major
+ *     order; 1 <= W, H <= 32768.
+ *   - Images are planar float32: image[c][y][x], c = 0..2.
+ *   - The model (the pages name it but print no equation; these are the
+ *     plainest readings of front-to-back alpha compositing of 2D Gaussians):
+ *       pixel (x, y) is sampled at (x + 0.5, y + 0.5); d = pixel - mean;
+ *       sigma = (a dx^2 + c dy^2) / 2 + b dx dy,  G = exp(-sigma);
+ *       alpha = min(0.99, opacity G); splats with alpha < 1/255 are skipped;
+ *       T starts at 1; a splat whose blend would take T below 1e-4 ends the
+ *       pixel unblended; otherwise color += rgb alpha T and T *= (1 - alpha);
+ *       image = color + T_final * bg.
+ */
+#ifndef SS_H
+#define SS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the same pointer type); NULL is the legacy default stream. */
+typedef struct CUstream_st *ss_stream_t;
+
+typedef enum {
+    SS_OK = 0,
+    SS_ERR_INVALID_ARG = 1,  /* bad pointer, size or flag; nothing was enqueued */
+    SS_ERR_CAPACITY = 2,     /* more pairs than the caller's capacity (ss_pair_count) */
+    SS_ERR_CUDA = 3,         /* a CUDA call failed; message in ss_last_error() */
+    SS_ERR_TIMEOUT = 4,      /* a bounded device wait gave up (ss_sort_status) */
+    SS_ERR_UNSUPPORTED = 5,  /* a size beyond the documented limits */
+    SS_ERR_DEVICE = 6        /* a device-side check failed (ss_sort_status) */
+} ss_status;
+
+/* flags of ss_raster_fwd / ss_raster_bwd: optional outputs, each compiled
+ * as its own kernel variant so that a disabled output costs no shared memory
+ * or registers (the pattern of "从 8.6 KB 到 4.2 KB ...", section 最小改动:
+ * optional per-pixel arrays sized by a compile-time constant). */
+enum {
+    SS_ACCUM_WEIGHT = 1u,  /* bwd: per-splat accumulated blend weight sum_p alpha T */
+    SS_MEDIAN_DEPTH = 2u   /* fwd: per-pixel depth of the last splat blended while T > 0.5 */
+};
+
+/* Splats, structure of arrays, float32, device memory.  The pages' inputs:
+ * per-splat 2D mean, conic (inverse 2D covariance), opacity, RGB and depth
+ * ("Phase 5 step 30b", hotspot ranking: 9 gradient fields per splat). */
+typedef struct {
+    const float *mean2d;   /* [n][2] pixel coordinates */
+    const float *conic;    /* [n][3] (a, b, c) of [[a, b], [b, c]] */
+    const float *opacity;  /* [n] */
+    const float *rgb;      /* [n][3] */
+    const float *depth;    /* [n] > 0; sort key within a tile (front = small) */
+    int32_t n;             /* 0 <= n < 2^31; pointers may be NULL when n == 0 */
+} ss_splats;
+
+/* Per-splat gradients of L, float32, device memory, same layouts as ss_splats.
+ * db is the full partial derivative of L with respect to the stored b. */
+typedef struct {
+    float *dmean2d;        /* [n][2] */
+    float *dconic;         /* [n][3] */
+    float *dopacity;       /* [n] */
+    float *drgb;           /* [n][3] */
+} ss_grads;
+
+/* Version of this ABI (incremented on any change of a signature). */
+int32_t ss_abi_version(void);
+
+/* Host: the model's constants as the kernels use them:
+ * out[0] = 1/255 (alpha floor), out[1] = 0.99 (alpha cap),
+ * out[2] = 1e-4 (transmittance floor), out[3] = 16 (tile side). */
+void ss_constants(float out[4]);
+
+/* Host: message of the last failed call on this thread ("" if none).  The
+ * string stays valid until the next ss_* call on the same thread. */
+const char *ss_last_error(void);
+
+/* Host: bytes of workspace that ss_sort_pairs (for n_pairs pairs on a W x H
+ * image) and ss_raster_bwd (for n_splats splats) need.  One buffer of this
+ * size serves both calls, in any order on one stream.  Returns 0 if a size
+ * is out of range. */
+size_t ss_workspace_bytes(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H);
+
+/* Tile binning ("Phase 5 step 30b", emit_pairs: tile id computation and an
+ * atomic counter).  For each splat that is not culled, one pair per tile of
+ * the axis-aligned box of the ellipse where alpha >= 1/255 is possible,
+ * {d : d^T conic d <= k}, k = 2 ln(255 opacity) widened by 2^-10 relative and
+ * absolute, clipped to the image's tiles:
+ *   keys[p] = tile << 32 | bits of depth (float32, > 0, so ordered as u32)
+ *   vals[p] = splat index
+ * A splat is culled (no pairs, counted) unless all its inputs are finite,
+ * depth > 0, a > 0, c > 0, ac - b^2 > 0 and 1/255 <= opacity.
+ * Pairs are written in no particular order (a warp-aggregated atomic counter
+ * hands out slots); pairs beyond `capacity` are counted but not written.
+ *   d_counters: device uint64[2]; zeroed here, then [0] = pairs needed,
+ *               [1] = culled splats.
+ *   keys, vals: device, `capacity` entries each (may be NULL if capacity 0).
+ */
+ss_status ss_bin_tiles(const ss_splats *splats, int32_t W, int32_t H, uint64_t *keys,
+                       uint32_t *vals, int64_t capacity, uint64_t *d_counters, ss_stream_t stream);
+
+/* Host: synchronizes `stream` and reads the counters of ss_bin_tiles.
+ * *h_pairs = pairs needed, *h_culled = culled splats (either may be NULL).
+ * Returns SS_ERR_CAPACITY if pairs needed > capacity (re-run ss_bin_tiles
+ * with a capacity of at least *h_pairs). */
+ss_status ss_pair_count(const uint64_t *d_counters, int64_t capacity, int64_t *h_pairs,
+                        int64_t *h_culled, ss_stream_t stream);
+
+/* Radix sort of the pairs by key, then by value within equal keys, in place
+ * ("Phase 5 step 30b", radix_hist / radix_scatter; here a onesweep LSD sort
+ * with decoupled look-back: one histogram pass, then one pass per 8-bit
+ * digit of the 32 + ceil(log2 tiles) key bits), followed by the per-tile
+ * ranges (extract_offsets):
+ *   tile_offsets[t] = number of pairs whose tile is < t, t = 0..tiles;
+ *   pairs of tile t are [tile_offsets[t], tile_offsets[t+1]), by ascending
+ *   depth, ties by ascending splat index.
+ *   keys, vals: device, n_pairs entries, sorted in place.
+ *   tile_offsets: device uint32[tiles + 1].
+ *   workspace: device, >= ss_workspace_bytes(0, n_pairs, W, H) bytes, 256-byte
+ *   aligned; its contents need no initialisation.
+ * 0 <= n_pairs < 2^32.  The look-back waits are bounded: a wait that gives up
+ * records SS_ERR_TIMEOUT for ss_sort_status (the result is then invalid);
+ * a key whose tile is >= tiles records SS_ERR_DEVICE. */
+ss_status ss_sort_pairs(uint64_t *keys, uint32_t *vals, int64_t n_pairs, int32_t W, int32_t H,
+                        uint32_t *tile_offsets, void *workspace, size_t workspace_bytes,
+                        ss_stream_t stream);
+
+/* Host: synchronizes `stream` and returns SS_OK, SS_ERR_TIMEOUT or
+ * SS_ERR_DEVICE for the last ss_sort_pairs that used `workspace`. */
+ss_status ss_sort_status(const void *workspace, ss_stream_t stream);
+
+/* Forward rasterization ("Phase 5 step 30b", rasterize_f32): one CTA per
+ * 16x16 tile, one thread per pixel, the tile's pairs staged in shared memory
+ * in batches; each pixel composites its tile's splats front to back (model
+ * above).  Outputs (device, W x H each, planar):
+ *   image[3][H][W]      color + T_final * bg
+ *   T_final[H][W]       transmittance after the last blended splat (>= 1e-4)
+ *   last_contrib[H][W]  1 + position in the tile's list of the last blended
+ *                       splat, 0 if none (what ss_raster_bwd replays from)
+ *   median_depth[H][W]  only with SS_MEDIAN_DEPTH (else may be NULL): depth
+ *                       of the last splat blended while T > 0.5, 0 if none
+ *   bg: HOST float[3] background, or NULL for black.
+ *   vals, tile_offsets: the output of ss_sort_pairs for the same W, H.
+ * Pair values >= splats->n are ignored. */
+ss_status ss_raster_fwd(const ss_splats *splats, const uint32_t *vals,
+                        const uint32_t *tile_offsets, int32_t W, int32_t H, const float *bg,
+                        uint32_t flags, float *image, float *T_final, uint32_t *last_contrib,
+                        float *median_depth, ss_stream_t stream);
+
+/* Backward rasterization ("从 8.6 KB 到 4.2 KB ...", rasterize_bwd_2d on the
+ * 2D screen-space path; "Phase 5 step 30b", rasterize_backwards: the 9-field
+ * per-splat gradient).  Each pixel walks its tile's list back to front from
+ * last_contrib, recovering T before each blended splat as T / (1 - alpha),
+ * and adds, for L = sum dL/dimage * image:
+ *   dL/drgb += g w,  w = alpha T
+ *   dL/dalpha = sum_c g_c (rgb_c T - (S_c + T_final bg_c) / (1 - alpha)),
+ *     S = sum of rgb w over the splats blended after this one
+ *   dL/dopacity += G dL/dalpha; dL/dsigma = -alpha dL/dalpha
+ *   dL/dmean += dL/dsigma (-(a dx + b dy), -(b dx + c dy))
+ *   dL/dconic += dL/dsigma (dx^2 / 2, dx dy, dy^2 / 2)
+ * (through the 0.99 cap alpha has zero derivative).  The per-pixel terms of
+ * a splat are summed across each warp with shuffles before one atomic add
+ * per field per warp ("Phase 5 step 30b", conclusion: one atomic per warp
+ * instead of per thread).
+ *   T_final, last_contrib: from ss_raster_fwd with the same inputs.
+ *   dL_dimage: device float[3][H][W].
+ *   grads: all four arrays required; overwritten (zeroed here first).
+ *   accum_weight: with SS_ACCUM_WEIGHT, device float[n] overwritten with
+ *   sum over pixels of alpha T (summed exactly in 32.32 fixed point, so the
+ *   result does not depend on the order of the atomics); else may be NULL.
+ *   workspace: >= ss_workspace_bytes(n, 0, W, H) bytes, 256-byte aligned.
+ *   bg: HOST float[3] or NULL (must match the forward call). */
+ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals,
+                        const uint32_t *tile_offsets, int32_t W, int32_t H, const float *bg,
+                        uint32_t flags, const float *T_final, const uint32_t *last_contrib,
+                        const float *dL_dimage, const ss_grads *grads, float *accum_weight,
+                        void *workspace, size_t workspace_bytes, ss_stream_t stream);
+
+/* Per-kernel timing ("从 8.6 KB 到 4.2 KB ...", section 亲手验证: SS_PROFILE=1
+ * gives per-kernel segment timings).  Off unless the environment has
+ * SS_PROFILE=1 when the library loads or ss_profile_enable(1) is called.
+ * When on, each kernel launch is bracketed by two CUDA events on its own
+ * stream (host-side cost only; nothing is added to the kernels). */
+void ss_profile_enable(int32_t on);
+
+/* Host: waits for the events recorded since the last collect and writes one
+ * line per kernel name, "name launches total_ms min_ms max_ms\n", into
+ * buf[0..len) (NUL-terminated, truncated if short; buf may be NULL).
+ * Returns the full length of the text. */
+int64_t ss_profile_collect(char *buf, size_t len);
+
+/* Measurement helper, not part of the path: `rounds` rounds of float atomic
+ * adds (red.global.add.f32), one per thread per round, into buf[0..n)
+ * (device, n >= 1) with consecutive threads on consecutive addresses.  Timed
+ * by the caller, it gives the L2 atomic throughput that bounds the backward
+ * pass's gradient accumulation. */
+ss_status ss_probe_red_f32(float *buf, int64_t n, int32_t rounds, ss_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SS_H */

@@ -1,0 +1,190 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerances (the rasterizer's stated bar):
+  * pairs (as a multiset), sorted keys/values, tile offsets: bit-exact;
+  * image, T_final: 1e-5 absolute; last_contrib and median depth: exact;
+  * gradients: max(1e-4, 1e-3 * max|field|) per element, field = one of
+    dmean2d, dconic, dopacity, drgb;
+  * accumulated weight: max(1e-5, e) + 2^-23 |w|, e = the oracle's bound on the
+    error of a float32 evaluation of the sum (1e-5 alone is below one float32
+    ulp for sums above 128), the last term the output's own rounding.
+A knife-edge pixel (a float32 decision within rounding of its threshold)
+must equal the oracle's normal outcome or one of its alternatives; each
+gradient element's tolerance grows by the oracle's slack, the sum over knife
+edges of |alternative - normal| contribution.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import gaussian_splatting_differentiable_gb300 as ss
+
+GRAD_FIELDS = ("dmean2d", "dconic", "dopacity", "drgb")
+
+
+def flags_of(scene) -> int:
+    return (ss.SS_ACCUM_WEIGHT if scene.accum_weight else 0) | \
+        (ss.SS_MEDIAN_DEPTH if scene.median_depth else 0)
+
+
+def run_gpu(scene, capacity=None, stream=None):
+    """Whole path through the C ABI; returns numpy copies of every stage."""
+    dev = torch.device("cuda")
+    sp = ss.Splats.from_numpy(scene, dev)
+    flags = flags_of(scene)
+    cap = capacity if capacity is not None else max(64, 4 * scene.n)
+    r = ss.Rasterizer(scene.W, scene.H, scene.n, cap, flags, bg=scene.bg, device=dev)
+    ss.ss_bin_tiles(sp, scene.W, scene.H, r.keys, r.vals, r.capacity, r.counters, stream)
+    st, pairs, culled = ss.ss_pair_count(r.counters, r.capacity, stream)
+    if st != ss.SS_OK:
+        r._alloc_pairs(pairs + 16)
+        ss.ss_bin_tiles(sp, scene.W, scene.H, r.keys, r.vals, r.capacity, r.counters, stream)
+        st, pairs, culled = ss.ss_pair_count(r.counters, r.capacity, stream)
+        assert st == ss.SS_OK
+    out = {"count": pairs, "culled": culled,
+           "keys_binned": r.keys[:pairs].cpu().numpy().view(np.uint64).copy(),
+           "vals_binned": r.vals[:pairs].cpu().numpy().view(np.uint32).copy()}
+    ss.ss_sort_pairs(r.keys, r.vals, pairs, scene.W, scene.H, r.tile_offsets, r.workspace, stream)
+    out["sort_status"] = ss.ss_sort_status(r.workspace, stream)
+    out["keys"] = r.keys[:pairs].cpu().numpy().view(np.uint64).copy()
+    out["vals"] = r.vals[:pairs].cpu().numpy().view(np.uint32).copy()
+    out["offs"] = r.tile_offsets.cpu().numpy().view(np.uint32).copy()
+    r.forward(sp, stream)
+    dL = torch.from_numpy(scene.dL_dimage).to(dev).contiguous()
+    r.backward(sp, dL, stream)
+    torch.cuda.synchronize()
+    out["image"] = r.image.cpu().numpy()
+    out["T_final"] = r.T_final.cpu().numpy()
+    out["last"] = r.last_contrib.cpu().numpy().view(np.uint32)
+    out["median"] = r.median_depth.cpu().numpy() if r.median_depth is not None else None
+    for k in GRAD_FIELDS:
+        out[k] = r.grads[k].cpu().numpy()
+    out["accum"] = r.accum_weight.cpu().numpy() if r.accum_weight is not None else None
+    return out
+
+
+def _pairs_sorted(keys, vals):
+    o = np.lexsort((vals, keys))
+    return keys[o], vals[o]
+
+
+def check_pairs(scene, gpu, orc=None):
+    orc = orc or oracle.tile_lists(scene)
+    assert gpu["sort_status"] == ss.SS_OK
+    assert gpu["count"] == orc["count"], (gpu["count"], orc["count"])
+    assert gpu["culled"] == orc["culled"]
+    gk, gv = _pairs_sorted(gpu["keys_binned"], gpu["vals_binned"])
+    assert np.array_equal(gk, orc["keys"]) and np.array_equal(gv, orc["vals"]), "binned multiset"
+    assert np.array_equal(gpu["keys"], orc["keys"]), "sorted keys"
+    assert np.array_equal(gpu["vals"], orc["vals"]), "sorted values"
+    assert np.array_equal(gpu["offs"], orc["offs"]), "tile offsets"
+    return orc
+
+
+def check_forward(scene, gpu, ofw, pixel_mask=None, atol=1e-5):
+    """Compare per pixel; returns dict of counts."""
+    H, W = scene.H, scene.W
+    sel = np.ones((H, W), bool) if pixel_mask is None else pixel_mask
+    clean = sel & (ofw["n_amb"] == 0)
+    img_err = np.abs(gpu["image"] - ofw["image"]).max(axis=0)
+    T_err = np.abs(gpu["T_final"] - ofw["T_final"])
+    bad = clean & ((img_err > atol) | (T_err > atol) | (gpu["last"] != ofw["last"]))
+    if gpu["median"] is not None:
+        bad |= clean & (gpu["median"] != ofw["median"].astype(np.float32))
+    assert not bad.any(), _describe_bad(bad, gpu, ofw, img_err, T_err)
+    # knife edges: the GPU must take the normal outcome or one alternative
+    amb = np.argwhere(sel & (ofw["n_amb"] > 0))
+    alts = ofw["alts"]
+    unmatched = 0
+    for (y, x) in amb:
+        p = y * W + x
+        cands = [(ofw["image"][:, y, x], ofw["T_final"][y, x], ofw["last"][y, x],
+                  ofw["median"][y, x])]
+        for a in alts[alts["pixel"] == p]:
+            cands.append((a["image"], a["T_final"], a["last"], a["median"]))
+        ok = False
+        for im, T, last, med in cands:
+            if (np.abs(gpu["image"][:, y, x] - im).max() <= atol and abs(gpu["T_final"][y, x] - T) <= atol
+                    and gpu["last"][y, x] == last
+                    and (gpu["median"] is None or gpu["median"][y, x] == np.float32(med))):
+                ok = True
+                break
+        unmatched += not ok
+    assert unmatched == 0, "%d knife-edge pixels match no oracle outcome" % unmatched
+    return {"pixels": int(sel.sum()), "knife_edge": int(len(amb)),
+            "max_img_err": float(img_err[clean].max()) if clean.any() else 0.0}
+
+
+def _describe_bad(bad, gpu, ofw, img_err, T_err):
+    ys, xs = np.nonzero(bad)
+    y, x = ys[0], xs[0]
+    return ("%d pixels differ; first (%d,%d): img err %.3g T err %.3g last gpu %d oracle %d" %
+            (bad.sum(), x, y, img_err[y, x], T_err[y, x], gpu["last"][y, x], ofw["last"][y, x]))
+
+
+def check_backward(scene, gpu, obw, splat_mask=None):
+    n = scene.n
+    sel = np.ones(n, bool) if splat_mask is None else splat_mask
+    g = obw["grads"]
+    sl = obw["slack"]
+    report = {}
+    for k in GRAD_FIELDS:
+        ref = g[k].reshape(n, -1)
+        got = gpu[k].reshape(n, -1).astype(np.float64)
+        slack = sl[k].reshape(n, -1) if sl is not None else 0.0
+        tol = max(1e-4, 1e-3 * np.abs(ref[sel]).max(initial=0.0)) + slack
+        err = np.abs(got - ref)
+        bad = (err > tol) & sel[:, None]
+        assert not bad.any(), "%s: %d elements off; worst err %.3g tol %.3g (ref %.3g got %.3g)" % (
+            k, bad.sum(), err[bad].max(), np.broadcast_to(tol, err.shape)[bad][np.argmax(err[bad])],
+            ref[bad][np.argmax(err[bad])], got[bad][np.argmax(err[bad])])
+        report[k] = float((err[sel] / np.maximum(np.broadcast_to(tol, err.shape)[sel], 1e-30)).max(
+            initial=0.0))
+    if gpu["accum"] is not None:
+        ref = g["accum"]
+        tol = np.maximum(1e-5, obw["accum_err"]) + 2.0 ** -23 * np.abs(ref)
+        if sl is not None:
+            tol = tol + sl["accum"]
+        err = np.abs(gpu["accum"].astype(np.float64) - ref)
+        bad = (err > tol) & sel
+        assert not bad.any(), "accum: %d off; worst %.3g" % (bad.sum(), err[bad].max())
+        report["accum"] = float((err[sel] / tol[sel]).max(initial=0.0))
+    return report
+
+
+def full_parity(scene, capacity=None):
+    gpu = run_gpu(scene, capacity)
+    tl = check_pairs(scene, gpu)
+    ofw = oracle.forward(scene, tl["vals"], tl["offs"], alt_capacity=1 << 20)
+    f = check_forward(scene, gpu, ofw)
+    obw = oracle.backward(scene, tl["vals"], tl["offs"])
+    b = check_backward(scene, gpu, obw)
+    return {"fwd": f, "bwd": b, "pairs": tl["count"]}
+
+
+def sampled_parity(scene, n_tiles=192, n_splats=256, seed=0):
+    """Full-size check: every pair, sort and offset; the forward on a sample
+    of tiles; the gradients of a sample of splats (all of their tiles)."""
+    gpu = run_gpu(scene)
+    tl = check_pairs(scene, gpu)
+    tx, ty = oracle.tiles_xy(scene.W, scene.H)
+    T = tx * ty
+    rng = np.random.default_rng(seed)
+    mask = np.zeros(T, np.uint8)
+    mask[rng.choice(T, min(n_tiles, T), replace=False)] = 1
+    ofw = oracle.forward(scene, tl["vals"], tl["offs"], tile_mask=mask, alt_capacity=1 << 20)
+    pix = np.repeat(np.repeat(mask.reshape(ty, tx), 16, 0), 16, 1)[:scene.H, :scene.W].astype(bool)
+    f = check_forward(scene, gpu, ofw, pixel_mask=pix)
+    # splats with at least one pair; their tiles
+    keys, vals = tl["keys"], tl["vals"]
+    has = np.unique(vals)
+    pick = rng.choice(has, min(n_splats, has.size), replace=False)
+    smask = np.zeros(scene.n, bool)
+    smask[pick] = True
+    tmask = np.zeros(T, np.uint8)
+    tmask[(keys[smask[vals]] >> np.uint64(32)).astype(np.int64)] = 1
+    obw = oracle.backward(scene, tl["vals"], tl["offs"], tile_mask=tmask)
+    b = check_backward(scene, gpu, obw, splat_mask=smask)
+    return {"fwd": f, "bwd": b, "pairs": tl["count"], "bwd_tiles": int(tmask.sum())}

@@ -1,0 +1,117 @@
+"""The C-ABI library on the host (no GPU): it loads, exports every function
+that include/ss.h declares, reports the oracle's constants, sizes its
+workspace, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ss.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from gaussian_splatting_differentiable_gb300 import _lib
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ss_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("ss_bin_tiles", "ss_pair_count", "ss_sort_pairs", "ss_raster_fwd", "ss_raster_bwd",
+              "ss_workspace_bytes", "ss_last_error", "ss_constants"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from gaussian_splatting_differentiable_gb300 import _lib
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (ss_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    assert set(_lib.PROTOTYPES) == set(declared_functions())
+
+
+def test_constants_match_oracle(lib):
+    buf = (ctypes.c_float * 4)()
+    lib.ss_constants(buf)
+    c = oracle.constants()
+    assert buf[0] == np.float32(c["alpha_min"])
+    assert buf[1] == np.float32(c["alpha_max"])
+    assert buf[2] == np.float32(c["T_eps"])
+    assert buf[3] == c["tile"]
+    assert lib.ss_abi_version() == 1
+
+
+def test_workspace_bytes(lib):
+    a = lib.ss_workspace_bytes(2_000_000, 5_000_000, 1237, 822)
+    assert a >= 5_000_000 * 12 and a % 256 == 0
+    assert lib.ss_workspace_bytes(2_000_000, 0, 1237, 822) >= 2_000_000 * 8
+    assert lib.ss_workspace_bytes(0, 0, 1, 1) > 0
+    assert lib.ss_workspace_bytes(-1, 0, 16, 16) == 0
+    assert lib.ss_workspace_bytes(0, 0, 0, 16) == 0
+    assert lib.ss_workspace_bytes(0, 1 << 32, 16, 16) == 0
+    assert lib.ss_workspace_bytes(0, 0, 40000, 16) == 0
+
+
+def test_argument_errors_are_reported_before_any_launch(lib):
+    from gaussian_splatting_differentiable_gb300._lib import SsSplats, SsGrads
+    s = SsSplats(None, None, None, None, None, 10)
+    cnt = ctypes.c_void_p(0x1000)
+    # image size
+    assert lib.ss_bin_tiles(ctypes.byref(s), 0, 16, None, None, 0, cnt, None) == 5
+    assert "image" in lib.ss_last_error().decode()
+    # NULL splat arrays with n > 0
+    assert lib.ss_bin_tiles(ctypes.byref(s), 16, 16, None, None, 0, cnt, None) == 1
+    assert lib.ss_bin_tiles(None, 16, 16, None, None, 0, cnt, None) == 1
+    # counters NULL
+    s0 = SsSplats(None, None, None, None, None, 0)
+    assert lib.ss_bin_tiles(ctypes.byref(s0), 16, 16, None, None, 0, None, None) == 1
+    # sort: too many pairs, NULL offsets, unaligned workspace, small workspace
+    assert lib.ss_sort_pairs(None, None, 1 << 32, 16, 16, 0x1000, 0x1000, 1 << 30, None) == 5
+    assert lib.ss_sort_pairs(0x1000, 0x1000, 10, 16, 16, None, 0x1000, 1 << 30, None) == 1
+    assert lib.ss_sort_pairs(0x1000, 0x1000, 10, 16, 16, 0x1000, 0x1001, 1 << 30, None) == 1
+    assert lib.ss_sort_pairs(0x1000, 0x1000, 10, 16, 16, 0x1000, 0x1000, 16, None) == 1
+    assert "workspace" in lib.ss_last_error().decode()
+    # forward: unknown flags, NULL outputs, median flag without buffer
+    assert lib.ss_raster_fwd(ctypes.byref(s0), 0x1000, 0x1000, 16, 16, None, 8, 0x1000, 0x1000,
+                             0x1000, None, None) == 1
+    assert lib.ss_raster_fwd(ctypes.byref(s0), 0x1000, 0x1000, 16, 16, None, 0, None, 0x1000,
+                             0x1000, None, None) == 1
+    assert lib.ss_raster_fwd(ctypes.byref(s0), 0x1000, 0x1000, 16, 16, None, 2, 0x1000, 0x1000,
+                             0x1000, None, None) == 1
+    # backward: NULL gradient array, accum flag without buffer or workspace
+    sp = SsSplats(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 4)
+    g = SsGrads(0x1000, None, 0x1000, 0x1000)
+    assert lib.ss_raster_bwd(ctypes.byref(sp), 0x1000, 0x1000, 16, 16, None, 0, 0x1000, 0x1000,
+                             0x1000, ctypes.byref(g), None, None, 0, None) == 1
+    g = SsGrads(0x1000, 0x1000, 0x1000, 0x1000)
+    assert lib.ss_raster_bwd(ctypes.byref(sp), 0x1000, 0x1000, 16, 16, None, 1, 0x1000, 0x1000,
+                             0x1000, ctypes.byref(g), None, 0x1000, 1 << 20, None) == 1
+    assert lib.ss_raster_bwd(ctypes.byref(sp), 0x1000, 0x1000, 16, 16, None, 1, 0x1000, 0x1000,
+                             0x1000, ctypes.byref(g), 0x1000, 0x1000, 8, None) == 1
+    # pair count / sort status with NULL
+    assert lib.ss_pair_count(None, 0, None, None, None) == 1
+    assert lib.ss_sort_status(None, None) == 1
+    assert lib.ss_probe_red_f32(None, 1, 1, None) == 1
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    from gaussian_splatting_differentiable_gb300 import _lib
+    with pytest.raises(ImportError):
+        _lib.load(str(tmp_path / "nope.so"))

@@ -1,0 +1,145 @@
+"""Parity of the CUDA path against the CPU oracle on the GPU (through the C ABI).
+
+Workloads 1-3 are compared in full; the two 2M-splat workloads at their full
+size and launch configuration on every pair, the sorted order, the offsets,
+the forward on sampled tiles and the gradients of sampled splats.  Edge cases
+cover empty and culled inputs, ragged and tiny images, huge and off-screen
+splats, equal depths, dense tiles, the alpha cap, a background, every flag
+variant and the pair-capacity overflow path.
+"""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def P():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import parity
+    return parity
+
+
+@pytest.mark.parametrize("wl", [1, 2, 3])
+def test_workload_full_parity(P, wl):
+    r = P.full_parity(synth.make_scene(wl))
+    print("workload", wl, r)
+
+
+@pytest.mark.parametrize("wl", [4, 5])
+def test_workload_full_size_sampled_parity(P, wl):
+    r = P.sampled_parity(synth.make_scene(wl))
+    print("workload", wl, r)
+
+
+def _scene(W, H, n, seed=0, wl=1, **over):
+    sc = synth.make_scene(wl, seed=seed, n=n, W=W, H=H)
+    for k, v in over.items():
+        setattr(sc, k, v)
+    return sc
+
+
+@pytest.mark.parametrize("W,H", [(37, 23), (1, 1), (16, 16), (17, 1), (1, 300), (129, 65)])
+def test_ragged_and_tiny_images(P, W, H):
+    sc = _scene(W, H, 80, seed=W * 1000 + H)
+    sc.mean2d[:, 0] = sc.mean2d[:, 0] * 1.2 - 0.1 * W
+    sc.mean2d[:, 1] = sc.mean2d[:, 1] * 1.2 - 0.1 * H
+    P.full_parity(sc)
+
+
+def test_no_splats(P):
+    sc = _scene(40, 30, 0)
+    gpu = P.run_gpu(sc)
+    assert gpu["count"] == 0
+    assert np.all(gpu["offs"] == 0)
+    assert np.all(gpu["T_final"] == 1.0) and np.all(gpu["last"] == 0)
+    assert np.all(gpu["image"] == 0.0)
+
+
+def test_all_culled(P):
+    sc = _scene(48, 48, 100, seed=3)
+    sc.depth[:] = -1.0
+    gpu = P.run_gpu(sc)
+    assert gpu["count"] == 0 and gpu["culled"] == 100
+    assert all(np.all(gpu[k] == 0) for k in P.GRAD_FIELDS)
+
+
+def test_invalid_inputs_are_culled(P):
+    sc = _scene(64, 64, 200, seed=4)
+    sc.depth[::7] = 0.0
+    sc.conic[1::11, 1] = 5.0           # indefinite
+    sc.opacity[2::13] = 1e-3           # below 1/255
+    sc.mean2d[3::17, 0] = np.inf
+    sc.rgb[5::19, 2] = np.nan
+    P.full_parity(sc)
+
+
+def test_huge_and_offscreen_splats(P):
+    sc = _scene(100, 70, 60, seed=5)
+    sc.conic[:10] = synth.conic_from_scales(np.zeros(10), np.full(10, 40.0),
+                                            np.full(10, 25.0)).astype(np.float32)
+    sc.mean2d[10:20] += np.float32([500.0, 0.0])
+    sc.mean2d[20:30] -= np.float32([0.0, 300.0])
+    sc.mean2d[30:35] = np.float32([-20.0, -20.0])
+    P.full_parity(sc)
+
+
+def test_equal_depths_tie_break_by_index(P):
+    sc = _scene(64, 64, 400, seed=6)
+    sc.depth[:] = np.float32(3.0)
+    sc.depth[::3] = np.float32(2.0)
+    P.full_parity(sc)
+
+
+def test_dense_single_tile_many_batches(P):
+    """3000 splats in one tile: many 256-splat batches, early termination."""
+    sc = _scene(16, 16, 3000, seed=7)
+    sc.opacity[:] = np.float32(0.05)
+    P.full_parity(sc)
+    sc.opacity[:] = np.float32(0.02)   # survives deep into the list
+    P.full_parity(sc)
+
+
+def test_alpha_cap_and_background(P):
+    sc = _scene(64, 48, 150, seed=8)
+    sc.opacity[:40] = np.float32(1.0)   # alpha capped at 0.99 near their centres
+    sc.bg = np.float32([0.25, 0.5, 0.75])
+    P.full_parity(sc)
+
+
+@pytest.mark.parametrize("accum,median", [(False, False), (True, False), (False, True),
+                                          (True, True)])
+def test_flag_variants(P, accum, median):
+    sc = _scene(96, 80, 500, seed=9, wl=2)
+    sc.accum_weight, sc.median_depth = accum, median
+    P.full_parity(sc)
+
+
+def test_capacity_overflow_reports_and_recovers(P):
+    import torch
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = _scene(128, 128, 400, seed=10, wl=2)
+    sp = ss.Splats.from_numpy(sc)
+    keys = torch.full((50,), -1, dtype=torch.int64, device="cuda")
+    vals = torch.full((50,), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(2, dtype=torch.int64, device="cuda")
+    ss.ss_bin_tiles(sp, sc.W, sc.H, keys, vals, 40, cnt)
+    st, pairs, culled = ss.ss_pair_count(cnt, 40)
+    import oracle
+    assert st == ss.SS_ERR_CAPACITY and pairs == oracle.tile_lists(sc)["count"] > 40
+    # nothing written past the capacity
+    assert torch.all(keys[40:] == -1) and torch.all(vals[40:] == -1)
+    assert "capacity" in ss.ss_last_error()
+    P.full_parity(sc, capacity=pairs)
+
+
+def test_two_calls_in_a_row_agree(P):
+    sc = synth.make_scene(2)
+    a = P.run_gpu(sc)
+    b = P.run_gpu(sc)
+    for k in ("keys", "vals", "offs", "image", "T_final", "last", "accum"):
+        assert np.array_equal(a[k], b[k]), k
