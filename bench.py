@@ -272,6 +272,10 @@ def run_ours(args, rank: int, world: int, dist):
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = statistics.mean(step_ms)
+    print("step ms: mean %.4f min %.4f max %.4f; kernels %s" % (
+        ms, min(step_ms), max(step_ms), prof), file=sys.stderr, flush=True)
+    if not prof:
+        raise RuntimeError("SS_PROFILE recorded no kernel launches")
     if dist:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -376,7 +380,7 @@ def run_ours(args, rank: int, world: int, dist):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_tiles = 12
+        n_tiles = 256   # ~10-30 s of single-core oracle work
         t_step, det = oracle_sample(scene, n_tiles)
         cpu = {"value": det["full_candidates"] / t_step, "unit": UNIT, "cores": 1,
                "kind": "oracle",

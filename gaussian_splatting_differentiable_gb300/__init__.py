@@ -162,8 +162,7 @@ def ss_profile_enable(on: bool) -> None:
 
 def ss_profile_collect() -> dict:
     """{kernel name: (launches, total_ms, min_ms, max_ms)} since the last collect."""
-    n = _L.ss_profile_collect(None, 0)
-    buf = ctypes.create_string_buffer(int(n) + 1)
+    buf = ctypes.create_string_buffer(1 << 20)   # one line per kernel name
     _L.ss_profile_collect(buf, len(buf))
     out = {}
     for line in buf.value.decode().splitlines():
@@ -175,6 +174,11 @@ def ss_profile_collect() -> dict:
 def ss_probe_red_f32(buf, rounds: int, stream=None) -> None:
     _check(_L.ss_probe_red_f32(_ptr(buf), buf.numel(), rounds, _stream(stream)),
            "ss_probe_red_f32")
+
+
+def ss_test_sort_wait_timeout(workspace, stream=None) -> None:
+    _check(_L.ss_test_sort_wait_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "ss_test_sort_wait_timeout")
 
 
 # ------------------------------------------------------------------ whole path

@@ -49,6 +49,7 @@ PROTOTYPES = {
     "ss_profile_enable": (None, [I32]),
     "ss_profile_collect": (I64, [ctypes.c_char_p, SZ]),
     "ss_probe_red_f32": (ctypes.c_int, [P, I64, I32, P]),
+    "ss_test_sort_wait_timeout": (ctypes.c_int, [P, SZ, P]),
 }
 
 _lib = None

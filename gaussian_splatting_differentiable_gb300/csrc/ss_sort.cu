@@ -267,6 +267,8 @@ __global__ void __launch_bounds__(256) k_sort_final(const uint64_t *__restrict__
 
 static int g_attr_set[64];
 
+__global__ void k_set_u32(uint32_t *p, uint32_t v) { *p = v; }
+
 }  // namespace ss
 
 using namespace ss;
@@ -345,4 +347,40 @@ extern "C" ss_status ss_sort_pairs(uint64_t *keys, uint32_t *vals, int64_t n_pai
               k_sort_final<<<int(blocks), 256, 0, st>>>(bk[r], bv[r], keys, vals, n_pairs, tiles,
                                                         tile_offsets, err));
     return check_launch("ss_sort_pairs");
+}
+
+// Test hook: one onesweep pass CTA that holds partition 1 of a 2-partition
+// problem whose partition 0 never publishes, so its look-back wait runs out
+// (a flag that nothing sets).  All of its reads and writes stay inside the
+// workspace: keys are the zeroed ping-pong buffer, every key has digit 0 and
+// lands in the first partition's range.
+extern "C" ss_status ss_test_sort_wait_timeout(void *workspace, size_t workspace_bytes,
+                                               ss_stream_t stream) {
+    clear_error();
+    const int64_t n = 2 * kSortPart;
+    const WsLayout L = ws_layout(0, n, kTile, kTile);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return fail(SS_ERR_INVALID_ARG, "ss_test_sort_wait_timeout: workspace NULL or unaligned");
+    if (workspace_bytes < L.sort_end)
+        return fail(SS_ERR_INVALID_ARG, "ss_test_sort_wait_timeout: workspace %zu bytes < %zu",
+                    workspace_bytes, L.sort_end);
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    ss_status s = check_cuda(cudaMemsetAsync(ws, 0, L.sort_end, st), "memset");
+    if (s != SS_OK) return s;
+    uint32_t *tickets = reinterpret_cast<uint32_t *>(ws + L.tickets);
+    SS_LAUNCH("k_set_u32", st, k_set_u32<<<1, 1, 0, st>>>(tickets, 1u));
+    PassParams p{};
+    p.kin = reinterpret_cast<const uint64_t *>(ws + L.alt_keys);
+    p.vin = reinterpret_cast<const uint32_t *>(ws + L.alt_vals);
+    p.kout = reinterpret_cast<uint64_t *>(ws + L.alt_keys);
+    p.vout = reinterpret_cast<uint32_t *>(ws + L.alt_vals);
+    p.n = n;
+    p.shift = 0;
+    p.gofs = reinterpret_cast<const uint32_t *>(ws + L.gofs);
+    p.lookback = reinterpret_cast<uint64_t *>(ws + L.lookback);
+    p.ticket = tickets;
+    p.err = reinterpret_cast<uint32_t *>(ws + L.status_word);
+    SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<1, 256, kSortPart * 12, st>>>(p));
+    return check_launch("ss_test_sort_wait_timeout");
 }

@@ -214,6 +214,7 @@ void ss_profile_enable(int32_t on);
 /* Host: waits for the events recorded since the last collect and writes one
  * line per kernel name, "name launches total_ms min_ms max_ms\n", into
  * buf[0..len) (NUL-terminated, truncated if short; buf may be NULL).
+ * The records are consumed by the call, with or without a buffer.
  * Returns the full length of the text. */
 int64_t ss_profile_collect(char *buf, size_t len);
 
@@ -223,6 +224,14 @@ int64_t ss_profile_collect(char *buf, size_t len);
  * by the caller, it gives the L2 atomic throughput that bounds the backward
  * pass's gradient accumulation. */
 ss_status ss_probe_red_f32(float *buf, int64_t n, int32_t rounds, ss_stream_t stream);
+
+/* Test hook for failure detection, not part of the path: runs one onesweep
+ * pass CTA whose look-back waits on a partition that never publishes, so
+ * the bounded wait gives up (after roughly 0.2-0.5 s); ss_sort_status on the
+ * same workspace then returns SS_ERR_TIMEOUT and the CUDA context stays
+ * usable.  workspace: >= ss_workspace_bytes(0, 8192, 16, 16) bytes, 256-byte
+ * aligned; its contents are overwritten. */
+ss_status ss_test_sort_wait_timeout(void *workspace, size_t workspace_bytes, ss_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -143,3 +143,22 @@ def test_two_calls_in_a_row_agree(P):
     b = P.run_gpu(sc)
     for k in ("keys", "vals", "offs", "image", "T_final", "last", "accum"):
         assert np.array_equal(a[k], b[k]), k
+
+
+def test_profile_counts_every_launch(P):
+    import torch
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = synth.make_scene(2)
+    sp = ss.Splats.from_numpy(sc)
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, 4 * sc.n, ss.SS_ACCUM_WEIGHT, device="cuda")
+    dL = torch.from_numpy(sc.dL_dimage).cuda()
+    ss.ss_profile_collect()
+    ss.ss_profile_enable(True)
+    r.step(sp, dL)
+    r.step(sp, dL)
+    ss.ss_profile_enable(False)
+    prof = ss.ss_profile_collect()
+    assert prof["k_emit_pairs"][0] == 2 and prof["k_raster_bwd"][0] == 2
+    assert prof["k_sort_pass"][0] == 2 * 5   # 8 tile bits + 32 depth bits -> 5 digits
+    assert all(v[1] > 0 for v in prof.values())
+    assert ss.ss_profile_collect() == {}
