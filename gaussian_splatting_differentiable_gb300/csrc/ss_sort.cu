@@ -267,6 +267,19 @@ __global__ void __launch_bounds__(256) k_sort_final(const uint64_t *__restrict__
 
 static int g_attr_set[64];
 
+// k_sort_pass needs 48 KB of dynamic shared memory on top of its static
+// arrays: raise its limit once per device.
+static ss_status ensure_pass_smem(int dyn) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && g_attr_set[dev]) return SS_OK;
+    ss_status s = check_cuda(
+        cudaFuncSetAttribute(k_sort_pass, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn),
+        "ss_sort_pairs: cudaFuncSetAttribute");
+    if (s == SS_OK && dev >= 0 && dev < 64) g_attr_set[dev] = 1;
+    return s;
+}
+
 __global__ void k_set_u32(uint32_t *p, uint32_t v) { *p = v; }
 
 }  // namespace ss
@@ -307,13 +320,8 @@ extern "C" ss_status ss_sort_pairs(uint64_t *keys, uint32_t *vals, int64_t n_pai
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int dyn = kSortPart * 12;
-    if (dev < 64 && !g_attr_set[dev]) {
-        s = check_cuda(cudaFuncSetAttribute(k_sort_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            dyn),
-                       "ss_sort_pairs: cudaFuncSetAttribute");
-        if (s != SS_OK) return s;
-        g_attr_set[dev] = 1;
-    }
+    s = ensure_pass_smem(dyn);
+    if (s != SS_OK) return s;
 
     uint32_t *hist = reinterpret_cast<uint32_t *>(ws + L.hist);
     uint32_t *gofs = reinterpret_cast<uint32_t *>(ws + L.gofs);
@@ -367,6 +375,8 @@ extern "C" ss_status ss_test_sort_wait_timeout(void *workspace, size_t workspace
     cudaStream_t st = (cudaStream_t)stream;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     ss_status s = check_cuda(cudaMemsetAsync(ws, 0, L.sort_end, st), "memset");
+    if (s != SS_OK) return s;
+    s = ensure_pass_smem(kSortPart * 12);
     if (s != SS_OK) return s;
     uint32_t *tickets = reinterpret_cast<uint32_t *>(ws + L.tickets);
     SS_LAUNCH("k_set_u32", st, k_set_u32<<<1, 1, 0, st>>>(tickets, 1u));
