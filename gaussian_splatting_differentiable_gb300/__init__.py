@@ -156,6 +156,21 @@ def ss_raster_bwd(splats: Splats, vals, tile_offsets, W: int, H: int, bg, flags:
                             _ptr(workspace), nbytes, _stream(stream)), "ss_raster_bwd")
 
 
+def ss_raster_bwd_noalloc(splats: Splats, vals, tile_offsets, W: int, H: int, bg, flags: int,
+                          T_final, last_contrib, dL_dimage, grads: dict, accum_weight,
+                          stream=None) -> None:
+    """ss_raster_bwd for callers that cannot allocate: no workspace argument;
+    the weight scratch is a fixed array inside the library (at most 2,097,152
+    splats; concurrent calls race on it)."""
+    s = splats.c()
+    g = SsGrads(_ptr(grads["dmean2d"]), _ptr(grads["dconic"]), _ptr(grads["dopacity"]),
+                _ptr(grads["drgb"]))
+    _check(_L.ss_raster_bwd_noalloc(ctypes.byref(s), _ptr(vals), _ptr(tile_offsets), W, H,
+                                    _f32_host3(bg), flags, _ptr(T_final), _ptr(last_contrib),
+                                    _ptr(dL_dimage), ctypes.byref(g), _ptr(accum_weight),
+                                    _stream(stream)), "ss_raster_bwd_noalloc")
+
+
 def ss_profile_enable(on: bool) -> None:
     _L.ss_profile_enable(1 if on else 0)
 

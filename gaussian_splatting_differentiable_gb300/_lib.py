@@ -46,6 +46,8 @@ PROTOTYPES = {
                                      P, P]),
     "ss_raster_bwd": (ctypes.c_int, [ctypes.POINTER(SsSplats), P, P, I32, I32, P, U32, P, P, P,
                                      ctypes.POINTER(SsGrads), P, P, SZ, P]),
+    "ss_raster_bwd_noalloc": (ctypes.c_int, [ctypes.POINTER(SsSplats), P, P, I32, I32, P, U32, P,
+                                             P, P, ctypes.POINTER(SsGrads), P, P]),
     "ss_profile_enable": (None, [I32]),
     "ss_profile_collect": (I64, [ctypes.c_char_p, SZ]),
     "ss_probe_red_f32": (ctypes.c_int, [P, I64, I32, P]),

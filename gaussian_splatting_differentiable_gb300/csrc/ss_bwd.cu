@@ -303,3 +303,113 @@ extern "C" ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals
         SS_LAUNCH("k_accum_final", st, k_accum_final<<<zgrid, 256, 0, st>>>(p.accum, accum_weight, n));
     return check_launch("ss_raster_bwd");
 }
+
+// ---------------------------------------------------------------------------
+// ss_raster_bwd_noalloc: the backward pass for callers that cannot allocate.
+//
+// Some callers may not call cudaMalloc, and cannot hand the library a
+// workspace either: plugins living inside an application that owns all
+// device memory through its own pool, or real-time render threads that must
+// not risk the device-wide synchronisation that cudaMalloc / cudaFree can
+// cause.  For them the accumulated-weight scratch of the backward (one
+// 32.32 fixed-point uint64 per splat) lives in the fixed array below
+// instead of a caller workspace.  Every GPU that loads the library holds it
+// (16 MiB) until the process exits.
+//
+// The array is shared by every call: each call clears the part it uses
+// before accumulating, but two calls that run at the same time on the GPU
+// (different streams, or different host threads) race on it and corrupt each
+// other's accumulated weights.  Serialise them.
+namespace ss {
+
+constexpr int32_t kNoAllocMaxSplats = 1 << 21;  // 2,097,152 splats -> 16 MiB of scratch
+
+static __device__ __align__(256) unsigned long long g_noalloc_accum[kNoAllocMaxSplats];
+
+static unsigned long long *g_noalloc_ptr[64];  // device address of the array, per device
+
+}  // namespace ss
+
+extern "C" ss_status ss_raster_bwd_noalloc(const ss_splats *splats, const uint32_t *vals,
+                                           const uint32_t *tile_offsets, int32_t W, int32_t H,
+                                           const float *bg, uint32_t flags, const float *T_final,
+                                           const uint32_t *last_contrib, const float *dL_dimage,
+                                           const ss_grads *grads, float *accum_weight,
+                                           ss_stream_t stream) {
+    clear_error();
+    if (!splats) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: splats is NULL");
+    if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
+        return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd_noalloc: image %dx%d outside 1..%d", W, H,
+                    kMaxSide);
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: unknown flag bits 0x%x", flags);
+    const int32_t n = splats->n;
+    if (n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: n < 0");
+    if (n > kNoAllocMaxSplats)
+        return fail(SS_ERR_UNSUPPORTED,
+                    "ss_raster_bwd_noalloc: %d splats exceed its fixed scratch of %d splats; "
+                    "use ss_raster_bwd with a workspace",
+                    n, kNoAllocMaxSplats);
+    if (n > 0 && (!splats->mean2d || !splats->conic || !splats->opacity || !splats->rgb ||
+                  !splats->depth))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: a splat array is NULL");
+    if (!vals || !tile_offsets)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: vals/offsets NULL");
+    if (!T_final || !last_contrib || !dL_dimage)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: T_final/last_contrib/dL_dimage NULL");
+    if (!grads || (n > 0 && (!grads->dmean2d || !grads->dconic || !grads->dopacity || !grads->drgb)))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: a gradient array is NULL");
+    const bool accum = flags & SS_ACCUM_WEIGHT;
+    if (accum && n > 0 && !accum_weight)
+        return fail(SS_ERR_INVALID_ARG,
+                    "ss_raster_bwd_noalloc: SS_ACCUM_WEIGHT set but accum_weight NULL");
+    if (n > 0 && (reinterpret_cast<uintptr_t>(splats->mean2d) & 7))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: mean2d not 8-byte aligned");
+    if (n == 0) return SS_OK;
+
+    int dev = 0, sms = 0;
+    ss_status s = check_cuda(cudaGetDevice(&dev), "ss_raster_bwd_noalloc: cudaGetDevice");
+    if (s != SS_OK) return s;
+    if (dev < 0 || dev >= 64)
+        return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd_noalloc: device %d >= 64", dev);
+    if (accum && !g_noalloc_ptr[dev]) {
+        // First call on this device (with this device current): look up the
+        // array's device address once.
+        void *ptr = nullptr;
+        s = check_cuda(cudaGetSymbolAddress(&ptr, g_noalloc_accum),
+                       "ss_raster_bwd_noalloc: cudaGetSymbolAddress");
+        if (s != SS_OK) return s;
+        g_noalloc_ptr[dev] = static_cast<unsigned long long *>(ptr);
+    }
+
+    BwdParams p{};
+    p.s = SplatPtrs{splats->mean2d, splats->conic, splats->opacity, splats->rgb, splats->depth, n};
+    p.vals = vals;
+    p.offs = tile_offsets;
+    p.W = W;
+    p.H = H;
+    p.tiles_x = tiles_x(W);
+    for (int c = 0; c < 3; ++c) p.bg[c] = bg ? bg[c] : 0.0f;
+    p.T_final = T_final;
+    p.last = last_contrib;
+    p.dL = dL_dimage;
+    p.dmean2d = grads->dmean2d;
+    p.dconic = grads->dconic;
+    p.dopacity = grads->dopacity;
+    p.drgb = grads->drgb;
+    p.accum = accum ? g_noalloc_ptr[dev] : nullptr;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (int64_t(n) + 255) / 256;
+    const int zgrid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+    // k_bwd_zero clears this call's part of the shared array before use.
+    SS_LAUNCH("k_bwd_zero", st, k_bwd_zero<<<zgrid, 256, 0, st>>>(p, n, accum));
+    const int grid = tiles_x(W) * tiles_y(H);
+    if (accum)
+        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true><<<grid, 256, 0, st>>>(p));
+    else
+        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false><<<grid, 256, 0, st>>>(p));
+    if (accum)
+        SS_LAUNCH("k_accum_final", st, k_accum_final<<<zgrid, 256, 0, st>>>(p.accum, accum_weight, n));
+    return check_launch("ss_raster_bwd_noalloc");
+}

@@ -204,6 +204,30 @@ ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals,
                         const float *dL_dimage, const ss_grads *grads, float *accum_weight,
                         void *workspace, size_t workspace_bytes, ss_stream_t stream);
 
+/* The backward pass for callers that cannot allocate (the pages have no
+ * counterpart: this is a property of the library, not of the method).
+ * Some callers may not call cudaMalloc and cannot provide a workspace: a
+ * plugin inside an application that owns all device memory through its own
+ * pool, or a real-time thread that must not risk the device-wide
+ * synchronisation cudaMalloc / cudaFree can cause.  This entry point
+ * computes exactly what ss_raster_bwd computes, with the same arguments
+ * minus the workspace, and calls no allocator: the accumulated-weight
+ * scratch (8 bytes per splat) is a fixed array inside the library,
+ * 2,097,152 splats (16 MiB), which every GPU that loads the library holds
+ * until the process exits.
+ *   - n > 2,097,152 returns SS_ERR_UNSUPPORTED (use ss_raster_bwd).
+ *   - The first call on a device, made with that device current, looks up
+ *     the array's device address (cudaGetSymbolAddress); make that first
+ *     call before any stream capture.
+ *   - All calls share the array.  Each call clears the part it uses, but
+ *     calls that overlap on the GPU (other streams, other host threads) race
+ *     on it: serialise them. */
+ss_status ss_raster_bwd_noalloc(const ss_splats *splats, const uint32_t *vals,
+                                const uint32_t *tile_offsets, int32_t W, int32_t H,
+                                const float *bg, uint32_t flags, const float *T_final,
+                                const uint32_t *last_contrib, const float *dL_dimage,
+                                const ss_grads *grads, float *accum_weight, ss_stream_t stream);
+
 /* Per-kernel timing ("从 8.6 KB 到 4.2 KB ...", section 亲手验证: SS_PROFILE=1
  * gives per-kernel segment timings).  Off unless the environment has
  * SS_PROFILE=1 when the library loads or ss_profile_enable(1) is called.
