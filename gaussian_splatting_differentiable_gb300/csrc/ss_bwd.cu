@@ -13,14 +13,24 @@
 //
 // Reduction.  The pages' baseline issues 9 atomics per (pixel, splat); their
 // proposed fix sums each field across the warp first and issues one atomic
-// per warp ("Phase 5 step 30b", conclusion).  Here the warp's 10 fields
-// (9 gradients + the accumulated weight) are reduced together by a
-// reduce-scatter butterfly: at each of the 5 xor steps every lane keeps half
-// of its remaining fields and trades the other half with its partner, so
-// 5 + 3 + 2 + 1 + 1 = 12 shuffles (instead of 10 x 5 = 50) leave each field's
-// warp total in one even lane; those 10 lanes then issue the warp's atomics
-// as one instruction.  Warps where no pixel blends the splat skip all of it
-// (a warp vote).  The accumulated weight is summed in 32.32 fixed point with
+// per warp ("Phase 5 step 30b", conclusion).  Summing 10 fields across 32
+// lanes with shuffles costs ~46 instructions per (warp, splat), while only
+// ~9 of the 32 pixels of a warp touch a given splat.  Here the sum is
+// transposed instead: every field is linear in two per-pixel scalars,
+//   q = dL/dsigma  and  w = alpha T  (the pixel's blend weight),
+// so for each splat blended somewhere in the warp the 32 pixels write (q, w)
+// into a shared-memory slot (zeros where the splat is not blended), and
+// once 16 slots are full each lane pair takes one slot and sums its 32
+// pixels with plain FMAs into ten moments:
+//   Q = sum q, Qx = sum q dx, Qy = sum q dy, Qxx, Qxy, Qyy, W = sum w,
+//   Wr, Wg, Wb = sum w dL/dimage_c,
+// from which (a dx + b dy = -(2A dx + B dy) ln 2 with the base-2 scaled
+// A, B, C of the staged splat)
+//   dmean = ln2 (2A Qx + B Qy, B Qx + 2C Qy),  dconic = (Qxx/2, Qxy, Qyy/2),
+//   dopacity = -Q / o  (G dL/dalpha = -q / o when alpha is not capped),
+//   drgb = (Wr, Wg, Wb),  accumulated weight = W,
+// and issues the splat's 10 atomics (one per field per warp, as the pages
+// propose).  The accumulated weight is added in 32.32 fixed point with
 // 64-bit integer atomics, so it is exact and independent of atomic order.
 #include "ss_device.cuh"
 #include "ss_internal.h"
@@ -41,37 +51,94 @@ struct BwdParams {
     unsigned long long *accum;  // 32.32 fixed point
 };
 
-// One butterfly step of the reduce-scatter: N values, lanes with `hi` set
-// keep the upper half, the others the lower half (zero-padded), each adding
-// its partner's copy of the kept half.  Result in v[0 .. (N+1)/2).
-template <int N>
-__device__ __forceinline__ void rs_step(float *v, int off, bool hi) {
-    constexpr int H = (N + 1) / 2;
-#pragma unroll
-    for (int k = 0; k < H; ++k) {
-        const float lo_v = v[k];
-        const float hi_v = (k + H < N) ? v[k + H] : 0.0f;
-        const float send = hi ? lo_v : hi_v;
-        const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-        v[k] = (hi ? hi_v : lo_v) + recv;
-    }
+constexpr int kSlots = 16;     // slots per warp
+constexpr int kSlotPad = 33;   // row pitch: lane pairs read 32 rows without bank conflicts
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-// Field whose warp total lane `lane` holds after the reduce-scatter of 10
-// values, or -1: field = 5 h16 + 3 h8 + 2 h4 + h2 (h* = lane bits), valid
-// when 2 h4 + h2 < 3 and 3 h8 + 2 h4 + h2 < 5, and only even lanes.
-__device__ __forceinline__ int rs_field(int lane) {
-    if (lane & 1) return -1;
-    const int h2 = (lane >> 1) & 1, h4 = (lane >> 2) & 1, h8 = (lane >> 3) & 1, h16 = (lane >> 4) & 1;
-    const int b = 2 * h4 + h2;
-    if (b >= 3) return -1;
-    const int a = 3 * h8 + b;
-    if (a >= 5) return -1;
-    return 5 * h16 + a;
+// Per-warp slot storage.
+struct __align__(16) SlotRec {
+    float mx, my, A, B;   // staged geometry of the slot's splat
+    float C, o;
+    uint32_t idx, pad;
+};
+
+template <bool ACCUM>
+__device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int lane, float wx0,
+                                            float wy0, const float (*q)[kSlotPad],
+                                            const float (*w)[kSlotPad], const float4 *g,
+                                            const SlotRec *rec) {
+    __syncwarp();
+    // Every lane runs the sums (lanes of unused slots read stale, in-bounds
+    // rows) so that the pair shuffles see the whole warp; only the atomics
+    // are limited to the filled slots.
+    const int slot = lane >> 1, half = lane & 1;
+    {
+        const SlotRec r = rec[slot];
+        float dxu[8], dyv[2];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dxu[u] = __fsub_rn(wx0 + float(u), r.mx);
+#pragma unroll
+        for (int v = 0; v < 2; ++v) dyv[v] = __fsub_rn(wy0 + float(2 * half + v), r.my);
+        float Q = 0.f, Qx = 0.f, Qy = 0.f, Qxx = 0.f, Qxy = 0.f, Qyy = 0.f;
+        float Wt = 0.f, Wr = 0.f, Wg = 0.f, Wb = 0.f;
+        const float *qs = q[slot] + 16 * half;
+        const float *ws = w[slot] + 16 * half;
+        const float4 *gs = g + 16 * half;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float qi = qs[i], wi = ws[i];
+            const float dx = dxu[i & 7], dy = dyv[i >> 3];
+            Q += qi;
+            const float t = qi * dx;
+            Qx += t;
+            Qxx = fmaf(t, dx, Qxx);
+            Qxy = fmaf(t, dy, Qxy);
+            const float s = qi * dy;
+            Qy += s;
+            Qyy = fmaf(s, dy, Qyy);
+            const float4 gg = gs[i];
+            Wt += wi;
+            Wr = fmaf(wi, gg.x, Wr);
+            Wg = fmaf(wi, gg.y, Wg);
+            Wb = fmaf(wi, gg.z, Wb);
+        }
+        // Sum the two halves of the slot (lanes 2k and 2k+1).
+        Q += __shfl_xor_sync(0xffffffffu, Q, 1, 2);
+        Qx += __shfl_xor_sync(0xffffffffu, Qx, 1, 2);
+        Qy += __shfl_xor_sync(0xffffffffu, Qy, 1, 2);
+        Qxx += __shfl_xor_sync(0xffffffffu, Qxx, 1, 2);
+        Qxy += __shfl_xor_sync(0xffffffffu, Qxy, 1, 2);
+        Qyy += __shfl_xor_sync(0xffffffffu, Qyy, 1, 2);
+        Wt += __shfl_xor_sync(0xffffffffu, Wt, 1, 2);
+        Wr += __shfl_xor_sync(0xffffffffu, Wr, 1, 2);
+        Wg += __shfl_xor_sync(0xffffffffu, Wg, 1, 2);
+        Wb += __shfl_xor_sync(0xffffffffu, Wb, 1, 2);
+        const size_t i = r.idx;
+        if (slot >= nslots) {
+        } else if (half == 0) {
+            atomicAdd(p.dmean2d + 2 * i, kLn2 * (2.0f * r.A * Qx + r.B * Qy));
+            atomicAdd(p.dmean2d + 2 * i + 1, kLn2 * (r.B * Qx + 2.0f * r.C * Qy));
+            atomicAdd(p.dconic + 3 * i, 0.5f * Qxx);
+            atomicAdd(p.dconic + 3 * i + 1, Qxy);
+            atomicAdd(p.dconic + 3 * i + 2, 0.5f * Qyy);
+        } else {
+            atomicAdd(p.dopacity + i, -Q / r.o);
+            atomicAdd(p.drgb + 3 * i, Wr);
+            atomicAdd(p.drgb + 3 * i + 1, Wg);
+            atomicAdd(p.drgb + 3 * i + 2, Wb);
+            if (ACCUM) atomicAdd(p.accum + i, (unsigned long long)__float2ull_rn(Wt * 4294967296.0f));
+        }
+    }
+    __syncwarp();
 }
 
 template <bool ACCUM>
-__global__ void __launch_bounds__(256) k_raster_bwd(BwdParams p) {
+__global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     __shared__ SplatGeo s_geo[256];
     __shared__ SplatGeo2 s_geo2[256];
     __shared__ SplatCol s_col[256];
@@ -79,6 +146,12 @@ __global__ void __launch_bounds__(256) k_raster_bwd(BwdParams p) {
     __shared__ uint32_t s_idx[256];
     __shared__ uint8_t s_list[8][256];
     __shared__ uint32_t s_wmax[8];
+    __shared__ float4 s_g[8][32];
+    __shared__ SlotRec s_rec[8][kSlots];
+    // dynamic: q and w slots, [8 warps][kSlots][kSlotPad] floats each
+    extern __shared__ __align__(16) float s_dyn[];
+    float(*s_q)[kSlots][kSlotPad] = reinterpret_cast<float(*)[kSlots][kSlotPad]>(s_dyn);
+    float(*s_w)[kSlots][kSlotPad] = reinterpret_cast<float(*)[kSlots][kSlotPad]>(s_dyn + 8 * kSlots * kSlotPad);
 
     const int tile = blockIdx.x;
     const int tx = tile % p.tiles_x, ty = tile / p.tiles_x;
@@ -102,6 +175,7 @@ __global__ void __launch_bounds__(256) k_raster_bwd(BwdParams p) {
         g1 = p.dL[HW + pix];
         g2 = p.dL[2 * HW + pix];
     }
+    s_g[warp][lane] = make_float4(g0, g1, g2, 0.0f);
     const float Tb0 = T * p.bg[0], Tb1 = T * p.bg[1], Tb2 = T * p.bg[2];
     float S0 = 0.0f, S1 = 0.0f, S2 = 0.0f;
 
@@ -112,16 +186,7 @@ __global__ void __launch_bounds__(256) k_raster_bwd(BwdParams p) {
 #pragma unroll
     for (int w = 0; w < 8; ++w) bmax = max(bmax, s_wmax[w]);
 
-    // Where this lane's reduced field goes.
-    const int fld = rs_field(lane);
-    float *fptr = nullptr;
-    int fstride = 0;
-    if (fld >= 0 && fld < 2) { fptr = p.dmean2d + fld; fstride = 2; }
-    else if (fld >= 2 && fld < 5) { fptr = p.dconic + (fld - 2); fstride = 3; }
-    else if (fld == 5) { fptr = p.dopacity; fstride = 1; }
-    else if (fld >= 6 && fld < 9) { fptr = p.drgb + (fld - 6); fstride = 3; }
-    const bool hi16 = lane & 16, hi8 = lane & 8, hi4 = lane & 4, hi2 = lane & 2;
-
+    int nslots = 0;  // warp-uniform
     for (int32_t hi = int32_t(bmax); hi > 0; hi -= 256) {
         const int32_t lo = hi > 256 ? hi - 256 : 0;
         const int nb = hi - lo;
@@ -156,56 +221,58 @@ __global__ void __launch_bounds__(256) k_raster_bwd(BwdParams p) {
             const float e2 = eval_e2(g, gg.C, px, py, dx, dy);
             const bool act = uint32_t(lo + j) < n_p && e2 >= gg.thr;
             if (!__any_sync(0xffffffffu, act)) continue;
-            float v[10];
-#pragma unroll
-            for (int k = 0; k < 10; ++k) v[k] = 0.0f;
+            const SplatCol c = s_col[j];
+            float qv = 0.0f, wv = 0.0f;
             if (act) {
-                const SplatCol c = s_col[j];
                 const float G = ex2_approx(e2);
                 float oG;
                 const float alpha = eval_alpha(c.o, G, oG);
-                const float om = __fsub_rn(1.0f, alpha);
-                const float inv = __frcp_rn(om);
-                const float Ti = T * inv;          // T in front of this splat
-                const float w = alpha * Ti;
+                const float inv = rcp_approx(__fsub_rn(1.0f, alpha));
+                const float Ti = T * inv;  // T in front of this splat
+                wv = alpha * Ti;
                 const float dLda = g0 * (c.r * Ti - (S0 + Tb0) * inv) +
                                    g1 * (c.g * Ti - (S1 + Tb1) * inv) +
                                    g2 * (c.b * Ti - (S2 + Tb2) * inv);
-                v[6] = g0 * w;
-                v[7] = g1 * w;
-                v[8] = g2 * w;
-                v[9] = w;
-                if (oG <= kAlphaMax) {  // through the cap alpha is constant
-                    const float dsig = -alpha * dLda;  // dL/dsigma
-                    v[5] = G * dLda;                   // dL/dopacity
-                    // a dx + b dy = -(2A dx + B dy) ln 2 (A, B, C are base-2 scaled)
-                    const float s = dsig * kLn2;
-                    v[0] = s * (2.0f * g.A * dx + g.B * dy);   // -dsig (a dx + b dy)
-                    v[1] = s * (g.B * dx + 2.0f * gg.C * dy);  // -dsig (b dx + c dy)
-                    v[2] = 0.5f * dsig * dx * dx;
-                    v[3] = dsig * dx * dy;
-                    v[4] = 0.5f * dsig * dy * dy;
-                }
-                S0 = fmaf(c.r, w, S0);
-                S1 = fmaf(c.g, w, S1);
-                S2 = fmaf(c.b, w, S2);
+                qv = oG <= kAlphaMax ? -alpha * dLda : 0.0f;  // through the cap alpha is constant
+                S0 = fmaf(c.r, wv, S0);
+                S1 = fmaf(c.g, wv, S1);
+                S2 = fmaf(c.b, wv, S2);
                 T = Ti;
             }
-            rs_step<10>(v, 16, hi16);
-            rs_step<5>(v, 8, hi8);
-            rs_step<3>(v, 4, hi4);
-            rs_step<2>(v, 2, hi2);
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-            if (fld >= 0) {
-                const uint32_t idx = s_idx[j];
-                if (fld < 9) {
-                    atomicAdd(fptr + size_t(fstride) * idx, v[0]);
-                } else if (ACCUM) {
-                    atomicAdd(p.accum + idx, (unsigned long long)__float2ull_rn(v[0] * 4294967296.0f));
-                }
+            s_q[warp][nslots][lane] = qv;
+            s_w[warp][nslots][lane] = wv;
+            if (lane == 0)
+                s_rec[warp][nslots] = SlotRec{g.mx, g.my, g.A, g.B, gg.C, c.o, s_idx[j], 0u};
+            if (++nslots == kSlots) {
+                flush_slots<ACCUM>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
+                                   s_rec[warp]);
+                nslots = 0;
             }
         }
     }
+    if (nslots) flush_slots<ACCUM>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
+                                   s_rec[warp]);
+}
+
+constexpr int kBwdDynSmem = 2 * 8 * kSlots * kSlotPad * 4;
+
+// k_raster_bwd's slot buffers are dynamic shared memory on top of ~25 KB of
+// static arrays: raise its limit once per device.
+static int g_bwd_attr_set[64];
+static ss_status ensure_bwd_smem() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && g_bwd_attr_set[dev]) return SS_OK;
+    ss_status s = check_cuda(cudaFuncSetAttribute(k_raster_bwd<true>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  kBwdDynSmem),
+                             "ss_raster_bwd: cudaFuncSetAttribute");
+    if (s == SS_OK)
+        s = check_cuda(cudaFuncSetAttribute(k_raster_bwd<false>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdDynSmem),
+                       "ss_raster_bwd: cudaFuncSetAttribute");
+    if (s == SS_OK && dev >= 0 && dev < 64) g_bwd_attr_set[dev] = 1;
+    return s;
 }
 
 __global__ void k_bwd_zero(BwdParams p, int64_t n, bool accum) {
@@ -288,6 +355,8 @@ extern "C" ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals
                                                               L.accum)
                     : nullptr;
     cudaStream_t st = (cudaStream_t)stream;
+    ss_status es = ensure_bwd_smem();
+    if (es != SS_OK) return es;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -296,9 +365,9 @@ extern "C" ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals
     SS_LAUNCH("k_bwd_zero", st, k_bwd_zero<<<zgrid, 256, 0, st>>>(p, n, accum));
     const int grid = tiles_x(W) * tiles_y(H);
     if (accum)
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true><<<grid, 256, 0, st>>>(p));
+        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true><<<grid, 256, kBwdDynSmem, st>>>(p));
     else
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false><<<grid, 256, 0, st>>>(p));
+        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false><<<grid, 256, kBwdDynSmem, st>>>(p));
     if (accum)
         SS_LAUNCH("k_accum_final", st, k_accum_final<<<zgrid, 256, 0, st>>>(p.accum, accum_weight, n));
     return check_launch("ss_raster_bwd");
@@ -399,6 +468,8 @@ extern "C" ss_status ss_raster_bwd_noalloc(const ss_splats *splats, const uint32
     p.drgb = grads->drgb;
     p.accum = accum ? g_noalloc_ptr[dev] : nullptr;
     cudaStream_t st = (cudaStream_t)stream;
+    s = ensure_bwd_smem();
+    if (s != SS_OK) return s;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t want = (int64_t(n) + 255) / 256;
     const int zgrid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
@@ -406,9 +477,9 @@ extern "C" ss_status ss_raster_bwd_noalloc(const ss_splats *splats, const uint32
     SS_LAUNCH("k_bwd_zero", st, k_bwd_zero<<<zgrid, 256, 0, st>>>(p, n, accum));
     const int grid = tiles_x(W) * tiles_y(H);
     if (accum)
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true><<<grid, 256, 0, st>>>(p));
+        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true><<<grid, 256, kBwdDynSmem, st>>>(p));
     else
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false><<<grid, 256, 0, st>>>(p));
+        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false><<<grid, 256, kBwdDynSmem, st>>>(p));
     if (accum)
         SS_LAUNCH("k_accum_final", st, k_accum_final<<<zgrid, 256, 0, st>>>(p.accum, accum_weight, n));
     return check_launch("ss_raster_bwd_noalloc");
