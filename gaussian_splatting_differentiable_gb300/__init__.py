@@ -106,11 +106,15 @@ def ss_workspace_bytes(n_splats: int, n_pairs: int, W: int, H: int) -> int:
     return int(_L.ss_workspace_bytes(n_splats, n_pairs, W, H))
 
 
-def ss_bin_tiles(splats: Splats, W: int, H: int, keys, vals, capacity: int, counters,
+def ss_record_bytes(n_splats: int) -> int:
+    return int(_L.ss_record_bytes(n_splats))
+
+
+def ss_bin_tiles(splats: Splats, W: int, H: int, keys, vals, capacity: int, counters, records,
                  stream=None) -> None:
     s = splats.c()
     _check(_L.ss_bin_tiles(ctypes.byref(s), W, H, _ptr(keys), _ptr(vals), capacity,
-                           _ptr(counters), _stream(stream)), "ss_bin_tiles")
+                           _ptr(counters), _ptr(records), _stream(stream)), "ss_bin_tiles")
 
 
 def ss_pair_count(counters, capacity: int, stream=None):
@@ -134,38 +138,35 @@ def ss_sort_status(workspace, stream=None) -> int:
     return int(_L.ss_sort_status(_ptr(workspace), _stream(stream)))
 
 
-def ss_raster_fwd(splats: Splats, vals, tile_offsets, W: int, H: int, bg, flags: int, image,
-                  T_final, last_contrib, median_depth=None, stream=None) -> None:
-    s = splats.c()
-    _check(_L.ss_raster_fwd(ctypes.byref(s), _ptr(vals), _ptr(tile_offsets), W, H,
+def ss_raster_fwd(records, n_splats: int, vals, tile_offsets, W: int, H: int, bg, flags: int,
+                  image, T_final, last_contrib, median_depth=None, stream=None) -> None:
+    _check(_L.ss_raster_fwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), W, H,
                             _f32_host3(bg), flags, _ptr(image), _ptr(T_final),
                             _ptr(last_contrib), _ptr(median_depth), _stream(stream)),
            "ss_raster_fwd")
 
 
-def ss_raster_bwd(splats: Splats, vals, tile_offsets, W: int, H: int, bg, flags: int, T_final,
-                  last_contrib, dL_dimage, grads: dict, accum_weight, workspace,
+def ss_raster_bwd(records, n_splats: int, vals, tile_offsets, W: int, H: int, bg, flags: int,
+                  T_final, last_contrib, dL_dimage, grads: dict, accum_weight, workspace,
                   stream=None) -> None:
-    s = splats.c()
     g = SsGrads(_ptr(grads["dmean2d"]), _ptr(grads["dconic"]), _ptr(grads["dopacity"]),
                 _ptr(grads["drgb"]))
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(_L.ss_raster_bwd(ctypes.byref(s), _ptr(vals), _ptr(tile_offsets), W, H,
+    _check(_L.ss_raster_bwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), W, H,
                             _f32_host3(bg), flags, _ptr(T_final), _ptr(last_contrib),
                             _ptr(dL_dimage), ctypes.byref(g), _ptr(accum_weight),
                             _ptr(workspace), nbytes, _stream(stream)), "ss_raster_bwd")
 
 
-def ss_raster_bwd_noalloc(splats: Splats, vals, tile_offsets, W: int, H: int, bg, flags: int,
-                          T_final, last_contrib, dL_dimage, grads: dict, accum_weight,
+def ss_raster_bwd_noalloc(records, n_splats: int, vals, tile_offsets, W: int, H: int, bg,
+                          flags: int, T_final, last_contrib, dL_dimage, grads: dict, accum_weight,
                           stream=None) -> None:
     """ss_raster_bwd for callers that cannot allocate: no workspace argument;
     the weight scratch is a fixed array inside the library (at most 2,097,152
     splats; concurrent calls race on it)."""
-    s = splats.c()
     g = SsGrads(_ptr(grads["dmean2d"]), _ptr(grads["dconic"]), _ptr(grads["dopacity"]),
                 _ptr(grads["drgb"]))
-    _check(_L.ss_raster_bwd_noalloc(ctypes.byref(s), _ptr(vals), _ptr(tile_offsets), W, H,
+    _check(_L.ss_raster_bwd_noalloc(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), W, H,
                                     _f32_host3(bg), flags, _ptr(T_final), _ptr(last_contrib),
                                     _ptr(dL_dimage), ctypes.byref(g), _ptr(accum_weight),
                                     _stream(stream)), "ss_raster_bwd_noalloc")
@@ -213,6 +214,7 @@ class Rasterizer:
         self.tiles = ((W + TILE - 1) // TILE) * ((H + TILE - 1) // TILE)
         d = self.device
         self.counters = torch.zeros(2, dtype=torch.int64, device=d)
+        self.records = torch.empty(max(ss_record_bytes(n_splats), 16), dtype=torch.uint8, device=d)
         self.tile_offsets = torch.zeros(self.tiles + 1, dtype=torch.int32, device=d)
         self._alloc_pairs(max(int(pair_capacity), 1))
         self.image = torch.empty(3, H, W, dtype=torch.float32, device=d)
@@ -242,12 +244,12 @@ class Rasterizer:
     def bin_and_sort(self, splats: Splats, stream=None) -> int:
         """Tile lists of `splats`; returns the number of pairs (one host sync)."""
         ss_bin_tiles(splats, self.W, self.H, self.keys, self.vals, self.capacity, self.counters,
-                     stream)
+                     self.records, stream)
         st, pairs, culled = ss_pair_count(self.counters, self.capacity, stream)
         if st == SS_ERR_CAPACITY:
             self._alloc_pairs(int(pairs * 1.25) + 1024)
             ss_bin_tiles(splats, self.W, self.H, self.keys, self.vals, self.capacity,
-                         self.counters, stream)
+                         self.counters, self.records, stream)
             st, pairs, culled = ss_pair_count(self.counters, self.capacity, stream)
             _check(st, "ss_pair_count")
         self.n_pairs, self.culled = pairs, culled
@@ -255,14 +257,17 @@ class Rasterizer:
                       self.workspace, stream)
         return pairs
 
-    def forward(self, splats: Splats, stream=None) -> None:
-        ss_raster_fwd(splats, self.vals, self.tile_offsets, self.W, self.H, self.bg, self.flags,
-                      self.image, self.T_final, self.last_contrib, self.median_depth, stream)
+    def forward(self, splats: Splats = None, stream=None) -> None:
+        """Composite; uses the records written by the last bin_and_sort."""
+        ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.W, self.H, self.bg,
+                      self.flags, self.image, self.T_final, self.last_contrib, self.median_depth,
+                      stream)
 
-    def backward(self, splats: Splats, dL_dimage: torch.Tensor, stream=None) -> None:
-        ss_raster_bwd(splats, self.vals, self.tile_offsets, self.W, self.H, self.bg, self.flags,
-                      self.T_final, self.last_contrib, dL_dimage, self.grads, self.accum_weight,
-                      self.workspace, stream)
+    def backward(self, splats, dL_dimage: torch.Tensor, stream=None) -> None:
+        """Gradients; uses the records written by the last bin_and_sort."""
+        ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.W, self.H,
+                      self.bg, self.flags, self.T_final, self.last_contrib, dL_dimage, self.grads,
+                      self.accum_weight, self.workspace, stream)
 
     def step(self, splats: Splats, dL_dimage: torch.Tensor, stream=None) -> int:
         """One pass of the whole path: bin, sort, forward, backward."""

@@ -74,7 +74,9 @@ using namespace ss;
 
 extern "C" {
 
-int32_t ss_abi_version(void) { return 1; }
+int32_t ss_abi_version(void) { return 2; }
+
+size_t ss_record_bytes(int32_t n_splats) { return n_splats < 0 ? 0 : size_t(n_splats) * 64; }
 
 void ss_constants(float out[4]) {
     out[0] = kAlphaMin;

@@ -4,7 +4,10 @@
 // One thread per splat computes its tile rectangle; the warp sums its pair
 // counts with shuffles and lane 31 takes the warp's slots with a single
 // 64-bit atomic add, so the global counter sees one atomic per warp rather
-// than one per splat.  Each lane then writes its pairs into its slots.
+// than one per splat.  Each lane then writes its pairs into its slots.  The
+// same thread also writes the splat's 64-byte record (derived exponent
+// coefficients, threshold, colour, depth, cull box), which the forward and
+// backward rasterizers gather by index instead of the five SoA inputs.
 #include "ss_device.cuh"
 #include "ss_internal.h"
 #include "ss_profile.h"
@@ -18,6 +21,7 @@ struct BinParams {
     uint32_t *vals;
     int64_t capacity;
     unsigned long long *counters;  // [0] pairs, [1] culled
+    SplatRecord *records;          // [n] 64-byte records for the rasterizers
 };
 
 __global__ void __launch_bounds__(256) k_emit_pairs(BinParams p) {
@@ -27,6 +31,14 @@ __global__ void __launch_bounds__(256) k_emit_pairs(BinParams p) {
     uint32_t dbits = 0;
     if (i < p.s.n) st = splat_tile_rect(p.s, i, p.tiles_x, p.tiles_y, x0, y0, x1, y1, dbits);
     const uint32_t cnt = st > 0 ? uint32_t(x1 - x0 + 1) * uint32_t(y1 - y0 + 1) : 0u;
+    if (i < p.s.n) {
+        const SplatRecord r = st >= 0 ? make_record(p.s, uint32_t(i)) : invisible_record();
+        float4 *dst = reinterpret_cast<float4 *>(p.records + i);
+        dst[0] = *reinterpret_cast<const float4 *>(&r.geo);
+        dst[1] = *reinterpret_cast<const float4 *>(&r.geo2);
+        dst[2] = *reinterpret_cast<const float4 *>(&r.col);
+        dst[3] = *reinterpret_cast<const float4 *>(&r.box);
+    }
 
     uint32_t inc = cnt;  // warp inclusive scan of pair counts
 #pragma unroll
@@ -61,7 +73,7 @@ using namespace ss;
 
 extern "C" ss_status ss_bin_tiles(const ss_splats *splats, int32_t W, int32_t H, uint64_t *keys,
                                   uint32_t *vals, int64_t capacity, uint64_t *d_counters,
-                                  ss_stream_t stream) {
+                                  void *records, ss_stream_t stream) {
     clear_error();
     if (!splats) return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: splats is NULL");
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
@@ -74,6 +86,9 @@ extern "C" ss_status ss_bin_tiles(const ss_splats *splats, int32_t W, int32_t H,
     if (capacity > 0 && (!keys || !vals))
         return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: keys/vals NULL with capacity > 0");
     if (!d_counters) return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: d_counters is NULL");
+    if (splats->n > 0 && !records) return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: records is NULL");
+    if (reinterpret_cast<uintptr_t>(records) & 15)
+        return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: records not 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(d_counters) & 7) || (reinterpret_cast<uintptr_t>(keys) & 7) ||
         (splats->n > 0 && (reinterpret_cast<uintptr_t>(splats->mean2d) & 7)))
         return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: keys, counters and mean2d need 8-byte alignment");
@@ -89,6 +104,7 @@ extern "C" ss_status ss_bin_tiles(const ss_splats *splats, int32_t W, int32_t H,
     p.vals = vals;
     p.capacity = capacity;
     p.counters = reinterpret_cast<unsigned long long *>(d_counters);
+    p.records = static_cast<SplatRecord *>(records);
     const int grid = int((int64_t(splats->n) + 255) / 256);
     SS_LAUNCH("k_emit_pairs", st, k_emit_pairs<<<grid, 256, 0, st>>>(p));
     return check_launch("ss_bin_tiles: k_emit_pairs");

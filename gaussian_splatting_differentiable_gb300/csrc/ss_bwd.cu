@@ -39,7 +39,8 @@
 namespace ss {
 
 struct BwdParams {
-    SplatPtrs s;
+    const SplatRecord *recs;
+    int32_t n;
     const uint32_t *vals;
     const uint32_t *offs;
     int32_t W, H, tiles_x;
@@ -52,7 +53,9 @@ struct BwdParams {
 };
 
 constexpr int kSlots = 16;     // slots per warp
-constexpr int kSlotPad = 33;   // row pitch: lane pairs read 32 rows without bank conflicts
+constexpr int kChunk = 16;     // list entries evaluated together (<= kSlots)
+constexpr int kSlotPad = 32;   // row pitch; pixel p of slot r is stored at column p ^ r, which
+                               // keeps the lane pairs' column reads free of bank conflicts
 
 __device__ __forceinline__ float rcp_approx(float x) {
     float y;
@@ -86,12 +89,12 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
         for (int v = 0; v < 2; ++v) dyv[v] = __fsub_rn(wy0 + float(2 * half + v), r.my);
         float Q = 0.f, Qx = 0.f, Qy = 0.f, Qxx = 0.f, Qxy = 0.f, Qyy = 0.f;
         float Wt = 0.f, Wr = 0.f, Wg = 0.f, Wb = 0.f;
-        const float *qs = q[slot] + 16 * half;
-        const float *ws = w[slot] + 16 * half;
+        const float *qs = q[slot];
+        const float *ws = w[slot];
         const float4 *gs = g + 16 * half;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const float qi = qs[i], wi = ws[i];
+            const float qi = qs[(16 * half + i) ^ slot], wi = ws[(16 * half + i) ^ slot];
             const float dx = dxu[i & 7], dy = dyv[i >> 3];
             Q += qi;
             const float t = qi * dx;
@@ -139,11 +142,10 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
 
 template <bool ACCUM>
 __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
-    __shared__ SplatGeo s_geo[256];
-    __shared__ SplatGeo2 s_geo2[256];
-    __shared__ SplatCol s_col[256];
-    __shared__ SplatBox s_box[256];
-    __shared__ uint32_t s_idx[256];
+    __shared__ SplatGeo s_geo_[2][256];
+    __shared__ SplatGeo2 s_geo2_[2][256];
+    __shared__ SplatCol s_col_[2][256];
+    __shared__ SplatBox s_box_[2][256];
     __shared__ uint8_t s_list[8][256];
     __shared__ uint32_t s_wmax[8];
     __shared__ float4 s_g[8][32];
@@ -187,17 +189,48 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     for (int w = 0; w < 8; ++w) bmax = max(bmax, s_wmax[w]);
 
     int nslots = 0;  // warp-uniform
-    for (int32_t hi = int32_t(bmax); hi > 0; hi -= 256) {
+    // Batches back to front: batch b covers positions [lo_b, hi_b) of the
+    // tile's list, hi_b = bmax - 256 b, lo_b = max(0, hi_b - 256).  Its
+    // records are copied into buffer b & 1 while batch b - 1 is processed.
+    const int tid = threadIdx.x;
+    if (bmax > 0) {
+        const int32_t lo0 = bmax > 256u ? int32_t(bmax) - 256 : 0;
+        if (tid < int32_t(bmax) - lo0) {
+            const uint32_t idx = p.vals[start + uint32_t(lo0) + tid];
+            stage_record_async(p.recs, idx, p.n, s_geo_[0], s_geo2_[0], s_col_[0], s_box_[0], tid);
+        }
+        cp_async_commit();
+    }
+    uint32_t next_idx = 0;
+    {
+        const int32_t hi1 = int32_t(bmax) - 256;
+        const int32_t lo1 = hi1 > 256 ? hi1 - 256 : 0;
+        if (hi1 > 0 && tid < hi1 - lo1) next_idx = p.vals[start + uint32_t(lo1) + tid];
+    }
+    int buf = 0;
+    for (int32_t hi = int32_t(bmax); hi > 0; hi -= 256, buf ^= 1) {
         const int32_t lo = hi > 256 ? hi - 256 : 0;
         const int nb = hi - lo;
-        __syncthreads();  // the previous batch is no longer read
-        if (int(threadIdx.x) < nb) {
-            const uint32_t idx = p.vals[start + uint32_t(lo) + threadIdx.x];
-            s_idx[threadIdx.x] = idx;
-            stage_splat(p.s, idx, s_geo[threadIdx.x], s_geo2[threadIdx.x], s_col[threadIdx.x],
-                        s_box[threadIdx.x], nullptr);
+        cp_async_wait<0>();
+        __syncthreads();  // batch staged everywhere; the other buffer is free
+        {
+            const int32_t nhi = hi - 256;  // prefetch the next batch (further to the front)
+            if (nhi > 0) {
+                const int32_t nlo = nhi > 256 ? nhi - 256 : 0;
+                if (tid < nhi - nlo) {
+                    stage_record_async(p.recs, next_idx, p.n, s_geo_[buf ^ 1], s_geo2_[buf ^ 1],
+                                       s_col_[buf ^ 1], s_box_[buf ^ 1], tid);
+                }
+                cp_async_commit();
+                const int32_t nnhi = nhi - 256;
+                const int32_t nnlo = nnhi > 256 ? nnhi - 256 : 0;
+                next_idx = (nnhi > 0 && tid < nnhi - nnlo) ? p.vals[start + uint32_t(nnlo) + tid] : 0u;
+            }
         }
-        __syncthreads();
+        const SplatGeo *s_geo = s_geo_[buf];
+        const SplatGeo2 *s_geo2 = s_geo2_[buf];
+        const SplatCol *s_col = s_col_[buf];
+        const SplatBox *s_box = s_box_[buf];
         if (uint32_t(lo) >= wmax) continue;
         int cnt = 0;
 #pragma unroll
@@ -213,43 +246,78 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
             cnt += __popc(m);
         }
         __syncwarp();
-        for (int q = cnt - 1; q >= 0; --q) {
-            const int j = s_list[warp][q];
-            const SplatGeo g = s_geo[j];
-            const SplatGeo2 gg = s_geo2[j];
-            float dx, dy;
-            const float e2 = eval_e2(g, gg.C, px, py, dx, dy);
-            const bool act = uint32_t(lo + j) < n_p && e2 >= gg.thr;
-            if (!__any_sync(0xffffffffu, act)) continue;
-            const SplatCol c = s_col[j];
-            float qv = 0.0f, wv = 0.0f;
-            if (act) {
-                const float G = ex2_approx(e2);
-                float oG;
-                const float alpha = eval_alpha(c.o, G, oG);
-                const float inv = rcp_approx(__fsub_rn(1.0f, alpha));
-                const float Ti = T * inv;  // T in front of this splat
-                wv = alpha * Ti;
-                const float dLda = g0 * (c.r * Ti - (S0 + Tb0) * inv) +
-                                   g1 * (c.g * Ti - (S1 + Tb1) * inv) +
-                                   g2 * (c.b * Ti - (S2 + Tb2) * inv);
-                qv = oG <= kAlphaMax ? -alpha * dLda : 0.0f;  // through the cap alpha is constant
-                S0 = fmaf(c.r, wv, S0);
-                S1 = fmaf(c.g, wv, S1);
-                S2 = fmaf(c.b, wv, S2);
-                T = Ti;
+        const uint8_t *list = s_list[warp];
+        // The warp's list, back to front, in chunks of kChunk entries.
+        for (int hq = cnt; hq > 0; hq -= kChunk) {
+            const int lq = hq > kChunk ? hq - kChunk : 0;
+            const int nq = hq - lq;
+            // 1. Lockstep evaluation: which pixels of the warp blend each entry.
+            uint32_t mine = 0, any = 0;
+#pragma unroll
+            for (int k = 0; k < kChunk; ++k) {
+                bool act = false;
+                if (k < nq) {
+                    const int j = list[lq + k];
+                    const SplatGeo g = s_geo[j];
+                    const SplatGeo2 gg = s_geo2[j];
+                    float dx, dy;
+                    const float e2 = eval_e2(g, gg.C, px, py, dx, dy);
+                    act = uint32_t(lo + j) < n_p && e2 >= gg.thr;
+                }
+                mine |= uint32_t(act) << k;
+                any |= uint32_t(__ballot_sync(0xffffffffu, act) != 0u) << k;
             }
-            s_q[warp][nslots][lane] = qv;
-            s_w[warp][nslots][lane] = wv;
-            if (lane == 0)
-                s_rec[warp][nslots] = SlotRec{g.mx, g.my, g.A, g.B, gg.C, c.o, s_idx[j], 0u};
-            if (++nslots == kSlots) {
+            if (!any) continue;
+            // 2. One slot row per entry that any pixel blends: zero my column,
+            //    record the splat.
+            const int nrows = __popc(any);
+            if (nslots + nrows > kSlots) {
                 flush_slots<ACCUM>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
                                    s_rec[warp]);
                 nslots = 0;
             }
+            for (int r = 0; r < nrows; ++r) {
+                s_q[warp][nslots + r][lane] = 0.0f;
+                s_w[warp][nslots + r][lane] = 0.0f;
+            }
+            if (lane < nq && ((any >> lane) & 1u)) {
+                const int j = list[lq + lane];
+                const SplatGeo g = s_geo[j];
+                s_rec[warp][nslots + __popc(any & lt)] =
+                    SlotRec{g.mx, g.my, g.A, g.B, s_geo2[j].C, s_geo2[j].o, s_col[j].idx, 0u};
+            }
+            // 3. Each pixel walks only its own blended entries, back to front.
+            while (mine) {
+                const int k = 31 - __clz(mine);
+                mine &= ~(1u << k);
+                const int j = list[lq + k];
+                const SplatGeo g = s_geo[j];
+                const SplatGeo2 gg = s_geo2[j];
+                const SplatCol c = s_col[j];
+                float dx, dy;
+                const float e2 = eval_e2(g, gg.C, px, py, dx, dy);
+                const float G = ex2_approx(e2);
+                float oG;
+                const float alpha = eval_alpha(gg.o, G, oG);
+                const float inv = rcp_approx(__fsub_rn(1.0f, alpha));
+                const float Ti = T * inv;  // T in front of this splat
+                const float wv = alpha * Ti;
+                const float dLda = g0 * (c.r * Ti - (S0 + Tb0) * inv) +
+                                   g1 * (c.g * Ti - (S1 + Tb1) * inv) +
+                                   g2 * (c.b * Ti - (S2 + Tb2) * inv);
+                const float qv = oG <= kAlphaMax ? -alpha * dLda : 0.0f;  // capped: constant
+                S0 = fmaf(c.r, wv, S0);
+                S1 = fmaf(c.g, wv, S1);
+                S2 = fmaf(c.b, wv, S2);
+                T = Ti;
+                const int row = nslots + __popc(any & ((1u << k) - 1u));
+                s_q[warp][row][lane ^ row] = qv;
+                s_w[warp][row][lane ^ row] = wv;
+            }
+            nslots += nrows;
         }
     }
+    cp_async_wait<0>();  // no copy may outlive the CTA
     if (nslots) flush_slots<ACCUM>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
                                    s_rec[warp]);
 }
@@ -301,23 +369,23 @@ __global__ void k_accum_final(const unsigned long long *acc, float *out, int64_t
 
 using namespace ss;
 
-extern "C" ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals,
+extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
+                                   const uint32_t *vals,
                                    const uint32_t *tile_offsets, int32_t W, int32_t H,
                                    const float *bg, uint32_t flags, const float *T_final,
                                    const uint32_t *last_contrib, const float *dL_dimage,
                                    const ss_grads *grads, float *accum_weight, void *workspace,
                                    size_t workspace_bytes, ss_stream_t stream) {
     clear_error();
-    if (!splats) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: splats is NULL");
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd: image %dx%d outside 1..%d", W, H, kMaxSide);
     if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: unknown flag bits 0x%x", flags);
-    const int32_t n = splats->n;
+    const int32_t n = n_splats;
     if (n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: n < 0");
-    if (n > 0 && (!splats->mean2d || !splats->conic || !splats->opacity || !splats->rgb ||
-                  !splats->depth))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: a splat array is NULL");
+    if (n > 0 && !records) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: records is NULL");
+    if (reinterpret_cast<uintptr_t>(records) & 15)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: records not 16-byte aligned");
     if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: vals/offsets NULL");
     if (!T_final || !last_contrib || !dL_dimage)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: T_final/last_contrib/dL_dimage NULL");
@@ -326,8 +394,6 @@ extern "C" ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals
     const bool accum = flags & SS_ACCUM_WEIGHT;
     if (accum && n > 0 && !accum_weight)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: SS_ACCUM_WEIGHT set but accum_weight NULL");
-    if (n > 0 && (reinterpret_cast<uintptr_t>(splats->mean2d) & 7))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: mean2d not 8-byte aligned");
     const WsLayout L = ws_layout(n, 0, W, H);
     if (accum && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: workspace NULL or not 256-byte aligned");
@@ -337,7 +403,8 @@ extern "C" ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals
     if (n == 0) return SS_OK;
 
     BwdParams p{};
-    p.s = SplatPtrs{splats->mean2d, splats->conic, splats->opacity, splats->rgb, splats->depth, n};
+    p.recs = static_cast<const SplatRecord *>(records);
+    p.n = n;
     p.vals = vals;
     p.offs = tile_offsets;
     p.W = W;
@@ -399,29 +466,29 @@ static unsigned long long *g_noalloc_ptr[64];  // device address of the array, p
 
 }  // namespace ss
 
-extern "C" ss_status ss_raster_bwd_noalloc(const ss_splats *splats, const uint32_t *vals,
+extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats,
+                                   const uint32_t *vals,
                                            const uint32_t *tile_offsets, int32_t W, int32_t H,
                                            const float *bg, uint32_t flags, const float *T_final,
                                            const uint32_t *last_contrib, const float *dL_dimage,
                                            const ss_grads *grads, float *accum_weight,
                                            ss_stream_t stream) {
     clear_error();
-    if (!splats) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: splats is NULL");
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd_noalloc: image %dx%d outside 1..%d", W, H,
                     kMaxSide);
     if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: unknown flag bits 0x%x", flags);
-    const int32_t n = splats->n;
+    const int32_t n = n_splats;
     if (n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: n < 0");
     if (n > kNoAllocMaxSplats)
         return fail(SS_ERR_UNSUPPORTED,
                     "ss_raster_bwd_noalloc: %d splats exceed its fixed scratch of %d splats; "
                     "use ss_raster_bwd with a workspace",
                     n, kNoAllocMaxSplats);
-    if (n > 0 && (!splats->mean2d || !splats->conic || !splats->opacity || !splats->rgb ||
-                  !splats->depth))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: a splat array is NULL");
+    if (n > 0 && !records) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: records is NULL");
+    if (reinterpret_cast<uintptr_t>(records) & 15)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: records not 16-byte aligned");
     if (!vals || !tile_offsets)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: vals/offsets NULL");
     if (!T_final || !last_contrib || !dL_dimage)
@@ -432,8 +499,6 @@ extern "C" ss_status ss_raster_bwd_noalloc(const ss_splats *splats, const uint32
     if (accum && n > 0 && !accum_weight)
         return fail(SS_ERR_INVALID_ARG,
                     "ss_raster_bwd_noalloc: SS_ACCUM_WEIGHT set but accum_weight NULL");
-    if (n > 0 && (reinterpret_cast<uintptr_t>(splats->mean2d) & 7))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: mean2d not 8-byte aligned");
     if (n == 0) return SS_OK;
 
     int dev = 0, sms = 0;
@@ -452,7 +517,8 @@ extern "C" ss_status ss_raster_bwd_noalloc(const ss_splats *splats, const uint32
     }
 
     BwdParams p{};
-    p.s = SplatPtrs{splats->mean2d, splats->conic, splats->opacity, splats->rgb, splats->depth, n};
+    p.recs = static_cast<const SplatRecord *>(records);
+    p.n = n;
     p.vals = vals;
     p.offs = tile_offsets;
     p.W = W;

@@ -103,48 +103,91 @@ __device__ __forceinline__ int splat_tile_rect(const SplatPtrs &s, int64_t i, in
     return 1;
 }
 
-// A splat as the rasterizers keep it in shared memory.  The exponent is
-// handled in base 2: e2 = -sigma log2(e) = A dx^2 + B dx dy + C dy^2 with
-// A = -a log2(e) / 2, B = -b log2(e), C = -c log2(e) / 2; the splat is
-// skipped at a pixel iff e2 < thr = -log2(255 o)  (alpha < 1/255).
+// A splat as the rasterizers read it: one 64-byte record, written once by
+// the binning kernel, gathered by index (two aligned 32-byte sectors) by
+// the forward and backward kernels.  The exponent is handled in base 2:
+// e2 = -sigma log2(e) = A dx^2 + B dx dy + C dy^2 with A = -a log2(e) / 2,
+// B = -b log2(e), C = -c log2(e) / 2; the splat is skipped at a pixel iff
+// e2 < thr = -log2(255 o)  (alpha < 1/255).
 struct __align__(16) SplatGeo {
     float mx, my, A, B;
 };
-struct __align__(8) SplatGeo2 {
-    float C, thr;
+struct __align__(16) SplatGeo2 {
+    float C, thr, o, depth;
 };
 struct __align__(16) SplatCol {
-    float o, r, g, b;
+    float r, g, b;
+    uint32_t idx;  // the splat's own index (the backward's atomic target)
 };
 // Conservative box of pixel centres where e2 >= thr can hold (the alpha
 // ellipse's bounding box grown by 0.4 % + 0.01 px); used only to skip work.
 struct __align__(16) SplatBox {
     float x0, x1, y0, y1;
 };
+struct __align__(16) SplatRecord {
+    SplatGeo geo;
+    SplatGeo2 geo2;
+    SplatCol col;
+    SplatBox box;
+};
+static_assert(sizeof(SplatRecord) == 64, "record is 64 bytes");
 
-__device__ __forceinline__ void stage_splat(const SplatPtrs &s, uint32_t idx, SplatGeo &geo,
-                                            SplatGeo2 &geo2, SplatCol &col, SplatBox &box,
-                                            float *depth) {
-    if (idx >= uint32_t(s.n)) {  // not a splat: never blended
-        geo = SplatGeo{0.f, 0.f, 0.f, 0.f};
-        geo2 = SplatGeo2{0.f, __int_as_float(0x7f800000)};
-        col = SplatCol{0.f, 0.f, 0.f, 0.f};
-        box = SplatBox{1.f, -1.f, 1.f, -1.f};
-        if (depth) *depth = 0.f;
-        return;
-    }
+// The record of a splat that is never blended (culled or not a splat).
+__device__ __forceinline__ SplatRecord invisible_record() {
+    SplatRecord r;
+    r.geo = SplatGeo{0.f, 0.f, 0.f, 0.f};
+    r.geo2 = SplatGeo2{0.f, __int_as_float(0x7f800000), 0.f, 0.f};
+    r.col = SplatCol{0.f, 0.f, 0.f, 0u};
+    r.box = SplatBox{1.f, -1.f, 1.f, -1.f};
+    return r;
+}
+
+// Record of splat idx from the SoA inputs.
+__device__ __forceinline__ SplatRecord make_record(const SplatPtrs &s, uint32_t idx) {
     const float2 mu = reinterpret_cast<const float2 *>(s.mean2d)[idx];
     const float a = s.conic[3 * idx], b = s.conic[3 * idx + 1], c = s.conic[3 * idx + 2];
     const float o = s.opacity[idx];
-    geo = SplatGeo{mu.x, mu.y, __fmul_rn(-0.5f * kLog2e, a), __fmul_rn(-kLog2e, b)};
-    geo2 = SplatGeo2{__fmul_rn(-0.5f * kLog2e, c), -log2f(__fmul_rn(255.0f, o))};
-    col = SplatCol{o, s.rgb[3 * idx], s.rgb[3 * idx + 1], s.rgb[3 * idx + 2]};
+    SplatRecord r;
+    r.geo = SplatGeo{mu.x, mu.y, __fmul_rn(-0.5f * kLog2e, a), __fmul_rn(-kLog2e, b)};
+    r.geo2 = SplatGeo2{__fmul_rn(-0.5f * kLog2e, c), -log2f(__fmul_rn(255.0f, o)), o, s.depth[idx]};
+    r.col = SplatCol{s.rgb[3 * idx], s.rgb[3 * idx + 1], s.rgb[3 * idx + 2], idx};
     const float k = 2.0f * fmaxf(__logf(255.0f * o), 0.0f);
     const float det = a * c - b * b;
     const float rx = sqrtf(k * c / det) * 1.004f + 0.01f;
     const float ry = sqrtf(k * a / det) * 1.004f + 0.01f;
-    box = SplatBox{mu.x - rx, mu.x + rx, mu.y - ry, mu.y + ry};
-    if (depth) *depth = s.depth[idx];
+    r.box = SplatBox{mu.x - rx, mu.x + rx, mu.y - ry, mu.y + ry};
+    return r;
+}
+
+// 16-byte asynchronous global -> shared copy (cp.async, L2 only).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Stage record `idx` (or the invisible record if idx >= n) into shared
+// memory slot `t` of the four arrays with 16-byte asynchronous copies.
+__device__ __forceinline__ void stage_record_async(const SplatRecord *recs, uint32_t idx, int32_t n,
+                                                   SplatGeo *geo, SplatGeo2 *geo2, SplatCol *col,
+                                                   SplatBox *box, int t) {
+    if (idx < uint32_t(n)) {
+        const SplatRecord *r = recs + idx;
+        cp_async16(&geo[t], &r->geo);
+        cp_async16(&geo2[t], &r->geo2);
+        cp_async16(&col[t], &r->col);
+        cp_async16(&box[t], &r->box);
+    } else {
+        const SplatRecord r = invisible_record();
+        geo[t] = r.geo;
+        geo2[t] = r.geo2;
+        col[t] = r.col;
+        box[t] = r.box;
+    }
 }
 
 // Base-2 exponent of the splat's Gaussian at pixel centre (px, py); also

@@ -3,14 +3,14 @@
 //
 // One 256-thread CTA per 16x16 tile, one thread per pixel; warp w covers the
 // 8x4 pixel block (8 (w & 1), 4 (w >> 1)) of the tile.  The tile's list is
-// walked front to back in batches of 256 splats: every thread stages one
-// splat of the batch into shared memory (gathered by index from the SoA
-// inputs, which stay resident in L2), then each warp compacts the batch to
-// the splats whose conservative box reaches its 8x4 block, and each pixel
-// composites that short list.  A pixel stops at the first splat whose blend
-// would take T below 1e-4; the CTA stops staging once all its pixels have.
-// The median-depth output is a template variant, so the default variant
-// carries neither its shared array nor its registers.
+// walked front to back in batches of 256 splats.  Each batch's 64-byte
+// splat records are copied into shared memory with cp.async while the
+// previous batch is composited (two buffers; the pair indices are read one
+// batch further ahead), then each warp compacts the batch to the splats
+// whose conservative box reaches its 8x4 block and each pixel composites
+// that short list.  A pixel stops at the first splat whose blend would take
+// T below 1e-4; the CTA stops once all its pixels have.  The median-depth
+// output is a template variant, so the default variant does no median work.
 #include "ss_device.cuh"
 #include "ss_internal.h"
 #include "ss_profile.h"
@@ -18,7 +18,8 @@
 namespace ss {
 
 struct FwdParams {
-    SplatPtrs s;
+    const SplatRecord *recs;
+    int32_t n;
     const uint32_t *vals;
     const uint32_t *offs;
     int32_t W, H, tiles_x;
@@ -31,16 +32,16 @@ struct FwdParams {
 
 template <bool MEDIAN>
 __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
-    __shared__ SplatGeo s_geo[256];
-    __shared__ SplatGeo2 s_geo2[256];
-    __shared__ SplatCol s_col[256];
-    __shared__ SplatBox s_box[256];
-    __shared__ float s_depth[MEDIAN ? 256 : 1];
+    __shared__ SplatGeo s_geo[2][256];
+    __shared__ SplatGeo2 s_geo2[2][256];
+    __shared__ SplatCol s_col[2][256];
+    __shared__ SplatBox s_box[2][256];
     __shared__ uint8_t s_list[8][256];
 
+    const int tid = threadIdx.x;
     const int tile = blockIdx.x;
     const int tx = tile % p.tiles_x, ty = tile / p.tiles_x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = tid >> 5, lane = tid & 31;
     const int bx = tx * kTile + ((warp & 1) << 3), by = ty * kTile + ((warp >> 1) << 2);
     const int x = bx + (lane & 7), y = by + (lane >> 3);
     const bool inside = x < p.W && y < p.H;
@@ -54,15 +55,29 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
     uint32_t last = 0;
     bool done = !inside;
 
-    for (uint32_t base = start; base < end; base += 256) {
+    // Batch b covers list positions [start + 256 b, min(end, start + 256 (b + 1))).
+    if (start < end) {
+        if (uint32_t(tid) < end - start)
+            stage_record_async(p.recs, p.vals[start + tid], p.n, s_geo[0], s_geo2[0], s_col[0],
+                               s_box[0], tid);
+        cp_async_commit();
+    }
+    uint32_t next_idx = start + 256u + uint32_t(tid) < end ? p.vals[start + 256u + tid] : 0u;
+    int buf = 0;
+    for (uint32_t base = start; base < end; base += 256, buf ^= 1) {
+        cp_async_wait<0>();
         if (__syncthreads_count(!done) == 0) break;
-        const int nb = int(min(256u, end - base));
-        if (int(threadIdx.x) < nb) {
-            const uint32_t idx = p.vals[base + threadIdx.x];
-            stage_splat(p.s, idx, s_geo[threadIdx.x], s_geo2[threadIdx.x], s_col[threadIdx.x],
-                        s_box[threadIdx.x], MEDIAN ? &s_depth[threadIdx.x] : nullptr);
+        // Prefetch the next batch into the other buffer (free: every thread
+        // has passed the barrier, so nobody still reads the batch before).
+        const uint32_t nbase = base + 256;
+        if (nbase < end) {
+            if (nbase + uint32_t(tid) < end)
+                stage_record_async(p.recs, next_idx, p.n, s_geo[buf ^ 1], s_geo2[buf ^ 1],
+                                   s_col[buf ^ 1], s_box[buf ^ 1], tid);
+            cp_async_commit();
+            next_idx = nbase + 256u + uint32_t(tid) < end ? p.vals[nbase + 256u + tid] : 0u;
         }
-        __syncthreads();
+        const int nb = int(min(256u, end - base));
         if (!__any_sync(0xffffffffu, !done)) continue;
         int cnt = 0;
 #pragma unroll
@@ -70,7 +85,7 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
             const int j = q * 32 + lane;
             bool hit = false;
             if (j < nb) {
-                const SplatBox b = s_box[j];
+                const SplatBox b = s_box[buf][j];
                 hit = b.x0 <= wx1 && b.x1 >= wx0 && b.y0 <= wy1 && b.y1 >= wy0;
             }
             const uint32_t m = __ballot_sync(0xffffffffu, hit);
@@ -81,28 +96,29 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
         if (done) continue;
         for (int q = 0; q < cnt; ++q) {
             const int j = s_list[warp][q];
-            const SplatGeo g = s_geo[j];
-            const SplatGeo2 g2 = s_geo2[j];
+            const SplatGeo g = s_geo[buf][j];
+            const SplatGeo2 g2 = s_geo2[buf][j];
             float dx, dy;
             const float e2 = eval_e2(g, g2.C, px, py, dx, dy);
             if (!(e2 >= g2.thr)) continue;  // skipped (alpha < 1/255); NaN-safe
-            const SplatCol c = s_col[j];
             float oG;
-            const float alpha = eval_alpha(c.o, ex2_approx(e2), oG);
+            const float alpha = eval_alpha(g2.o, ex2_approx(e2), oG);
             const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
             if (Tn < kTEps) {
                 done = true;
                 break;
             }
+            const SplatCol c = s_col[buf][j];
             const float w = alpha * T;
             cr = fmaf(c.r, w, cr);
             cg = fmaf(c.g, w, cg);
             cb = fmaf(c.b, w, cb);
-            if (MEDIAN && T > 0.5f) med = s_depth[j];
+            if (MEDIAN && T > 0.5f) med = g2.depth;
             T = Tn;
             last = base - start + uint32_t(j) + 1u;
         }
     }
+    cp_async_wait<0>();  // no copy may outlive the CTA
     if (inside) {
         const size_t HW = size_t(p.W) * p.H, pix = size_t(y) * p.W + x;
         p.image[pix] = fmaf(T, p.bg[0], cr);
@@ -118,32 +134,29 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
 
 using namespace ss;
 
-extern "C" ss_status ss_raster_fwd(const ss_splats *splats, const uint32_t *vals,
+extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *vals,
                                    const uint32_t *tile_offsets, int32_t W, int32_t H,
                                    const float *bg, uint32_t flags, float *image, float *T_final,
                                    uint32_t *last_contrib, float *median_depth,
                                    ss_stream_t stream) {
     clear_error();
-    if (!splats) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: splats is NULL");
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_fwd: image %dx%d outside 1..%d", W, H, kMaxSide);
     if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: unknown flag bits 0x%x", flags);
-    if (splats->n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: n < 0");
-    if (splats->n > 0 && (!splats->mean2d || !splats->conic || !splats->opacity || !splats->rgb ||
-                          !splats->depth))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: a splat array is NULL");
+    if (n_splats < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: n_splats < 0");
+    if (n_splats > 0 && !records) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: records is NULL");
+    if (reinterpret_cast<uintptr_t>(records) & 15)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: records not 16-byte aligned");
     if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: vals/offsets NULL");
     if (!image || !T_final || !last_contrib)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: an output is NULL");
     const bool median = flags & SS_MEDIAN_DEPTH;
     if (median && !median_depth)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: SS_MEDIAN_DEPTH set but median_depth NULL");
-    if (splats->n > 0 && (reinterpret_cast<uintptr_t>(splats->mean2d) & 7))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: mean2d not 8-byte aligned");
     FwdParams p{};
-    p.s = SplatPtrs{splats->mean2d, splats->conic, splats->opacity, splats->rgb, splats->depth,
-                    splats->n};
+    p.recs = static_cast<const SplatRecord *>(records);
+    p.n = n_splats;
     p.vals = vals;
     p.offs = tile_offsets;
     p.W = W;

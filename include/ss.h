@@ -123,9 +123,19 @@ size_t ss_workspace_bytes(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t 
  *   d_counters: device uint64[2]; zeroed here, then [0] = pairs needed,
  *               [1] = culled splats.
  *   keys, vals: device, `capacity` entries each (may be NULL if capacity 0).
+ *   records: device, ss_record_bytes(n) bytes, 16-byte aligned; receives one
+ *            64-byte record per splat (its position, base-2 exponent
+ *            coefficients and threshold, opacity, depth, colour, index and a
+ *            conservative pixel box), the form in which the rasterizers
+ *            gather splats.  Opaque to the caller; valid while the splat
+ *            inputs are unchanged.
  */
 ss_status ss_bin_tiles(const ss_splats *splats, int32_t W, int32_t H, uint64_t *keys,
-                       uint32_t *vals, int64_t capacity, uint64_t *d_counters, ss_stream_t stream);
+                       uint32_t *vals, int64_t capacity, uint64_t *d_counters, void *records,
+                       ss_stream_t stream);
+
+/* Host: bytes of the record buffer for n splats (64 n). */
+size_t ss_record_bytes(int32_t n_splats);
 
 /* Host: synchronizes `stream` and reads the counters of ss_bin_tiles.
  * *h_pairs = pairs needed, *h_culled = culled splats (either may be NULL).
@@ -168,9 +178,10 @@ ss_status ss_sort_status(const void *workspace, ss_stream_t stream);
  *   median_depth[H][W]  only with SS_MEDIAN_DEPTH (else may be NULL): depth
  *                       of the last splat blended while T > 0.5, 0 if none
  *   bg: HOST float[3] background, or NULL for black.
+ *   records, n_splats: the records ss_bin_tiles wrote for these splats.
  *   vals, tile_offsets: the output of ss_sort_pairs for the same W, H.
- * Pair values >= splats->n are ignored. */
-ss_status ss_raster_fwd(const ss_splats *splats, const uint32_t *vals,
+ * Pair values >= n_splats are ignored. */
+ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *vals,
                         const uint32_t *tile_offsets, int32_t W, int32_t H, const float *bg,
                         uint32_t flags, float *image, float *T_final, uint32_t *last_contrib,
                         float *median_depth, ss_stream_t stream);
@@ -190,6 +201,7 @@ ss_status ss_raster_fwd(const ss_splats *splats, const uint32_t *vals,
  * a splat are summed across each warp with shuffles before one atomic add
  * per field per warp ("Phase 5 step 30b", conclusion: one atomic per warp
  * instead of per thread).
+ *   records, n_splats: the records ss_bin_tiles wrote for these splats.
  *   T_final, last_contrib: from ss_raster_fwd with the same inputs.
  *   dL_dimage: device float[3][H][W].
  *   grads: all four arrays required; overwritten (zeroed here first).
@@ -198,7 +210,7 @@ ss_status ss_raster_fwd(const ss_splats *splats, const uint32_t *vals,
  *   result does not depend on the order of the atomics); else may be NULL.
  *   workspace: >= ss_workspace_bytes(n, 0, W, H) bytes, 256-byte aligned.
  *   bg: HOST float[3] or NULL (must match the forward call). */
-ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals,
+ss_status ss_raster_bwd(const void *records, int32_t n_splats, const uint32_t *vals,
                         const uint32_t *tile_offsets, int32_t W, int32_t H, const float *bg,
                         uint32_t flags, const float *T_final, const uint32_t *last_contrib,
                         const float *dL_dimage, const ss_grads *grads, float *accum_weight,
@@ -215,14 +227,14 @@ ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals,
  * scratch (8 bytes per splat) is a fixed array inside the library,
  * 2,097,152 splats (16 MiB), which every GPU that loads the library holds
  * until the process exits.
- *   - n > 2,097,152 returns SS_ERR_UNSUPPORTED (use ss_raster_bwd).
+ *   - n_splats > 2,097,152 returns SS_ERR_UNSUPPORTED (use ss_raster_bwd).
  *   - The first call on a device, made with that device current, looks up
  *     the array's device address (cudaGetSymbolAddress); make that first
  *     call before any stream capture.
  *   - All calls share the array.  Each call clears the part it uses, but
  *     calls that overlap on the GPU (other streams, other host threads) race
  *     on it: serialise them. */
-ss_status ss_raster_bwd_noalloc(const ss_splats *splats, const uint32_t *vals,
+ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats, const uint32_t *vals,
                                 const uint32_t *tile_offsets, int32_t W, int32_t H,
                                 const float *bg, uint32_t flags, const float *T_final,
                                 const uint32_t *last_contrib, const float *dL_dimage,

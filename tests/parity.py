@@ -36,11 +36,12 @@ def run_gpu(scene, capacity=None, stream=None):
     flags = flags_of(scene)
     cap = capacity if capacity is not None else max(64, 4 * scene.n)
     r = ss.Rasterizer(scene.W, scene.H, scene.n, cap, flags, bg=scene.bg, device=dev)
-    ss.ss_bin_tiles(sp, scene.W, scene.H, r.keys, r.vals, r.capacity, r.counters, stream)
+    ss.ss_bin_tiles(sp, scene.W, scene.H, r.keys, r.vals, r.capacity, r.counters, r.records, stream)
     st, pairs, culled = ss.ss_pair_count(r.counters, r.capacity, stream)
     if st != ss.SS_OK:
         r._alloc_pairs(pairs + 16)
-        ss.ss_bin_tiles(sp, scene.W, scene.H, r.keys, r.vals, r.capacity, r.counters, stream)
+        ss.ss_bin_tiles(sp, scene.W, scene.H, r.keys, r.vals, r.capacity, r.counters, r.records,
+                        stream)
         st, pairs, culled = ss.ss_pair_count(r.counters, r.capacity, stream)
         assert st == ss.SS_OK
     out = {"count": pairs, "culled": culled,

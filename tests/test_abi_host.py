@@ -55,7 +55,7 @@ def test_constants_match_oracle(lib):
     assert buf[1] == np.float32(c["alpha_max"])
     assert buf[2] == np.float32(c["T_eps"])
     assert buf[3] == c["tile"]
-    assert lib.ss_abi_version() == 1
+    assert lib.ss_abi_version() == 2
 
 
 def test_workspace_bytes(lib):
@@ -74,14 +74,18 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     s = SsSplats(None, None, None, None, None, 10)
     cnt = ctypes.c_void_p(0x1000)
     # image size
-    assert lib.ss_bin_tiles(ctypes.byref(s), 0, 16, None, None, 0, cnt, None) == 5
+    assert lib.ss_bin_tiles(ctypes.byref(s), 0, 16, None, None, 0, cnt, 0x1000, None) == 5
     assert "image" in lib.ss_last_error().decode()
     # NULL splat arrays with n > 0
-    assert lib.ss_bin_tiles(ctypes.byref(s), 16, 16, None, None, 0, cnt, None) == 1
-    assert lib.ss_bin_tiles(None, 16, 16, None, None, 0, cnt, None) == 1
-    # counters NULL
+    assert lib.ss_bin_tiles(ctypes.byref(s), 16, 16, None, None, 0, cnt, 0x1000, None) == 1
+    assert lib.ss_bin_tiles(None, 16, 16, None, None, 0, cnt, 0x1000, None) == 1
+    # counters NULL; records NULL or unaligned
     s0 = SsSplats(None, None, None, None, None, 0)
-    assert lib.ss_bin_tiles(ctypes.byref(s0), 16, 16, None, None, 0, None, None) == 1
+    assert lib.ss_bin_tiles(ctypes.byref(s0), 16, 16, None, None, 0, None, None, None) == 1
+    sp = SsSplats(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 4)
+    assert lib.ss_bin_tiles(ctypes.byref(sp), 16, 16, None, None, 0, cnt, None, None) == 1
+    assert lib.ss_bin_tiles(ctypes.byref(sp), 16, 16, None, None, 0, cnt, 0x1008, None) == 1
+    assert lib.ss_record_bytes(10) == 640 and lib.ss_record_bytes(-1) == 0
     # sort: too many pairs, NULL offsets, unaligned workspace, small workspace
     assert lib.ss_sort_pairs(None, None, 1 << 32, 16, 16, 0x1000, 0x1000, 1 << 30, None) == 5
     assert lib.ss_sort_pairs(0x1000, 0x1000, 10, 16, 16, None, 0x1000, 1 << 30, None) == 1
@@ -89,22 +93,25 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert lib.ss_sort_pairs(0x1000, 0x1000, 10, 16, 16, 0x1000, 0x1000, 16, None) == 1
     assert "workspace" in lib.ss_last_error().decode()
     # forward: unknown flags, NULL outputs, median flag without buffer
-    assert lib.ss_raster_fwd(ctypes.byref(s0), 0x1000, 0x1000, 16, 16, None, 8, 0x1000, 0x1000,
+    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 16, 16, None, 8, 0x1000, 0x1000,
                              0x1000, None, None) == 1
-    assert lib.ss_raster_fwd(ctypes.byref(s0), 0x1000, 0x1000, 16, 16, None, 0, None, 0x1000,
+    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 16, 16, None, 0, None, 0x1000,
                              0x1000, None, None) == 1
-    assert lib.ss_raster_fwd(ctypes.byref(s0), 0x1000, 0x1000, 16, 16, None, 2, 0x1000, 0x1000,
+    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 16, 16, None, 2, 0x1000, 0x1000,
+                             0x1000, None, None) == 1
+    assert lib.ss_raster_fwd(None, 5, 0x1000, 0x1000, 16, 16, None, 0, 0x1000, 0x1000,
                              0x1000, None, None) == 1
     # backward: NULL gradient array, accum flag without buffer or workspace
-    sp = SsSplats(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 4)
     g = SsGrads(0x1000, None, 0x1000, 0x1000)
-    assert lib.ss_raster_bwd(ctypes.byref(sp), 0x1000, 0x1000, 16, 16, None, 0, 0x1000, 0x1000,
+    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 16, 16, None, 0, 0x1000, 0x1000,
                              0x1000, ctypes.byref(g), None, None, 0, None) == 1
     g = SsGrads(0x1000, 0x1000, 0x1000, 0x1000)
-    assert lib.ss_raster_bwd(ctypes.byref(sp), 0x1000, 0x1000, 16, 16, None, 1, 0x1000, 0x1000,
+    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 16, 16, None, 1, 0x1000, 0x1000,
                              0x1000, ctypes.byref(g), None, 0x1000, 1 << 20, None) == 1
-    assert lib.ss_raster_bwd(ctypes.byref(sp), 0x1000, 0x1000, 16, 16, None, 1, 0x1000, 0x1000,
+    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 16, 16, None, 1, 0x1000, 0x1000,
                              0x1000, ctypes.byref(g), 0x1000, 0x1000, 8, None) == 1
+    assert lib.ss_raster_bwd(None, 4, 0x1000, 0x1000, 16, 16, None, 0, 0x1000, 0x1000,
+                             0x1000, ctypes.byref(g), None, None, 0, None) == 1
     # pair count / sort status with NULL
     assert lib.ss_pair_count(None, 0, None, None, None) == 1
     assert lib.ss_sort_status(None, None) == 1

@@ -127,7 +127,8 @@ def test_capacity_overflow_reports_and_recovers(P):
     keys = torch.full((50,), -1, dtype=torch.int64, device="cuda")
     vals = torch.full((50,), -1, dtype=torch.int32, device="cuda")
     cnt = torch.zeros(2, dtype=torch.int64, device="cuda")
-    ss.ss_bin_tiles(sp, sc.W, sc.H, keys, vals, 40, cnt)
+    recs = torch.empty(ss.ss_record_bytes(sc.n), dtype=torch.uint8, device="cuda")
+    ss.ss_bin_tiles(sp, sc.W, sc.H, keys, vals, 40, cnt, recs)
     st, pairs, culled = ss.ss_pair_count(cnt, 40)
     import oracle
     assert st == ss.SS_ERR_CAPACITY and pairs == oracle.tile_lists(sc)["count"] > 40
