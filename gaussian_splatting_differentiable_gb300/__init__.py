@@ -138,37 +138,39 @@ def ss_sort_status(workspace, stream=None) -> int:
     return int(_L.ss_sort_status(_ptr(workspace), _stream(stream)))
 
 
-def ss_raster_fwd(records, n_splats: int, vals, tile_offsets, W: int, H: int, bg, flags: int,
-                  image, T_final, last_contrib, median_depth=None, stream=None) -> None:
-    _check(_L.ss_raster_fwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), W, H,
-                            _f32_host3(bg), flags, _ptr(image), _ptr(T_final),
-                            _ptr(last_contrib), _ptr(median_depth), _stream(stream)),
-           "ss_raster_fwd")
-
-
-def ss_raster_bwd(records, n_splats: int, vals, tile_offsets, W: int, H: int, bg, flags: int,
-                  T_final, last_contrib, dL_dimage, grads: dict, accum_weight, workspace,
+def ss_raster_fwd(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int, H: int, bg,
+                  flags: int, image, T_final, last_contrib, median_depth, blend_masks,
                   stream=None) -> None:
+    _check(_L.ss_raster_fwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), n_pairs, W,
+                            H, _f32_host3(bg), flags, _ptr(image), _ptr(T_final),
+                            _ptr(last_contrib), _ptr(median_depth), _ptr(blend_masks),
+                            _stream(stream)), "ss_raster_fwd")
+
+
+def ss_raster_bwd(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int, H: int, bg,
+                  flags: int, T_final, last_contrib, blend_masks, dL_dimage, grads: dict,
+                  accum_weight, workspace, stream=None) -> None:
     g = SsGrads(_ptr(grads["dmean2d"]), _ptr(grads["dconic"]), _ptr(grads["dopacity"]),
                 _ptr(grads["drgb"]))
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(_L.ss_raster_bwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), W, H,
-                            _f32_host3(bg), flags, _ptr(T_final), _ptr(last_contrib),
-                            _ptr(dL_dimage), ctypes.byref(g), _ptr(accum_weight),
+    _check(_L.ss_raster_bwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), n_pairs, W,
+                            H, _f32_host3(bg), flags, _ptr(T_final), _ptr(last_contrib),
+                            _ptr(blend_masks), _ptr(dL_dimage), ctypes.byref(g), _ptr(accum_weight),
                             _ptr(workspace), nbytes, _stream(stream)), "ss_raster_bwd")
 
 
-def ss_raster_bwd_noalloc(records, n_splats: int, vals, tile_offsets, W: int, H: int, bg,
-                          flags: int, T_final, last_contrib, dL_dimage, grads: dict, accum_weight,
-                          stream=None) -> None:
+def ss_raster_bwd_noalloc(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int,
+                          H: int, bg, flags: int, T_final, last_contrib, blend_masks, dL_dimage,
+                          grads: dict, accum_weight, stream=None) -> None:
     """ss_raster_bwd for callers that cannot allocate: no workspace argument;
     the weight scratch is a fixed array inside the library (at most 2,097,152
     splats; concurrent calls race on it)."""
     g = SsGrads(_ptr(grads["dmean2d"]), _ptr(grads["dconic"]), _ptr(grads["dopacity"]),
                 _ptr(grads["drgb"]))
-    _check(_L.ss_raster_bwd_noalloc(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), W, H,
-                                    _f32_host3(bg), flags, _ptr(T_final), _ptr(last_contrib),
-                                    _ptr(dL_dimage), ctypes.byref(g), _ptr(accum_weight),
+    _check(_L.ss_raster_bwd_noalloc(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets),
+                                    n_pairs, W, H, _f32_host3(bg), flags, _ptr(T_final),
+                                    _ptr(last_contrib), _ptr(blend_masks), _ptr(dL_dimage),
+                                    ctypes.byref(g), _ptr(accum_weight),
                                     _stream(stream)), "ss_raster_bwd_noalloc")
 
 
@@ -236,6 +238,7 @@ class Rasterizer:
         self.capacity = cap
         self.keys = torch.empty(cap, dtype=torch.int64, device=d)
         self.vals = torch.empty(cap, dtype=torch.int32, device=d)
+        self.blend_masks = torch.empty(8 * cap, dtype=torch.int32, device=d)
         ws = ss_workspace_bytes(self.n, cap, self.W, self.H)
         if ws == 0:
             raise ValueError("sizes out of range")
@@ -259,15 +262,16 @@ class Rasterizer:
 
     def forward(self, splats: Splats = None, stream=None) -> None:
         """Composite; uses the records written by the last bin_and_sort."""
-        ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.W, self.H, self.bg,
-                      self.flags, self.image, self.T_final, self.last_contrib, self.median_depth,
-                      stream)
+        ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs, self.W,
+                      self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
+                      self.median_depth, self.blend_masks, stream)
 
     def backward(self, splats, dL_dimage: torch.Tensor, stream=None) -> None:
         """Gradients; uses the records written by the last bin_and_sort."""
-        ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.W, self.H,
-                      self.bg, self.flags, self.T_final, self.last_contrib, dL_dimage, self.grads,
-                      self.accum_weight, self.workspace, stream)
+        ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs, self.W,
+                      self.H, self.bg, self.flags, self.T_final, self.last_contrib,
+                      self.blend_masks, dL_dimage, self.grads, self.accum_weight, self.workspace,
+                      stream)
 
     def step(self, splats: Splats, dL_dimage: torch.Tensor, stream=None) -> int:
         """One pass of the whole path: bin, sort, forward, backward."""

@@ -43,6 +43,8 @@ struct BwdParams {
     int32_t n;
     const uint32_t *vals;
     const uint32_t *offs;
+    const uint32_t *masks;  // [8][n_pairs] the forward's blend decisions
+    int64_t n_pairs;
     int32_t W, H, tiles_x;
     float bg[3];
     const float *T_final;
@@ -145,8 +147,8 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     __shared__ SplatGeo s_geo_[2][256];
     __shared__ SplatGeo2 s_geo2_[2][256];
     __shared__ SplatCol s_col_[2][256];
-    __shared__ SplatBox s_box_[2][256];
     __shared__ uint8_t s_list[8][256];
+    __shared__ uint32_t s_lmask[8][256];
     __shared__ uint32_t s_wmax[8];
     __shared__ float4 s_g[8][32];
     __shared__ SlotRec s_rec[8][kSlots];
@@ -162,8 +164,7 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     const int x = bx + (lane & 7), y = by + (lane >> 3);
     const bool inside = x < p.W && y < p.H;
     const float px = float(x) + 0.5f, py = float(y) + 0.5f;
-    const float wx0 = float(bx) + 0.5f, wx1 = wx0 + 7.0f;
-    const float wy0 = float(by) + 0.5f, wy1 = wy0 + 3.0f;
+    const float wx0 = float(bx) + 0.5f, wy0 = float(by) + 0.5f;
     const uint32_t start = p.offs[tile], len = p.offs[tile + 1] - start;
     const uint32_t lt = lanemask_lt();
 
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
         const int32_t lo0 = bmax > 256u ? int32_t(bmax) - 256 : 0;
         if (tid < int32_t(bmax) - lo0) {
             const uint32_t idx = p.vals[start + uint32_t(lo0) + tid];
-            stage_record_async(p.recs, idx, p.n, s_geo_[0], s_geo2_[0], s_col_[0], s_box_[0], tid);
+            stage_record3_async(p.recs, idx, p.n, s_geo_[0], s_geo2_[0], s_col_[0], tid);
         }
         cp_async_commit();
     }
@@ -218,8 +219,8 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
             if (nhi > 0) {
                 const int32_t nlo = nhi > 256 ? nhi - 256 : 0;
                 if (tid < nhi - nlo) {
-                    stage_record_async(p.recs, next_idx, p.n, s_geo_[buf ^ 1], s_geo2_[buf ^ 1],
-                                       s_col_[buf ^ 1], s_box_[buf ^ 1], tid);
+                    stage_record3_async(p.recs, next_idx, p.n, s_geo_[buf ^ 1], s_geo2_[buf ^ 1],
+                                        s_col_[buf ^ 1], tid);
                 }
                 cp_async_commit();
                 const int32_t nnhi = nhi - 256;
@@ -230,47 +231,44 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
         const SplatGeo *s_geo = s_geo_[buf];
         const SplatGeo2 *s_geo2 = s_geo2_[buf];
         const SplatCol *s_col = s_col_[buf];
-        const SplatBox *s_box = s_box_[buf];
         if (uint32_t(lo) >= wmax) continue;
+        // The warp's entries of this batch that the forward blended somewhere
+        // in its 8x4 block, with their masks, in list order.
         int cnt = 0;
+        {
+            const uint32_t *gm = p.masks + size_t(warp) * size_t(p.n_pairs) + start + uint32_t(lo);
+            uint32_t mv[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int j = q * 32 + lane;
-            bool hit = false;
-            if (j < nb && uint32_t(lo + j) < wmax) {
-                const SplatBox b = s_box[j];
-                hit = b.x0 <= wx1 && b.x1 >= wx0 && b.y0 <= wy1 && b.y1 >= wy0;
+            for (int q = 0; q < 8; ++q) {
+                const int j = q * 32 + lane;
+                mv[q] = (j < nb && uint32_t(lo + j) < wmax &&
+                         int64_t(start) + lo + j < p.n_pairs) ? gm[j] : 0u;
             }
-            const uint32_t m = __ballot_sync(0xffffffffu, hit);
-            if (hit) s_list[warp][cnt + __popc(m & lt)] = uint8_t(j);
-            cnt += __popc(m);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t b = __ballot_sync(0xffffffffu, mv[q] != 0u);
+                if (mv[q]) {
+                    const int at = cnt + __popc(b & lt);
+                    s_list[warp][at] = uint8_t(q * 32 + lane);
+                    s_lmask[warp][at] = mv[q];
+                }
+                cnt += __popc(b);
+            }
         }
         __syncwarp();
         const uint8_t *list = s_list[warp];
-        // The warp's list, back to front, in chunks of kChunk entries.
+        const uint32_t *lmask = s_lmask[warp];
+        // The list, back to front, in chunks of kChunk entries.
         for (int hq = cnt; hq > 0; hq -= kChunk) {
             const int lq = hq > kChunk ? hq - kChunk : 0;
             const int nq = hq - lq;
-            // 1. Lockstep evaluation: which pixels of the warp blend each entry.
-            uint32_t mine = 0, any = 0;
+            // 1. This pixel's bit of each entry's mask.
+            uint32_t mine = 0;
 #pragma unroll
-            for (int k = 0; k < kChunk; ++k) {
-                bool act = false;
-                if (k < nq) {
-                    const int j = list[lq + k];
-                    const SplatGeo g = s_geo[j];
-                    const SplatGeo2 gg = s_geo2[j];
-                    float dx, dy;
-                    const float e2 = eval_e2(g, gg.C, px, py, dx, dy);
-                    act = uint32_t(lo + j) < n_p && e2 >= gg.thr;
-                }
-                mine |= uint32_t(act) << k;
-                any |= uint32_t(__ballot_sync(0xffffffffu, act) != 0u) << k;
-            }
-            if (!any) continue;
-            // 2. One slot row per entry that any pixel blends: zero my column,
-            //    record the splat.
-            const int nrows = __popc(any);
+            for (int k = 0; k < kChunk; ++k)
+                if (k < nq) mine |= ((lmask[lq + k] >> lane) & 1u) << k;
+            // 2. One slot row per entry: zero my column, record the splat.
+            const int nrows = nq;
             if (nslots + nrows > kSlots) {
                 flush_slots<ACCUM>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
                                    s_rec[warp]);
@@ -280,10 +278,10 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                 s_q[warp][nslots + r][lane] = 0.0f;
                 s_w[warp][nslots + r][lane] = 0.0f;
             }
-            if (lane < nq && ((any >> lane) & 1u)) {
+            if (lane < nq) {
                 const int j = list[lq + lane];
                 const SplatGeo g = s_geo[j];
-                s_rec[warp][nslots + __popc(any & lt)] =
+                s_rec[warp][nslots + lane] =
                     SlotRec{g.mx, g.my, g.A, g.B, s_geo2[j].C, s_geo2[j].o, s_col[j].idx, 0u};
             }
             // 3. Each pixel walks only its own blended entries, back to front.
@@ -310,7 +308,7 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                 S1 = fmaf(c.g, wv, S1);
                 S2 = fmaf(c.b, wv, S2);
                 T = Ti;
-                const int row = nslots + __popc(any & ((1u << k) - 1u));
+                const int row = nslots + k;
                 s_q[warp][row][lane ^ row] = qv;
                 s_w[warp][row][lane ^ row] = wv;
             }
@@ -371,9 +369,10 @@ using namespace ss;
 
 extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
                                    const uint32_t *vals,
-                                   const uint32_t *tile_offsets, int32_t W, int32_t H,
-                                   const float *bg, uint32_t flags, const float *T_final,
-                                   const uint32_t *last_contrib, const float *dL_dimage,
+                                   const uint32_t *tile_offsets, int64_t n_pairs, int32_t W,
+                                   int32_t H, const float *bg, uint32_t flags, const float *T_final,
+                                   const uint32_t *last_contrib, const uint32_t *blend_masks,
+                                   const float *dL_dimage,
                                    const ss_grads *grads, float *accum_weight, void *workspace,
                                    size_t workspace_bytes, ss_stream_t stream) {
     clear_error();
@@ -389,6 +388,10 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: vals/offsets NULL");
     if (!T_final || !last_contrib || !dL_dimage)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: T_final/last_contrib/dL_dimage NULL");
+    if (n_pairs < 0 || n_pairs > int64_t(0xffffffffu))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: n_pairs outside 0..2^32-1");
+    if (n_pairs > 0 && !blend_masks)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: blend_masks is NULL");
     if (!grads || (n > 0 && (!grads->dmean2d || !grads->dconic || !grads->dopacity || !grads->drgb)))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: a gradient array is NULL");
     const bool accum = flags & SS_ACCUM_WEIGHT;
@@ -407,6 +410,8 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     p.n = n;
     p.vals = vals;
     p.offs = tile_offsets;
+    p.masks = blend_masks;
+    p.n_pairs = n_pairs;
     p.W = W;
     p.H = H;
     p.tiles_x = tiles_x(W);
@@ -468,9 +473,11 @@ static unsigned long long *g_noalloc_ptr[64];  // device address of the array, p
 
 extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats,
                                    const uint32_t *vals,
-                                           const uint32_t *tile_offsets, int32_t W, int32_t H,
+                                           const uint32_t *tile_offsets, int64_t n_pairs,
+                                           int32_t W, int32_t H,
                                            const float *bg, uint32_t flags, const float *T_final,
-                                           const uint32_t *last_contrib, const float *dL_dimage,
+                                           const uint32_t *last_contrib,
+                                           const uint32_t *blend_masks, const float *dL_dimage,
                                            const ss_grads *grads, float *accum_weight,
                                            ss_stream_t stream) {
     clear_error();
@@ -493,6 +500,10 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: vals/offsets NULL");
     if (!T_final || !last_contrib || !dL_dimage)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: T_final/last_contrib/dL_dimage NULL");
+    if (n_pairs < 0 || n_pairs > int64_t(0xffffffffu))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: n_pairs outside 0..2^32-1");
+    if (n_pairs > 0 && !blend_masks)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: blend_masks is NULL");
     if (!grads || (n > 0 && (!grads->dmean2d || !grads->dconic || !grads->dopacity || !grads->drgb)))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: a gradient array is NULL");
     const bool accum = flags & SS_ACCUM_WEIGHT;
@@ -521,6 +532,8 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     p.n = n;
     p.vals = vals;
     p.offs = tile_offsets;
+    p.masks = blend_masks;
+    p.n_pairs = n_pairs;
     p.W = W;
     p.H = H;
     p.tiles_x = tiles_x(W);

@@ -170,6 +170,24 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// The backward's staging: the record without its cull box (the forward's
+// blend masks replace the box test there).
+__device__ __forceinline__ void stage_record3_async(const SplatRecord *recs, uint32_t idx, int32_t n,
+                                                    SplatGeo *geo, SplatGeo2 *geo2, SplatCol *col,
+                                                    int t) {
+    if (idx < uint32_t(n)) {
+        const SplatRecord *r = recs + idx;
+        cp_async16(&geo[t], &r->geo);
+        cp_async16(&geo2[t], &r->geo2);
+        cp_async16(&col[t], &r->col);
+    } else {
+        const SplatRecord r = invisible_record();
+        geo[t] = r.geo;
+        geo2[t] = r.geo2;
+        col[t] = r.col;
+    }
+}
+
 // Stage record `idx` (or the invisible record if idx >= n) into shared
 // memory slot `t` of the four arrays with 16-byte asynchronous copies.
 __device__ __forceinline__ void stage_record_async(const SplatRecord *recs, uint32_t idx, int32_t n,

@@ -11,6 +11,12 @@
 // that short list.  A pixel stops at the first splat whose blend would take
 // T below 1e-4; the CTA stops once all its pixels have.  The median-depth
 // output is a template variant, so the default variant does no median work.
+//
+// The warp also records, for each pair it reached, which of its 32 pixels
+// blended the splat (a ballot): blend_masks[b * n_pairs + p], b = warp.
+// The backward reads these decisions instead of re-evaluating every
+// (pixel, splat) of the list, and they are by construction exactly the
+// forward's.
 #include "ss_device.cuh"
 #include "ss_internal.h"
 #include "ss_profile.h"
@@ -24,6 +30,8 @@ struct FwdParams {
     const uint32_t *offs;
     int32_t W, H, tiles_x;
     float bg[3];
+    uint32_t *masks;   // [8][n_pairs]
+    int64_t n_pairs;
     float *image;
     float *T_final;
     uint32_t *last;
@@ -37,6 +45,7 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
     __shared__ SplatCol s_col[2][256];
     __shared__ SplatBox s_box[2][256];
     __shared__ uint8_t s_list[8][256];
+    __shared__ uint32_t s_mask[8][256];
 
     const int tid = threadIdx.x;
     const int tile = blockIdx.x;
@@ -92,31 +101,41 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
             if (hit) s_list[warp][cnt + __popc(m & lt)] = uint8_t(j);
             cnt += __popc(m);
         }
+        for (int k = lane; k < nb; k += 32) s_mask[warp][k] = 0u;
         __syncwarp();
-        if (done) continue;
         for (int q = 0; q < cnt; ++q) {
             const int j = s_list[warp][q];
             const SplatGeo g = s_geo[buf][j];
             const SplatGeo2 g2 = s_geo2[buf][j];
             float dx, dy;
             const float e2 = eval_e2(g, g2.C, px, py, dx, dy);
-            if (!(e2 >= g2.thr)) continue;  // skipped (alpha < 1/255); NaN-safe
-            float oG;
-            const float alpha = eval_alpha(g2.o, ex2_approx(e2), oG);
-            const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
-            if (Tn < kTEps) {
-                done = true;
-                break;
+            bool blend = false;
+            if (!done && e2 >= g2.thr) {  // else skipped (alpha < 1/255); NaN-safe
+                float oG;
+                const float alpha = eval_alpha(g2.o, ex2_approx(e2), oG);
+                const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
+                if (Tn < kTEps) {
+                    done = true;
+                } else {
+                    blend = true;
+                    const SplatCol c = s_col[buf][j];
+                    const float w = alpha * T;
+                    cr = fmaf(c.r, w, cr);
+                    cg = fmaf(c.g, w, cg);
+                    cb = fmaf(c.b, w, cb);
+                    if (MEDIAN && T > 0.5f) med = g2.depth;
+                    T = Tn;
+                    last = base - start + uint32_t(j) + 1u;
+                }
             }
-            const SplatCol c = s_col[buf][j];
-            const float w = alpha * T;
-            cr = fmaf(c.r, w, cr);
-            cg = fmaf(c.g, w, cg);
-            cb = fmaf(c.b, w, cb);
-            if (MEDIAN && T > 0.5f) med = g2.depth;
-            T = Tn;
-            last = base - start + uint32_t(j) + 1u;
+            const uint32_t m = __ballot_sync(0xffffffffu, blend);
+            if (lane == 0) s_mask[warp][j] = m;
+            if (__all_sync(0xffffffffu, done)) break;
         }
+        __syncwarp();
+        uint32_t *gm = p.masks + size_t(warp) * size_t(p.n_pairs) + base;
+        for (int k = lane; k < nb; k += 32)
+            if (base + uint32_t(k) < p.n_pairs) gm[k] = s_mask[warp][k];
     }
     cp_async_wait<0>();  // no copy may outlive the CTA
     if (inside) {
@@ -135,10 +154,10 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
 using namespace ss;
 
 extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *vals,
-                                   const uint32_t *tile_offsets, int32_t W, int32_t H,
-                                   const float *bg, uint32_t flags, float *image, float *T_final,
-                                   uint32_t *last_contrib, float *median_depth,
-                                   ss_stream_t stream) {
+                                   const uint32_t *tile_offsets, int64_t n_pairs, int32_t W,
+                                   int32_t H, const float *bg, uint32_t flags, float *image,
+                                   float *T_final, uint32_t *last_contrib, float *median_depth,
+                                   uint32_t *blend_masks, ss_stream_t stream) {
     clear_error();
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_fwd: image %dx%d outside 1..%d", W, H, kMaxSide);
@@ -151,6 +170,10 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
     if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: vals/offsets NULL");
     if (!image || !T_final || !last_contrib)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: an output is NULL");
+    if (n_pairs < 0 || n_pairs > int64_t(0xffffffffu))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: n_pairs outside 0..2^32-1");
+    if (n_pairs > 0 && !blend_masks)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: blend_masks is NULL");
     const bool median = flags & SS_MEDIAN_DEPTH;
     if (median && !median_depth)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: SS_MEDIAN_DEPTH set but median_depth NULL");
@@ -167,6 +190,8 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
     p.T_final = T_final;
     p.last = last_contrib;
     p.median = median_depth;
+    p.masks = blend_masks;
+    p.n_pairs = n_pairs;
     const int grid = tiles_x(W) * tiles_y(H);
     cudaStream_t st = (cudaStream_t)stream;
     if (median)

@@ -178,13 +178,22 @@ ss_status ss_sort_status(const void *workspace, ss_stream_t stream);
  *   median_depth[H][W]  only with SS_MEDIAN_DEPTH (else may be NULL): depth
  *                       of the last splat blended while T > 0.5, 0 if none
  *   bg: HOST float[3] background, or NULL for black.
+ *   blend_masks: device uint32[8][n_pairs]; for each pair p the forward
+ *                reached and each 8x4 pixel block b of p's tile
+ *                (b = 2 (row / 4) + (column / 8) within the tile),
+ *                blend_masks[b * n_pairs + p] has bit i set iff pixel
+ *                (column 8 (b & 1) + (i & 7), row 4 (b >> 1) + (i >> 3)) blended
+ *                the splat.  The backward replays exactly these decisions.
+ *                Entries past the point where every pixel of a block stopped
+ *                are left unwritten.
  *   records, n_splats: the records ss_bin_tiles wrote for these splats.
- *   vals, tile_offsets: the output of ss_sort_pairs for the same W, H.
+ *   vals, tile_offsets, n_pairs: the output of ss_sort_pairs for the same W, H.
  * Pair values >= n_splats are ignored. */
 ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *vals,
-                        const uint32_t *tile_offsets, int32_t W, int32_t H, const float *bg,
-                        uint32_t flags, float *image, float *T_final, uint32_t *last_contrib,
-                        float *median_depth, ss_stream_t stream);
+                        const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,
+                        const float *bg, uint32_t flags, float *image, float *T_final,
+                        uint32_t *last_contrib, float *median_depth, uint32_t *blend_masks,
+                        ss_stream_t stream);
 
 /* Backward rasterization ("从 8.6 KB 到 4.2 KB ...", rasterize_bwd_2d on the
  * 2D screen-space path; "Phase 5 step 30b", rasterize_backwards: the 9-field
@@ -202,7 +211,8 @@ ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *v
  * per field per warp ("Phase 5 step 30b", conclusion: one atomic per warp
  * instead of per thread).
  *   records, n_splats: the records ss_bin_tiles wrote for these splats.
- *   T_final, last_contrib: from ss_raster_fwd with the same inputs.
+ *   T_final, last_contrib, blend_masks: from ss_raster_fwd with the same
+ *   inputs (the blend decisions are the forward's, not re-evaluated).
  *   dL_dimage: device float[3][H][W].
  *   grads: all four arrays required; overwritten (zeroed here first).
  *   accum_weight: with SS_ACCUM_WEIGHT, device float[n] overwritten with
@@ -211,8 +221,9 @@ ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *v
  *   workspace: >= ss_workspace_bytes(n, 0, W, H) bytes, 256-byte aligned.
  *   bg: HOST float[3] or NULL (must match the forward call). */
 ss_status ss_raster_bwd(const void *records, int32_t n_splats, const uint32_t *vals,
-                        const uint32_t *tile_offsets, int32_t W, int32_t H, const float *bg,
-                        uint32_t flags, const float *T_final, const uint32_t *last_contrib,
+                        const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,
+                        const float *bg, uint32_t flags, const float *T_final,
+                        const uint32_t *last_contrib, const uint32_t *blend_masks,
                         const float *dL_dimage, const ss_grads *grads, float *accum_weight,
                         void *workspace, size_t workspace_bytes, ss_stream_t stream);
 
@@ -235,10 +246,11 @@ ss_status ss_raster_bwd(const void *records, int32_t n_splats, const uint32_t *v
  *     calls that overlap on the GPU (other streams, other host threads) race
  *     on it: serialise them. */
 ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats, const uint32_t *vals,
-                                const uint32_t *tile_offsets, int32_t W, int32_t H,
-                                const float *bg, uint32_t flags, const float *T_final,
-                                const uint32_t *last_contrib, const float *dL_dimage,
-                                const ss_grads *grads, float *accum_weight, ss_stream_t stream);
+                                const uint32_t *tile_offsets, int64_t n_pairs, int32_t W,
+                                int32_t H, const float *bg, uint32_t flags, const float *T_final,
+                                const uint32_t *last_contrib, const uint32_t *blend_masks,
+                                const float *dL_dimage, const ss_grads *grads,
+                                float *accum_weight, ss_stream_t stream);
 
 /* Per-kernel timing ("从 8.6 KB 到 4.2 KB ...", section 亲手验证: SS_PROFILE=1
  * gives per-kernel segment timings).  Off unless the environment has

@@ -47,6 +47,7 @@ def run_gpu(scene, capacity=None, stream=None):
     out = {"count": pairs, "culled": culled,
            "keys_binned": r.keys[:pairs].cpu().numpy().view(np.uint64).copy(),
            "vals_binned": r.vals[:pairs].cpu().numpy().view(np.uint32).copy()}
+    r.n_pairs = pairs
     ss.ss_sort_pairs(r.keys, r.vals, pairs, scene.W, scene.H, r.tile_offsets, r.workspace, stream)
     out["sort_status"] = ss.ss_sort_status(r.workspace, stream)
     out["keys"] = r.keys[:pairs].cpu().numpy().view(np.uint64).copy()

@@ -93,25 +93,29 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert lib.ss_sort_pairs(0x1000, 0x1000, 10, 16, 16, 0x1000, 0x1000, 16, None) == 1
     assert "workspace" in lib.ss_last_error().decode()
     # forward: unknown flags, NULL outputs, median flag without buffer
-    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 16, 16, None, 8, 0x1000, 0x1000,
-                             0x1000, None, None) == 1
-    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 16, 16, None, 0, None, 0x1000,
-                             0x1000, None, None) == 1
-    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 16, 16, None, 2, 0x1000, 0x1000,
-                             0x1000, None, None) == 1
-    assert lib.ss_raster_fwd(None, 5, 0x1000, 0x1000, 16, 16, None, 0, 0x1000, 0x1000,
-                             0x1000, None, None) == 1
+    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 8, 0x1000, 0x1000,
+                             0x1000, None, 0x1000, None) == 1
+    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 0, None, 0x1000,
+                             0x1000, None, 0x1000, None) == 1
+    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 2, 0x1000, 0x1000,
+                             0x1000, None, 0x1000, None) == 1
+    assert lib.ss_raster_fwd(None, 5, 0x1000, 0x1000, 0, 16, 16, None, 0, 0x1000, 0x1000,
+                             0x1000, None, 0x1000, None) == 1
+    assert lib.ss_raster_fwd(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 0, 0x1000, 0x1000,
+                             0x1000, None, None, None) == 1   # blend_masks NULL
     # backward: NULL gradient array, accum flag without buffer or workspace
     g = SsGrads(0x1000, None, 0x1000, 0x1000)
-    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 16, 16, None, 0, 0x1000, 0x1000,
-                             0x1000, ctypes.byref(g), None, None, 0, None) == 1
+    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 0, 0x1000, 0x1000,
+                             0x1000, 0x1000, ctypes.byref(g), None, None, 0, None) == 1
     g = SsGrads(0x1000, 0x1000, 0x1000, 0x1000)
-    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 16, 16, None, 1, 0x1000, 0x1000,
-                             0x1000, ctypes.byref(g), None, 0x1000, 1 << 20, None) == 1
-    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 16, 16, None, 1, 0x1000, 0x1000,
-                             0x1000, ctypes.byref(g), 0x1000, 0x1000, 8, None) == 1
-    assert lib.ss_raster_bwd(None, 4, 0x1000, 0x1000, 16, 16, None, 0, 0x1000, 0x1000,
-                             0x1000, ctypes.byref(g), None, None, 0, None) == 1
+    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 1, 0x1000, 0x1000,
+                             0x1000, 0x1000, ctypes.byref(g), None, 0x1000, 1 << 20, None) == 1
+    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 1, 0x1000, 0x1000,
+                             0x1000, 0x1000, ctypes.byref(g), 0x1000, 0x1000, 8, None) == 1
+    assert lib.ss_raster_bwd(None, 4, 0x1000, 0x1000, 8, 16, 16, None, 0, 0x1000, 0x1000,
+                             0x1000, 0x1000, ctypes.byref(g), None, None, 0, None) == 1
+    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 0, 0x1000, 0x1000,
+                             None, 0x1000, ctypes.byref(g), None, None, 0, None) == 1
     # pair count / sort status with NULL
     assert lib.ss_pair_count(None, 0, None, None, None) == 1
     assert lib.ss_sort_status(None, None) == 1

@@ -48,8 +48,9 @@ def test_noalloc_backward_matches_workspace_backward_twice(ss):
     for call in range(2):
         grads = {k: torch.full_like(r.grads[k], float("nan")) for k in FIELDS}
         w = torch.full_like(r.accum_weight, float("nan"))
-        ss.ss_raster_bwd_noalloc(r.records, sc.n, r.vals, r.tile_offsets, sc.W, sc.H, sc.bg,
-                                 flags, r.T_final, r.last_contrib, dL, grads, w)
+        ss.ss_raster_bwd_noalloc(r.records, sc.n, r.vals, r.tile_offsets, r.n_pairs, sc.W, sc.H,
+                                 sc.bg, flags, r.T_final, r.last_contrib, r.blend_masks, dL,
+                                 grads, w)
         torch.cuda.synchronize()
         for k in FIELDS:
             got = grads[k].cpu().numpy().astype(np.float64)
@@ -65,7 +66,7 @@ def test_noalloc_rejects_more_splats_than_its_scratch(ss):
     L = ss._L
     big = (1 << 21) + 1
     g = SsGrads(0x1000, 0x1000, 0x1000, 0x1000)
-    st = L.ss_raster_bwd_noalloc(0x1000, big, 0x1000, 0x1000, 64, 64, None, 1, 0x1000, 0x1000,
-                                 0x1000, ctypes.byref(g), 0x1000, None)
+    st = L.ss_raster_bwd_noalloc(0x1000, big, 0x1000, 0x1000, 16, 64, 64, None, 1, 0x1000,
+                                 0x1000, 0x1000, 0x1000, ctypes.byref(g), 0x1000, None)
     assert st == 5                     # SS_ERR_UNSUPPORTED, nothing launched
     assert "fixed scratch" in ss.ss_last_error()
