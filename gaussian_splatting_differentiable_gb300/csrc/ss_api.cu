@@ -54,7 +54,7 @@ WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H) {
     off = align256(off + size_t(n_pairs) * 4);
     L.sort_end = off;
     L.accum = 256;  // after the status word; the sort's regions are dead by then
-    L.bwd_end = align256(L.accum + size_t(n_splats) * 8);
+    L.bwd_end = align256(L.accum + size_t(n_splats) * 48);  // 48-byte gradient record per splat
     L.total = L.sort_end > L.bwd_end ? L.sort_end : L.bwd_end;
     return L;
 }

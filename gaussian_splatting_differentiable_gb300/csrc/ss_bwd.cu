@@ -51,8 +51,21 @@ struct BwdParams {
     const uint32_t *last;
     const float *dL;
     float *dmean2d, *dconic, *dopacity, *drgb;
-    unsigned long long *accum;  // 32.32 fixed point
+    unsigned long long *accum;  // 32.32 fixed point (SoA mode)
+    float *scratch;             // [n][12] per-splat gradient record (AoS mode)
 };
+
+// Per-splat gradient scratch record (AoS mode), 48 bytes, 16-byte aligned:
+// [0..3] dmean x, dmean y, dconic a, dconic b; [4..7] dconic c, dopacity,
+// drgb r, drgb g; [8] drgb b; [9] unused; [10..11] accumulated weight as a
+// uint64 in 32.32 fixed point.
+constexpr int kGradRec = 12;
+
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
 
 constexpr int kSlots = 16;     // slots per warp
 constexpr int kChunk = 16;     // list entries evaluated together (<= kSlots)
@@ -72,7 +85,7 @@ struct __align__(16) SlotRec {
     uint32_t idx, pad;
 };
 
-template <bool ACCUM>
+template <bool ACCUM, bool AOS>
 __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int lane, float wx0,
                                             float wy0, const float (*q)[kSlotPad],
                                             const float (*w)[kSlotPad], const float4 *g,
@@ -124,10 +137,24 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
         Wg += __shfl_xor_sync(0xffffffffu, Wg, 1, 2);
         Wb += __shfl_xor_sync(0xffffffffu, Wb, 1, 2);
         const size_t i = r.idx;
+        const float dmx = kLn2 * (2.0f * r.A * Qx + r.B * Qy);
+        const float dmy = kLn2 * (r.B * Qx + 2.0f * r.C * Qy);
         if (slot >= nslots) {
+        } else if (AOS) {
+            // Four reductions per (warp, splat) into one 48-byte record.
+            float *g = p.scratch + kGradRec * i;
+            if (half == 0) {
+                red_add_v4(g, dmx, dmy, 0.5f * Qxx, Qxy);
+            } else {
+                red_add_v4(g + 4, 0.5f * Qyy, -Q / r.o, Wr, Wg);
+                atomicAdd(g + 8, Wb);
+                if (ACCUM)
+                    atomicAdd(reinterpret_cast<unsigned long long *>(g + 10),
+                              (unsigned long long)__float2ull_rn(Wt * 4294967296.0f));
+            }
         } else if (half == 0) {
-            atomicAdd(p.dmean2d + 2 * i, kLn2 * (2.0f * r.A * Qx + r.B * Qy));
-            atomicAdd(p.dmean2d + 2 * i + 1, kLn2 * (r.B * Qx + 2.0f * r.C * Qy));
+            atomicAdd(p.dmean2d + 2 * i, dmx);
+            atomicAdd(p.dmean2d + 2 * i + 1, dmy);
             atomicAdd(p.dconic + 3 * i, 0.5f * Qxx);
             atomicAdd(p.dconic + 3 * i + 1, Qxy);
             atomicAdd(p.dconic + 3 * i + 2, 0.5f * Qyy);
@@ -142,7 +169,7 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
     __syncwarp();
 }
 
-template <bool ACCUM>
+template <bool ACCUM, bool AOS>
 __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     __shared__ SplatGeo s_geo_[2][256];
     __shared__ SplatGeo2 s_geo2_[2][256];
@@ -270,7 +297,7 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
             // 2. One slot row per entry: zero my column, record the splat.
             const int nrows = nq;
             if (nslots + nrows > kSlots) {
-                flush_slots<ACCUM>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
+                flush_slots<ACCUM, AOS>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
                                    s_rec[warp]);
                 nslots = 0;
             }
@@ -316,7 +343,7 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
         }
     }
     cp_async_wait<0>();  // no copy may outlive the CTA
-    if (nslots) flush_slots<ACCUM>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
+    if (nslots) flush_slots<ACCUM, AOS>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
                                    s_rec[warp]);
 }
 
@@ -329,13 +356,12 @@ static ss_status ensure_bwd_smem() {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && g_bwd_attr_set[dev]) return SS_OK;
-    ss_status s = check_cuda(cudaFuncSetAttribute(k_raster_bwd<true>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  kBwdDynSmem),
-                             "ss_raster_bwd: cudaFuncSetAttribute");
-    if (s == SS_OK)
-        s = check_cuda(cudaFuncSetAttribute(k_raster_bwd<false>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdDynSmem),
+    const void *fns[4] = {(const void *)k_raster_bwd<true, true>, (const void *)k_raster_bwd<false, true>,
+                          (const void *)k_raster_bwd<true, false>, (const void *)k_raster_bwd<false, false>};
+    ss_status s = SS_OK;
+    for (int f = 0; f < 4 && s == SS_OK; ++f)
+        s = check_cuda(cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            kBwdDynSmem),
                        "ss_raster_bwd: cudaFuncSetAttribute");
     if (s == SS_OK && dev >= 0 && dev < 64) g_bwd_attr_set[dev] = 1;
     return s;
@@ -354,6 +380,36 @@ __global__ void k_bwd_zero(BwdParams p, int64_t n, bool accum) {
         p.drgb[3 * i + 1] = 0.0f;
         p.drgb[3 * i + 2] = 0.0f;
         if (accum) p.accum[i] = 0ull;
+    }
+}
+
+// AoS mode: clear the per-splat gradient records.
+__global__ void k_grad_zero(float4 *scratch, int64_t n4) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
+        scratch[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// AoS mode: gradient records -> the SoA outputs (and the weight to float).
+__global__ void k_grad_final(BwdParams p, int64_t n, float *accum_out) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const float4 *g = reinterpret_cast<const float4 *>(p.scratch + kGradRec * i);
+        const float4 a = g[0], b = g[1], c = g[2];
+        p.dmean2d[2 * i] = a.x;
+        p.dmean2d[2 * i + 1] = a.y;
+        p.dconic[3 * i] = a.z;
+        p.dconic[3 * i + 1] = a.w;
+        p.dconic[3 * i + 2] = b.x;
+        p.dopacity[i] = b.y;
+        p.drgb[3 * i] = b.z;
+        p.drgb[3 * i + 1] = b.w;
+        p.drgb[3 * i + 2] = c.x;
+        if (accum_out) {
+            const unsigned long long w =
+                *reinterpret_cast<const unsigned long long *>(p.scratch + kGradRec * i + 10);
+            accum_out[i] = float(double(w) * (1.0 / 4294967296.0));
+        }
     }
 }
 
@@ -398,9 +454,9 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     if (accum && n > 0 && !accum_weight)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: SS_ACCUM_WEIGHT set but accum_weight NULL");
     const WsLayout L = ws_layout(n, 0, W, H);
-    if (accum && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)))
+    if (n > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: workspace NULL or not 256-byte aligned");
-    if (accum && workspace_bytes < L.bwd_end)
+    if (n > 0 && workspace_bytes < L.bwd_end)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: workspace %zu bytes < %zu needed",
                     workspace_bytes, L.bwd_end);
     if (n == 0) return SS_OK;
@@ -423,9 +479,8 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     p.dconic = grads->dconic;
     p.dopacity = grads->dopacity;
     p.drgb = grads->drgb;
-    p.accum = accum ? reinterpret_cast<unsigned long long *>(static_cast<unsigned char *>(workspace) +
-                                                              L.accum)
-                    : nullptr;
+    p.accum = nullptr;
+    p.scratch = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + L.accum);
     cudaStream_t st = (cudaStream_t)stream;
     ss_status es = ensure_bwd_smem();
     if (es != SS_OK) return es;
@@ -434,14 +489,15 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t want = (int64_t(n) + 255) / 256;
     const int zgrid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
-    SS_LAUNCH("k_bwd_zero", st, k_bwd_zero<<<zgrid, 256, 0, st>>>(p, n, accum));
+    SS_LAUNCH("k_grad_zero", st,
+              k_grad_zero<<<zgrid, 256, 0, st>>>(reinterpret_cast<float4 *>(p.scratch), 3 * int64_t(n)));
     const int grid = tiles_x(W) * tiles_y(H);
     if (accum)
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true><<<grid, 256, kBwdDynSmem, st>>>(p));
+        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true, true><<<grid, 256, kBwdDynSmem, st>>>(p));
     else
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false><<<grid, 256, kBwdDynSmem, st>>>(p));
-    if (accum)
-        SS_LAUNCH("k_accum_final", st, k_accum_final<<<zgrid, 256, 0, st>>>(p.accum, accum_weight, n));
+        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false, true><<<grid, 256, kBwdDynSmem, st>>>(p));
+    SS_LAUNCH("k_grad_final", st,
+              k_grad_final<<<zgrid, 256, 0, st>>>(p, n, accum ? accum_weight : nullptr));
     return check_launch("ss_raster_bwd");
 }
 
@@ -556,9 +612,9 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     SS_LAUNCH("k_bwd_zero", st, k_bwd_zero<<<zgrid, 256, 0, st>>>(p, n, accum));
     const int grid = tiles_x(W) * tiles_y(H);
     if (accum)
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true><<<grid, 256, kBwdDynSmem, st>>>(p));
+        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true, false><<<grid, 256, kBwdDynSmem, st>>>(p));
     else
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false><<<grid, 256, kBwdDynSmem, st>>>(p));
+        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false, false><<<grid, 256, kBwdDynSmem, st>>>(p));
     if (accum)
         SS_LAUNCH("k_accum_final", st, k_accum_final<<<zgrid, 256, 0, st>>>(p.accum, accum_weight, n));
     return check_launch("ss_raster_bwd_noalloc");

@@ -48,7 +48,7 @@ struct WsLayout {
     size_t alt_keys;      // uint64 [n_pairs] ping-pong buffer
     size_t alt_vals;      // uint32 [n_pairs]
     size_t sort_end;
-    size_t accum;         // uint64 [n_splats] backward 32.32 fixed-point accumulator
+    size_t accum;         // backward per-splat gradient records, 48 bytes each
     size_t bwd_end;
     size_t total;
     int ndig;
