@@ -206,8 +206,11 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
         g2 = p.dL[2 * HW + pix];
     }
     s_g[warp][lane] = make_float4(g0, g1, g2, 0.0f);
-    const float Tb0 = T * p.bg[0], Tb1 = T * p.bg[1], Tb2 = T * p.bg[2];
-    float S0 = 0.0f, S1 = 0.0f, S2 = 0.0f;
+    // GR = dL/dimage . (S + T_final bg), S the colour blended behind the
+    // current splat: with it dL/dalpha = (T gc - GR) / (1 - alpha), where
+    // gc = dL/dimage . rgb and T is the transmittance behind the splat, and
+    // blending the splat adds w gc to GR.
+    float GR = T * (g0 * p.bg[0] + g1 * p.bg[1] + g2 * p.bg[2]);
 
     const uint32_t wmax = __reduce_max_sync(0xffffffffu, n_p);
     if (lane == 0) s_wmax[warp] = wmax;
@@ -327,13 +330,10 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                 const float inv = rcp_approx(__fsub_rn(1.0f, alpha));
                 const float Ti = T * inv;  // T in front of this splat
                 const float wv = alpha * Ti;
-                const float dLda = g0 * (c.r * Ti - (S0 + Tb0) * inv) +
-                                   g1 * (c.g * Ti - (S1 + Tb1) * inv) +
-                                   g2 * (c.b * Ti - (S2 + Tb2) * inv);
+                const float gc = fmaf(g0, c.r, fmaf(g1, c.g, g2 * c.b));
+                const float dLda = inv * fmaf(T, gc, -GR);
                 const float qv = oG <= kAlphaMax ? -alpha * dLda : 0.0f;  // capped: constant
-                S0 = fmaf(c.r, wv, S0);
-                S1 = fmaf(c.g, wv, S1);
-                S2 = fmaf(c.b, wv, S2);
+                GR = fmaf(wv, gc, GR);
                 T = Ti;
                 const int row = nslots + k;
                 s_q[warp][row][lane ^ row] = qv;
