@@ -97,34 +97,40 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
     const int slot = lane >> 1, half = lane & 1;
     {
         const SlotRec r = rec[slot];
-        float dxu[8], dyv[2];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) dxu[u] = __fsub_rn(wx0 + float(u), r.mx);
-#pragma unroll
-        for (int v = 0; v < 2; ++v) dyv[v] = __fsub_rn(wy0 + float(2 * half + v), r.my);
-        float Q = 0.f, Qx = 0.f, Qy = 0.f, Qxx = 0.f, Qxy = 0.f, Qyy = 0.f;
+        // Raw moments around this half's first pixel centre (offsets u in
+        // 0..7, v in {0, 1} are constants of the unrolled loop; v^2 = v), then
+        // re-centred on the splat mean: dx = u + ex, dy = v + ey.
+        float M1 = 0.f, Mu = 0.f, Mv = 0.f, Muu = 0.f, Muv = 0.f;
         float Wt = 0.f, Wr = 0.f, Wg = 0.f, Wb = 0.f;
         const float *qs = q[slot];
         const float *ws = w[slot];
         const float4 *gs = g + 16 * half;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
+            const int u = i & 7, v = i >> 3;
             const float qi = qs[(16 * half + i) ^ slot], wi = ws[(16 * half + i) ^ slot];
-            const float dx = dxu[i & 7], dy = dyv[i >> 3];
-            Q += qi;
-            const float t = qi * dx;
-            Qx += t;
-            Qxx = fmaf(t, dx, Qxx);
-            Qxy = fmaf(t, dy, Qxy);
-            const float s = qi * dy;
-            Qy += s;
-            Qyy = fmaf(s, dy, Qyy);
+            M1 += qi;
+            if (u) {
+                Mu = fmaf(float(u), qi, Mu);
+                Muu = fmaf(float(u * u), qi, Muu);
+            }
+            if (v) {
+                Mv += qi;
+                if (u) Muv = fmaf(float(u), qi, Muv);
+            }
             const float4 gg = gs[i];
             Wt += wi;
             Wr = fmaf(wi, gg.x, Wr);
             Wg = fmaf(wi, gg.y, Wg);
             Wb = fmaf(wi, gg.z, Wb);
         }
+        const float ex = __fsub_rn(wx0, r.mx), ey = __fsub_rn(wy0 + float(2 * half), r.my);
+        float Q = M1;
+        float Qx = fmaf(ex, M1, Mu);
+        float Qy = fmaf(ey, M1, Mv);
+        float Qxx = fmaf(ex, fmaf(ex, M1, 2.0f * Mu), Muu);
+        float Qxy = fmaf(ex, fmaf(ey, M1, Mv), fmaf(ey, Mu, Muv));
+        float Qyy = fmaf(ey, fmaf(ey, M1, 2.0f * Mv), Mv);
         // Sum the two halves of the slot (lanes 2k and 2k+1).
         Q += __shfl_xor_sync(0xffffffffu, Q, 1, 2);
         Qx += __shfl_xor_sync(0xffffffffu, Qx, 1, 2);
