@@ -69,8 +69,11 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
 
 constexpr int kSlots = 16;     // slots per warp
 constexpr int kChunk = 16;     // list entries evaluated together (<= kSlots)
-constexpr int kSlotPad = 32;   // row pitch; pixel p of slot r is stored at column p ^ r, which
-                               // keeps the lane pairs' column reads free of bank conflicts
+constexpr int kSlotPad = 32;   // entries per slot row (one per pixel of the warp's block)
+// Pixel p of slot row r is stored at column p ^ (2 (r & 7)): the replay's
+// row writes are permutations, and the flush's 64-bit reads, where lane pair
+// (r, h) takes pixels 2i + h, hit 32 distinct bank pairs.
+__device__ __forceinline__ int slot_col(int row, int pix) { return pix ^ ((row & 7) << 1); }
 
 __device__ __forceinline__ float rcp_approx(float x) {
     float y;
@@ -87,9 +90,8 @@ struct __align__(16) SlotRec {
 
 template <bool ACCUM, bool AOS>
 __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int lane, float wx0,
-                                            float wy0, const float (*q)[kSlotPad],
-                                            const float (*w)[kSlotPad], const float4 *g,
-                                            const SlotRec *rec) {
+                                            float wy0, const float2 (*qw)[kSlotPad],
+                                            const float4 *g, const SlotRec *rec) {
     __syncwarp();
     // Every lane runs the sums (lanes of unused slots read stale, in-bounds
     // rows) so that the pair shuffles see the whole warp; only the atomics
@@ -97,40 +99,46 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
     const int slot = lane >> 1, half = lane & 1;
     {
         const SlotRec r = rec[slot];
-        // Raw moments around this half's first pixel centre (offsets u in
-        // 0..7, v in {0, 1} are constants of the unrolled loop; v^2 = v), then
-        // re-centred on the splat mean: dx = u + ex, dy = v + ey.
-        float M1 = 0.f, Mu = 0.f, Mv = 0.f, Muu = 0.f, Muv = 0.f;
+        // Lane half h sums pixels 2i + h, i.e. column u = 2k + h (k = i & 3)
+        // and row v = i >> 2 of the 8x4 block; k and v are constants of the
+        // unrolled loop.  Raw moments in (k, v), then u = 2k + h and the
+        // centring dx = u + ex, dy = v + ey.
+        float M1 = 0.f, Mk = 0.f, Mkk = 0.f, Mv = 0.f, Mkv = 0.f, Mvv = 0.f;
         float Wt = 0.f, Wr = 0.f, Wg = 0.f, Wb = 0.f;
-        const float *qs = q[slot];
-        const float *ws = w[slot];
-        const float4 *gs = g + 16 * half;
+        const float2 *row = qw[slot];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const int u = i & 7, v = i >> 3;
-            const float qi = qs[(16 * half + i) ^ slot], wi = ws[(16 * half + i) ^ slot];
+            const int k = i & 3, v = i >> 2;
+            const int pix = 2 * i + half;
+            const float2 e = row[slot_col(slot, pix)];
+            const float qi = e.x, wi = e.y;
             M1 += qi;
-            if (u) {
-                Mu = fmaf(float(u), qi, Mu);
-                Muu = fmaf(float(u * u), qi, Muu);
+            if (k) {
+                Mk = fmaf(float(k), qi, Mk);
+                Mkk = fmaf(float(k * k), qi, Mkk);
             }
             if (v) {
-                Mv += qi;
-                if (u) Muv = fmaf(float(u), qi, Muv);
+                Mv = fmaf(float(v), qi, Mv);
+                Mvv = fmaf(float(v * v), qi, Mvv);
+                if (k) Mkv = fmaf(float(k * v), qi, Mkv);
             }
-            const float4 gg = gs[i];
+            const float4 gg = g[pix];
             Wt += wi;
             Wr = fmaf(wi, gg.x, Wr);
             Wg = fmaf(wi, gg.y, Wg);
             Wb = fmaf(wi, gg.z, Wb);
         }
-        const float ex = __fsub_rn(wx0, r.mx), ey = __fsub_rn(wy0 + float(2 * half), r.my);
+        const float hf = float(half);
+        const float Mu = fmaf(2.0f, Mk, hf * M1);
+        const float Muu = fmaf(4.0f, Mkk, hf * fmaf(4.0f, Mk, M1));
+        const float Muv = fmaf(2.0f, Mkv, hf * Mv);
+        const float ex = __fsub_rn(wx0, r.mx), ey = __fsub_rn(wy0, r.my);
         float Q = M1;
         float Qx = fmaf(ex, M1, Mu);
         float Qy = fmaf(ey, M1, Mv);
         float Qxx = fmaf(ex, fmaf(ex, M1, 2.0f * Mu), Muu);
         float Qxy = fmaf(ex, fmaf(ey, M1, Mv), fmaf(ey, Mu, Muv));
-        float Qyy = fmaf(ey, fmaf(ey, M1, 2.0f * Mv), Mv);
+        float Qyy = fmaf(ey, fmaf(ey, M1, 2.0f * Mv), Mvv);
         // Sum the two halves of the slot (lanes 2k and 2k+1).
         Q += __shfl_xor_sync(0xffffffffu, Q, 1, 2);
         Qx += __shfl_xor_sync(0xffffffffu, Qx, 1, 2);
@@ -185,10 +193,9 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     __shared__ uint32_t s_wmax[8];
     __shared__ float4 s_g[8][32];
     __shared__ SlotRec s_rec[8][kSlots];
-    // dynamic: q and w slots, [8 warps][kSlots][kSlotPad] floats each
-    extern __shared__ __align__(16) float s_dyn[];
-    float(*s_q)[kSlots][kSlotPad] = reinterpret_cast<float(*)[kSlots][kSlotPad]>(s_dyn);
-    float(*s_w)[kSlots][kSlotPad] = reinterpret_cast<float(*)[kSlots][kSlotPad]>(s_dyn + 8 * kSlots * kSlotPad);
+    // dynamic: (q, w) slots, [8 warps][kSlots][kSlotPad] float2
+    extern __shared__ __align__(16) float2 s_dyn[];
+    float2(*s_qw)[kSlots][kSlotPad] = reinterpret_cast<float2(*)[kSlots][kSlotPad]>(s_dyn);
 
     const int tile = blockIdx.x;
     const int tx = tile % p.tiles_x, ty = tile / p.tiles_x;
@@ -306,13 +313,12 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
             // 2. One slot row per entry: zero my column, record the splat.
             const int nrows = nq;
             if (nslots + nrows > kSlots) {
-                flush_slots<ACCUM, AOS>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
-                                   s_rec[warp]);
+                flush_slots<ACCUM, AOS>(p, nslots, lane, wx0, wy0, s_qw[warp], s_g[warp],
+                                        s_rec[warp]);
                 nslots = 0;
             }
             for (int r = 0; r < nrows; ++r) {
-                s_q[warp][nslots + r][lane] = 0.0f;
-                s_w[warp][nslots + r][lane] = 0.0f;
+                s_qw[warp][nslots + r][lane] = make_float2(0.0f, 0.0f);
             }
             if (lane < nq) {
                 const int j = list[lq + lane];
@@ -342,15 +348,14 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                 GR = fmaf(wv, gc, GR);
                 T = Ti;
                 const int row = nslots + k;
-                s_q[warp][row][lane ^ row] = qv;
-                s_w[warp][row][lane ^ row] = wv;
+                s_qw[warp][row][slot_col(row, lane)] = make_float2(qv, wv);
             }
             nslots += nrows;
         }
     }
     cp_async_wait<0>();  // no copy may outlive the CTA
-    if (nslots) flush_slots<ACCUM, AOS>(p, nslots, lane, wx0, wy0, s_q[warp], s_w[warp], s_g[warp],
-                                   s_rec[warp]);
+    if (nslots) flush_slots<ACCUM, AOS>(p, nslots, lane, wx0, wy0, s_qw[warp], s_g[warp],
+                                        s_rec[warp]);
 }
 
 constexpr int kBwdDynSmem = 2 * 8 * kSlots * kSlotPad * 4;
