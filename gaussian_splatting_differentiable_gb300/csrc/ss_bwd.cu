@@ -81,6 +81,14 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
+// A list entry's replay data, gathered per chunk next to the chunk's other
+// entries: the per-lane walk then reads 16 nearby records instead of 256.
+struct __align__(16) ChunkEnt {
+    SplatGeo g;   // mx, my, A, B
+    float4 c1;    // C, o, r, g
+    float4 c2;    // b
+};
+
 // Per-warp slot storage.
 struct __align__(16) SlotRec {
     float mx, my, A, B;   // staged geometry of the slot's splat
@@ -188,8 +196,9 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     __shared__ SplatGeo s_geo_[2][256];
     __shared__ SplatGeo2 s_geo2_[2][256];
     __shared__ SplatCol s_col_[2][256];
-    __shared__ uint8_t s_list[8][256];
-    __shared__ uint32_t s_lmask[8][256];
+    __shared__ uint8_t s_list[8][64];
+    __shared__ uint32_t s_lmask[8][64];
+    __shared__ ChunkEnt s_ck[8][kChunk];
     __shared__ uint32_t s_wmax[8];
     __shared__ float4 s_g[8][32];
     __shared__ SlotRec s_rec[8][kSlots];
@@ -275,82 +284,103 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
         const SplatGeo2 *s_geo2 = s_geo2_[buf];
         const SplatCol *s_col = s_col_[buf];
         if (uint32_t(lo) >= wmax) continue;
-        // The warp's entries of this batch that the forward blended somewhere
-        // in its 8x4 block, with their masks, in list order.
-        int cnt = 0;
+        // Positions [0, lim) of this batch may be blended in this warp's block.
+        // They are taken in segments of 64, top segment first; each segment's
+        // entries that the forward blended somewhere in the block are listed
+        // with their masks (the next segment's masks load meanwhile) and then
+        // processed back to front in chunks of kChunk.
+        const int lim = min(nb, int(wmax) - lo);
+        const uint32_t *gm = p.masks + size_t(warp) * size_t(p.n_pairs) + start + uint32_t(lo);
+        const int64_t gbase = int64_t(start) + lo;
+        int sg = (lim - 1) >> 6;
+        uint32_t ma = 0, mb = 0;
         {
-            const uint32_t *gm = p.masks + size_t(warp) * size_t(p.n_pairs) + start + uint32_t(lo);
-            uint32_t mv[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int j = q * 32 + lane;
-                mv[q] = (j < nb && uint32_t(lo + j) < wmax &&
-                         int64_t(start) + lo + j < p.n_pairs) ? gm[j] : 0u;
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint32_t b = __ballot_sync(0xffffffffu, mv[q] != 0u);
-                if (mv[q]) {
-                    const int at = cnt + __popc(b & lt);
-                    s_list[warp][at] = uint8_t(q * 32 + lane);
-                    s_lmask[warp][at] = mv[q];
-                }
-                cnt += __popc(b);
-            }
+            const int j0 = 64 * sg + lane, j1 = j0 + 32;
+            ma = (j0 < lim && gbase + j0 < p.n_pairs) ? gm[j0] : 0u;
+            mb = (j1 < lim && gbase + j1 < p.n_pairs) ? gm[j1] : 0u;
         }
-        __syncwarp();
-        const uint8_t *list = s_list[warp];
-        const uint32_t *lmask = s_lmask[warp];
-        // The list, back to front, in chunks of kChunk entries.
-        for (int hq = cnt; hq > 0; hq -= kChunk) {
-            const int lq = hq > kChunk ? hq - kChunk : 0;
-            const int nq = hq - lq;
-            // 1. This pixel's bit of each entry's mask.
-            uint32_t mine = 0;
+        for (; sg >= 0; --sg) {
+            const uint32_t ca = ma, cb = mb;
+            if (sg > 0) {
+                const int j0 = 64 * (sg - 1) + lane, j1 = j0 + 32;
+                ma = (j0 < lim && gbase + j0 < p.n_pairs) ? gm[j0] : 0u;
+                mb = (j1 < lim && gbase + j1 < p.n_pairs) ? gm[j1] : 0u;
+            }
+            int cnt = 0;
+            {
+                const uint32_t b0 = __ballot_sync(0xffffffffu, ca != 0u);
+                if (ca) {
+                    const int at = __popc(b0 & lt);
+                    s_list[warp][at] = uint8_t(64 * sg + lane);
+                    s_lmask[warp][at] = ca;
+                }
+                cnt = __popc(b0);
+                const uint32_t b1 = __ballot_sync(0xffffffffu, cb != 0u);
+                if (cb) {
+                    const int at = cnt + __popc(b1 & lt);
+                    s_list[warp][at] = uint8_t(64 * sg + 32 + lane);
+                    s_lmask[warp][at] = cb;
+                }
+                cnt += __popc(b1);
+            }
+            __syncwarp();
+            const uint8_t *list = s_list[warp];
+            const uint32_t *lmask = s_lmask[warp];
+            for (int hq = cnt; hq > 0; hq -= kChunk) {
+                const int lq = hq > kChunk ? hq - kChunk : 0;
+                const int nq = hq - lq;
+                // 1. This pixel's bit of each entry's mask.
+                uint32_t mine = 0;
 #pragma unroll
-            for (int k = 0; k < kChunk; ++k)
-                if (k < nq) mine |= ((lmask[lq + k] >> lane) & 1u) << k;
-            // 2. One slot row per entry: zero my column, record the splat.
-            const int nrows = nq;
-            if (nslots + nrows > kSlots) {
-                flush_slots<ACCUM, AOS>(p, nslots, lane, wx0, wy0, s_qw[warp], s_g[warp],
-                                        s_rec[warp]);
-                nslots = 0;
+                for (int k = 0; k < kChunk; ++k)
+                    if (k < nq) mine |= ((lmask[lq + k] >> lane) & 1u) << k;
+                // 2. One slot row per entry: zero my column; lane k copies
+                //    entry k's replay data next to the others' and records
+                //    the splat for the flush.
+                const int nrows = nq;
+                if (nslots + nrows > kSlots) {
+                    flush_slots<ACCUM, AOS>(p, nslots, lane, wx0, wy0, s_qw[warp], s_g[warp],
+                                            s_rec[warp]);
+                    nslots = 0;
+                }
+                for (int r = 0; r < nrows; ++r)
+                    s_qw[warp][nslots + r][lane] = make_float2(0.0f, 0.0f);
+                if (lane < nq) {
+                    const int j = list[lq + lane];
+                    const SplatGeo g = s_geo[j];
+                    const SplatGeo2 g2 = s_geo2[j];
+                    const SplatCol c = s_col[j];
+                    s_ck[warp][lane] = ChunkEnt{g, make_float4(g2.C, g2.o, c.r, c.g),
+                                                make_float4(c.b, 0.f, 0.f, 0.f)};
+                    s_rec[warp][nslots + lane] = SlotRec{g.mx, g.my, g.A, g.B, g2.C, g2.o, c.idx, 0u};
+                }
+                __syncwarp();
+                // 3. Each pixel walks only its own blended entries, back to front.
+                while (mine) {
+                    const int k = 31 - __clz(mine);
+                    mine &= ~(1u << k);
+                    const SplatGeo g = s_ck[warp][k].g;
+                    const float4 c1 = s_ck[warp][k].c1;   // C, o, r, g
+                    const float cb_ = s_ck[warp][k].c2.x; // b
+                    float dx, dy;
+                    const float e2 = eval_e2(g, c1.x, px, py, dx, dy);
+                    const float G = ex2_approx(e2);
+                    float oG;
+                    const float alpha = eval_alpha(c1.y, G, oG);
+                    const float inv = rcp_approx(__fsub_rn(1.0f, alpha));
+                    const float Ti = T * inv;  // T in front of this splat
+                    const float wv = alpha * Ti;
+                    const float gc = fmaf(g0, c1.z, fmaf(g1, c1.w, g2 * cb_));
+                    const float dLda = inv * fmaf(T, gc, -GR);
+                    const float qv = oG <= kAlphaMax ? -alpha * dLda : 0.0f;  // capped: constant
+                    GR = fmaf(wv, gc, GR);
+                    T = Ti;
+                    const int row = nslots + k;
+                    s_qw[warp][row][slot_col(row, lane)] = make_float2(qv, wv);
+                }
+                __syncwarp();
+                nslots += nrows;
             }
-            for (int r = 0; r < nrows; ++r) {
-                s_qw[warp][nslots + r][lane] = make_float2(0.0f, 0.0f);
-            }
-            if (lane < nq) {
-                const int j = list[lq + lane];
-                const SplatGeo g = s_geo[j];
-                s_rec[warp][nslots + lane] =
-                    SlotRec{g.mx, g.my, g.A, g.B, s_geo2[j].C, s_geo2[j].o, s_col[j].idx, 0u};
-            }
-            // 3. Each pixel walks only its own blended entries, back to front.
-            while (mine) {
-                const int k = 31 - __clz(mine);
-                mine &= ~(1u << k);
-                const int j = list[lq + k];
-                const SplatGeo g = s_geo[j];
-                const SplatGeo2 gg = s_geo2[j];
-                const SplatCol c = s_col[j];
-                float dx, dy;
-                const float e2 = eval_e2(g, gg.C, px, py, dx, dy);
-                const float G = ex2_approx(e2);
-                float oG;
-                const float alpha = eval_alpha(gg.o, G, oG);
-                const float inv = rcp_approx(__fsub_rn(1.0f, alpha));
-                const float Ti = T * inv;  // T in front of this splat
-                const float wv = alpha * Ti;
-                const float gc = fmaf(g0, c.r, fmaf(g1, c.g, g2 * c.b));
-                const float dLda = inv * fmaf(T, gc, -GR);
-                const float qv = oG <= kAlphaMax ? -alpha * dLda : 0.0f;  // capped: constant
-                GR = fmaf(wv, gc, GR);
-                T = Ti;
-                const int row = nslots + k;
-                s_qw[warp][row][slot_col(row, lane)] = make_float2(qv, wv);
-            }
-            nslots += nrows;
         }
     }
     cp_async_wait<0>();  // no copy may outlive the CTA
