@@ -5,11 +5,10 @@
 //
 // Same CTA/tile and warp/8x4-block layout as the forward.  Each pixel starts
 // from its forward state (T_final, last_contrib) and walks its tile's list
-// back to front in batches of 256 staged splats, recovering the
-// transmittance in front of each blended splat as T / (1 - alpha) and
-// keeping the colour S of what lies behind it; the blend decision is the
-// forward's own (same staging and exponent functions), so exactly the
-// forward's splats are revisited.
+// back to front in batches of 256 staged 64-byte splat records (cp.async,
+// double buffered), recovering the transmittance in front of each blended
+// splat as T / (1 - alpha) and keeping dL/dimage . (colour behind + T_final
+// bg) as one scalar.
 //
 // Reduction.  The pages' baseline issues 9 atomics per (pixel, splat); their
 // proposed fix sums each field across the warp first and issues one atomic
@@ -29,9 +28,17 @@
 //   dmean = ln2 (2A Qx + B Qy, B Qx + 2C Qy),  dconic = (Qxx/2, Qxy, Qyy/2),
 //   dopacity = -Q / o  (G dL/dalpha = -q / o when alpha is not capped),
 //   drgb = (Wr, Wg, Wb),  accumulated weight = W,
-// and issues the splat's 10 atomics (one per field per warp, as the pages
-// propose).  The accumulated weight is added in 32.32 fixed point with
+// and adds them, with four reductions per (warp, splat) (two
+// red.global.add.v4.f32, one f32, one u64), into a 48-byte per-splat record
+// that k_grad_final converts to the SoA outputs (the entry point for
+// callers that cannot allocate adds the ten fields directly to the outputs
+// instead).  The accumulated weight is added in 32.32 fixed point with
 // 64-bit integer atomics, so it is exact and independent of atomic order.
+//
+// The blend decisions are the forward's: its per-(pair, 8x4 block) masks
+// select the entries each warp handles and each pixel's bit, so nothing is
+// re-evaluated; after a chunk of 16 selected entries each pixel walks only
+// its own blended entries (independent trip counts per lane).
 #include "ss_device.cuh"
 #include "ss_internal.h"
 #include "ss_profile.h"

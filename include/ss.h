@@ -207,9 +207,12 @@ ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *v
  *   dL/dmean += dL/dsigma (-(a dx + b dy), -(b dx + c dy))
  *   dL/dconic += dL/dsigma (dx^2 / 2, dx dy, dy^2 / 2)
  * (through the 0.99 cap alpha has zero derivative).  The per-pixel terms of
- * a splat are summed across each warp with shuffles before one atomic add
- * per field per warp ("Phase 5 step 30b", conclusion: one atomic per warp
- * instead of per thread).
+ * a splat are summed over each 8x4 pixel block before any atomic
+ * ("Phase 5 step 30b", conclusion: reduce within the warp, then one atomic
+ * per warp instead of per thread); here the block's pixels store
+ * (dL/dsigma, alpha T) in shared memory and are summed into moments from
+ * which all fields follow, then added with four vector reductions per
+ * (block, splat) into a per-splat record in the workspace.
  *   records, n_splats: the records ss_bin_tiles wrote for these splats.
  *   T_final, last_contrib, blend_masks: from ss_raster_fwd with the same
  *   inputs (the blend decisions are the forward's, not re-evaluated).
@@ -218,7 +221,8 @@ ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *v
  *   accum_weight: with SS_ACCUM_WEIGHT, device float[n] overwritten with
  *   sum over pixels of alpha T (summed exactly in 32.32 fixed point, so the
  *   result does not depend on the order of the atomics); else may be NULL.
- *   workspace: >= ss_workspace_bytes(n, 0, W, H) bytes, 256-byte aligned.
+ *   workspace: >= ss_workspace_bytes(n, 0, W, H) bytes (48 per splat + 256),
+ *   256-byte aligned; required whenever n > 0.
  *   bg: HOST float[3] or NULL (must match the forward call). */
 ss_status ss_raster_bwd(const void *records, int32_t n_splats, const uint32_t *vals,
                         const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,
