@@ -1,8 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of the splat rasterization path on the 2M-splat, 1237x822 workload.
 
-One step = the whole path over one scene: tile binning, pair count (one
-host read), onesweep sort + tile ranges, forward, backward.  Prints one JSON
+One step = the whole path over one scene: tile binning, onesweep sort +
+tile ranges on the device-side pair count, forward, backward, replayed as
+one CUDA graph (per-kernel times come from a second timed pass of the same
+step launched without the graph).  Prints one JSON
 line (rank 0).  Under torchrun each rank runs an independent replica (the path
 does not shard across GPUs here); value = all ranks' candidate splat-pixel
 pairs / the slowest rank's time.
@@ -235,23 +237,28 @@ def run_ours(args, rank: int, world: int, dist):
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
+    r.step(sp, dL)                      # sizes the pair buffers (the one host read)
     for _ in range(args.warmup):
-        r.step(sp, dL)
+        r.step_async(sp, dL)
     torch.cuda.synchronize()
-    assert ss.ss_sort_status(r.workspace) == ss.SS_OK
+    r.check()
     offs = r.tile_offsets.cpu().numpy().view(np.uint32)
     cand = candidate_pairs(offs, scene.W, scene.H)
     active = int(r.last_contrib.sum().item())
     P = r.n_pairs
 
-    # --- device-resident timed region
+    # The step as one CUDA graph: bin -> sort on the device-side pair count ->
+    # forward -> backward, no host synchronisation inside.
+    graph = r.capture(sp, dL)
+    graph.replay()
+    r.check()
+
+    # --- device-resident timed region (headline): graph replays
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    ss.ss_profile_collect()
-    ss.ss_profile_enable(True)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -260,20 +267,38 @@ def run_ours(args, rank: int, world: int, dist):
     for k in range(args.steps):
         flush.fill_(float(k))           # > L2: every step starts cold
         ev[k][0].record(stream)
-        r.step(sp, dL)
+        graph.replay()
         ev[k][1].record(stream)
     torch.cuda.synchronize()
     wall1 = time.perf_counter()
     if dist:
         dist.barrier()
     clocks.mark(False)
+    r.check()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(step_ms)
+
+    # --- per-kernel timed region: the same step launched without the graph,
+    # every kernel bracketed by CUDA events on its stream (SS_PROFILE)
+    ss.ss_profile_collect()
+    ss.ss_profile_enable(True)
+    torch.cuda.synchronize()
+    synced_ms = []
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        r.step_async(sp, dL)
+        e1.record(stream)
+        synced_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    clocks.mark(False)
     ss.ss_profile_enable(False)
     prof = ss.ss_profile_collect()
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = statistics.mean(step_ms)
-    print("step ms: mean %.4f min %.4f max %.4f; kernels %s" % (
-        ms, min(step_ms), max(step_ms), prof), file=sys.stderr, flush=True)
+    nograph_ms = statistics.mean(a.elapsed_time(b) for a, b in synced_ms)
+    print("step ms (graph): mean %.4f min %.4f max %.4f; without graph %.4f; kernels %s" % (
+        ms, min(step_ms), max(step_ms), nograph_ms, prof), file=sys.stderr, flush=True)
     if not prof:
         raise RuntimeError("SS_PROFILE recorded no kernel launches")
     if dist:
@@ -281,7 +306,7 @@ def run_ours(args, rank: int, world: int, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     value = world * cand / (ms * 1e-3)
-    launches = sum(c for (c, _, _, _) in prof.values())
+    launches = sum(c for (c, _, _, _) in prof.values())   # per-kernel region; same per graph replay
 
     kernels = {k: {"launches": c, "ms_per_call": tot / c, "ms_total": tot, "min_ms": mn,
                    "max_ms": mx} for k, (c, tot, mn, mx) in prof.items()}
@@ -352,11 +377,13 @@ def run_ours(args, rank: int, world: int, dist):
         bo = sum(o.numel() * o.element_size() for o in host_out)
         n_e2e = max(3, min(args.steps, 20))
 
+        e2e_graph = r.capture(dev_in, dev_dL)
+
         def e2e_step():
             for k, v in host_in.items():
                 getattr(dev_in, k).copy_(v, non_blocking=True)
             dev_dL.copy_(host_dL, non_blocking=True)
-            r.step(dev_in, dev_dL)
+            e2e_graph.replay()
             for h, o in zip(host_out, outs):
                 h.copy_(o, non_blocking=True)
             torch.cuda.synchronize()
@@ -375,8 +402,9 @@ def run_ours(args, rank: int, world: int, dist):
             em = float(t.item())
         e2e = {"value": world * cand / (em * 1e-3), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "ms_per_step": em, "steps": n_e2e,
-               "how": "pinned host inputs -> device, bin/count/sort/fwd/bwd, gradients + image + "
+               "how": "pinned host inputs -> device, the step's CUDA graph, gradients + image + "
                       "weights -> pinned host, synchronize; wall clock"}
+        r.check()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -400,6 +428,7 @@ def run_ours(args, rank: int, world: int, dist):
                    "flags": {"accum_weight": scene.accum_weight, "median_depth": scene.median_depth},
                    "l2": "256 MB buffer written between timed steps (L2 is 129 MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "ms_per_step_without_graph": nograph_ms,
         "rasterize_bwd_ms_per_call": bwd_ms,
         "rasterize_bwd_pairs_per_s": cand / (bwd_ms * 1e-3),
         "stages_ms_per_step": stages,

@@ -134,6 +134,14 @@ def ss_sort_pairs(keys, vals, n_pairs: int, W: int, H: int, tile_offsets, worksp
                             _stream(stream)), "ss_sort_pairs")
 
 
+def ss_sort_pairs_dev(keys, vals, counters, capacity: int, W: int, H: int, tile_offsets,
+                      workspace, stream=None) -> None:
+    _check(_L.ss_sort_pairs_dev(_ptr(keys), _ptr(vals), _ptr(counters), capacity, W, H,
+                                _ptr(tile_offsets), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ss_sort_pairs_dev")
+
+
 def ss_sort_status(workspace, stream=None) -> int:
     return int(_L.ss_sort_status(_ptr(workspace), _stream(stream)))
 
@@ -279,3 +287,34 @@ class Rasterizer:
         self.forward(splats, stream)
         self.backward(splats, dL_dimage, stream)
         return n
+
+    def step_async(self, splats: Splats, dL_dimage: torch.Tensor, stream=None) -> None:
+        """bin -> sort -> forward -> backward with the pair count kept on the
+        device: no host synchronisation, so the step can be captured in a
+        CUDA graph.  The pair buffers must already be large enough (size them
+        with one step() first); check() reports an overflow afterwards."""
+        ss_bin_tiles(splats, self.W, self.H, self.keys, self.vals, self.capacity, self.counters,
+                     self.records, stream)
+        ss_sort_pairs_dev(self.keys, self.vals, self.counters, self.capacity, self.W, self.H,
+                          self.tile_offsets, self.workspace, stream)
+        ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.capacity, self.W,
+                      self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
+                      self.median_depth, self.blend_masks, stream)
+        ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.capacity, self.W,
+                      self.H, self.bg, self.flags, self.T_final, self.last_contrib,
+                      self.blend_masks, dL_dimage, self.grads, self.accum_weight, self.workspace,
+                      stream)
+
+    def check(self, stream=None) -> None:
+        """Raise if the last sort reported a device-side problem (capacity
+        overflow, look-back timeout, out-of-range key)."""
+        _check(ss_sort_status(self.workspace, stream), "sort status")
+
+    def capture(self, splats: Splats, dL_dimage: torch.Tensor) -> "torch.cuda.CUDAGraph":
+        """A CUDA graph of step_async on these buffers (replay with .replay())."""
+        self.step_async(splats, dL_dimage)        # first calls set kernel attributes
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step_async(splats, dL_dimage)
+        return g

@@ -42,6 +42,7 @@ PROTOTYPES = {
     "ss_record_bytes": (SZ, [I32]),
     "ss_pair_count": (ctypes.c_int, [P, I64, ctypes.POINTER(I64), ctypes.POINTER(I64), P]),
     "ss_sort_pairs": (ctypes.c_int, [P, P, I64, I32, I32, P, P, SZ, P]),
+    "ss_sort_pairs_dev": (ctypes.c_int, [P, P, P, I64, I32, I32, P, P, SZ, P]),
     "ss_sort_status": (ctypes.c_int, [P, P]),
     "ss_raster_fwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P, P]),
     "ss_raster_bwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P,

@@ -126,6 +126,10 @@ ss_status ss_sort_status(const void *workspace, ss_stream_t stream) {
     if (st != SS_OK) return st;
     if (word & kDevErrTimeout)
         return fail(SS_ERR_TIMEOUT, "ss_sort_pairs: a look-back wait gave up (status 0x%x)", word);
+    if (word & kDevErrCapacity)
+        return fail(SS_ERR_CAPACITY,
+                    "ss_sort_pairs_dev: more pairs than the capacity; the first capacity were "
+                    "sorted (status 0x%x)", word);
     if (word & kDevErrKeyRange)
         return fail(SS_ERR_DEVICE, "ss_sort_pairs: a key's tile id is >= the tile count (status 0x%x)",
                     word);

@@ -58,6 +58,6 @@ struct WsLayout {
 WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H);
 
 // Device status bits written by the sort kernels.
-enum : uint32_t { kDevErrTimeout = 1u, kDevErrKeyRange = 2u };
+enum : uint32_t { kDevErrTimeout = 1u, kDevErrKeyRange = 2u, kDevErrCapacity = 4u };
 
 }  // namespace ss

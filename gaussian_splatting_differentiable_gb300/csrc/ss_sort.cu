@@ -41,6 +41,13 @@ __device__ __forceinline__ void st_relaxed(uint64_t *p, uint64_t v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Number of pairs to sort: n_max, or the device count *dn clamped to n_max.
+__device__ __forceinline__ int64_t pair_count(const unsigned long long *dn, int64_t n_max) {
+    if (!dn) return n_max;
+    const unsigned long long c = *dn;
+    return c < (unsigned long long)n_max ? int64_t(c) : n_max;
+}
+
 // Exclusive scan of one value per thread over a 256-thread block.
 __device__ __forceinline__ uint32_t block_excl_scan256(uint32_t v, uint32_t *s_warp,
                                                        uint32_t *total) {
@@ -65,9 +72,11 @@ __device__ __forceinline__ uint32_t block_excl_scan256(uint32_t v, uint32_t *s_w
     return before + inc - v;
 }
 
-__global__ void __launch_bounds__(256) k_sort_hist(const uint64_t *__restrict__ keys, int64_t n,
-                                                   int ndig, uint32_t *__restrict__ hist) {
+__global__ void __launch_bounds__(256) k_sort_hist(const uint64_t *__restrict__ keys, int64_t n_max,
+                                                   const unsigned long long *dn, int ndig,
+                                                   uint32_t *__restrict__ hist) {
     __shared__ uint32_t s_h[8][256];
+    const int64_t n = pair_count(dn, n_max);
     for (int k = threadIdx.x; k < 8 * 256; k += 256) (&s_h[0][0])[k] = 0;
     __syncthreads();
     const int64_t stride = int64_t(gridDim.x) * 256;
@@ -100,6 +109,7 @@ struct PassParams {
     uint64_t *lookback;    // [nparts][256]
     uint32_t *ticket;
     uint32_t *err;
+    const unsigned long long *dn;  // device pair count (clamped to n), or null
 };
 
 __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
@@ -119,6 +129,11 @@ __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
     __syncthreads();
     const int64_t part = s_part;
     const int64_t base = part * kSortPart;
+    if (p.dn) {  // grid sized for the capacity: surplus partitions leave
+        const int64_t n = pair_count(p.dn, p.n);
+        if (base >= n) return;
+        p.n = n;
+    }
     const int64_t wbase = base + warp * (KPT * 32);
 
     uint64_t key[KPT];
@@ -220,9 +235,13 @@ __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
 //  - when src != dst the element is copied (run members by the run head).
 __global__ void __launch_bounds__(256) k_sort_final(const uint64_t *__restrict__ sk,
                                                     uint32_t *sv, uint64_t *dk, uint32_t *dv,
-                                                    int64_t n, int64_t tiles, uint32_t *offs,
-                                                    uint32_t *err) {
+                                                    int64_t n_max, const unsigned long long *dn,
+                                                    int64_t tiles, uint32_t *offs, uint32_t *err) {
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t n = pair_count(dn, n_max);
+    if (i == 0 && dn && *dn > (unsigned long long)n_max) atomicOr(err, kDevErrCapacity);
+    if (n == 0 && i == 0)
+        for (int64_t u = 0; u <= tiles; ++u) offs[u] = 0u;
     if (i >= n) return;
     const uint64_t key = sk[i];
     int64_t t = int64_t(key >> 32);
@@ -282,39 +301,35 @@ static ss_status ensure_pass_smem(int dyn) {
 
 __global__ void k_set_u32(uint32_t *p, uint32_t v) { *p = v; }
 
-}  // namespace ss
-
-using namespace ss;
-
-extern "C" ss_status ss_sort_pairs(uint64_t *keys, uint32_t *vals, int64_t n_pairs, int32_t W,
-                                   int32_t H, uint32_t *tile_offsets, void *workspace,
-                                   size_t workspace_bytes, ss_stream_t stream) {
-    clear_error();
+// Sort of n_max pairs, or of the device count *dn (clamped to n_max) when dn
+// is not null: grids are then sized for n_max and surplus CTAs leave.
+static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int64_t n_max,
+                           const unsigned long long *dn, int32_t W, int32_t H,
+                           uint32_t *tile_offsets, void *workspace, size_t workspace_bytes,
+                           cudaStream_t st) {
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
-        return fail(SS_ERR_UNSUPPORTED, "ss_sort_pairs: image %dx%d outside 1..%d", W, H, kMaxSide);
-    if (n_pairs < 0) return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: n_pairs < 0");
-    if (n_pairs > int64_t(0xffffffffu))
-        return fail(SS_ERR_UNSUPPORTED, "ss_sort_pairs: n_pairs %lld >= 2^32", (long long)n_pairs);
-    if (!tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: tile_offsets is NULL");
-    if (n_pairs > 0 && (!keys || !vals))
-        return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: keys/vals NULL");
+        return fail(SS_ERR_UNSUPPORTED, "%s: image %dx%d outside 1..%d", who, W, H, kMaxSide);
+    if (n_max < 0) return fail(SS_ERR_INVALID_ARG, "%s: pair count < 0", who);
+    if (n_max > int64_t(0xffffffffu))
+        return fail(SS_ERR_UNSUPPORTED, "%s: %lld pairs >= 2^32", who, (long long)n_max);
+    if (!tile_offsets) return fail(SS_ERR_INVALID_ARG, "%s: tile_offsets is NULL", who);
+    if (n_max > 0 && (!keys || !vals)) return fail(SS_ERR_INVALID_ARG, "%s: keys/vals NULL", who);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255))
-        return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: workspace NULL or not 256-byte aligned");
-    if (reinterpret_cast<uintptr_t>(keys) & 7)
-        return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: keys not 8-byte aligned");
-    const WsLayout L = ws_layout(0, n_pairs, W, H);
+        return fail(SS_ERR_INVALID_ARG, "%s: workspace NULL or not 256-byte aligned", who);
+    if ((reinterpret_cast<uintptr_t>(keys) & 7) || (reinterpret_cast<uintptr_t>(dn) & 7))
+        return fail(SS_ERR_INVALID_ARG, "%s: keys / counters not 8-byte aligned", who);
+    const WsLayout L = ws_layout(0, n_max, W, H);
     if (workspace_bytes < L.sort_end)
-        return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs: workspace %zu bytes < %zu needed",
+        return fail(SS_ERR_INVALID_ARG, "%s: workspace %zu bytes < %zu needed", who,
                     workspace_bytes, L.sort_end);
-    cudaStream_t st = (cudaStream_t)stream;
     const int64_t tiles = int64_t(tiles_x(W)) * tiles_y(H);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     uint32_t *err = reinterpret_cast<uint32_t *>(ws + L.status_word);
-    ss_status s = check_cuda(cudaMemsetAsync(ws, 0, L.zero_end, st), "ss_sort_pairs: memset");
+    ss_status s = check_cuda(cudaMemsetAsync(ws, 0, L.zero_end, st), "sort: memset");
     if (s != SS_OK) return s;
-    if (n_pairs == 0)
+    if (n_max == 0)
         return check_cuda(cudaMemsetAsync(tile_offsets, 0, size_t(tiles + 1) * 4, st),
-                          "ss_sort_pairs: memset offsets");
+                          "sort: memset offsets");
 
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
@@ -330,9 +345,9 @@ extern "C" ss_status ss_sort_pairs(uint64_t *keys, uint32_t *vals, int64_t n_pai
     uint64_t *ak = reinterpret_cast<uint64_t *>(ws + L.alt_keys);
     uint32_t *av = reinterpret_cast<uint32_t *>(ws + L.alt_vals);
 
-    const int64_t blocks = (n_pairs + 255) / 256;
+    const int64_t blocks = (n_max + 255) / 256;
     const int hgrid = int(blocks < int64_t(sms) * 4 ? blocks : int64_t(sms) * 4);
-    SS_LAUNCH("k_sort_hist", st, k_sort_hist<<<hgrid, 256, 0, st>>>(keys, n_pairs, L.ndig, hist));
+    SS_LAUNCH("k_sort_hist", st, k_sort_hist<<<hgrid, 256, 0, st>>>(keys, n_max, dn, L.ndig, hist));
     SS_LAUNCH("k_sort_scan", st, k_sort_scan<<<L.ndig, 256, 0, st>>>(hist, gofs));
     uint64_t *bk[2] = {keys, ak};
     uint32_t *bv[2] = {vals, av};
@@ -342,19 +357,43 @@ extern "C" ss_status ss_sort_pairs(uint64_t *keys, uint32_t *vals, int64_t n_pai
         p.vin = bv[d & 1];
         p.kout = bk[(d + 1) & 1];
         p.vout = bv[(d + 1) & 1];
-        p.n = n_pairs;
+        p.n = n_max;
         p.shift = 8 * d;
         p.gofs = gofs + 256 * d;
         p.lookback = lookback + size_t(d) * size_t(L.nparts) * 256;
         p.ticket = tickets + d;
         p.err = err;
+        p.dn = dn;
         SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<int(L.nparts), 256, dyn, st>>>(p));
     }
     const int r = L.ndig & 1;
     SS_LAUNCH("k_sort_final", st,
-              k_sort_final<<<int(blocks), 256, 0, st>>>(bk[r], bv[r], keys, vals, n_pairs, tiles,
+              k_sort_final<<<int(blocks), 256, 0, st>>>(bk[r], bv[r], keys, vals, n_max, dn, tiles,
                                                         tile_offsets, err));
-    return check_launch("ss_sort_pairs");
+    return check_launch(who);
+}
+
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" ss_status ss_sort_pairs(uint64_t *keys, uint32_t *vals, int64_t n_pairs, int32_t W,
+                                   int32_t H, uint32_t *tile_offsets, void *workspace,
+                                   size_t workspace_bytes, ss_stream_t stream) {
+    clear_error();
+    return sort_impl("ss_sort_pairs", keys, vals, n_pairs, nullptr, W, H, tile_offsets, workspace,
+                     workspace_bytes, (cudaStream_t)stream);
+}
+
+extern "C" ss_status ss_sort_pairs_dev(uint64_t *keys, uint32_t *vals, const uint64_t *d_counters,
+                                       int64_t capacity, int32_t W, int32_t H,
+                                       uint32_t *tile_offsets, void *workspace,
+                                       size_t workspace_bytes, ss_stream_t stream) {
+    clear_error();
+    if (!d_counters) return fail(SS_ERR_INVALID_ARG, "ss_sort_pairs_dev: d_counters is NULL");
+    return sort_impl("ss_sort_pairs_dev", keys, vals, capacity,
+                     reinterpret_cast<const unsigned long long *>(d_counters), W, H, tile_offsets,
+                     workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 // Test hook: one onesweep pass CTA that holds partition 1 of a 2-partition

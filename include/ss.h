@@ -163,8 +163,21 @@ ss_status ss_sort_pairs(uint64_t *keys, uint32_t *vals, int64_t n_pairs, int32_t
                         uint32_t *tile_offsets, void *workspace, size_t workspace_bytes,
                         ss_stream_t stream);
 
-/* Host: synchronizes `stream` and returns SS_OK, SS_ERR_TIMEOUT or
- * SS_ERR_DEVICE for the last ss_sort_pairs that used `workspace`. */
+/* ss_sort_pairs with the pair count read on the device: sorts
+ * min(d_counters[0], capacity) pairs, where d_counters are the counters
+ * ss_bin_tiles filled and capacity the size of keys / vals.  Nothing is read
+ * back to the host, so bin -> sort -> forward -> backward can be enqueued
+ * without a synchronisation (and captured in a CUDA graph); the grids are
+ * sized for `capacity` and the surplus CTAs exit at once.  If the count
+ * exceeded the capacity, ss_sort_status reports SS_ERR_CAPACITY (the first
+ * `capacity` pairs were sorted; re-bin with a larger buffer).  workspace:
+ * >= ss_workspace_bytes(0, capacity, W, H) bytes. */
+ss_status ss_sort_pairs_dev(uint64_t *keys, uint32_t *vals, const uint64_t *d_counters,
+                            int64_t capacity, int32_t W, int32_t H, uint32_t *tile_offsets,
+                            void *workspace, size_t workspace_bytes, ss_stream_t stream);
+
+/* Host: synchronizes `stream` and returns SS_OK, SS_ERR_TIMEOUT,
+ * SS_ERR_DEVICE or SS_ERR_CAPACITY for the last sort that used `workspace`. */
 ss_status ss_sort_status(const void *workspace, ss_stream_t stream);
 
 /* Forward rasterization ("Phase 5 step 30b", rasterize_f32): one CTA per
@@ -187,7 +200,10 @@ ss_status ss_sort_status(const void *workspace, ss_stream_t stream);
  *                Entries past the point where every pixel of a block stopped
  *                are left unwritten.
  *   records, n_splats: the records ss_bin_tiles wrote for these splats.
- *   vals, tile_offsets, n_pairs: the output of ss_sort_pairs for the same W, H.
+ *   vals, tile_offsets: the output of ss_sort_pairs for the same W, H.
+ *   n_pairs: the stride of blend_masks and a bound on the pairs sorted: the
+ *            pair count, or the capacity when the count stayed on the device
+ *            (ss_sort_pairs_dev).  The backward must get the same value.
  * Pair values >= n_splats are ignored. */
 ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *vals,
                         const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,

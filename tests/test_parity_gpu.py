@@ -163,3 +163,71 @@ def test_profile_counts_every_launch(P):
     assert prof["k_sort_pass"][0] == 2 * 5   # 8 tile bits + 32 depth bits -> 5 digits
     assert all(v[1] > 0 for v in prof.values())
     assert ss.ss_profile_collect() == {}
+
+
+def _snapshot(r):
+    import torch
+    torch.cuda.synchronize()
+    return {"offs": r.tile_offsets.cpu().numpy().copy(), "image": r.image.cpu().numpy().copy(),
+            "T": r.T_final.cpu().numpy().copy(), "last": r.last_contrib.cpu().numpy().copy(),
+            **{k: v.cpu().numpy().copy() for k, v in r.grads.items()},
+            "accum": r.accum_weight.cpu().numpy().copy()}
+
+
+def _same(a, b, P):
+    for k in ("offs", "image", "T", "last", "accum"):
+        assert np.array_equal(a[k], b[k]), k
+    for k in P.GRAD_FIELDS:
+        tol = max(1e-4, 1e-3 * np.abs(a[k]).max())
+        assert np.abs(a[k] - b[k]).max() <= tol, k
+
+
+def test_device_count_step_and_graph_replay_match_synced_step(P):
+    """bin -> sort on the device count -> fwd -> bwd without a host read, and a
+    CUDA graph of it, give what the synchronised path gives."""
+    import torch
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = synth.make_scene(3)
+    sp = ss.Splats.from_numpy(sc)
+    dL = torch.from_numpy(sc.dL_dimage).cuda()
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, 16, ss.SS_ACCUM_WEIGHT)
+    r.step(sp, dL)                      # grows the pair buffers
+    ref = _snapshot(r)
+    r.step_async(sp, dL)
+    r.check()
+    _same(ref, _snapshot(r), P)
+    g = r.capture(sp, dL)
+    for _ in range(2):
+        r.image.zero_()
+        g.replay()
+        r.check()
+        _same(ref, _snapshot(r), P)
+
+
+def test_device_count_sort_reports_capacity_overflow(P):
+    import torch
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = synth.make_scene(2)
+    sp = ss.Splats.from_numpy(sc)
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, 1000, 0)    # far fewer than the ~18k pairs
+    ss.ss_bin_tiles(sp, sc.W, sc.H, r.keys, r.vals, r.capacity, r.counters, r.records)
+    ss.ss_sort_pairs_dev(r.keys, r.vals, r.counters, r.capacity, sc.W, sc.H, r.tile_offsets,
+                         r.workspace)
+    assert ss.ss_sort_status(r.workspace) == ss.SS_ERR_CAPACITY
+    offs = r.tile_offsets.cpu().numpy().view(np.uint32)
+    assert offs[-1] == 1000 and np.all(np.diff(offs.astype(np.int64)) >= 0)
+
+
+def test_device_count_sort_of_no_pairs(P):
+    import torch
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = _scene(40, 30, 50, seed=12)
+    sc.depth[:] = -1.0                 # every splat culled: zero pairs
+    sp = ss.Splats.from_numpy(sc)
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, 64, 0)
+    r.tile_offsets.fill_(7)
+    ss.ss_bin_tiles(sp, sc.W, sc.H, r.keys, r.vals, r.capacity, r.counters, r.records)
+    ss.ss_sort_pairs_dev(r.keys, r.vals, r.counters, r.capacity, sc.W, sc.H, r.tile_offsets,
+                         r.workspace)
+    assert ss.ss_sort_status(r.workspace) == ss.SS_OK
+    assert np.all(r.tile_offsets.cpu().numpy() == 0)
