@@ -53,7 +53,8 @@ class _Frame(ctypes.Structure):
 
 
 class _FwdOut(ctypes.Structure):
-    _fields_ = [(k, ctypes.c_void_p) for k in ("image", "T_final", "last", "median", "n_amb")]
+    _fields_ = [(k, ctypes.c_void_p) for k in ("image", "T_final", "last", "median", "n_amb",
+                                               "max_w", "count", "splat_amb")]
 
 
 class _Alt(ctypes.Structure):
@@ -207,7 +208,9 @@ def forward(scene, vals, offs, tile_mask=None, params=None, bg=None, alt_capacit
     """Front-to-back compositing of every pixel of the (masked) tiles.
 
     Returns image [3][H][W], T_final, last, median, n_amb (knife-edge count per
-    pixel) and alts (structured array of alternative outcomes)."""
+    pixel), alts (structured array of alternative outcomes) and the per-splat
+    max_w (max blend weight), count (blended pixels) and splat_amb (blended at
+    a knife-edge pixel in some outcome)."""
     lib = load()
     keep = []
     s = _splats_d(scene, params, keep)
@@ -215,8 +218,10 @@ def forward(scene, vals, offs, tile_mask=None, params=None, bg=None, alt_capacit
     H, W = scene.H, scene.W
     res = {"image": np.zeros((3, H, W)), "T_final": np.ones((H, W)),
            "last": np.zeros((H, W), np.uint32), "median": np.zeros((H, W)),
-           "n_amb": np.zeros((H, W), np.uint8)}
-    out = _FwdOut(*[_p(res[k]) for k in ("image", "T_final", "last", "median", "n_amb")])
+           "n_amb": np.zeros((H, W), np.uint8), "max_w": np.zeros(scene.n),
+           "count": np.zeros(scene.n, np.uint32), "splat_amb": np.zeros(scene.n, np.uint8)}
+    out = _FwdOut(*[_p(res[k]) for k in ("image", "T_final", "last", "median", "n_amb",
+                                         "max_w", "count", "splat_amb")])
     alts = np.zeros(max(alt_capacity, 1), ALT_DTYPE)
     n_alt = lib.orc_forward(ctypes.byref(s), ctypes.byref(f), ctypes.byref(out), _p(alts),
                             alt_capacity)

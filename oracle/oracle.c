@@ -34,7 +34,10 @@
  *   R11 accumulated weight of a splat = sum over pixels of alpha T (the sum;
  *      an average is the caller's division);
  *   R12 median depth = depth of the last blended splat whose T before
- *      blending was > 0.5 (0 when none was blended).
+ *      blending was > 0.5 (0 when none was blended);
+ *   R13 per-splat weight statistics: the maximum over pixels of the blend
+ *      weight alpha T, and the number of pixels that blended the splat (the
+ *      "Avg" accumulated weight is R11's sum divided by that count).
  */
 #include "oracle.h"
 
@@ -372,6 +375,16 @@ int64_t orc_forward(const orc_splats_d *s, const orc_frame *f, orc_fwd_out *out,
                         out->median[p] = r.median;
                     if (out->n_amb)
                         out->n_amb[p] = (uint8_t)(r.n_amb > 255 ? 255 : r.n_amb);
+                    for (int64_t k = 0; k < r.n; ++k) {   /* R13 */
+                        const int64_t i = list[r.rec[k].pos];
+                        const double w = r.rec[k].alpha * r.rec[k].T;
+                        if (out->max_w && w > out->max_w[i])
+                            out->max_w[i] = w;
+                        if (out->count)
+                            out->count[i] += 1;
+                        if (out->splat_amb && r.n_amb)
+                            out->splat_amb[i] = 1;
+                    }
                     const int na = r.n_amb < MAX_AMB ? r.n_amb : MAX_AMB;
                     for (int j = 0; j < na; ++j) {
                         if (alts && n_alt < alt_capacity) {
@@ -386,6 +399,9 @@ int64_t orc_forward(const orc_splats_d *s, const orc_frame *f, orc_fwd_out *out,
                                 e->image[ch] = r2.C[ch] + r2.T * f->bg[ch];
                             e->T_final = r2.T;
                             e->median = r2.median;
+                            if (out->splat_amb)
+                                for (int64_t k = 0; k < r2.n; ++k)
+                                    out->splat_amb[list[r2.rec[k].pos]] = 1;
                         }
                         ++n_alt;
                     }

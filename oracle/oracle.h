@@ -58,6 +58,9 @@ typedef struct {               /* forward outputs; any pointer may be NULL */
     uint32_t *last;            /* [H][W] */
     double *median;            /* [H][W] */
     uint8_t *n_amb;            /* [H][W] ambiguous float32 decisions (knife edges) */
+    double *max_w;             /* [n] max over pixels of the blend weight alpha T (+=max) */
+    uint32_t *count;           /* [n] pixels that blended the splat (+=) */
+    uint8_t *splat_amb;        /* [n] 1 if blended at a knife-edge pixel in any outcome */
 } orc_fwd_out;
 
 /* One alternative outcome of a pixel: the result when one knife-edge

@@ -278,6 +278,32 @@ def test_tiled_equals_brute_force_over_all_splats(wl, n, W, H):
             assert np.array_equal(f[k], b[k]), k
 
 
+def test_weight_statistics_single_splat_closed_form():
+    """max blend weight = alpha at the pixel centre nearest the mean, count =
+    pixels with alpha >= 1/255 (one splat, T = 1 everywhere)."""
+    s, o = 2.0, 0.6
+    sc = scene_of(40, 40, [[19.3, 21.8]], [[1 / s**2, 0, 1 / s**2]], [o], [[1, 1, 1]], [2.0])
+    _, f = render(sc)
+    ys, xs = np.mgrid[0:40, 0:40]
+    a32 = float(np.float32(1 / s**2))
+    r2 = (xs + 0.5 - float(np.float32(19.3))) ** 2 + (ys + 0.5 - float(np.float32(21.8))) ** 2
+    al = float(np.float32(o)) * np.exp(-0.5 * r2 * a32)
+    assert f["max_w"][0] == pytest.approx(al.max(), rel=1e-14)
+    assert f["count"][0] == int((al >= ALPHA_MIN).sum())
+
+
+def test_weight_statistics_consistent_with_backward():
+    """count >= 1 and max_w > 0 exactly for splats with a positive accumulated
+    weight, and max_w <= accum <= count * max_w."""
+    sc = synth.make_scene(2, seed=5, n=1500, W=128, H=96)
+    tl, f = render(sc)
+    acc = oracle.backward(sc, tl["vals"], tl["offs"])["grads"]["accum"]
+    pos = acc > 0
+    assert np.array_equal(pos, f["count"] > 0) and np.array_equal(pos, f["max_w"] > 0)
+    assert np.all(f["max_w"][pos] <= acc[pos] * (1 + 1e-12))
+    assert np.all(acc[pos] <= f["count"][pos] * f["max_w"][pos] * (1 + 1e-12))
+
+
 # ---------------------------------------------------------------- knife edges
 
 def test_knife_edge_pixel_has_alternative():
@@ -396,6 +422,9 @@ MUTATIONS = [
     ("sort descending", "return a->key < b->key ? -1 : 1;", "return a->key < b->key ? 1 : -1;"),
     ("median uses first", "if (med)\n            r->median", "if (med && r->median == 0.0)\n            r->median"),
     ("k margin dropped", "k = k * K_REL + K_ABS;", "k = k * 0.9f;"),
+    ("max weight over alpha", "const double w = r.rec[k].alpha * r.rec[k].T;",
+     "const double w = r.rec[k].alpha;"),
+    ("count of evaluated splats", "out->count[i] += 1;", "out->count[i] += 2;"),
 ]
 
 
