@@ -17,7 +17,7 @@ import torch
 
 from . import _lib
 from ._lib import (SS_ACCUM_WEIGHT, SS_ERR_CAPACITY, SS_MEDIAN_DEPTH, SS_OK,  # noqa: F401
-                   STATUS_NAMES, SsGrads, SsSplats)
+                   SS_WEIGHT_STATS, STATUS_NAMES, SsGrads, SsSplats)
 
 _L = _lib.load()
 TILE = 16
@@ -148,11 +148,12 @@ def ss_sort_status(workspace, stream=None) -> int:
 
 def ss_raster_fwd(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int, H: int, bg,
                   flags: int, image, T_final, last_contrib, median_depth, blend_masks,
-                  stream=None) -> None:
+                  max_weight=None, blend_count=None, stream=None) -> None:
     _check(_L.ss_raster_fwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), n_pairs, W,
                             H, _f32_host3(bg), flags, _ptr(image), _ptr(T_final),
                             _ptr(last_contrib), _ptr(median_depth), _ptr(blend_masks),
-                            _stream(stream)), "ss_raster_fwd")
+                            _ptr(max_weight), _ptr(blend_count), _stream(stream)),
+           "ss_raster_fwd")
 
 
 def ss_raster_bwd(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int, H: int, bg,
@@ -238,6 +239,9 @@ class Rasterizer:
                       "drgb": torch.empty(n_splats, 3, dtype=torch.float32, device=d)}
         self.accum_weight = (torch.empty(n_splats, dtype=torch.float32, device=d)
                              if flags & SS_ACCUM_WEIGHT else None)
+        stats = flags & SS_WEIGHT_STATS
+        self.max_weight = torch.empty(n_splats, dtype=torch.float32, device=d) if stats else None
+        self.blend_count = torch.empty(n_splats, dtype=torch.int32, device=d) if stats else None
         self.n_pairs = 0
         self.culled = 0
 
@@ -272,7 +276,8 @@ class Rasterizer:
         """Composite; uses the records written by the last bin_and_sort."""
         ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs, self.W,
                       self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
-                      self.median_depth, self.blend_masks, stream)
+                      self.median_depth, self.blend_masks, self.max_weight, self.blend_count,
+                      stream)
 
     def backward(self, splats, dL_dimage: torch.Tensor, stream=None) -> None:
         """Gradients; uses the records written by the last bin_and_sort."""
@@ -299,7 +304,8 @@ class Rasterizer:
                           self.tile_offsets, self.workspace, stream)
         ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.capacity, self.W,
                       self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
-                      self.median_depth, self.blend_masks, stream)
+                      self.median_depth, self.blend_masks, self.max_weight, self.blend_count,
+                      stream)
         ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.capacity, self.W,
                       self.H, self.bg, self.flags, self.T_final, self.last_contrib,
                       self.blend_masks, dL_dimage, self.grads, self.accum_weight, self.workspace,

@@ -17,6 +17,7 @@ STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_ARG", 2: "SS_ERR_CAPACITY", 3: "S
                 4: "SS_ERR_TIMEOUT", 5: "SS_ERR_UNSUPPORTED", 6: "SS_ERR_DEVICE"}
 SS_ACCUM_WEIGHT = 1
 SS_MEDIAN_DEPTH = 2
+SS_WEIGHT_STATS = 4
 
 
 class SsSplats(ctypes.Structure):
@@ -44,7 +45,8 @@ PROTOTYPES = {
     "ss_sort_pairs": (ctypes.c_int, [P, P, I64, I32, I32, P, P, SZ, P]),
     "ss_sort_pairs_dev": (ctypes.c_int, [P, P, P, I64, I32, I32, P, P, SZ, P]),
     "ss_sort_status": (ctypes.c_int, [P, P]),
-    "ss_raster_fwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P, P]),
+    "ss_raster_fwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P, P, P,
+                                     P]),
     "ss_raster_bwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P,
                                      ctypes.POINTER(SsGrads), P, P, SZ, P]),
     "ss_raster_bwd_noalloc": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P,

@@ -482,7 +482,7 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     clear_error();
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd: image %dx%d outside 1..%d", W, H, kMaxSide);
-    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH))
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: unknown flag bits 0x%x", flags);
     const int32_t n = n_splats;
     if (n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: n < 0");
@@ -588,7 +588,7 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd_noalloc: image %dx%d outside 1..%d", W, H,
                     kMaxSide);
-    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH))
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: unknown flag bits 0x%x", flags);
     const int32_t n = n_splats;
     if (n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: n < 0");

@@ -12,6 +12,12 @@
 // T below 1e-4; the CTA stops once all its pixels have.  The median-depth
 // output is a template variant, so the default variant does no median work.
 //
+// With SS_WEIGHT_STATS (the STATS variant) the warp also takes, per splat
+// that any of its pixels blended, the maximum blend weight alpha T (a warp
+// max of the float bits, which order like the values for w >= 0) and the
+// number of blending pixels (the mask's popcount), and adds them to the
+// splat's statistics with one atomicMax and one atomicAdd.
+//
 // The warp also records, for each pair it reached, which of its 32 pixels
 // blended the splat (a ballot): blend_masks[b * n_pairs + p], b = warp.
 // The backward reads these decisions instead of re-evaluating every
@@ -36,9 +42,11 @@ struct FwdParams {
     float *T_final;
     uint32_t *last;
     float *median;
+    uint32_t *max_w_bits;  // [n] float bits of the max blend weight (STATS)
+    uint32_t *count;       // [n] blending pixels (STATS)
 };
 
-template <bool MEDIAN>
+template <bool MEDIAN, bool STATS>
 __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
     __shared__ SplatGeo s_geo[2][256];
     __shared__ SplatGeo2 s_geo2[2][256];
@@ -110,6 +118,7 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
             float dx, dy;
             const float e2 = eval_e2(g, g2.C, px, py, dx, dy);
             bool blend = false;
+            float wblend = 0.0f;
             if (!done && e2 >= g2.thr) {  // else skipped (alpha < 1/255); NaN-safe
                 float oG;
                 const float alpha = eval_alpha(g2.o, ex2_approx(e2), oG);
@@ -120,6 +129,7 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
                     blend = true;
                     const SplatCol c = s_col[buf][j];
                     const float w = alpha * T;
+                    wblend = w;
                     cr = fmaf(c.r, w, cr);
                     cg = fmaf(c.g, w, cg);
                     cb = fmaf(c.b, w, cb);
@@ -130,6 +140,14 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
             }
             const uint32_t m = __ballot_sync(0xffffffffu, blend);
             if (lane == 0) s_mask[warp][j] = m;
+            if (STATS && m) {
+                const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(wblend));
+                if (lane == 0) {
+                    const uint32_t idx = s_col[buf][j].idx;
+                    atomicMax(p.max_w_bits + idx, wmax);
+                    atomicAdd(p.count + idx, uint32_t(__popc(m)));
+                }
+            }
             if (__all_sync(0xffffffffu, done)) break;
         }
         __syncwarp();
@@ -157,12 +175,17 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
                                    const uint32_t *tile_offsets, int64_t n_pairs, int32_t W,
                                    int32_t H, const float *bg, uint32_t flags, float *image,
                                    float *T_final, uint32_t *last_contrib, float *median_depth,
-                                   uint32_t *blend_masks, ss_stream_t stream) {
+                                   uint32_t *blend_masks, float *max_weight,
+                                   uint32_t *blend_count, ss_stream_t stream) {
     clear_error();
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_fwd: image %dx%d outside 1..%d", W, H, kMaxSide);
-    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH))
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: unknown flag bits 0x%x", flags);
+    const bool stats = flags & SS_WEIGHT_STATS;
+    if (stats && n_splats > 0 && (!max_weight || !blend_count))
+        return fail(SS_ERR_INVALID_ARG,
+                    "ss_raster_fwd: SS_WEIGHT_STATS set but max_weight / blend_count NULL");
     if (n_splats < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: n_splats < 0");
     if (n_splats > 0 && !records) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: records is NULL");
     if (reinterpret_cast<uintptr_t>(records) & 15)
@@ -192,11 +215,25 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
     p.median = median_depth;
     p.masks = blend_masks;
     p.n_pairs = n_pairs;
+    p.max_w_bits = reinterpret_cast<uint32_t *>(max_weight);
+    p.count = blend_count;
     const int grid = tiles_x(W) * tiles_y(H);
     cudaStream_t st = (cudaStream_t)stream;
-    if (median)
-        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<true><<<grid, 256, 0, st>>>(p));
+    if (stats && n_splats > 0) {
+        ss_status s = check_cuda(cudaMemsetAsync(max_weight, 0, size_t(n_splats) * 4, st),
+                                 "ss_raster_fwd: memset");
+        if (s == SS_OK)
+            s = check_cuda(cudaMemsetAsync(blend_count, 0, size_t(n_splats) * 4, st),
+                           "ss_raster_fwd: memset");
+        if (s != SS_OK) return s;
+    }
+    if (median && stats)
+        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<true, true><<<grid, 256, 0, st>>>(p));
+    else if (median)
+        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<true, false><<<grid, 256, 0, st>>>(p));
+    else if (stats)
+        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<false, true><<<grid, 256, 0, st>>>(p));
     else
-        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<false><<<grid, 256, 0, st>>>(p));
+        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<false, false><<<grid, 256, 0, st>>>(p));
     return check_launch("ss_raster_fwd");
 }

@@ -67,7 +67,10 @@ typedef enum {
  * optional per-pixel arrays sized by a compile-time constant). */
 enum {
     SS_ACCUM_WEIGHT = 1u,  /* bwd: per-splat accumulated blend weight sum_p alpha T */
-    SS_MEDIAN_DEPTH = 2u   /* fwd: per-pixel depth of the last splat blended while T > 0.5 */
+    SS_MEDIAN_DEPTH = 2u,  /* fwd: per-pixel depth of the last splat blended while T > 0.5 */
+    SS_WEIGHT_STATS = 4u   /* fwd: per-splat max blend weight and blending-pixel count
+                              ("max wt" and, with the accumulated weight, the "Avg"
+                              weight of the Spirula Studio write-up, 机制拆解 / 亲手验证) */
 };
 
 /* Splats, structure of arrays, float32, device memory.  The pages' inputs:
@@ -191,6 +194,10 @@ ss_status ss_sort_status(const void *workspace, ss_stream_t stream);
  *   median_depth[H][W]  only with SS_MEDIAN_DEPTH (else may be NULL): depth
  *                       of the last splat blended while T > 0.5, 0 if none
  *   bg: HOST float[3] background, or NULL for black.
+ *   max_weight, blend_count: only with SS_WEIGHT_STATS (else may be NULL):
+ *                device float[n] / uint32[n], overwritten with, per splat, the
+ *                maximum over pixels of alpha T and the number of pixels that
+ *                blended it (average weight = accumulated weight / count).
  *   blend_masks: device uint32[8][n_pairs]; for each pair p the forward
  *                reached and each 8x4 pixel block b of p's tile
  *                (b = 2 (row / 4) + (column / 8) within the tile),
@@ -209,7 +216,7 @@ ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *v
                         const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,
                         const float *bg, uint32_t flags, float *image, float *T_final,
                         uint32_t *last_contrib, float *median_depth, uint32_t *blend_masks,
-                        ss_stream_t stream);
+                        float *max_weight, uint32_t *blend_count, ss_stream_t stream);
 
 /* Backward rasterization ("从 8.6 KB 到 4.2 KB ...", rasterize_bwd_2d on the
  * 2D screen-space path; "Phase 5 step 30b", rasterize_backwards: the 9-field

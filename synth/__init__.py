@@ -89,20 +89,22 @@ class Workload:
     blobs: int = 0        # number of Gaussian position blobs
     blob_frac: float = 0.0
     blob_sigma: float = 0.0
+    weight_stats: bool = False   # per-splat max blend weight and blend count
 
 
 # The five workloads; index 1..5.
 WORKLOADS = {
     1: Workload("tiny-64x64-256", 64, 64, 256, (0.5, 4.0), (0.05, 0.99), (1.0, 10.0), 1.0,
-                True, False),
+                True, False, weight_stats=True),
     2: Workload("256x256-5207", 256, 256, 5207, (0.5, 6.0), (0.05, 0.99), (1.0, 10.0), 0.1,
                 True, False),
     3: Workload("1237x822-76363", 1237, 822, 76363, (0.3, 8.0), (0.05, 0.99), (1.0, 50.0), 0.1,
-                True, False),
+                True, False, weight_stats=True),
     4: Workload("1237x822-2M", 1237, 822, 2_000_000, (0.3, 3.0), (0.02, 0.9), (1.0, 100.0), 0.1,
                 True, False),
     5: Workload("1920x1080-2M-blobs", 1920, 1080, 2_000_000, (0.3, 4.0), (0.02, 0.9),
-                (1.0, 100.0), 0.1, True, True, blobs=4, blob_frac=0.3, blob_sigma=60.0),
+                (1.0, 100.0), 0.1, True, True, blobs=4, blob_frac=0.3, blob_sigma=60.0,
+                weight_stats=True),
 }
 
 
@@ -120,6 +122,7 @@ class Scene:
     accum_weight: bool
     median_depth: bool
     name: str = ""
+    weight_stats: bool = False
 
     @property
     def n(self) -> int:
@@ -171,7 +174,7 @@ def make_scene(workload: int | Workload, seed: int = 0, n: int | None = None,
                  mean2d=f32(np.stack([mx, my], axis=1)), conic=f32(conic), opacity=f32(opacity),
                  rgb=f32(rgb), depth=f32(depth), dL_dimage=f32(dL),
                  bg=np.zeros(3, np.float32), accum_weight=wl.accum_weight,
-                 median_depth=wl.median_depth, name=wl.name)
+                 median_depth=wl.median_depth, name=wl.name, weight_stats=wl.weight_stats)
 
 
 def subset(scene: Scene, idx: np.ndarray) -> Scene:

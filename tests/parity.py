@@ -3,6 +3,8 @@
 Tolerances (the rasterizer's stated bar):
   * pairs (as a multiset), sorted keys/values, tile offsets: bit-exact;
   * image, T_final: 1e-5 absolute; last_contrib and median depth: exact;
+  * per-splat max blend weight: 1e-5 absolute; blending-pixel count: exact
+    (splats blended at a knife-edge pixel in some outcome are skipped);
   * gradients: max(1e-4, 1e-3 * max|field|) per element, field = one of
     dmean2d, dconic, dopacity, drgb;
   * accumulated weight: max(1e-5, e) + 2^-23 |w|, e = the oracle's bound on the
@@ -26,7 +28,8 @@ GRAD_FIELDS = ("dmean2d", "dconic", "dopacity", "drgb")
 
 def flags_of(scene) -> int:
     return (ss.SS_ACCUM_WEIGHT if scene.accum_weight else 0) | \
-        (ss.SS_MEDIAN_DEPTH if scene.median_depth else 0)
+        (ss.SS_MEDIAN_DEPTH if scene.median_depth else 0) | \
+        (ss.SS_WEIGHT_STATS if getattr(scene, "weight_stats", False) else 0)
 
 
 def run_gpu(scene, capacity=None, stream=None):
@@ -64,6 +67,9 @@ def run_gpu(scene, capacity=None, stream=None):
     for k in GRAD_FIELDS:
         out[k] = r.grads[k].cpu().numpy()
     out["accum"] = r.accum_weight.cpu().numpy() if r.accum_weight is not None else None
+    out["max_w"] = r.max_weight.cpu().numpy() if r.max_weight is not None else None
+    out["bcount"] = (r.blend_count.cpu().numpy().view(np.uint32)
+                     if r.blend_count is not None else None)
     return out
 
 
@@ -119,6 +125,25 @@ def check_forward(scene, gpu, ofw, pixel_mask=None, atol=1e-5):
             "max_img_err": float(img_err[clean].max()) if clean.any() else 0.0}
 
 
+def check_weight_stats(scene, gpu, ofw, splat_mask=None, atol=1e-5):
+    """Per-splat max blend weight and blending-pixel count; ofw must cover
+    every tile of the selected splats."""
+    if gpu["max_w"] is None:
+        return None
+    sel = np.ones(scene.n, bool) if splat_mask is None else splat_mask
+    clean = sel & (ofw["splat_amb"] == 0)
+    err = np.abs(gpu["max_w"].astype(np.float64) - ofw["max_w"])
+    bad = clean & (err > atol)
+    assert not bad.any(), "max weight: %d splats off; worst %.3g" % (bad.sum(), err[bad].max())
+    badc = clean & (gpu["bcount"] != ofw["count"])
+    assert not badc.any(), "blend count: %d splats off; first %d gpu %d oracle %d" % (
+        badc.sum(), np.argmax(badc), gpu["bcount"][np.argmax(badc)],
+        ofw["count"][np.argmax(badc)])
+    return {"splats": int(clean.sum()), "knife_edge_splats": int((sel & ~clean).sum()),
+            "max_w_err": float(err[clean].max(initial=0.0)),
+            "blended": int((clean & (ofw["count"] > 0)).sum())}
+
+
 def _describe_bad(bad, gpu, ofw, img_err, T_err):
     ys, xs = np.nonzero(bad)
     y, x = ys[0], xs[0]
@@ -161,9 +186,10 @@ def full_parity(scene, capacity=None):
     tl = check_pairs(scene, gpu)
     ofw = oracle.forward(scene, tl["vals"], tl["offs"], alt_capacity=1 << 20)
     f = check_forward(scene, gpu, ofw)
+    s = check_weight_stats(scene, gpu, ofw)
     obw = oracle.backward(scene, tl["vals"], tl["offs"])
     b = check_backward(scene, gpu, obw)
-    return {"fwd": f, "bwd": b, "pairs": tl["count"]}
+    return {"fwd": f, "stats": s, "bwd": b, "pairs": tl["count"]}
 
 
 def sampled_parity(scene, n_tiles=192, n_splats=256, seed=0):
@@ -189,4 +215,10 @@ def sampled_parity(scene, n_tiles=192, n_splats=256, seed=0):
     tmask[(keys[smask[vals]] >> np.uint64(32)).astype(np.int64)] = 1
     obw = oracle.backward(scene, tl["vals"], tl["offs"], tile_mask=tmask)
     b = check_backward(scene, gpu, obw, splat_mask=smask)
-    return {"fwd": f, "bwd": b, "pairs": tl["count"], "bwd_tiles": int(tmask.sum())}
+    s = None
+    if gpu["max_w"] is not None:
+        ofw2 = oracle.forward(scene, tl["vals"], tl["offs"], tile_mask=tmask,
+                              alt_capacity=1 << 20)
+        s = check_weight_stats(scene, gpu, ofw2, splat_mask=smask)
+    return {"fwd": f, "stats": s, "bwd": b, "pairs": tl["count"],
+            "bwd_tiles": int(tmask.sum())}

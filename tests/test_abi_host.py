@@ -55,7 +55,7 @@ def test_constants_match_oracle(lib):
     assert buf[1] == np.float32(c["alpha_max"])
     assert buf[2] == np.float32(c["T_eps"])
     assert buf[3] == c["tile"]
-    assert lib.ss_abi_version() == 2
+    assert lib.ss_abi_version() == 3
 
 
 def test_workspace_bytes(lib):
@@ -94,15 +94,17 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert "workspace" in lib.ss_last_error().decode()
     # forward: unknown flags, NULL outputs, median flag without buffer
     assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 8, 0x1000, 0x1000,
-                             0x1000, None, 0x1000, None) == 1
+                             0x1000, None, 0x1000, None, None, None) == 1
     assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 0, None, 0x1000,
-                             0x1000, None, 0x1000, None) == 1
+                             0x1000, None, 0x1000, None, None, None) == 1
     assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 2, 0x1000, 0x1000,
-                             0x1000, None, 0x1000, None) == 1
+                             0x1000, None, 0x1000, None, None, None) == 1
     assert lib.ss_raster_fwd(None, 5, 0x1000, 0x1000, 0, 16, 16, None, 0, 0x1000, 0x1000,
-                             0x1000, None, 0x1000, None) == 1
+                             0x1000, None, 0x1000, None, None, None) == 1
     assert lib.ss_raster_fwd(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 0, 0x1000, 0x1000,
-                             0x1000, None, None, None) == 1   # blend_masks NULL
+                             0x1000, None, None, None, None, None) == 1   # blend_masks NULL
+    assert lib.ss_raster_fwd(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 4, 0x1000, 0x1000,
+                             0x1000, None, 0x1000, None, None, None) == 1   # stats outputs NULL
     # backward: NULL gradient array, accum flag without buffer or workspace
     g = SsGrads(0x1000, None, 0x1000, 0x1000)
     assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 0, 0x1000, 0x1000,

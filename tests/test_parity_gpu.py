@@ -111,12 +111,27 @@ def test_alpha_cap_and_background(P):
     P.full_parity(sc)
 
 
-@pytest.mark.parametrize("accum,median", [(False, False), (True, False), (False, True),
-                                          (True, True)])
-def test_flag_variants(P, accum, median):
+@pytest.mark.parametrize("accum,median,stats", [(False, False, False), (True, False, False),
+                                                (False, True, False), (True, True, False),
+                                                (False, False, True), (True, False, True),
+                                                (False, True, True), (True, True, True)])
+def test_flag_variants(P, accum, median, stats):
     sc = _scene(96, 80, 500, seed=9, wl=2)
-    sc.accum_weight, sc.median_depth = accum, median
-    P.full_parity(sc)
+    sc.accum_weight, sc.median_depth, sc.weight_stats = accum, median, stats
+    r = P.full_parity(sc)
+    assert (r["stats"] is not None) == stats
+    if stats:
+        assert r["stats"]["blended"] > 100
+
+
+def test_weight_stats_with_dense_overlap(P):
+    """Many splats over one tile: the per-warp reductions see up to 32
+    blending lanes and the atomics many warps per splat."""
+    sc = _scene(16, 16, 3000, seed=7)
+    sc.opacity[:] = np.float32(0.02)
+    sc.weight_stats = True
+    r = P.full_parity(sc)
+    assert r["stats"]["blended"] > 1000
 
 
 def test_capacity_overflow_reports_and_recovers(P):
