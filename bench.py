@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--workload", type=int, default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the projection / SSIM legs")
     return ap.parse_args()
 
 
@@ -213,6 +214,52 @@ def measured_peaks():
         return {}
 
 
+def measure_projection(ss, dev, flush, steps: int, hbm: float, hbm_src: str) -> dict:
+    """The projection forward and backward on the 2M-splat, degree-3 scene at
+    1237x822, each call timed alone with CUDA events after an L2 flush."""
+    import torch
+    from synth.scene3d import make_scene3d
+    sc = make_scene3d(13)
+    sp = ss.Splats3D.from_numpy(sc, dev)
+    cam = ss.camera(sc.cam.R, sc.cam.t, sc.cam.fx, sc.cam.fy, sc.cam.cx, sc.cam.cy, sc.cam.near,
+                    sc.cam.blur)
+    pr = ss.Projector(sc.n, sc.sh_degree, dev)
+    f = lambda a: torch.from_numpy(a).to(dev).contiguous()  # noqa: E731
+    gm, gc, gr = f(sc.dmean2d), f(sc.dconic), f(sc.drgb)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        pr.forward(sp, cam)
+        pr.backward(sp, cam, gm, gc, gr)
+    torch.cuda.synchronize()
+    times = {"fwd": [], "bwd": []}
+    for k in range(steps):
+        for name, call in (("fwd", lambda: pr.forward(sp, cam)),
+                           ("bwd", lambda: pr.backward(sp, cam, gm, gc, gr))):
+            flush.fill_(float(k))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            times[name].append((e0, e1))
+    torch.cuda.synchronize()
+    K = (sc.sh_degree + 1) ** 2
+    bytes_ = {"fwd": sc.n * (40 + 12 * K + 36), "bwd": sc.n * (40 + 12 * K + 32 + 40 + 12 * K)}
+    out = {"workload": sc.name, "splats": sc.n, "sh_degree": sc.sh_degree,
+           "culled": int((pr.depth == 0).sum().item())}
+    for name in ("fwd", "bwd"):
+        ms = statistics.mean(a.elapsed_time(b) for a, b in times[name])
+        ach = bytes_[name] / (ms * 1e-3) / 1e9
+        out[name] = {"kernel": "k_project_" + name, "ms_per_call": ms,
+                     "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                                  "frac": ach / hbm, "algorithmic_bytes": bytes_[name],
+                                  "peak_source": hbm_src}}
+    out["fwd"]["roofline"]["bytes_model"] = "per splat: mean3 12 + scale 12 + quat 16 + SH 12K " \
+        "in, mean2d 8 + conic 12 + depth 4 + rgb 12 out (K = 16)"
+    out["bwd"]["roofline"]["bytes_model"] = "per splat: mean3, scale, quat 40 + SH 12K + " \
+        "upstream 32 in, 40 + 12K gradients out (K = 16)"
+    return out
+
+
 def run_ours(args, rank: int, world: int, dist):
     import torch
     try:
@@ -362,6 +409,12 @@ def run_ours(args, rank: int, world: int, dist):
                        "peak_source": "measured here: red.global.add.f32, 64M distinct addresses"}
     hbm_atomic_frac = max(t_hbm, t_atom) / (bwd_ms * 1e-3)
 
+    # --- the next rows of the path, each timed on its own workload
+    next_rows = {}
+    if not args.no_next:
+        next_rows["f1_projection"] = measure_projection(ss, dev, flush, args.steps, hbm,
+                                                        hbm_src + " (MEASURED_PEAKS.json hbm_gbs)")
+
     # --- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -437,6 +490,7 @@ def run_ours(args, rank: int, world: int, dist):
         "bwd_hbm_atomic_roofline_frac": hbm_atomic_frac,
         "l2_red_f32_per_s": red_rate,
         "gpu_launches": launches,
+        "next_rows": next_rows,
         "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
         "wall_ms_per_step": (wall1 - wall0) * 1e3 / args.steps,
     }

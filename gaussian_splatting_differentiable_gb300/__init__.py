@@ -1,7 +1,7 @@
 """Tile-based differentiable rasterization of projected 2D Gaussian splats on GB300.
 
 The compute path is libss.so (hand-written CUDA for sm_103a behind the C ABI
-of include/ss.h).  This module is its thin Python binding: each ss_* function
+of include/ss.h and include/ss_project.h).  This module is its thin Python binding: each ss_* function
 here has the C function's name and arguments and only marshals torch tensors
 (device memory) and streams into pointers.  PyTorch provides memory and
 streams; every step of the path runs in the library's kernels.  There is no
@@ -206,6 +206,87 @@ def ss_probe_red_f32(buf, rounds: int, stream=None) -> None:
 def ss_test_sort_wait_timeout(workspace, stream=None) -> None:
     _check(_L.ss_test_sort_wait_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)), "ss_test_sort_wait_timeout")
+
+
+# ------------------------------------------------------------------ projection (ss_project.h)
+
+@dataclasses.dataclass
+class Splats3D:
+    """Device 3D splats (float32, contiguous): mean3 [n,3], scale [n,3],
+    quat [n,4] (w, x, y, z), sh [K,3,n] coefficient-major, K = (degree+1)^2."""
+    mean3: torch.Tensor
+    scale: torch.Tensor
+    quat: torch.Tensor
+    sh: torch.Tensor
+    sh_degree: int
+
+    @property
+    def n(self) -> int:
+        return int(self.mean3.shape[0])
+
+    def c(self) -> _lib.SsSplats3d:
+        for k in ("mean3", "scale", "quat", "sh"):
+            t = getattr(self, k)
+            if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+                raise ValueError("Splats3D.%s must be a contiguous float32 CUDA tensor" % k)
+        return _lib.SsSplats3d(_ptr(self.mean3), _ptr(self.scale), _ptr(self.quat),
+                               _ptr(self.sh), self.n, self.sh_degree)
+
+    @staticmethod
+    def from_numpy(scene, device="cuda") -> "Splats3D":
+        f = lambda a: torch.from_numpy(a).to(device=device, dtype=torch.float32).contiguous()  # noqa
+        return Splats3D(f(scene.mean3), f(scene.scale), f(scene.quat), f(scene.sh),
+                        scene.sh_degree)
+
+
+def camera(R, t, fx: float, fy: float, cx: float, cy: float, near: float,
+           blur: float) -> _lib.SsCamera:
+    """The host ss_camera struct (R row-major world-to-camera rotation)."""
+    c = _lib.SsCamera()
+    for k, v in enumerate([float(x) for row in R for x in row]):
+        c.R[k] = v
+    for k in range(3):
+        c.t[k] = float(t[k])
+    c.fx, c.fy, c.cx, c.cy, c.near_z, c.blur = fx, fy, cx, cy, near, blur
+    return c
+
+
+def ss_project_fwd(splats: Splats3D, cam: _lib.SsCamera, mean2d, conic, depth, rgb,
+                   stream=None) -> None:
+    s = splats.c()
+    _check(_L.ss_project_fwd(ctypes.byref(s), ctypes.byref(cam), _ptr(mean2d), _ptr(conic),
+                             _ptr(depth), _ptr(rgb), _stream(stream)), "ss_project_fwd")
+
+
+def ss_project_bwd(splats: Splats3D, cam: _lib.SsCamera, dmean2d, dconic, drgb, grads: dict,
+                   stream=None) -> None:
+    """grads: dict of device tensors dmean3, dscale, dquat, dsh (overwritten)."""
+    s = splats.c()
+    g = _lib.SsGrads3d(*[_ptr(grads[k]) for k in ("dmean3", "dscale", "dquat", "dsh")])
+    _check(_L.ss_project_bwd(ctypes.byref(s), ctypes.byref(cam), _ptr(dmean2d), _ptr(dconic),
+                             _ptr(drgb), ctypes.byref(g), _stream(stream)), "ss_project_bwd")
+
+
+class Projector:
+    """Output and gradient buffers of the projection for n splats; the 2D
+    outputs plus a caller's opacity form the rasterizer's Splats."""
+
+    def __init__(self, n: int, sh_degree: int, device="cuda"):
+        d = torch.device(device)
+        f = lambda *s: torch.empty(*s, dtype=torch.float32, device=d)  # noqa: E731
+        K = (sh_degree + 1) ** 2
+        self.n, self.sh_degree = n, sh_degree
+        self.mean2d, self.conic, self.depth, self.rgb = f(n, 2), f(n, 3), f(n), f(n, 3)
+        self.grads = {"dmean3": f(n, 3), "dscale": f(n, 3), "dquat": f(n, 4), "dsh": f(K, 3, n)}
+
+    def forward(self, splats: Splats3D, cam, stream=None) -> None:
+        ss_project_fwd(splats, cam, self.mean2d, self.conic, self.depth, self.rgb, stream)
+
+    def backward(self, splats: Splats3D, cam, dmean2d, dconic, drgb, stream=None) -> None:
+        ss_project_bwd(splats, cam, dmean2d, dconic, drgb, self.grads, stream)
+
+    def splats2d(self, opacity) -> Splats:
+        return Splats(self.mean2d, self.conic, opacity, self.rgb, self.depth)
 
 
 # ------------------------------------------------------------------ whole path

@@ -1,4 +1,5 @@
-"""ctypes prototypes of libss.so (the C ABI declared in include/ss.h).
+"""ctypes prototypes of libss.so (the C ABI declared in include/ss.h and
+include/ss_project.h).
 
 Loading fails with an ImportError when the library has not been built: there
 is no fallback implementation behind this package.
@@ -31,7 +32,23 @@ class SsGrads(ctypes.Structure):
                 ("dopacity", ctypes.c_void_p), ("drgb", ctypes.c_void_p)]
 
 
-# name -> (restype, argtypes), in the order of include/ss.h
+class SsSplats3d(ctypes.Structure):
+    _fields_ = [("mean3", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("quat", ctypes.c_void_p),
+                ("sh", ctypes.c_void_p), ("n", ctypes.c_int32), ("sh_degree", ctypes.c_int32)]
+
+
+class SsCamera(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_float * 9), ("t", ctypes.c_float * 3), ("fx", ctypes.c_float),
+                ("fy", ctypes.c_float), ("cx", ctypes.c_float), ("cy", ctypes.c_float),
+                ("near_z", ctypes.c_float), ("blur", ctypes.c_float)]
+
+
+class SsGrads3d(ctypes.Structure):
+    _fields_ = [("dmean3", ctypes.c_void_p), ("dscale", ctypes.c_void_p),
+                ("dquat", ctypes.c_void_p), ("dsh", ctypes.c_void_p)]
+
+
+# name -> (restype, argtypes), in the order of include/ss.h, then include/ss_project.h
 P = ctypes.c_void_p
 I32, I64, U32, SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_size_t
 PROTOTYPES = {
@@ -55,6 +72,10 @@ PROTOTYPES = {
     "ss_profile_collect": (I64, [ctypes.c_char_p, SZ]),
     "ss_probe_red_f32": (ctypes.c_int, [P, I64, I32, P]),
     "ss_test_sort_wait_timeout": (ctypes.c_int, [P, SZ, P]),
+    "ss_project_fwd": (ctypes.c_int, [ctypes.POINTER(SsSplats3d), ctypes.POINTER(SsCamera), P, P,
+                                      P, P, P]),
+    "ss_project_bwd": (ctypes.c_int, [ctypes.POINTER(SsSplats3d), ctypes.POINTER(SsCamera), P, P,
+                                      P, ctypes.POINTER(SsGrads3d), P]),
 }
 
 _lib = None

@@ -40,7 +40,8 @@ def sources() -> list:
 
 
 def _deps() -> list:
-    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "ss.h")]
+    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + \
+        [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
 
 
 def up_to_date() -> bool:

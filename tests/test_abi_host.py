@@ -1,5 +1,5 @@
 """The C-ABI library on the host (no GPU): it loads, exports every function
-that include/ss.h declares, reports the oracle's constants, sizes its
+that include/ss.h and include/ss_project.h declare, reports the oracle's constants, sizes its
 workspace, and rejects bad arguments before touching CUDA."""
 import ctypes
 import os
@@ -12,7 +12,7 @@ import pytest
 import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "ss.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("ss.h", "ss_project.h")]
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +24,7 @@ def lib():
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    src = "".join(open(h).read() for h in HEADERS)
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(ss_[a-z0-9_]+)\s*\(", src)))
 
@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_path():
     names = declared_functions()
     for n in ("ss_bin_tiles", "ss_pair_count", "ss_sort_pairs", "ss_raster_fwd", "ss_raster_bwd",
-              "ss_workspace_bytes", "ss_last_error", "ss_constants"):
+              "ss_workspace_bytes", "ss_last_error", "ss_constants", "ss_project_fwd",
+              "ss_project_bwd"):
         assert n in names
 
 
@@ -128,3 +129,41 @@ def test_missing_library_fails_loudly(tmp_path):
     from gaussian_splatting_differentiable_gb300 import _lib
     with pytest.raises(ImportError):
         _lib.load(str(tmp_path / "nope.so"))
+
+
+def test_projection_rejects_bad_arguments_on_the_host(lib):
+    from gaussian_splatting_differentiable_gb300._lib import SsCamera, SsGrads3d, SsSplats3d
+
+    def cam(**kw):
+        c = SsCamera()
+        for k in range(9):
+            c.R[k] = 1.0 if k in (0, 4, 8) else 0.0
+        c.fx = c.fy = 100.0
+        c.cx, c.cy, c.near_z, c.blur = 32.0, 32.0, 0.2, 0.3
+        for k, v in kw.items():
+            setattr(c, k, v)
+        return c
+    s = SsSplats3d(0x1000, 0x1000, 0x1000, 0x1000, 10, 3)
+    g = SsGrads3d(0x1000, 0x1000, 0x1000, 0x1000)
+    P = ctypes.byref
+    assert lib.ss_project_fwd(None, P(cam()), 0x1000, 0x1000, 0x1000, 0x1000, None) == 1
+    assert lib.ss_project_fwd(P(s), None, 0x1000, 0x1000, 0x1000, 0x1000, None) == 1
+    bad_deg = SsSplats3d(0x1000, 0x1000, 0x1000, 0x1000, 10, 4)
+    assert lib.ss_project_fwd(P(bad_deg), P(cam()), 0x1000, 0x1000, 0x1000, 0x1000, None) == 1
+    assert "sh_degree" in lib.ss_last_error().decode()
+    misaligned = SsSplats3d(0x1000, 0x1000, 0x1004, 0x1000, 10, 3)
+    assert lib.ss_project_fwd(P(misaligned), P(cam()), 0x1000, 0x1000, 0x1000, 0x1000, None) == 1
+    null_sh = SsSplats3d(0x1000, 0x1000, 0x1000, None, 10, 3)
+    assert lib.ss_project_fwd(P(null_sh), P(cam()), 0x1000, 0x1000, 0x1000, 0x1000, None) == 1
+    assert lib.ss_project_fwd(P(s), P(cam(fx=0.0)), 0x1000, 0x1000, 0x1000, 0x1000, None) == 1
+    assert lib.ss_project_fwd(P(s), P(cam(blur=float("nan"))), 0x1000, 0x1000, 0x1000, 0x1000,
+                              None) == 1
+    assert lib.ss_project_fwd(P(s), P(cam()), 0x1004, 0x1000, 0x1000, 0x1000, None) == 1
+    assert lib.ss_project_fwd(P(s), P(cam()), None, 0x1000, 0x1000, 0x1000, None) == 1
+    assert lib.ss_project_bwd(P(s), P(cam()), 0x1000, None, 0x1000, P(g), None) == 1
+    assert lib.ss_project_bwd(P(s), P(cam()), 0x1000, 0x1000, 0x1000, None, None) == 1
+    g_mis = SsGrads3d(0x1000, 0x1000, 0x1008, 0x1000)
+    assert lib.ss_project_bwd(P(s), P(cam()), 0x1000, 0x1000, 0x1000, P(g_mis), None) == 1
+    empty = SsSplats3d(None, None, None, None, 0, 3)
+    assert lib.ss_project_fwd(P(empty), P(cam()), None, None, None, None, None) == 0
+    assert lib.ss_project_bwd(P(empty), P(cam()), None, None, None, P(g), None) == 0
