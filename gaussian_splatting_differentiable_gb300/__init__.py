@@ -1,7 +1,7 @@
 """Tile-based differentiable rasterization of projected 2D Gaussian splats on GB300.
 
 The compute path is libss.so (hand-written CUDA for sm_103a behind the C ABI
-of include/ss.h and include/ss_project.h).  This module is its thin Python binding: each ss_* function
+of include/ss.h, include/ss_project.h and include/ss_ssim.h).  This module is its thin Python binding: each ss_* function
 here has the C function's name and arguments and only marshals torch tensors
 (device memory) and streams into pointers.  PyTorch provides memory and
 streams; every step of the path runs in the library's kernels.  There is no
@@ -287,6 +287,38 @@ class Projector:
 
     def splats2d(self, opacity) -> Splats:
         return Splats(self.mean2d, self.conic, opacity, self.rgb, self.depth)
+
+
+# ------------------------------------------------------------------ L1 + SSIM loss (ss_ssim.h)
+
+def ss_ssim_workspace_bytes(C: int, H: int, W: int) -> int:
+    return int(_L.ss_ssim_workspace_bytes(C, H, W))
+
+
+def ss_ssim_loss(img, target, lam: float, loss, dL_dimg, workspace, stream=None) -> None:
+    """img, target, dL_dimg: [C,H,W] float32 device tensors; loss: float32[3]
+    device tensor (loss, mean SSIM, mean |x - y|)."""
+    C, H, W = img.shape
+    _check(_L.ss_ssim_loss(_ptr(img), _ptr(target), C, H, W, float(lam), _ptr(loss),
+                           _ptr(dL_dimg), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ss_ssim_loss")
+
+
+class SsimLoss:
+    """Buffers of ss_ssim_loss for one image size."""
+
+    def __init__(self, C: int, H: int, W: int, lam: float = 0.2, device="cuda"):
+        d = torch.device(device)
+        self.lam = lam
+        self.loss = torch.zeros(3, dtype=torch.float32, device=d)
+        self.grad = torch.empty(C, H, W, dtype=torch.float32, device=d)
+        nb = max(ss_ssim_workspace_bytes(C, H, W), 16)
+        self.workspace = torch.empty((nb + 15) // 16, 2, dtype=torch.float64, device=d)
+
+    def __call__(self, img, target, stream=None) -> torch.Tensor:
+        ss_ssim_loss(img, target, self.lam, self.loss, self.grad, self.workspace, stream)
+        return self.grad
 
 
 # ------------------------------------------------------------------ whole path

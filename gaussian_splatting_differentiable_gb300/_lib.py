@@ -1,5 +1,5 @@
-"""ctypes prototypes of libss.so (the C ABI declared in include/ss.h and
-include/ss_project.h).
+"""ctypes prototypes of libss.so (the C ABI declared in include/ss.h,
+include/ss_project.h and include/ss_ssim.h).
 
 Loading fails with an ImportError when the library has not been built: there
 is no fallback implementation behind this package.
@@ -48,7 +48,7 @@ class SsGrads3d(ctypes.Structure):
                 ("dquat", ctypes.c_void_p), ("dsh", ctypes.c_void_p)]
 
 
-# name -> (restype, argtypes), in the order of include/ss.h, then include/ss_project.h
+# name -> (restype, argtypes), in the order of include/ss.h, ss_project.h, ss_ssim.h
 P = ctypes.c_void_p
 I32, I64, U32, SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_size_t
 PROTOTYPES = {
@@ -76,6 +76,8 @@ PROTOTYPES = {
                                       P, P, P]),
     "ss_project_bwd": (ctypes.c_int, [ctypes.POINTER(SsSplats3d), ctypes.POINTER(SsCamera), P, P,
                                       P, ctypes.POINTER(SsGrads3d), P]),
+    "ss_ssim_workspace_bytes": (SZ, [I32, I32, I32]),
+    "ss_ssim_loss": (ctypes.c_int, [P, P, I32, I32, I32, ctypes.c_float, P, P, P, SZ, P]),
 }
 
 _lib = None

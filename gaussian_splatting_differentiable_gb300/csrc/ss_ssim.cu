@@ -1,0 +1,257 @@
+// L1 + SSIM training loss and its gradient with respect to the rendered
+// image in one pass ("ssim_fwd_bwd" of "Phase 5 step 30b -- kernel-by-kernel
+// timing": SSIM forward and backward in one command buffer; lambda = 0.20,
+// K = 7 window).  The model is stated in include/ss_ssim.h.
+//
+// The gradient is a correlation of the SSIM map's three adjoint maps
+// (d SSIM / d mu_x, d SSIM / d E[x^2], d SSIM / d E[xy]) with the window, so
+// the pixel at q needs the statistics of every p within 3 px, which need the
+// images within 6 px.  One CTA owns a 32 x 32 output tile of one channel and
+// does everything for it in shared memory: it loads the 44 x 44 input
+// region (zero outside the image), forms the five window moments on the
+// 38 x 38 region by two 1D passes, evaluates SSIM and the adjoint maps there
+// (0 outside the image), correlates them back by two more 1D passes and
+// writes dL/dimage.  HBM traffic is the two input images once (plus the
+// halo, which neighbouring CTAs read from L2) and the gradient once: 12 bytes
+// a pixel and channel.  Per-CTA partial sums of SSIM and |x - y| go to the
+// workspace in double; one small kernel adds them in a fixed order, so the
+// loss is deterministic.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "ss_internal.h"
+#include "ss_profile.h"
+#include "ss_ssim.h"
+
+namespace ss {
+namespace {
+
+constexpr int kT = 32;               // output tile side
+constexpr int kR = 3;                // window radius
+constexpr int kIn = kT + 4 * kR;     // 44: input region side
+constexpr int kMom = kT + 2 * kR;    // 38: moment / adjoint region side
+constexpr int kThreads = 256;
+constexpr float kC1 = 0.01f * 0.01f;
+constexpr float kC2 = 0.03f * 0.03f;
+
+struct SsimParams {
+    const float *img, *tgt;
+    float *grad;
+    double2 *partial;    // [blocks] (sum SSIM, sum |x - y|)
+    int C, H, W, tiles_x;
+    float g[2 * kR + 1];
+    float cs;            // dL/dSSIM(p) = -lambda / N
+    float cl;            // dL/d|x - y| = (1 - lambda) / N
+};
+
+struct SsimSmem {
+    float x[kIn][kIn];
+    float y[kIn][kIn];
+    float h[5][kIn][kMom];   // horizontal pass: moments, then the adjoint maps
+    float a[3][kMom][kMom];  // adjoint maps on the moment region
+    double red[2][kThreads / 32];
+};
+
+__global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SsimSmem &s = *reinterpret_cast<SsimSmem *>(smem_raw);
+    const int tid = threadIdx.x;
+    const int tx = blockIdx.x, ty = blockIdx.y, c = blockIdx.z;
+    const int x0 = tx * kT, y0 = ty * kT;
+    const size_t plane = size_t(p.H) * p.W;
+    const float *img = p.img + c * plane, *tgt = p.tgt + c * plane;
+
+    // A: the input region, zero outside the image
+    for (int k = tid; k < kIn * kIn; k += kThreads) {
+        const int r = k / kIn, q = k % kIn;
+        const int gy = y0 - 2 * kR + r, gx = x0 - 2 * kR + q;
+        const bool in = gy >= 0 && gy < p.H && gx >= 0 && gx < p.W;
+        const size_t o = size_t(gy) * p.W + gx;
+        s.x[r][q] = in ? __ldg(img + o) : 0.0f;
+        s.y[r][q] = in ? __ldg(tgt + o) : 0.0f;
+    }
+    __syncthreads();
+
+    // B: horizontal window sums of x, y, x^2, y^2, xy
+    for (int k = tid; k < kIn * kMom; k += kThreads) {
+        const int r = k / kMom, q = k % kMom;
+        float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f, m4 = 0.f;
+#pragma unroll
+        for (int j = 0; j <= 2 * kR; ++j) {
+            const float a = s.x[r][q + j], b = s.y[r][q + j], w = p.g[j];
+            const float wa = w * a, wb = w * b;
+            m0 += wa;
+            m1 += wb;
+            m2 = fmaf(wa, a, m2);
+            m3 = fmaf(wb, b, m3);
+            m4 = fmaf(wa, b, m4);
+        }
+        s.h[0][r][q] = m0, s.h[1][r][q] = m1, s.h[2][r][q] = m2, s.h[3][r][q] = m3,
+        s.h[4][r][q] = m4;
+    }
+    __syncthreads();
+
+    // C: vertical sums -> statistics, SSIM and the adjoint maps
+    double ssim_sum = 0.0;
+    for (int k = tid; k < kMom * kMom; k += kThreads) {
+        const int r = k / kMom, q = k % kMom;
+        float m[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j <= 2 * kR; ++j)
+#pragma unroll
+            for (int t = 0; t < 5; ++t) m[t] = fmaf(p.g[j], s.h[t][r + j][q], m[t]);
+        const int gy = y0 - kR + r, gx = x0 - kR + q;
+        const bool in = gy >= 0 && gy < p.H && gx >= 0 && gx < p.W;
+        const float mx = m[0], my = m[1];
+        const float A1 = 2.0f * mx * my + kC1;
+        const float A2 = 2.0f * (m[4] - mx * my) + kC2;
+        const float B1 = mx * mx + my * my + kC1;
+        const float B2 = (m[2] - mx * mx) + (m[3] - my * my) + kC2;
+        const float iA1 = 1.0f / A1, iA2 = 1.0f / A2, iB1 = 1.0f / B1, iB2 = 1.0f / B2;
+        const float S = A1 * A2 * iB1 * iB2;
+        const float cS = in ? p.cs * S : 0.0f;
+        s.a[0][r][q] = cS * 2.0f * (my * (iA1 - iA2) - mx * (iB1 - iB2));   // d/d mu_x
+        s.a[1][r][q] = -cS * iB2;                                            // d/d E[x^2]
+        s.a[2][r][q] = 2.0f * cS * iA2;                                      // d/d E[xy]
+        if (in && r >= kR && r < kR + kT && q >= kR && q < kR + kT) ssim_sum += S;
+    }
+    __syncthreads();
+
+    // D: horizontal correlation of the adjoint maps (reuses h)
+    for (int k = tid; k < kMom * kT; k += kThreads) {
+        const int r = k / kT, q = k % kT;
+        float v0 = 0.f, v1 = 0.f, v2 = 0.f;
+#pragma unroll
+        for (int j = 0; j <= 2 * kR; ++j) {
+            v0 = fmaf(p.g[j], s.a[0][r][q + j], v0);
+            v1 = fmaf(p.g[j], s.a[1][r][q + j], v1);
+            v2 = fmaf(p.g[j], s.a[2][r][q + j], v2);
+        }
+        s.h[0][r][q] = v0, s.h[1][r][q] = v1, s.h[2][r][q] = v2;
+    }
+    __syncthreads();
+
+    // E: vertical correlation and the gradient
+    double l1_sum = 0.0;
+    float *grad = p.grad + c * plane;
+    for (int k = tid; k < kT * kT; k += kThreads) {
+        const int r = k / kT, q = k % kT;
+        const int gy = y0 + r, gx = x0 + q;
+        if (gy >= p.H || gx >= p.W) continue;
+        float v0 = 0.f, v1 = 0.f, v2 = 0.f;
+#pragma unroll
+        for (int j = 0; j <= 2 * kR; ++j) {
+            v0 = fmaf(p.g[j], s.h[0][r + j][q], v0);
+            v1 = fmaf(p.g[j], s.h[1][r + j][q], v1);
+            v2 = fmaf(p.g[j], s.h[2][r + j][q], v2);
+        }
+        const float xv = s.x[r + 2 * kR][q + 2 * kR], yv = s.y[r + 2 * kR][q + 2 * kR];
+        const float d = xv - yv;
+        const float sg = d > 0.0f ? 1.0f : (d < 0.0f ? -1.0f : 0.0f);
+        grad[size_t(gy) * p.W + gx] = v0 + 2.0f * xv * v1 + yv * v2 + p.cl * sg;
+        l1_sum += fabsf(d);
+    }
+
+    // per-CTA partial sums, in double, in a fixed order
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ssim_sum += __shfl_xor_sync(0xffffffffu, ssim_sum, o);
+        l1_sum += __shfl_xor_sync(0xffffffffu, l1_sum, o);
+    }
+    if ((tid & 31) == 0) s.red[0][tid >> 5] = ssim_sum, s.red[1][tid >> 5] = l1_sum;
+    __syncthreads();
+    if (tid == 0) {
+        double a = 0.0, b = 0.0;
+        for (int w = 0; w < kThreads / 32; ++w) a += s.red[0][w], b += s.red[1][w];
+        const int blk = (c * gridDim.y + ty) * gridDim.x + tx;
+        p.partial[blk] = make_double2(a, b);
+    }
+}
+
+__global__ void __launch_bounds__(1024) k_ssim_final(const double2 *partial, int n_blocks,
+                                                     double inv_n, float lambda, float *out) {
+    __shared__ double red[2][32];
+    double a = 0.0, b = 0.0;
+    for (int k = threadIdx.x; k < n_blocks; k += blockDim.x) a += partial[k].x, b += partial[k].y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+    if ((threadIdx.x & 31) == 0) red[0][threadIdx.x >> 5] = a, red[1][threadIdx.x >> 5] = b;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double sa = 0.0, sb = 0.0;
+        for (int w = 0; w < int(blockDim.x >> 5); ++w) sa += red[0][w], sb += red[1][w];
+        const double ssim = sa * inv_n, l1 = sb * inv_n;
+        out[0] = float((1.0 - lambda) * l1 + lambda * (1.0 - ssim));
+        out[1] = float(ssim);
+        out[2] = float(l1);
+    }
+}
+
+int64_t ssim_blocks(int32_t C, int32_t H, int32_t W) {
+    return int64_t((W + kT - 1) / kT) * ((H + kT - 1) / kT) * C;
+}
+
+}  // namespace
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" size_t ss_ssim_workspace_bytes(int32_t C, int32_t H, int32_t W) {
+    if (C < 1 || H < 1 || W < 1 || H > kMaxSide || W > kMaxSide || C > 64) return 0;
+    return size_t(ssim_blocks(C, H, W)) * sizeof(double2);
+}
+
+extern "C" ss_status ss_ssim_loss(const float *img, const float *target, int32_t C, int32_t H,
+                                  int32_t W, float lambda, float *loss, float *dL_dimg,
+                                  void *workspace, size_t workspace_bytes, ss_stream_t stream) {
+    clear_error();
+    if (C < 1 || C > 64 || H < 1 || W < 1 || H > kMaxSide || W > kMaxSide)
+        return fail(SS_ERR_UNSUPPORTED, "ss_ssim_loss: image %dx%dx%d outside 1..64 x 1..%d x 1..%d",
+                    C, H, W, kMaxSide, kMaxSide);
+    if (!img || !target || !loss || !dL_dimg || !workspace)
+        return fail(SS_ERR_INVALID_ARG, "ss_ssim_loss: a pointer is NULL");
+    if (!(lambda >= 0.0f && lambda <= 1.0f))
+        return fail(SS_ERR_INVALID_ARG, "ss_ssim_loss: lambda outside [0, 1]");
+    if (reinterpret_cast<uintptr_t>(workspace) & 15)
+        return fail(SS_ERR_INVALID_ARG, "ss_ssim_loss: workspace not 16-byte aligned");
+    const size_t need = ss_ssim_workspace_bytes(C, H, W);
+    if (workspace_bytes < need)
+        return fail(SS_ERR_INVALID_ARG, "ss_ssim_loss: workspace %zu bytes < %zu", workspace_bytes,
+                    need);
+    static bool attr_set[64] = {};
+    int dev = 0;
+    ss_status st = check_cuda(cudaGetDevice(&dev), "ss_ssim_loss: cudaGetDevice");
+    if (st != SS_OK) return st;
+    if (dev < 64 && !attr_set[dev]) {
+        st = check_cuda(cudaFuncSetAttribute(k_ssim, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(sizeof(SsimSmem))),
+                        "ss_ssim_loss: cudaFuncSetAttribute");
+        if (st != SS_OK) return st;
+        attr_set[dev] = true;
+    }
+    SsimParams p{};
+    p.img = img, p.tgt = target, p.grad = dL_dimg;
+    p.partial = static_cast<double2 *>(workspace);
+    p.C = C, p.H = H, p.W = W, p.tiles_x = (W + kT - 1) / kT;
+    // the 1D window exp(-i^2 / (2 sigma^2)), sigma = 1.5, normalised in double
+    double g[2 * kR + 1], gs = 0.0;
+    for (int i = -kR; i <= kR; ++i) gs += (g[i + kR] = std::exp(-double(i * i) / (2.0 * 1.5 * 1.5)));
+    for (int i = 0; i <= 2 * kR; ++i) p.g[i] = float(g[i] / gs);
+    const double n = double(C) * H * W;
+    p.cs = float(-double(lambda) / n);
+    p.cl = float((1.0 - double(lambda)) / n);
+    cudaStream_t s = (cudaStream_t)stream;
+    const dim3 grid((W + kT - 1) / kT, (H + kT - 1) / kT, C);
+    SS_LAUNCH("k_ssim", s, k_ssim<<<grid, kThreads, sizeof(SsimSmem), s>>>(p));
+    st = check_launch("ss_ssim_loss");
+    if (st != SS_OK) return st;
+    SS_LAUNCH("k_ssim_final", s,
+              k_ssim_final<<<1, 1024, 0, s>>>(p.partial, int(ssim_blocks(C, H, W)), 1.0 / n,
+                                               lambda, loss));
+    return check_launch("ss_ssim_loss");
+}

@@ -1,5 +1,5 @@
 """The C-ABI library on the host (no GPU): it loads, exports every function
-that include/ss.h and include/ss_project.h declare, reports the oracle's constants, sizes its
+that include/ss.h, ss_project.h and ss_ssim.h declare, reports the oracle's constants, sizes its
 workspace, and rejects bad arguments before touching CUDA."""
 import ctypes
 import os
@@ -12,7 +12,7 @@ import pytest
 import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADERS = [os.path.join(ROOT, "include", f) for f in ("ss.h", "ss_project.h")]
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("ss.h", "ss_project.h", "ss_ssim.h")]
 
 
 @pytest.fixture(scope="module")
@@ -33,7 +33,7 @@ def test_header_declares_the_path():
     names = declared_functions()
     for n in ("ss_bin_tiles", "ss_pair_count", "ss_sort_pairs", "ss_raster_fwd", "ss_raster_bwd",
               "ss_workspace_bytes", "ss_last_error", "ss_constants", "ss_project_fwd",
-              "ss_project_bwd"):
+              "ss_project_bwd", "ss_ssim_loss", "ss_ssim_workspace_bytes"):
         assert n in names
 
 
@@ -167,3 +167,18 @@ def test_projection_rejects_bad_arguments_on_the_host(lib):
     empty = SsSplats3d(None, None, None, None, 0, 3)
     assert lib.ss_project_fwd(P(empty), P(cam()), None, None, None, None, None) == 0
     assert lib.ss_project_bwd(P(empty), P(cam()), None, None, None, P(g), None) == 0
+
+
+def test_ssim_rejects_bad_arguments_on_the_host(lib):
+    assert lib.ss_ssim_workspace_bytes(3, 822, 1237) == 16 * 3 * 26 * 39
+    assert lib.ss_ssim_workspace_bytes(0, 8, 8) == 0
+    ws = 16 * 3
+    assert lib.ss_ssim_loss(0x1000, 0x1000, 0, 8, 8, 0.2, 0x1000, 0x1000, 0x1000, ws, None) == 5
+    assert lib.ss_ssim_loss(0x1000, 0x1000, 3, 8, 40000, 0.2, 0x1000, 0x1000, 0x1000, ws, None) == 5
+    assert lib.ss_ssim_loss(None, 0x1000, 3, 8, 8, 0.2, 0x1000, 0x1000, 0x1000, ws, None) == 1
+    assert lib.ss_ssim_loss(0x1000, 0x1000, 3, 8, 8, 1.5, 0x1000, 0x1000, 0x1000, ws, None) == 1
+    assert lib.ss_ssim_loss(0x1000, 0x1000, 3, 8, 8, float("nan"), 0x1000, 0x1000, 0x1000, ws,
+                            None) == 1
+    assert lib.ss_ssim_loss(0x1000, 0x1000, 3, 8, 8, 0.2, 0x1000, 0x1000, 0x1008, ws, None) == 1
+    assert lib.ss_ssim_loss(0x1000, 0x1000, 3, 8, 8, 0.2, 0x1000, 0x1000, 0x1000, ws - 1, None) == 1
+    assert "workspace" in lib.ss_last_error().decode()
