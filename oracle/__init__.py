@@ -49,26 +49,30 @@ class _SplatsD(ctypes.Structure):
 class _Frame(ctypes.Structure):
     _fields_ = [("W", ctypes.c_int32), ("H", ctypes.c_int32), ("bg", ctypes.c_double * 3),
                 ("vals", ctypes.c_void_p), ("offs", ctypes.c_void_p),
-                ("tile_mask", ctypes.c_void_p)]
+                ("tile_mask", ctypes.c_void_p), ("dL_ddist", ctypes.c_void_p)]
 
 
 class _FwdOut(ctypes.Structure):
     _fields_ = [(k, ctypes.c_void_p) for k in ("image", "T_final", "last", "median", "n_amb",
-                                               "max_w", "count", "splat_amb")]
+                                               "max_w", "count", "splat_amb", "dist",
+                                               "dist_err")]
 
 
 class _Alt(ctypes.Structure):
     _fields_ = [("pixel", ctypes.c_int32), ("kind", ctypes.c_int32), ("list_pos", ctypes.c_int32),
                 ("last", ctypes.c_uint32), ("image", ctypes.c_double * 3),
-                ("T_final", ctypes.c_double), ("median", ctypes.c_double)]
+                ("T_final", ctypes.c_double), ("median", ctypes.c_double),
+                ("dist", ctypes.c_double)]
 
 
 class _Grads(ctypes.Structure):
-    _fields_ = [(k, ctypes.c_void_p) for k in ("dmean2d", "dconic", "dopacity", "drgb", "accum")]
+    _fields_ = [(k, ctypes.c_void_p) for k in ("dmean2d", "dconic", "dopacity", "drgb", "accum",
+                                               "ddepth")]
 
 
 ALT_DTYPE = np.dtype([("pixel", "<i4"), ("kind", "<i4"), ("list_pos", "<i4"), ("last", "<u4"),
-                      ("image", "<f8", (3,)), ("T_final", "<f8"), ("median", "<f8")])
+                      ("image", "<f8", (3,)), ("T_final", "<f8"), ("median", "<f8"),
+                      ("dist", "<f8")])
 assert ALT_DTYPE.itemsize == ctypes.sizeof(_Alt)
 
 
@@ -190,7 +194,7 @@ def tile_lists(scene):
             "culled": culled}
 
 
-def _frame(scene, vals, offs, tile_mask, bg, keep):
+def _frame(scene, vals, offs, tile_mask, bg, keep, dL_ddist=None):
     vals = np.ascontiguousarray(vals, np.uint32)
     offs = np.ascontiguousarray(offs, np.uint32)
     keep.extend([vals, offs])
@@ -200,8 +204,12 @@ def _frame(scene, vals, offs, tile_mask, bg, keep):
         keep.append(m)
         mask_p = _p(m)
     bgv = scene.bg if bg is None else bg
+    dd = None
+    if dL_ddist is not None:
+        dd = np.ascontiguousarray(dL_ddist, np.float64)
+        keep.append(dd)
     return _Frame(scene.W, scene.H, (ctypes.c_double * 3)(*[float(x) for x in bgv]),
-                  _p(vals) if vals.size else None, _p(offs), mask_p)
+                  _p(vals) if vals.size else None, _p(offs), mask_p, _p(dd))
 
 
 def forward(scene, vals, offs, tile_mask=None, params=None, bg=None, alt_capacity=1 << 16):
@@ -210,7 +218,8 @@ def forward(scene, vals, offs, tile_mask=None, params=None, bg=None, alt_capacit
     Returns image [3][H][W], T_final, last, median, n_amb (knife-edge count per
     pixel), alts (structured array of alternative outcomes) and the per-splat
     max_w (max blend weight), count (blended pixels) and splat_amb (blended at
-    a knife-edge pixel in some outcome)."""
+    a knife-edge pixel in some outcome), dist (the depth distortion per
+    pixel) and dist_err (a bound on its float32 evaluation error)."""
     lib = load()
     keep = []
     s = _splats_d(scene, params, keep)
@@ -219,9 +228,10 @@ def forward(scene, vals, offs, tile_mask=None, params=None, bg=None, alt_capacit
     res = {"image": np.zeros((3, H, W)), "T_final": np.ones((H, W)),
            "last": np.zeros((H, W), np.uint32), "median": np.zeros((H, W)),
            "n_amb": np.zeros((H, W), np.uint8), "max_w": np.zeros(scene.n),
-           "count": np.zeros(scene.n, np.uint32), "splat_amb": np.zeros(scene.n, np.uint8)}
+           "count": np.zeros(scene.n, np.uint32), "splat_amb": np.zeros(scene.n, np.uint8),
+           "dist": np.zeros((H, W)), "dist_err": np.zeros((H, W))}
     out = _FwdOut(*[_p(res[k]) for k in ("image", "T_final", "last", "median", "n_amb",
-                                         "max_w", "count", "splat_amb")])
+                                         "max_w", "count", "splat_amb", "dist", "dist_err")])
     alts = np.zeros(max(alt_capacity, 1), ALT_DTYPE)
     n_alt = lib.orc_forward(ctypes.byref(s), ctypes.byref(f), ctypes.byref(out), _p(alts),
                             alt_capacity)
@@ -231,28 +241,31 @@ def forward(scene, vals, offs, tile_mask=None, params=None, bg=None, alt_capacit
     return res
 
 
+_GRAD_KEYS = ("dmean2d", "dconic", "dopacity", "drgb", "accum", "ddepth")
+
+
 def _grads(n):
     return {"dmean2d": np.zeros((n, 2)), "dconic": np.zeros((n, 3)), "dopacity": np.zeros(n),
-            "drgb": np.zeros((n, 3)), "accum": np.zeros(n)}
+            "drgb": np.zeros((n, 3)), "accum": np.zeros(n), "ddepth": np.zeros(n)}
 
 
 def backward(scene, vals, offs, tile_mask=None, params=None, bg=None, dL_dimage=None,
-             slack=True):
-    """Per-splat gradients of L = sum dL/dimage * image (contributions of the masked tiles).
+             slack=True, dL_ddist=None):
+    """Per-splat gradients of L = sum dL/dimage * image (+ sum dL/ddist * dist
+    when dL_ddist is given) from the masked tiles.
 
     Returns dict(grads=..., slack=... or None, accum_err=...)."""
     lib = load()
     keep = []
     s = _splats_d(scene, params, keep)
-    f = _frame(scene, vals, offs, tile_mask, bg, keep)
+    f = _frame(scene, vals, offs, tile_mask, bg, keep, dL_ddist)
     g = np.ascontiguousarray(scene.dL_dimage if dL_dimage is None else dL_dimage, np.float64)
     keep.append(g)
     gr = _grads(scene.n)
     sl = _grads(scene.n) if slack else None
     aerr = np.zeros(scene.n)
-    cg = _Grads(*[_p(gr[k]) for k in ("dmean2d", "dconic", "dopacity", "drgb", "accum")])
-    cs = _Grads(*[_p(sl[k]) for k in ("dmean2d", "dconic", "dopacity", "drgb", "accum")]) \
-        if slack else None
+    cg = _Grads(*[_p(gr[k]) for k in _GRAD_KEYS])
+    cs = _Grads(*[_p(sl[k]) for k in _GRAD_KEYS]) if slack else None
     lib.orc_backward(ctypes.byref(s), ctypes.byref(f), _p(g), ctypes.byref(cg),
                      ctypes.byref(cs) if slack else None, _p(aerr))
     return {"grads": gr, "slack": sl, "accum_err": aerr}

@@ -38,6 +38,11 @@
  *   R13 per-splat weight statistics: the maximum over pixels of the blend
  *      weight alpha T, and the number of pixels that blended the splat (the
  *      "Avg" accumulated weight is R11's sum divided by that count).
+ *   R17 depth distortion of a pixel (the "distortion" option, whose per-pixel
+ *      totals the backward keeps): D = sum over pairs i < j of the pixel's
+ *      blended splats of w_i w_j (z_i - z_j)^2, w = alpha T, z the splat's
+ *      depth; its upstream gradient dL/dD per pixel adds to the backward,
+ *      which then also gives dL/ddepth.
  */
 #include "oracle.h"
 
@@ -330,6 +335,39 @@ static void run_pixel(const orc_splats_d *s, const uint32_t *list, int64_t len, 
     }
 }
 
+/* R17 by its definition: the double sum over pairs of blended splats.
+ * err receives a bound on the error of a float32 evaluation by running
+ * totals of depths taken relative to the first blended splat's: per blended
+ * splat i, 16 u w_i (z'_i^2 A + 2 |z'_i| |D1'| + D2') over the totals A, D1',
+ * D2' of the splats before it, plus |w_i E_i| (2 relT + mrel + 4 u (n + 2)). */
+static double pixel_dist(const orc_splats_d *s, const uint32_t *list, const pix_run *r,
+                         double *err)
+{
+    double D = 0.0;
+    for (int64_t i = 0; i < r->n; ++i)
+        for (int64_t j = 0; j < i; ++j) {
+            const double wi = r->rec[i].alpha * r->rec[i].T, wj = r->rec[j].alpha * r->rec[j].T;
+            const double dz = s->depth[list[r->rec[i].pos]] - s->depth[list[r->rec[j].pos]];
+            D += wi * wj * dz * dz;
+        }
+    if (err) {
+        double e = 0.0, A = 0.0, D1 = 0.0, D2 = 0.0;
+        const double z0 = r->n ? s->depth[list[r->rec[0].pos]] : 0.0;
+        for (int64_t i = 0; i < r->n; ++i) {
+            const double w = r->rec[i].alpha * r->rec[i].T;
+            const double z = s->depth[list[r->rec[i].pos]] - z0;
+            const double term = z * z * A - 2.0 * z * D1 + D2;
+            const double relw = 2.0 * r->relT + r->rec[i].mrel + 4.0 * U32 * (double)(r->n + 2);
+            e += 16.0 * U32 * w * (z * z * A + 2.0 * fabs(z) * fabs(D1) + D2) + fabs(w * term) * relw;
+            A += w;
+            D1 += w * z;
+            D2 += w * z * z;
+        }
+        *err = e;
+    }
+    return D;
+}
+
 static int64_t max_list(const orc_frame *f, int32_t n_tiles)
 {
     int64_t m = 1;
@@ -375,6 +413,8 @@ int64_t orc_forward(const orc_splats_d *s, const orc_frame *f, orc_fwd_out *out,
                         out->median[p] = r.median;
                     if (out->n_amb)
                         out->n_amb[p] = (uint8_t)(r.n_amb > 255 ? 255 : r.n_amb);
+                    if (out->dist)
+                        out->dist[p] = pixel_dist(s, list, &r, out->dist_err ? &out->dist_err[p] : NULL);
                     for (int64_t k = 0; k < r.n; ++k) {   /* R13 */
                         const int64_t i = list[r.rec[k].pos];
                         const double w = r.rec[k].alpha * r.rec[k].T;
@@ -399,6 +439,7 @@ int64_t orc_forward(const orc_splats_d *s, const orc_frame *f, orc_fwd_out *out,
                                 e->image[ch] = r2.C[ch] + r2.T * f->bg[ch];
                             e->T_final = r2.T;
                             e->median = r2.median;
+                            e->dist = pixel_dist(s, list, &r2, NULL);
                             if (out->splat_amb)
                                 for (int64_t k = 0; k < r2.n; ++k)
                                     out->splat_amb[list[r2.rec[k].pos]] = 1;
@@ -414,7 +455,8 @@ int64_t orc_forward(const orc_splats_d *s, const orc_frame *f, orc_fwd_out *out,
 
 /* --------------------------------------------------------------- backward */
 
-enum { F_MX, F_MY, F_A, F_B, F_C, F_O, F_R, F_G, F_BL, F_W, NF };
+enum { F_MX, F_MY, F_A, F_B, F_C, F_O, F_R, F_G, F_BL, F_W, F_Z, NF };
+
 
 /* Gradient contributions of one pixel by the plain definition (R10, R11):
  * with T_k the transmittance before blended splat k, w_k = alpha_k T_k and
@@ -425,12 +467,18 @@ enum { F_MX, F_MY, F_A, F_B, F_C, F_O, F_R, F_G, F_BL, F_W, NF };
  *   dL/do_k     = G_k dL/dalpha_k
  *   dL/dmean    = dL/dsigma * (-(a dx + b dy), -(b dx + c dy))
  *   dL/d(a,b,c) = dL/dsigma * (dx^2 / 2, dx dy, dy^2 / 2)
- * written to out[k][F_*]; out[k][F_W] = w_k. */
+ * written to out[k][F_*]; out[k][F_W] = w_k.
+ * With an upstream gradient gD of the distortion D (R17), D's own terms add:
+ * with E_k = dD/dw_k = sum_j w_j (z_k - z_j)^2 and dw_i/dalpha_k = T_k (i = k),
+ * -w_i / (1 - alpha_k) (i after k),
+ *   dL/dalpha_k += gD (E_k T_k - sum_{i after k} w_i E_i / (1 - alpha_k))
+ *   dL/dz_k      = gD sum_j 2 w_k w_j (z_k - z_j)                  (out[k][F_Z]). */
 static void pixel_backward(const orc_splats_d *s, const uint32_t *list, const pix_run *r,
                            double px, double py, const double g[3], const double bg[3],
-                           double *out)
+                           double gD, double *out)
 {
     double S[3] = {0.0, 0.0, 0.0};
+    double SE = 0.0;   /* sum over later blended splats of w E */
     for (int64_t k = r->n - 1; k >= 0; --k) {
         const blend_rec *e = &r->rec[k];
         const int64_t i = list[e->pos];
@@ -439,7 +487,19 @@ static void pixel_backward(const orc_splats_d *s, const uint32_t *list, const pi
         double dL_dalpha = 0.0;
         for (int ch = 0; ch < 3; ++ch)
             dL_dalpha += g[ch] * (col[ch] * e->T - (S[ch] + r->T * bg[ch]) / (1.0 - e->alpha));
+        double E = 0.0, dz_sum = 0.0;
+        if (gD != 0.0) {
+            const double zk = s->depth[i];
+            for (int64_t j = 0; j < r->n; ++j) {
+                const double wj = r->rec[j].alpha * r->rec[j].T;
+                const double dz = zk - s->depth[list[r->rec[j].pos]];
+                E += wj * dz * dz;
+                dz_sum += 2.0 * w * wj * dz;
+            }
+            dL_dalpha += gD * (E * e->T - SE / (1.0 - e->alpha));
+        }
         double *o = out + NF * k;
+        o[F_Z] = gD * dz_sum;
         for (int ch = 0; ch < 3; ++ch)
             o[F_R + ch] = g[ch] * w;
         o[F_W] = w;
@@ -459,6 +519,7 @@ static void pixel_backward(const orc_splats_d *s, const uint32_t *list, const pi
         }
         for (int ch = 0; ch < 3; ++ch)
             S[ch] += col[ch] * w;
+        SE += w * E;
     }
 }
 
@@ -476,6 +537,8 @@ static void add_fields(orc_grads *gr, int64_t i, const double *v, int absval)
     ACC(gr->drgb[3 * i + 2], v[F_BL]);
     if (gr->accum)
         ACC(gr->accum[i], v[F_W]);
+    if (gr->ddepth)
+        ACC(gr->ddepth[i], v[F_Z]);
 #undef ACC
 }
 
@@ -511,8 +574,9 @@ int orc_backward(const orc_splats_d *s, const orc_frame *f, const double *dL_dim
                     const int64_t p = (int64_t)y * W + x;
                     const double g[3] = {dL_dimage[p], dL_dimage[HW + p], dL_dimage[2 * HW + p]};
                     const double px = x + 0.5, py = y + 0.5;
+                    const double gD = f->dL_ddist ? f->dL_ddist[p] : 0.0;
                     run_pixel(s, list, len, px, py, -1, 0, &r);
-                    pixel_backward(s, list, &r, px, py, g, f->bg, c1);
+                    pixel_backward(s, list, &r, px, py, g, f->bg, gD, c1);
                     for (int64_t k = 0; k < r.n; ++k) {
                         const int64_t i = list[r.rec[k].pos];
                         add_fields(grads, i, c1 + NF * k, 0);
@@ -528,7 +592,7 @@ int orc_backward(const orc_splats_d *s, const orc_frame *f, const double *dL_dim
                     const int na = r.n_amb < MAX_AMB ? r.n_amb : MAX_AMB;
                     for (int j = 0; j < na; ++j) {
                         run_pixel(s, list, len, px, py, r.amb_pos[j], r.amb_kind[j], &r2);
-                        pixel_backward(s, list, &r2, px, py, g, f->bg, c2);
+                        pixel_backward(s, list, &r2, px, py, g, f->bg, gD, c2);
                         memset(byp1, 0, sizeof(double) * NF * (size_t)len);
                         memset(byp2, 0, sizeof(double) * NF * (size_t)len);
                         for (int64_t k = 0; k < r.n; ++k)

@@ -50,6 +50,7 @@ typedef struct {
     const uint32_t *vals;      /* splat index per sorted pair */
     const uint32_t *offs;      /* [tiles + 1] CSR ranges into vals */
     const uint8_t *tile_mask;  /* NULL: all tiles; else only tiles with mask != 0 */
+    const double *dL_ddist;    /* [H][W] upstream gradient of the distortion image, or NULL */
 } orc_frame;
 
 typedef struct {               /* forward outputs; any pointer may be NULL */
@@ -61,6 +62,8 @@ typedef struct {               /* forward outputs; any pointer may be NULL */
     double *max_w;             /* [n] max over pixels of the blend weight alpha T (+=max) */
     uint32_t *count;           /* [n] pixels that blended the splat (+=) */
     uint8_t *splat_amb;        /* [n] 1 if blended at a knife-edge pixel in any outcome */
+    double *dist;              /* [H][W] depth distortion sum_{i<j} w_i w_j (z_i - z_j)^2 */
+    double *dist_err;          /* [H][W] bound on the error of its float32 evaluation */
 } orc_fwd_out;
 
 /* One alternative outcome of a pixel: the result when one knife-edge
@@ -73,6 +76,7 @@ typedef struct {
     double image[3];
     double T_final;
     double median;
+    double dist;
 } orc_alt;
 
 enum { ORC_AMB_ALPHA = 1, ORC_AMB_TERM = 2, ORC_AMB_CLAMP = 3, ORC_AMB_MEDIAN = 4 };
@@ -83,6 +87,7 @@ typedef struct {               /* per-splat fields, all double */
     double *dopacity;          /* [n]    */
     double *drgb;              /* [n][3] */
     double *accum;             /* [n]    */
+    double *ddepth;            /* [n] (only with dL_ddist; may be NULL) */
 } orc_grads;
 
 void orc_constants(double out[4]);   /* alpha_min, alpha_max, T_eps, tile */

@@ -26,6 +26,8 @@ image cut into 16x16 tiles):
   and stored as float32 (a, b, c) = upper triangle of the symmetric inverse;
 * opacity, RGB, depth uniform over the workload's ranges;
 * dL/dimage ~ N(0, sigma^2) with sigma the standard deviation;
+* dL/ddistortion per pixel ~ N(0, (sigma / dz^2)^2), dz the width of the depth
+  range, so that the distortion's gradients have the colour's scale;
 * background black.
 """
 from __future__ import annotations
@@ -90,9 +92,10 @@ class Workload:
     blob_frac: float = 0.0
     blob_sigma: float = 0.0
     weight_stats: bool = False   # per-splat max blend weight and blend count
+    distortion: bool = False     # per-pixel depth distortion and its gradient
 
 
-# The five workloads; index 1..5.
+# The six workloads; index 1..6 (6 = workload 4 with the distortion output).
 WORKLOADS = {
     1: Workload("tiny-64x64-256", 64, 64, 256, (0.5, 4.0), (0.05, 0.99), (1.0, 10.0), 1.0,
                 True, False, weight_stats=True),
@@ -105,6 +108,8 @@ WORKLOADS = {
     5: Workload("1920x1080-2M-blobs", 1920, 1080, 2_000_000, (0.3, 4.0), (0.02, 0.9),
                 (1.0, 100.0), 0.1, True, True, blobs=4, blob_frac=0.3, blob_sigma=60.0,
                 weight_stats=True),
+    6: Workload("1237x822-2M-dist", 1237, 822, 2_000_000, (0.3, 3.0), (0.02, 0.9), (1.0, 100.0),
+                0.1, True, False, distortion=True),
 }
 
 
@@ -123,6 +128,8 @@ class Scene:
     median_depth: bool
     name: str = ""
     weight_stats: bool = False
+    distortion: bool = False
+    dL_ddist: np.ndarray | None = None   # f32 [H][W]
 
     @property
     def n(self) -> int:
@@ -169,12 +176,15 @@ def make_scene(workload: int | Workload, seed: int = 0, n: int | None = None,
     rgb = uniform01(k(7), 3 * n).reshape(n, 3)
     depth = wl.depth[0] + (wl.depth[1] - wl.depth[0]) * uniform01(k(8), n)
     dL = normal(k(9), 3 * H * W, wl.grad_std).reshape(3, H, W)
+    dz = wl.depth[1] - wl.depth[0]
+    dLd = normal(k(14), H * W, wl.grad_std / (dz * dz)).reshape(H, W)
     f32 = lambda x: np.ascontiguousarray(x, dtype=np.float32)  # noqa: E731
     return Scene(W=W, H=H,
                  mean2d=f32(np.stack([mx, my], axis=1)), conic=f32(conic), opacity=f32(opacity),
                  rgb=f32(rgb), depth=f32(depth), dL_dimage=f32(dL),
                  bg=np.zeros(3, np.float32), accum_weight=wl.accum_weight,
-                 median_depth=wl.median_depth, name=wl.name, weight_stats=wl.weight_stats)
+                 median_depth=wl.median_depth, name=wl.name, weight_stats=wl.weight_stats,
+                 distortion=wl.distortion, dL_ddist=f32(dLd))
 
 
 def subset(scene: Scene, idx: np.ndarray) -> Scene:

@@ -262,7 +262,7 @@ def test_tiled_equals_brute_force_over_all_splats(wl, n, W, H):
     vals = np.tile(order, tx * ty)
     offs = (np.arange(tx * ty + 1) * order.size).astype(np.uint32)
     b = oracle.forward(sc, vals, offs)
-    for k in ("image", "T_final", "last", "median"):
+    for k in ("image", "T_final", "last", "median", "dist"):
         if k == "last":   # positions differ (whole list vs tile list); compare the splat
             lt = np.zeros_like(f[k], np.int64) - 1
             lb = np.zeros_like(b[k], np.int64) - 1
@@ -325,17 +325,22 @@ def test_knife_edge_pixel_has_alternative():
 
 # ---------------------------------------------------------------- backward
 
-def _loss(sc, tl, params, bg):
+def _loss(sc, tl, params, bg, gD=None):
     f = oracle.forward(sc, tl["vals"], tl["offs"], params=params, bg=bg)
-    return float(np.sum(f["image"] * sc.dL_dimage.astype(np.float64)))
+    L = float(np.sum(f["image"] * sc.dL_dimage.astype(np.float64)))
+    if gD is not None:
+        L += float(np.sum(f["dist"] * gD))
+    return L
 
 
 FIELDS = [("mean2d", "dmean2d", 2), ("conic", "dconic", 3), ("opacity", "dopacity", 1),
           ("rgb", "drgb", 3)]
 
 
-@pytest.mark.parametrize("seed,clamp", [(0, False), (1, False), (2, True)])
-def test_backward_matches_central_finite_differences(seed, clamp):
+@pytest.mark.parametrize("seed,clamp,dist", [(0, False, False), (1, False, False),
+                                             (2, True, False), (3, False, True),
+                                             (4, True, True)])
+def test_backward_matches_central_finite_differences(seed, clamp, dist):
     rng = np.random.default_rng(seed)
     n, W, H = 12, 32, 32
     th = rng.uniform(0, np.pi, n)
@@ -349,9 +354,11 @@ def test_backward_matches_central_finite_differences(seed, clamp):
     tl = oracle.tile_lists(sc)
     bgd = sc.bg.astype(np.float64)
     base = {k: getattr(sc, k).astype(np.float64) for k in ("mean2d", "conic", "opacity", "rgb", "depth")}
-    an = oracle.backward(sc, tl["vals"], tl["offs"])["grads"]
+    gD = rng.normal(0, 0.05, (H, W)) if dist else None
+    an = oracle.backward(sc, tl["vals"], tl["offs"], dL_ddist=gD)["grads"]
     checked = 0
-    for name, gname, width in FIELDS:
+    fields = FIELDS + ([("depth", "ddepth", 1)] if dist else [])
+    for name, gname, width in fields:
         ref = np.abs(an[gname]).max()
         for i in range(n):
             for c in range(width):
@@ -360,7 +367,7 @@ def test_backward_matches_central_finite_differences(seed, clamp):
                     p2 = {k: v.copy() for k, v in base.items()}
                     p1[name].reshape(n, -1)[i, c] += h
                     p2[name].reshape(n, -1)[i, c] -= h
-                    return (_loss(sc, tl, p1, bgd) - _loss(sc, tl, p2, bgd)) / (2 * h)
+                    return (_loss(sc, tl, p1, bgd, gD) - _loss(sc, tl, p2, bgd, gD)) / (2 * h)
                 x = abs(base[name].reshape(n, -1)[i, c])
                 h = 1e-5 * max(1.0, x)
                 f1, f2 = fd(h), fd(h / 2)
@@ -369,7 +376,38 @@ def test_backward_matches_central_finite_differences(seed, clamp):
                 g = an[gname].reshape(n, -1)[i, c]
                 assert abs(f2 - g) <= 2e-6 * max(abs(g), 1e-2 * ref), (name, i, c, f2, g)
                 checked += 1
-    assert checked >= 0.9 * n * 9
+    assert checked >= 0.9 * n * (10 if dist else 9)
+
+
+def test_distortion_two_splats_closed_form():
+    a1, a2 = 0.6, 0.7
+    for d1, d2 in ((1.0, 4.0), (4.0, 1.0)):
+        sc = scene_of(16, 16, [[8.5, 8.5]] * 2, [[4, 0, 4]] * 2, [a1, a2], [[1, 1, 1]] * 2,
+                      [d1, d2])
+        _, f = render(sc)
+        A1, A2 = float(np.float32(a1)), float(np.float32(a2))
+        wf, wb = (A1, A2 * (1 - A1)) if d1 < d2 else (A2, A1 * (1 - A2))
+        assert f["dist"][8, 8] == pytest.approx(wf * wb * 9.0, rel=1e-14)
+    sc = scene_of(16, 16, [[8.5, 8.5]] * 3, [[4, 0, 4]] * 3, [0.5, 0.5, 0.5], [[1, 1, 1]] * 3,
+                  [1.0, 2.0, 5.0])
+    _, f = render(sc)
+    w = [0.5, 0.25, 0.125]
+    ref = w[0] * w[1] * 1 + w[0] * w[2] * 16 + w[1] * w[2] * 9
+    assert f["dist"][8, 8] == pytest.approx(ref, rel=1e-14)
+
+
+def test_distortion_invariants():
+    sc = synth.make_scene(2, seed=4, n=600, W=64, H=48)
+    _, f = render(sc)
+    assert np.all(f["dist"] >= 0) and f["dist"].max() > 0
+    one = synth.subset(sc, np.array([5]))
+    assert not render(one)[1]["dist"].any()                    # one splat: no pair
+    flat = synth.subset(sc, np.arange(sc.n))
+    flat.depth[:] = np.float32(3.0)
+    assert not render(flat)[1]["dist"].any()                   # equal depths
+    dbl = synth.subset(sc, np.arange(sc.n))
+    dbl.depth *= np.float32(2.0)                               # exact; same order
+    np.testing.assert_allclose(render(dbl)[1]["dist"], 4.0 * f["dist"], rtol=1e-12, atol=0)
 
 
 def test_accum_weight_equals_red_gradient_under_unit_red_loss():
@@ -425,6 +463,11 @@ MUTATIONS = [
     ("max weight over alpha", "const double w = r.rec[k].alpha * r.rec[k].T;",
      "const double w = r.rec[k].alpha;"),
     ("count of evaluated splats", "out->count[i] += 1;", "out->count[i] += 2;"),
+    ("distortion |dz|", "D += wi * wj * dz * dz;", "D += wi * wj * fabs(dz);"),
+    ("distortion without the later splats' term",
+     "dL_dalpha += gD * (E * e->T - SE / (1.0 - e->alpha));", "dL_dalpha += gD * (E * e->T);"),
+    ("ddepth halved", "dz_sum += 2.0 * w * wj * dz;", "dz_sum += w * wj * dz;"),
+    ("suffix sum without w", "SE += w * E;", "SE += E;"),
 ]
 
 
