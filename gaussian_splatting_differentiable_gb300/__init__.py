@@ -16,8 +16,8 @@ import dataclasses
 import torch
 
 from . import _lib
-from ._lib import (SS_ACCUM_WEIGHT, SS_ERR_CAPACITY, SS_MEDIAN_DEPTH, SS_OK,  # noqa: F401
-                   SS_WEIGHT_STATS, STATUS_NAMES, SsGrads, SsSplats)
+from ._lib import (SS_ACCUM_WEIGHT, SS_DISTORTION, SS_ERR_CAPACITY, SS_MEDIAN_DEPTH,  # noqa: F401
+                   SS_OK, SS_WEIGHT_STATS, STATUS_NAMES, SsGrads, SsSplats)
 
 _L = _lib.load()
 TILE = 16
@@ -148,23 +148,31 @@ def ss_sort_status(workspace, stream=None) -> int:
 
 def ss_raster_fwd(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int, H: int, bg,
                   flags: int, image, T_final, last_contrib, median_depth, blend_masks,
-                  max_weight=None, blend_count=None, stream=None) -> None:
+                  max_weight=None, blend_count=None, distortion=None, dist_totals=None,
+                  stream=None) -> None:
     _check(_L.ss_raster_fwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), n_pairs, W,
                             H, _f32_host3(bg), flags, _ptr(image), _ptr(T_final),
                             _ptr(last_contrib), _ptr(median_depth), _ptr(blend_masks),
-                            _ptr(max_weight), _ptr(blend_count), _stream(stream)),
+                            _ptr(max_weight), _ptr(blend_count), _ptr(distortion),
+                            _ptr(dist_totals), _stream(stream)),
            "ss_raster_fwd")
+
+
+def _grads_struct(grads: dict) -> SsGrads:
+    return SsGrads(_ptr(grads["dmean2d"]), _ptr(grads["dconic"]), _ptr(grads["dopacity"]),
+                   _ptr(grads["drgb"]), _ptr(grads.get("ddepth")))
 
 
 def ss_raster_bwd(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int, H: int, bg,
                   flags: int, T_final, last_contrib, blend_masks, dL_dimage, grads: dict,
-                  accum_weight, workspace, stream=None) -> None:
-    g = SsGrads(_ptr(grads["dmean2d"]), _ptr(grads["dconic"]), _ptr(grads["dopacity"]),
-                _ptr(grads["drgb"]))
+                  accum_weight, workspace, stream=None, dist_totals=None,
+                  dL_ddist=None) -> None:
+    g = _grads_struct(grads)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_L.ss_raster_bwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), n_pairs, W,
                             H, _f32_host3(bg), flags, _ptr(T_final), _ptr(last_contrib),
-                            _ptr(blend_masks), _ptr(dL_dimage), ctypes.byref(g), _ptr(accum_weight),
+                            _ptr(blend_masks), _ptr(dL_dimage), _ptr(dist_totals),
+                            _ptr(dL_ddist), ctypes.byref(g), _ptr(accum_weight),
                             _ptr(workspace), nbytes, _stream(stream)), "ss_raster_bwd")
 
 
@@ -174,8 +182,7 @@ def ss_raster_bwd_noalloc(records, n_splats: int, vals, tile_offsets, n_pairs: i
     """ss_raster_bwd for callers that cannot allocate: no workspace argument;
     the weight scratch is a fixed array inside the library (at most 2,097,152
     splats; concurrent calls race on it)."""
-    g = SsGrads(_ptr(grads["dmean2d"]), _ptr(grads["dconic"]), _ptr(grads["dopacity"]),
-                _ptr(grads["drgb"]))
+    g = _grads_struct(grads)
     _check(_L.ss_raster_bwd_noalloc(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets),
                                     n_pairs, W, H, _f32_host3(bg), flags, _ptr(T_final),
                                     _ptr(last_contrib), _ptr(blend_masks), _ptr(dL_dimage),
@@ -355,6 +362,11 @@ class Rasterizer:
         stats = flags & SS_WEIGHT_STATS
         self.max_weight = torch.empty(n_splats, dtype=torch.float32, device=d) if stats else None
         self.blend_count = torch.empty(n_splats, dtype=torch.int32, device=d) if stats else None
+        dist = flags & SS_DISTORTION
+        self.distortion = torch.empty(H, W, dtype=torch.float32, device=d) if dist else None
+        self.dist_totals = torch.empty(H, W, 4, dtype=torch.float32, device=d) if dist else None
+        if dist:
+            self.grads["ddepth"] = torch.empty(n_splats, dtype=torch.float32, device=d)
         self.n_pairs = 0
         self.culled = 0
 
@@ -390,23 +402,25 @@ class Rasterizer:
         ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs, self.W,
                       self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
                       self.median_depth, self.blend_masks, self.max_weight, self.blend_count,
-                      stream)
+                      self.distortion, self.dist_totals, stream)
 
-    def backward(self, splats, dL_dimage: torch.Tensor, stream=None) -> None:
-        """Gradients; uses the records written by the last bin_and_sort."""
+    def backward(self, splats, dL_dimage: torch.Tensor, stream=None, dL_ddist=None) -> None:
+        """Gradients; uses the records written by the last bin_and_sort.
+        dL_ddist: [H, W] upstream gradient of the distortion (SS_DISTORTION)."""
         ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs, self.W,
                       self.H, self.bg, self.flags, self.T_final, self.last_contrib,
                       self.blend_masks, dL_dimage, self.grads, self.accum_weight, self.workspace,
-                      stream)
+                      stream, self.dist_totals, dL_ddist)
 
-    def step(self, splats: Splats, dL_dimage: torch.Tensor, stream=None) -> int:
+    def step(self, splats: Splats, dL_dimage: torch.Tensor, stream=None, dL_ddist=None) -> int:
         """One pass of the whole path: bin, sort, forward, backward."""
         n = self.bin_and_sort(splats, stream)
         self.forward(splats, stream)
-        self.backward(splats, dL_dimage, stream)
+        self.backward(splats, dL_dimage, stream, dL_ddist)
         return n
 
-    def step_async(self, splats: Splats, dL_dimage: torch.Tensor, stream=None) -> None:
+    def step_async(self, splats: Splats, dL_dimage: torch.Tensor, stream=None,
+                   dL_ddist=None) -> None:
         """bin -> sort -> forward -> backward with the pair count kept on the
         device: no host synchronisation, so the step can be captured in a
         CUDA graph.  The pair buffers must already be large enough (size them
@@ -418,22 +432,23 @@ class Rasterizer:
         ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.capacity, self.W,
                       self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
                       self.median_depth, self.blend_masks, self.max_weight, self.blend_count,
-                      stream)
+                      self.distortion, self.dist_totals, stream)
         ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.capacity, self.W,
                       self.H, self.bg, self.flags, self.T_final, self.last_contrib,
                       self.blend_masks, dL_dimage, self.grads, self.accum_weight, self.workspace,
-                      stream)
+                      stream, self.dist_totals, dL_ddist)
 
     def check(self, stream=None) -> None:
         """Raise if the last sort reported a device-side problem (capacity
         overflow, look-back timeout, out-of-range key)."""
         _check(ss_sort_status(self.workspace, stream), "sort status")
 
-    def capture(self, splats: Splats, dL_dimage: torch.Tensor) -> "torch.cuda.CUDAGraph":
+    def capture(self, splats: Splats, dL_dimage: torch.Tensor,
+                dL_ddist=None) -> "torch.cuda.CUDAGraph":
         """A CUDA graph of step_async on these buffers (replay with .replay())."""
-        self.step_async(splats, dL_dimage)        # first calls set kernel attributes
+        self.step_async(splats, dL_dimage, dL_ddist=dL_ddist)   # first calls set attributes
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.step_async(splats, dL_dimage)
+            self.step_async(splats, dL_dimage, dL_ddist=dL_ddist)
         return g

@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "SS_OK", 1: "SS_ERR_INVALID_ARG", 2: "SS_ERR_CAPACITY", 3: "S
 SS_ACCUM_WEIGHT = 1
 SS_MEDIAN_DEPTH = 2
 SS_WEIGHT_STATS = 4
+SS_DISTORTION = 8
 
 
 class SsSplats(ctypes.Structure):
@@ -29,7 +30,8 @@ class SsSplats(ctypes.Structure):
 
 class SsGrads(ctypes.Structure):
     _fields_ = [("dmean2d", ctypes.c_void_p), ("dconic", ctypes.c_void_p),
-                ("dopacity", ctypes.c_void_p), ("drgb", ctypes.c_void_p)]
+                ("dopacity", ctypes.c_void_p), ("drgb", ctypes.c_void_p),
+                ("ddepth", ctypes.c_void_p)]
 
 
 class SsSplats3d(ctypes.Structure):
@@ -63,8 +65,8 @@ PROTOTYPES = {
     "ss_sort_pairs_dev": (ctypes.c_int, [P, P, P, I64, I32, I32, P, P, SZ, P]),
     "ss_sort_status": (ctypes.c_int, [P, P]),
     "ss_raster_fwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P, P, P,
-                                     P]),
-    "ss_raster_bwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P,
+                                     P, P, P]),
+    "ss_raster_bwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P, P,
                                      ctypes.POINTER(SsGrads), P, P, SZ, P]),
     "ss_raster_bwd_noalloc": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P,
                                              ctypes.POINTER(SsGrads), P, P]),

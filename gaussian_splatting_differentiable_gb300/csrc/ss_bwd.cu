@@ -35,6 +35,16 @@
 // instead).  The accumulated weight is added in 32.32 fixed point with
 // 64-bit integer atomics, so it is exact and independent of atomic order.
 //
+// Distortion (the DIST variant).  The depth distortion's gradient has the
+// colour's shape: with E = dD/dw = z'^2 A - 2 z' D1 + D2 from the forward's
+// per-pixel totals (depths z' relative to the pixel's first blended splat),
+// dD/dalpha = E T_front - (sum of w E over later splats) / (1 - alpha), so
+// dL/ddist E joins dL/dimage . rgb in the per-splat scalar and in GR, and
+// dL/ddepth = 2 dL/ddist w (z A - D1) sums, per warp and splat, to
+// 2 (z Wa - Wd) with Wa = sum w dL/ddist A and Wd = sum w dL/ddist D1 --
+// two more moments of the slot sums, added with the blue gradient as one
+// 8-byte reduction into the record's spare tenth float.
+//
 // The blend decisions are the forward's: its per-(pair, 8x4 block) masks
 // select the entries each warp handles and each pixel's bit, so nothing is
 // re-evaluated; after a chunk of 16 selected entries each pixel walks only
@@ -58,20 +68,27 @@ struct BwdParams {
     const uint32_t *last;
     const float *dL;
     float *dmean2d, *dconic, *dopacity, *drgb;
+    float *ddepth;              // (DIST)
+    const float4 *dist_totals;  // [H][W] (A, D1, D2, z_ref) from the forward (DIST)
+    const float *dL_ddist;      // [H][W] (DIST)
     unsigned long long *accum;  // 32.32 fixed point (SoA mode)
     float *scratch;             // [n][12] per-splat gradient record (AoS mode)
 };
 
 // Per-splat gradient scratch record (AoS mode), 48 bytes, 16-byte aligned:
 // [0..3] dmean x, dmean y, dconic a, dconic b; [4..7] dconic c, dopacity,
-// drgb r, drgb g; [8] drgb b; [9] unused; [10..11] accumulated weight as a
-// uint64 in 32.32 fixed point.
+// drgb r, drgb g; [8] drgb b; [9] ddepth (DIST); [10..11] accumulated weight
+// as a uint64 in 32.32 fixed point.
 constexpr int kGradRec = 12;
 
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
                  "f"(c), "f"(d)
                  : "memory");
+}
+
+__device__ __forceinline__ void red_add_v2(float *addr, float a, float b) {
+    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(a), "f"(b) : "memory");
 }
 
 constexpr int kSlots = 16;     // slots per warp
@@ -93,20 +110,21 @@ __device__ __forceinline__ float rcp_approx(float x) {
 struct __align__(16) ChunkEnt {
     SplatGeo g;   // mx, my, A, B
     float4 c1;    // C, o, r, g
-    float4 c2;    // b
+    float4 c2;    // b, depth
 };
 
 // Per-warp slot storage.
 struct __align__(16) SlotRec {
     float mx, my, A, B;   // staged geometry of the slot's splat
     float C, o;
-    uint32_t idx, pad;
+    uint32_t idx;
+    float depth;
 };
 
-template <bool ACCUM, bool AOS>
+template <bool ACCUM, bool AOS, bool DIST>
 __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int lane, float wx0,
                                             float wy0, const float2 (*qw)[kSlotPad],
-                                            const float4 *g, const SlotRec *rec) {
+                                            const float4 *g, const float *gd1, const SlotRec *rec) {
     __syncwarp();
     // Every lane runs the sums (lanes of unused slots read stale, in-bounds
     // rows) so that the pair shuffles see the whole warp; only the atomics
@@ -119,7 +137,7 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
         // unrolled loop.  Raw moments in (k, v), then u = 2k + h and the
         // centring dx = u + ex, dy = v + ey.
         float M1 = 0.f, Mk = 0.f, Mkk = 0.f, Mv = 0.f, Mkv = 0.f, Mvv = 0.f;
-        float Wt = 0.f, Wr = 0.f, Wg = 0.f, Wb = 0.f;
+        float Wt = 0.f, Wr = 0.f, Wg = 0.f, Wb = 0.f, Wa = 0.f, Wd = 0.f;
         const float2 *row = qw[slot];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -142,6 +160,10 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
             Wr = fmaf(wi, gg.x, Wr);
             Wg = fmaf(wi, gg.y, Wg);
             Wb = fmaf(wi, gg.z, Wb);
+            if (DIST) {
+                Wa = fmaf(wi, gg.w, Wa);
+                Wd = fmaf(wi, gd1[pix], Wd);
+            }
         }
         const float hf = float(half);
         const float Mu = fmaf(2.0f, Mk, hf * M1);
@@ -165,6 +187,12 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
         Wr += __shfl_xor_sync(0xffffffffu, Wr, 1, 2);
         Wg += __shfl_xor_sync(0xffffffffu, Wg, 1, 2);
         Wb += __shfl_xor_sync(0xffffffffu, Wb, 1, 2);
+        float dz = 0.0f;
+        if (DIST) {
+            Wa += __shfl_xor_sync(0xffffffffu, Wa, 1, 2);
+            Wd += __shfl_xor_sync(0xffffffffu, Wd, 1, 2);
+            dz = 2.0f * fmaf(r.depth, Wa, -Wd);
+        }
         const size_t i = r.idx;
         const float dmx = kLn2 * (2.0f * r.A * Qx + r.B * Qy);
         const float dmy = kLn2 * (r.B * Qx + 2.0f * r.C * Qy);
@@ -176,7 +204,10 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
                 red_add_v4(g, dmx, dmy, 0.5f * Qxx, Qxy);
             } else {
                 red_add_v4(g + 4, 0.5f * Qyy, -Q / r.o, Wr, Wg);
-                atomicAdd(g + 8, Wb);
+                if (DIST)
+                    red_add_v2(g + 8, Wb, dz);
+                else
+                    atomicAdd(g + 8, Wb);
                 if (ACCUM)
                     atomicAdd(reinterpret_cast<unsigned long long *>(g + 10),
                               (unsigned long long)__float2ull_rn(Wt * 4294967296.0f));
@@ -198,7 +229,7 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
     __syncwarp();
 }
 
-template <bool ACCUM, bool AOS>
+template <bool ACCUM, bool AOS, bool DIST>
 __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     __shared__ SplatGeo s_geo_[2][256];
     __shared__ SplatGeo2 s_geo2_[2][256];
@@ -208,6 +239,7 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     __shared__ ChunkEnt s_ck[8][kChunk];
     __shared__ uint32_t s_wmax[8];
     __shared__ float4 s_g[8][32];
+    __shared__ float s_gd1[DIST ? 8 : 1][32];
     __shared__ SlotRec s_rec[8][kSlots];
     // dynamic: (q, w) slots, [8 warps][kSlots][kSlotPad] float2
     extern __shared__ __align__(16) float2 s_dyn[];
@@ -234,7 +266,15 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
         g1 = p.dL[HW + pix];
         g2 = p.dL[2 * HW + pix];
     }
-    s_g[warp][lane] = make_float4(g0, g1, g2, 0.0f);
+    // DIST: the pixel's distortion gradient and the forward's totals
+    float gD = 0.0f, dA = 0.0f, dD1 = 0.0f, dD2 = 0.0f, zref = 0.0f;
+    if (DIST && inside) {
+        gD = p.dL_ddist[pix];
+        const float4 t = p.dist_totals[pix];
+        dA = t.x, dD1 = t.y, dD2 = t.z, zref = t.w;
+    }
+    s_g[warp][lane] = make_float4(g0, g1, g2, gD * dA);
+    if (DIST) s_gd1[warp][lane] = gD * fmaf(zref, dA, dD1);
     // GR = dL/dimage . (S + T_final bg), S the colour blended behind the
     // current splat: with it dL/dalpha = (T gc - GR) / (1 - alpha), where
     // gc = dL/dimage . rgb and T is the transmittance behind the splat, and
@@ -346,8 +386,9 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                 //    the splat for the flush.
                 const int nrows = nq;
                 if (nslots + nrows > kSlots) {
-                    flush_slots<ACCUM, AOS>(p, nslots, lane, wx0, wy0, s_qw[warp], s_g[warp],
-                                            s_rec[warp]);
+                    flush_slots<ACCUM, AOS, DIST>(p, nslots, lane, wx0, wy0, s_qw[warp],
+                                                  s_g[warp], s_gd1[DIST ? warp : 0],
+                                                  s_rec[warp]);
                     nslots = 0;
                 }
                 for (int r = 0; r < nrows; ++r)
@@ -358,8 +399,9 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                     const SplatGeo2 g2 = s_geo2[j];
                     const SplatCol c = s_col[j];
                     s_ck[warp][lane] = ChunkEnt{g, make_float4(g2.C, g2.o, c.r, c.g),
-                                                make_float4(c.b, 0.f, 0.f, 0.f)};
-                    s_rec[warp][nslots + lane] = SlotRec{g.mx, g.my, g.A, g.B, g2.C, g2.o, c.idx, 0u};
+                                                make_float4(c.b, g2.depth, 0.f, 0.f)};
+                    s_rec[warp][nslots + lane] = SlotRec{g.mx, g.my, g.A, g.B, g2.C, g2.o, c.idx,
+                                                         g2.depth};
                 }
                 __syncwarp();
                 // 3. Each pixel walks only its own blended entries, back to front.
@@ -368,7 +410,7 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                     mine &= ~(1u << k);
                     const SplatGeo g = s_ck[warp][k].g;
                     const float4 c1 = s_ck[warp][k].c1;   // C, o, r, g
-                    const float cb_ = s_ck[warp][k].c2.x; // b
+                    const float4 c2 = s_ck[warp][k].c2;   // b, depth
                     float dx, dy;
                     const float e2 = eval_e2(g, c1.x, px, py, dx, dy);
                     const float G = ex2_approx(e2);
@@ -377,7 +419,11 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                     const float inv = rcp_approx(__fsub_rn(1.0f, alpha));
                     const float Ti = T * inv;  // T in front of this splat
                     const float wv = alpha * Ti;
-                    const float gc = fmaf(g0, c1.z, fmaf(g1, c1.w, g2 * cb_));
+                    float gc = fmaf(g0, c1.z, fmaf(g1, c1.w, g2 * c2.x));
+                    if (DIST) {
+                        const float z = c2.y - zref;
+                        gc = fmaf(gD, fmaf(z, fmaf(z, dA, -2.0f * dD1), dD2), gc);
+                    }
                     const float dLda = inv * fmaf(T, gc, -GR);
                     const float qv = oG <= kAlphaMax ? -alpha * dLda : 0.0f;  // capped: constant
                     GR = fmaf(wv, gc, GR);
@@ -391,8 +437,9 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
         }
     }
     cp_async_wait<0>();  // no copy may outlive the CTA
-    if (nslots) flush_slots<ACCUM, AOS>(p, nslots, lane, wx0, wy0, s_qw[warp], s_g[warp],
-                                        s_rec[warp]);
+    if (nslots)
+        flush_slots<ACCUM, AOS, DIST>(p, nslots, lane, wx0, wy0, s_qw[warp], s_g[warp],
+                                      s_gd1[DIST ? warp : 0], s_rec[warp]);
 }
 
 constexpr int kBwdDynSmem = 2 * 8 * kSlots * kSlotPad * 4;
@@ -404,10 +451,14 @@ static ss_status ensure_bwd_smem() {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && g_bwd_attr_set[dev]) return SS_OK;
-    const void *fns[4] = {(const void *)k_raster_bwd<true, true>, (const void *)k_raster_bwd<false, true>,
-                          (const void *)k_raster_bwd<true, false>, (const void *)k_raster_bwd<false, false>};
+    const void *fns[6] = {(const void *)k_raster_bwd<true, true, false>,
+                          (const void *)k_raster_bwd<false, true, false>,
+                          (const void *)k_raster_bwd<true, false, false>,
+                          (const void *)k_raster_bwd<false, false, false>,
+                          (const void *)k_raster_bwd<true, true, true>,
+                          (const void *)k_raster_bwd<false, true, true>};
     ss_status s = SS_OK;
-    for (int f = 0; f < 4 && s == SS_OK; ++f)
+    for (int f = 0; f < 6 && s == SS_OK; ++f)
         s = check_cuda(cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             kBwdDynSmem),
                        "ss_raster_bwd: cudaFuncSetAttribute");
@@ -453,6 +504,7 @@ __global__ void k_grad_final(BwdParams p, int64_t n, float *accum_out) {
         p.drgb[3 * i] = b.z;
         p.drgb[3 * i + 1] = b.w;
         p.drgb[3 * i + 2] = c.x;
+        if (p.ddepth) p.ddepth[i] = c.y;
         if (accum_out) {
             const unsigned long long w =
                 *reinterpret_cast<const unsigned long long *>(p.scratch + kGradRec * i + 10);
@@ -476,14 +528,21 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
                                    const uint32_t *tile_offsets, int64_t n_pairs, int32_t W,
                                    int32_t H, const float *bg, uint32_t flags, const float *T_final,
                                    const uint32_t *last_contrib, const uint32_t *blend_masks,
-                                   const float *dL_dimage,
+                                   const float *dL_dimage, const float *dist_totals,
+                                   const float *dL_ddist,
                                    const ss_grads *grads, float *accum_weight, void *workspace,
                                    size_t workspace_bytes, ss_stream_t stream) {
     clear_error();
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd: image %dx%d outside 1..%d", W, H, kMaxSide);
-    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS))
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: unknown flag bits 0x%x", flags);
+    const bool dist = flags & SS_DISTORTION;
+    if (dist && (!dist_totals || !dL_ddist))
+        return fail(SS_ERR_INVALID_ARG,
+                    "ss_raster_bwd: SS_DISTORTION set but dist_totals / dL_ddist NULL");
+    if (dist && (reinterpret_cast<uintptr_t>(dist_totals) & 15))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: dist_totals not 16-byte aligned");
     const int32_t n = n_splats;
     if (n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: n < 0");
     if (n > 0 && !records) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: records is NULL");
@@ -498,6 +557,8 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: blend_masks is NULL");
     if (!grads || (n > 0 && (!grads->dmean2d || !grads->dconic || !grads->dopacity || !grads->drgb)))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: a gradient array is NULL");
+    if (dist && n > 0 && !grads->ddepth)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: SS_DISTORTION set but grads->ddepth NULL");
     const bool accum = flags & SS_ACCUM_WEIGHT;
     if (accum && n > 0 && !accum_weight)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: SS_ACCUM_WEIGHT set but accum_weight NULL");
@@ -527,6 +588,9 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     p.dconic = grads->dconic;
     p.dopacity = grads->dopacity;
     p.drgb = grads->drgb;
+    p.ddepth = dist ? grads->ddepth : nullptr;
+    p.dist_totals = reinterpret_cast<const float4 *>(dist_totals);
+    p.dL_ddist = dL_ddist;
     p.accum = nullptr;
     p.scratch = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + L.accum);
     cudaStream_t st = (cudaStream_t)stream;
@@ -540,10 +604,14 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     SS_LAUNCH("k_grad_zero", st,
               k_grad_zero<<<zgrid, 256, 0, st>>>(reinterpret_cast<float4 *>(p.scratch), 3 * int64_t(n)));
     const int grid = tiles_x(W) * tiles_y(H);
-    if (accum)
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true, true><<<grid, 256, kBwdDynSmem, st>>>(p));
+    if (accum && dist)
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, true, true><<<grid, 256, kBwdDynSmem, st>>>(p)));
+    else if (dist)
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, true, true><<<grid, 256, kBwdDynSmem, st>>>(p)));
+    else if (accum)
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, true, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
     else
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false, true><<<grid, 256, kBwdDynSmem, st>>>(p));
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, true, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
     SS_LAUNCH("k_grad_final", st,
               k_grad_final<<<zgrid, 256, 0, st>>>(p, n, accum ? accum_weight : nullptr));
     return check_launch("ss_raster_bwd");
@@ -588,8 +656,11 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd_noalloc: image %dx%d outside 1..%d", W, H,
                     kMaxSide);
-    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS))
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: unknown flag bits 0x%x", flags);
+    if (flags & SS_DISTORTION)
+        return fail(SS_ERR_UNSUPPORTED,
+                    "ss_raster_bwd_noalloc: SS_DISTORTION needs ss_raster_bwd");
     const int32_t n = n_splats;
     if (n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: n < 0");
     if (n > kNoAllocMaxSplats)
@@ -660,9 +731,9 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     SS_LAUNCH("k_bwd_zero", st, k_bwd_zero<<<zgrid, 256, 0, st>>>(p, n, accum));
     const int grid = tiles_x(W) * tiles_y(H);
     if (accum)
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<true, false><<<grid, 256, kBwdDynSmem, st>>>(p));
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, false, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
     else
-        SS_LAUNCH("k_raster_bwd", st, k_raster_bwd<false, false><<<grid, 256, kBwdDynSmem, st>>>(p));
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, false, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
     if (accum)
         SS_LAUNCH("k_accum_final", st, k_accum_final<<<zgrid, 256, 0, st>>>(p.accum, accum_weight, n));
     return check_launch("ss_raster_bwd_noalloc");

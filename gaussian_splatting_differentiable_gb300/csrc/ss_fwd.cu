@@ -18,6 +18,15 @@
 // number of blending pixels (the mask's popcount), and adds them to the
 // splat's statistics with one atomicMax and one atomicAdd.
 //
+// With SS_DISTORTION (the DIST variant) each pixel also keeps running totals
+// of its blended splats' weights and depths, A = sum w, D1 = sum w z',
+// D2 = sum w z'^2, with z' = z - z_ref the depth relative to the first
+// blended splat (the distortion does not change when every depth shifts, and
+// the shift keeps the float32 terms small), and adds w (z'^2 A - 2 z' D1 + D2)
+// -- the new splat's pairs with every splat in front -- to its depth
+// distortion sum_{i<j} w_i w_j (z_i - z_j)^2.  It writes the distortion and
+// the totals (A, D1, D2, z_ref), which the backward reads.
+//
 // The warp also records, for each pair it reached, which of its 32 pixels
 // blended the splat (a ballot): blend_masks[b * n_pairs + p], b = warp.
 // The backward reads these decisions instead of re-evaluating every
@@ -44,9 +53,11 @@ struct FwdParams {
     float *median;
     uint32_t *max_w_bits;  // [n] float bits of the max blend weight (STATS)
     uint32_t *count;       // [n] blending pixels (STATS)
+    float *dist;           // [H][W] depth distortion (DIST)
+    float4 *dist_totals;   // [H][W] (A, D1, D2, z_ref) (DIST)
 };
 
-template <bool MEDIAN, bool STATS>
+template <bool MEDIAN, bool STATS, bool DIST>
 __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
     __shared__ SplatGeo s_geo[2][256];
     __shared__ SplatGeo2 s_geo2[2][256];
@@ -69,6 +80,7 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
     const uint32_t lt = lanemask_lt();
 
     float T = 1.0f, cr = 0.0f, cg = 0.0f, cb = 0.0f, med = 0.0f;
+    float dA = 0.0f, dD1 = 0.0f, dD2 = 0.0f, dD = 0.0f, zref = 0.0f;
     uint32_t last = 0;
     bool done = !inside;
 
@@ -134,6 +146,14 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
                     cg = fmaf(c.g, w, cg);
                     cb = fmaf(c.b, w, cb);
                     if (MEDIAN && T > 0.5f) med = g2.depth;
+                    if (DIST) {
+                        if (dA == 0.0f) zref = g2.depth;   // first blend: w > 0 always
+                        const float z = g2.depth - zref;
+                        dD = fmaf(w, fmaf(z, fmaf(z, dA, -2.0f * dD1), dD2), dD);
+                        dA += w;
+                        dD1 = fmaf(w, z, dD1);
+                        dD2 = fmaf(w * z, z, dD2);
+                    }
                     T = Tn;
                     last = base - start + uint32_t(j) + 1u;
                 }
@@ -164,7 +184,16 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
         p.T_final[pix] = T;
         p.last[pix] = last;
         if (MEDIAN) p.median[pix] = med;
+        if (DIST) {
+            p.dist[pix] = dD;
+            p.dist_totals[pix] = make_float4(dA, dD1, dD2, zref);
+        }
     }
+}
+
+template <bool MEDIAN, bool STATS, bool DIST>
+static void launch_fwd(const FwdParams &p, int grid, cudaStream_t st) {
+    SS_LAUNCH("k_raster_fwd", st, (k_raster_fwd<MEDIAN, STATS, DIST><<<grid, 256, 0, st>>>(p)));
 }
 
 }  // namespace ss
@@ -176,12 +205,19 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
                                    int32_t H, const float *bg, uint32_t flags, float *image,
                                    float *T_final, uint32_t *last_contrib, float *median_depth,
                                    uint32_t *blend_masks, float *max_weight,
-                                   uint32_t *blend_count, ss_stream_t stream) {
+                                   uint32_t *blend_count, float *distortion, float *dist_totals,
+                                   ss_stream_t stream) {
     clear_error();
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_fwd: image %dx%d outside 1..%d", W, H, kMaxSide);
-    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS))
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: unknown flag bits 0x%x", flags);
+    const bool dist = flags & SS_DISTORTION;
+    if (dist && (!distortion || !dist_totals))
+        return fail(SS_ERR_INVALID_ARG,
+                    "ss_raster_fwd: SS_DISTORTION set but distortion / dist_totals NULL");
+    if (dist && (reinterpret_cast<uintptr_t>(dist_totals) & 15))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: dist_totals not 16-byte aligned");
     const bool stats = flags & SS_WEIGHT_STATS;
     if (stats && n_splats > 0 && (!max_weight || !blend_count))
         return fail(SS_ERR_INVALID_ARG,
@@ -217,6 +253,8 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
     p.n_pairs = n_pairs;
     p.max_w_bits = reinterpret_cast<uint32_t *>(max_weight);
     p.count = blend_count;
+    p.dist = distortion;
+    p.dist_totals = reinterpret_cast<float4 *>(dist_totals);
     const int grid = tiles_x(W) * tiles_y(H);
     cudaStream_t st = (cudaStream_t)stream;
     if (stats && n_splats > 0) {
@@ -227,13 +265,15 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
                            "ss_raster_fwd: memset");
         if (s != SS_OK) return s;
     }
-    if (median && stats)
-        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<true, true><<<grid, 256, 0, st>>>(p));
-    else if (median)
-        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<true, false><<<grid, 256, 0, st>>>(p));
-    else if (stats)
-        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<false, true><<<grid, 256, 0, st>>>(p));
-    else
-        SS_LAUNCH("k_raster_fwd", st, k_raster_fwd<false, false><<<grid, 256, 0, st>>>(p));
+    switch ((median ? 4 : 0) | (stats ? 2 : 0) | (dist ? 1 : 0)) {
+        case 0: launch_fwd<false, false, false>(p, grid, st); break;
+        case 1: launch_fwd<false, false, true>(p, grid, st); break;
+        case 2: launch_fwd<false, true, false>(p, grid, st); break;
+        case 3: launch_fwd<false, true, true>(p, grid, st); break;
+        case 4: launch_fwd<true, false, false>(p, grid, st); break;
+        case 5: launch_fwd<true, false, true>(p, grid, st); break;
+        case 6: launch_fwd<true, true, false>(p, grid, st); break;
+        default: launch_fwd<true, true, true>(p, grid, st); break;
+    }
     return check_launch("ss_raster_fwd");
 }

@@ -68,9 +68,12 @@ typedef enum {
 enum {
     SS_ACCUM_WEIGHT = 1u,  /* bwd: per-splat accumulated blend weight sum_p alpha T */
     SS_MEDIAN_DEPTH = 2u,  /* fwd: per-pixel depth of the last splat blended while T > 0.5 */
-    SS_WEIGHT_STATS = 4u   /* fwd: per-splat max blend weight and blending-pixel count
+    SS_WEIGHT_STATS = 4u,  /* fwd: per-splat max blend weight and blending-pixel count
                               ("max wt" and, with the accumulated weight, the "Avg"
                               weight of the Spirula Studio write-up, 机制拆解 / 亲手验证) */
+    SS_DISTORTION = 8u     /* fwd: per-pixel depth distortion and its totals; bwd: its
+                              gradient, including dL/ddepth (the write-up's distortion
+                              option with per-pixel float4 totals, 最小改动) */
 };
 
 /* Splats, structure of arrays, float32, device memory.  The pages' inputs:
@@ -92,6 +95,7 @@ typedef struct {
     float *dconic;         /* [n][3] */
     float *dopacity;       /* [n] */
     float *drgb;           /* [n][3] */
+    float *ddepth;         /* [n], only with SS_DISTORTION (else may be NULL) */
 } ss_grads;
 
 /* Version of this ABI (incremented on any change of a signature). */
@@ -194,6 +198,14 @@ ss_status ss_sort_status(const void *workspace, ss_stream_t stream);
  *   median_depth[H][W]  only with SS_MEDIAN_DEPTH (else may be NULL): depth
  *                       of the last splat blended while T > 0.5, 0 if none
  *   bg: HOST float[3] background, or NULL for black.
+ *   distortion, dist_totals: only with SS_DISTORTION (else may be NULL):
+ *                device float [H][W] and float4 [H][W] (16-byte aligned),
+ *                overwritten with each pixel's depth distortion
+ *                D = sum over pairs i < j of its blended splats of
+ *                w_i w_j (z_i - z_j)^2 (w = alpha T, z = depth), and with the
+ *                running totals (A = sum w, D1 = sum w z', D2 = sum w z'^2,
+ *                z_ref), z' = z - z_ref, z_ref the first blended splat's depth,
+ *                which the backward reads.
  *   max_weight, blend_count: only with SS_WEIGHT_STATS (else may be NULL):
  *                device float[n] / uint32[n], overwritten with, per splat, the
  *                maximum over pixels of alpha T and the number of pixels that
@@ -216,7 +228,8 @@ ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *v
                         const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,
                         const float *bg, uint32_t flags, float *image, float *T_final,
                         uint32_t *last_contrib, float *median_depth, uint32_t *blend_masks,
-                        float *max_weight, uint32_t *blend_count, ss_stream_t stream);
+                        float *max_weight, uint32_t *blend_count, float *distortion,
+                        float *dist_totals, ss_stream_t stream);
 
 /* Backward rasterization ("从 8.6 KB 到 4.2 KB ...", rasterize_bwd_2d on the
  * 2D screen-space path; "Phase 5 step 30b", rasterize_backwards: the 9-field
@@ -240,7 +253,14 @@ ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *v
  *   T_final, last_contrib, blend_masks: from ss_raster_fwd with the same
  *   inputs (the blend decisions are the forward's, not re-evaluated).
  *   dL_dimage: device float[3][H][W].
- *   grads: all four arrays required; overwritten (zeroed here first).
+ *   dist_totals, dL_ddist: only with SS_DISTORTION (else may be NULL): the
+ *   forward's totals and the upstream gradient of its distortion image,
+ *   device float [H][W]; L then also has the term sum dL/ddist * D, which
+ *   adds, with E_k = dD/dw_k = sum_j w_j (z_k - z_j)^2,
+ *     dL/dalpha_k += dL/ddist (E_k T_k - sum_{i after k} w_i E_i / (1 - alpha_k))
+ *     dL/ddepth_k  = dL/ddist 2 w_k sum_j w_j (z_k - z_j)   (grads->ddepth).
+ *   grads: the four 2D arrays required (and ddepth with SS_DISTORTION);
+ *   overwritten (zeroed here first).
  *   accum_weight: with SS_ACCUM_WEIGHT, device float[n] overwritten with
  *   sum over pixels of alpha T (summed exactly in 32.32 fixed point, so the
  *   result does not depend on the order of the atomics); else may be NULL.
@@ -251,8 +271,9 @@ ss_status ss_raster_bwd(const void *records, int32_t n_splats, const uint32_t *v
                         const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,
                         const float *bg, uint32_t flags, const float *T_final,
                         const uint32_t *last_contrib, const uint32_t *blend_masks,
-                        const float *dL_dimage, const ss_grads *grads, float *accum_weight,
-                        void *workspace, size_t workspace_bytes, ss_stream_t stream);
+                        const float *dL_dimage, const float *dist_totals, const float *dL_ddist,
+                        const ss_grads *grads, float *accum_weight, void *workspace,
+                        size_t workspace_bytes, ss_stream_t stream);
 
 /* The backward pass for callers that cannot allocate (the pages have no
  * counterpart: this is a property of the library, not of the method).
@@ -266,6 +287,7 @@ ss_status ss_raster_bwd(const void *records, int32_t n_splats, const uint32_t *v
  * 2,097,152 splats (16 MiB), which every GPU that loads the library holds
  * until the process exits.
  *   - n_splats > 2,097,152 returns SS_ERR_UNSUPPORTED (use ss_raster_bwd).
+ *   - SS_DISTORTION returns SS_ERR_UNSUPPORTED (use ss_raster_bwd).
  *   - The first call on a device, made with that device current, looks up
  *     the array's device address (cudaGetSymbolAddress); make that first
  *     call before any stream capture.

@@ -3,6 +3,10 @@
 Tolerances (the rasterizer's stated bar):
   * pairs (as a multiset), sorted keys/values, tile offsets: bit-exact;
   * image, T_final: 1e-5 absolute; last_contrib and median depth: exact;
+  * depth distortion: max(1e-5, e_D), e_D the oracle's bound on a float32
+    evaluation by running totals (the totals' terms z'^2 A, z' D1, D2 are
+    large next to their difference when depths are far apart); dL/ddepth
+    under the gradient bar below;
   * per-splat max blend weight: 1e-5 absolute; blending-pixel count: exact
     (splats blended at a knife-edge pixel in some outcome are skipped);
   * gradients: max(1e-4, 1e-3 * max|field|) per element, field = one of
@@ -24,12 +28,14 @@ import oracle
 import gaussian_splatting_differentiable_gb300 as ss
 
 GRAD_FIELDS = ("dmean2d", "dconic", "dopacity", "drgb")
+DIST_FIELD = "ddepth"
 
 
 def flags_of(scene) -> int:
     return (ss.SS_ACCUM_WEIGHT if scene.accum_weight else 0) | \
         (ss.SS_MEDIAN_DEPTH if scene.median_depth else 0) | \
-        (ss.SS_WEIGHT_STATS if getattr(scene, "weight_stats", False) else 0)
+        (ss.SS_WEIGHT_STATS if getattr(scene, "weight_stats", False) else 0) | \
+        (ss.SS_DISTORTION if getattr(scene, "distortion", False) else 0)
 
 
 def run_gpu(scene, capacity=None, stream=None):
@@ -58,14 +64,17 @@ def run_gpu(scene, capacity=None, stream=None):
     out["offs"] = r.tile_offsets.cpu().numpy().view(np.uint32).copy()
     r.forward(sp, stream)
     dL = torch.from_numpy(scene.dL_dimage).to(dev).contiguous()
-    r.backward(sp, dL, stream)
+    dLd = (torch.from_numpy(scene.dL_ddist).to(dev).contiguous()
+           if flags & ss.SS_DISTORTION else None)
+    r.backward(sp, dL, stream, dLd)
     torch.cuda.synchronize()
     out["image"] = r.image.cpu().numpy()
     out["T_final"] = r.T_final.cpu().numpy()
     out["last"] = r.last_contrib.cpu().numpy().view(np.uint32)
     out["median"] = r.median_depth.cpu().numpy() if r.median_depth is not None else None
-    for k in GRAD_FIELDS:
-        out[k] = r.grads[k].cpu().numpy()
+    out["dist"] = r.distortion.cpu().numpy() if r.distortion is not None else None
+    for k in GRAD_FIELDS + (DIST_FIELD,):
+        out[k] = r.grads[k].cpu().numpy() if k in r.grads else None
     out["accum"] = r.accum_weight.cpu().numpy() if r.accum_weight is not None else None
     out["max_w"] = r.max_weight.cpu().numpy() if r.max_weight is not None else None
     out["bcount"] = (r.blend_count.cpu().numpy().view(np.uint32)
@@ -101,6 +110,12 @@ def check_forward(scene, gpu, ofw, pixel_mask=None, atol=1e-5):
     bad = clean & ((img_err > atol) | (T_err > atol) | (gpu["last"] != ofw["last"]))
     if gpu["median"] is not None:
         bad |= clean & (gpu["median"] != ofw["median"].astype(np.float32))
+    dist_tol = np.maximum(atol, ofw["dist_err"])
+    if gpu.get("dist") is not None:
+        dist_err = np.abs(gpu["dist"] - ofw["dist"])
+        bad_d = clean & (dist_err > dist_tol)
+        assert not bad_d.any(), "distortion: %d pixels off; worst err %.3g (tol %.3g)" % (
+            bad_d.sum(), dist_err[bad_d].max(), dist_tol[bad_d][np.argmax(dist_err[bad_d])])
     assert not bad.any(), _describe_bad(bad, gpu, ofw, img_err, T_err)
     # knife edges: the GPU must take the normal outcome or one alternative
     amb = np.argwhere(sel & (ofw["n_amb"] > 0))
@@ -109,14 +124,16 @@ def check_forward(scene, gpu, ofw, pixel_mask=None, atol=1e-5):
     for (y, x) in amb:
         p = y * W + x
         cands = [(ofw["image"][:, y, x], ofw["T_final"][y, x], ofw["last"][y, x],
-                  ofw["median"][y, x])]
+                  ofw["median"][y, x], ofw["dist"][y, x])]
         for a in alts[alts["pixel"] == p]:
-            cands.append((a["image"], a["T_final"], a["last"], a["median"]))
+            cands.append((a["image"], a["T_final"], a["last"], a["median"], a["dist"]))
         ok = False
-        for im, T, last, med in cands:
+        for im, T, last, med, dd in cands:
             if (np.abs(gpu["image"][:, y, x] - im).max() <= atol and abs(gpu["T_final"][y, x] - T) <= atol
                     and gpu["last"][y, x] == last
-                    and (gpu["median"] is None or gpu["median"][y, x] == np.float32(med))):
+                    and (gpu["median"] is None or gpu["median"][y, x] == np.float32(med))
+                    and (gpu.get("dist") is None
+                         or abs(gpu["dist"][y, x] - dd) <= 2 * dist_tol[y, x])):
                 ok = True
                 break
         unmatched += not ok
@@ -157,7 +174,8 @@ def check_backward(scene, gpu, obw, splat_mask=None):
     g = obw["grads"]
     sl = obw["slack"]
     report = {}
-    for k in GRAD_FIELDS:
+    fields = GRAD_FIELDS + ((DIST_FIELD,) if gpu.get(DIST_FIELD) is not None else ())
+    for k in fields:
         ref = g[k].reshape(n, -1)
         got = gpu[k].reshape(n, -1).astype(np.float64)
         slack = sl[k].reshape(n, -1) if sl is not None else 0.0
@@ -181,13 +199,17 @@ def check_backward(scene, gpu, obw, splat_mask=None):
     return report
 
 
+def _dist_grad(scene):
+    return scene.dL_ddist if getattr(scene, "distortion", False) else None
+
+
 def full_parity(scene, capacity=None):
     gpu = run_gpu(scene, capacity)
     tl = check_pairs(scene, gpu)
     ofw = oracle.forward(scene, tl["vals"], tl["offs"], alt_capacity=1 << 20)
     f = check_forward(scene, gpu, ofw)
     s = check_weight_stats(scene, gpu, ofw)
-    obw = oracle.backward(scene, tl["vals"], tl["offs"])
+    obw = oracle.backward(scene, tl["vals"], tl["offs"], dL_ddist=_dist_grad(scene))
     b = check_backward(scene, gpu, obw)
     return {"fwd": f, "stats": s, "bwd": b, "pairs": tl["count"]}
 
@@ -213,7 +235,8 @@ def sampled_parity(scene, n_tiles=192, n_splats=256, seed=0):
     smask[pick] = True
     tmask = np.zeros(T, np.uint8)
     tmask[(keys[smask[vals]] >> np.uint64(32)).astype(np.int64)] = 1
-    obw = oracle.backward(scene, tl["vals"], tl["offs"], tile_mask=tmask)
+    obw = oracle.backward(scene, tl["vals"], tl["offs"], tile_mask=tmask,
+                          dL_ddist=_dist_grad(scene))
     b = check_backward(scene, gpu, obw, splat_mask=smask)
     s = None
     if gpu["max_w"] is not None:

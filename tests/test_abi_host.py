@@ -56,7 +56,7 @@ def test_constants_match_oracle(lib):
     assert buf[1] == np.float32(c["alpha_max"])
     assert buf[2] == np.float32(c["T_eps"])
     assert buf[3] == c["tile"]
-    assert lib.ss_abi_version() == 3
+    assert lib.ss_abi_version() == 4
 
 
 def test_workspace_bytes(lib):
@@ -93,32 +93,43 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert lib.ss_sort_pairs(0x1000, 0x1000, 10, 16, 16, 0x1000, 0x1001, 1 << 30, None) == 1
     assert lib.ss_sort_pairs(0x1000, 0x1000, 10, 16, 16, 0x1000, 0x1000, 16, None) == 1
     assert "workspace" in lib.ss_last_error().decode()
-    # forward: unknown flags, NULL outputs, median flag without buffer
-    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 8, 0x1000, 0x1000,
-                             0x1000, None, 0x1000, None, None, None) == 1
-    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 0, None, 0x1000,
-                             0x1000, None, 0x1000, None, None, None) == 1
-    assert lib.ss_raster_fwd(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 2, 0x1000, 0x1000,
-                             0x1000, None, 0x1000, None, None, None) == 1
-    assert lib.ss_raster_fwd(None, 5, 0x1000, 0x1000, 0, 16, 16, None, 0, 0x1000, 0x1000,
-                             0x1000, None, 0x1000, None, None, None) == 1
-    assert lib.ss_raster_fwd(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 0, 0x1000, 0x1000,
-                             0x1000, None, None, None, None, None) == 1   # blend_masks NULL
-    assert lib.ss_raster_fwd(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 4, 0x1000, 0x1000,
-                             0x1000, None, 0x1000, None, None, None) == 1   # stats outputs NULL
-    # backward: NULL gradient array, accum flag without buffer or workspace
-    g = SsGrads(0x1000, None, 0x1000, 0x1000)
-    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 0, 0x1000, 0x1000,
-                             0x1000, 0x1000, ctypes.byref(g), None, None, 0, None) == 1
-    g = SsGrads(0x1000, 0x1000, 0x1000, 0x1000)
-    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 1, 0x1000, 0x1000,
-                             0x1000, 0x1000, ctypes.byref(g), None, 0x1000, 1 << 20, None) == 1
-    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 1, 0x1000, 0x1000,
-                             0x1000, 0x1000, ctypes.byref(g), 0x1000, 0x1000, 8, None) == 1
-    assert lib.ss_raster_bwd(None, 4, 0x1000, 0x1000, 8, 16, 16, None, 0, 0x1000, 0x1000,
-                             0x1000, 0x1000, ctypes.byref(g), None, None, 0, None) == 1
-    assert lib.ss_raster_bwd(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 0, 0x1000, 0x1000,
-                             None, 0x1000, ctypes.byref(g), None, None, 0, None) == 1
+    # forward: unknown flags, NULL outputs, median / stats / distortion flag without buffers
+    F = lambda *a: lib.ss_raster_fwd(*a)  # noqa: E731
+    assert F(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 16, 0x1000, 0x1000, 0x1000, None, 0x1000,
+             None, None, None, None, None) == 1
+    assert F(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 0, None, 0x1000, 0x1000, None, 0x1000,
+             None, None, None, None, None) == 1
+    assert F(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 2, 0x1000, 0x1000, 0x1000, None, 0x1000,
+             None, None, None, None, None) == 1
+    assert F(None, 5, 0x1000, 0x1000, 0, 16, 16, None, 0, 0x1000, 0x1000, 0x1000, None, 0x1000,
+             None, None, None, None, None) == 1
+    assert F(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 0, 0x1000, 0x1000, 0x1000, None, None,
+             None, None, None, None, None) == 1   # blend_masks NULL
+    assert F(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 4, 0x1000, 0x1000, 0x1000, None, 0x1000,
+             None, None, None, None, None) == 1   # stats outputs NULL
+    assert F(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 8, 0x1000, 0x1000, 0x1000, None, 0x1000,
+             None, None, 0x1000, None, None) == 1   # distortion totals NULL
+    assert F(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 8, 0x1000, 0x1000, 0x1000, None, 0x1000,
+             None, None, 0x1000, 0x1008, None) == 1   # totals not 16-byte aligned
+    assert "aligned" in lib.ss_last_error().decode()
+    # backward: NULL gradient array, accum flag without buffer or workspace, distortion inputs
+    B = lambda flags, g, ws=None, nbytes=0, acc=None, dt=None, dd=None, rec=0x1000, masks=0x1000: \
+        lib.ss_raster_bwd(rec, 4, 0x1000, 0x1000, 8, 16, 16, None, flags, 0x1000, 0x1000, masks,
+                          0x1000, dt, dd, ctypes.byref(g), acc, ws, nbytes, None)  # noqa: E731
+    g = SsGrads(0x1000, None, 0x1000, 0x1000, None)
+    assert B(0, g) == 1
+    g = SsGrads(0x1000, 0x1000, 0x1000, 0x1000, None)
+    assert B(1, g, ws=0x1000, nbytes=1 << 20) == 1            # accum without buffer
+    assert B(1, g, ws=0x1000, nbytes=8, acc=0x1000) == 1      # small workspace
+    assert B(0, g, rec=None) == 1
+    assert B(0, g, masks=None) == 1
+    assert B(16, g, ws=0x1000, nbytes=1 << 20) == 1           # unknown flag
+    assert B(8, g, ws=0x1000, nbytes=1 << 20, dt=0x1000) == 1   # dL_ddist NULL
+    assert B(8, g, ws=0x1000, nbytes=1 << 20, dt=0x1008, dd=0x1000) == 1   # misaligned totals
+    assert B(8, g, ws=0x1000, nbytes=1 << 20, dt=0x1000, dd=0x1000) == 1   # ddepth NULL
+    assert "ddepth" in lib.ss_last_error().decode()
+    assert lib.ss_raster_bwd_noalloc(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 8, 0x1000,
+                                     0x1000, 0x1000, 0x1000, ctypes.byref(g), None, None) == 5
     # pair count / sort status with NULL
     assert lib.ss_pair_count(None, 0, None, None, None) == 1
     assert lib.ss_sort_status(None, None) == 1

@@ -1,11 +1,12 @@
 """Parity of the CUDA path against the CPU oracle on the GPU (through the C ABI).
 
-Workloads 1-3 are compared in full; the two 2M-splat workloads at their full
+Workloads 1-3 are compared in full; the 2M-splat workloads (4-6) at their full
 size and launch configuration on every pair, the sorted order, the offsets,
-the forward on sampled tiles and the gradients of sampled splats.  Edge cases
-cover empty and culled inputs, ragged and tiny images, huge and off-screen
-splats, equal depths, dense tiles, the alpha cap, a background, every flag
-variant and the pair-capacity overflow path.
+the forward on sampled tiles and the gradients of sampled splats (workload 6
+adds the depth distortion).  Edge cases cover empty and culled inputs, ragged
+and tiny images, huge and off-screen splats, equal depths, dense tiles, the
+alpha cap, a background, every combination of the four flags and the
+pair-capacity overflow path.
 """
 import numpy as np
 import pytest
@@ -30,10 +31,17 @@ def test_workload_full_parity(P, wl):
     print("workload", wl, r)
 
 
-@pytest.mark.parametrize("wl", [4, 5])
+@pytest.mark.parametrize("wl", [4, 5, 6])
 def test_workload_full_size_sampled_parity(P, wl):
     r = P.sampled_parity(synth.make_scene(wl))
     print("workload", wl, r)
+
+
+def test_workload_3_with_distortion(P):
+    sc = synth.make_scene(3)
+    sc.distortion = True
+    r = P.full_parity(sc)
+    print("workload 3 + distortion", r)
 
 
 def _scene(W, H, n, seed=0, wl=1, **over):
@@ -111,17 +119,30 @@ def test_alpha_cap_and_background(P):
     P.full_parity(sc)
 
 
-@pytest.mark.parametrize("accum,median,stats", [(False, False, False), (True, False, False),
-                                                (False, True, False), (True, True, False),
-                                                (False, False, True), (True, False, True),
-                                                (False, True, True), (True, True, True)])
-def test_flag_variants(P, accum, median, stats):
+@pytest.mark.parametrize("flags", range(16))
+def test_flag_variants(P, flags):
+    """Every combination of accumulated weight, median depth, weight
+    statistics and distortion."""
+    accum, median, stats, dist = [bool(flags >> k & 1) for k in range(4)]
     sc = _scene(96, 80, 500, seed=9, wl=2)
-    sc.accum_weight, sc.median_depth, sc.weight_stats = accum, median, stats
+    sc.accum_weight, sc.median_depth, sc.weight_stats, sc.distortion = accum, median, stats, dist
     r = P.full_parity(sc)
     assert (r["stats"] is not None) == stats
+    assert ("ddepth" in r["bwd"]) == dist
     if stats:
         assert r["stats"]["blended"] > 100
+
+
+def test_distortion_dense_tile_and_far_depths(P):
+    """3,000 splats on one tile with depths over [1, 100]: long per-pixel
+    lists and totals whose terms are far larger than the distortion."""
+    sc = _scene(16, 16, 3000, seed=12)
+    sc.opacity[:] = np.float32(0.02)
+    sc.depth[:] = np.float32(1.0) + np.float32(99.0) * np.random.default_rng(3).random(
+        sc.n).astype(np.float32)
+    sc.distortion = True
+    sc.dL_ddist = np.random.default_rng(4).normal(0, 1e-5, (sc.H, sc.W)).astype(np.float32)
+    P.full_parity(sc)
 
 
 def test_weight_stats_with_dense_overlap(P):
