@@ -300,6 +300,48 @@ def measure_ssim(ss, dev, flush, steps: int, hbm: float, hbm_src: str) -> dict:
                                         "gradient 4 written"}}
 
 
+def measure_distortion(ss, dev, flush, steps: int) -> dict:
+    """The step with the depth-distortion variant (accumulated weight +
+    distortion) on the 2M-splat 1237x822 scene, as a CUDA graph, L2 flushed
+    before each replay; per-kernel times from a second, profiled pass."""
+    import torch
+    import synth
+    sc = synth.make_scene(6)
+    flags = ss.SS_ACCUM_WEIGHT | ss.SS_DISTORTION
+    sp = ss.Splats.from_numpy(sc, dev)
+    dL = torch.from_numpy(sc.dL_dimage).to(dev).contiguous()
+    dLd = torch.from_numpy(sc.dL_ddist).to(dev).contiguous()
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, int(2.5 * sc.n), flags, bg=sc.bg, device=dev)
+    r.step(sp, dL, dL_ddist=dLd)
+    g = r.capture(sp, dL, dL_ddist=dLd)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    r.check()
+    stream = torch.cuda.current_stream()
+    ev = []
+    for k in range(steps):
+        flush.fill_(float(k))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    ss.ss_profile_collect()
+    ss.ss_profile_enable(True)
+    for k in range(steps):
+        flush.fill_(float(k))
+        r.step_async(sp, dL, dL_ddist=dLd)
+    torch.cuda.synchronize()
+    ss.ss_profile_enable(False)
+    prof = ss.ss_profile_collect()
+    r.check()
+    return {"workload": synth.WORKLOADS[6].name, "flags": "accum_weight + distortion",
+            "ms_per_step": statistics.mean(a.elapsed_time(b) for a, b in ev),
+            "kernels_ms_per_call": {k: v[1] / v[0] for k, v in prof.items()}}
+
+
 def run_ours(args, rank: int, world: int, dist):
     import torch
     try:
@@ -456,6 +498,7 @@ def run_ours(args, rank: int, world: int, dist):
                                                         hbm_src + " (MEASURED_PEAKS.json hbm_gbs)")
         next_rows["f4_ssim"] = measure_ssim(ss, dev, flush, args.steps, hbm,
                                             hbm_src + " (MEASURED_PEAKS.json hbm_gbs)")
+        next_rows["f2_distortion"] = measure_distortion(ss, dev, flush, args.steps)
 
     # --- end to end through the public API with host buffers
     e2e = None

@@ -14,8 +14,8 @@
 // writes dL/dimage.  HBM traffic is the two input images once (plus the
 // halo, which neighbouring CTAs read from L2) and the gradient once: 12 bytes
 // a pixel and channel.  Per-CTA partial sums of SSIM and |x - y| go to the
-// workspace in double; one small kernel adds them in a fixed order, so the
-// loss is deterministic.
+// workspace in double; the last CTA to finish (a ticket counter) adds them
+// in block order, so the loss is deterministic.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -30,8 +30,9 @@ namespace {
 
 constexpr int kT = 32;               // output tile side
 constexpr int kR = 3;                // window radius
+constexpr int kW = 2 * kR + 1;       // window taps
 constexpr int kIn = kT + 4 * kR;     // 44: input region side
-constexpr int kMom = kT + 2 * kR;    // 38: moment / adjoint region side
+constexpr int kMom = kT + 2 * kR;    // 38: statistics / adjoint region side
 constexpr int kThreads = 256;
 constexpr float kC1 = 0.01f * 0.01f;
 constexpr float kC2 = 0.03f * 0.03f;
@@ -40,10 +41,14 @@ struct SsimParams {
     const float *img, *tgt;
     float *grad;
     double2 *partial;    // [blocks] (sum SSIM, sum |x - y|)
-    int C, H, W, tiles_x;
-    float g[2 * kR + 1];
+    unsigned int *ticket;
+    float *out;          // (loss, mean SSIM, mean |x - y|)
+    int C, H, W, n_blocks;
+    float g[kW];
     float cs;            // dL/dSSIM(p) = -lambda / N
     float cl;            // dL/d|x - y| = (1 - lambda) / N
+    float lambda;
+    double inv_n;
 };
 
 struct SsimSmem {
@@ -52,6 +57,7 @@ struct SsimSmem {
     float h[5][kIn][kMom];   // horizontal pass: moments, then the adjoint maps
     float a[3][kMom][kMom];  // adjoint maps on the moment region
     double red[2][kThreads / 32];
+    int last;
 };
 
 __global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
@@ -154,7 +160,7 @@ __global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
         l1_sum += fabsf(d);
     }
 
-    // per-CTA partial sums, in double, in a fixed order
+    // per-CTA partial sums in double, then the last CTA adds them in order
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         ssim_sum += __shfl_xor_sync(0xffffffffu, ssim_sum, o);
@@ -167,28 +173,33 @@ __global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
         for (int w = 0; w < kThreads / 32; ++w) a += s.red[0][w], b += s.red[1][w];
         const int blk = (c * gridDim.y + ty) * gridDim.x + tx;
         p.partial[blk] = make_double2(a, b);
+        __threadfence();
+        s.last = atomicAdd(p.ticket, 1u) == unsigned(p.n_blocks - 1);
     }
-}
-
-__global__ void __launch_bounds__(1024) k_ssim_final(const double2 *partial, int n_blocks,
-                                                     double inv_n, float lambda, float *out) {
-    __shared__ double red[2][32];
+    __syncthreads();
+    if (!s.last) return;
+    __threadfence();
     double a = 0.0, b = 0.0;
-    for (int k = threadIdx.x; k < n_blocks; k += blockDim.x) a += partial[k].x, b += partial[k].y;
+    for (int k = tid; k < p.n_blocks; k += kThreads) {
+        const double2 v = __ldcg(p.partial + k);
+        a += v.x, b += v.y;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         a += __shfl_xor_sync(0xffffffffu, a, o);
         b += __shfl_xor_sync(0xffffffffu, b, o);
     }
-    if ((threadIdx.x & 31) == 0) red[0][threadIdx.x >> 5] = a, red[1][threadIdx.x >> 5] = b;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if ((tid & 31) == 0) s.red[0][tid >> 5] = a, s.red[1][tid >> 5] = b;
+    __syncthreads();
+    if (tid == 0) {
         double sa = 0.0, sb = 0.0;
-        for (int w = 0; w < int(blockDim.x >> 5); ++w) sa += red[0][w], sb += red[1][w];
-        const double ssim = sa * inv_n, l1 = sb * inv_n;
-        out[0] = float((1.0 - lambda) * l1 + lambda * (1.0 - ssim));
-        out[1] = float(ssim);
-        out[2] = float(l1);
+        for (int w = 0; w < kThreads / 32; ++w) sa += s.red[0][w], sb += s.red[1][w];
+        const double ssim = sa * p.inv_n, l1 = sb * p.inv_n;
+        p.out[0] = float((1.0 - p.lambda) * l1 + p.lambda * (1.0 - ssim));
+        p.out[1] = float(ssim);
+        p.out[2] = float(l1);
+        *p.ticket = 0u;
     }
 }
 
@@ -203,7 +214,7 @@ using namespace ss;
 
 extern "C" size_t ss_ssim_workspace_bytes(int32_t C, int32_t H, int32_t W) {
     if (C < 1 || H < 1 || W < 1 || H > kMaxSide || W > kMaxSide || C > 64) return 0;
-    return size_t(ssim_blocks(C, H, W)) * sizeof(double2);
+    return size_t(ssim_blocks(C, H, W)) * sizeof(double2) + 16;   // partials + ticket
 }
 
 extern "C" ss_status ss_ssim_loss(const float *img, const float *target, int32_t C, int32_t H,
@@ -237,7 +248,11 @@ extern "C" ss_status ss_ssim_loss(const float *img, const float *target, int32_t
     SsimParams p{};
     p.img = img, p.tgt = target, p.grad = dL_dimg;
     p.partial = static_cast<double2 *>(workspace);
-    p.C = C, p.H = H, p.W = W, p.tiles_x = (W + kT - 1) / kT;
+    p.n_blocks = int(ssim_blocks(C, H, W));
+    p.ticket = reinterpret_cast<unsigned int *>(p.partial + p.n_blocks);
+    p.out = loss;
+    p.lambda = lambda;
+    p.C = C, p.H = H, p.W = W;
     // the 1D window exp(-i^2 / (2 sigma^2)), sigma = 1.5, normalised in double
     double g[2 * kR + 1], gs = 0.0;
     for (int i = -kR; i <= kR; ++i) gs += (g[i + kR] = std::exp(-double(i * i) / (2.0 * 1.5 * 1.5)));
@@ -245,13 +260,11 @@ extern "C" ss_status ss_ssim_loss(const float *img, const float *target, int32_t
     const double n = double(C) * H * W;
     p.cs = float(-double(lambda) / n);
     p.cl = float((1.0 - double(lambda)) / n);
+    p.inv_n = 1.0 / n;
     cudaStream_t s = (cudaStream_t)stream;
+    st = check_cuda(cudaMemsetAsync(p.ticket, 0, sizeof(unsigned int), s), "ss_ssim_loss: memset");
+    if (st != SS_OK) return st;
     const dim3 grid((W + kT - 1) / kT, (H + kT - 1) / kT, C);
     SS_LAUNCH("k_ssim", s, k_ssim<<<grid, kThreads, sizeof(SsimSmem), s>>>(p));
-    st = check_launch("ss_ssim_loss");
-    if (st != SS_OK) return st;
-    SS_LAUNCH("k_ssim_final", s,
-              k_ssim_final<<<1, 1024, 0, s>>>(p.partial, int(ssim_blocks(C, H, W)), 1.0 / n,
-                                               lambda, loss));
     return check_launch("ss_ssim_loss");
 }

@@ -32,7 +32,8 @@ extern "C" {
 #endif
 
 /* Bytes of workspace ss_ssim_loss needs (one 16-byte partial sum per
- * 32 x 32 tile and channel); 0 for sizes outside the limits below. */
+ * 32 x 32 tile and channel, and a 16-byte slot for the completion counter);
+ * 0 for sizes outside the limits below. */
 size_t ss_ssim_workspace_bytes(int32_t C, int32_t H, int32_t W);
 
 /* loss:    device float[3], overwritten with (loss, mean SSIM, mean |x - y|),
@@ -40,7 +41,8 @@ size_t ss_ssim_workspace_bytes(int32_t C, int32_t H, int32_t W);
  * img, target: device float [C][H][W] (planar, as ss_raster_fwd writes).
  * dL_dimg: device float [C][H][W], overwritten; may be passed straight to
  *          ss_raster_bwd as its dL_dimage.
- * workspace: device, 16-byte aligned, >= ss_ssim_workspace_bytes.
+ * workspace: device, 16-byte aligned, >= ss_ssim_workspace_bytes (partial sums
+ *          and a counter, which the call clears itself).
  * Errors: SS_ERR_UNSUPPORTED unless 1 <= C <= 64 and 1 <= H, W <= 32768;
  * SS_ERR_INVALID_ARG for a NULL pointer, lambda outside [0, 1], or a small
  * or misaligned workspace. */

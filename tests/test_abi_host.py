@@ -181,9 +181,9 @@ def test_projection_rejects_bad_arguments_on_the_host(lib):
 
 
 def test_ssim_rejects_bad_arguments_on_the_host(lib):
-    assert lib.ss_ssim_workspace_bytes(3, 822, 1237) == 16 * 3 * 26 * 39
+    assert lib.ss_ssim_workspace_bytes(3, 822, 1237) == 16 * 3 * 26 * 39 + 16
     assert lib.ss_ssim_workspace_bytes(0, 8, 8) == 0
-    ws = 16 * 3
+    ws = 16 * 3 + 16
     assert lib.ss_ssim_loss(0x1000, 0x1000, 0, 8, 8, 0.2, 0x1000, 0x1000, 0x1000, ws, None) == 5
     assert lib.ss_ssim_loss(0x1000, 0x1000, 3, 8, 40000, 0.2, 0x1000, 0x1000, 0x1000, ws, None) == 5
     assert lib.ss_ssim_loss(None, 0x1000, 3, 8, 8, 0.2, 0x1000, 0x1000, 0x1000, ws, None) == 1
