@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the projection / SSIM legs")
+    ap.add_argument("--only", choices=["projection", "ssim", "distortion"],
+                    help="run one leg of the next rows alone and print its JSON (for profiling)")
     return ap.parse_args()
 
 
@@ -582,6 +584,29 @@ def run_ours(args, rank: int, world: int, dist):
     print(json.dumps(line), flush=True)
 
 
+def run_only(args):
+    """One leg of the next rows on its own (a few GB on the device), for ncu."""
+    import torch
+    try:
+        import gaussian_splatting_differentiable_gb300 as ss
+    except ImportError:
+        import __graft_entry__
+        __graft_entry__.build()
+        import gaussian_splatting_differentiable_gb300 as ss
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs") or 6800.0
+    src = ("measured" if peaks.get("hbm_gbs") else "fallback") + " (MEASURED_PEAKS.json hbm_gbs)"
+    if args.only == "projection":
+        out = measure_projection(ss, dev, flush, args.steps, hbm, src)
+    elif args.only == "ssim":
+        out = measure_ssim(ss, dev, flush, args.steps, hbm, src)
+    else:
+        out = measure_distortion(ss, dev, flush, args.steps)
+    print(json.dumps({"only": args.only, **out}), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -596,6 +621,9 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
         dist = tdist
+    if args.only:
+        run_only(args)
+        return
     try:
         run_ours(args, rank, world, dist)
     finally:
