@@ -43,8 +43,8 @@ WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H) {
     off = align256(off + size_t(L.ndig) * 256 * 4);
     L.gofs = off;
     off = align256(off + size_t(L.ndig) * 256 * 4);
-    L.tickets = off;
-    off = align256(off + 8 * 4);
+    L.tickets = off;              // [0, 8) pass tickets, [8] long tie runs
+    off = align256(off + 16 * 4);
     L.lookback = off;
     off = align256(off + size_t(L.ndig) * size_t(L.nparts) * 256 * 8);
     L.zero_end = off;
@@ -52,6 +52,8 @@ WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H) {
     off = align256(off + size_t(n_pairs) * 8);
     L.alt_vals = off;
     off = align256(off + size_t(n_pairs) * 4);
+    L.ties = off;                 // uint2 (start, length) of runs of > 32 equal keys
+    off = align256(off + size_t(n_pairs / 33 + 1) * 8);
     L.sort_end = off;
     L.accum = 256;  // after the status word; the sort's regions are dead by then
     L.bwd_end = align256(L.accum + size_t(n_splats) * 48);  // 48-byte gradient record per splat

@@ -18,7 +18,12 @@
 //   k_sort_final  equal keys (same tile, same depth) come out in emission
 //                 order, which the atomic counter of the binning makes
 //                 arbitrary: each run of equal keys is re-sorted by splat
-//                 index, and the tile boundaries give the CSR offsets.
+//                 index (by its first thread when it is short; runs longer
+//                 than 32 go to a list), and the tile boundaries give the
+//                 CSR offsets;
+//   k_sort_ties   one CTA per long run: a stable radix sort of its indices
+//                 in global memory (no quadratic insertion sort, whatever
+//                 the number of equal depths).
 // Only 32 + ceil(log2 tiles) key bits are sorted.
 #include "ss_device.cuh"
 #include "ss_internal.h"
@@ -233,10 +238,13 @@ __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
 //  - a run of equal keys starting at i is re-sorted by value (insertion sort
 //    by the run's first thread; runs are a few elements);
 //  - when src != dst the element is copied (run members by the run head).
+constexpr int kTieInsert = 32;   // longest run of equal keys sorted by insertion
+
 __global__ void __launch_bounds__(256) k_sort_final(const uint64_t *__restrict__ sk,
                                                     uint32_t *sv, uint64_t *dk, uint32_t *dv,
                                                     int64_t n_max, const unsigned long long *dn,
-                                                    int64_t tiles, uint32_t *offs, uint32_t *err) {
+                                                    int64_t tiles, uint32_t *offs, uint32_t *err,
+                                                    uint32_t *tie_count, uint2 *ties) {
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t n = pair_count(dn, n_max);
     if (i == 0 && dn && *dn > (unsigned long long)n_max) atomicOr(err, kDevErrCapacity);
@@ -270,7 +278,12 @@ __global__ void __launch_bounds__(256) k_sort_final(const uint64_t *__restrict__
         return;
     }
     int64_t e = i + 1;
-    while (e < n && sk[e] == key) ++e;
+    while (e < n && sk[e] == key && e - i <= kTieInsert) ++e;
+    if (e - i > kTieInsert) {   // a long run: k_sort_ties sorts (and copies) it
+        while (e < n && sk[e] == key) ++e;
+        ties[atomicAdd(tie_count, 1u)] = make_uint2(uint32_t(i), uint32_t(e - i));
+        return;
+    }
     // insertion sort of sv[i..e) by value, written to dv[i..e)
     for (int64_t a = i; a < e; ++a) {
         const uint32_t v = sv[a];
@@ -281,6 +294,98 @@ __global__ void __launch_bounds__(256) k_sort_final(const uint64_t *__restrict__
         }
         dv[b] = v;
         if (copy) dk[a] = key;
+    }
+}
+
+// Stable LSD radix sort of one range in global memory by one CTA, over the
+// 64-bit key (depth bits << 32 | splat index): 8 passes of 8 bits (passes
+// whose digit is the same for the whole range are skipped -- for a run of
+// equal keys, all four depth digits), each a histogram, a scan and a stable
+// scatter in chunks of 256 elements.  Data ping-pongs between the range in
+// buffer a and in buffer b; the result is written to (dk, dv) with tile bits
+// `tile`.
+__device__ void segment_sort_global(uint64_t *ak, uint32_t *av, uint64_t *bk, uint32_t *bv,
+                                    uint64_t *dk, uint32_t *dv, int64_t lo, int len, uint64_t tile,
+                                    uint32_t *s_cnt, uint32_t *s_wc, uint32_t *s_warp) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t lt = lanemask_lt();
+    uint64_t *ck[2] = {ak + lo, bk + lo};
+    uint32_t *cv[2] = {av + lo, bv + lo};
+    int cur = 0;
+    // composite key of element e in buffer c: (key & 0xffffffff) << 32 | val
+    for (int pass = 0; pass < 8; ++pass) {
+        const int sh = 8 * pass;
+        for (int d = tid; d < 256; d += 256) s_cnt[d] = 0;
+        __syncthreads();
+        for (int e = tid; e < len; e += 256) {
+            const uint64_t c = (ck[cur][e] << 32) | cv[cur][e];
+            atomicAdd(&s_cnt[uint32_t(c >> sh) & 255u], 1u);
+        }
+        __syncthreads();
+        const uint32_t mine = s_cnt[tid];
+        const uint32_t uniform = __syncthreads_or(mine == uint32_t(len));
+        if (uniform) continue;   // every element has the same digit: nothing moves
+        uint32_t run = block_excl_scan256(mine, s_warp, nullptr);   // running output offset of digit tid
+        const int nxt = cur ^ 1;
+        for (int base = 0; base < len; base += 256) {
+            const int e = base + tid;
+            const bool ok = e < len;
+            uint64_t kk = 0;
+            uint32_t vv = 0, dig = 256u + uint32_t(lane);
+            if (ok) {
+                kk = ck[cur][e];
+                vv = cv[cur][e];
+                dig = uint32_t(((kk << 32) | vv) >> sh) & 255u;
+            }
+            const uint32_t peers = __match_any_sync(0xffffffffu, dig);
+            const uint32_t before = __popc(peers & lt);
+            for (int k = tid; k < 8 * 256; k += 256) s_wc[k] = 0;
+            __syncthreads();
+            if (ok && before == 0) s_wc[warp * 256 + dig] = __popc(peers);
+            __syncthreads();
+            // thread d: exclusive prefix over warps of digit d, chunk total
+            uint32_t tot = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                const uint32_t c = s_wc[w * 256 + tid];
+                s_wc[w * 256 + tid] = tot;
+                tot += c;
+            }
+            s_cnt[tid] = run;
+            __syncthreads();
+            if (ok) {
+                const uint32_t pos = s_cnt[dig] + s_wc[warp * 256 + dig] + before;
+                ck[nxt][pos] = kk;
+                cv[nxt][pos] = vv;
+            }
+            run += tot;
+            __syncthreads();
+        }
+        cur = nxt;
+        __syncthreads();
+    }
+    for (int e = tid; e < len; e += 256) {
+        const uint64_t kk = ck[cur][e];
+        dk[lo + e] = (tile << 32) | (kk & 0xffffffffull);
+        dv[lo + e] = cv[cur][e];
+    }
+}
+
+// One CTA per long run of equal keys (grid-stride over the list that
+// k_sort_final filled): the run's indices in ascending order.  (ok, ov) is
+// the other buffer, scratch for the radix passes.
+__global__ void __launch_bounds__(256) k_sort_ties(uint64_t *sk, uint32_t *sv, uint64_t *dk,
+                                                   uint32_t *dv, uint64_t *ok_, uint32_t *ov,
+                                                   const uint32_t *tie_count, const uint2 *ties) {
+    __shared__ uint32_t s_wc[8 * 256];
+    __shared__ uint32_t s_cnt[256];
+    __shared__ uint32_t s_warp[8];
+    const uint32_t nt = *tie_count;
+    for (uint32_t r = blockIdx.x; r < nt; r += gridDim.x) {
+        const uint2 run = ties[r];
+        segment_sort_global(sk, sv, ok_, ov, dk, dv, int64_t(run.x), int(run.y),
+                            sk[run.x] >> 32, s_cnt, s_wc, s_warp);
+        __syncthreads();
     }
 }
 
@@ -367,9 +472,16 @@ static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int6
         SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<int(L.nparts), 256, dyn, st>>>(p));
     }
     const int r = L.ndig & 1;
+    uint32_t *tie_count = tickets + 8;
+    uint2 *ties = reinterpret_cast<uint2 *>(ws + L.ties);
     SS_LAUNCH("k_sort_final", st,
               k_sort_final<<<int(blocks), 256, 0, st>>>(bk[r], bv[r], keys, vals, n_max, dn, tiles,
-                                                        tile_offsets, err));
+                                                        tile_offsets, err, tie_count, ties));
+    const int64_t max_runs = n_max / (kTieInsert + 1) + 1;
+    const int tgrid = int(max_runs < int64_t(sms) * 2 ? max_runs : int64_t(sms) * 2);
+    SS_LAUNCH("k_sort_ties", st,
+              k_sort_ties<<<tgrid, 256, 0, st>>>(bk[r], bv[r], keys, vals, bk[r ^ 1], bv[r ^ 1],
+                                                 tie_count, ties));
     return check_launch(who);
 }
 

@@ -197,6 +197,7 @@ def test_profile_counts_every_launch(P):
     prof = ss.ss_profile_collect()
     assert prof["k_emit_pairs"][0] == 2 and prof["k_raster_bwd"][0] == 2
     assert prof["k_sort_pass"][0] == 2 * 5   # 8 tile bits + 32 depth bits -> 5 digits
+    assert prof["k_sort_final"][0] == 2 and prof["k_sort_ties"][0] == 2
     assert all(v[1] > 0 for v in prof.values())
     assert ss.ss_profile_collect() == {}
 
@@ -267,3 +268,16 @@ def test_device_count_sort_of_no_pairs(P):
                          r.workspace)
     assert ss.ss_sort_status(r.workspace) == ss.SS_OK
     assert np.all(r.tile_offsets.cpu().numpy() == 0)
+
+
+def test_long_runs_of_equal_depths_sort_bit_exact(P):
+    """40,000 small splats on 2x2 tiles, a quarter of them at one depth: runs
+    of ~2,500 equal keys per tile, ordered by splat index by the long-run
+    radix sort (a quadratic insertion sort would take seconds), compared
+    pair by pair."""
+    import synth
+    sc = _scene(32, 32, 40000, seed=13)
+    sc.depth[::4] = np.float32(5.0)
+    gpu = P.run_gpu(sc, capacity=8 * sc.n)
+    tl = P.check_pairs(sc, gpu)
+    assert np.diff(tl["offs"]).max() > 8192
