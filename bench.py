@@ -548,7 +548,7 @@ def run_ours(args, rank: int, world: int, dist):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_tiles = 256   # ~10-30 s of single-core oracle work
+        n_tiles = 1024  # ~10-30 s of single-core oracle work on the GPU machine's host
         t_step, det = oracle_sample(scene, n_tiles)
         cpu = {"value": det["full_candidates"] / t_step, "unit": UNIT, "cores": 1,
                "kind": "oracle",
