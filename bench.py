@@ -446,7 +446,8 @@ def run_ours(args, rank: int, world: int, dist):
                                      if k.startswith(("k_emit", "k_sort"))) / args.steps,
         "raster fwd": kernels.get("k_raster_fwd", {}).get("ms_total", 0.0) / args.steps,
         "raster bwd": sum(v["ms_total"] for k, v in kernels.items()
-                          if k in ("k_bwd_zero", "k_raster_bwd", "k_accum_final")) / args.steps,
+                          if k in ("k_grad_zero", "k_raster_bwd", "k_grad_final", "k_bwd_zero",
+                                   "k_accum_final")) / args.steps,
     }
     k_total = sum(v["ms_total"] for v in kernels.values())
     dom = max(kernels, key=lambda k: kernels[k]["ms_total"])
@@ -569,8 +570,9 @@ def run_ours(args, rank: int, world: int, dist):
                    "l2": "256 MB buffer written between timed steps (L2 is 129 MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "ms_per_step_without_graph": nograph_ms,
-        "rasterize_bwd_ms_per_call": bwd_ms,
-        "rasterize_bwd_pairs_per_s": cand / (bwd_ms * 1e-3),
+        "rasterize_bwd_ms_per_call": stages["raster bwd"],
+        "rasterize_bwd_pairs_per_s": cand / (stages["raster bwd"] * 1e-3),
+        "k_raster_bwd_ms_per_call": bwd_ms,
         "stages_ms_per_step": stages,
         "kernels": kernels, "dominant_kernel": dom,
         "roofline": roofline, "roofline_atomic": roofline_atomic,
