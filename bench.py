@@ -186,6 +186,23 @@ def run_reference(args, rank: int):
 
 # ------------------------------------------------------------------ GPU arm
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (the slowest replica's time); x itself
+    when not distributed."""
+    if not dist:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, units_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: the units every replica processed over the
+    slowest replica's time (replicas of the same step, weak scaling)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def source_sha(paths) -> str:
     h = hashlib.sha256()
     for p in paths:
@@ -432,11 +449,8 @@ def run_ours(args, rank: int, world: int, dist):
         ms, min(step_ms), max(step_ms), nograph_ms, prof), file=sys.stderr, flush=True)
     if not prof:
         raise RuntimeError("SS_PROFILE recorded no kernel launches")
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * cand / (ms * 1e-3)
+    ms = max_over_ranks(ms, dist, dev)
+    value = job_value(world, cand, ms)
     launches = sum(c for (c, _, _, _) in prof.values())   # per-kernel region; same per graph replay
 
     kernels = {k: {"launches": c, "ms_per_call": tot / c, "ms_total": tot, "min_ms": mn,
@@ -537,11 +551,8 @@ def run_ours(args, rank: int, world: int, dist):
             e2e_step()
             e2e_ms.append((time.perf_counter() - t0) * 1e3)
         em = statistics.mean(e2e_ms)
-        if dist:
-            t = torch.tensor([em], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            em = float(t.item())
-        e2e = {"value": world * cand / (em * 1e-3), "unit": UNIT, "h2d_bytes_per_step": bi,
+        em = max_over_ranks(em, dist, dev)
+        e2e = {"value": job_value(world, cand, em), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "ms_per_step": em, "steps": n_e2e,
                "how": "pinned host inputs -> device, the step's CUDA graph, gradients + image + "
                       "weights -> pinned host, synchronize; wall clock"}
