@@ -225,37 +225,51 @@ __global__ void __launch_bounds__(256) k_project_bwd(ProjParams P) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= P.n) return;
     const size_t n = size_t(P.n);
+    // Colour first, from the view direction alone, so that the 48 SH
+    // coefficients and the geometry's ~45 intermediates are never live
+    // together (128 -> fewer registers, more warps per SM).  Its outputs are
+    // written as if the splat were visible; a culled splat's are zeroed at
+    // the end.
+    float dm[3];
+    bool col_ok;
+    {
+        const float px = P.mean3[3 * i], py = P.mean3[3 * i + 1], pz = P.mean3[3 * i + 2];
+        const float vx = px - P.campos[0], vy = py - P.campos[1], vz = pz - P.campos[2];
+        const float inv_len = 1.0f / sqrtf(vx * vx + vy * vy + vz * vz);
+        const float ux = vx * inv_len, uy = vy * inv_len, uz = vz * inv_len;
+        float Y[K];
+        sh_eval<DEG>(ux, uy, uz, Y);
+        float sh[K][3];
+        float raw[3] = {0.5f, 0.5f, 0.5f};
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int c = 0; c < 3; ++c) {
+                sh[k][c] = __ldg(P.sh + size_t(3 * k + c) * n + i);
+                raw[c] = fmaf(sh[k][c], Y[k], raw[c]);
+            }
+        col_ok = isfinite(raw[0]) && isfinite(raw[1]) && isfinite(raw[2]) && isfinite(inv_len);
+        // the clamp passes the gradient where raw >= 0
+        float gcol[3];
+#pragma unroll
+        for (int c = 0; c < 3; ++c) gcol[c] = raw[c] >= 0.0f ? P.grgb[3 * i + c] : 0.0f;
+        float dY[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            dY[k] = gcol[0] * sh[k][0] + gcol[1] * sh[k][1] + gcol[2] * sh[k][2];
+#pragma unroll
+            for (int c = 0; c < 3; ++c) P.dsh[size_t(3 * k + c) * n + i] = gcol[c] * Y[k];
+        }
+        float gdx = 0.0f, gdy = 0.0f, gdz = 0.0f;
+        sh_grad<DEG>(ux, uy, uz, dY, gdx, gdy, gdz);
+        const float dd = gdx * ux + gdy * uy + gdz * uz;
+        dm[0] = (gdx - ux * dd) * inv_len;
+        dm[1] = (gdy - uy * dd) * inv_len;
+        dm[2] = (gdz - uz * dd) * inv_len;
+    }
     Geo g;
     geometry(P, i, g);
-    float Y[K];
-    sh_eval<DEG>(g.dx, g.dy, g.dz, Y);
-    float sh[K][3];
-    float raw[3] = {0.5f, 0.5f, 0.5f};
-#pragma unroll
-    for (int k = 0; k < K; ++k)
-#pragma unroll
-        for (int c = 0; c < 3; ++c) {
-            sh[k][c] = __ldg(P.sh + size_t(3 * k + c) * n + i);
-            raw[c] = fmaf(sh[k][c], Y[k], raw[c]);
-        }
-    const bool ok = g.valid && isfinite(raw[0]) && isfinite(raw[1]) && isfinite(raw[2]);
-
-    // colour: the clamp passes the gradient where raw >= 0
-    float gcol[3];
-#pragma unroll
-    for (int c = 0; c < 3; ++c) gcol[c] = (ok && raw[c] >= 0.0f) ? P.grgb[3 * i + c] : 0.0f;
-    float dY[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        dY[k] = gcol[0] * sh[k][0] + gcol[1] * sh[k][1] + gcol[2] * sh[k][2];
-#pragma unroll
-        for (int c = 0; c < 3; ++c) P.dsh[size_t(3 * k + c) * n + i] = ok ? gcol[c] * Y[k] : 0.0f;
-    }
-    float gdx = 0.0f, gdy = 0.0f, gdz = 0.0f;
-    sh_grad<DEG>(g.dx, g.dy, g.dz, dY, gdx, gdy, gdz);
-    const float dd = gdx * g.dx + gdy * g.dy + gdz * g.dz;
-    float dm[3] = {(gdx - g.dx * dd) * g.inv_len, (gdy - g.dy * dd) * g.inv_len,
-                   (gdz - g.dz * dd) * g.inv_len};
+    const bool ok = g.valid && col_ok;
 
     const float gu = ok ? P.gmean2d[2 * i] : 0.0f, gv = ok ? P.gmean2d[2 * i + 1] : 0.0f;
     const float ga = ok ? P.gconic[3 * i] : 0.0f, gb = ok ? P.gconic[3 * i + 1] : 0.0f,
@@ -332,6 +346,9 @@ __global__ void __launch_bounds__(256) k_project_bwd(ProjParams P) {
         P.dscale[3 * i + j] = ok ? ds[j] : 0.0f;
     }
     reinterpret_cast<float4 *>(P.dquat)[i] = ok ? dq : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!ok)
+#pragma unroll
+        for (int k = 0; k < 3 * K; ++k) P.dsh[size_t(k) * n + i] = 0.0f;
 }
 
 ss_status fill_params(const char *fn, const ss_splats3d *s, const ss_camera *cam, ProjParams &P) {
