@@ -69,95 +69,149 @@ __global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
     const size_t plane = size_t(p.H) * p.W;
     const float *img = p.img + c * plane, *tgt = p.tgt + c * plane;
 
-    // A: the input region, zero outside the image
-    for (int k = tid; k < kIn * kIn; k += kThreads) {
+    // A: the input region, zero outside the image; every load of a thread is
+    // issued before its first shared store (one memory latency, not eight)
+    constexpr int kLoads = (kIn * kIn + kThreads - 1) / kThreads;
+    float lx[kLoads], ly[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+        const int k = tid + u * kThreads;
         const int r = k / kIn, q = k % kIn;
         const int gy = y0 - 2 * kR + r, gx = x0 - 2 * kR + q;
-        const bool in = gy >= 0 && gy < p.H && gx >= 0 && gx < p.W;
+        const bool in = k < kIn * kIn && gy >= 0 && gy < p.H && gx >= 0 && gx < p.W;
         const size_t o = size_t(gy) * p.W + gx;
-        s.x[r][q] = in ? __ldg(img + o) : 0.0f;
-        s.y[r][q] = in ? __ldg(tgt + o) : 0.0f;
+        lx[u] = in ? __ldg(img + o) : 0.0f;
+        ly[u] = in ? __ldg(tgt + o) : 0.0f;
     }
-    __syncthreads();
-
-    // B: horizontal window sums of x, y, x^2, y^2, xy
-    for (int k = tid; k < kIn * kMom; k += kThreads) {
-        const int r = k / kMom, q = k % kMom;
-        float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f, m4 = 0.f;
 #pragma unroll
-        for (int j = 0; j <= 2 * kR; ++j) {
-            const float a = s.x[r][q + j], b = s.y[r][q + j], w = p.g[j];
-            const float wa = w * a, wb = w * b;
-            m0 += wa;
-            m1 += wb;
-            m2 = fmaf(wa, a, m2);
-            m3 = fmaf(wb, b, m3);
-            m4 = fmaf(wa, b, m4);
+    for (int u = 0; u < kLoads; ++u) {
+        const int k = tid + u * kThreads;
+        if (k < kIn * kIn) {
+            const int r = k / kIn, q = k % kIn;
+            s.x[r][q] = lx[u];
+            s.y[r][q] = ly[u];
         }
-        s.h[0][r][q] = m0, s.h[1][r][q] = m1, s.h[2][r][q] = m2, s.h[3][r][q] = m3,
-        s.h[4][r][q] = m4;
     }
     __syncthreads();
 
-    // C: vertical sums -> statistics, SSIM and the adjoint maps
+    // Each thread computes two neighbouring outputs of a 1D pass (they share
+    // six of their eight window inputs, which it reads once).
+
+    // B: horizontal window sums of x, y, x^2, y^2, xy (pairs along a row)
+    for (int k = tid; k < kIn * (kMom / 2); k += kThreads) {
+        const int r = k / (kMom / 2), q = 2 * (k % (kMom / 2));
+        float xa[kW + 1], ya[kW + 1];
+#pragma unroll
+        for (int j = 0; j <= kW; ++j) xa[j] = s.x[r][q + j], ya[j] = s.y[r][q + j];
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+            float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f, m4 = 0.f;
+#pragma unroll
+            for (int j = 0; j < kW; ++j) {
+                const float a = xa[o + j], b = ya[o + j], w = p.g[j];
+                const float wa = w * a, wb = w * b;
+                m0 += wa;
+                m1 += wb;
+                m2 = fmaf(wa, a, m2);
+                m3 = fmaf(wb, b, m3);
+                m4 = fmaf(wa, b, m4);
+            }
+            s.h[0][r][q + o] = m0, s.h[1][r][q + o] = m1, s.h[2][r][q + o] = m2,
+            s.h[3][r][q + o] = m3, s.h[4][r][q + o] = m4;
+        }
+    }
+    __syncthreads();
+
+    // C: vertical sums -> statistics, SSIM and the adjoint maps (pairs down a column)
     double ssim_sum = 0.0;
-    for (int k = tid; k < kMom * kMom; k += kThreads) {
-        const int r = k / kMom, q = k % kMom;
-        float m[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k = tid; k < (kMom / 2) * kMom; k += kThreads) {
+        const int q = k % kMom, r0 = 2 * (k / kMom);
+        float v[5][kW + 1];
 #pragma unroll
-        for (int j = 0; j <= 2 * kR; ++j)
+        for (int t = 0; t < 5; ++t)
 #pragma unroll
-            for (int t = 0; t < 5; ++t) m[t] = fmaf(p.g[j], s.h[t][r + j][q], m[t]);
-        const int gy = y0 - kR + r, gx = x0 - kR + q;
-        const bool in = gy >= 0 && gy < p.H && gx >= 0 && gx < p.W;
-        const float mx = m[0], my = m[1];
-        const float A1 = 2.0f * mx * my + kC1;
-        const float A2 = 2.0f * (m[4] - mx * my) + kC2;
-        const float B1 = mx * mx + my * my + kC1;
-        const float B2 = (m[2] - mx * mx) + (m[3] - my * my) + kC2;
-        const float iA1 = 1.0f / A1, iA2 = 1.0f / A2, iB1 = 1.0f / B1, iB2 = 1.0f / B2;
-        const float S = A1 * A2 * iB1 * iB2;
-        const float cS = in ? p.cs * S : 0.0f;
-        s.a[0][r][q] = cS * 2.0f * (my * (iA1 - iA2) - mx * (iB1 - iB2));   // d/d mu_x
-        s.a[1][r][q] = -cS * iB2;                                            // d/d E[x^2]
-        s.a[2][r][q] = 2.0f * cS * iA2;                                      // d/d E[xy]
-        if (in && r >= kR && r < kR + kT && q >= kR && q < kR + kT) ssim_sum += S;
-    }
-    __syncthreads();
-
-    // D: horizontal correlation of the adjoint maps (reuses h)
-    for (int k = tid; k < kMom * kT; k += kThreads) {
-        const int r = k / kT, q = k % kT;
-        float v0 = 0.f, v1 = 0.f, v2 = 0.f;
+            for (int j = 0; j <= kW; ++j) v[t][j] = s.h[t][r0 + j][q];
+        const int gx = x0 - kR + q;
+        const bool col_in = gx >= 0 && gx < p.W, col_mid = q >= kR && q < kR + kT;
 #pragma unroll
-        for (int j = 0; j <= 2 * kR; ++j) {
-            v0 = fmaf(p.g[j], s.a[0][r][q + j], v0);
-            v1 = fmaf(p.g[j], s.a[1][r][q + j], v1);
-            v2 = fmaf(p.g[j], s.a[2][r][q + j], v2);
+        for (int o = 0; o < 2; ++o) {
+            const int r = r0 + o;
+            float m[5];
+#pragma unroll
+            for (int t = 0; t < 5; ++t) {
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < kW; ++j) acc = fmaf(p.g[j], v[t][o + j], acc);
+                m[t] = acc;
+            }
+            const int gy = y0 - kR + r;
+            const bool in = col_in && gy >= 0 && gy < p.H;
+            const float mx = m[0], my = m[1];
+            const float A1 = 2.0f * mx * my + kC1;
+            const float A2 = 2.0f * (m[4] - mx * my) + kC2;
+            const float B1 = mx * mx + my * my + kC1;
+            const float B2 = (m[2] - mx * mx) + (m[3] - my * my) + kC2;
+            const float iA1 = 1.0f / A1, iA2 = 1.0f / A2, iB1 = 1.0f / B1, iB2 = 1.0f / B2;
+            const float S = A1 * A2 * iB1 * iB2;
+            const float cS = in ? p.cs * S : 0.0f;
+            s.a[0][r][q] = cS * 2.0f * (my * (iA1 - iA2) - mx * (iB1 - iB2));   // d/d mu_x
+            s.a[1][r][q] = -cS * iB2;                                            // d/d E[x^2]
+            s.a[2][r][q] = 2.0f * cS * iA2;                                      // d/d E[xy]
+            if (in && col_mid && r >= kR && r < kR + kT) ssim_sum += S;
         }
-        s.h[0][r][q] = v0, s.h[1][r][q] = v1, s.h[2][r][q] = v2;
     }
     __syncthreads();
 
-    // E: vertical correlation and the gradient
+    // D: horizontal correlation of the adjoint maps (reuses h; pairs along a row)
+    for (int k = tid; k < kMom * (kT / 2); k += kThreads) {
+        const int r = k / (kT / 2), q = 2 * (k % (kT / 2));
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            float v[kW + 1];
+#pragma unroll
+            for (int j = 0; j <= kW; ++j) v[j] = s.a[t][r][q + j];
+            float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < kW; ++j) {
+                v0 = fmaf(p.g[j], v[j], v0);
+                v1 = fmaf(p.g[j], v[j + 1], v1);
+            }
+            s.h[t][r][q] = v0, s.h[t][r][q + 1] = v1;
+        }
+    }
+    __syncthreads();
+
+    // E: vertical correlation and the gradient (pairs down a column)
     double l1_sum = 0.0;
     float *grad = p.grad + c * plane;
-    for (int k = tid; k < kT * kT; k += kThreads) {
-        const int r = k / kT, q = k % kT;
-        const int gy = y0 + r, gx = x0 + q;
-        if (gy >= p.H || gx >= p.W) continue;
-        float v0 = 0.f, v1 = 0.f, v2 = 0.f;
+    for (int k = tid; k < (kT / 2) * kT; k += kThreads) {
+        const int q = k % kT, r0 = 2 * (k / kT);
+        const int gx = x0 + q;
+        float acc[3][2];
 #pragma unroll
-        for (int j = 0; j <= 2 * kR; ++j) {
-            v0 = fmaf(p.g[j], s.h[0][r + j][q], v0);
-            v1 = fmaf(p.g[j], s.h[1][r + j][q], v1);
-            v2 = fmaf(p.g[j], s.h[2][r + j][q], v2);
+        for (int t = 0; t < 3; ++t) {
+            float v[kW + 1];
+#pragma unroll
+            for (int j = 0; j <= kW; ++j) v[j] = s.h[t][r0 + j][q];
+            float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < kW; ++j) {
+                v0 = fmaf(p.g[j], v[j], v0);
+                v1 = fmaf(p.g[j], v[j + 1], v1);
+            }
+            acc[t][0] = v0, acc[t][1] = v1;
         }
-        const float xv = s.x[r + 2 * kR][q + 2 * kR], yv = s.y[r + 2 * kR][q + 2 * kR];
-        const float d = xv - yv;
-        const float sg = d > 0.0f ? 1.0f : (d < 0.0f ? -1.0f : 0.0f);
-        grad[size_t(gy) * p.W + gx] = v0 + 2.0f * xv * v1 + yv * v2 + p.cl * sg;
-        l1_sum += fabsf(d);
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+            const int r = r0 + o, gy = y0 + r;
+            if (gy >= p.H || gx >= p.W) continue;
+            const float xv = s.x[r + 2 * kR][q + 2 * kR], yv = s.y[r + 2 * kR][q + 2 * kR];
+            const float d = xv - yv;
+            const float sg = d > 0.0f ? 1.0f : (d < 0.0f ? -1.0f : 0.0f);
+            grad[size_t(gy) * p.W + gx] =
+                acc[0][o] + 2.0f * xv * acc[1][o] + yv * acc[2][o] + p.cl * sg;
+            l1_sum += fabsf(d);
+        }
     }
 
     // per-CTA partial sums in double, then the last CTA adds them in order
