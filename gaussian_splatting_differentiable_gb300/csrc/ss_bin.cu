@@ -1,10 +1,10 @@
 // Tile binning ("Phase 5 step 30b -- kernel-by-kernel timing", emit_pairs:
 // tile id computation plus an atomic counter update).
 //
-// One thread per splat computes its tile rectangle; the warp sums its pair
-// counts with shuffles and lane 31 takes the warp's slots with a single
-// 64-bit atomic add, so the global counter sees one atomic per warp rather
-// than one per splat.  Each lane then writes its pairs into its slots.  The
+// One thread per splat computes its tile rectangle; the CTA scans its pair
+// counts (warp shuffles, then the eight warp totals) and one thread takes
+// the CTA's slots with a single 64-bit atomic add, so the global counter
+// sees one atomic per 256 splats rather than one per splat.  Each lane then writes its pairs into its slots.  The
 // same thread also writes the splat's 64-byte record (derived exponent
 // coefficients, threshold, colour, depth, cull box), which the forward and
 // backward rasterizers gather by index instead of the five SoA inputs.
@@ -40,21 +40,33 @@ __global__ void __launch_bounds__(256) k_emit_pairs(BinParams p) {
         dst[3] = *reinterpret_cast<const float4 *>(&r.box);
     }
 
-    uint32_t inc = cnt;  // warp inclusive scan of pair counts
+    // Block-wide exclusive scan of the pair counts, then one 64-bit atomic
+    // per CTA on the global counter (same-address atomics serialise in L2).
+    __shared__ uint32_t s_wsum[8], s_wcull[8];
+    __shared__ unsigned long long s_base;
+    const int warp = threadIdx.x >> 5;
+    uint32_t inc = cnt;  // warp inclusive scan
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += t;
     }
-    const uint32_t total = __shfl_sync(0xffffffffu, inc, 31);
-    unsigned long long base = 0;
-    if (lane == 31 && total) base = atomicAdd(p.counters, (unsigned long long)total);
-    base = __shfl_sync(0xffffffffu, base, 31);
     const uint32_t culled = __ballot_sync(0xffffffffu, st < 0);
-    if (lane == 0 && culled) atomicAdd(p.counters + 1, (unsigned long long)__popc(culled));
+    if (lane == 31) s_wsum[warp] = inc;
+    if (lane == 0) s_wcull[warp] = __popc(culled);
+    __syncthreads();
+    uint32_t before = 0;
+    if (threadIdx.x == 0) {
+        uint32_t tot = 0, tc = 0;
+        for (int w = 0; w < 8; ++w) tot += s_wsum[w], tc += s_wcull[w];
+        s_base = tot ? atomicAdd(p.counters, (unsigned long long)tot) : 0ull;
+        if (tc) atomicAdd(p.counters + 1, (unsigned long long)tc);
+    }
+    for (int w = 0; w < warp; ++w) before += s_wsum[w];
+    __syncthreads();
     if (!cnt) return;
 
-    unsigned long long pos = base + (inc - cnt);
+    unsigned long long pos = s_base + before + (inc - cnt);
     const unsigned long long cap = (unsigned long long)p.capacity;
     for (int ty = y0; ty <= y1; ++ty) {
         const uint64_t row = uint64_t(ty) * uint64_t(p.tiles_x);
