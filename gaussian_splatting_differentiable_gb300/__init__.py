@@ -452,3 +452,96 @@ class Rasterizer:
         with torch.cuda.graph(g):
             self.step_async(splats, dL_dimage, dL_ddist=dL_ddist)
         return g
+
+
+class StepPipeline:
+    """The whole step (bin, sort, forward, backward) fed from and returned to
+    pinned host memory, double-buffered across steps on one GPU.
+
+    Two buffer sets, each a Rasterizer with its own captured CUDA graph and
+    device input buffers, and three streams: step k's host-to-device input
+    copy runs on one copy stream while step k-1 computes, step k's results
+    (image, gradients, accumulated weight) come back on a second copy stream
+    while step k+1 computes, and events order each buffer set's copy in,
+    compute and copy out.  Every step still copies all of its inputs in and
+    all of its results out; the copies overlap the other set's compute.
+
+    The pair buffers must be sized first (the constructor runs one
+    synchronous step on the given inputs); check() after run() reports a
+    capacity overflow or another device-side problem of the last steps."""
+
+    KEYS = ("mean2d", "conic", "opacity", "rgb", "depth")
+
+    def __init__(self, W: int, H: int, n_splats: int, flags: int, host_splats: dict, host_dL,
+                 bg=None, device="cuda", capacity=None):
+        d = torch.device(device)
+        self.device = d
+        cap = capacity if capacity is not None else max(64, 3 * n_splats)
+        self.r, self.dev_in, self.dev_dL, self.graphs = [], [], [], []
+        for b in range(2):
+            r = Rasterizer(W, H, n_splats, cap, flags, bg=bg, device=d)
+            sp = Splats(**{k: torch.empty(host_splats[k].shape, dtype=torch.float32, device=d)
+                           for k in self.KEYS})
+            dL = torch.empty(host_dL.shape, dtype=torch.float32, device=d)
+            for k in self.KEYS:
+                getattr(sp, k).copy_(host_splats[k])
+            dL.copy_(host_dL)
+            r.step(sp, dL)                 # sizes the pair buffers (one host read)
+            self.r.append(r)
+            self.dev_in.append(sp)
+            self.dev_dL.append(dL)
+        for b in range(2):
+            self.graphs.append(self.r[b].capture(self.dev_in[b], self.dev_dL[b]))
+        torch.cuda.synchronize()
+        self.h2d = torch.cuda.Stream(device=d)
+        self.comp = torch.cuda.Stream(device=d)
+        self.d2h = torch.cuda.Stream(device=d)
+        ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]  # noqa: E731
+        self.in_ready, self.computed, self.out_read, self.in_free = ev(), ev(), ev(), ev()
+        self.started = [False, False]
+
+    def outputs(self, b: int) -> list:
+        r = self.r[b]
+        out = [r.image] + [r.grads[k] for k in ("dmean2d", "dconic", "dopacity", "drgb")]
+        if r.accum_weight is not None:
+            out.append(r.accum_weight)
+        return out
+
+    def host_output_buffers(self, pin=True) -> list:
+        return [torch.empty(o.shape, dtype=o.dtype, pin_memory=pin) for o in self.outputs(0)]
+
+    def submit(self, k: int, host_splats: dict, host_dL, host_out: list) -> None:
+        """Enqueue step k: copy in, compute, copy out (all asynchronous)."""
+        b = k & 1
+        with torch.cuda.stream(self.h2d):
+            if self.started[b]:
+                self.h2d.wait_event(self.in_free[b])        # step k-2 has read its inputs
+            for key in self.KEYS:
+                getattr(self.dev_in[b], key).copy_(host_splats[key], non_blocking=True)
+            self.dev_dL[b].copy_(host_dL, non_blocking=True)
+            self.in_ready[b].record(self.h2d)
+        with torch.cuda.stream(self.comp):
+            self.comp.wait_event(self.in_ready[b])
+            if self.started[b]:
+                self.comp.wait_event(self.out_read[b])      # step k-2's results are out
+            self.graphs[b].replay()
+            self.computed[b].record(self.comp)
+            self.in_free[b].record(self.comp)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.computed[b])
+            for h, o in zip(host_out, self.outputs(b)):
+                h.copy_(o, non_blocking=True)
+            self.out_read[b].record(self.d2h)
+        self.started[b] = True
+
+    def run(self, steps: int, host_splats: dict, host_dL, host_outs: list) -> None:
+        """Enqueue `steps` steps (host_outs: two lists of host output buffers,
+        used alternately) and wait for all of them."""
+        for k in range(steps):
+            self.submit(k, host_splats, host_dL, host_outs[k & 1])
+        self.d2h.synchronize()
+
+    def check(self) -> None:
+        torch.cuda.synchronize()
+        for r in self.r:
+            r.check()

@@ -281,3 +281,30 @@ def test_long_runs_of_equal_depths_sort_bit_exact(P):
     gpu = P.run_gpu(sc, capacity=8 * sc.n)
     tl = P.check_pairs(sc, gpu)
     assert np.diff(tl["offs"]).max() > 8192
+
+
+def test_step_pipeline_matches_single_steps(P):
+    """ss.StepPipeline (double-buffered copies in and out around the step's
+    graph) returns what a synchronous step computes: the image and the
+    accumulated weight bit for bit, gradients to float-atomic reordering."""
+    import torch
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = synth.make_scene(2)
+    host_in = {k: torch.from_numpy(getattr(sc, k)).pin_memory() for k in ss.StepPipeline.KEYS}
+    host_dL = torch.from_numpy(sc.dL_dimage).pin_memory()
+    pipe = ss.StepPipeline(sc.W, sc.H, sc.n, ss.SS_ACCUM_WEIGHT, host_in, host_dL, device="cuda")
+    outs = [pipe.host_output_buffers(), pipe.host_output_buffers()]
+    pipe.run(5, host_in, host_dL, outs)
+    pipe.check()
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, 4 * sc.n, ss.SS_ACCUM_WEIGHT, device="cuda")
+    r.step(ss.Splats.from_numpy(sc), torch.from_numpy(sc.dL_dimage).cuda())
+    torch.cuda.synchronize()
+    ref = [r.image] + [r.grads[k] for k in ("dmean2d", "dconic", "dopacity", "drgb")] + \
+        [r.accum_weight]
+    for host in outs:
+        got = [h.numpy() for h in host]
+        refn = [t.cpu().numpy() for t in ref]
+        assert np.array_equal(got[0], refn[0])              # image
+        assert np.array_equal(got[-1], refn[-1])            # accumulated weight (fixed point)
+        for g, e in zip(got[1:-1], refn[1:-1]):
+            assert np.abs(g - e).max() <= 1e-5 * max(np.abs(e).max(), 1e-30)
