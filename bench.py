@@ -319,17 +319,19 @@ def measure_ssim(ss, dev, flush, steps: int, hbm: float, hbm_src: str) -> dict:
                                         "gradient 4 written"}}
 
 
-def measure_distortion(ss, dev, flush, steps: int) -> dict:
-    """The step with the depth-distortion variant (accumulated weight +
-    distortion) on the 2M-splat 1237x822 scene, as a CUDA graph, L2 flushed
+def measure_distortion(ss, dev, flush, steps: int, workload: int = 6, extra_flags=None,
+                       label: str = "accum_weight + distortion") -> dict:
+    """The step with an output variant (default: accumulated weight + depth
+    distortion) on a 2M-splat 1237x822 scene, as a CUDA graph, L2 flushed
     before each replay; per-kernel times from a second, profiled pass."""
     import torch
     import synth
-    sc = synth.make_scene(6)
-    flags = ss.SS_ACCUM_WEIGHT | ss.SS_DISTORTION
+    sc = synth.make_scene(workload)
+    flags = ss.SS_ACCUM_WEIGHT | (ss.SS_DISTORTION if extra_flags is None else extra_flags)
     sp = ss.Splats.from_numpy(sc, dev)
     dL = torch.from_numpy(sc.dL_dimage).to(dev).contiguous()
-    dLd = torch.from_numpy(sc.dL_ddist).to(dev).contiguous()
+    dLd = (torch.from_numpy(sc.dL_ddist).to(dev).contiguous()
+           if flags & ss.SS_DISTORTION else None)
     r = ss.Rasterizer(sc.W, sc.H, sc.n, int(2.5 * sc.n), flags, bg=sc.bg, device=dev)
     r.step(sp, dL, dL_ddist=dLd)
     g = r.capture(sp, dL, dL_ddist=dLd)
@@ -356,7 +358,7 @@ def measure_distortion(ss, dev, flush, steps: int) -> dict:
     ss.ss_profile_enable(False)
     prof = ss.ss_profile_collect()
     r.check()
-    return {"workload": synth.WORKLOADS[6].name, "flags": "accum_weight + distortion",
+    return {"workload": synth.WORKLOADS[workload].name, "flags": label,
             "ms_per_step": statistics.mean(a.elapsed_time(b) for a, b in ev),
             "kernels_ms_per_call": {k: v[1] / v[0] for k, v in prof.items()}}
 
@@ -516,6 +518,9 @@ def run_ours(args, rank: int, world: int, dist):
         next_rows["f4_ssim"] = measure_ssim(ss, dev, flush, args.steps, hbm,
                                             hbm_src + " (MEASURED_PEAKS.json hbm_gbs)")
         next_rows["f2_distortion"] = measure_distortion(ss, dev, flush, args.steps)
+        next_rows["f3_weight_stats"] = measure_distortion(
+            ss, dev, flush, args.steps, workload=4, extra_flags=ss.SS_WEIGHT_STATS,
+            label="accum_weight + weight statistics (max blend weight, blending-pixel count)")
 
     # --- end to end through the public API with host buffers
     e2e = None
