@@ -308,3 +308,27 @@ def test_step_pipeline_matches_single_steps(P):
         assert np.array_equal(got[-1], refn[-1])            # accumulated weight (fixed point)
         for g, e in zip(got[1:-1], refn[1:-1]):
             assert np.abs(g - e).max() <= 1e-5 * max(np.abs(e).max(), 1e-30)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_scenes(P, seed):
+    """Seeded random configurations: image size, splat count, scale,
+    opacity (up to the alpha cap) and depth ranges (with equal-depth
+    clusters), background and every output flag drawn at random, each
+    compared in full with the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    W, H = int(rng.integers(1, 200)), int(rng.integers(1, 200))
+    n = int(rng.integers(0, 3000))
+    lo = float(rng.uniform(0.2, 2.0))
+    wl = synth.Workload("random", W, H, n, (lo, lo * float(rng.uniform(1.0, 8.0))),
+                        (float(rng.uniform(0.004, 0.5)), float(rng.uniform(0.5, 1.0))),
+                        (1.0, float(rng.uniform(1.5, 200.0))), float(rng.uniform(0.01, 1.0)),
+                        bool(rng.integers(2)), bool(rng.integers(2)),
+                        weight_stats=bool(rng.integers(2)), distortion=bool(rng.integers(2)))
+    sc = synth.make_scene(wl, seed=seed)
+    if n and rng.integers(2):
+        k = max(1, n // 5)
+        sc.depth[rng.choice(n, k, replace=False)] = np.float32(rng.uniform(1, 5))
+    sc.bg = rng.uniform(0, 1, 3).astype(np.float32)
+    r = P.full_parity(sc)
+    print(seed, W, H, n, r["pairs"])
