@@ -471,19 +471,44 @@ MUTATIONS = [
 ]
 
 
-@pytest.mark.slow
-@pytest.mark.parametrize("label,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_planted_mistake_is_caught(tmp_path, label, old, new):
+def _run_mutant(tmp_dir, idx, old, new):
+    """Build oracle.c with one planted mistake and run the fast pins on it;
+    returns the pin run's exit code (0: every pin passed)."""
     here = os.path.dirname(oracle.__file__)
     src = open(os.path.join(here, "oracle.c")).read()
-    assert src.count(old) == 1, label
-    (tmp_path / "oracle.c").write_text(src.replace(old, new))
-    (tmp_path / "oracle.h").write_text(open(os.path.join(here, "oracle.h")).read())
-    lib = tmp_path / "libmut.so"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", str(lib),
-                    str(tmp_path / "oracle.c"), "-lm"], check=True)
-    env = dict(os.environ, ORACLE_LIB=str(lib))
-    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-m", "not slow",
-                        os.path.abspath(__file__)], env=env, capture_output=True, text=True,
-                       cwd=os.path.dirname(here))
-    assert r.returncode != 0, "planted mistake '%s' passed every pin" % label
+    if src.count(old) != 1:
+        return "pattern"
+    d = os.path.join(tmp_dir, "m%02d" % idx)
+    os.makedirs(d)
+    with open(os.path.join(d, "oracle.c"), "w") as f:
+        f.write(src.replace(old, new))
+    with open(os.path.join(d, "oracle.h"), "w") as f:
+        f.write(open(os.path.join(here, "oracle.h")).read())
+    lib = os.path.join(d, "libmut.so")
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", lib,
+                    os.path.join(d, "oracle.c"), "-lm"], check=True)
+    env = dict(os.environ, ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "-m", "not slow", os.path.abspath(__file__)], env=env,
+                       capture_output=True, text=True, cwd=os.path.dirname(here))
+    return r.returncode
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    """All planted mistakes, run concurrently (independent subprocesses)."""
+    import concurrent.futures as cf
+    tmp = str(tmp_path_factory.mktemp("mutants"))
+    workers = max(1, min(len(MUTATIONS), os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(workers) as ex:
+        futs = [ex.submit(_run_mutant, tmp, i, old, new)
+                for i, (_, old, new) in enumerate(MUTATIONS)]
+        return [f.result() for f in futs]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("k", range(len(MUTATIONS)), ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(mutant_results, k):
+    label = MUTATIONS[k][0]
+    assert mutant_results[k] != "pattern", "mutation '%s' does not match oracle.c" % label
+    assert mutant_results[k] != 0, "planted mistake '%s' passed every pin" % label
