@@ -69,6 +69,11 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
     __shared__ SplatBox s_box[2][256];
     __shared__ uint8_t s_list[8][256];
     __shared__ uint32_t s_mask[8][256];
+    // STATS: per-batch statistics of the batch's 256 entries (by buffer
+    // parity), summed over the CTA's warps with shared atomics and sent to
+    // the splats once per (tile, splat) when the batch is done.
+    __shared__ uint32_t s_smax[STATS ? 2 : 1][STATS ? 256 : 1];
+    __shared__ uint32_t s_scnt[STATS ? 2 : 1][STATS ? 256 : 1];
 
     const int tid = threadIdx.x;
     const int tile = blockIdx.x;
@@ -83,6 +88,24 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
     const float wy0 = float(by) + 0.5f, wy1 = wy0 + 3.0f;
     const uint32_t start = p.offs[tile], end = p.offs[tile + 1];
     const uint32_t lt = lanemask_lt();
+
+    if (STATS) {
+        s_smax[0][tid] = 0u, s_smax[1][tid] = 0u;
+        s_scnt[0][tid] = 0u, s_scnt[1][tid] = 0u;
+    }
+    // STATS: thread t sends entry t of a finished batch (buffer b, nb entries)
+    // and clears its slots; each thread reads only its own record slot, which
+    // only its own prefetch overwrites afterwards.
+    auto flush_stats = [&](int b, int nb) {
+        if (STATS && tid < nb && s_scnt[b][tid]) {
+            const uint32_t idx = s_col[b][tid].idx;
+            atomicMax(p.max_w_bits + idx, s_smax[b][tid]);
+            atomicAdd(p.count + idx, s_scnt[b][tid]);
+            s_smax[b][tid] = 0u;
+            s_scnt[b][tid] = 0u;
+        }
+    };
+    int prev_nb = 0;
 
     float T = 1.0f, cr = 0.0f, cg = 0.0f, cb = 0.0f, med = 0.0f;
     float dA = 0.0f, dD1 = 0.0f, dD2 = 0.0f, dD = 0.0f, zref = 0.0f;
@@ -101,6 +124,7 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
     for (uint32_t base = start; base < end; base += 256, buf ^= 1) {
         cp_async_wait<0>();
         if (__syncthreads_count(!done) == 0) break;
+        flush_stats(buf ^ 1, prev_nb);   // the previous batch, before its buffer is refilled
         // Prefetch the next batch into the other buffer (free: every thread
         // has passed the barrier, so nobody still reads the batch before).
         const uint32_t nbase = base + 256;
@@ -112,6 +136,7 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
             next_idx = nbase + 256u + uint32_t(tid) < end ? p.vals[nbase + 256u + tid] : 0u;
         }
         const int nb = int(min(256u, end - base));
+        prev_nb = nb;
         if (!__any_sync(0xffffffffu, !done)) continue;
         int cnt = 0;
 #pragma unroll
@@ -168,9 +193,8 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
             if (STATS && m) {
                 const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(wblend));
                 if (lane == 0) {
-                    const uint32_t idx = s_col[buf][j].idx;
-                    atomicMax(p.max_w_bits + idx, wmax);
-                    atomicAdd(p.count + idx, uint32_t(__popc(m)));
+                    atomicMax(&s_smax[buf][j], wmax);
+                    atomicAdd(&s_scnt[buf][j], uint32_t(__popc(m)));
                 }
             }
             if (__all_sync(0xffffffffu, done)) break;
@@ -181,6 +205,10 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
             if (base + uint32_t(k) < p.n_pairs) gm[k] = s_mask[warp][k];
     }
     cp_async_wait<0>();  // no copy may outlive the CTA
+    if (STATS) {
+        __syncthreads();                 // every warp is done with the last batch
+        flush_stats(buf ^ 1, prev_nb);   // (the loop toggled buf past it)
+    }
     if (inside) {
         const size_t HW = size_t(p.W) * p.H, pix = size_t(y) * p.W + x;
         p.image[pix] = fmaf(T, p.bg[0], cr);
