@@ -15,8 +15,9 @@
 // With SS_WEIGHT_STATS (the STATS variant) the warp also takes, per splat
 // that any of its pixels blended, the maximum blend weight alpha T (a warp
 // max of the float bits, which order like the values for w >= 0) and the
-// number of blending pixels (the mask's popcount), and adds them to the
-// splat's statistics with one atomicMax and one atomicAdd.
+// number of blending pixels (the mask's popcount); the CTA's warps combine
+// them in shared memory per batch entry, and when the batch is done one
+// atomicMax and one atomicAdd per (tile, splat) go to the splat.
 //
 // With SS_DISTORTION (the DIST variant) each pixel also keeps running totals
 // of its blended splats' weights and depths, A = sum w, D1 = sum w z',
