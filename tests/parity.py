@@ -38,6 +38,47 @@ def flags_of(scene) -> int:
         (ss.SS_DISTORTION if getattr(scene, "distortion", False) else 0)
 
 
+def run_gpu_graph(scene):
+    """The step as bench.py times it: pair buffers of 2.5 n, one synchronous
+    step to size them, then the CUDA graph of bin -> sort on the device-side
+    pair count -> forward -> backward, replayed twice; numpy copies of the
+    outputs of the last replay (the binned, unsorted pairs are not kept by
+    this path, so the multiset check uses the sorted ones)."""
+    dev = torch.device("cuda")
+    sp = ss.Splats.from_numpy(scene, dev)
+    flags = flags_of(scene)
+    r = ss.Rasterizer(scene.W, scene.H, scene.n, int(2.5 * scene.n), flags, bg=scene.bg,
+                      device=dev)
+    dL = torch.from_numpy(scene.dL_dimage).to(dev).contiguous()
+    dLd = (torch.from_numpy(scene.dL_ddist).to(dev).contiguous()
+           if flags & ss.SS_DISTORTION else None)
+    r.step(sp, dL, dL_ddist=dLd)
+    g = r.capture(sp, dL, dL_ddist=dLd)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    r.check()
+    st, pairs, culled = ss.ss_pair_count(r.counters, r.capacity)
+    assert st == ss.SS_OK
+    out = {"count": pairs, "culled": culled, "sort_status": ss.ss_sort_status(r.workspace)}
+    out["keys"] = r.keys[:pairs].cpu().numpy().view(np.uint64).copy()
+    out["vals"] = r.vals[:pairs].cpu().numpy().view(np.uint32).copy()
+    out["keys_binned"], out["vals_binned"] = out["keys"], out["vals"]
+    out["offs"] = r.tile_offsets.cpu().numpy().view(np.uint32).copy()
+    out["image"] = r.image.cpu().numpy()
+    out["T_final"] = r.T_final.cpu().numpy()
+    out["last"] = r.last_contrib.cpu().numpy().view(np.uint32)
+    out["median"] = r.median_depth.cpu().numpy() if r.median_depth is not None else None
+    out["dist"] = r.distortion.cpu().numpy() if r.distortion is not None else None
+    for k in GRAD_FIELDS + (DIST_FIELD,):
+        out[k] = r.grads[k].cpu().numpy() if k in r.grads else None
+    out["accum"] = r.accum_weight.cpu().numpy() if r.accum_weight is not None else None
+    out["max_w"] = r.max_weight.cpu().numpy() if r.max_weight is not None else None
+    out["bcount"] = (r.blend_count.cpu().numpy().view(np.uint32)
+                     if r.blend_count is not None else None)
+    return out
+
+
 def run_gpu(scene, capacity=None, stream=None):
     """Whole path through the C ABI; returns numpy copies of every stage."""
     dev = torch.device("cuda")
@@ -214,10 +255,11 @@ def full_parity(scene, capacity=None):
     return {"fwd": f, "stats": s, "bwd": b, "pairs": tl["count"]}
 
 
-def sampled_parity(scene, n_tiles=192, n_splats=256, seed=0):
+def sampled_parity(scene, n_tiles=192, n_splats=256, seed=0, graph=False):
     """Full-size check: every pair, sort and offset; the forward on a sample
-    of tiles; the gradients of a sample of splats (all of their tiles)."""
-    gpu = run_gpu(scene)
+    of tiles; the gradients of a sample of splats (all of their tiles).
+    graph=True runs the step the way bench.py times it (run_gpu_graph)."""
+    gpu = run_gpu_graph(scene) if graph else run_gpu(scene)
     tl = check_pairs(scene, gpu)
     tx, ty = oracle.tiles_xy(scene.W, scene.H)
     T = tx * ty

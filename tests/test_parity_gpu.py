@@ -37,6 +37,15 @@ def test_workload_full_size_sampled_parity(P, wl):
     print("workload", wl, r)
 
 
+@pytest.mark.parametrize("wl", [4, 6])
+def test_full_size_in_the_benchmarked_launch_configuration(P, wl):
+    """The 2M-splat workloads through the captured CUDA graph with the pair
+    count on the device and 2.5 n pair buffers -- the launches bench.py
+    times -- against the oracle on sampled tiles and splats."""
+    r = P.sampled_parity(synth.make_scene(wl), n_tiles=256, n_splats=512, seed=7, graph=True)
+    print("workload", wl, "graph path", r)
+
+
 def test_workload_3_with_distortion(P):
     sc = synth.make_scene(3)
     sc.distortion = True
