@@ -341,3 +341,12 @@ def test_random_scenes(P, seed):
     sc.bg = rng.uniform(0, 1, 3).astype(np.float32)
     r = P.full_parity(sc)
     print(seed, W, H, n, r["pairs"])
+
+
+@pytest.mark.parametrize("W,H", [(32768, 40), (40, 32768)])
+def test_maximum_side_length(P, W, H):
+    """The longest image side the ABI accepts (32,768 px), with a ragged
+    other side: 2,048 x 3 tiles (13 tile-id bits), compared in full."""
+    sc = _scene(W, H, 4000, seed=14, wl=3)
+    r = P.full_parity(sc)
+    assert r["pairs"] > 4000
