@@ -59,7 +59,8 @@ def test_lambda_extremes(run, lam):
     _check(run, x, y, lam)
 
 
-@pytest.mark.parametrize("C,H,W", [(1, 1, 1), (1, 5, 3), (2, 33, 65), (3, 31, 97), (4, 70, 40)])
+@pytest.mark.parametrize("C,H,W", [(1, 1, 1), (1, 5, 3), (2, 33, 65), (3, 31, 97), (4, 70, 40),
+                                   (1, 32768, 3), (2, 5, 32768)])
 def test_ragged_and_tiny(run, C, H, W):
     x, y = make_image_pair(21, seed=C * 100 + H, C=C, H=H, W=W)
     _check(run, x, y)
