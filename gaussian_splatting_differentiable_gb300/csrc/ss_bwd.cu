@@ -102,6 +102,20 @@ constexpr int kSlotPad = 32;   // entries per slot row (one per pixel of the war
 // (r, h) takes pixels 2i + h, hit 32 distinct bank pairs.
 __device__ __forceinline__ int slot_col(int row, int pix) { return pix ^ ((row & 7) << 1); }
 
+// 32 x 32 bit transpose across the warp: on return, bit k of lane p's word
+// is bit p of lane k's word on entry (five butterfly stages of shuffles).
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+    constexpr uint32_t kMask[5] = {0x0000ffffu, 0x00ff00ffu, 0x0f0f0f0fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int s = 0; s < 5; ++s) {
+        const int j = 16 >> s;
+        const uint32_t m = kMask[s];
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+        x = (lane & j) ? ((x & ~m) | ((y >> j) & m)) : ((x & m) | ((y & m) << j));
+    }
+    return x;
+}
+
 __device__ __forceinline__ float rcp_approx(float x) {
     float y;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -379,14 +393,12 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
             for (int hq = cnt; hq > 0; hq -= kChunk) {
                 const int lq = hq > kChunk ? hq - kChunk : 0;
                 const int nq = hq - lq;
-                // 1. This pixel's bit of each entry's mask.
-                uint32_t mine = 0;
-#pragma unroll
-                for (int k = 0; k < kChunk; ++k)
-                    if (k < nq) mine |= ((lmask[lq + k] >> lane) & 1u) << k;
-                // 2. One slot row per entry: zero my column; lane k copies
-                //    entry k's replay data next to the others' and records
-                //    the splat for the flush.
+                // 1. This pixel's bit of each entry's mask: lane k holds entry
+                //    k's mask, and the warp transposes the 32 x 32 bit matrix.
+                const uint32_t mine0 = warp_transpose32(lane < nq ? lmask[lq + lane] : 0u, lane);
+                // 2. One slot row per entry, zeroed (16 bytes a lane, two rows
+                //    per store); lane k copies entry k's replay data next to
+                //    the others' and records the splat for the flush.
                 const int nrows = nq;
                 if (nslots + nrows > kSlots) {
                     flush_slots<ACCUM, AOS, DIST>(p, nslots, lane, wx0, wy0, s_qw[warp],
@@ -394,8 +406,11 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                                                   s_rec[warp]);
                     nslots = 0;
                 }
-                for (int r = 0; r < nrows; ++r)
-                    s_qw[warp][nslots + r][lane] = make_float2(0.0f, 0.0f);
+                {
+                    float4 *z = reinterpret_cast<float4 *>(&s_qw[warp][nslots][0]);
+                    for (int i = lane; i < nrows * (kSlotPad / 2); i += 32)
+                        z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
                 if (lane < nq) {
                     const int j = list[lq + lane];
                     const SplatGeo g = s_geo[j];
@@ -408,6 +423,7 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                 }
                 __syncwarp();
                 // 3. Each pixel walks only its own blended entries, back to front.
+                uint32_t mine = mine0;
                 while (mine) {
                     const int k = 31 - __clz(mine);
                     mine &= ~(1u << k);
