@@ -198,7 +198,10 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
                     atomicAdd(&s_scnt[buf][j], uint32_t(__popc(m)));
                 }
             }
-            if (__all_sync(0xffffffffu, done)) break;
+            // No per-entry exit once every pixel of the warp is done (the
+            // batch and CTA checks above end the work): the vote cost more
+            // than the entries it saved (measured 0.496 vs 0.470 ms on the
+            // 2M-splat scene, 0.520 vs 0.498 ms with the four dense blobs).
         }
         __syncwarp();
         uint32_t *gm = p.masks + size_t(warp) * size_t(p.n_pairs) + base;
