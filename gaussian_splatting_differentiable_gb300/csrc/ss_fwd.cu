@@ -160,34 +160,35 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
             const SplatGeo2 g2 = s_geo2[buf][j];
             float dx, dy;
             const float e2 = eval_e2(g, g2.C, px, py, dx, dy);
-            bool blend = false;
+            float oG;
+            const float alpha = eval_alpha(g2.o, ex2_approx(e2), oG);
+            const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
+            // skipped where alpha < 1/255 (e2 < thr; false for NaN too)
+            const bool cand = !done && e2 >= g2.thr;
+            const bool stop = cand && Tn < kTEps;
+            const bool blend = cand && !stop;
+            done = done || stop;
+            // The evaluation runs on every lane and the decisions are
+            // predicates (measured 7 % faster than branching on them).
             float wblend = 0.0f;
-            if (!done && e2 >= g2.thr) {  // else skipped (alpha < 1/255); NaN-safe
-                float oG;
-                const float alpha = eval_alpha(g2.o, ex2_approx(e2), oG);
-                const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
-                if (Tn < kTEps) {
-                    done = true;
-                } else {
-                    blend = true;
-                    const SplatCol c = s_col[buf][j];
-                    const float w = alpha * T;
-                    wblend = w;
-                    cr = fmaf(c.r, w, cr);
-                    cg = fmaf(c.g, w, cg);
-                    cb = fmaf(c.b, w, cb);
-                    if (MEDIAN && T > 0.5f) med = g2.depth;
-                    if (DIST) {
-                        if (dA == 0.0f) zref = g2.depth;   // first blend: w > 0 always
-                        const float z = g2.depth - zref;
-                        dD = fmaf(w, fmaf(z, fmaf(z, dA, -2.0f * dD1), dD2), dD);
-                        dA += w;
-                        dD1 = fmaf(w, z, dD1);
-                        dD2 = fmaf(w * z, z, dD2);
-                    }
-                    T = Tn;
-                    last = base - start + uint32_t(j) + 1u;
+            if (blend) {
+                const SplatCol c = s_col[buf][j];
+                const float w = alpha * T;
+                wblend = w;
+                cr = fmaf(c.r, w, cr);
+                cg = fmaf(c.g, w, cg);
+                cb = fmaf(c.b, w, cb);
+                if (MEDIAN && T > 0.5f) med = g2.depth;
+                if (DIST) {
+                    if (dA == 0.0f) zref = g2.depth;   // first blend: w > 0 always
+                    const float z = g2.depth - zref;
+                    dD = fmaf(w, fmaf(z, fmaf(z, dA, -2.0f * dD1), dD2), dD);
+                    dA += w;
+                    dD1 = fmaf(w, z, dD1);
+                    dD2 = fmaf(w * z, z, dD2);
                 }
+                T = Tn;
+                last = base - start + uint32_t(j) + 1u;
             }
             const uint32_t m = __ballot_sync(0xffffffffu, blend);
             if (lane == 0) s_mask[warp][j] = m;
