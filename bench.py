@@ -363,6 +363,75 @@ def measure_distortion(ss, dev, flush, steps: int, workload: int = 6, extra_flag
             "kernels_ms_per_call": {k: v[1] / v[0] for k, v in prof.items()}}
 
 
+def blended_pairs(masks, cap: int, n_pairs: int) -> int:
+    """(pixel, splat) pairs that blended: the bits set in the forward's blend
+    masks ([8][cap] words, the first n_pairs of each row in use)."""
+    import torch
+    lut = torch.tensor([bin(i).count("1") for i in range(256)], dtype=torch.int64,
+                       device=masks.device)
+    m = masks.view(8, cap)
+    return sum(int(lut[m[b, :n_pairs].contiguous().view(torch.uint8).long()].sum().item())
+               for b in range(8))
+
+
+def kernel_rooflines(kernels: dict, steps: int, n: int, P: int, HW: int, cand: int, active: int,
+                     blended: int, hbm: float, hbm_src: str, red_rate: float, accum: bool,
+                     sms: int, sm_mhz: float) -> dict:
+    """Every kernel of the step against its roofline, with the per-unit
+    algorithmic figures of the path's scope table: HBM bytes for the binning
+    and the sort; HBM bytes, L2 reductions and the plain-ALU term (FP32 + MUFU
+    instructions at SMs x 128 lanes x the SM clock under load) for the
+    rasterizers."""
+    def per_call(*names):
+        return sum(kernels[k]["ms_total"] for k in names if k in kernels) / steps
+
+    def hbm_row(nbytes, ms, model):
+        ach = nbytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "algorithmic_bytes": nbytes, "bytes_model": model,
+                "ms_per_call": ms, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "peak_source": hbm_src}
+
+    lanes = sms * 128 * sm_mhz * 1e6          # FP32 lane-instructions per second
+
+    def alu_row(evals, per_eval, ms, what):
+        t = evals * per_eval / lanes
+        return {"bound": "alu", "evaluations": evals, "instructions_per_evaluation": per_eval,
+                "what": what, "model_ms": t * 1e3, "frac": t / (ms * 1e-3),
+                "peak": "%d SMs x 128 FP32 lanes x %.0f MHz (median SM clock under load)" % (
+                    sms, sm_mhz)}
+
+    passes = kernels.get("k_sort_pass", {}).get("launches", 0) // max(1, steps)
+    out = {
+        "k_emit_pairs": hbm_row(28 * n + 12 * P, per_call("k_emit_pairs"),
+                                "28 B/splat read + 12 B/pair written"),
+        "sort (hist, scan, passes, final, ties)": hbm_row(
+            (24 * passes + 8 + 8) * P,
+            per_call("k_sort_hist", "k_sort_scan", "k_sort_pass", "k_sort_final", "k_sort_ties"),
+            "8 B/pair histogram read + 24 B/pair per pass x %d passes + 8 B/pair offsets" % passes),
+    }
+    fwd_ms = per_call("k_raster_fwd")
+    out["k_raster_fwd"] = {
+        "hbm": hbm_row(40 * P + 20 * HW, fwd_ms, "40 B/pair gather + 20 B/pixel written"),
+        "alu": alu_row(cand, 16, fwd_ms, "every candidate (pixel, splat) of every tile list, "
+                                         "~15 FP32 + 1 MUFU each"),
+    }
+    bwd_ms = per_call("k_raster_bwd")
+    nat = (10 if accum else 9) * P
+    out["k_raster_bwd"] = {
+        "hbm": hbm_row(40 * P + 20 * HW + (36 + (8 if accum else 0)) * n, bwd_ms,
+                       "40 B/pair + 20 B/pixel + %d B/splat" % (36 + (8 if accum else 0))),
+        "l2_atomic": {"bound": "l2_atomic", "atomics": nat, "model_ms": nat / red_rate * 1e3,
+                      "frac": (nat / red_rate) / (bwd_ms * 1e-3), "peak": red_rate,
+                      "unit": "atomic/s"},
+        "alu_active": alu_row(active, 47, bwd_ms, "every list entry up to each pixel's last "
+                                                  "blended splat (sum of last_contrib), ~45 FP32 "
+                                                  "+ 2 MUFU each: a replay without blend masks"),
+        "alu_blended": alu_row(blended, 47, bwd_ms, "only the (pixel, splat) pairs that "
+                                                    "blended, ~45 FP32 + 2 MUFU each"),
+    }
+    return out
+
+
 def run_ours(args, rank: int, world: int, dist):
     import torch
     try:
@@ -402,6 +471,8 @@ def run_ours(args, rank: int, world: int, dist):
     graph = r.capture(sp, dL)
     graph.replay()
     r.check()
+    torch.cuda.synchronize()
+    blended = blended_pairs(r.blend_masks, r.capacity, P)   # the graph's masks: rows of `capacity`
 
     # --- device-resident timed region (headline): graph replays
     clocks = ClockSampler(local)
@@ -607,7 +678,8 @@ def run_ours(args, rank: int, world: int, dist):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "W": scene.W, "H": scene.H, "splats": scene.n,
-                   "pairs": P, "candidate_splat_px": cand, "blended_px_splat": active,
+                   "pairs": P, "candidate_splat_px": cand, "active_px_splat": active,
+                   "blended_px_splat": blended,
                    "flags": {"accum_weight": scene.accum_weight, "median_depth": scene.median_depth},
                    "l2": "256 MB buffer written between timed steps (L2 is 129 MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -619,6 +691,11 @@ def run_ours(args, rank: int, world: int, dist):
         "kernels": kernels, "dominant_kernel": dom,
         "roofline": roofline, "roofline_atomic": roofline_atomic,
         "bwd_hbm_atomic_roofline_frac": hbm_atomic_frac,
+        "kernel_rooflines": kernel_rooflines(
+            kernels, args.steps, scene.n, P, HW, cand, active, blended, hbm,
+            hbm_src + " (MEASURED_PEAKS.json hbm_gbs)", red_rate, scene.accum_weight,
+            torch.cuda.get_device_properties(dev).multi_processor_count,
+            clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0),
         "l2_red_f32_per_s": red_rate,
         "gpu_launches": launches,
         "next_rows": next_rows,

@@ -1,0 +1,57 @@
+"""Host arithmetic of bench.py's report, on the CPU: the blended-pair count
+read from the forward's blend masks and the per-kernel roofline rows."""
+import os
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+def test_blended_pairs_counts_set_bits_of_the_used_columns_only():
+    cap, n = 7, 5
+    m = torch.zeros(8 * cap, dtype=torch.int32)
+    rows = m.view(8, cap)
+    rows[0, 0] = 0b1011                       # 3 bits
+    rows[3, 4] = -1                           # all 32 bits (0xffffffff)
+    rows[7, 2] = -(1 << 31)                   # 1 bit (0x80000000)
+    rows[5, 5] = -1                           # past n: not counted
+    rows[6, 6] = 0x0f0f                       # past n: not counted
+    assert bench.blended_pairs(m, cap, n) == 3 + 32 + 1
+
+
+def test_kernel_rooflines_divide_the_model_by_the_measured_time():
+    steps = 10
+    kernels = {
+        "k_emit_pairs": {"launches": 10, "ms_total": 0.5},
+        "k_sort_hist": {"launches": 10, "ms_total": 0.2},
+        "k_sort_scan": {"launches": 10, "ms_total": 0.05},
+        "k_sort_pass": {"launches": 60, "ms_total": 3.0},
+        "k_sort_final": {"launches": 10, "ms_total": 0.15},
+        "k_sort_ties": {"launches": 10, "ms_total": 0.05},
+        "k_raster_fwd": {"launches": 10, "ms_total": 4.0},
+        "k_raster_bwd": {"launches": 10, "ms_total": 6.0},
+    }
+    n, P, HW = 1000, 4000, 2000
+    hbm, red = 1000.0, 1e10
+    rows = bench.kernel_rooflines(kernels, steps, n, P, HW, cand=10 ** 8, active=5 * 10 ** 7,
+                                  blended=10 ** 7, hbm=hbm, hbm_src="test", red_rate=red,
+                                  accum=True, sms=100, sm_mhz=1000.0)
+    b = rows["k_emit_pairs"]
+    assert b["algorithmic_bytes"] == 28 * n + 12 * P
+    assert b["frac"] == pytest.approx((28 * n + 12 * P) / 0.05e-3 / 1e9 / hbm)
+    s = rows["sort (hist, scan, passes, final, ties)"]
+    assert s["algorithmic_bytes"] == (24 * 6 + 16) * P        # 6 passes a step
+    assert s["ms_per_call"] == pytest.approx(0.345)
+    f = rows["k_raster_fwd"]
+    lanes = 100 * 128 * 1000e6
+    assert f["alu"]["frac"] == pytest.approx(10 ** 8 * 16 / lanes / 0.4e-3)
+    assert f["hbm"]["algorithmic_bytes"] == 40 * P + 20 * HW
+    k = rows["k_raster_bwd"]
+    assert k["hbm"]["algorithmic_bytes"] == 40 * P + 20 * HW + 44 * n
+    assert k["l2_atomic"]["atomics"] == 10 * P
+    assert k["l2_atomic"]["frac"] == pytest.approx(10 * P / red / 0.6e-3)
+    assert k["alu_active"]["frac"] == pytest.approx(5e7 * 47 / lanes / 0.6e-3)
+    assert k["alu_blended"]["frac"] == pytest.approx(1e7 * 47 / lanes / 0.6e-3)
