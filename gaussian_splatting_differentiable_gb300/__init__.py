@@ -16,8 +16,9 @@ import dataclasses
 import torch
 
 from . import _lib
-from ._lib import (SS_ACCUM_WEIGHT, SS_DISTORTION, SS_ERR_CAPACITY, SS_MEDIAN_DEPTH,  # noqa: F401
-                   SS_OK, SS_WEIGHT_STATS, STATUS_NAMES, SsGrads, SsSplats)
+from ._lib import (SS_ACCUM_WEIGHT, SS_DISTORTION, SS_ERR_CAPACITY, SS_ERR_DEVICE,  # noqa: F401
+                   SS_ERR_TIMEOUT, SS_MEDIAN_DEPTH, SS_OK, SS_WEIGHT_STATS, STATUS_NAMES, SsGrads,
+                   SsSplats)
 
 _L = _lib.load()
 TILE = 16
@@ -344,7 +345,7 @@ class Rasterizer:
         self.device = torch.device(device)
         self.tiles = ((W + TILE - 1) // TILE) * ((H + TILE - 1) // TILE)
         d = self.device
-        self.counters = torch.zeros(2, dtype=torch.int64, device=d)
+        self.counters = torch.zeros(4, dtype=torch.int64, device=d)
         self.records = torch.empty(max(ss_record_bytes(n_splats), 16), dtype=torch.uint8, device=d)
         self.tile_offsets = torch.zeros(self.tiles + 1, dtype=torch.int32, device=d)
         self._alloc_pairs(max(int(pair_capacity), 1))

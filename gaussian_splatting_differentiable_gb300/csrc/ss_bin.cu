@@ -8,6 +8,9 @@
 // same thread also writes the splat's 64-byte record (derived exponent
 // coefficients, threshold, colour, depth, cull box), which the forward and
 // backward rasterizers gather by index instead of the five SoA inputs.
+// The CTA also takes the smallest and largest depth bits of its splats that
+// have pairs (warp reductions, one 64-bit atomic min and max per CTA): the
+// device-count sort sorts only the depth bits in which the pairs can differ.
 #include "ss_device.cuh"
 #include "ss_internal.h"
 #include "ss_profile.h"
@@ -20,7 +23,7 @@ struct BinParams {
     uint64_t *keys;
     uint32_t *vals;
     int64_t capacity;
-    unsigned long long *counters;  // [0] pairs, [1] culled
+    unsigned long long *counters;  // [0] pairs, [1] culled, [2] / [3] min / max depth bits
     SplatRecord *records;          // [n] 64-byte records for the rasterizers
 };
 
@@ -42,7 +45,7 @@ __global__ void __launch_bounds__(256) k_emit_pairs(BinParams p) {
 
     // Block-wide exclusive scan of the pair counts, then one 64-bit atomic
     // per CTA on the global counter (same-address atomics serialise in L2).
-    __shared__ uint32_t s_wsum[8], s_wcull[8];
+    __shared__ uint32_t s_wsum[8], s_wcull[8], s_wlo[8], s_whi[8];
     __shared__ unsigned long long s_base;
     const int warp = threadIdx.x >> 5;
     uint32_t inc = cnt;  // warp inclusive scan
@@ -52,15 +55,29 @@ __global__ void __launch_bounds__(256) k_emit_pairs(BinParams p) {
         if (lane >= o) inc += t;
     }
     const uint32_t culled = __ballot_sync(0xffffffffu, st < 0);
+    const uint32_t wlo = __reduce_min_sync(0xffffffffu, cnt ? dbits : 0xffffffffu);
+    const uint32_t whi = __reduce_max_sync(0xffffffffu, cnt ? dbits : 0u);
     if (lane == 31) s_wsum[warp] = inc;
-    if (lane == 0) s_wcull[warp] = __popc(culled);
+    if (lane == 0) {
+        s_wcull[warp] = __popc(culled);
+        s_wlo[warp] = wlo;
+        s_whi[warp] = whi;
+    }
     __syncthreads();
     uint32_t before = 0;
     if (threadIdx.x == 0) {
-        uint32_t tot = 0, tc = 0;
-        for (int w = 0; w < 8; ++w) tot += s_wsum[w], tc += s_wcull[w];
+        uint32_t tot = 0, tc = 0, lo = 0xffffffffu, hi = 0u;
+        for (int w = 0; w < 8; ++w) {
+            tot += s_wsum[w], tc += s_wcull[w];
+            lo = min(lo, s_wlo[w]);
+            hi = max(hi, s_whi[w]);
+        }
         s_base = tot ? atomicAdd(p.counters, (unsigned long long)tot) : 0ull;
         if (tc) atomicAdd(p.counters + 1, (unsigned long long)tc);
+        if (tot) {
+            atomicMin(p.counters + 2, (unsigned long long)lo);
+            atomicMax(p.counters + 3, (unsigned long long)hi);
+        }
     }
     for (int w = 0; w < warp; ++w) before += s_wsum[w];
     __syncthreads();
@@ -105,7 +122,9 @@ extern "C" ss_status ss_bin_tiles(const ss_splats *splats, int32_t W, int32_t H,
         (splats->n > 0 && (reinterpret_cast<uintptr_t>(splats->mean2d) & 7)))
         return fail(SS_ERR_INVALID_ARG, "ss_bin_tiles: keys, counters and mean2d need 8-byte alignment");
     cudaStream_t st = (cudaStream_t)stream;
-    ss_status s = check_cuda(cudaMemsetAsync(d_counters, 0, 16, st), "ss_bin_tiles: memset");
+    ss_status s = check_cuda(cudaMemsetAsync(d_counters, 0, 32, st), "ss_bin_tiles: memset");
+    if (s == SS_OK)  // [2] = the largest u64: no depth seen yet
+        s = check_cuda(cudaMemsetAsync(d_counters + 2, 0xff, 8, st), "ss_bin_tiles: memset");
     if (s != SS_OK || splats->n == 0) return s;
     BinParams p{};
     p.s = SplatPtrs{splats->mean2d, splats->conic, splats->opacity, splats->rgb, splats->depth,

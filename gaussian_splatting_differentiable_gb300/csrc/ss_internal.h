@@ -29,12 +29,15 @@ ss_status check_cuda(cudaError_t e, const char *what);
 inline int32_t tiles_x(int32_t W) { return (W + kTile - 1) / kTile; }
 inline int32_t tiles_y(int32_t H) { return (H + kTile - 1) / kTile; }
 
-// Number of 8-bit digits in a (tile << 32 | depth bits) key for `tiles` tiles.
-inline int sort_digits(int64_t tiles) {
-    int tile_bits = 0;
-    while (tile_bits < 32 && (int64_t(1) << tile_bits) < tiles) ++tile_bits;
-    return (32 + tile_bits + 7) / 8;
+// Bits of a tile id for `tiles` tiles (ceil log2).
+inline int tile_bits(int64_t tiles) {
+    int b = 0;
+    while (b < 32 && (int64_t(1) << b) < tiles) ++b;
+    return b;
 }
+
+// Number of 8-bit digits in a (tile << 32 | depth bits) key for `tiles` tiles.
+inline int sort_digits(int64_t tiles) { return (32 + tile_bits(tiles) + 7) / 8; }
 
 // Workspace layout.  The first 256 bytes hold the device status word of the
 // last sort; the rest is shared by ss_sort_pairs and ss_raster_bwd.

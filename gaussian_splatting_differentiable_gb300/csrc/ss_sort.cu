@@ -24,7 +24,12 @@
 //   k_sort_ties   one CTA per long run: a stable radix sort of its indices
 //                 in global memory (no quadratic insertion sort, whatever
 //                 the number of equal depths).
-// Only 32 + ceil(log2 tiles) key bits are sorted.
+// Only 32 + ceil(log2 tiles) key bits are sorted -- and with the depth range
+// that the binning recorded (the device-count sort), only the depth bits in
+// which two pairs can differ: each kernel maps a key to
+// (tile << db) | (depth bits - lo) on db + ceil(log2 tiles) bits and takes
+// its digits from that; passes past the last digit return at once, and the
+// final kernels find the sorted data by the parity of the passes run.
 #include "ss_device.cuh"
 #include "ss_internal.h"
 #include "ss_profile.h"
@@ -44,6 +49,34 @@ __device__ __forceinline__ uint64_t ld_relaxed(const uint64_t *p) {
 
 __device__ __forceinline__ void st_relaxed(uint64_t *p, uint64_t v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// The sorted key bits: identity (lo = 0, db = 32, nd = ndig) unless dr holds
+// a recorded depth-bit range [dr[0], dr[1]]; then lo = dr[0] with its low 16
+// bits cleared, db = max(16, bits of dr[1] - lo) and nd = the 8-bit digits of
+// the db + tile_bits bit key.
+struct KeyMap {
+    uint32_t lo;
+    int db, nd;
+};
+
+__device__ __forceinline__ KeyMap key_map(const unsigned long long *dr, int tile_bits, int ndig) {
+    KeyMap m{0u, 32, ndig};
+    if (dr) {
+        const unsigned long long lo64 = dr[0], hi64 = dr[1];
+        if (lo64 <= hi64 && hi64 <= 0xffffffffull) {
+            m.lo = uint32_t(lo64) & 0xffff0000u;
+            m.db = max(16, 32 - __clz(int(uint32_t(hi64) - m.lo)));
+            m.nd = min(ndig, (m.db + tile_bits + 7) / 8);
+        }
+    }
+    return m;
+}
+
+// The key as sorted: (tile << db) | (depth bits - lo); the identity map
+// returns the key itself.
+__device__ __forceinline__ uint64_t mapped_key(uint64_t key, const KeyMap &m) {
+    return ((key >> 32) << m.db) | uint64_t(uint32_t(key) - m.lo);
 }
 
 // Number of pairs to sort: n_max, or the device count *dn clamped to n_max.
@@ -78,17 +111,24 @@ __device__ __forceinline__ uint32_t block_excl_scan256(uint32_t v, uint32_t *s_w
 }
 
 __global__ void __launch_bounds__(256) k_sort_hist(const uint64_t *__restrict__ keys, int64_t n_max,
-                                                   const unsigned long long *dn, int ndig,
-                                                   uint32_t *__restrict__ hist) {
+                                                   const unsigned long long *dn,
+                                                   const unsigned long long *dr, int tile_bits,
+                                                   int ndig, uint32_t *__restrict__ hist,
+                                                   uint32_t *err) {
     __shared__ uint32_t s_h[8][256];
     const int64_t n = pair_count(dn, n_max);
+    const KeyMap m = key_map(dr, tile_bits, ndig);
     for (int k = threadIdx.x; k < 8 * 256; k += 256) (&s_h[0][0])[k] = 0;
     __syncthreads();
     const int64_t stride = int64_t(gridDim.x) * 256;
+    bool bad = false;
     for (int64_t i = int64_t(blockIdx.x) * 256 + threadIdx.x; i < n; i += stride) {
         const uint64_t k = keys[i];
-        for (int d = 0; d < ndig; ++d) atomicAdd(&s_h[d][(k >> (8 * d)) & 255u], 1u);
+        bad |= m.db < 32 && ((uint32_t(k) - m.lo) >> m.db) != 0u;   // depth outside the range
+        const uint64_t v = mapped_key(k, m);
+        for (int d = 0; d < m.nd; ++d) atomicAdd(&s_h[d][(v >> (8 * d)) & 255u], 1u);
     }
+    if (bad) atomicOr(err, kDevErrKeyRange);
     __syncthreads();
     for (int k = threadIdx.x; k < ndig * 256; k += 256) {
         const uint32_t v = (&s_h[0][0])[k];
@@ -115,6 +155,8 @@ struct PassParams {
     uint32_t *ticket;
     uint32_t *err;
     const unsigned long long *dn;  // device pair count (clamped to n), or null
+    const unsigned long long *dr;  // device depth-bit range [lo, hi], or null (identity map)
+    int tile_bits, ndig;
 };
 
 __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
@@ -129,6 +171,8 @@ __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
     uint32_t *s_vals = reinterpret_cast<uint32_t *>(s_dyn + kSortPart * 8);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const KeyMap km = key_map(p.dr, p.tile_bits, p.ndig);
+    if (p.shift / 8 >= km.nd) return;   // past the last digit of the mapped key
     if (tid == 0) s_part = atomicAdd(p.ticket, 1u);
     for (int k = tid; k < 8 * 256; k += 256) (&s_whist[0][0])[k] = 0;
     __syncthreads();
@@ -157,7 +201,7 @@ __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
     for (int j = 0; j < KPT; ++j) {
         const int64_t idx = wbase + j * 32 + lane;
         const bool ok = idx < p.n;
-        const uint32_t dig = ok ? uint32_t(key[j] >> p.shift) & 255u : 256u + lane;
+        const uint32_t dig = ok ? uint32_t(mapped_key(key[j], km) >> p.shift) & 255u : 256u + lane;
         const uint32_t peers = __match_any_sync(0xffffffffu, dig);
         const uint32_t before = __popc(peers & lt);
         uint32_t cur = 0;
@@ -214,7 +258,7 @@ __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
     for (int j = 0; j < KPT; ++j) {
         const int64_t idx = wbase + j * 32 + lane;
         if (idx < p.n) {
-            const uint32_t dig = uint32_t(key[j] >> p.shift) & 255u;
+            const uint32_t dig = uint32_t(mapped_key(key[j], km) >> p.shift) & 255u;
             const uint32_t pos = s_lstart[dig] + s_whist[warp][dig] + rank[j];
             s_keys[pos] = key[j];
             s_vals[pos] = val[j];
@@ -225,7 +269,7 @@ __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
     const int cnt = int(left < kSortPart ? left : kSortPart);
     for (int i = tid; i < cnt; i += 256) {
         const uint64_t k = s_keys[i];
-        const uint32_t dig = uint32_t(k >> p.shift) & 255u;
+        const uint32_t dig = uint32_t(mapped_key(k, km) >> p.shift) & 255u;
         const uint32_t g = s_gbase[dig] + uint32_t(i) - s_lstart[dig];
         p.kout[g] = k;
         p.vout[g] = s_vals[i];
@@ -240,11 +284,18 @@ __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
 //  - when src != dst the element is copied (run members by the run head).
 constexpr int kTieInsert = 32;   // longest run of equal keys sorted by insertion
 
-__global__ void __launch_bounds__(256) k_sort_final(const uint64_t *__restrict__ sk,
-                                                    uint32_t *sv, uint64_t *dk, uint32_t *dv,
-                                                    int64_t n_max, const unsigned long long *dn,
-                                                    int64_t tiles, uint32_t *offs, uint32_t *err,
-                                                    uint32_t *tie_count, uint2 *ties) {
+__global__ void __launch_bounds__(256) k_sort_final(uint64_t *dk, uint32_t *dv, uint64_t *ak,
+                                                    uint32_t *av, int64_t n_max,
+                                                    const unsigned long long *dn,
+                                                    const unsigned long long *dr, int tile_bits,
+                                                    int ndig, int64_t tiles, uint32_t *offs,
+                                                    uint32_t *err, uint32_t *tie_count,
+                                                    uint2 *ties) {
+    // the passes ping-pong between (dk, dv) and (ak, av): after nd of them
+    // the sorted data is in (ak, av) iff nd is odd
+    const bool alt = key_map(dr, tile_bits, ndig).nd & 1;
+    const uint64_t *__restrict__ sk = alt ? ak : dk;
+    uint32_t *sv = alt ? av : dv;
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t n = pair_count(dn, n_max);
     if (i == 0 && dn && *dn > (unsigned long long)n_max) atomicOr(err, kDevErrCapacity);
@@ -374,12 +425,17 @@ __device__ void segment_sort_global(uint64_t *ak, uint32_t *av, uint64_t *bk, ui
 // One CTA per long run of equal keys (grid-stride over the list that
 // k_sort_final filled): the run's indices in ascending order.  (ok, ov) is
 // the other buffer, scratch for the radix passes.
-__global__ void __launch_bounds__(256) k_sort_ties(uint64_t *sk, uint32_t *sv, uint64_t *dk,
-                                                   uint32_t *dv, uint64_t *ok_, uint32_t *ov,
+__global__ void __launch_bounds__(256) k_sort_ties(uint64_t *dk, uint32_t *dv, uint64_t *ak,
+                                                   uint32_t *av, const unsigned long long *dr,
+                                                   int tile_bits, int ndig,
                                                    const uint32_t *tie_count, const uint2 *ties) {
     __shared__ uint32_t s_wc[8 * 256];
     __shared__ uint32_t s_cnt[256];
     __shared__ uint32_t s_warp[8];
+    // source: the passes' last output buffer; scratch: the other one
+    const bool alt = key_map(dr, tile_bits, ndig).nd & 1;
+    uint64_t *sk = alt ? ak : dk, *ok_ = alt ? dk : ak;
+    uint32_t *sv = alt ? av : dv, *ov = alt ? dv : av;
     const uint32_t nt = *tie_count;
     for (uint32_t r = blockIdx.x; r < nt; r += gridDim.x) {
         const uint2 run = ties[r];
@@ -452,7 +508,10 @@ static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int6
 
     const int64_t blocks = (n_max + 255) / 256;
     const int hgrid = int(blocks < int64_t(sms) * 4 ? blocks : int64_t(sms) * 4);
-    SS_LAUNCH("k_sort_hist", st, k_sort_hist<<<hgrid, 256, 0, st>>>(keys, n_max, dn, L.ndig, hist));
+    const unsigned long long *dr = dn ? dn + 2 : nullptr;   // depth-bit range from the binning
+    const int tbits = tile_bits(tiles);
+    SS_LAUNCH("k_sort_hist", st,
+              k_sort_hist<<<hgrid, 256, 0, st>>>(keys, n_max, dn, dr, tbits, L.ndig, hist, err));
     SS_LAUNCH("k_sort_scan", st, k_sort_scan<<<L.ndig, 256, 0, st>>>(hist, gofs));
     uint64_t *bk[2] = {keys, ak};
     uint32_t *bv[2] = {vals, av};
@@ -469,19 +528,22 @@ static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int6
         p.ticket = tickets + d;
         p.err = err;
         p.dn = dn;
+        p.dr = dr;
+        p.tile_bits = tbits;
+        p.ndig = L.ndig;
         SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<int(L.nparts), 256, dyn, st>>>(p));
     }
-    const int r = L.ndig & 1;
     uint32_t *tie_count = tickets + 8;
     uint2 *ties = reinterpret_cast<uint2 *>(ws + L.ties);
     SS_LAUNCH("k_sort_final", st,
-              k_sort_final<<<int(blocks), 256, 0, st>>>(bk[r], bv[r], keys, vals, n_max, dn, tiles,
-                                                        tile_offsets, err, tie_count, ties));
+              k_sort_final<<<int(blocks), 256, 0, st>>>(keys, vals, ak, av, n_max, dn, dr, tbits,
+                                                        L.ndig, tiles, tile_offsets, err,
+                                                        tie_count, ties));
     const int64_t max_runs = n_max / (kTieInsert + 1) + 1;
     const int tgrid = int(max_runs < int64_t(sms) * 2 ? max_runs : int64_t(sms) * 2);
     SS_LAUNCH("k_sort_ties", st,
-              k_sort_ties<<<tgrid, 256, 0, st>>>(bk[r], bv[r], keys, vals, bk[r ^ 1], bv[r ^ 1],
-                                                 tie_count, ties));
+              k_sort_ties<<<tgrid, 256, 0, st>>>(keys, vals, ak, av, dr, tbits, L.ndig, tie_count,
+                                                 ties));
     return check_launch(who);
 }
 
@@ -542,6 +604,7 @@ extern "C" ss_status ss_test_sort_wait_timeout(void *workspace, size_t workspace
     p.lookback = reinterpret_cast<uint64_t *>(ws + L.lookback);
     p.ticket = tickets;
     p.err = reinterpret_cast<uint32_t *>(ws + L.status_word);
+    p.ndig = L.ndig;   // no depth range: the identity map, pass 0 active
     SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<1, 256, kSortPart * 12, st>>>(p));
     return check_launch("ss_test_sort_wait_timeout");
 }

@@ -125,10 +125,13 @@ size_t ss_workspace_bytes(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t 
  *   vals[p] = splat index
  * A splat is culled (no pairs, counted) unless all its inputs are finite,
  * depth > 0, a > 0, c > 0, ac - b^2 > 0 and 1/255 <= opacity.
- * Pairs are written in no particular order (a warp-aggregated atomic counter
- * hands out slots); pairs beyond `capacity` are counted but not written.
- *   d_counters: device uint64[2]; zeroed here, then [0] = pairs needed,
- *               [1] = culled splats.
+ * Pairs are written in no particular order (each CTA takes its slots from an
+ * atomic counter); pairs beyond `capacity` are counted but not written.
+ *   d_counters: device uint64[4], 8-byte aligned; set here, then
+ *               [0] = pairs needed, [1] = culled splats,
+ *               [2] / [3] = the smallest / largest float bits of the depth of
+ *               a splat that has pairs (2^64 - 1 / 0 if no splat has any);
+ *               ss_sort_pairs_dev reads [0], [2] and [3].
  *   keys, vals: device, `capacity` entries each (may be NULL if capacity 0).
  *   records: device, ss_record_bytes(n) bytes, 16-byte aligned; receives one
  *            64-byte record per splat (its position, base-2 exponent
@@ -177,8 +180,14 @@ ss_status ss_sort_pairs(uint64_t *keys, uint32_t *vals, int64_t n_pairs, int32_t
  * without a synchronisation (and captured in a CUDA graph); the grids are
  * sized for `capacity` and the surplus CTAs exit at once.  If the count
  * exceeded the capacity, ss_sort_status reports SS_ERR_CAPACITY (the first
- * `capacity` pairs were sorted; re-bin with a larger buffer).  workspace:
- * >= ss_workspace_bytes(0, capacity, W, H) bytes. */
+ * `capacity` pairs were sorted; re-bin with a larger buffer).  The depth
+ * range d_counters[2..3] lets the radix passes skip the depth bits that no
+ * two pairs can differ in: the depth part is sorted as (bits - lo) on
+ * max(16, ceil log2(hi - lo + 1)) bits, lo = d_counters[2] with its low 16
+ * bits cleared (one 8-bit pass fewer for depths in [1, 100]); a key whose
+ * depth bits are outside [lo, lo + 2^that) records SS_ERR_DEVICE.  The result
+ * is the same order.  workspace: >= ss_workspace_bytes(0, capacity, W, H)
+ * bytes. */
 ss_status ss_sort_pairs_dev(uint64_t *keys, uint32_t *vals, const uint64_t *d_counters,
                             int64_t capacity, int32_t W, int32_t H, uint32_t *tile_offsets,
                             void *workspace, size_t workspace_bytes, ss_stream_t stream);

@@ -279,6 +279,65 @@ def test_device_count_sort_of_no_pairs(P):
     assert np.all(r.tile_offsets.cpu().numpy() == 0)
 
 
+def _bin_for_sort(sc, cap_factor=8):
+    import gaussian_splatting_differentiable_gb300 as ss
+    sp = ss.Splats.from_numpy(sc)
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, cap_factor * sc.n, 0)
+    ss.ss_bin_tiles(sp, sc.W, sc.H, r.keys, r.vals, r.capacity, r.counters, r.records)
+    st, n, _ = ss.ss_pair_count(r.counters, r.capacity)
+    assert st == ss.SS_OK
+    keys = r.keys[:n].cpu().numpy().view(np.uint64).copy()
+    vals = r.vals[:n].cpu().numpy().view(np.uint32).copy()
+    return r, n, keys, vals
+
+
+@pytest.mark.parametrize("kind", ["wide", "narrow", "equal", "three_values"])
+def test_device_count_sort_over_the_recorded_depth_range(P, kind):
+    """The device-count sort takes its digits from (tile, depth bits - lo)
+    on the bits the recorded depth range needs (fewer passes when the range
+    is narrow); the order must still be (key, value): checked against a
+    lexsort of the binned pairs, with the range the binning recorded
+    checked against the splats that have pairs."""
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = _scene(300, 200, 20000, seed=21)
+    rng = np.random.default_rng(21)
+    if kind == "wide":        # every exponent from 1e-3 to 1e5: all 32 depth bits
+        sc.depth[:] = (10.0 ** rng.uniform(-3, 5, sc.n)).astype(np.float32)
+    elif kind == "narrow":    # a few ulps apart: the 16-bit minimum
+        sc.depth[:] = rng.uniform(2.0, 2.001, sc.n).astype(np.float32)
+    elif kind == "equal":
+        sc.depth[:] = np.float32(3.0)
+    else:
+        sc.depth[:] = rng.choice(np.float32([1.5, 7.25, 40.0]), sc.n)
+    r, n, keys, vals = _bin_for_sort(sc)
+    cnt = r.counters.cpu().numpy().view(np.uint64)
+    dbits = sc.depth.view(np.uint32)[vals]
+    assert cnt[2] == dbits.min() and cnt[3] == dbits.max()
+    ss.ss_sort_pairs_dev(r.keys, r.vals, r.counters, r.capacity, sc.W, sc.H, r.tile_offsets,
+                         r.workspace)
+    assert ss.ss_sort_status(r.workspace) == ss.SS_OK
+    order = np.lexsort((vals, keys))
+    assert np.array_equal(r.keys[:n].cpu().numpy().view(np.uint64), keys[order])
+    assert np.array_equal(r.vals[:n].cpu().numpy().view(np.uint32), vals[order])
+    tiles = ((sc.W + 15) // 16) * ((sc.H + 15) // 16)
+    want = np.searchsorted(keys[order] >> np.uint64(32), np.arange(tiles + 1, dtype=np.uint64))
+    assert np.array_equal(r.tile_offsets.cpu().numpy().view(np.uint32), want.astype(np.uint32))
+
+
+def test_device_count_sort_flags_a_depth_outside_the_recorded_range(P):
+    """Counters whose range leaves out some pair's depth (not the binning's
+    own) make the sort report SS_ERR_DEVICE instead of a wrong order."""
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = _scene(64, 64, 2000, seed=22)
+    sc.depth[:] = np.linspace(1.0, 100.0, sc.n, dtype=np.float32)
+    r, n, keys, vals = _bin_for_sort(sc)
+    hi = int(r.counters[3].item())
+    r.counters[2] = (hi - (1 << 20)) & ~0xffff      # above the smallest depths' bits
+    ss.ss_sort_pairs_dev(r.keys, r.vals, r.counters, r.capacity, sc.W, sc.H, r.tile_offsets,
+                         r.workspace)
+    assert ss.ss_sort_status(r.workspace) == ss.SS_ERR_DEVICE
+
+
 def test_long_runs_of_equal_depths_sort_bit_exact(P):
     """40,000 small splats on 2x2 tiles, a quarter of them at one depth: runs
     of ~2,500 equal keys per tile, ordered by splat index by the long-run
