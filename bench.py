@@ -374,9 +374,23 @@ def blended_pairs(masks, cap: int, n_pairs: int) -> int:
                for b in range(8))
 
 
+def sort_passes(counters, tiles: int) -> int:
+    """Radix passes the device-count sort runs: 8-bit digits of the key
+    (tile, depth bits - lo) over the depth range the binning recorded
+    (counters [2] / [3]), as the library maps it."""
+    tb = max(0, (int(tiles) - 1).bit_length())
+    full = (32 + tb + 7) // 8
+    lo64, hi64 = int(counters[2]), int(counters[3])
+    if not (lo64 <= hi64 <= 0xffffffff):
+        return full
+    lo = lo64 & 0xffff0000
+    db = max(16, (hi64 - lo).bit_length())
+    return min(full, (db + tb + 7) // 8)
+
+
 def kernel_rooflines(kernels: dict, steps: int, n: int, P: int, HW: int, cand: int, active: int,
                      blended: int, hbm: float, hbm_src: str, red_rate: float, accum: bool,
-                     sms: int, sm_mhz: float) -> dict:
+                     sms: int, sm_mhz: float, passes: int = None) -> dict:
     """Every kernel of the step against its roofline, with the per-unit
     algorithmic figures of the path's scope table: HBM bytes for the binning
     and the sort; HBM bytes, L2 reductions and the plain-ALU term (FP32 + MUFU
@@ -400,14 +414,15 @@ def kernel_rooflines(kernels: dict, steps: int, n: int, P: int, HW: int, cand: i
                 "peak": "%d SMs x 128 FP32 lanes x %.0f MHz (median SM clock under load)" % (
                     sms, sm_mhz)}
 
-    passes = kernels.get("k_sort_pass", {}).get("launches", 0) // max(1, steps)
+    if passes is None:
+        passes = kernels.get("k_sort_pass", {}).get("launches", 0) // max(1, steps)
     out = {
         "k_emit_pairs": hbm_row(28 * n + 12 * P, per_call("k_emit_pairs"),
                                 "28 B/splat read + 12 B/pair written"),
         "sort (hist, scan, passes, final, ties)": hbm_row(
             (24 * passes + 8 + 8) * P,
             per_call("k_sort_hist", "k_sort_scan", "k_sort_pass", "k_sort_final", "k_sort_ties"),
-            "8 B/pair histogram read + 24 B/pair per pass x %d passes + 8 B/pair offsets" % passes),
+            "8 B/pair histogram read + 24 B/pair per pass x %d passes run + 8 B/pair offsets" % passes),
     }
     fwd_ms = per_call("k_raster_fwd")
     out["k_raster_fwd"] = {
@@ -473,6 +488,8 @@ def run_ours(args, rank: int, world: int, dist):
     r.check()
     torch.cuda.synchronize()
     blended = blended_pairs(r.blend_masks, r.capacity, P)   # the graph's masks: rows of `capacity`
+    n_tiles = ((scene.W + 15) // 16) * ((scene.H + 15) // 16)
+    passes_run = sort_passes(r.counters.cpu().numpy().view(np.uint64), n_tiles)
 
     # --- device-resident timed region (headline): graph replays
     clocks = ClockSampler(local)
@@ -695,7 +712,8 @@ def run_ours(args, rank: int, world: int, dist):
             kernels, args.steps, scene.n, P, HW, cand, active, blended, hbm,
             hbm_src + " (MEASURED_PEAKS.json hbm_gbs)", red_rate, scene.accum_weight,
             torch.cuda.get_device_properties(dev).multi_processor_count,
-            clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0),
+            clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0, passes_run),
+        "sort_passes_run": passes_run,
         "l2_red_f32_per_s": red_rate,
         "gpu_launches": launches,
         "next_rows": next_rows,

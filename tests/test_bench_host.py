@@ -55,3 +55,16 @@ def test_kernel_rooflines_divide_the_model_by_the_measured_time():
     assert k["l2_atomic"]["frac"] == pytest.approx(10 * P / red / 0.6e-3)
     assert k["alu_active"]["frac"] == pytest.approx(5e7 * 47 / lanes / 0.6e-3)
     assert k["alu_blended"]["frac"] == pytest.approx(1e7 * 47 / lanes / 0.6e-3)
+
+
+def test_sort_passes_follow_the_recorded_depth_range():
+    import numpy as np
+    c = np.zeros(4, np.uint64)
+    c[2], c[3] = np.float32(1.0).view(np.uint32), np.float32(100.0).view(np.uint32)
+    assert bench.sort_passes(c, 4056) == 5           # 12 tile bits + 26 depth bits
+    c[3] = np.float32(1e30).view(np.uint32)
+    assert bench.sort_passes(c, 4056) == 6           # all 32 depth bits
+    c[2], c[3] = np.float32(3.0).view(np.uint32), np.float32(3.0).view(np.uint32)
+    assert bench.sort_passes(c, 16) == 3             # 16-bit floor + 4 tile bits
+    c[2], c[3] = np.uint64(2 ** 64 - 1), 0           # no pairs: the full key
+    assert bench.sort_passes(c, 4056) == 6
