@@ -151,7 +151,10 @@ __global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
             const float A2 = 2.0f * (m[4] - mx * my) + kC2;
             const float B1 = mx * mx + my * my + kC1;
             const float B2 = (m[2] - mx * mx) + (m[3] - my * my) + kC2;
-            const float iA1 = 1.0f / A1, iA2 = 1.0f / A2, iB1 = 1.0f / B1, iB2 = 1.0f / B2;
+            // the hardware reciprocal (about 1 ulp; the loss sums in double
+            // and the gradient's tolerance are far coarser)
+            const float iA1 = __fdividef(1.0f, A1), iA2 = __fdividef(1.0f, A2);
+            const float iB1 = __fdividef(1.0f, B1), iB2 = __fdividef(1.0f, B2);
             const float S = A1 * A2 * iB1 * iB2;
             const float cS = in ? p.cs * S : 0.0f;
             s.a[0][r][q] = cS * 2.0f * (my * (iA1 - iA2) - mx * (iB1 - iB2));   // d/d mu_x
