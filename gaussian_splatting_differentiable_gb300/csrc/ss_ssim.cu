@@ -51,11 +51,18 @@ struct SsimParams {
     double inv_n;
 };
 
+// The input region is dead once the horizontal pass has read it, so the
+// adjoint maps take its place (~51 KB in all: four CTAs per SM instead of
+// three); the gradient phase reads its pixel's x and y again from L2.
 struct SsimSmem {
-    float x[kIn][kIn];
-    float y[kIn][kIn];
+    union {
+        struct {
+            float x[kIn][kIn];
+            float y[kIn][kIn];
+        } in;
+        float a[3][kMom][kMom];  // adjoint maps on the moment region
+    } u;
     float h[5][kIn][kMom];   // horizontal pass: moments, then the adjoint maps
-    float a[3][kMom][kMom];  // adjoint maps on the moment region
     double red[2][kThreads / 32];
     int last;
 };
@@ -88,8 +95,8 @@ __global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
         const int k = tid + u * kThreads;
         if (k < kIn * kIn) {
             const int r = k / kIn, q = k % kIn;
-            s.x[r][q] = lx[u];
-            s.y[r][q] = ly[u];
+            s.u.in.x[r][q] = lx[u];
+            s.u.in.y[r][q] = ly[u];
         }
     }
     __syncthreads();
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
         const int r = k / (kMom / 2), q = 2 * (k % (kMom / 2));
         float xa[kW + 1], ya[kW + 1];
 #pragma unroll
-        for (int j = 0; j <= kW; ++j) xa[j] = s.x[r][q + j], ya[j] = s.y[r][q + j];
+        for (int j = 0; j <= kW; ++j) xa[j] = s.u.in.x[r][q + j], ya[j] = s.u.in.y[r][q + j];
 #pragma unroll
         for (int o = 0; o < 2; ++o) {
             float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f, m4 = 0.f;
@@ -157,9 +164,9 @@ __global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
             const float iB1 = __fdividef(1.0f, B1), iB2 = __fdividef(1.0f, B2);
             const float S = A1 * A2 * iB1 * iB2;
             const float cS = in ? p.cs * S : 0.0f;
-            s.a[0][r][q] = cS * 2.0f * (my * (iA1 - iA2) - mx * (iB1 - iB2));   // d/d mu_x
-            s.a[1][r][q] = -cS * iB2;                                            // d/d E[x^2]
-            s.a[2][r][q] = 2.0f * cS * iA2;                                      // d/d E[xy]
+            s.u.a[0][r][q] = cS * 2.0f * (my * (iA1 - iA2) - mx * (iB1 - iB2));   // d/d mu_x
+            s.u.a[1][r][q] = -cS * iB2;                                            // d/d E[x^2]
+            s.u.a[2][r][q] = 2.0f * cS * iA2;                                      // d/d E[xy]
             if (in && col_mid && r >= kR && r < kR + kT) ssim_sum += S;
         }
     }
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
         for (int t = 0; t < 3; ++t) {
             float v[kW + 1];
 #pragma unroll
-            for (int j = 0; j <= kW; ++j) v[j] = s.a[t][r][q + j];
+            for (int j = 0; j <= kW; ++j) v[j] = s.u.a[t][r][q + j];
             float v0 = 0.f, v1 = 0.f;
 #pragma unroll
             for (int j = 0; j < kW; ++j) {
@@ -208,10 +215,11 @@ __global__ void __launch_bounds__(kThreads) k_ssim(SsimParams p) {
         for (int o = 0; o < 2; ++o) {
             const int r = r0 + o, gy = y0 + r;
             if (gy >= p.H || gx >= p.W) continue;
-            const float xv = s.x[r + 2 * kR][q + 2 * kR], yv = s.y[r + 2 * kR][q + 2 * kR];
+            const size_t off = size_t(gy) * p.W + gx;
+            const float xv = __ldg(img + off), yv = __ldg(tgt + off);
             const float d = xv - yv;
             const float sg = d > 0.0f ? 1.0f : (d < 0.0f ? -1.0f : 0.0f);
-            grad[size_t(gy) * p.W + gx] =
+            grad[off] =
                 acc[0][o] + 2.0f * xv * acc[1][o] + yv * acc[2][o] + p.cl * sg;
             l1_sum += fabsf(d);
         }
