@@ -1,10 +1,7 @@
 // Tile binning ("Phase 5 step 30b -- kernel-by-kernel timing", emit_pairs:
 // tile id computation plus an atomic counter update).
 //
-// One thread per splat computes its tile rectangle -- the tiles of the
-// bounding box of the ellipse where alpha >= 1/255 is possible -- and keeps
-// the tiles whose rectangle of pixel centres the ellipse meets (tile_hit:
-// the box's corner tiles are often missed by the ellipse); the CTA scans its pair
+// One thread per splat computes its tile rectangle; the CTA scans its pair
 // counts (warp shuffles, then the eight warp totals) and one thread takes
 // the CTA's slots with a single 64-bit atomic add, so the global counter
 // sees one atomic per 256 splats rather than one per splat.  Each lane then writes its pairs into its slots.  The
@@ -35,22 +32,8 @@ __global__ void __launch_bounds__(256) k_emit_pairs(BinParams p) {
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     int x0 = 0, y0 = 0, x1 = -1, y1 = -1, st = 0;
     uint32_t dbits = 0;
-    BinGeom geo{};
-    if (i < p.s.n) st = splat_tile_rect(p.s, i, p.tiles_x, p.tiles_y, x0, y0, x1, y1, dbits, geo);
-    float ia = 0.0f, ic = 0.0f;
-    uint32_t cnt = 0u;
-    uint64_t hits = 0u;   // the test's answers for the rectangle's first 64 tiles
-    if (st > 0) {
-        ia = __fdiv_rn(1.0f, geo.a);
-        ic = __fdiv_rn(1.0f, geo.c);
-        int t = 0;
-        for (int ty = y0; ty <= y1; ++ty)
-            for (int tx = x0; tx <= x1; ++tx, ++t)
-                if (tile_hit(geo, ia, ic, tx, ty)) {
-                    ++cnt;
-                    if (t < 64) hits |= 1ull << t;
-                }
-    }
+    if (i < p.s.n) st = splat_tile_rect(p.s, i, p.tiles_x, p.tiles_y, x0, y0, x1, y1, dbits);
+    const uint32_t cnt = st > 0 ? uint32_t(x1 - x0 + 1) * uint32_t(y1 - y0 + 1) : 0u;
     if (i < p.s.n) {
         const SplatRecord r = st >= 0 ? make_record(p.s, uint32_t(i)) : invisible_record();
         float4 *dst = reinterpret_cast<float4 *>(p.records + i);
@@ -102,16 +85,13 @@ __global__ void __launch_bounds__(256) k_emit_pairs(BinParams p) {
 
     unsigned long long pos = s_base + before + (inc - cnt);
     const unsigned long long cap = (unsigned long long)p.capacity;
-    int t = 0;
     for (int ty = y0; ty <= y1; ++ty) {
         const uint64_t row = uint64_t(ty) * uint64_t(p.tiles_x);
-        for (int tx = x0; tx <= x1; ++tx, ++t) {
-            if (t < 64 ? !((hits >> t) & 1u) : !tile_hit(geo, ia, ic, tx, ty)) continue;
+        for (int tx = x0; tx <= x1; ++tx, ++pos) {
             if (pos < cap) {
                 p.keys[pos] = ((row + uint64_t(tx)) << 32) | dbits;
                 p.vals[pos] = uint32_t(i);
             }
-            ++pos;
         }
     }
 }

@@ -59,13 +59,6 @@ __device__ __forceinline__ float ln_series(float x) {
     return __fadd_rn(__fmul_rn(__int2float_rn(e), kLn2), lnm);
 }
 
-// The binning's view of a splat: its ellipse {d : d^T Q d <= k} where
-// alpha >= 1/255 is possible (Q = [[a, b], [b, c]], k = 2 ln(255 o) widened
-// by 2^-10 relative and absolute) and the tile rectangle of its bounding box.
-struct BinGeom {
-    float mx, my, a, b, c, k;
-};
-
 // Tile rectangle of splat i (inclusive tile coordinates).  Returns -1 if the
 // splat is culled (non-finite input, depth <= 0, conic not positive
 // definite, opacity < 1/255), 0 if it touches no tile of the image, else 1.
@@ -74,7 +67,7 @@ struct BinGeom {
 // sqrt(k c / det) and sqrt(k a / det), Q = [[a, b], [b, c]].
 __device__ __forceinline__ int splat_tile_rect(const SplatPtrs &s, int64_t i, int32_t tiles_x,
                                                int32_t tiles_y, int &x0, int &y0, int &x1,
-                                               int &y1, uint32_t &depth_bits, BinGeom &geo) {
+                                               int &y1, uint32_t &depth_bits) {
     const float2 mu = reinterpret_cast<const float2 *>(s.mean2d)[i];
     const float a = s.conic[3 * i], b = s.conic[3 * i + 1], c = s.conic[3 * i + 2];
     const float o = s.opacity[i], d = s.depth[i];
@@ -93,7 +86,6 @@ __device__ __forceinline__ int splat_tile_rect(const SplatPtrs &s, int64_t i, in
     const float rx = __fsqrt_rn(__fdiv_rn(__fmul_rn(k, c), det));
     const float ry = __fsqrt_rn(__fdiv_rn(__fmul_rn(k, a), det));
     if (rx != rx || ry != ry) return -1;
-    geo = BinGeom{mu.x, mu.y, a, b, c, k};
     float fx0 = floorf(__fmul_rn(__fsub_rn(mu.x, rx), 0.0625f));
     float fx1 = floorf(__fmul_rn(__fadd_rn(mu.x, rx), 0.0625f));
     float fy0 = floorf(__fmul_rn(__fsub_rn(mu.y, ry), 0.0625f));
@@ -109,38 +101,6 @@ __device__ __forceinline__ int splat_tile_rect(const SplatPtrs &s, int64_t i, in
     x1 = int(fx1);
     y1 = int(fy1);
     return 1;
-}
-
-// Does the rectangle of pixel centres of tile (tx, ty) meet the splat's
-// ellipse?  If the mean lies inside the rectangle, yes; otherwise the
-// minimum of the convex d^T Q d over the rectangle lies on an edge, where it
-// is a parabola in one coordinate whose vertex, clamped to the edge, is the
-// edge's minimum.  Every operation is an explicitly rounded float32 one, in
-// the order an independent CPU evaluation uses, so both keep the same tiles.
-__device__ __forceinline__ bool tile_hit(const BinGeom &g, float ia, float ic, int tx, int ty) {
-    const float fx = __fmul_rn(16.0f, float(tx)), fy = __fmul_rn(16.0f, float(ty));
-    const float X0 = __fsub_rn(__fadd_rn(fx, 0.5f), g.mx), X1 = __fsub_rn(__fadd_rn(fx, 15.5f), g.mx);
-    const float Y0 = __fsub_rn(__fadd_rn(fy, 0.5f), g.my), Y1 = __fsub_rn(__fadd_rn(fy, 15.5f), g.my);
-    if (X0 <= 0.0f && X1 >= 0.0f && Y0 <= 0.0f && Y1 >= 0.0f) return true;
-    const float b2 = __fmul_rn(2.0f, g.b);
-    float best = __int_as_float(0x7f800000);
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const float Y = e ? Y1 : Y0;   // edge y = Y: vertex x = -b Y / a
-        const float x = fminf(fmaxf(__fmul_rn(-__fmul_rn(g.b, Y), ia), X0), X1);
-        const float q = __fadd_rn(__fadd_rn(__fmul_rn(__fmul_rn(g.a, x), x), __fmul_rn(__fmul_rn(b2, Y), x)),
-                                  __fmul_rn(__fmul_rn(g.c, Y), Y));
-        best = fminf(best, q);
-    }
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const float X = e ? X1 : X0;   // edge x = X: vertex y = -b X / c
-        const float y = fminf(fmaxf(__fmul_rn(-__fmul_rn(g.b, X), ic), Y0), Y1);
-        const float q = __fadd_rn(__fadd_rn(__fmul_rn(__fmul_rn(g.c, y), y), __fmul_rn(__fmul_rn(b2, X), y)),
-                                  __fmul_rn(__fmul_rn(g.a, X), X));
-        best = fminf(best, q);
-    }
-    return best <= g.k;
 }
 
 // A splat as the rasterizers read it: one 64-byte record, written once by

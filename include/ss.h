@@ -117,12 +117,10 @@ const char *ss_last_error(void);
 size_t ss_workspace_bytes(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H);
 
 /* Tile binning ("Phase 5 step 30b", emit_pairs: tile id computation and an
- * atomic counter).  For each splat that is not culled, one pair per tile
- * whose rectangle of pixel centres [16 tx + 0.5, 16 tx + 15.5] x [16 ty +
- * 0.5, 16 ty + 15.5] meets the ellipse where alpha >= 1/255 is possible,
+ * atomic counter).  For each splat that is not culled, one pair per tile of
+ * the axis-aligned box of the ellipse where alpha >= 1/255 is possible,
  * {d : d^T conic d <= k}, k = 2 ln(255 opacity) widened by 2^-10 relative and
- * absolute (the tiles are searched in the ellipse's axis-aligned box, clipped
- * to the image; the test is exact in float32, each operation rounded):
+ * absolute, clipped to the image's tiles:
  *   keys[p] = tile << 32 | bits of depth (float32, > 0, so ordered as u32)
  *   vals[p] = splat index
  * A splat is culled (no pairs, counted) unless all its inputs are finite,

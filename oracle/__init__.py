@@ -97,11 +97,6 @@ def _bind(lib):
     lib.orc_splat_rect.argtypes = [P(_SplatsF), ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                    P(ctypes.c_int32)]
     lib.orc_splat_rect.restype = ctypes.c_int
-    lib.orc_splat_k.argtypes = [P(_SplatsF), ctypes.c_int64]
-    lib.orc_splat_k.restype = ctypes.c_float
-    lib.orc_tile_hit.argtypes = [P(_SplatsF), ctypes.c_int64, ctypes.c_float, ctypes.c_int32,
-                                 ctypes.c_int32]
-    lib.orc_tile_hit.restype = ctypes.c_int
     lib.orc_bin.argtypes = [P(_SplatsF), ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                             ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_int64)]
     lib.orc_bin.restype = ctypes.c_int64
@@ -157,20 +152,6 @@ def splat_rect(scene, i: int):
     r = (ctypes.c_int32 * 4)()
     v = load().orc_splat_rect(ctypes.byref(s), i, scene.W, scene.H, r)
     return v, tuple(r)
-
-
-def tile_hits(scene, i: int):
-    """(k, {(tx, ty): hit}) for splat i over the tiles of its rectangle: the
-    widened ellipse bound and the exact ellipse-vs-tile test of the binning."""
-    keep = []
-    s = _splats_f(scene, keep)
-    lib = load()
-    st, r = splat_rect(scene, i)
-    k = float(lib.orc_splat_k(ctypes.byref(s), i))
-    if st != 1:
-        return k, {}
-    return k, {(tx, ty): bool(lib.orc_tile_hit(ctypes.byref(s), i, ctypes.c_float(k), tx, ty))
-               for ty in range(r[1], r[3] + 1) for tx in range(r[0], r[2] + 1)}
 
 
 def bin_tiles(scene, capacity: int | None = None):

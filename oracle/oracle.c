@@ -20,11 +20,9 @@
  *      and T = T';
  *   R5 image = C + T_final * bg;
  *   R6 last_contrib = 1 + list position of the last blended splat (0: none);
- *   R7 binning: a splat touches the tiles whose rectangle of pixel centres
- *      meets the ellipse where alpha >= 1/255 is possible,
- *      {d : d^T conic d <= k}, k = 2 ln(255 o); they are found among the
- *      tiles of the ellipse's AABB (half widths sqrt(k c / det),
- *      sqrt(k a / det)) by the minimum of d^T conic d over each rectangle;
+ *   R7 binning: a splat touches the tiles of the AABB of the ellipse where
+ *      alpha >= 1/255 is possible, {d : d^T conic d <= 2 ln(255 o)}, whose
+ *      half widths are sqrt(k c / det), sqrt(k a / det);
  *   R8 a splat is culled (no pairs) unless every input is finite, depth > 0,
  *      a > 0, c > 0, det = ac - b^2 > 0, and 1/255 <= opacity (255 o finite);
  *   R9 pair key = tile << 32 | float bits of depth; list order is (tile,
@@ -102,60 +100,6 @@ float orc_ln(float x)
     return (float)e * 0.69314718055994531f + lnm;
 }
 
-/* The widened k of splat i (R7), or a negative value if it is culled. */
-float orc_splat_k(const orc_splats_f *s, int64_t i)
-{
-    const float mx = s->mean2d[2 * i], my = s->mean2d[2 * i + 1];
-    const float a = s->conic[3 * i], b = s->conic[3 * i + 1], c = s->conic[3 * i + 2];
-    const float o = s->opacity[i], d = s->depth[i];
-    const float *col = s->rgb + 3 * i;
-    if (!isfinite(mx) || !isfinite(my) || !isfinite(a) || !isfinite(b) || !isfinite(c) ||
-        !isfinite(o) || !isfinite(d) || !isfinite(col[0]) || !isfinite(col[1]) ||
-        !isfinite(col[2]))
-        return -1.0f;
-    if (!(d > 0.0f) || !(a > 0.0f) || !(c > 0.0f))
-        return -1.0f;
-    if (!(a * c - b * b > 0.0f))
-        return -1.0f;
-    if (!(o >= (float)ALPHA_MIN) || isinf(255.0f * o))
-        return -1.0f;
-    const float k = 2.0f * orc_ln(255.0f * o);
-    return k * K_REL + K_ABS;
-}
-
-/* Does the rectangle of pixel centres of tile (tx, ty) meet the ellipse
- * {d : q(d) <= k}, q(d) = a dx^2 + 2 b dx dy + c dy^2, d = centre - mean?
- * If the mean is inside the rectangle, yes; otherwise the minimum of the
- * convex q over the rectangle lies on an edge, where q is a parabola in one
- * coordinate: its vertex clamped to the edge is the edge's minimum.  Float32,
- * every operation rounded as written. */
-int orc_tile_hit(const orc_splats_f *s, int64_t i, float k, int32_t tx, int32_t ty)
-{
-    const float mx = s->mean2d[2 * i], my = s->mean2d[2 * i + 1];
-    const float a = s->conic[3 * i], b = s->conic[3 * i + 1], c = s->conic[3 * i + 2];
-    const float X0 = (16.0f * (float)tx + 0.5f) - mx, X1 = (16.0f * (float)tx + 15.5f) - mx;
-    const float Y0 = (16.0f * (float)ty + 0.5f) - my, Y1 = (16.0f * (float)ty + 15.5f) - my;
-    if (X0 <= 0.0f && X1 >= 0.0f && Y0 <= 0.0f && Y1 >= 0.0f)
-        return 1;
-    const float ia = 1.0f / a, ic = 1.0f / c, b2 = 2.0f * b;
-    float best = INFINITY;
-    for (int e = 0; e < 2; ++e) {
-        const float Y = e ? Y1 : Y0;          /* edge y = Y: vertex x = -b Y / a */
-        float x = -(b * Y) * ia;
-        x = fminf(fmaxf(x, X0), X1);
-        const float q = ((a * x) * x + (b2 * Y) * x) + (c * Y) * Y;
-        best = fminf(best, q);
-    }
-    for (int e = 0; e < 2; ++e) {
-        const float X = e ? X1 : X0;          /* edge x = X: vertex y = -b X / c */
-        float y = -(b * X) * ic;
-        y = fminf(fmaxf(y, Y0), Y1);
-        const float q = ((c * y) * y + (b2 * X) * y) + (a * X) * X;
-        best = fminf(best, q);
-    }
-    return best <= k;
-}
-
 int orc_splat_rect(const orc_splats_f *s, int64_t i, int32_t W, int32_t H, int32_t r[4])
 {
     const float mx = s->mean2d[2 * i], my = s->mean2d[2 * i + 1];
@@ -215,11 +159,8 @@ int64_t orc_bin(const orc_splats_f *s, int32_t W, int32_t H, uint64_t *keys, uin
             continue;
         uint32_t dbits;
         memcpy(&dbits, &s->depth[i], 4);
-        const float k = orc_splat_k(s, i);
         for (int32_t ty = r[1]; ty <= r[3]; ++ty)
             for (int32_t tx = r[0]; tx <= r[2]; ++tx) {
-                if (!orc_tile_hit(s, i, k, tx, ty))
-                    continue;
                 if (count < capacity) {
                     const uint64_t tile = (uint64_t)ty * (uint64_t)tiles_x + (uint64_t)tx;
                     keys[count] = (tile << 32) | dbits;

@@ -96,12 +96,6 @@ float orc_ln(float x);               /* natural log by the atanh series, float32
 /* -1: splat culled (invalid); 0: valid, touches no tile; 1: rect in r[4] =
  * (x0, y0, x1, y1) inclusive tile coordinates. */
 int orc_splat_rect(const orc_splats_f *s, int64_t i, int32_t W, int32_t H, int32_t r[4]);
-/* The widened ellipse bound k = 2 ln(255 o) (1 + 2^-10) + 2^-10 of splat i
- * (R7), float32 as the binning computes it; negative if the splat is culled. */
-float orc_splat_k(const orc_splats_f *s, int64_t i);
-/* 1 if tile (tx, ty)'s rectangle of pixel centres meets splat i's ellipse
- * {d^T conic d <= k} (k: the widened bound of R7), else 0. */
-int orc_tile_hit(const orc_splats_f *s, int64_t i, float k, int32_t tx, int32_t ty);
 int64_t orc_bin(const orc_splats_f *s, int32_t W, int32_t H, uint64_t *keys, uint32_t *vals,
                 int64_t capacity, int64_t *culled);
 void orc_sort(uint64_t *keys, uint32_t *vals, int64_t n);
