@@ -95,6 +95,10 @@ __device__ __forceinline__ void red_add_v2(float *addr, float a, float b) {
 }
 
 constexpr int kSlots = 16;     // slots per warp
+// A warp's list: up to 64 entries of a segment below up to kChunk - 1
+// entries left over from the segments above (chunks are always full but
+// for the batch's last).
+constexpr int kListCap = 64 + 16;
 constexpr int kChunk = 16;     // list entries evaluated together (<= kSlots)
 constexpr int kSlotPad = 32;   // entries per slot row (one per pixel of the warp's block)
 // Pixel p of slot row r is stored at column p ^ (2 (r & 7)): the replay's
@@ -251,8 +255,8 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     __shared__ SplatGeo s_geo_[2][256];
     __shared__ SplatGeo2 s_geo2_[2][256];
     __shared__ SplatCol s_col_[2][256];
-    __shared__ uint8_t s_list[8][64];
-    __shared__ uint32_t s_lmask[8][64];
+    __shared__ uint8_t s_list[8][kListCap];
+    __shared__ uint32_t s_lmask[8][kListCap];
     __shared__ ChunkEnt s_ck[8][kChunk];
     __shared__ uint32_t s_wmax[8];
     __shared__ float4 s_g[8][32];
@@ -363,6 +367,10 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
             ma = (j0 < lim && gbase + j0 < p.n_pairs) ? gm[j0] : 0u;
             mb = (j1 < lim && gbase + j1 < p.n_pairs) ? gm[j1] : 0u;
         }
+        // The listed entries of the batch, in ascending position, occupy
+        // [kListCap - npend, kListCap) between segments: the ones left over
+        // (fewer than kChunk) from the segments above.
+        int npend = 0;
         for (; sg >= 0; --sg) {
             const uint32_t ca = ma, cb = mb;
             if (sg > 0) {
@@ -370,29 +378,30 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                 ma = (j0 < lim && gbase + j0 < p.n_pairs) ? gm[j0] : 0u;
                 mb = (j1 < lim && gbase + j1 < p.n_pairs) ? gm[j1] : 0u;
             }
-            int cnt = 0;
-            {
-                const uint32_t b0 = __ballot_sync(0xffffffffu, ca != 0u);
-                if (ca) {
-                    const int at = __popc(b0 & lt);
-                    s_list[warp][at] = uint8_t(64 * sg + lane);
-                    s_lmask[warp][at] = ca;
-                }
-                cnt = __popc(b0);
-                const uint32_t b1 = __ballot_sync(0xffffffffu, cb != 0u);
-                if (cb) {
-                    const int at = cnt + __popc(b1 & lt);
-                    s_list[warp][at] = uint8_t(64 * sg + 32 + lane);
-                    s_lmask[warp][at] = cb;
-                }
-                cnt += __popc(b1);
+            // This segment's entries go just below the left-over ones.
+            const uint32_t b0 = __ballot_sync(0xffffffffu, ca != 0u);
+            const uint32_t b1 = __ballot_sync(0xffffffffu, cb != 0u);
+            const int cnt = __popc(b0) + __popc(b1);
+            const int lbase = kListCap - npend - cnt;
+            if (ca) {
+                const int at = lbase + __popc(b0 & lt);
+                s_list[warp][at] = uint8_t(64 * sg + lane);
+                s_lmask[warp][at] = ca;
+            }
+            if (cb) {
+                const int at = lbase + __popc(b0) + __popc(b1 & lt);
+                s_list[warp][at] = uint8_t(64 * sg + 32 + lane);
+                s_lmask[warp][at] = cb;
             }
             __syncwarp();
             const uint8_t *list = s_list[warp];
             const uint32_t *lmask = s_lmask[warp];
-            for (int hq = cnt; hq > 0; hq -= kChunk) {
-                const int lq = hq > kChunk ? hq - kChunk : 0;
-                const int nq = hq - lq;
+            // Full chunks from the top (the back of the list); the batch's
+            // last segment also takes the rest.
+            int have = npend + cnt, hq = kListCap;
+            for (; have >= kChunk || (sg == 0 && have > 0); hq -= kChunk, have -= kChunk) {
+                const int nq = have < kChunk ? have : kChunk;
+                const int lq = hq - nq;
                 // 1. This pixel's bit of each entry's mask: lane k holds entry
                 //    k's mask, and the warp transposes the 32 x 32 bit matrix.
                 const uint32_t mine0 = warp_transpose32(lane < nq ? lmask[lq + lane] : 0u, lane);
@@ -453,6 +462,20 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                 __syncwarp();
                 nslots += nrows;
             }
+            // Move the left-over entries (below hq) up to the end of the list.
+            have = have > 0 ? have : 0;
+            if (hq != kListCap && have > 0) {
+                uint8_t e = 0;
+                uint32_t em = 0;
+                if (lane < have) e = list[hq - have + lane], em = lmask[hq - have + lane];
+                __syncwarp();
+                if (lane < have) {
+                    s_list[warp][kListCap - have + lane] = e;
+                    s_lmask[warp][kListCap - have + lane] = em;
+                }
+                __syncwarp();
+            }
+            npend = have;
         }
     }
     cp_async_wait<0>();  // no copy may outlive the CTA
