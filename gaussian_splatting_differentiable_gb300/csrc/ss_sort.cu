@@ -122,12 +122,21 @@ __global__ void __launch_bounds__(256) k_sort_hist(const uint64_t *__restrict__ 
     __syncthreads();
     const int64_t stride = int64_t(gridDim.x) * 256;
     bool bad = false;
-    for (int64_t i = int64_t(blockIdx.x) * 256 + threadIdx.x; i < n; i += stride) {
-        const uint64_t k = keys[i];
+    auto count = [&](uint64_t k) {
         bad |= m.db < 32 && ((uint32_t(k) - m.lo) >> m.db) != 0u;   // depth outside the range
         const uint64_t v = mapped_key(k, m);
         for (int d = 0; d < m.nd; ++d) atomicAdd(&s_h[d][(v >> (8 * d)) & 255u], 1u);
+    };
+    // four keys in flight a thread (their loads issued together), then the rest
+    int64_t i = int64_t(blockIdx.x) * 256 + threadIdx.x;
+    for (; i + 3 * stride < n; i += 4 * stride) {
+        uint64_t k4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) k4[u] = keys[i + u * stride];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) count(k4[u]);
     }
+    for (; i < n; i += stride) count(keys[i]);
     if (bad) atomicOr(err, kDevErrKeyRange);
     __syncthreads();
     for (int k = threadIdx.x; k < ndig * 256; k += 256) {
