@@ -211,9 +211,9 @@ def source_sha(paths) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str):
+def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of the kernel."""
+    on the current source of the kernel and on this workload."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -222,6 +222,8 @@ def recorded_traffic(kernel: str):
     except (OSError, ValueError):
         return None
     if not rec or rec.get("source_sha") != source_sha(BWD_SOURCES):
+        return None
+    if rec.get("workload_name") != workload:
         return None
     return rec.get("dram_bytes_per_launch_full")
 
@@ -583,7 +585,7 @@ def run_ours(args, rank: int, world: int, dist):
     t_atom = n_atomics / red_rate
     t_hbm = bwd_bytes / (hbm * 1e9)
     roofline = {"kernel": "k_raster_bwd", "bound": "hbm", "achieved": achieved, "peak": hbm,
-                "unit": "GB/s", "frac": achieved / hbm, "traffic": recorded_traffic("k_raster_bwd"),
+                "unit": "GB/s", "frac": achieved / hbm, "traffic": recorded_traffic("k_raster_bwd", wl.name),
                 "peak_source": hbm_src + " (MEASURED_PEAKS.json hbm_gbs, copy test)",
                 "algorithmic_bytes": bwd_bytes,
                 "bytes_model": "40 B/pair (index + 36 B splat gather) + 20 B/pixel "

@@ -68,3 +68,30 @@ def test_sort_passes_follow_the_recorded_depth_range():
     assert bench.sort_passes(c, 16) == 3             # 16-bit floor + 4 tile bits
     c[2], c[3] = np.uint64(2 ** 64 - 1), 0           # no pairs: the full key
     assert bench.sort_passes(c, 4056) == 6
+
+
+def _last_json_line(out: str) -> dict:
+    import json
+    lines = [l for l in out.splitlines() if l.startswith("{")]
+    assert lines, out[-2000:]
+    return json.loads(lines[-1])
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference times the oracle on the host cores and prints
+    one JSON line with the arm's fields (tiny workload, a second or so)."""
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "1",
+                        "--steps", "3", "--warmup", "3"], cwd=root, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = _last_json_line(r.stdout)
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
