@@ -107,6 +107,18 @@ def ss_workspace_bytes(n_splats: int, n_pairs: int, W: int, H: int) -> int:
     return int(_L.ss_workspace_bytes(n_splats, n_pairs, W, H))
 
 
+COUNTER_WORDS = 4   # ss_bin_tiles' uint64 counters: pairs, culled, depth-bit range
+
+
+def _counters(counters):
+    """The counters tensor's pointer, after checking that it holds the four
+    64-bit words the library writes (a plain pointer crosses the C ABI)."""
+    if isinstance(counters, torch.Tensor) and counters.numel() * counters.element_size() < 8 * COUNTER_WORDS:
+        raise ValueError("counters must hold %d 64-bit words (got %d bytes)"
+                         % (COUNTER_WORDS, counters.numel() * counters.element_size()))
+    return _ptr(counters)
+
+
 def ss_record_bytes(n_splats: int) -> int:
     return int(_L.ss_record_bytes(n_splats))
 
@@ -115,13 +127,13 @@ def ss_bin_tiles(splats: Splats, W: int, H: int, keys, vals, capacity: int, coun
                  stream=None) -> None:
     s = splats.c()
     _check(_L.ss_bin_tiles(ctypes.byref(s), W, H, _ptr(keys), _ptr(vals), capacity,
-                           _ptr(counters), _ptr(records), _stream(stream)), "ss_bin_tiles")
+                           _counters(counters), _ptr(records), _stream(stream)), "ss_bin_tiles")
 
 
 def ss_pair_count(counters, capacity: int, stream=None):
     """(status, pairs needed, culled); status is SS_OK or SS_ERR_CAPACITY."""
     pairs, culled = ctypes.c_int64(0), ctypes.c_int64(0)
-    st = _L.ss_pair_count(_ptr(counters), capacity, ctypes.byref(pairs), ctypes.byref(culled),
+    st = _L.ss_pair_count(_counters(counters), capacity, ctypes.byref(pairs), ctypes.byref(culled),
                           _stream(stream))
     if st not in (SS_OK, SS_ERR_CAPACITY):
         raise SSError(st, "ss_pair_count")
@@ -137,7 +149,7 @@ def ss_sort_pairs(keys, vals, n_pairs: int, W: int, H: int, tile_offsets, worksp
 
 def ss_sort_pairs_dev(keys, vals, counters, capacity: int, W: int, H: int, tile_offsets,
                       workspace, stream=None) -> None:
-    _check(_L.ss_sort_pairs_dev(_ptr(keys), _ptr(vals), _ptr(counters), capacity, W, H,
+    _check(_L.ss_sort_pairs_dev(_ptr(keys), _ptr(vals), _counters(counters), capacity, W, H,
                                 _ptr(tile_offsets), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream)),
            "ss_sort_pairs_dev")
@@ -345,7 +357,7 @@ class Rasterizer:
         self.device = torch.device(device)
         self.tiles = ((W + TILE - 1) // TILE) * ((H + TILE - 1) // TILE)
         d = self.device
-        self.counters = torch.zeros(4, dtype=torch.int64, device=d)
+        self.counters = torch.zeros(COUNTER_WORDS, dtype=torch.int64, device=d)
         self.records = torch.empty(max(ss_record_bytes(n_splats), 16), dtype=torch.uint8, device=d)
         self.tile_offsets = torch.zeros(self.tiles + 1, dtype=torch.int32, device=d)
         self._alloc_pairs(max(int(pair_capacity), 1))

@@ -193,3 +193,18 @@ def test_ssim_rejects_bad_arguments_on_the_host(lib):
     assert lib.ss_ssim_loss(0x1000, 0x1000, 3, 8, 8, 0.2, 0x1000, 0x1000, 0x1008, ws, None) == 1
     assert lib.ss_ssim_loss(0x1000, 0x1000, 3, 8, 8, 0.2, 0x1000, 0x1000, 0x1000, ws - 1, None) == 1
     assert "workspace" in lib.ss_last_error().decode()
+
+
+def test_binding_rejects_a_short_counters_buffer():
+    """The counters cross the C ABI as a plain pointer; the binding checks that
+    the tensor holds the four 64-bit words the library writes."""
+    torch = pytest.importorskip("torch")
+    import gaussian_splatting_differentiable_gb300 as ss
+    short = torch.zeros(2, dtype=torch.int64)
+    with pytest.raises(ValueError, match="four|4 64-bit"):
+        ss.ss_pair_count(short, 10)
+    keys = torch.zeros(4, dtype=torch.int64)
+    vals = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        ss.ss_sort_pairs_dev(keys, vals, short, 4, 16, 16, torch.zeros(2, dtype=torch.int32),
+                             torch.zeros(256, dtype=torch.uint8), stream=0)
