@@ -98,7 +98,8 @@ typedef struct {
     float *ddepth;         /* [n], only with SS_DISTORTION (else may be NULL) */
 } ss_grads;
 
-/* Version of this ABI (incremented on any change of a signature). */
+/* Version of this ABI (incremented on any change of a signature, or of the
+ * meaning or size of an argument). */
 int32_t ss_abi_version(void);
 
 /* Host: the model's constants as the kernels use them:
