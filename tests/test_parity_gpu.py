@@ -171,7 +171,7 @@ def test_capacity_overflow_reports_and_recovers(P):
     sp = ss.Splats.from_numpy(sc)
     keys = torch.full((50,), -1, dtype=torch.int64, device="cuda")
     vals = torch.full((50,), -1, dtype=torch.int32, device="cuda")
-    cnt = torch.zeros(2, dtype=torch.int64, device="cuda")
+    cnt = torch.zeros(ss.COUNTER_WORDS, dtype=torch.int64, device="cuda")
     recs = torch.empty(ss.ss_record_bytes(sc.n), dtype=torch.uint8, device="cuda")
     ss.ss_bin_tiles(sp, sc.W, sc.H, keys, vals, 40, cnt, recs)
     st, pairs, culled = ss.ss_pair_count(cnt, 40)
