@@ -43,7 +43,7 @@ WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H) {
     off = align256(off + size_t(L.ndig) * 256 * 4);
     L.gofs = off;
     off = align256(off + size_t(L.ndig) * 256 * 4);
-    L.tickets = off;              // [0, 8) pass tickets, [8] long tie runs
+    L.tickets = off;              // [0, 8) pass tickets, [8] long tie runs, [9] largest value
     off = align256(off + 16 * 4);
     L.lookback = off;
     off = align256(off + size_t(L.ndig) * size_t(L.nparts) * 256 * 8);
@@ -54,6 +54,8 @@ WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H) {
     off = align256(off + size_t(n_pairs) * 4);
     L.ties = off;                 // uint2 (start, length) of runs of > 32 equal keys
     off = align256(off + size_t(n_pairs / 33 + 1) * 8);
+    L.pack_words = off;           // uint64 [n_pairs]: the packed passes' third buffer
+    off = align256(off + size_t(n_pairs) * 8);
     L.sort_end = off;
     L.accum = 256;  // after the status word; the sort's regions are dead by then
     L.bwd_end = align256(L.accum + size_t(n_splats) * 48);  // 48-byte gradient record per splat
@@ -76,7 +78,7 @@ using namespace ss;
 
 extern "C" {
 
-int32_t ss_abi_version(void) { return 5; }
+int32_t ss_abi_version(void) { return 6; }
 
 size_t ss_record_bytes(int32_t n_splats) { return n_splats < 0 ? 0 : size_t(n_splats) * 64; }
 

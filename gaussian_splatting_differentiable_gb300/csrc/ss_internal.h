@@ -16,6 +16,7 @@ constexpr int32_t kMaxSide = 32768;
 constexpr int kSortThreads = 256;
 constexpr int kSortKeysPerThread = 16;
 constexpr int kSortPart = kSortThreads * kSortKeysPerThread;  // keys per onesweep partition
+static_assert(kSortPart <= 65536, "k_sort_pass keeps two 16-bit ranks in a register");
 
 // Records `st` and a printf-style message as this thread's last error.
 ss_status fail(ss_status st, const char *fmt, ...);
@@ -45,12 +46,14 @@ struct WsLayout {
     size_t status_word;   // uint32, offset 0
     size_t hist;          // uint32 [ndig][256] digit counts
     size_t gofs;          // uint32 [ndig][256] exclusive digit starts
-    size_t tickets;       // uint32 [16]: partition tickets per pass, [8] long-run count
+    size_t tickets;       // uint32 [16]: partition tickets per pass, [8] long-run count,
+                          // [9] largest value (packed-pass decision)
     size_t lookback;      // uint64 [ndig][nparts][256] onesweep look-back words
     size_t zero_end;      // [0, zero_end) is cleared before each sort
     size_t alt_keys;      // uint64 [n_pairs] ping-pong buffer
     size_t alt_vals;      // uint32 [n_pairs]
     size_t ties;          // uint2 [n_pairs / 33 + 1] long runs of equal keys
+    size_t pack_words;    // uint64 [n_pairs] third buffer of the packed passes
     size_t sort_end;
     size_t accum;         // backward per-splat gradient records, 48 bytes each
     size_t bwd_end;

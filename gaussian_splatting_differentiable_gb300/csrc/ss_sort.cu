@@ -24,6 +24,12 @@
 //   k_sort_ties   one CTA per long run: a stable radix sort of its indices
 //                 in global memory (no quadratic insertion sort, whatever
 //                 the number of equal depths).
+// Packed words: when the sorted key bits (below) and the bits of the largest
+// value fit in 64 together, the passes move one word per pair, (mapped key
+// << value bits) | value, instead of a 64-bit key and a 32-bit value (16
+// instead of 24 bytes a pair and a pass, and one less shared-memory array);
+// k_sort_hist finds the largest value, every kernel takes the same decision
+// from it, and k_sort_final unpacks the words into the caller's buffers.
 // Only 32 + ceil(log2 tiles) key bits are sorted -- and with the depth range
 // that the binning recorded (the device-count sort), only the depth bits in
 // which two pairs can differ: each kernel maps a key to
@@ -54,14 +60,18 @@ __device__ __forceinline__ void st_relaxed(uint64_t *p, uint64_t v) {
 // The sorted key bits: identity (lo = 0, db = 32, nd = ndig) unless dr holds
 // a recorded depth-bit range [dr[0], dr[1]]; then lo = dr[0] with its low 16
 // bits cleared, db = max(16, bits of dr[1] - lo) and nd = the 8-bit digits of
-// the db + tile_bits bit key.
+// the db + tile_bits bit key.  Packed mode: when the mapped key and the
+// largest value (*vmax, vb bits) fit in 64 bits together, the passes move one
+// word (mapped key << vb | value) per pair instead of a key and a value.
 struct KeyMap {
     uint32_t lo;
-    int db, nd;
+    int db, nd, vb;
+    bool packed;
 };
 
-__device__ __forceinline__ KeyMap key_map(const unsigned long long *dr, int tile_bits, int ndig) {
-    KeyMap m{0u, 32, ndig};
+__device__ __forceinline__ KeyMap key_map(const unsigned long long *dr, int tile_bits, int ndig,
+                                          const uint32_t *vmax) {
+    KeyMap m{0u, 32, ndig, 32, false};
     if (dr) {
         const unsigned long long lo64 = dr[0], hi64 = dr[1];
         if (lo64 <= hi64 && hi64 <= 0xffffffffull) {
@@ -70,6 +80,10 @@ __device__ __forceinline__ KeyMap key_map(const unsigned long long *dr, int tile
             m.nd = min(ndig, (m.db + tile_bits + 7) / 8);
         }
     }
+    if (vmax) {
+        m.vb = 32 - __clz(int(*vmax));
+        m.packed = m.db + tile_bits + m.vb <= 64;
+    }
     return m;
 }
 
@@ -77,6 +91,31 @@ __device__ __forceinline__ KeyMap key_map(const unsigned long long *dr, int tile
 // returns the key itself.
 __device__ __forceinline__ uint64_t mapped_key(uint64_t key, const KeyMap &m) {
     return ((key >> 32) << m.db) | uint64_t(uint32_t(key) - m.lo);
+}
+
+// Packed mode: the word of a pair, and the key and value it holds.
+__device__ __forceinline__ uint64_t pack_word(uint64_t key, uint32_t val, const KeyMap &m) {
+    return (mapped_key(key, m) << m.vb) | val;
+}
+
+__device__ __forceinline__ uint64_t unpack_key(uint64_t w, const KeyMap &m) {
+    const uint64_t mk = w >> m.vb;
+    const uint32_t dbits = uint32_t(mk & ((1ull << m.db) - 1ull)) + m.lo;
+    return ((mk >> m.db) << 32) | dbits;
+}
+
+__device__ __forceinline__ uint32_t unpack_val(uint64_t w, const KeyMap &m) {
+    return uint32_t(w & ((1ull << m.vb) - 1ull));
+}
+
+// Packed mode: the buffer pass d writes.  Pass 0 reads the caller's keys and
+// values; the last pass always lands in the alternate key buffer `ak`, so
+// that the final kernel unpacks into the caller's buffers without reading
+// what it overwrites; the passes between alternate with the caller's key
+// buffer, and `zk` serves pass 0 when the pass count is even.
+__device__ __forceinline__ uint64_t *packed_dest(int d, int nd, uint64_t *keys, uint64_t *ak,
+                                                 uint64_t *zk) {
+    return ((nd - 1 - d) & 1) == 0 ? ak : (d == 0 ? zk : keys);
 }
 
 // Number of pairs to sort: n_max, or the device count *dn clamped to n_max.
@@ -110,14 +149,17 @@ __device__ __forceinline__ uint32_t block_excl_scan256(uint32_t v, uint32_t *s_w
     return before + inc - v;
 }
 
-__global__ void __launch_bounds__(256) k_sort_hist(const uint64_t *__restrict__ keys, int64_t n_max,
+// Also finds the largest value (*vmax, zeroed before), which decides
+// whether the passes run packed.
+__global__ void __launch_bounds__(256) k_sort_hist(const uint64_t *__restrict__ keys,
+                                                   const uint32_t *__restrict__ vals, int64_t n_max,
                                                    const unsigned long long *dn,
                                                    const unsigned long long *dr, int tile_bits,
                                                    int ndig, uint32_t *__restrict__ hist,
-                                                   uint32_t *err) {
+                                                   uint32_t *vmax, uint32_t *err) {
     __shared__ uint32_t s_h[8][256];
     const int64_t n = pair_count(dn, n_max);
-    const KeyMap m = key_map(dr, tile_bits, ndig);
+    const KeyMap m = key_map(dr, tile_bits, ndig, nullptr);
     for (int k = threadIdx.x; k < 8 * 256; k += 256) (&s_h[0][0])[k] = 0;
     __syncthreads();
     const int64_t stride = int64_t(gridDim.x) * 256;
@@ -128,16 +170,29 @@ __global__ void __launch_bounds__(256) k_sort_hist(const uint64_t *__restrict__ 
         for (int d = 0; d < m.nd; ++d) atomicAdd(&s_h[d][(v >> (8 * d)) & 255u], 1u);
     };
     // four keys in flight a thread (their loads issued together), then the rest
+    uint32_t vm = 0;
     int64_t i = int64_t(blockIdx.x) * 256 + threadIdx.x;
     for (; i + 3 * stride < n; i += 4 * stride) {
         uint64_t k4[4];
+        uint32_t v4[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) k4[u] = keys[i + u * stride];
+        for (int u = 0; u < 4; ++u) {
+            k4[u] = keys[i + u * stride];
+            v4[u] = vals[i + u * stride];
+        }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) count(k4[u]);
+        for (int u = 0; u < 4; ++u) {
+            count(k4[u]);
+            vm = max(vm, v4[u]);
+        }
     }
-    for (; i < n; i += stride) count(keys[i]);
+    for (; i < n; i += stride) {
+        count(keys[i]);
+        vm = max(vm, vals[i]);
+    }
     if (bad) atomicOr(err, kDevErrKeyRange);
+    vm = __reduce_max_sync(0xffffffffu, vm);
+    if ((threadIdx.x & 31) == 0 && vm) atomicMax(vmax, vm);
     __syncthreads();
     for (int k = threadIdx.x; k < ndig * 256; k += 256) {
         const uint32_t v = (&s_h[0][0])[k];
@@ -166,10 +221,142 @@ struct PassParams {
     const unsigned long long *dn;  // device pair count (clamped to n), or null
     const unsigned long long *dr;  // device depth-bit range [lo, hi], or null (identity map)
     int tile_bits, ndig;
+    // packed mode (null vmax: never packed)
+    const uint32_t *vmax;  // largest value, from k_sort_hist
+    uint64_t *keys;        // the caller's key buffer
+    uint64_t *ak;          // alternate key buffer
+    uint64_t *zk;          // third word buffer (pass 0 of an even pass count)
 };
 
-__global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
+// One onesweep pass over one partition; PACKED moves words (mapped key << vb
+// | value), otherwise keys and values.
+template <bool PACKED>
+__device__ __forceinline__ void sort_pass_body(const PassParams &p, const KeyMap &km, int64_t part,
+                                               uint32_t (*s_whist)[256], uint32_t *s_lstart,
+                                               uint32_t *s_gbase, uint32_t *s_warp,
+                                               uint64_t *s_keys, uint32_t *s_vals) {
     constexpr int KPT = kSortKeysPerThread;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t base = part * kSortPart;
+    const int64_t n = p.n;
+    const int64_t wbase = base + warp * (KPT * 32);
+    const int d = p.shift / 8;
+    const uint64_t *win = nullptr;
+    uint64_t *wout = nullptr;
+    if (PACKED) {
+        wout = packed_dest(d, km.nd, p.keys, p.ak, p.zk);
+        if (d > 0) win = packed_dest(d - 1, km.nd, p.keys, p.ak, p.zk);
+    }
+    const int dsh = PACKED ? km.vb + p.shift : p.shift;
+    auto digit = [&](uint64_t k) -> uint32_t {
+        return PACKED ? uint32_t(k >> dsh) & 255u : uint32_t(mapped_key(k, km) >> dsh) & 255u;
+    };
+
+    uint64_t key[KPT];
+    uint32_t val[KPT];
+    uint32_t rank2[KPT / 2];   // ranks (< kSortPart <= 2^16), two to a register
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int64_t idx = wbase + j * 32 + lane;
+        const bool ok = idx < n;
+        if (PACKED) {
+            key[j] = !ok ? ~0ull : (d == 0 ? pack_word(p.kin[idx], p.vin[idx], km) : win[idx]);
+            val[j] = 0u;
+        } else {
+            key[j] = ok ? p.kin[idx] : ~0ull;
+            val[j] = ok ? p.vin[idx] : 0u;
+        }
+    }
+    // Stable rank within the warp: keys in order (j, lane).
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int64_t idx = wbase + j * 32 + lane;
+        const bool ok = idx < n;
+        const uint32_t dig = ok ? digit(key[j]) : 256u + lane;
+        const uint32_t peers = __match_any_sync(0xffffffffu, dig);
+        const uint32_t before = __popc(peers & lt);
+        uint32_t cur = 0;
+        if (ok) cur = s_whist[warp][dig];
+        if (j & 1)
+            rank2[j >> 1] |= (cur + before) << 16;
+        else
+            rank2[j >> 1] = cur + before;
+        __syncwarp();
+        if (ok && before == 0) s_whist[warp][dig] = cur + __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // Per digit (thread = digit): warp-exclusive offsets and partition total.
+    const int dg = tid;
+    uint32_t total = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t c = s_whist[w][dg];
+        s_whist[w][dg] = total;
+        total += c;
+    }
+    uint64_t *my = p.lookback + part * 256 + dg;
+    st_relaxed(my, (part == 0 ? kFlagInc : kFlagAgg) | uint64_t(total));
+
+    s_lstart[dg] = block_excl_scan256(total, s_warp, nullptr);
+
+    // Decoupled look-back: sum the counts of digit dg in earlier partitions.
+    uint64_t excl = 0;
+    if (part > 0) {
+        int64_t q = part - 1;
+        uint32_t spins = 0;
+        while (true) {
+            const uint64_t sw = ld_relaxed(p.lookback + q * 256 + dg);
+            const uint64_t flag = sw & ~kValMask;
+            if (flag == 0) {
+                if (++spins > kSpinLimit) {
+                    atomicOr(p.err, kDevErrTimeout);
+                    break;
+                }
+                if (spins > 32) __nanosleep(100);
+                continue;
+            }
+            excl += sw & kValMask;
+            if (flag == kFlagInc || q == 0) break;
+            --q;
+            spins = 0;
+        }
+        st_relaxed(my, kFlagInc | (excl + total));
+    }
+    s_gbase[dg] = p.gofs[dg] + uint32_t(excl);
+    __syncthreads();
+
+    // Scatter into shared memory in (digit, rank) order, then out.
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        const int64_t idx = wbase + j * 32 + lane;
+        if (idx < n) {
+            const uint32_t dig = digit(key[j]);
+            const uint32_t rank = (j & 1) ? rank2[j >> 1] >> 16 : rank2[j >> 1] & 0xffffu;
+            const uint32_t pos = s_lstart[dig] + s_whist[warp][dig] + rank;
+            s_keys[pos] = key[j];
+            if (!PACKED) s_vals[pos] = val[j];
+        }
+    }
+    __syncthreads();
+    const int64_t left = n - base;
+    const int cnt = int(left < kSortPart ? left : kSortPart);
+    for (int i = tid; i < cnt; i += 256) {
+        const uint64_t k = s_keys[i];
+        const uint32_t dig = digit(k);
+        const uint32_t g = s_gbase[dig] + uint32_t(i) - s_lstart[dig];
+        if (PACKED) {
+            wout[g] = k;
+        } else {
+            p.kout[g] = k;
+            p.vout[g] = s_vals[i];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256, 3) k_sort_pass(PassParams p) {
     __shared__ uint32_t s_whist[8][256];  // per-warp digit counts, then warp-exclusive offsets
     __shared__ uint32_t s_lstart[256];    // digit start within the partition
     __shared__ uint32_t s_gbase[256];     // global start of the partition's keys of each digit
@@ -179,110 +366,22 @@ __global__ void __launch_bounds__(256, 2) k_sort_pass(PassParams p) {
     uint64_t *s_keys = reinterpret_cast<uint64_t *>(s_dyn);
     uint32_t *s_vals = reinterpret_cast<uint32_t *>(s_dyn + kSortPart * 8);
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const KeyMap km = key_map(p.dr, p.tile_bits, p.ndig);
+    const int tid = threadIdx.x;
+    const KeyMap km = key_map(p.dr, p.tile_bits, p.ndig, p.vmax);
     if (p.shift / 8 >= km.nd) return;   // past the last digit of the mapped key
     if (tid == 0) s_part = atomicAdd(p.ticket, 1u);
     for (int k = tid; k < 8 * 256; k += 256) (&s_whist[0][0])[k] = 0;
     __syncthreads();
     const int64_t part = s_part;
-    const int64_t base = part * kSortPart;
     if (p.dn) {  // grid sized for the capacity: surplus partitions leave
         const int64_t n = pair_count(p.dn, p.n);
-        if (base >= n) return;
+        if (part * kSortPart >= n) return;
         p.n = n;
     }
-    const int64_t wbase = base + warp * (KPT * 32);
-
-    uint64_t key[KPT];
-    uint32_t val[KPT];
-    uint32_t rank[KPT];
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-        const int64_t idx = wbase + j * 32 + lane;
-        const bool ok = idx < p.n;
-        key[j] = ok ? p.kin[idx] : ~0ull;
-        val[j] = ok ? p.vin[idx] : 0u;
-    }
-    // Stable rank within the warp: keys in order (j, lane).
-    const uint32_t lt = lanemask_lt();
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-        const int64_t idx = wbase + j * 32 + lane;
-        const bool ok = idx < p.n;
-        const uint32_t dig = ok ? uint32_t(mapped_key(key[j], km) >> p.shift) & 255u : 256u + lane;
-        const uint32_t peers = __match_any_sync(0xffffffffu, dig);
-        const uint32_t before = __popc(peers & lt);
-        uint32_t cur = 0;
-        if (ok) cur = s_whist[warp][dig];
-        rank[j] = cur + before;
-        __syncwarp();
-        if (ok && before == 0) s_whist[warp][dig] = cur + __popc(peers);
-        __syncwarp();
-    }
-    __syncthreads();
-
-    // Per digit (thread = digit): warp-exclusive offsets and partition total.
-    const int d = tid;
-    uint32_t total = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        const uint32_t c = s_whist[w][d];
-        s_whist[w][d] = total;
-        total += c;
-    }
-    uint64_t *my = p.lookback + part * 256 + d;
-    st_relaxed(my, (part == 0 ? kFlagInc : kFlagAgg) | uint64_t(total));
-
-    s_lstart[d] = block_excl_scan256(total, s_warp, nullptr);
-
-    // Decoupled look-back: sum the counts of digit d in earlier partitions.
-    uint64_t excl = 0;
-    if (part > 0) {
-        int64_t q = part - 1;
-        uint32_t spins = 0;
-        while (true) {
-            const uint64_t s = ld_relaxed(p.lookback + q * 256 + d);
-            const uint64_t flag = s & ~kValMask;
-            if (flag == 0) {
-                if (++spins > kSpinLimit) {
-                    atomicOr(p.err, kDevErrTimeout);
-                    break;
-                }
-                if (spins > 32) __nanosleep(100);
-                continue;
-            }
-            excl += s & kValMask;
-            if (flag == kFlagInc || q == 0) break;
-            --q;
-            spins = 0;
-        }
-        st_relaxed(my, kFlagInc | (excl + total));
-    }
-    s_gbase[d] = p.gofs[d] + uint32_t(excl);
-    __syncthreads();
-
-    // Scatter into shared memory in (digit, rank) order, then out.
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-        const int64_t idx = wbase + j * 32 + lane;
-        if (idx < p.n) {
-            const uint32_t dig = uint32_t(mapped_key(key[j], km) >> p.shift) & 255u;
-            const uint32_t pos = s_lstart[dig] + s_whist[warp][dig] + rank[j];
-            s_keys[pos] = key[j];
-            s_vals[pos] = val[j];
-        }
-    }
-    __syncthreads();
-    const int64_t left = p.n - base;
-    const int cnt = int(left < kSortPart ? left : kSortPart);
-    for (int i = tid; i < cnt; i += 256) {
-        const uint64_t k = s_keys[i];
-        const uint32_t dig = uint32_t(mapped_key(k, km) >> p.shift) & 255u;
-        const uint32_t g = s_gbase[dig] + uint32_t(i) - s_lstart[dig];
-        p.kout[g] = k;
-        p.vout[g] = s_vals[i];
-    }
+    if (km.packed)
+        sort_pass_body<true>(p, km, part, s_whist, s_lstart, s_gbase, s_warp, s_keys, s_vals);
+    else
+        sort_pass_body<false>(p, km, part, s_whist, s_lstart, s_gbase, s_warp, s_keys, s_vals);
 }
 
 // Ties and offsets.  For element i of the sorted keys:
@@ -297,21 +396,26 @@ __global__ void __launch_bounds__(256) k_sort_final(uint64_t *dk, uint32_t *dv, 
                                                     uint32_t *av, int64_t n_max,
                                                     const unsigned long long *dn,
                                                     const unsigned long long *dr, int tile_bits,
-                                                    int ndig, int64_t tiles, uint32_t *offs,
-                                                    uint32_t *err, uint32_t *tie_count,
-                                                    uint2 *ties) {
-    // the passes ping-pong between (dk, dv) and (ak, av): after nd of them
-    // the sorted data is in (ak, av) iff nd is odd
-    const bool alt = key_map(dr, tile_bits, ndig).nd & 1;
-    const uint64_t *__restrict__ sk = alt ? ak : dk;
-    uint32_t *sv = alt ? av : dv;
+                                                    int ndig, const uint32_t *vmax, int64_t tiles,
+                                                    uint32_t *offs, uint32_t *err,
+                                                    uint32_t *tie_count, uint2 *ties) {
+    // Unpacked, the passes ping-pong between (dk, dv) and (ak, av): after nd
+    // of them the sorted data is in (ak, av) iff nd is odd.  Packed, the last
+    // pass wrote words to ak, which are unpacked into (dk, dv) here.
+    const KeyMap km = key_map(dr, tile_bits, ndig, vmax);
+    const bool packed = km.packed;
+    const bool alt = km.nd & 1;
+    const uint64_t *__restrict__ sk = packed || alt ? ak : dk;
+    const uint32_t *sv = alt ? av : dv;
+    auto K = [&](int64_t j) -> uint64_t { return packed ? unpack_key(sk[j], km) : sk[j]; };
+    auto V = [&](int64_t j) -> uint32_t { return packed ? unpack_val(sk[j], km) : sv[j]; };
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t n = pair_count(dn, n_max);
     if (i == 0 && dn && *dn > (unsigned long long)n_max) atomicOr(err, kDevErrCapacity);
     if (n == 0 && i == 0)
         for (int64_t u = 0; u <= tiles; ++u) offs[u] = 0u;
     if (i >= n) return;
-    const uint64_t key = sk[i];
+    const uint64_t key = K(i);
     int64_t t = int64_t(key >> 32);
     if (t >= tiles) {
         atomicOr(err, kDevErrKeyRange);
@@ -319,34 +423,34 @@ __global__ void __launch_bounds__(256) k_sort_final(uint64_t *dk, uint32_t *dv, 
     }
     int64_t tp = -1;
     if (i > 0) {
-        tp = int64_t(sk[i - 1] >> 32);
+        tp = int64_t(K(i - 1) >> 32);
         if (tp > tiles) tp = tiles;
     }
     for (int64_t u = tp + 1; u <= t; ++u) offs[u] = uint32_t(i);
     if (i == n - 1)
         for (int64_t u = t + 1; u <= tiles; ++u) offs[u] = uint32_t(n);
 
-    const bool copy = sk != dk;
-    const bool member = i > 0 && sk[i - 1] == key;
+    const bool copy = packed || sk != dk;
+    const bool member = i > 0 && K(i - 1) == key;
     if (member) return;
-    const bool head = i + 1 < n && sk[i + 1] == key;
+    const bool head = i + 1 < n && K(i + 1) == key;
     if (!head) {
         if (copy) {
             dk[i] = key;
-            dv[i] = sv[i];
+            dv[i] = V(i);
         }
         return;
     }
     int64_t e = i + 1;
-    while (e < n && sk[e] == key && e - i <= kTieInsert) ++e;
+    while (e < n && K(e) == key && e - i <= kTieInsert) ++e;
     if (e - i > kTieInsert) {   // a long run: k_sort_ties sorts (and copies) it
-        while (e < n && sk[e] == key) ++e;
+        while (e < n && K(e) == key) ++e;
         ties[atomicAdd(tie_count, 1u)] = make_uint2(uint32_t(i), uint32_t(e - i));
         return;
     }
-    // insertion sort of sv[i..e) by value, written to dv[i..e)
+    // insertion sort of the run's values by value, written to dv[i..e)
     for (int64_t a = i; a < e; ++a) {
-        const uint32_t v = sv[a];
+        const uint32_t v = V(a);
         int64_t b = a;
         while (b > i && dv[b - 1] > v) {
             dv[b] = dv[b - 1];
@@ -436,18 +540,29 @@ __device__ void segment_sort_global(uint64_t *ak, uint32_t *av, uint64_t *bk, ui
 // the other buffer, scratch for the radix passes.
 __global__ void __launch_bounds__(256) k_sort_ties(uint64_t *dk, uint32_t *dv, uint64_t *ak,
                                                    uint32_t *av, const unsigned long long *dr,
-                                                   int tile_bits, int ndig,
+                                                   int tile_bits, int ndig, const uint32_t *vmax,
                                                    const uint32_t *tie_count, const uint2 *ties) {
     __shared__ uint32_t s_wc[8 * 256];
     __shared__ uint32_t s_cnt[256];
     __shared__ uint32_t s_warp[8];
-    // source: the passes' last output buffer; scratch: the other one
-    const bool alt = key_map(dr, tile_bits, ndig).nd & 1;
-    uint64_t *sk = alt ? ak : dk, *ok_ = alt ? dk : ak;
-    uint32_t *sv = alt ? av : dv, *ov = alt ? dv : av;
+    const KeyMap km = key_map(dr, tile_bits, ndig, vmax);
+    // Unpacked -- source: the passes' last output buffer; scratch: the other
+    // one.  Packed -- each run is first unpacked from ak into (dk, dv), then
+    // sorted there with (ak, av) as scratch.
+    const bool alt = km.nd & 1;
+    uint64_t *sk = km.packed ? dk : alt ? ak : dk, *ok_ = km.packed ? ak : alt ? dk : ak;
+    uint32_t *sv = km.packed ? dv : alt ? av : dv, *ov = km.packed ? av : alt ? dv : av;
     const uint32_t nt = *tie_count;
     for (uint32_t r = blockIdx.x; r < nt; r += gridDim.x) {
         const uint2 run = ties[r];
+        if (km.packed) {
+            for (uint32_t e = threadIdx.x; e < run.y; e += 256) {
+                const uint64_t w = ak[run.x + e];
+                dk[run.x + e] = unpack_key(w, km);
+                dv[run.x + e] = unpack_val(w, km);
+            }
+            __syncthreads();
+        }
         segment_sort_global(sk, sv, ok_, ov, dk, dv, int64_t(run.x), int(run.y),
                             sk[run.x] >> 32, s_cnt, s_wc, s_warp);
         __syncthreads();
@@ -456,8 +571,8 @@ __global__ void __launch_bounds__(256) k_sort_ties(uint64_t *dk, uint32_t *dv, u
 
 static int g_attr_set[64];
 
-// k_sort_pass needs 48 KB of dynamic shared memory on top of its static
-// arrays: raise its limit once per device.
+// k_sort_pass needs 48 KB of dynamic shared memory (32 KB when packed) on
+// top of its static arrays: raise its limit once per device.
 static ss_status ensure_pass_smem(int dyn) {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -514,13 +629,16 @@ static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int6
     uint64_t *lookback = reinterpret_cast<uint64_t *>(ws + L.lookback);
     uint64_t *ak = reinterpret_cast<uint64_t *>(ws + L.alt_keys);
     uint32_t *av = reinterpret_cast<uint32_t *>(ws + L.alt_vals);
+    uint64_t *zk = reinterpret_cast<uint64_t *>(ws + L.pack_words);
+    uint32_t *vmax = tickets + 9;   // largest value (cleared with the tickets)
 
     const int64_t blocks = (n_max + 255) / 256;
     const int hgrid = int(blocks < int64_t(sms) * 4 ? blocks : int64_t(sms) * 4);
     const unsigned long long *dr = dn ? dn + 2 : nullptr;   // depth-bit range from the binning
     const int tbits = tile_bits(tiles);
     SS_LAUNCH("k_sort_hist", st,
-              k_sort_hist<<<hgrid, 256, 0, st>>>(keys, n_max, dn, dr, tbits, L.ndig, hist, err));
+              k_sort_hist<<<hgrid, 256, 0, st>>>(keys, vals, n_max, dn, dr, tbits, L.ndig, hist,
+                                                 vmax, err));
     SS_LAUNCH("k_sort_scan", st, k_sort_scan<<<L.ndig, 256, 0, st>>>(hist, gofs));
     uint64_t *bk[2] = {keys, ak};
     uint32_t *bv[2] = {vals, av};
@@ -540,19 +658,23 @@ static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int6
         p.dr = dr;
         p.tile_bits = tbits;
         p.ndig = L.ndig;
+        p.vmax = vmax;
+        p.keys = keys;
+        p.ak = ak;
+        p.zk = zk;
         SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<int(L.nparts), 256, dyn, st>>>(p));
     }
     uint32_t *tie_count = tickets + 8;
     uint2 *ties = reinterpret_cast<uint2 *>(ws + L.ties);
     SS_LAUNCH("k_sort_final", st,
               k_sort_final<<<int(blocks), 256, 0, st>>>(keys, vals, ak, av, n_max, dn, dr, tbits,
-                                                        L.ndig, tiles, tile_offsets, err,
+                                                        L.ndig, vmax, tiles, tile_offsets, err,
                                                         tie_count, ties));
     const int64_t max_runs = n_max / (kTieInsert + 1) + 1;
     const int tgrid = int(max_runs < int64_t(sms) * 2 ? max_runs : int64_t(sms) * 2);
     SS_LAUNCH("k_sort_ties", st,
-              k_sort_ties<<<tgrid, 256, 0, st>>>(keys, vals, ak, av, dr, tbits, L.ndig, tie_count,
-                                                 ties));
+              k_sort_ties<<<tgrid, 256, 0, st>>>(keys, vals, ak, av, dr, tbits, L.ndig, vmax,
+                                                 tie_count, ties));
     return check_launch(who);
 }
 

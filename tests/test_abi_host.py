@@ -56,7 +56,7 @@ def test_constants_match_oracle(lib):
     assert buf[1] == np.float32(c["alpha_max"])
     assert buf[2] == np.float32(c["T_eps"])
     assert buf[3] == c["tile"]
-    assert lib.ss_abi_version() == 5
+    assert lib.ss_abi_version() == 6
 
 
 def test_workspace_bytes(lib):

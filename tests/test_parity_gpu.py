@@ -351,6 +351,47 @@ def test_long_runs_of_equal_depths_sort_bit_exact(P):
     assert np.diff(tl["offs"]).max() > 8192
 
 
+@pytest.mark.parametrize("case", ["packed_odd_passes", "packed_even_passes", "unpacked",
+                                  "packed_long_runs"])
+def test_sort_modes_against_the_oracle(P, case):
+    """The passes move one 64-bit word (key bits << value bits | value) when
+    the sorted key bits and the largest value fit in 64 bits together, else a
+    key and a value; the packed words ping-pong so that the last pass lands
+    in the alternate buffer, through a third buffer when the pass count is
+    even.  Synthetic pairs reach each mode: 256 tiles (40 key bits, 5
+    passes), 1,024 tiles (42 bits, 6 passes), 31-bit values (73 bits: not
+    packed), and runs of 3,000 equal keys (the long-run sort after
+    unpacking).  Compared with the oracle's sort and offsets."""
+    import torch
+    import oracle
+    import gaussian_splatting_differentiable_gb300 as ss
+    W, H = (256, 256) if case == "packed_odd_passes" else (512, 512)
+    tiles = ((W + 15) // 16) * ((H + 15) // 16)
+    n = 50000
+    rng = np.random.default_rng(["packed_odd_passes", "packed_even_passes", "unpacked",
+                                 "packed_long_runs"].index(case) + 31)
+    tile = rng.integers(0, tiles, n).astype(np.uint64)
+    dbits = rng.integers(0x3F800000, 0x42C80000, n).astype(np.uint64)
+    vmax = (1 << 31) - 1 if case == "unpacked" else (1 << 20) - 1
+    vals = rng.integers(0, vmax + 1, n).astype(np.uint32)
+    vals[0] = vmax
+    if case == "packed_long_runs":
+        tile[: 2 * 3000] = 7
+        dbits[:3000] = 0x40400000
+        dbits[3000: 2 * 3000] = 0x40A00000
+    keys = (tile << np.uint64(32)) | dbits
+    k_d = torch.from_numpy(keys.view(np.int64)).cuda()
+    v_d = torch.from_numpy(vals.view(np.int32)).cuda()
+    offs = torch.zeros(tiles + 1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(ss.ss_workspace_bytes(0, n, W, H), dtype=torch.uint8, device="cuda")
+    ss.ss_sort_pairs(k_d, v_d, n, W, H, offs, ws)
+    assert ss.ss_sort_status(ws) == ss.SS_OK
+    want_k, want_v = oracle.sort_pairs(keys, vals)
+    assert np.array_equal(k_d.cpu().numpy().view(np.uint64), want_k)
+    assert np.array_equal(v_d.cpu().numpy().view(np.uint32), want_v)
+    assert np.array_equal(offs.cpu().numpy().view(np.uint32), oracle.offsets(want_k, tiles))
+
+
 def test_step_pipeline_matches_single_steps(P):
     """ss.StepPipeline (double-buffered copies in and out around the step's
     graph) returns what a synchronous step computes: the image and the
