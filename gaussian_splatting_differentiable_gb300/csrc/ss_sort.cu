@@ -82,7 +82,7 @@ __device__ __forceinline__ KeyMap key_map(const unsigned long long *dr, int tile
     }
     if (vmax) {
         m.vb = 32 - __clz(int(*vmax));
-        m.packed = m.db + tile_bits + m.vb <= 64;
+        m.packed = m.db + tile_bits + m.vb <= 64 && m.nd >= 2;
     }
     return m;
 }
@@ -108,14 +108,15 @@ __device__ __forceinline__ uint32_t unpack_val(uint64_t w, const KeyMap &m) {
     return uint32_t(w & ((1ull << m.vb) - 1ull));
 }
 
-// Packed mode: the buffer pass d writes.  Pass 0 reads the caller's keys and
-// values; the last pass always lands in the alternate key buffer `ak`, so
-// that the final kernel unpacks into the caller's buffers without reading
-// what it overwrites; the passes between alternate with the caller's key
-// buffer, and `zk` serves pass 0 when the pass count is even.
+// Packed mode: the word buffer pass d < nd - 1 writes.  Pass 0 reads the
+// caller's keys and values, and the last pass writes them back unpacked, so
+// the pass before the last always lands in the alternate key buffer `ak`;
+// the ones before alternate with the caller's key buffer, and `zk` serves
+// pass 0 when it is not the one before the last and would otherwise write
+// the keys it reads.
 __device__ __forceinline__ uint64_t *packed_dest(int d, int nd, uint64_t *keys, uint64_t *ak,
                                                  uint64_t *zk) {
-    return ((nd - 1 - d) & 1) == 0 ? ak : (d == 0 ? zk : keys);
+    return ((nd - 2 - d) & 1) == 0 ? ak : (d == 0 ? zk : keys);
 }
 
 // Number of pairs to sort: n_max, or the device count *dn clamped to n_max.
@@ -224,6 +225,7 @@ struct PassParams {
     // packed mode (null vmax: never packed)
     const uint32_t *vmax;  // largest value, from k_sort_hist
     uint64_t *keys;        // the caller's key buffer
+    uint32_t *vals;        // the caller's value buffer (the last pass's output)
     uint64_t *ak;          // alternate key buffer
     uint64_t *zk;          // third word buffer (pass 0 of an even pass count)
 };
@@ -243,8 +245,9 @@ __device__ __forceinline__ void sort_pass_body(const PassParams &p, const KeyMap
     const int d = p.shift / 8;
     const uint64_t *win = nullptr;
     uint64_t *wout = nullptr;
+    const bool last = d == km.nd - 1;   // packed: writes unpacked keys and values
     if (PACKED) {
-        wout = packed_dest(d, km.nd, p.keys, p.ak, p.zk);
+        if (!last) wout = packed_dest(d, km.nd, p.keys, p.ak, p.zk);
         if (d > 0) win = packed_dest(d - 1, km.nd, p.keys, p.ak, p.zk);
     }
     const int dsh = PACKED ? km.vb + p.shift : p.shift;
@@ -347,8 +350,11 @@ __device__ __forceinline__ void sort_pass_body(const PassParams &p, const KeyMap
         const uint64_t k = s_keys[i];
         const uint32_t dig = digit(k);
         const uint32_t g = s_gbase[dig] + uint32_t(i) - s_lstart[dig];
-        if (PACKED) {
+        if (PACKED && !last) {
             wout[g] = k;
+        } else if (PACKED) {
+            p.keys[g] = unpack_key(k, km);
+            p.vals[g] = unpack_val(k, km);
         } else {
             p.kout[g] = k;
             p.vout[g] = s_vals[i];
@@ -392,6 +398,8 @@ __global__ void __launch_bounds__(256, 3) k_sort_pass(PassParams p) {
 //  - when src != dst the element is copied (run members by the run head).
 constexpr int kTieInsert = 32;   // longest run of equal keys sorted by insertion
 
+constexpr int kFinalPer = 4;   // consecutive sorted elements per k_sort_final thread (measured: 1, 4, 8, 16)
+
 __global__ void __launch_bounds__(256) k_sort_final(uint64_t *dk, uint32_t *dv, uint64_t *ak,
                                                     uint32_t *av, int64_t n_max,
                                                     const unsigned long long *dn,
@@ -401,63 +409,74 @@ __global__ void __launch_bounds__(256) k_sort_final(uint64_t *dk, uint32_t *dv, 
                                                     uint32_t *tie_count, uint2 *ties) {
     // Unpacked, the passes ping-pong between (dk, dv) and (ak, av): after nd
     // of them the sorted data is in (ak, av) iff nd is odd.  Packed, the last
-    // pass wrote words to ak, which are unpacked into (dk, dv) here.
+    // pass wrote it unpacked to (dk, dv).
     const KeyMap km = key_map(dr, tile_bits, ndig, vmax);
-    const bool packed = km.packed;
-    const bool alt = km.nd & 1;
-    const uint64_t *__restrict__ sk = packed || alt ? ak : dk;
+    const bool alt = !km.packed && (km.nd & 1);
+    const uint64_t *sk = alt ? ak : dk;
     const uint32_t *sv = alt ? av : dv;
-    auto K = [&](int64_t j) -> uint64_t { return packed ? unpack_key(sk[j], km) : sk[j]; };
-    auto V = [&](int64_t j) -> uint32_t { return packed ? unpack_val(sk[j], km) : sv[j]; };
-    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const bool copy = alt;
+    const int64_t t0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t n = pair_count(dn, n_max);
-    if (i == 0 && dn && *dn > (unsigned long long)n_max) atomicOr(err, kDevErrCapacity);
-    if (n == 0 && i == 0)
+    if (t0 == 0 && dn && *dn > (unsigned long long)n_max) atomicOr(err, kDevErrCapacity);
+    if (n == 0 && t0 == 0)
         for (int64_t u = 0; u <= tiles; ++u) offs[u] = 0u;
-    if (i >= n) return;
-    const uint64_t key = K(i);
-    int64_t t = int64_t(key >> 32);
-    if (t >= tiles) {
-        atomicOr(err, kDevErrKeyRange);
-        t = tiles;
+    // Elements [i0, i0 + kFinalPer), with their neighbours: all loads issued
+    // together (one element a thread left the kernel waiting on memory).
+    const int64_t i0 = t0 * kFinalPer;
+    if (i0 >= n) return;
+    uint64_t kk[kFinalPer + 2];
+#pragma unroll
+    for (int j = 0; j < kFinalPer + 2; ++j) {
+        const int64_t idx = i0 - 1 + j;
+        kk[j] = idx >= 0 && idx < n ? sk[idx] : 0ull;
     }
-    int64_t tp = -1;
-    if (i > 0) {
-        tp = int64_t(K(i - 1) >> 32);
-        if (tp > tiles) tp = tiles;
-    }
-    for (int64_t u = tp + 1; u <= t; ++u) offs[u] = uint32_t(i);
-    if (i == n - 1)
-        for (int64_t u = t + 1; u <= tiles; ++u) offs[u] = uint32_t(n);
+#pragma unroll
+    for (int j = 0; j < kFinalPer; ++j) {
+        const int64_t i = i0 + j;
+        if (i >= n) continue;
+        const uint64_t key = kk[j + 1];
+        int64_t t = int64_t(key >> 32);
+        if (t >= tiles) {
+            atomicOr(err, kDevErrKeyRange);
+            t = tiles;
+        }
+        int64_t tp = -1;
+        if (i > 0) {
+            tp = int64_t(kk[j] >> 32);
+            if (tp > tiles) tp = tiles;
+        }
+        for (int64_t u = tp + 1; u <= t; ++u) offs[u] = uint32_t(i);
+        if (i == n - 1)
+            for (int64_t u = t + 1; u <= tiles; ++u) offs[u] = uint32_t(n);
 
-    const bool copy = packed || sk != dk;
-    const bool member = i > 0 && K(i - 1) == key;
-    if (member) return;
-    const bool head = i + 1 < n && K(i + 1) == key;
-    if (!head) {
-        if (copy) {
-            dk[i] = key;
-            dv[i] = V(i);
+        const bool member = i > 0 && kk[j] == key;
+        if (member) continue;
+        const bool head = i + 1 < n && kk[j + 2] == key;
+        if (!head) {
+            if (copy) {
+                dk[i] = key;
+                dv[i] = sv[i];
+            }
+            continue;
         }
-        return;
-    }
-    int64_t e = i + 1;
-    while (e < n && K(e) == key && e - i <= kTieInsert) ++e;
-    if (e - i > kTieInsert) {   // a long run: k_sort_ties sorts (and copies) it
-        while (e < n && K(e) == key) ++e;
-        ties[atomicAdd(tie_count, 1u)] = make_uint2(uint32_t(i), uint32_t(e - i));
-        return;
-    }
-    // insertion sort of the run's values by value, written to dv[i..e)
-    for (int64_t a = i; a < e; ++a) {
-        const uint32_t v = V(a);
-        int64_t b = a;
-        while (b > i && dv[b - 1] > v) {
-            dv[b] = dv[b - 1];
-            --b;
+        int64_t e = i + 1;
+        while (e < n && sk[e] == key && e - i <= kTieInsert) ++e;
+        if (e - i > kTieInsert) {   // a long run: k_sort_ties sorts (and copies) it
+            while (e < n && sk[e] == key) ++e;
+            ties[atomicAdd(tie_count, 1u)] = make_uint2(uint32_t(i), uint32_t(e - i));
+            continue;
         }
-        dv[b] = v;
-        if (copy) dk[a] = key;
+        // insertion sort of sv[i..e) by value, written to dv[i..e)
+        for (int64_t a = i; a < e; ++a) {
+            const uint32_t v = sv[a];
+            int64_t b = a;
+            while (b > i && dv[b - 1] > v) {
+                dv[b] = dv[b - 1];
+                --b;
+            }
+            dv[b] = v;
+            if (copy) dk[a] = key;
+        }
     }
 }
 
@@ -545,24 +564,15 @@ __global__ void __launch_bounds__(256) k_sort_ties(uint64_t *dk, uint32_t *dv, u
     __shared__ uint32_t s_wc[8 * 256];
     __shared__ uint32_t s_cnt[256];
     __shared__ uint32_t s_warp[8];
+    // source: the passes' last output buffer (packed: the caller's, which
+    // the last pass wrote unpacked); scratch: the other one
     const KeyMap km = key_map(dr, tile_bits, ndig, vmax);
-    // Unpacked -- source: the passes' last output buffer; scratch: the other
-    // one.  Packed -- each run is first unpacked from ak into (dk, dv), then
-    // sorted there with (ak, av) as scratch.
-    const bool alt = km.nd & 1;
-    uint64_t *sk = km.packed ? dk : alt ? ak : dk, *ok_ = km.packed ? ak : alt ? dk : ak;
-    uint32_t *sv = km.packed ? dv : alt ? av : dv, *ov = km.packed ? av : alt ? dv : av;
+    const bool alt = !km.packed && (km.nd & 1);
+    uint64_t *sk = alt ? ak : dk, *ok_ = alt ? dk : ak;
+    uint32_t *sv = alt ? av : dv, *ov = alt ? dv : av;
     const uint32_t nt = *tie_count;
     for (uint32_t r = blockIdx.x; r < nt; r += gridDim.x) {
         const uint2 run = ties[r];
-        if (km.packed) {
-            for (uint32_t e = threadIdx.x; e < run.y; e += 256) {
-                const uint64_t w = ak[run.x + e];
-                dk[run.x + e] = unpack_key(w, km);
-                dv[run.x + e] = unpack_val(w, km);
-            }
-            __syncthreads();
-        }
         segment_sort_global(sk, sv, ok_, ov, dk, dv, int64_t(run.x), int(run.y),
                             sk[run.x] >> 32, s_cnt, s_wc, s_warp);
         __syncthreads();
@@ -660,14 +670,16 @@ static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int6
         p.ndig = L.ndig;
         p.vmax = vmax;
         p.keys = keys;
+        p.vals = vals;
         p.ak = ak;
         p.zk = zk;
         SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<int(L.nparts), 256, dyn, st>>>(p));
     }
     uint32_t *tie_count = tickets + 8;
     uint2 *ties = reinterpret_cast<uint2 *>(ws + L.ties);
+    const int64_t fblocks = (n_max + 256 * kFinalPer - 1) / (256 * kFinalPer);
     SS_LAUNCH("k_sort_final", st,
-              k_sort_final<<<int(blocks), 256, 0, st>>>(keys, vals, ak, av, n_max, dn, dr, tbits,
+              k_sort_final<<<int(fblocks), 256, 0, st>>>(keys, vals, ak, av, n_max, dn, dr, tbits,
                                                         L.ndig, vmax, tiles, tile_offsets, err,
                                                         tie_count, ties));
     const int64_t max_runs = n_max / (kTieInsert + 1) + 1;
