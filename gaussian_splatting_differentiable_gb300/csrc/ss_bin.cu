@@ -32,10 +32,12 @@ __global__ void __launch_bounds__(256) k_emit_pairs(BinParams p) {
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     int x0 = 0, y0 = 0, x1 = -1, y1 = -1, st = 0;
     uint32_t dbits = 0;
-    if (i < p.s.n) st = splat_tile_rect(p.s, i, p.tiles_x, p.tiles_y, x0, y0, x1, y1, dbits);
+    float rx = 0.0f, ry = 0.0f;
+    if (i < p.s.n)
+        st = splat_tile_rect(p.s, i, p.tiles_x, p.tiles_y, x0, y0, x1, y1, dbits, rx, ry);
     const uint32_t cnt = st > 0 ? uint32_t(x1 - x0 + 1) * uint32_t(y1 - y0 + 1) : 0u;
     if (i < p.s.n) {
-        const SplatRecord r = st >= 0 ? make_record(p.s, uint32_t(i)) : invisible_record();
+        const SplatRecord r = st >= 0 ? make_record(p.s, uint32_t(i), rx, ry) : invisible_record();
         float4 *dst = reinterpret_cast<float4 *>(p.records + i);
         dst[0] = *reinterpret_cast<const float4 *>(&r.geo);
         dst[1] = *reinterpret_cast<const float4 *>(&r.geo2);

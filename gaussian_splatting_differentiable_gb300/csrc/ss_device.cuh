@@ -67,7 +67,8 @@ __device__ __forceinline__ float ln_series(float x) {
 // sqrt(k c / det) and sqrt(k a / det), Q = [[a, b], [b, c]].
 __device__ __forceinline__ int splat_tile_rect(const SplatPtrs &s, int64_t i, int32_t tiles_x,
                                                int32_t tiles_y, int &x0, int &y0, int &x1,
-                                               int &y1, uint32_t &depth_bits) {
+                                               int &y1, uint32_t &depth_bits, float &rx_out,
+                                               float &ry_out) {
     const float2 mu = reinterpret_cast<const float2 *>(s.mean2d)[i];
     const float a = s.conic[3 * i], b = s.conic[3 * i + 1], c = s.conic[3 * i + 2];
     const float o = s.opacity[i], d = s.depth[i];
@@ -86,6 +87,8 @@ __device__ __forceinline__ int splat_tile_rect(const SplatPtrs &s, int64_t i, in
     const float rx = __fsqrt_rn(__fdiv_rn(__fmul_rn(k, c), det));
     const float ry = __fsqrt_rn(__fdiv_rn(__fmul_rn(k, a), det));
     if (rx != rx || ry != ry) return -1;
+    rx_out = rx;
+    ry_out = ry;
     float fx0 = floorf(__fmul_rn(__fsub_rn(mu.x, rx), 0.0625f));
     float fx1 = floorf(__fmul_rn(__fadd_rn(mu.x, rx), 0.0625f));
     float fy0 = floorf(__fmul_rn(__fsub_rn(mu.y, ry), 0.0625f));
@@ -142,8 +145,11 @@ __device__ __forceinline__ SplatRecord invisible_record() {
     return r;
 }
 
-// Record of splat idx from the SoA inputs.
-__device__ __forceinline__ SplatRecord make_record(const SplatPtrs &s, uint32_t idx) {
+// Record of splat idx from the SoA inputs; rx, ry: the half widths of its
+// binning rectangle (the alpha ellipse's box, k already widened), which the
+// cull box grows by 0.4 % + 0.01 px.
+__device__ __forceinline__ SplatRecord make_record(const SplatPtrs &s, uint32_t idx, float rx,
+                                                   float ry) {
     const float2 mu = reinterpret_cast<const float2 *>(s.mean2d)[idx];
     const float a = s.conic[3 * idx], b = s.conic[3 * idx + 1], c = s.conic[3 * idx + 2];
     const float o = s.opacity[idx];
@@ -151,11 +157,8 @@ __device__ __forceinline__ SplatRecord make_record(const SplatPtrs &s, uint32_t 
     r.geo = SplatGeo{mu.x, mu.y, __fmul_rn(-0.5f * kLog2e, a), __fmul_rn(-kLog2e, b)};
     r.geo2 = SplatGeo2{__fmul_rn(-0.5f * kLog2e, c), -log2f(__fmul_rn(255.0f, o)), o, s.depth[idx]};
     r.col = SplatCol{s.rgb[3 * idx], s.rgb[3 * idx + 1], s.rgb[3 * idx + 2], idx};
-    const float k = 2.0f * fmaxf(__logf(255.0f * o), 0.0f);
-    const float det = a * c - b * b;
-    const float rx = sqrtf(k * c / det) * 1.004f + 0.01f;
-    const float ry = sqrtf(k * a / det) * 1.004f + 0.01f;
-    r.box = SplatBox{mu.x - rx, mu.x + rx, mu.y - ry, mu.y + ry};
+    const float bx = rx * 1.004f + 0.01f, by = ry * 1.004f + 0.01f;
+    r.box = SplatBox{mu.x - bx, mu.x + bx, mu.y - by, mu.y + by};
     return r;
 }
 

@@ -375,19 +375,22 @@ __global__ void __launch_bounds__(256, 3) k_sort_pass(PassParams p) {
     const int tid = threadIdx.x;
     const KeyMap km = key_map(p.dr, p.tile_bits, p.ndig, p.vmax);
     if (p.shift / 8 >= km.nd) return;   // past the last digit of the mapped key
-    if (tid == 0) s_part = atomicAdd(p.ticket, 1u);
-    for (int k = tid; k < 8 * 256; k += 256) (&s_whist[0][0])[k] = 0;
-    __syncthreads();
-    const int64_t part = s_part;
-    if (p.dn) {  // grid sized for the capacity: surplus partitions leave
-        const int64_t n = pair_count(p.dn, p.n);
-        if (part * kSortPart >= n) return;
-        p.n = n;
+    if (p.dn) p.n = pair_count(p.dn, p.n);   // the device count, clamped to the capacity
+    // Persistent: each CTA takes partitions by ticket until none is left (a
+    // CTA only ever waits on partitions that running CTAs have taken).
+    for (;;) {
+        if (tid == 0) s_part = atomicAdd(p.ticket, 1u);
+        for (int k = tid; k < 8 * 256; k += 256) (&s_whist[0][0])[k] = 0;
+        __syncthreads();
+        const int64_t part = s_part;
+        if (part * kSortPart >= p.n) return;
+        if (km.packed)
+            sort_pass_body<true>(p, km, part, s_whist, s_lstart, s_gbase, s_warp, s_keys, s_vals);
+        else
+            sort_pass_body<false>(p, km, part, s_whist, s_lstart, s_gbase, s_warp, s_keys,
+                                  s_vals);
+        __syncthreads();   // the shared arrays are reused by the next partition
     }
-    if (km.packed)
-        sort_pass_body<true>(p, km, part, s_whist, s_lstart, s_gbase, s_warp, s_keys, s_vals);
-    else
-        sort_pass_body<false>(p, km, part, s_whist, s_lstart, s_gbase, s_warp, s_keys, s_vals);
 }
 
 // Ties and offsets.  For element i of the sorted keys:
@@ -652,6 +655,8 @@ static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int6
     SS_LAUNCH("k_sort_scan", st, k_sort_scan<<<L.ndig, 256, 0, st>>>(hist, gofs));
     uint64_t *bk[2] = {keys, ak};
     uint32_t *bv[2] = {vals, av};
+    // persistent pass CTAs: as many as fit on the GPU at once (3 a SM)
+    const int pgrid = int(L.nparts < int64_t(sms) * 3 ? L.nparts : int64_t(sms) * 3);
     for (int d = 0; d < L.ndig; ++d) {
         PassParams p{};
         p.kin = bk[d & 1];
@@ -673,7 +678,7 @@ static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int6
         p.vals = vals;
         p.ak = ak;
         p.zk = zk;
-        SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<int(L.nparts), 256, dyn, st>>>(p));
+        SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<pgrid, 256, dyn, st>>>(p));
     }
     uint32_t *tie_count = tickets + 8;
     uint2 *ties = reinterpret_cast<uint2 *>(ws + L.ties);
