@@ -43,7 +43,7 @@ WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H) {
     off = align256(off + size_t(L.ndig) * 256 * 4);
     L.gofs = off;
     off = align256(off + size_t(L.ndig) * 256 * 4);
-    L.tickets = off;              // [0, 8) pass tickets, [8] long tie runs, [9] largest value
+    L.tickets = off;              // [0, 8) pass tickets, [8] long tie runs, [9] largest value, [10] histogram CTAs done
     off = align256(off + 16 * 4);
     L.lookback = off;
     off = align256(off + size_t(L.ndig) * size_t(L.nparts) * 256 * 8);

@@ -47,7 +47,7 @@ struct WsLayout {
     size_t hist;          // uint32 [ndig][256] digit counts
     size_t gofs;          // uint32 [ndig][256] exclusive digit starts
     size_t tickets;       // uint32 [16]: partition tickets per pass, [8] long-run count,
-                          // [9] largest value (packed-pass decision)
+                          // [9] largest value (packed-pass decision), [10] histogram CTAs done
     size_t lookback;      // uint64 [ndig][nparts][256] onesweep look-back words
     size_t zero_end;      // [0, zero_end) is cleared before each sort
     size_t alt_keys;      // uint64 [n_pairs] ping-pong buffer

@@ -5,8 +5,7 @@
 // Here an LSD radix sort in the onesweep style (Adinets & Merrill, "Onesweep:
 // A Faster Least Significant Digit Radix Sort for GPUs", 2022):
 //   k_sort_hist   one read of all keys builds the histograms of every 8-bit
-//                 digit at once;
-//   k_sort_scan   exclusive scan of each digit's histogram;
+//                 digit at once; its last CTA scans them into digit starts;
 //   k_sort_pass   one launch per digit: each CTA takes the next partition of
 //                 4096 keys by an atomic ticket (so a CTA only ever waits on
 //                 CTAs that are already running), ranks its keys with warp
@@ -157,6 +156,7 @@ __global__ void __launch_bounds__(256) k_sort_hist(const uint64_t *__restrict__ 
                                                    const unsigned long long *dn,
                                                    const unsigned long long *dr, int tile_bits,
                                                    int ndig, uint32_t *__restrict__ hist,
+                                                   uint32_t *__restrict__ gofs, uint32_t *done,
                                                    uint32_t *vmax, uint32_t *err) {
     __shared__ uint32_t s_h[8][256];
     const int64_t n = pair_count(dn, n_max);
@@ -199,13 +199,18 @@ __global__ void __launch_bounds__(256) k_sort_hist(const uint64_t *__restrict__ 
         const uint32_t v = (&s_h[0][0])[k];
         if (v) atomicAdd(hist + k, v);
     }
-}
-
-__global__ void __launch_bounds__(256) k_sort_scan(const uint32_t *__restrict__ hist,
-                                                   uint32_t *__restrict__ gofs) {
-    __shared__ uint32_t s_warp[8];
-    const int d = blockIdx.x;
-    gofs[d * 256 + threadIdx.x] = block_excl_scan256(hist[d * 256 + threadIdx.x], s_warp, nullptr);
+    // The last CTA to finish turns the histograms into exclusive digit
+    // starts (the counts of every CTA are in L2 once it sees the count).
+    __shared__ uint32_t s_last, s_warp[8];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int d = 0; d < ndig; ++d)
+        gofs[d * 256 + threadIdx.x] =
+            block_excl_scan256(__ldcg(hist + d * 256 + threadIdx.x), s_warp, nullptr);
 }
 
 struct PassParams {
@@ -651,8 +656,7 @@ static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int6
     const int tbits = tile_bits(tiles);
     SS_LAUNCH("k_sort_hist", st,
               k_sort_hist<<<hgrid, 256, 0, st>>>(keys, vals, n_max, dn, dr, tbits, L.ndig, hist,
-                                                 vmax, err));
-    SS_LAUNCH("k_sort_scan", st, k_sort_scan<<<L.ndig, 256, 0, st>>>(hist, gofs));
+                                                 gofs, tickets + 10, vmax, err));
     uint64_t *bk[2] = {keys, ak};
     uint32_t *bv[2] = {vals, av};
     // persistent pass CTAs: as many as fit on the GPU at once (3 a SM)
