@@ -421,9 +421,9 @@ def kernel_rooflines(kernels: dict, steps: int, n: int, P: int, HW: int, cand: i
     out = {
         "k_emit_pairs": hbm_row(28 * n + 12 * P, per_call("k_emit_pairs"),
                                 "28 B/splat read + 12 B/pair written"),
-        "sort (hist, scan, passes, final, ties)": hbm_row(
+        "sort (hist, passes, final, ties)": hbm_row(
             (24 * passes + 8 + 8) * P,
-            per_call("k_sort_hist", "k_sort_scan", "k_sort_pass", "k_sort_final", "k_sort_ties"),
+            per_call("k_sort_hist", "k_sort_pass", "k_sort_final", "k_sort_ties"),
             "8 B/pair histogram read + 24 B/pair per pass x %d passes run + 8 B/pair offsets" % passes),
     }
     fwd_ms = per_call("k_raster_fwd")
