@@ -291,7 +291,7 @@ def _bin_for_sort(sc, cap_factor=8):
     return r, n, keys, vals
 
 
-@pytest.mark.parametrize("kind", ["wide", "narrow", "equal", "three_values"])
+@pytest.mark.parametrize("kind", ["wide", "narrow", "equal", "three_values", "narrow_1024_tiles"])
 def test_device_count_sort_over_the_recorded_depth_range(P, kind):
     """The device-count sort takes its digits from (tile, depth bits - lo)
     on the bits the recorded depth range needs (fewer passes when the range
@@ -299,11 +299,15 @@ def test_device_count_sort_over_the_recorded_depth_range(P, kind):
     lexsort of the binned pairs, with the range the binning recorded
     checked against the splats that have pairs."""
     import gaussian_splatting_differentiable_gb300 as ss
-    sc = _scene(300, 200, 20000, seed=21)
+    # 300 x 200 has 247 tiles (8 tile bits: 3 passes for a narrow range, 5
+    # for the wide one); 512 x 512 has 1,024 (10 bits: 4 passes, an even
+    # count, for a narrow range)
+    sc = _scene(512, 512, 20000, seed=21) if kind == "narrow_1024_tiles" else \
+        _scene(300, 200, 20000, seed=21)
     rng = np.random.default_rng(21)
     if kind == "wide":        # every exponent from 1e-3 to 1e5: all 32 depth bits
         sc.depth[:] = (10.0 ** rng.uniform(-3, 5, sc.n)).astype(np.float32)
-    elif kind == "narrow":    # a few ulps apart: the 16-bit minimum
+    elif kind in ("narrow", "narrow_1024_tiles"):    # a few ulps apart: the 16-bit minimum
         sc.depth[:] = rng.uniform(2.0, 2.001, sc.n).astype(np.float32)
     elif kind == "equal":
         sc.depth[:] = np.float32(3.0)
