@@ -17,8 +17,8 @@ import torch
 
 from . import _lib
 from ._lib import (SS_ACCUM_WEIGHT, SS_DISTORTION, SS_ERR_CAPACITY, SS_ERR_DEVICE,  # noqa: F401
-                   SS_ERR_TIMEOUT, SS_MEDIAN_DEPTH, SS_OK, SS_WEIGHT_STATS, STATUS_NAMES, SsGrads,
-                   SsSplats)
+                   SS_ERR_TIMEOUT, SS_MEDIAN_DEPTH, SS_OK, SS_RECORDS_CLEARED, SS_WEIGHT_STATS,
+                   STATUS_NAMES, SsGrads, SsSplats)
 
 _L = _lib.load()
 TILE = 16
@@ -162,12 +162,16 @@ def ss_sort_status(workspace, stream=None) -> int:
 def ss_raster_fwd(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int, H: int, bg,
                   flags: int, image, T_final, last_contrib, median_depth, blend_masks,
                   max_weight=None, blend_count=None, distortion=None, dist_totals=None,
-                  stream=None) -> None:
+                  stream=None, bwd_workspace=None) -> None:
+    """bwd_workspace: the workspace of the following ss_raster_bwd, whose
+    gradient records the forward then clears (pass SS_RECORDS_CLEARED to
+    that call; nothing may write the workspace in between)."""
+    nbytes = 0 if bwd_workspace is None else bwd_workspace.numel() * bwd_workspace.element_size()
     _check(_L.ss_raster_fwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), n_pairs, W,
                             H, _f32_host3(bg), flags, _ptr(image), _ptr(T_final),
                             _ptr(last_contrib), _ptr(median_depth), _ptr(blend_masks),
                             _ptr(max_weight), _ptr(blend_count), _ptr(distortion),
-                            _ptr(dist_totals), _stream(stream)),
+                            _ptr(dist_totals), _ptr(bwd_workspace), nbytes, _stream(stream)),
            "ss_raster_fwd")
 
 
@@ -382,6 +386,7 @@ class Rasterizer:
             self.grads["ddepth"] = torch.empty(n_splats, dtype=torch.float32, device=d)
         self.n_pairs = 0
         self.culled = 0
+        self._records_cleared = False   # the forward cleared the backward's records since the last sort
 
     def _alloc_pairs(self, cap: int):
         d = self.device
@@ -408,22 +413,28 @@ class Rasterizer:
         self.n_pairs, self.culled = pairs, culled
         ss_sort_pairs(self.keys, self.vals, pairs, self.W, self.H, self.tile_offsets,
                       self.workspace, stream)
+        self._records_cleared = False   # the sort wrote the workspace
         return pairs
 
     def forward(self, splats: Splats = None, stream=None) -> None:
-        """Composite; uses the records written by the last bin_and_sort."""
+        """Composite; uses the records written by the last bin_and_sort.  Also
+        clears the backward's gradient records in the workspace, so that the
+        next backward() skips that pass."""
         ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs, self.W,
                       self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
                       self.median_depth, self.blend_masks, self.max_weight, self.blend_count,
-                      self.distortion, self.dist_totals, stream)
+                      self.distortion, self.dist_totals, stream, bwd_workspace=self.workspace)
+        self._records_cleared = True
 
     def backward(self, splats, dL_dimage: torch.Tensor, stream=None, dL_ddist=None) -> None:
         """Gradients; uses the records written by the last bin_and_sort.
         dL_ddist: [H, W] upstream gradient of the distortion (SS_DISTORTION)."""
+        flags = self.flags | (SS_RECORDS_CLEARED if self._records_cleared else 0)
         ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs, self.W,
-                      self.H, self.bg, self.flags, self.T_final, self.last_contrib,
+                      self.H, self.bg, flags, self.T_final, self.last_contrib,
                       self.blend_masks, dL_dimage, self.grads, self.accum_weight, self.workspace,
                       stream, self.dist_totals, dL_ddist)
+        self._records_cleared = False   # the backward's sums are in them now
 
     def step(self, splats: Splats, dL_dimage: torch.Tensor, stream=None, dL_ddist=None) -> int:
         """One pass of the whole path: bin, sort, forward, backward."""
@@ -445,9 +456,10 @@ class Rasterizer:
         ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.capacity, self.W,
                       self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
                       self.median_depth, self.blend_masks, self.max_weight, self.blend_count,
-                      self.distortion, self.dist_totals, stream)
+                      self.distortion, self.dist_totals, stream, bwd_workspace=self.workspace)
         ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.capacity, self.W,
-                      self.H, self.bg, self.flags, self.T_final, self.last_contrib,
+                      self.H, self.bg, self.flags | SS_RECORDS_CLEARED, self.T_final,
+                      self.last_contrib,
                       self.blend_masks, dL_dimage, self.grads, self.accum_weight, self.workspace,
                       stream, self.dist_totals, dL_ddist)
 

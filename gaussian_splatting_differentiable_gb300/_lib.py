@@ -20,6 +20,7 @@ SS_ACCUM_WEIGHT = 1
 SS_MEDIAN_DEPTH = 2
 SS_WEIGHT_STATS = 4
 SS_DISTORTION = 8
+SS_RECORDS_CLEARED = 16   # bwd: the forward already cleared the gradient records
 
 
 class SsSplats(ctypes.Structure):
@@ -65,7 +66,7 @@ PROTOTYPES = {
     "ss_sort_pairs_dev": (ctypes.c_int, [P, P, P, I64, I32, I32, P, P, SZ, P]),
     "ss_sort_status": (ctypes.c_int, [P, P]),
     "ss_raster_fwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P, P, P,
-                                     P, P, P]),
+                                     P, P, P, SZ, P]),
     "ss_raster_bwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P, P,
                                      ctypes.POINTER(SsGrads), P, P, SZ, P]),
     "ss_raster_bwd_noalloc": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P,

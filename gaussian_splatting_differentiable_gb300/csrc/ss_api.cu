@@ -78,7 +78,7 @@ using namespace ss;
 
 extern "C" {
 
-int32_t ss_abi_version(void) { return 6; }
+int32_t ss_abi_version(void) { return 7; }
 
 size_t ss_record_bytes(int32_t n_splats) { return n_splats < 0 ? 0 : size_t(n_splats) * 64; }
 

@@ -524,7 +524,8 @@ __global__ void k_bwd_zero(BwdParams p, int64_t n, bool accum) {
     }
 }
 
-// AoS mode: clear the per-splat gradient records.
+// AoS mode: clear the per-splat gradient records (skipped when the forward
+// cleared them: SS_RECORDS_CLEARED).
 __global__ void k_grad_zero(float4 *scratch, int64_t n4) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
@@ -577,7 +578,8 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     clear_error();
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd: image %dx%d outside 1..%d", W, H, kMaxSide);
-    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION))
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION |
+                          SS_RECORDS_CLEARED))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: unknown flag bits 0x%x", flags);
     const bool dist = flags & SS_DISTORTION;
     if (dist && (!dist_totals || !dL_ddist))
@@ -643,8 +645,10 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t want = (int64_t(n) + 255) / 256;
     const int zgrid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
-    SS_LAUNCH("k_grad_zero", st,
-              k_grad_zero<<<zgrid, 256, 0, st>>>(reinterpret_cast<float4 *>(p.scratch), 3 * int64_t(n)));
+    if (!(flags & SS_RECORDS_CLEARED))   // else ss_raster_fwd cleared them
+        SS_LAUNCH("k_grad_zero", st,
+                  k_grad_zero<<<zgrid, 256, 0, st>>>(reinterpret_cast<float4 *>(p.scratch),
+                                                     3 * int64_t(n)));
     const int grid = tiles_x(W) * tiles_y(H);
     if (accum && dist)
         SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, true, true><<<grid, 256, kBwdDynSmem, st>>>(p)));

@@ -47,10 +47,6 @@ struct FwdParams {
     const uint32_t *vals;
     const uint32_t *offs;
     uint32_t *masks;   // [8][n_pairs]
-    int64_t n_pairs;
-    int32_t n;
-    int32_t W, H;
-    float bg[3];
     float *image;
     float *T_final;
     uint32_t *last;
@@ -59,6 +55,11 @@ struct FwdParams {
     uint32_t *count;       // [n] blending pixels (STATS)
     float *dist;           // [H][W] depth distortion (DIST)
     float4 *dist_totals;   // [H][W] (A, D1, D2, z_ref) (DIST)
+    float4 *clear;         // the backward's gradient records to clear (3 n float4), or null
+    uint32_t n_pairs;      // < 2^32 (checked on the host)
+    int32_t n;
+    uint16_t W, H;         // <= 32768 (checked on the host)
+    float bg[3];
 };
 static_assert(sizeof(FwdParams) <= 128, "kernel parameters over 128 bytes run slower");
 
@@ -93,6 +94,14 @@ __global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
     if (STATS) {
         s_smax[0][tid] = 0u, s_smax[1][tid] = 0u;
         s_scnt[0][tid] = 0u, s_scnt[1][tid] = 0u;
+    }
+    // The backward's gradient records, cleared here when the caller asks (a
+    // few 16-byte stores a thread, hidden under this kernel's arithmetic,
+    // instead of a separate bandwidth-bound pass before the backward).
+    if (p.clear) {
+        const int64_t n4 = 3 * int64_t(p.n), stride = int64_t(gridDim.x) * 256;
+        for (int64_t i = int64_t(tile) * 256 + tid; i < n4; i += stride)
+            p.clear[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     // STATS: thread t sends entry t of a finished batch (buffer b, nb entries)
     // and clears its slots; each thread reads only its own record slot, which
@@ -244,6 +253,7 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
                                    float *T_final, uint32_t *last_contrib, float *median_depth,
                                    uint32_t *blend_masks, float *max_weight,
                                    uint32_t *blend_count, float *distortion, float *dist_totals,
+                                   void *bwd_workspace, size_t bwd_workspace_bytes,
                                    ss_stream_t stream) {
     clear_error();
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
@@ -274,24 +284,35 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
     const bool median = flags & SS_MEDIAN_DEPTH;
     if (median && !median_depth)
         return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: SS_MEDIAN_DEPTH set but median_depth NULL");
+    if (bwd_workspace) {
+        if (reinterpret_cast<uintptr_t>(bwd_workspace) & 255)
+            return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: bwd_workspace not 256-byte aligned");
+        const size_t need = ws_layout(n_splats, 0, W, H).bwd_end;
+        if (bwd_workspace_bytes < need)
+            return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: bwd_workspace %zu bytes < %zu needed",
+                        bwd_workspace_bytes, need);
+    }
     FwdParams p{};
     p.recs = static_cast<const SplatRecord *>(records);
     p.n = n_splats;
     p.vals = vals;
     p.offs = tile_offsets;
-    p.W = W;
-    p.H = H;
+    p.W = uint16_t(W);
+    p.H = uint16_t(H);
     for (int c = 0; c < 3; ++c) p.bg[c] = bg ? bg[c] : 0.0f;
     p.image = image;
     p.T_final = T_final;
     p.last = last_contrib;
     p.median = median_depth;
     p.masks = blend_masks;
-    p.n_pairs = n_pairs;
+    p.n_pairs = uint32_t(n_pairs);
     p.max_w_bits = reinterpret_cast<uint32_t *>(max_weight);
     p.count = blend_count;
     p.dist = distortion;
     p.dist_totals = reinterpret_cast<float4 *>(dist_totals);
+    p.clear = bwd_workspace ? reinterpret_cast<float4 *>(static_cast<unsigned char *>(bwd_workspace) +
+                                                         ws_layout(n_splats, 0, W, H).accum)
+                            : nullptr;
     const int grid = tiles_x(W) * tiles_y(H);
     cudaStream_t st = (cudaStream_t)stream;
     if (stats && n_splats > 0) {

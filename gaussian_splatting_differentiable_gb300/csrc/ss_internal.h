@@ -12,7 +12,7 @@
 namespace ss {
 
 constexpr int kTile = 16;
-constexpr int32_t kMaxSide = 32768;
+constexpr int32_t kMaxSide = 32768;   // fits the forward's 16-bit image sides
 constexpr int kSortThreads = 256;
 constexpr int kSortKeysPerThread = 16;
 constexpr int kSortPart = kSortThreads * kSortKeysPerThread;  // keys per onesweep partition

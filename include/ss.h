@@ -71,9 +71,13 @@ enum {
     SS_WEIGHT_STATS = 4u,  /* fwd: per-splat max blend weight and blending-pixel count
                               ("max wt" and, with the accumulated weight, the "Avg"
                               weight of the Spirula Studio write-up, 机制拆解 / 亲手验证) */
-    SS_DISTORTION = 8u     /* fwd: per-pixel depth distortion and its totals; bwd: its
+    SS_DISTORTION = 8u,    /* fwd: per-pixel depth distortion and its totals; bwd: its
                               gradient, including dL/ddepth (the write-up's distortion
                               option with per-pixel float4 totals, 最小改动) */
+    SS_RECORDS_CLEARED = 16u  /* bwd only: the gradient records in the workspace were
+                                 cleared by ss_raster_fwd (its bwd_workspace argument)
+                                 and nothing wrote the workspace since; the backward
+                                 then skips its own clearing pass */
 };
 
 /* Splats, structure of arrays, float32, device memory.  The pages' inputs:
@@ -233,13 +237,22 @@ ss_status ss_sort_status(const void *workspace, ss_stream_t stream);
  *   n_pairs: the stride of blend_masks and a bound on the pairs sorted: the
  *            pair count, or the capacity when the count stayed on the device
  *            (ss_sort_pairs_dev).  The backward must get the same value.
+ *   bwd_workspace, bwd_workspace_bytes: optional (NULL: unused).  The
+ *            workspace the following ss_raster_bwd gets (256-byte aligned,
+ *            >= ss_workspace_bytes(n_splats, 0, W, H) bytes): the forward's
+ *            CTAs then also clear the backward's per-splat gradient records
+ *            in it (a few stores a thread, hidden under the compositing),
+ *            and that ss_raster_bwd call, given SS_RECORDS_CLEARED, skips its
+ *            separate clearing pass.  No call may write the workspace in
+ *            between (ss_sort_pairs uses the same bytes).
  * Pair values >= n_splats are ignored. */
 ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *vals,
                         const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,
                         const float *bg, uint32_t flags, float *image, float *T_final,
                         uint32_t *last_contrib, float *median_depth, uint32_t *blend_masks,
                         float *max_weight, uint32_t *blend_count, float *distortion,
-                        float *dist_totals, ss_stream_t stream);
+                        float *dist_totals, void *bwd_workspace, size_t bwd_workspace_bytes,
+                        ss_stream_t stream);
 
 /* Backward rasterization ("从 8.6 KB 到 4.2 KB ...", rasterize_bwd_2d on the
  * 2D screen-space path; "Phase 5 step 30b", rasterize_backwards: the 9-field
@@ -275,7 +288,9 @@ ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *v
  *   sum over pixels of alpha T (summed exactly in 32.32 fixed point, so the
  *   result does not depend on the order of the atomics); else may be NULL.
  *   workspace: >= ss_workspace_bytes(n, 0, W, H) bytes (48 per splat + 256),
- *   256-byte aligned; required whenever n > 0.
+ *   256-byte aligned; required whenever n > 0.  Its gradient records are
+ *   cleared here first, unless flags has SS_RECORDS_CLEARED (the forward
+ *   cleared them; see ss_raster_fwd's bwd_workspace).
  *   bg: HOST float[3] or NULL (must match the forward call). */
 ss_status ss_raster_bwd(const void *records, int32_t n_splats, const uint32_t *vals,
                         const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,

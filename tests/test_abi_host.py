@@ -56,7 +56,7 @@ def test_constants_match_oracle(lib):
     assert buf[1] == np.float32(c["alpha_max"])
     assert buf[2] == np.float32(c["T_eps"])
     assert buf[3] == c["tile"]
-    assert lib.ss_abi_version() == 6
+    assert lib.ss_abi_version() == 7
 
 
 def test_workspace_bytes(lib):
@@ -94,7 +94,7 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert lib.ss_sort_pairs(0x1000, 0x1000, 10, 16, 16, 0x1000, 0x1000, 16, None) == 1
     assert "workspace" in lib.ss_last_error().decode()
     # forward: unknown flags, NULL outputs, median / stats / distortion flag without buffers
-    F = lambda *a: lib.ss_raster_fwd(*a)  # noqa: E731
+    F = lambda *a: lib.ss_raster_fwd(*a[:-1], None, 0, a[-1])  # noqa: E731  (no bwd_workspace)
     assert F(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 16, 0x1000, 0x1000, 0x1000, None, 0x1000,
              None, None, None, None, None) == 1
     assert F(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 0, None, 0x1000, 0x1000, None, 0x1000,
@@ -123,7 +123,20 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert B(1, g, ws=0x1000, nbytes=8, acc=0x1000) == 1      # small workspace
     assert B(0, g, rec=None) == 1
     assert B(0, g, masks=None) == 1
-    assert B(16, g, ws=0x1000, nbytes=1 << 20) == 1           # unknown flag
+    assert B(32, g, ws=0x1000, nbytes=1 << 20) == 1           # unknown flag
+    # SS_RECORDS_CLEARED is the backward's; the forward and the static-scratch backward reject it
+    assert F(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 16, 0x1000, 0x1000, 0x1000, None,
+             0x1000, None, None, None, None, None) == 1
+    assert lib.ss_raster_bwd_noalloc(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 16, 0x1000,
+                                     0x1000, 0x1000, 0x1000, ctypes.byref(g), None, None) == 1
+    # the forward's optional bwd_workspace: 256-byte aligned and large enough for the records
+    Fw = lambda ws, nbytes: lib.ss_raster_fwd(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 0,  # noqa: E731
+                                              0x1000, 0x1000, 0x1000, None, 0x1000, None, None,
+                                              None, None, ws, nbytes, None)
+    assert Fw(0x1010, 1 << 20) == 1
+    assert "aligned" in lib.ss_last_error().decode()
+    assert Fw(0x1000, 8) == 1
+    assert "bwd_workspace" in lib.ss_last_error().decode()
     assert B(8, g, ws=0x1000, nbytes=1 << 20, dt=0x1000) == 1   # dL_ddist NULL
     assert B(8, g, ws=0x1000, nbytes=1 << 20, dt=0x1008, dd=0x1000) == 1   # misaligned totals
     assert B(8, g, ws=0x1000, nbytes=1 << 20, dt=0x1000, dd=0x1000) == 1   # ddepth NULL

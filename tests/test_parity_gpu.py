@@ -396,6 +396,39 @@ def test_sort_modes_against_the_oracle(P, case):
     assert np.array_equal(offs.cpu().numpy().view(np.uint32), oracle.offsets(want_k, tiles))
 
 
+def test_forward_clears_the_backward_records(P):
+    """ss_raster_fwd with bwd_workspace clears the backward's gradient records
+    and ss_raster_bwd with SS_RECORDS_CLEARED skips its own clearing pass:
+    the result equals that of a backward that clears them itself (gradients
+    to float-atomic ordering, the fixed-point weight bit for bit), although
+    the workspace started as non-zero bytes and the sort wrote over the
+    records' bytes.  A flagged backward on records that nobody cleared adds
+    to the old sums (the weight doubles), so the check is not vacuous."""
+    import torch
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = synth.make_scene(2)
+    sp = ss.Splats.from_numpy(sc)
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, 4 * sc.n, ss.SS_ACCUM_WEIGHT, device="cuda")
+    dL = torch.from_numpy(sc.dL_dimage).cuda()
+    r.workspace.fill_(0x7f)
+    r.bin_and_sort(sp)
+    r.forward(sp)
+    r.backward(sp, dL)            # flagged: the forward cleared the records
+    a = {k: v.clone() for k, v in r.grads.items()}
+    wa = r.accum_weight.clone()
+    args = (r.records, r.n, r.vals, r.tile_offsets, r.n_pairs, sc.W, sc.H, r.bg)
+    rest = (r.T_final, r.last_contrib, r.blend_masks, dL, r.grads, r.accum_weight, r.workspace)
+    ss.ss_raster_bwd(*args, r.flags, *rest)      # clears them itself
+    torch.cuda.synchronize()
+    assert torch.equal(r.accum_weight, wa)
+    for k, v in a.items():
+        tol = max(1e-4, 1e-3 * float(v.abs().max()))
+        assert float((r.grads[k] - v).abs().max()) <= tol, k
+    ss.ss_raster_bwd(*args, r.flags | ss.SS_RECORDS_CLEARED, *rest)   # stale sums kept
+    torch.cuda.synchronize()
+    assert torch.equal(r.accum_weight, 2 * wa)
+
+
 def test_step_pipeline_matches_single_steps(P):
     """ss.StepPipeline (double-buffered copies in and out around the step's
     graph) returns what a synchronous step computes: the image and the
