@@ -324,8 +324,8 @@ def measure_ssim(ss, dev, flush, steps: int, hbm: float, hbm_src: str) -> dict:
 def measure_distortion(ss, dev, flush, steps: int, workload: int = 6, extra_flags=None,
                        label: str = "accum_weight + distortion") -> dict:
     """The step with an output variant (default: accumulated weight + depth
-    distortion) on a 2M-splat 1237x822 scene, as a CUDA graph, L2 flushed
-    before each replay; per-kernel times from a second, profiled pass."""
+    distortion) on a 2M-splat scene, as a CUDA graph, L2 flushed before each
+    replay; per-kernel times from a second, profiled pass."""
     import torch
     import synth
     sc = synth.make_scene(workload)
@@ -611,6 +611,11 @@ def run_ours(args, rank: int, world: int, dist):
         next_rows["f3_weight_stats"] = measure_distortion(
             ss, dev, flush, args.steps, workload=4, extra_flags=ss.SS_WEIGHT_STATS,
             label="accum_weight + weight statistics (max blend weight, blending-pixel count)")
+        # the dense-cluster scene (30 % of the splats in four blobs: tiles of up
+        # to ~14k pairs), with every optional output of the default path on
+        next_rows["dense_blobs"] = measure_distortion(
+            ss, dev, flush, args.steps, workload=5, extra_flags=ss.SS_MEDIAN_DEPTH,
+            label="accum_weight + median depth, 30 % of the splats in four dense blobs")
 
     # --- end to end through the public API with host buffers
     e2e = None
