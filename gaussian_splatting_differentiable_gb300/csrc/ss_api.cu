@@ -29,6 +29,13 @@ ss_status check_cuda(cudaError_t e, const char *what) {
 
 ss_status check_launch(const char *what) { return check_cuda(cudaGetLastError(), what); }
 
+ss_status current_device(int *dev, int *sms, const char *what) {
+    ss_status s = check_cuda(cudaGetDevice(dev), what);
+    if (s == SS_OK && sms)
+        s = check_cuda(cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev), what);
+    return s;
+}
+
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H) {
@@ -145,8 +152,8 @@ ss_status ss_probe_red_f32(float *buf, int64_t n, int32_t rounds, ss_stream_t st
     if (!buf || n < 1 || rounds < 0)
         return fail(SS_ERR_INVALID_ARG, "ss_probe_red_f32: bad buffer, size or rounds");
     int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    ss_status s = current_device(&dev, &sms, "ss_probe_red_f32: device query");
+    if (s != SS_OK) return s;
     const int64_t want = (n + 255) / 256;
     const int grid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
     SS_LAUNCH("k_probe_red", (cudaStream_t)stream,

@@ -49,6 +49,8 @@
 // select the entries each warp handles and each pixel's bit, so nothing is
 // re-evaluated; after a chunk of 16 selected entries each pixel walks only
 // its own blended entries (independent trip counts per lane).
+#include <atomic>
+
 #include "ss_device.cuh"
 #include "ss_internal.h"
 #include "ss_profile.h"
@@ -488,11 +490,12 @@ constexpr int kBwdDynSmem = 2 * 8 * kSlots * kSlotPad * 4;
 
 // k_raster_bwd's slot buffers are dynamic shared memory on top of ~25 KB of
 // static arrays: raise its limit once per device.
-static int g_bwd_attr_set[64];
+static std::atomic<int> g_bwd_attr_set[64];   // set once per device; any thread
 static ss_status ensure_bwd_smem() {
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && g_bwd_attr_set[dev]) return SS_OK;
+    const ss_status ds = current_device(&dev, nullptr, "ss_raster_bwd: cudaGetDevice");
+    if (ds != SS_OK) return ds;
+    if (dev >= 0 && dev < 64 && g_bwd_attr_set[dev].load(std::memory_order_acquire)) return SS_OK;
     const void *fns[6] = {(const void *)k_raster_bwd<true, true, false>,
                           (const void *)k_raster_bwd<false, true, false>,
                           (const void *)k_raster_bwd<true, false, false>,
@@ -504,7 +507,7 @@ static ss_status ensure_bwd_smem() {
         s = check_cuda(cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             kBwdDynSmem),
                        "ss_raster_bwd: cudaFuncSetAttribute");
-    if (s == SS_OK && dev >= 0 && dev < 64) g_bwd_attr_set[dev] = 1;
+    if (s == SS_OK && dev >= 0 && dev < 64) g_bwd_attr_set[dev].store(1, std::memory_order_release);
     return s;
 }
 
@@ -641,8 +644,8 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     ss_status es = ensure_bwd_smem();
     if (es != SS_OK) return es;
     int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    es = current_device(&dev, &sms, "ss_raster_bwd: device query");
+    if (es != SS_OK) return es;
     const int64_t want = (int64_t(n) + 255) / 256;
     const int zgrid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
     if (!(flags & SS_RECORDS_CLEARED))   // else ss_raster_fwd cleared them
@@ -685,7 +688,7 @@ constexpr int32_t kNoAllocMaxSplats = 1 << 21;  // 2,097,152 splats -> 16 MiB of
 
 static __device__ __align__(256) unsigned long long g_noalloc_accum[kNoAllocMaxSplats];
 
-static unsigned long long *g_noalloc_ptr[64];  // device address of the array, per device
+static std::atomic<unsigned long long *> g_noalloc_ptr[64];  // device address of the array, per device
 
 }  // namespace ss
 
@@ -738,14 +741,14 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     if (s != SS_OK) return s;
     if (dev < 0 || dev >= 64)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd_noalloc: device %d >= 64", dev);
-    if (accum && !g_noalloc_ptr[dev]) {
+    if (accum && !g_noalloc_ptr[dev].load(std::memory_order_acquire)) {
         // First call on this device (with this device current): look up the
         // array's device address once.
         void *ptr = nullptr;
         s = check_cuda(cudaGetSymbolAddress(&ptr, g_noalloc_accum),
                        "ss_raster_bwd_noalloc: cudaGetSymbolAddress");
         if (s != SS_OK) return s;
-        g_noalloc_ptr[dev] = static_cast<unsigned long long *>(ptr);
+        g_noalloc_ptr[dev].store(static_cast<unsigned long long *>(ptr), std::memory_order_release);
     }
 
     BwdParams p{};
@@ -766,11 +769,12 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     p.dconic = grads->dconic;
     p.dopacity = grads->dopacity;
     p.drgb = grads->drgb;
-    p.accum = accum ? g_noalloc_ptr[dev] : nullptr;
+    p.accum = accum ? g_noalloc_ptr[dev].load(std::memory_order_acquire) : nullptr;
     cudaStream_t st = (cudaStream_t)stream;
     s = ensure_bwd_smem();
     if (s != SS_OK) return s;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    s = current_device(&dev, &sms, "ss_raster_bwd_noalloc: device query");
+    if (s != SS_OK) return s;
     const int64_t want = (int64_t(n) + 255) / 256;
     const int zgrid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
     // k_bwd_zero clears this call's part of the shared array before use.

@@ -26,6 +26,8 @@ void clear_error();
 ss_status check_launch(const char *what);
 // SS_ERR_CUDA with the text of `e` if e != cudaSuccess.
 ss_status check_cuda(cudaError_t e, const char *what);
+// The current device and its SM count (an error status if either query fails).
+ss_status current_device(int *dev, int *sms, const char *what);
 
 inline int32_t tiles_x(int32_t W) { return (W + kTile - 1) / kTile; }
 inline int32_t tiles_y(int32_t H) { return (H + kTile - 1) / kTile; }

@@ -35,6 +35,8 @@
 // (tile << db) | (depth bits - lo) on db + ceil(log2 tiles) bits and takes
 // its digits from that; passes past the last digit return at once, and the
 // final kernels find the sorted data by the parity of the passes run.
+#include <atomic>
+
 #include "ss_device.cuh"
 #include "ss_internal.h"
 #include "ss_profile.h"
@@ -587,18 +589,19 @@ __global__ void __launch_bounds__(256) k_sort_ties(uint64_t *dk, uint32_t *dv, u
     }
 }
 
-static int g_attr_set[64];
+static std::atomic<int> g_attr_set[64];   // set once per device; any thread
 
 // k_sort_pass needs 48 KB of dynamic shared memory (32 KB when packed) on
 // top of its static arrays: raise its limit once per device.
 static ss_status ensure_pass_smem(int dyn) {
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && g_attr_set[dev]) return SS_OK;
+    const ss_status ds = current_device(&dev, nullptr, "ss_sort_pairs: cudaGetDevice");
+    if (ds != SS_OK) return ds;
+    if (dev >= 0 && dev < 64 && g_attr_set[dev].load(std::memory_order_acquire)) return SS_OK;
     ss_status s = check_cuda(
         cudaFuncSetAttribute(k_sort_pass, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn),
         "ss_sort_pairs: cudaFuncSetAttribute");
-    if (s == SS_OK && dev >= 0 && dev < 64) g_attr_set[dev] = 1;
+    if (s == SS_OK && dev >= 0 && dev < 64) g_attr_set[dev].store(1, std::memory_order_release);
     return s;
 }
 
@@ -635,8 +638,8 @@ static ss_status sort_impl(const char *who, uint64_t *keys, uint32_t *vals, int6
                           "sort: memset offsets");
 
     int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    s = current_device(&dev, &sms, "ss_sort_pairs: device query");
+    if (s != SS_OK) return s;
     const int dyn = kSortPart * 12;
     s = ensure_pass_smem(dyn);
     if (s != SS_OK) return s;
