@@ -419,7 +419,9 @@ class Rasterizer:
     def forward(self, splats: Splats = None, stream=None) -> None:
         """Composite; uses the records written by the last bin_and_sort.  Also
         clears the backward's gradient records in the workspace, so that the
-        next backward() skips that pass."""
+        next backward() skips that pass; bin_and_sort() resets that, but a
+        sort called directly on this workspace between forward() and
+        backward() must be followed by forward() again."""
         ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs, self.W,
                       self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
                       self.median_depth, self.blend_masks, self.max_weight, self.blend_count,
