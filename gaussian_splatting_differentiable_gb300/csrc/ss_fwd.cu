@@ -63,8 +63,13 @@ struct FwdParams {
 };
 static_assert(sizeof(FwdParams) <= 128, "kernel parameters over 128 bytes run slower");
 
+// A minimum of CTAs a SM only where it measured faster: five for the plain
+// variant (48 registers, ~3 µs at 2M splats), four for the distortion one
+// (62 registers); the statistics and median variants ran slower bounded
+// (0.585 vs 0.567 and 0.517 vs 0.513 ms) and keep the compiler's choice.
 template <bool MEDIAN, bool STATS, bool DIST>
-__global__ void __launch_bounds__(256) k_raster_fwd(FwdParams p) {
+__global__ void __launch_bounds__(256, (!MEDIAN && !STATS && !DIST) ? 5 : (DIST && !STATS && !MEDIAN) ? 4 : 0)
+k_raster_fwd(FwdParams p) {
     __shared__ SplatGeo s_geo[2][256];
     __shared__ SplatGeo2 s_geo2[2][256];
     __shared__ SplatCol s_col[2][256];
