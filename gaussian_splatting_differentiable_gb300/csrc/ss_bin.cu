@@ -27,7 +27,9 @@ struct BinParams {
     SplatRecord *records;          // [n] 64-byte records for the rasterizers
 };
 
-__global__ void __launch_bounds__(256) k_emit_pairs(BinParams p) {
+// Six CTAs a SM (40 registers, one 4-byte spill): 0.068 -> 0.065 ms at 2M
+// splats, measured against the compiler's own choice (42 registers).
+__global__ void __launch_bounds__(256, 6) k_emit_pairs(BinParams p) {
     const int lane = threadIdx.x & 31;
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     int x0 = 0, y0 = 0, x1 = -1, y1 = -1, st = 0;
