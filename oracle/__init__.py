@@ -6,7 +6,9 @@ never imports it, and it imports nothing of the product package.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import ctypes
+import heapq
 import os
 import subprocess
 
@@ -109,7 +111,20 @@ def _bind(lib):
     lib.orc_backward.argtypes = [P(_SplatsD), P(_Frame), ctypes.c_void_p, P(_Grads), P(_Grads),
                                  ctypes.c_void_p]
     lib.orc_backward.restype = ctypes.c_int
+    lib.orc_margins.argtypes = [ctypes.c_double] * 6 + [P(ctypes.c_double)]
+    lib.orc_margins.restype = None
+    lib.orc_trace_pixel.argtypes = [P(_SplatsD), ctypes.c_void_p, ctypes.c_int64,
+                                    ctypes.c_double, ctypes.c_double, ctypes.c_void_p,
+                                    ctypes.c_int64, P(ctypes.c_double), P(ctypes.c_int32)]
+    lib.orc_trace_pixel.restype = ctypes.c_int64
+    lib.orc_margins_n.argtypes = [ctypes.c_int64] + [ctypes.c_void_p] * 8
+    lib.orc_margins_n.restype = None
     return lib
+
+
+TRACE_DTYPE = np.dtype([("pos", "<i8"), ("alpha", "<f8"), ("G", "<f8"), ("T", "<f8"),
+                        ("mrel", "<f8"), ("relT", "<f8"), ("clamped", "<i4"), ("pad", "<i4")])
+MAX_AMB = 8
 
 
 def _p(a):
@@ -212,32 +227,88 @@ def _frame(scene, vals, offs, tile_mask, bg, keep, dL_ddist=None):
                   _p(vals) if vals.size else None, _p(offs), mask_p, _p(dd))
 
 
-def forward(scene, vals, offs, tile_mask=None, params=None, bg=None, alt_capacity=1 << 16):
+def tile_parts(W: int, H: int, offs, tile_mask, parts: int) -> list:
+    """The selected tiles split into at most `parts` disjoint tile masks of
+    about equal work (a tile's pairs times its pixels, plus its pixels):
+    tiles in decreasing order of work, each onto the lightest part so far.
+    Only the partition is computed here; each part is an ordinary oracle
+    call restricted to its tiles."""
+    tx, ty = tiles_xy(W, H)
+    T = tx * ty
+    sel = np.ones(T, bool) if tile_mask is None else np.asarray(tile_mask).astype(bool)
+    idx = np.nonzero(sel)[0]
+    parts = max(1, min(int(parts), idx.size))
+    per = np.diff(np.asarray(offs, np.int64))[idx]
+    px = np.minimum(16, W - 16 * (idx % tx)) * np.minimum(16, H - 16 * (idx // tx))
+    cost = (per + 1) * px
+    heap = [(0, k) for k in range(parts)]
+    masks = np.zeros((parts, T), np.uint8)
+    for t in np.argsort(-cost, kind="stable"):
+        load_k, k = heapq.heappop(heap)
+        masks[k, idx[t]] = 1
+        heapq.heappush(heap, (load_k + int(cost[t]), k))
+    return [m for m in masks if m.any()] or [masks[0]]
+
+
+def default_threads() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def forward(scene, vals, offs, tile_mask=None, params=None, bg=None, alt_capacity=1 << 16,
+            threads: int = 1):
     """Front-to-back compositing of every pixel of the (masked) tiles.
 
     Returns image [3][H][W], T_final, last, median, n_amb (knife-edge count per
     pixel), alts (structured array of alternative outcomes) and the per-splat
     max_w (max blend weight), count (blended pixels) and splat_amb (blended at
     a knife-edge pixel in some outcome), dist (the depth distortion per
-    pixel) and dist_err (a bound on its float32 evaluation error)."""
+    pixel) and dist_err (a bound on its float32 evaluation error).
+
+    threads > 1 splits the tiles into parts (tile_parts) run concurrently,
+    one oracle call per part on its own thread (the C call releases the
+    interpreter lock).  Pixels are computed by exactly the same code either
+    way, so every per-pixel output is identical; the per-splat maximum,
+    count and flag are combined exactly (max, integer sum, or); alternatives
+    come out grouped by part."""
     lib = load()
     keep = []
     s = _splats_d(scene, params, keep)
-    f = _frame(scene, vals, offs, tile_mask, bg, keep)
     H, W = scene.H, scene.W
     res = {"image": np.zeros((3, H, W)), "T_final": np.ones((H, W)),
            "last": np.zeros((H, W), np.uint32), "median": np.zeros((H, W)),
            "n_amb": np.zeros((H, W), np.uint8), "max_w": np.zeros(scene.n),
            "count": np.zeros(scene.n, np.uint32), "splat_amb": np.zeros(scene.n, np.uint8),
            "dist": np.zeros((H, W)), "dist_err": np.zeros((H, W))}
-    out = _FwdOut(*[_p(res[k]) for k in ("image", "T_final", "last", "median", "n_amb",
-                                         "max_w", "count", "splat_amb", "dist", "dist_err")])
-    alts = np.zeros(max(alt_capacity, 1), ALT_DTYPE)
-    n_alt = lib.orc_forward(ctypes.byref(s), ctypes.byref(f), ctypes.byref(out), _p(alts),
-                            alt_capacity)
-    if n_alt > alt_capacity:
-        raise RuntimeError("oracle alternative buffer too small: %d > %d" % (n_alt, alt_capacity))
-    res["alts"] = alts[:n_alt].copy()
+    masks = [tile_mask] if threads <= 1 else tile_parts(W, H, offs, tile_mask, threads)
+
+    def run(mask):
+        # per-pixel arrays are shared (the parts' pixels are disjoint); the
+        # per-splat ones are the part's own
+        own = {"max_w": np.zeros(scene.n), "count": np.zeros(scene.n, np.uint32),
+               "splat_amb": np.zeros(scene.n, np.uint8)}
+        mine = []
+        f = _frame(scene, vals, offs, mask, bg, mine)
+        out = _FwdOut(*[_p(own[k] if k in own else res[k])
+                        for k in ("image", "T_final", "last", "median", "n_amb", "max_w",
+                                  "count", "splat_amb", "dist", "dist_err")])
+        alts = np.zeros(max(alt_capacity, 1), ALT_DTYPE)
+        n_alt = lib.orc_forward(ctypes.byref(s), ctypes.byref(f), ctypes.byref(out), _p(alts),
+                                alt_capacity)
+        if n_alt > alt_capacity:
+            raise RuntimeError("oracle alternative buffer too small: %d > %d" %
+                               (n_alt, alt_capacity))
+        return own, alts[:n_alt].copy()
+
+    if len(masks) == 1:
+        outs = [run(masks[0])]
+    else:
+        with concurrent.futures.ThreadPoolExecutor(len(masks)) as ex:
+            outs = list(ex.map(run, masks))
+    for own, _ in outs:
+        np.maximum(res["max_w"], own["max_w"], out=res["max_w"])
+        res["count"] += own["count"]
+        np.maximum(res["splat_amb"], own["splat_amb"], out=res["splat_amb"])
+    res["alts"] = np.concatenate([a for _, a in outs]) if len(outs) > 1 else outs[0][1]
     return res
 
 
@@ -250,22 +321,87 @@ def _grads(n):
 
 
 def backward(scene, vals, offs, tile_mask=None, params=None, bg=None, dL_dimage=None,
-             slack=True, dL_ddist=None):
+             slack=True, dL_ddist=None, threads: int = 1):
     """Per-splat gradients of L = sum dL/dimage * image (+ sum dL/ddist * dist
     when dL_ddist is given) from the masked tiles.
+
+    threads > 1 splits the tiles into parts (tile_parts), one oracle call per
+    part on its own thread, each into its own per-splat buffers, which are
+    then added in part order (the oracle's per-tile contributions are
+    additive; only the order of the double-precision sums differs).
 
     Returns dict(grads=..., slack=... or None, accum_err=...)."""
     lib = load()
     keep = []
     s = _splats_d(scene, params, keep)
-    f = _frame(scene, vals, offs, tile_mask, bg, keep, dL_ddist)
     g = np.ascontiguousarray(scene.dL_dimage if dL_dimage is None else dL_dimage, np.float64)
     keep.append(g)
-    gr = _grads(scene.n)
-    sl = _grads(scene.n) if slack else None
-    aerr = np.zeros(scene.n)
-    cg = _Grads(*[_p(gr[k]) for k in _GRAD_KEYS])
-    cs = _Grads(*[_p(sl[k]) for k in _GRAD_KEYS]) if slack else None
-    lib.orc_backward(ctypes.byref(s), ctypes.byref(f), _p(g), ctypes.byref(cg),
-                     ctypes.byref(cs) if slack else None, _p(aerr))
+    masks = [tile_mask] if threads <= 1 else tile_parts(scene.W, scene.H, offs, tile_mask,
+                                                        threads)
+
+    def run(mask):
+        mine = []
+        f = _frame(scene, vals, offs, mask, bg, mine, dL_ddist)
+        gr = _grads(scene.n)
+        sl = _grads(scene.n) if slack else None
+        aerr = np.zeros(scene.n)
+        cg = _Grads(*[_p(gr[k]) for k in _GRAD_KEYS])
+        cs = _Grads(*[_p(sl[k]) for k in _GRAD_KEYS]) if slack else None
+        lib.orc_backward(ctypes.byref(s), ctypes.byref(f), _p(g), ctypes.byref(cg),
+                         ctypes.byref(cs) if slack else None, _p(aerr))
+        return gr, sl, aerr
+
+    if len(masks) == 1:
+        outs = [run(masks[0])]
+    else:
+        with concurrent.futures.ThreadPoolExecutor(len(masks)) as ex:
+            outs = list(ex.map(run, masks))
+    gr, sl, aerr = outs[0]
+    for g2, s2, a2 in outs[1:]:
+        for k in _GRAD_KEYS:
+            gr[k] += g2[k]
+            if slack:
+                sl[k] += s2[k]
+        aerr += a2
     return {"grads": gr, "slack": sl, "accum_err": aerr}
+
+
+def margins(a, b, c, dx, dy, o):
+    """(skip margin, value margin) of the knife-edge model at one (pixel,
+    splat): relative bounds on a float32 evaluation's alpha-floor decision
+    and on its alpha."""
+    out = (ctypes.c_double * 2)()
+    load().orc_margins(float(a), float(b), float(c), float(dx), float(dy), float(o), out)
+    return out[0], out[1]
+
+
+def margins_n(a, b, c, dx, dy, o):
+    """margins() over arrays: (skip margins, value margins)."""
+    arrs = [np.ascontiguousarray(np.broadcast_to(np.asarray(v, np.float64), np.shape(a)))
+            for v in (a, b, c, dx, dy, o)]
+    n = arrs[0].size
+    skip, val = np.zeros(n), np.zeros(n)
+    load().orc_margins_n(n, *[_p(v) for v in arrs], _p(skip), _p(val))
+    return skip.reshape(np.shape(a)), val.reshape(np.shape(a))
+
+
+def trace_pixel(scene, vals, offs, x: int, y: int, params=None):
+    """The oracle's compositing of pixel (x, y) over its tile's list, with the
+    error bounds of its knife-edge decisions: dict(rec = blended splats
+    (TRACE_DTYPE), T_final, relT, last, n_amb, amb = [(list position, kind)])."""
+    lib = load()
+    keep = []
+    s = _splats_d(scene, params, keep)
+    tx, _ = tiles_xy(scene.W, scene.H)
+    t = (y // TILE) * tx + x // TILE
+    offs = np.asarray(offs, np.int64)
+    lst = np.ascontiguousarray(np.asarray(vals, np.uint32)[offs[t]:offs[t + 1]])
+    rec = np.zeros(max(lst.size, 1), TRACE_DTYPE)
+    tail = (ctypes.c_double * 4)()
+    amb = (ctypes.c_int32 * (2 * MAX_AMB))()
+    n = lib.orc_trace_pixel(ctypes.byref(s), _p(lst) if lst.size else None, lst.size, x + 0.5,
+                            y + 0.5, _p(rec), rec.size, tail, amb)
+    na = min(int(tail[3]), MAX_AMB)
+    return {"rec": rec[:n].copy(), "T_final": tail[0], "relT": tail[1], "last": int(tail[2]),
+            "n_amb": int(tail[3]), "amb": [(amb[2 * j], amb[2 * j + 1]) for j in range(na)],
+            "list": lst}

@@ -53,7 +53,7 @@
 #define ALPHA_MIN (1.0 / 255.0)
 #define ALPHA_MAX 0.99
 #define T_EPS 1e-4
-#define MAX_AMB 8
+#define MAX_AMB ORC_MAX_AMB
 
 /* Margins of the binning ellipse (R7): k is widened by a relative and an
  * absolute 2^-10 so that float32 rounding of ln, products and square roots
@@ -64,6 +64,12 @@
 /* Unit roundoff of float32: the error model of the GPU's float evaluation
  * that decides which pixels are knife edges. */
 #define U32 (1.0 / 16777216.0)
+/* Relative error of the hardware base-2 exponential (ex2.approx.f32, whose
+ * documented bound is 2^-22), taken with a factor 2. */
+#define EX2_REL (1.0 / 2097152.0)
+/* First-order bounds are used below; this factor covers the neglected
+ * higher-order terms (of relative size n u, n the operations chained). */
+#define FIRST_ORDER 1.05
 
 void orc_constants(double out[4])
 {
@@ -229,6 +235,7 @@ typedef struct {
     double alpha, G;
     double T;          /* transmittance before blending */
     double mrel;       /* relative error bound of a float32 alpha here */
+    double relT;       /* relative error bound of a float32 T before blending */
     int clamped;
 } blend_rec;
 
@@ -245,14 +252,59 @@ typedef struct {
     int amb_kind[MAX_AMB];
 } pix_run;
 
-/* Relative error bound of alpha evaluated in float32 (dx, dy rounded, three
- * products summed, exp): 32 u times the sum of the magnitudes of sigma's
- * terms, plus 2^-19 for the exponential.  A decision whose margin is inside
- * this bound may be taken either way by a float32 evaluation: a knife edge. */
-static double alpha_margin(double a, double b, double c, double dx, double dy)
+/* Error bounds of a float32 evaluation of a (pixel, splat).  The GPU takes
+ * the exponent in base 2, e2 = A dx^2 + B dx dy + C dy^2 with A, B, C the
+ * float32 products of -log2(e)/2, -log2(e) (each itself rounded) with a, b,
+ * c, dx and dy rounded differences, two products and two fused multiply-adds:
+ * every term carries at most 7 roundings, so |e2_f - e2| <= 7 u log2(e) tau
+ * with tau = |a| dx^2 / 2 + |b dx dy| + |c| dy^2 / 2 (u = 2^-24, first order).
+ *
+ * skip_margin: the floor decision compares e2 with thr = -log2f(fl(255 o)),
+ * whose error is one rounding of 255 o (log2(1 + u) < 1.45 u) plus log2f's
+ * documented 1 ulp (<= 2 u |thr|).  A float32 decision can differ from the
+ * exact one only if |ln(255 alpha)| <= ln 2 (|e2 error| + |thr error|)
+ * <= 7 u tau + 2 u ln(255 o) + u; the returned relative margin on alpha
+ * covers that with the first-order factor.
+ *
+ * value_margin: relative error of the float32 alpha = fl(o ex2(e2_f)):
+ * ln 2 |e2 error| + the exponential's EX2_REL + one rounding, plus the
+ * float32 cap 0.99f (0.16 u above 0.99).
+ *
+ * A decision whose distance to its threshold is inside these bounds may be
+ * taken either way by a float32 evaluation: a knife edge. */
+static double sigma_terms(double a, double b, double c, double dx, double dy)
 {
-    const double terms = 0.5 * fabs(a) * dx * dx + 0.5 * fabs(c) * dy * dy + fabs(b * dx * dy);
-    return 32.0 * U32 * (terms + 1.0) + 1.0 / 524288.0;
+    return 0.5 * fabs(a) * dx * dx + 0.5 * fabs(c) * dy * dy + fabs(b * dx * dy);
+}
+
+static double skip_margin(double tau, double o)
+{
+    const double l = log(255.0 * o);
+    return FIRST_ORDER * U32 * (7.0 * tau + 2.0 * fabs(l) + 1.0);
+}
+
+static double value_margin(double tau)
+{
+    return FIRST_ORDER * (7.0 * U32 * tau + EX2_REL + 1.5 * U32);
+}
+
+void orc_margins(double a, double b, double c, double dx, double dy, double o, double out[2])
+{
+    const double tau = sigma_terms(a, b, c, dx, dy);
+    out[0] = skip_margin(tau, o);
+    out[1] = value_margin(tau);
+}
+
+void orc_margins_n(int64_t n, const double *a, const double *b, const double *c,
+                   const double *dx, const double *dy, const double *o, double *skip,
+                   double *value)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double m[2];
+        orc_margins(a[i], b[i], c[i], dx[i], dy[i], o[i], m);
+        skip[i] = m[0];
+        value[i] = m[1];
+    }
 }
 
 static void note_amb(pix_run *r, int64_t pos, int kind)
@@ -284,7 +336,8 @@ static void run_pixel(const orc_splats_d *s, const uint32_t *list, int64_t len, 
         const double sigma = 0.5 * (a * dx * dx + c * dy * dy) + b * dx * dy;
         const double G = exp(-sigma);
         const double oG = s->opacity[i] * G;
-        const double mrel = alpha_margin(a, b, c, dx, dy);
+        const double tau = sigma_terms(a, b, c, dx, dy);
+        const double mrel = value_margin(tau);
 
         int clamped = oG > ALPHA_MAX;
         if (fabs(oG - ALPHA_MAX) <= mrel * ALPHA_MAX)
@@ -293,18 +346,23 @@ static void run_pixel(const orc_splats_d *s, const uint32_t *list, int64_t len, 
             clamped = !clamped;
         const double alpha = clamped ? ALPHA_MAX : oG;
 
+        /* the floor is decided on the unclamped exponent (alpha >= 1/255
+         * holds or fails for o G and min(0.99, o G) alike) */
         int skip = alpha < ALPHA_MIN;
-        if (fabs(alpha - ALPHA_MIN) <= mrel * alpha)
+        if (fabs(oG - ALPHA_MIN) <= skip_margin(tau, s->opacity[i]) * oG)
             note_amb(r, k, ORC_AMB_ALPHA);
         if (k == flip_pos && flip_kind == ORC_AMB_ALPHA)
             skip = !skip;
         if (skip)
             continue;
 
+        /* T' = fl(T fl(1 - alpha)): the subtraction carries alpha's error
+         * (alpha mrel / (1 - alpha)) and one rounding, the product one more;
+         * the threshold 1e-4f lies 0.42 u below 1e-4 */
         const double Tn = r->T * (1.0 - alpha);
-        const double rel_om = (alpha * mrel + U32) / (1.0 - alpha);
+        const double rel_om = alpha * mrel / (1.0 - alpha) + U32;
         int stop = Tn < T_EPS;
-        if (fabs(Tn - T_EPS) <= 4.0 * (r->relT + rel_om + U32) * Tn)
+        if (fabs(Tn - T_EPS) <= FIRST_ORDER * (r->relT + rel_om + 2.0 * U32) * Tn)
             note_amb(r, k, ORC_AMB_TERM);
         if (k == flip_pos && flip_kind == ORC_AMB_TERM)
             stop = !stop;
@@ -312,7 +370,7 @@ static void run_pixel(const orc_splats_d *s, const uint32_t *list, int64_t len, 
             break;
 
         int med = r->T > 0.5;
-        if (fabs(r->T - 0.5) <= 4.0 * (r->relT + U32) * r->T)
+        if (fabs(r->T - 0.5) <= FIRST_ORDER * r->relT * r->T)
             note_amb(r, k, ORC_AMB_MEDIAN);
         if (k == flip_pos && flip_kind == ORC_AMB_MEDIAN)
             med = !med;
@@ -328,11 +386,49 @@ static void run_pixel(const orc_splats_d *s, const uint32_t *list, int64_t len, 
         e->G = G;
         e->T = r->T;
         e->mrel = mrel;
+        e->relT = r->relT;
         e->clamped = clamped;
         r->T = Tn;
         r->relT += rel_om + U32;
         r->last = (uint32_t)(k + 1);
     }
+}
+
+/* Test accessor: one pixel's compositing as run_pixel does it, with the
+ * error bounds the knife-edge decisions use.  out[k] (k < min(n, cap))
+ * receives the k-th blended splat: list position, alpha, G, T before it,
+ * its alpha error bound and the bound on T before it.  tail = (T_final, the
+ * bound on T_final, last_contrib, number of knife-edge decisions); amb
+ * receives up to ORC_MAX_AMB (position, kind) pairs.  Returns n. */
+int64_t orc_trace_pixel(const orc_splats_d *s, const uint32_t *list, int64_t len, double px,
+                        double py, orc_trace_rec *out, int64_t cap, double tail[4],
+                        int32_t *amb)
+{
+    pix_run r;
+    r.rec = malloc(sizeof(blend_rec) * (size_t)(len > 0 ? len : 1));
+    run_pixel(s, list, len, px, py, -1, 0, &r);
+    for (int64_t k = 0; k < r.n && k < cap; ++k) {
+        out[k].pos = r.rec[k].pos;
+        out[k].alpha = r.rec[k].alpha;
+        out[k].G = r.rec[k].G;
+        out[k].T = r.rec[k].T;
+        out[k].mrel = r.rec[k].mrel;
+        out[k].relT = r.rec[k].relT;
+        out[k].clamped = r.rec[k].clamped;
+        out[k].pad = 0;
+    }
+    tail[0] = r.T;
+    tail[1] = r.relT;
+    tail[2] = (double)r.last;
+    tail[3] = (double)r.n_amb;
+    const int na = r.n_amb < MAX_AMB ? r.n_amb : MAX_AMB;
+    for (int j = 0; j < na && amb; ++j) {
+        amb[2 * j] = (int32_t)r.amb_pos[j];
+        amb[2 * j + 1] = r.amb_kind[j];
+    }
+    const int64_t n = r.n;
+    free(r.rec);
+    return n;
 }
 
 /* R17 by its definition: the double sum over pairs of blended splats.
@@ -545,8 +641,16 @@ static void add_fields(orc_grads *gr, int64_t i, const double *v, int absval)
 /* Accumulates (+=) into grads; the caller zeroes them.  slack (may be NULL)
  * receives, per splat and field, the sum over knife-edge decisions of
  * |alternative - normal| contribution.  accum_err (may be NULL) receives a
- * bound on the error of a float32 evaluation of the accumulated weight:
- * per blended pixel w (2 relT + mrel + 4 u (n + 2)) + 2^-32. */
+ * bound on the error of a float32 evaluation of the accumulated weight, per
+ * blended pixel w (2 relT + 3 u n + mrel + 33 u) + 2^-32 with relT the
+ * bound on the pixel's final T and n its blended splats: the backward
+ * recovers T in front of a splat from T_final by one rounded 1 - alpha, one
+ * reciprocal of at most 1 ulp (2 u) and one rounded product per later
+ * splat (at most relT + 3 u n beyond T_final's own relT), w = alpha T adds
+ * alpha's mrel and a rounding; the sum over the at most 32 pixels of a
+ * block in float32 adds at most 31 u of the block's weight (32 u a pixel),
+ * and the 32.32 fixed-point conversion at most 2^-33 a block (2^-32 a
+ * pixel). */
 int orc_backward(const orc_splats_d *s, const orc_frame *f, const double *dL_dimage,
                  orc_grads *grads, orc_grads *slack, double *accum_err)
 {
@@ -582,7 +686,7 @@ int orc_backward(const orc_splats_d *s, const orc_frame *f, const double *dL_dim
                         add_fields(grads, i, c1 + NF * k, 0);
                         if (accum_err) {
                             const double relw = 2.0 * r.relT + r.rec[k].mrel +
-                                                4.0 * U32 * (double)(r.n + 2);
+                                                3.0 * U32 * (double)r.n + 33.0 * U32;
                             accum_err[i] += c1[NF * k + F_W] * relw + 1.0 / 4294967296.0;
                         }
                     }

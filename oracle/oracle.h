@@ -90,6 +90,18 @@ typedef struct {               /* per-splat fields, all double */
     double *ddepth;            /* [n] (only with dL_ddist; may be NULL) */
 } orc_grads;
 
+/* One blended splat of a traced pixel (orc_trace_pixel). */
+typedef struct {
+    int64_t pos;               /* position in the tile's list */
+    double alpha, G;
+    double T;                  /* transmittance before blending */
+    double mrel;               /* bound on the relative error of a float32 alpha */
+    double relT;               /* bound on the relative error of a float32 T before it */
+    int32_t clamped, pad;
+} orc_trace_rec;
+
+#define ORC_MAX_AMB 8
+
 void orc_constants(double out[4]);   /* alpha_min, alpha_max, T_eps, tile */
 float orc_ln(float x);               /* natural log by the atanh series, float32 */
 
@@ -103,6 +115,19 @@ int orc_offsets(const uint64_t *keys, int64_t n, int32_t n_tiles, uint32_t *offs
 
 int64_t orc_forward(const orc_splats_d *s, const orc_frame *f, orc_fwd_out *out,
                     orc_alt *alts, int64_t alt_capacity);
+
+/* Error bounds of a float32 evaluation at one (pixel, splat), d = pixel -
+ * mean: out[0] the relative margin of the alpha-floor decision, out[1] the
+ * relative error bound of alpha (knife-edge model; see oracle.c). */
+void orc_margins(double a, double b, double c, double dx, double dy, double o, double out[2]);
+/* orc_margins over n (pixel, splat) pairs given as arrays. */
+void orc_margins_n(int64_t n, const double *a, const double *b, const double *c,
+                   const double *dx, const double *dy, const double *o, double *skip,
+                   double *value);
+/* One pixel's front-to-back compositing with its error bounds (test accessor). */
+int64_t orc_trace_pixel(const orc_splats_d *s, const uint32_t *list, int64_t len, double px,
+                        double py, orc_trace_rec *out, int64_t cap, double tail[4],
+                        int32_t *amb);
 int orc_backward(const orc_splats_d *s, const orc_frame *f, const double *dL_dimage,
                  orc_grads *grads, orc_grads *slack, double *accum_err);
 #endif

@@ -141,11 +141,41 @@ def check_pairs(scene, gpu, orc=None):
     return orc
 
 
-def check_forward(scene, gpu, ofw, pixel_mask=None, atol=1e-5):
-    """Compare per pixel; returns dict of counts."""
+# Largest fraction of compared pixels that may be knife edges: 1e-4 on the
+# smaller workloads; the 2M-splat ones blend ~70 splats a pixel, and the
+# sound (worst-case) bound on the float32 transmittance grows with the chain,
+# so more termination decisions fall inside it (measured 4.1e-4 on the
+# 1237x822 scene).
+KNIFE_EDGE_CAP = 1e-4
+KNIFE_EDGE_CAP_DENSE = 5e-4
+
+
+def relevant_knife_edges(scene, ofw):
+    """Pixels with a knife-edge decision that can change a compared output:
+    the alpha floor, the alpha cap and the termination always; the T = 0.5
+    decision only when the median depth is an output.  A pixel with more
+    flagged decisions than the oracle listed alternatives for counts as
+    flagged."""
+    H, W = scene.H, scene.W
+    alts = ofw["alts"]
+    kinds = [oracle.AMB_ALPHA, oracle.AMB_TERM, oracle.AMB_CLAMP]
+    if scene.median_depth:
+        kinds.append(oracle.AMB_MEDIAN)
+    amb = np.zeros(H * W, bool)
+    amb[alts["pixel"][np.isin(alts["kind"], kinds)]] = True
+    listed = np.bincount(alts["pixel"], minlength=H * W)
+    amb |= ofw["n_amb"].reshape(-1).astype(np.int64) > listed
+    return amb.reshape(H, W)
+
+
+def check_forward(scene, gpu, ofw, pixel_mask=None, atol=1e-5, knife_cap=None):
+    """Compare per pixel; returns dict of counts.  knife_cap: if given, the
+    knife-edge pixels (relevant_knife_edges) must be fewer than this
+    fraction of the compared pixels."""
     H, W = scene.H, scene.W
     sel = np.ones((H, W), bool) if pixel_mask is None else pixel_mask
-    clean = sel & (ofw["n_amb"] == 0)
+    flagged = relevant_knife_edges(scene, ofw)
+    clean = sel & ~flagged
     img_err = np.abs(gpu["image"] - ofw["image"]).max(axis=0)
     T_err = np.abs(gpu["T_final"] - ofw["T_final"])
     bad = clean & ((img_err > atol) | (T_err > atol) | (gpu["last"] != ofw["last"]))
@@ -159,7 +189,11 @@ def check_forward(scene, gpu, ofw, pixel_mask=None, atol=1e-5):
             bad_d.sum(), dist_err[bad_d].max(), dist_tol[bad_d][np.argmax(dist_err[bad_d])])
     assert not bad.any(), _describe_bad(bad, gpu, ofw, img_err, T_err)
     # knife edges: the GPU must take the normal outcome or one alternative
-    amb = np.argwhere(sel & (ofw["n_amb"] > 0))
+    amb = np.argwhere(sel & flagged)
+    if knife_cap is not None:
+        assert len(amb) < knife_cap * max(int(sel.sum()), 1), (
+            "%d knife-edge pixels of %d compared: not below %.0e" % (len(amb), sel.sum(),
+                                                                      knife_cap))
     alts = ofw["alts"]
     unmatched = 0
     for (y, x) in amb:
@@ -244,46 +278,19 @@ def _dist_grad(scene):
     return scene.dL_ddist if getattr(scene, "distortion", False) else None
 
 
-def full_parity(scene, capacity=None):
-    gpu = run_gpu(scene, capacity)
+def full_parity(scene, capacity=None, knife_cap=None, graph=False, threads=None):
+    """Every output of the whole path against the oracle, every pixel and
+    every splat.  The oracle runs tile-parallel on the host's cores
+    (oracle.forward / oracle.backward with threads > 1: the same per-pixel
+    code on disjoint tile sets).  graph=True runs the step the way bench.py
+    times it (run_gpu_graph)."""
+    threads = oracle.default_threads() if threads is None else threads
+    gpu = run_gpu_graph(scene) if graph else run_gpu(scene, capacity)
     tl = check_pairs(scene, gpu)
-    ofw = oracle.forward(scene, tl["vals"], tl["offs"], alt_capacity=1 << 20)
-    f = check_forward(scene, gpu, ofw)
+    ofw = oracle.forward(scene, tl["vals"], tl["offs"], alt_capacity=1 << 20, threads=threads)
+    f = check_forward(scene, gpu, ofw, knife_cap=knife_cap)
     s = check_weight_stats(scene, gpu, ofw)
-    obw = oracle.backward(scene, tl["vals"], tl["offs"], dL_ddist=_dist_grad(scene))
+    obw = oracle.backward(scene, tl["vals"], tl["offs"], dL_ddist=_dist_grad(scene),
+                          threads=threads)
     b = check_backward(scene, gpu, obw)
     return {"fwd": f, "stats": s, "bwd": b, "pairs": tl["count"]}
-
-
-def sampled_parity(scene, n_tiles=192, n_splats=256, seed=0, graph=False):
-    """Full-size check: every pair, sort and offset; the forward on a sample
-    of tiles; the gradients of a sample of splats (all of their tiles).
-    graph=True runs the step the way bench.py times it (run_gpu_graph)."""
-    gpu = run_gpu_graph(scene) if graph else run_gpu(scene)
-    tl = check_pairs(scene, gpu)
-    tx, ty = oracle.tiles_xy(scene.W, scene.H)
-    T = tx * ty
-    rng = np.random.default_rng(seed)
-    mask = np.zeros(T, np.uint8)
-    mask[rng.choice(T, min(n_tiles, T), replace=False)] = 1
-    ofw = oracle.forward(scene, tl["vals"], tl["offs"], tile_mask=mask, alt_capacity=1 << 20)
-    pix = np.repeat(np.repeat(mask.reshape(ty, tx), 16, 0), 16, 1)[:scene.H, :scene.W].astype(bool)
-    f = check_forward(scene, gpu, ofw, pixel_mask=pix)
-    # splats with at least one pair; their tiles
-    keys, vals = tl["keys"], tl["vals"]
-    has = np.unique(vals)
-    pick = rng.choice(has, min(n_splats, has.size), replace=False)
-    smask = np.zeros(scene.n, bool)
-    smask[pick] = True
-    tmask = np.zeros(T, np.uint8)
-    tmask[(keys[smask[vals]] >> np.uint64(32)).astype(np.int64)] = 1
-    obw = oracle.backward(scene, tl["vals"], tl["offs"], tile_mask=tmask,
-                          dL_ddist=_dist_grad(scene))
-    b = check_backward(scene, gpu, obw, splat_mask=smask)
-    s = None
-    if gpu["max_w"] is not None:
-        ofw2 = oracle.forward(scene, tl["vals"], tl["offs"], tile_mask=tmask,
-                              alt_capacity=1 << 20)
-        s = check_weight_stats(scene, gpu, ofw2, splat_mask=smask)
-    return {"fwd": f, "stats": s, "bwd": b, "pairs": tl["count"],
-            "bwd_tiles": int(tmask.sum())}
