@@ -128,57 +128,112 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(scene, n_tiles: int, seed: int = 0):
-    """Time the oracle: full binning and sort, forward + backward on n_tiles
-    random tiles; returns (seconds extrapolated to the whole step, details)."""
+def cpu_description() -> dict:
+    """The host's logical CPUs and model name (for the oracle's timings)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip() in ("model name", "Model", "CPU part") and v.strip():
+                    model = v.strip()
+                    break
+    except OSError:
+        pass
+    import platform
+    return {"nproc": os.cpu_count(), "model": model or platform.processor() or platform.machine()}
+
+
+def oracle_bin_sort(scene):
+    """The oracle's binning, sort and tile ranges of the whole scene
+    (single-threaded C)."""
     import oracle
-    t0 = time.perf_counter()
     keys, vals, count, _ = oracle.bin_tiles(scene)
-    t1 = time.perf_counter()
     keys, vals = oracle.sort_pairs(keys, vals)
     tx, ty = oracle.tiles_xy(scene.W, scene.H)
-    offs = oracle.offsets(keys, tx * ty)
-    t2 = time.perf_counter()
+    return vals, oracle.offsets(keys, tx * ty)
+
+
+def oracle_raster(scene, vals, offs, mask, threads: int, sums=None):
+    """The oracle's forward and backward over the tiles of `mask`, split over
+    `threads` host threads (tile-parallel; the per-pixel code as it stands).
+    sums: per-thread gradient accumulators shared by successive calls."""
+    import oracle
+    oracle.forward(scene, vals, offs, tile_mask=mask, threads=threads)
+    oracle.backward(scene, vals, offs, tile_mask=mask, slack=False, threads=threads, into=sums)
+
+
+def oracle_pieces(scene, pieces: int, threads: int, warmup: int = 0):
+    """One whole step of the oracle (bin + sort + forward + backward of every
+    tile) timed in `pieces` consecutive pieces: piece 0 bins and sorts the
+    scene and each piece composites and back-propagates its share of the
+    tiles (oracle.tile_parts: equal work).  Nothing is extrapolated: the
+    pieces together are the whole step.  Returns (piece seconds, details)."""
+    import oracle
+    vals, offs = oracle_bin_sort(scene)
+    masks = oracle.tile_parts(scene.W, scene.H, offs, None, pieces)
+    for k in range(warmup):
+        oracle_raster(scene, vals, offs, masks[k % len(masks)], threads)
+    sums = oracle.backward_sums(scene.n, threads, slack=False)   # zeroed before the timing
+    times = []
+    for k, m in enumerate(masks):
+        t0 = time.perf_counter()
+        if k == 0:
+            vals, offs = oracle_bin_sort(scene)
+        oracle_raster(scene, vals, offs, m, threads, sums)
+        if k == len(masks) - 1:
+            oracle.add_backward_sums(sums)        # the step's gradients
+        times.append(time.perf_counter() - t0)
+    return times, {"pieces": len(masks), "candidates": candidate_pairs(offs, scene.W, scene.H)}
+
+
+def oracle_single_core_rate(scene, n_tiles: int, seed: int = 0) -> dict:
+    """The single-threaded oracle's forward + backward rate on n_tiles random
+    tiles (candidate pairs per second of rasterization; bin + sort excluded)."""
+    import oracle
+    vals, offs = oracle_bin_sort(scene)
+    tx, ty = oracle.tiles_xy(scene.W, scene.H)
     rng = np.random.default_rng(seed)
     mask = np.zeros(tx * ty, np.uint8)
-    mask[rng.choice(tx * ty, n_tiles, replace=False)] = 1
-    t3 = time.perf_counter()
-    oracle.forward(scene, vals, offs, tile_mask=mask)
-    oracle.backward(scene, vals, offs, tile_mask=mask, slack=False)
-    t4 = time.perf_counter()
-    full = candidate_pairs(offs, scene.W, scene.H)
+    mask[rng.choice(tx * ty, min(n_tiles, tx * ty), replace=False)] = 1
+    t0 = time.perf_counter()
+    oracle_raster(scene, vals, offs, mask, 1)
+    dt = time.perf_counter() - t0
     per = np.diff(offs.astype(np.int64))
     wx = np.minimum(16, scene.W - 16 * (np.arange(tx * ty) % tx))
     wy = np.minimum(16, scene.H - 16 * (np.arange(tx * ty) // tx))
-    sample = int((per * wx * wy)[mask.astype(bool)].sum())
-    t_step = (t1 - t0) + (t2 - t1) + (t4 - t3) * full / max(sample, 1)
-    return t_step, {"bin_s": t1 - t0, "sort_s": t2 - t1, "raster_sample_s": t4 - t3,
-                    "sample_candidates": sample, "full_candidates": full, "measured_s": t4 - t0}
+    cand = int((per * wx * wy)[mask.astype(bool)].sum())
+    return {"value": cand / dt, "unit": UNIT, "cores": 1, "tiles": int(mask.sum()),
+            "candidates": cand, "seconds": dt,
+            "what": "forward + backward of %d random tiles, single-threaded" % int(mask.sum())}
 
 
 def run_reference(args, rank: int):
+    import oracle
     import synth
     if rank != 0:
         return
     scene = synth.make_scene(args.workload)
-    n_tiles = 6
-    times, det = [], None
-    for k in range(args.warmup + args.steps):
-        t, det = oracle_sample(scene, n_tiles, seed=k)
-        if k >= args.warmup:
-            times.append(t)
-    t = statistics.mean(times)
-    value = det["full_candidates"] / t
-    sample = ("per step: full binning and sort of the %d-splat scene, forward+backward on %d "
-              "random 16x16 tiles (%d candidate pairs), raster time scaled to all %d candidate "
-              "pairs" % (scene.n, n_tiles, det["sample_candidates"], det["full_candidates"]))
+    threads = oracle.default_threads()
+    times, det = oracle_pieces(scene, max(1, args.steps), threads, warmup=args.warmup)
+    total = sum(times)
+    steps = len(times)
+    value = det["candidates"] / total
+    sample = ("the %d timed steps are one whole step of the %d-splat scene: step 0 bins and "
+              "sorts the scene (single-threaded) and each step runs the forward and backward "
+              "of a 1/%d share of the tiles (equal work), tile-parallel on %d threads; %d "
+              "warm-up steps ran a share each first" % (steps, scene.n, steps, threads,
+                                                       args.warmup))
+    cpu = cpu_description()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": synth.WORKLOADS[args.workload].name, "W": scene.W, "H": scene.H,
-                       "splats": scene.n},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                       "splats": scene.n, "candidate_splat_px": det["candidates"]},
+            "whole_step_ms": 1e3 * total,
+            "host": cpu,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -691,14 +746,16 @@ def run_ours(args, rank: int, world: int, dist):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_tiles = 1024  # ~10-30 s of single-core oracle work on the GPU machine's host
-        t_step, det = oracle_sample(scene, n_tiles)
-        cpu = {"value": det["full_candidates"] / t_step, "unit": UNIT, "cores": 1,
+        import oracle
+        threads = oracle.default_threads()
+        pieces, det = oracle_pieces(scene, 1, threads)
+        single = oracle_single_core_rate(scene, 64)
+        cpu = {"value": det["candidates"] / sum(pieces), "unit": UNIT, "cores": threads,
                "kind": "oracle",
-               "sample": "full binning + sort of the scene, forward+backward on %d random tiles "
-                         "(%d of %d candidate pairs) scaled to the whole step; %.1f s measured" % (
-                             n_tiles, det["sample_candidates"], det["full_candidates"],
-                             det["measured_s"])}
+               "sample": "one whole step of the scene (bin + sort single-threaded, forward + "
+                         "backward of every tile tile-parallel on %d threads): %.1f s" % (
+                             threads, sum(pieces)),
+               "host": cpu_description(), "single_core": single}
 
     if rank != 0:
         return

@@ -50,6 +50,7 @@
 // re-evaluated; after a chunk of 16 selected entries each pixel walks only
 // its own blended entries (independent trip counts per lane).
 #include <atomic>
+#include <mutex>
 
 #include "ss_device.cuh"
 #include "ss_internal.h"
@@ -688,7 +689,100 @@ constexpr int32_t kNoAllocMaxSplats = 1 << 21;  // 2,097,152 splats -> 16 MiB of
 
 static __device__ __align__(256) unsigned long long g_noalloc_accum[kNoAllocMaxSplats];
 
-static std::atomic<unsigned long long *> g_noalloc_ptr[64];  // device address of the array, per device
+// The array's device address belongs to one CUDA context: it is looked up
+// (cudaGetSymbolAddress, with the device current) on the first call in a
+// context and cached per device under the context's process-unique id, so
+// a call in another context of the same device -- a driver-API context the
+// caller made current, or the primary context re-created after
+// cudaDeviceReset -- looks it up again instead of using a stale address.
+struct NoAllocSlot {
+    unsigned long long ctx_id;   // 0: empty
+    unsigned long long *ptr;
+};
+static std::mutex g_noalloc_mu;
+static NoAllocSlot g_noalloc_slot[64];
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, found through the runtime
+// (the library links no driver library, so that it loads where no driver
+// is installed).
+using CtxGetCurrentFn = int (*)(void **);
+using CtxGetIdFn = int (*)(void *, unsigned long long *);
+
+static std::atomic<CtxGetCurrentFn> g_get_current{nullptr};
+static std::atomic<CtxGetIdFn> g_get_id{nullptr};
+
+// The current context's id in *id (0 if no context is current yet).  The
+// first call resolves the two driver functions.
+static ss_status current_context_id(unsigned long long *id) {
+    CtxGetCurrentFn fc = g_get_current.load(std::memory_order_acquire);
+    CtxGetIdFn fi = g_get_id.load(std::memory_order_acquire);
+    if (!fc || !fi) {
+        void *pc = nullptr, *pi = nullptr;
+        cudaDriverEntryPointQueryResult qc = cudaDriverEntryPointSymbolNotFound, qi = qc;
+        ss_status s = check_cuda(
+            cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &pc, 12000, cudaEnableDefault, &qc),
+            "ss_raster_bwd_noalloc: cudaGetDriverEntryPointByVersion(cuCtxGetCurrent)");
+        if (s != SS_OK) return s;
+        s = check_cuda(
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &pi, 12000, cudaEnableDefault, &qi),
+            "ss_raster_bwd_noalloc: cudaGetDriverEntryPointByVersion(cuCtxGetId)");
+        if (s != SS_OK) return s;
+        if (qc != cudaDriverEntryPointSuccess || qi != cudaDriverEntryPointSuccess || !pc || !pi)
+            return fail(SS_ERR_CUDA, "ss_raster_bwd_noalloc: the driver has no cuCtxGetCurrent / "
+                                     "cuCtxGetId");
+        fc = reinterpret_cast<CtxGetCurrentFn>(pc);
+        fi = reinterpret_cast<CtxGetIdFn>(pi);
+        g_get_current.store(fc, std::memory_order_release);
+        g_get_id.store(fi, std::memory_order_release);
+    }
+    void *ctx = nullptr;
+    if (fc(&ctx) != 0) return fail(SS_ERR_CUDA, "ss_raster_bwd_noalloc: cuCtxGetCurrent failed");
+    *id = 0;
+    if (ctx && fi(ctx, id) != 0)
+        return fail(SS_ERR_CUDA, "ss_raster_bwd_noalloc: cuCtxGetId failed");
+    return SS_OK;
+}
+
+// The array's address in the current context of device dev (cached; see
+// above).  While `stream` is being captured only a cached address is used:
+// the first call in a context is refused then, before any other CUDA call.
+static ss_status noalloc_scratch(int dev, cudaStream_t stream, unsigned long long **out) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    ss_status s = check_cuda(cudaStreamIsCapturing(stream, &cs),
+                             "ss_raster_bwd_noalloc: cudaStreamIsCapturing");
+    if (s != SS_OK) return s;
+    const bool capturing = cs != cudaStreamCaptureStatusNone;
+    if (capturing && !g_get_id.load(std::memory_order_acquire))
+        return fail(SS_ERR_UNSUPPORTED,
+                    "ss_raster_bwd_noalloc: first call while the stream is being captured; make "
+                    "one call on this device before capturing");
+    unsigned long long id = 0;
+    s = current_context_id(&id);
+    if (s != SS_OK) return s;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (id != 0 && g_noalloc_slot[dev].ctx_id == id) {
+            *out = g_noalloc_slot[dev].ptr;
+            return SS_OK;
+        }
+    }
+    if (capturing)
+        return fail(SS_ERR_UNSUPPORTED,
+                    "ss_raster_bwd_noalloc: first call in this context while the stream is being "
+                    "captured; make one call on this device before capturing");
+    void *ptr = nullptr;
+    s = check_cuda(cudaGetSymbolAddress(&ptr, g_noalloc_accum),
+                   "ss_raster_bwd_noalloc: cudaGetSymbolAddress");
+    if (s != SS_OK) return s;
+    s = current_context_id(&id);   // the lookup made the device's context current if it was not
+    if (s != SS_OK) return s;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        g_noalloc_slot[dev] = NoAllocSlot{id, static_cast<unsigned long long *>(ptr)};
+    }
+    *out = static_cast<unsigned long long *>(ptr);
+    return SS_OK;
+}
 
 }  // namespace ss
 
@@ -705,7 +799,10 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd_noalloc: image %dx%d outside 1..%d", W, H,
                     kMaxSide);
-    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION))
+    // SS_RECORDS_CLEARED is accepted and ignored: this call keeps no gradient
+    // records and always clears its own outputs first.
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION |
+                          SS_RECORDS_CLEARED))
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: unknown flag bits 0x%x", flags);
     if (flags & SS_DISTORTION)
         return fail(SS_ERR_UNSUPPORTED,
@@ -741,14 +838,10 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     if (s != SS_OK) return s;
     if (dev < 0 || dev >= 64)
         return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd_noalloc: device %d >= 64", dev);
-    if (accum && !g_noalloc_ptr[dev].load(std::memory_order_acquire)) {
-        // First call on this device (with this device current): look up the
-        // array's device address once.
-        void *ptr = nullptr;
-        s = check_cuda(cudaGetSymbolAddress(&ptr, g_noalloc_accum),
-                       "ss_raster_bwd_noalloc: cudaGetSymbolAddress");
+    unsigned long long *scratch = nullptr;
+    if (accum) {
+        s = noalloc_scratch(dev, (cudaStream_t)stream, &scratch);
         if (s != SS_OK) return s;
-        g_noalloc_ptr[dev].store(static_cast<unsigned long long *>(ptr), std::memory_order_release);
     }
 
     BwdParams p{};
@@ -769,7 +862,7 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     p.dconic = grads->dconic;
     p.dopacity = grads->dopacity;
     p.drgb = grads->drgb;
-    p.accum = accum ? g_noalloc_ptr[dev].load(std::memory_order_acquire) : nullptr;
+    p.accum = scratch;
     cudaStream_t st = (cudaStream_t)stream;
     s = ensure_bwd_smem();
     if (s != SS_OK) return s;

@@ -313,9 +313,15 @@ ss_status ss_raster_bwd(const void *records, int32_t n_splats, const uint32_t *v
  * until the process exits.
  *   - n_splats > 2,097,152 returns SS_ERR_UNSUPPORTED (use ss_raster_bwd).
  *   - SS_DISTORTION returns SS_ERR_UNSUPPORTED (use ss_raster_bwd).
- *   - The first call on a device, made with that device current, looks up
- *     the array's device address (cudaGetSymbolAddress); make that first
- *     call before any stream capture.
+ *   - SS_RECORDS_CLEARED is accepted and ignored (this call keeps no
+ *     gradient records; it always clears its outputs first).
+ *   - The first call in a CUDA context on a device, made with that device
+ *     current, looks up the array's device address (cudaGetSymbolAddress)
+ *     and caches it under the context's id; a call in another context
+ *     (another driver-API context, or the primary context re-created after
+ *     cudaDeviceReset) looks it up again.  Make that first call before any
+ *     stream capture: a first call on a capturing stream returns
+ *     SS_ERR_UNSUPPORTED without touching the capture.
  *   - All calls share the array.  Each call clears the part it uses, but
  *     calls that overlap on the GPU (other streams, other host threads) race
  *     on it: serialise them. */

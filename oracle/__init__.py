@@ -320,8 +320,26 @@ def _grads(n):
             "drgb": np.zeros((n, 3)), "accum": np.zeros(n), "ddepth": np.zeros(n)}
 
 
+def backward_sums(n: int, parts: int, slack: bool = True) -> list:
+    """Zeroed per-part accumulators for backward(..., into=...)."""
+    return [(_grads(n), _grads(n) if slack else None, np.zeros(n)) for _ in range(parts)]
+
+
+def add_backward_sums(sums: list) -> dict:
+    """backward()'s result from per-part accumulators: their sum in part order."""
+    gr, sl, aerr = (_grads(sums[0][2].size), _grads(sums[0][2].size) if sums[0][1] else None,
+                    np.zeros(sums[0][2].size))
+    for g2, s2, a2 in sums:
+        for k in _GRAD_KEYS:
+            gr[k] += g2[k]
+            if sl is not None:
+                sl[k] += s2[k]
+        aerr += a2
+    return {"grads": gr, "slack": sl, "accum_err": aerr}
+
+
 def backward(scene, vals, offs, tile_mask=None, params=None, bg=None, dL_dimage=None,
-             slack=True, dL_ddist=None, threads: int = 1):
+             slack=True, dL_ddist=None, threads: int = 1, into=None):
     """Per-splat gradients of L = sum dL/dimage * image (+ sum dL/ddist * dist
     when dL_ddist is given) from the masked tiles.
 
@@ -329,6 +347,9 @@ def backward(scene, vals, offs, tile_mask=None, params=None, bg=None, dL_dimage=
     part on its own thread, each into its own per-splat buffers, which are
     then added in part order (the oracle's per-tile contributions are
     additive; only the order of the double-precision sums differs).
+    into: per-part accumulators (backward_sums(n, threads, slack)) that the
+    parts add into instead; nothing is returned then (add_backward_sums
+    gives the result), so that several calls on disjoint tiles share them.
 
     Returns dict(grads=..., slack=... or None, accum_err=...)."""
     lib = load()
@@ -338,32 +359,30 @@ def backward(scene, vals, offs, tile_mask=None, params=None, bg=None, dL_dimage=
     keep.append(g)
     masks = [tile_mask] if threads <= 1 else tile_parts(scene.W, scene.H, offs, tile_mask,
                                                         threads)
+    sums = into if into is not None else backward_sums(scene.n, len(masks), slack)
+    if len(sums) < len(masks):
+        raise ValueError("%d accumulators for %d parts" % (len(sums), len(masks)))
 
-    def run(mask):
+    def run(j):
         mine = []
-        f = _frame(scene, vals, offs, mask, bg, mine, dL_ddist)
-        gr = _grads(scene.n)
-        sl = _grads(scene.n) if slack else None
-        aerr = np.zeros(scene.n)
+        f = _frame(scene, vals, offs, masks[j], bg, mine, dL_ddist)
+        gr, sl, aerr = sums[j]
         cg = _Grads(*[_p(gr[k]) for k in _GRAD_KEYS])
         cs = _Grads(*[_p(sl[k]) for k in _GRAD_KEYS]) if slack else None
         lib.orc_backward(ctypes.byref(s), ctypes.byref(f), _p(g), ctypes.byref(cg),
                          ctypes.byref(cs) if slack else None, _p(aerr))
-        return gr, sl, aerr
 
     if len(masks) == 1:
-        outs = [run(masks[0])]
+        run(0)
     else:
         with concurrent.futures.ThreadPoolExecutor(len(masks)) as ex:
-            outs = list(ex.map(run, masks))
-    gr, sl, aerr = outs[0]
-    for g2, s2, a2 in outs[1:]:
-        for k in _GRAD_KEYS:
-            gr[k] += g2[k]
-            if slack:
-                sl[k] += s2[k]
-        aerr += a2
-    return {"grads": gr, "slack": sl, "accum_err": aerr}
+            list(ex.map(run, range(len(masks))))
+    if into is not None:
+        return None
+    if len(sums) == 1:
+        gr, sl, aerr = sums[0]
+        return {"grads": gr, "slack": sl, "accum_err": aerr}
+    return add_backward_sums(sums[:len(masks)])
 
 
 def margins(a, b, c, dx, dy, o):

@@ -89,6 +89,10 @@ def test_reference_arm_prints_the_contract_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
     assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT and d["higher_is_better"] is True
     assert d["value"] > 0 and d["ms_per_step"] > 0
+    # the timed steps are one whole step, measured, not extrapolated
+    assert abs(d["whole_step_ms"] - d["ms_per_step"] * d["steps"]) <= 1e-6 * d["whole_step_ms"]
+    assert abs(d["value"] * d["whole_step_ms"] * 1e-3 - d["config"]["candidate_splat_px"]) <= \
+        1e-6 * d["config"]["candidate_splat_px"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["sample"]
     e = d["e2e"]
