@@ -433,9 +433,18 @@ int64_t orc_trace_pixel(const orc_splats_d *s, const uint32_t *list, int64_t len
 
 /* R17 by its definition: the double sum over pairs of blended splats.
  * err receives a bound on the error of a float32 evaluation by running
- * totals of depths taken relative to the first blended splat's: per blended
- * splat i, 16 u w_i (z'_i^2 A + 2 |z'_i| |D1'| + D2') over the totals A, D1',
- * D2' of the splats before it, plus |w_i E_i| (2 relT + mrel + 4 u (n + 2)). */
+ * totals of depths taken relative to the first blended splat's.  For the
+ * k-th blended splat i (k = 0, 1, ...) with the totals A, D1', D2' of the
+ * splats before it:
+ *   (16 + k) u w_i (z'_i^2 A + 2 |z'_i| |D1'| + D2') -- its term's roundings
+ *     and those the totals gathered: each is a float32 running sum of k
+ *     non-negative terms (depths are ascending, so z' >= 0), off by at
+ *     most k u of itself;
+ *   w_i E_i (2 relT + mrel_i + 4 u (n + 2)), E_i = sum over the other blended
+ *     splats j of w_j (z_i - z_j)^2 -- the weights' own errors (a pair's
+ *     product carries both weights' errors, so each weight's error is
+ *     weighed against its pairs with earlier and later splats alike) and
+ *     the rounding of the sum of the n terms into D. */
 static double pixel_dist(const orc_splats_d *s, const uint32_t *list, const pix_run *r,
                          double *err)
 {
@@ -451,10 +460,16 @@ static double pixel_dist(const orc_splats_d *s, const uint32_t *list, const pix_
         const double z0 = r->n ? s->depth[list[r->rec[0].pos]] : 0.0;
         for (int64_t i = 0; i < r->n; ++i) {
             const double w = r->rec[i].alpha * r->rec[i].T;
-            const double z = s->depth[list[r->rec[i].pos]] - z0;
-            const double term = z * z * A - 2.0 * z * D1 + D2;
+            const double zi = s->depth[list[r->rec[i].pos]];
+            const double z = zi - z0;
+            double E = 0.0;
+            for (int64_t j = 0; j < r->n; ++j) {
+                const double dz = zi - s->depth[list[r->rec[j].pos]];
+                E += r->rec[j].alpha * r->rec[j].T * dz * dz;
+            }
             const double relw = 2.0 * r->relT + r->rec[i].mrel + 4.0 * U32 * (double)(r->n + 2);
-            e += 16.0 * U32 * w * (z * z * A + 2.0 * fabs(z) * fabs(D1) + D2) + fabs(w * term) * relw;
+            e += (16.0 + (double)i) * U32 * w * (z * z * A + 2.0 * fabs(z) * fabs(D1) + D2) +
+                 w * E * relw;
             A += w;
             D1 += w * z;
             D2 += w * z * z;

@@ -205,11 +205,12 @@ def _chain_scene(seed, n=2500, W=32, H=32):
     return synth.make_scene(wl, seed=seed)
 
 
-def emulate_forward(sc, tl, eps_ex2=0.0, thr_pick=1, dist=False):
+def emulate_forward(sc, tl, eps_ex2=0.0, thr_pick=1, dist=False, tiles=None):
     """The rasterizer's forward per pixel in float32 (tile by tile, pixels as
     vectors): blend decisions, T, last contributor, median depth, the
     blended steps' alpha and T before, and (dist) the distortion by the
-    running totals relative to the first blended depth."""
+    running totals relative to the first blended depth.  tiles: only these
+    tile ids (default all)."""
     W, H = sc.W, sc.H
     tx, ty = oracle.tiles_xy(W, H)
     a, b, c = (np.ascontiguousarray(sc.conic[:, k]) for k in range(3))
@@ -218,7 +219,7 @@ def emulate_forward(sc, tl, eps_ex2=0.0, thr_pick=1, dist=False):
     out = {"T": np.ones((H, W), F), "last": np.zeros((H, W), np.int64),
            "median": np.zeros((H, W), F), "dist": np.zeros((H, W), F), "steps": {}}
     offs = tl["offs"].astype(np.int64)
-    for t in range(tx * ty):
+    for t in (range(tx * ty) if tiles is None else tiles):
         x0, y0 = 16 * (t % tx), 16 * (t // tx)
         ys, xs = np.mgrid[y0:min(y0 + 16, H), x0:min(x0 + 16, W)]
         xs, ys = xs.ravel(), ys.ravel()
@@ -382,22 +383,32 @@ def test_accumulated_weight_error_inside_accum_err(chains):
 
 def test_distortion_error_inside_dist_err():
     """The float32 distortion by running totals relative to the first blended
-    depth (depths over [1, 50]) differs from the oracle's double sum over
-    pairs by at most the oracle's dist_err.  This bound is the loosest of
-    the model (it sums the magnitudes of the totals' terms): within 70x of
-    the largest error seen."""
-    sc = _chain_scene(8, n=1500)
+    depth differs from the oracle's double sum over pairs by at most the
+    oracle's dist_err, on the tiles of workload 3 (depths over [1, 50], up
+    to ~100 blends a pixel) where the totals' accumulated rounding is
+    largest; the bound is within 10x of the largest error seen there."""
+    sc = synth.make_scene(3)
     tl = oracle.tile_lists(sc)
-    ofw = oracle.forward(sc, tl["vals"], tl["offs"])
+    tx, ty = oracle.tiles_xy(sc.W, sc.H)
+    tiles = sorted({(py // 16 + dy) * tx + px // 16 + dx
+                    for px, py in ((678, 467), (275, 227), (677, 466), (233, 123))
+                    for dy in (-1, 0, 1) for dx in (-1, 0, 1)})
+    mask = np.zeros(tx * ty, np.uint8)
+    mask[tiles] = 1
+    ofw = oracle.forward(sc, tl["vals"], tl["offs"], tile_mask=mask, alt_capacity=1 << 20)
+    flagged = np.zeros(sc.W * sc.H, bool)
+    flagged[ofw["alts"]["pixel"]] = True
+    flagged = flagged.reshape(sc.H, sc.W)
+    pix = np.repeat(np.repeat(mask.reshape(ty, tx), 16, 0), 16, 1)[:sc.H, :sc.W].astype(bool)
     worst = 0.0
     for eps, pick in ((0.0, 1), (EX2_DOC, 2), (-EX2_DOC, 0)):
-        emu = emulate_forward(sc, tl, eps, pick, dist=True)
-        same = emu["last"] == ofw["last"]
+        emu = emulate_forward(sc, tl, eps, pick, dist=True, tiles=tiles)
+        same = pix & (emu["last"] == ofw["last"]) & ~flagged
         err = np.abs(emu["dist"].astype(D) - ofw["dist"])
-        assert np.all(err[same] <= ofw["dist_err"][same]), np.max(err / ofw["dist_err"])
+        assert np.all(err[same] <= ofw["dist_err"][same]), np.max(err[same] / ofw["dist_err"][same])
         used = same & (ofw["dist_err"] > 0)
         worst = max(worst, float(np.max(err[used] / ofw["dist_err"][used])))
-    assert worst >= 0.015, worst
+    assert worst >= 0.1, worst
 
 
 # ---------------------------------------------------------------- slack
@@ -476,7 +487,7 @@ MUTATIONS = [
      "accum_err[i] += 0.125 * (c1[NF * k + F_W] * relw + 1.0 / 4294967296.0);"),
     ("accum_err x100", "accum_err[i] += c1[NF * k + F_W] * relw + 1.0 / 4294967296.0;",
      "accum_err[i] += 100.0 * (c1[NF * k + F_W] * relw + 1.0 / 4294967296.0);"),
-    ("dist_err / 64", "        *err = e;", "        *err = e / 64.0;"),
+    ("dist_err / 16", "        *err = e;", "        *err = e / 16.0;"),
     ("slack halved", "d[fld] = byp2[NF * q + fld] - byp1[NF * q + fld];",
      "d[fld] = 0.5 * (byp2[NF * q + fld] - byp1[NF * q + fld]);"),
 ]
