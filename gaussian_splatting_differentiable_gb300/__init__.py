@@ -159,20 +159,29 @@ def ss_sort_status(workspace, stream=None) -> int:
     return int(_L.ss_sort_status(_ptr(workspace), _stream(stream)))
 
 
-def ss_raster_fwd(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int, H: int, bg,
-                  flags: int, image, T_final, last_contrib, median_depth, blend_masks,
-                  max_weight=None, blend_count=None, distortion=None, dist_totals=None,
-                  stream=None, bwd_workspace=None) -> None:
-    """bwd_workspace: the workspace of the following ss_raster_bwd, whose
-    gradient records the forward then clears (pass SS_RECORDS_CLEARED to
-    that call; nothing may write the workspace in between)."""
+def ss_raster_fwd(splats: Splats, vals, tile_offsets, W: int, H: int, bg, flags: int, image,
+                  T_final, last_contrib, median_depth=None, stream=None) -> None:
+    """The forward from the splats themselves (no records, no blend masks)."""
+    s = splats.c()
+    _check(_L.ss_raster_fwd(ctypes.byref(s), _ptr(vals), _ptr(tile_offsets), W, H,
+                            _f32_host3(bg), flags, _ptr(image), _ptr(T_final), _ptr(last_contrib),
+                            _ptr(median_depth), _stream(stream)), "ss_raster_fwd")
+
+
+def ss_raster_fwd_records(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int,
+                          H: int, bg, flags: int, image, T_final, last_contrib, median_depth,
+                          blend_masks, max_weight=None, blend_count=None, distortion=None,
+                          dist_totals=None, stream=None, bwd_workspace=None) -> None:
+    """bwd_workspace: the workspace of the following ss_raster_bwd_records,
+    whose gradient records the forward then clears (pass SS_RECORDS_CLEARED
+    to that call; nothing may write the workspace in between)."""
     nbytes = 0 if bwd_workspace is None else bwd_workspace.numel() * bwd_workspace.element_size()
-    _check(_L.ss_raster_fwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), n_pairs, W,
-                            H, _f32_host3(bg), flags, _ptr(image), _ptr(T_final),
-                            _ptr(last_contrib), _ptr(median_depth), _ptr(blend_masks),
-                            _ptr(max_weight), _ptr(blend_count), _ptr(distortion),
-                            _ptr(dist_totals), _ptr(bwd_workspace), nbytes, _stream(stream)),
-           "ss_raster_fwd")
+    _check(_L.ss_raster_fwd_records(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets),
+                                    n_pairs, W, H, _f32_host3(bg), flags, _ptr(image),
+                                    _ptr(T_final), _ptr(last_contrib), _ptr(median_depth),
+                                    _ptr(blend_masks), _ptr(max_weight), _ptr(blend_count),
+                                    _ptr(distortion), _ptr(dist_totals), _ptr(bwd_workspace),
+                                    nbytes, _stream(stream)), "ss_raster_fwd_records")
 
 
 def _grads_struct(grads: dict) -> SsGrads:
@@ -180,23 +189,40 @@ def _grads_struct(grads: dict) -> SsGrads:
                    _ptr(grads["drgb"]), _ptr(grads.get("ddepth")))
 
 
-def ss_raster_bwd(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int, H: int, bg,
-                  flags: int, T_final, last_contrib, blend_masks, dL_dimage, grads: dict,
-                  accum_weight, workspace, stream=None, dist_totals=None,
-                  dL_ddist=None) -> None:
+def ss_raster_bwd(splats: Splats, vals, tile_offsets, W: int, H: int, bg, flags: int, T_final,
+                  last_contrib, dL_dimage, grads: dict, accum_weight, workspace,
+                  stream=None) -> None:
+    """The backward from the splats themselves: records and blend decisions
+    rebuilt in the workspace (ss_workspace_bytes(n, pairs, W, H) bytes)."""
+    s = splats.c()
     g = _grads_struct(grads)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(_L.ss_raster_bwd(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets), n_pairs, W,
-                            H, _f32_host3(bg), flags, _ptr(T_final), _ptr(last_contrib),
-                            _ptr(blend_masks), _ptr(dL_dimage), _ptr(dist_totals),
-                            _ptr(dL_ddist), ctypes.byref(g), _ptr(accum_weight),
+    _check(_L.ss_raster_bwd(ctypes.byref(s), _ptr(vals), _ptr(tile_offsets), W, H,
+                            _f32_host3(bg), flags, _ptr(T_final), _ptr(last_contrib),
+                            _ptr(dL_dimage), ctypes.byref(g), _ptr(accum_weight),
                             _ptr(workspace), nbytes, _stream(stream)), "ss_raster_bwd")
+
+
+def ss_raster_bwd_records(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int,
+                          H: int, bg, flags: int, T_final, last_contrib, blend_masks, dL_dimage,
+                          grads: dict, accum_weight, workspace, stream=None, dist_totals=None,
+                          dL_ddist=None) -> None:
+    """blend_masks may be None: the decisions are then re-evaluated into the
+    workspace."""
+    g = _grads_struct(grads)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_L.ss_raster_bwd_records(_ptr(records), n_splats, _ptr(vals), _ptr(tile_offsets),
+                                    n_pairs, W, H, _f32_host3(bg), flags, _ptr(T_final),
+                                    _ptr(last_contrib), _ptr(blend_masks), _ptr(dL_dimage),
+                                    _ptr(dist_totals), _ptr(dL_ddist), ctypes.byref(g),
+                                    _ptr(accum_weight), _ptr(workspace), nbytes,
+                                    _stream(stream)), "ss_raster_bwd_records")
 
 
 def ss_raster_bwd_noalloc(records, n_splats: int, vals, tile_offsets, n_pairs: int, W: int,
                           H: int, bg, flags: int, T_final, last_contrib, blend_masks, dL_dimage,
                           grads: dict, accum_weight, stream=None) -> None:
-    """ss_raster_bwd for callers that cannot allocate: no workspace argument;
+    """ss_raster_bwd_records for callers that cannot allocate: no workspace argument;
     the weight scratch is a fixed array inside the library (at most 2,097,152
     splats; concurrent calls race on it)."""
     g = _grads_struct(grads)
@@ -422,20 +448,21 @@ class Rasterizer:
         next backward() skips that pass; bin_and_sort() resets that, but a
         sort called directly on this workspace between forward() and
         backward() must be followed by forward() again."""
-        ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs, self.W,
-                      self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
-                      self.median_depth, self.blend_masks, self.max_weight, self.blend_count,
-                      self.distortion, self.dist_totals, stream, bwd_workspace=self.workspace)
+        ss_raster_fwd_records(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs,
+                              self.W, self.H, self.bg, self.flags, self.image, self.T_final,
+                              self.last_contrib, self.median_depth, self.blend_masks,
+                              self.max_weight, self.blend_count, self.distortion,
+                              self.dist_totals, stream, bwd_workspace=self.workspace)
         self._records_cleared = True
 
     def backward(self, splats, dL_dimage: torch.Tensor, stream=None, dL_ddist=None) -> None:
         """Gradients; uses the records written by the last bin_and_sort.
         dL_ddist: [H, W] upstream gradient of the distortion (SS_DISTORTION)."""
         flags = self.flags | (SS_RECORDS_CLEARED if self._records_cleared else 0)
-        ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs, self.W,
-                      self.H, self.bg, flags, self.T_final, self.last_contrib,
-                      self.blend_masks, dL_dimage, self.grads, self.accum_weight, self.workspace,
-                      stream, self.dist_totals, dL_ddist)
+        ss_raster_bwd_records(self.records, self.n, self.vals, self.tile_offsets, self.n_pairs,
+                              self.W, self.H, self.bg, flags, self.T_final, self.last_contrib,
+                              self.blend_masks, dL_dimage, self.grads, self.accum_weight,
+                              self.workspace, stream, self.dist_totals, dL_ddist)
         self._records_cleared = False   # the backward's sums are in them now
 
     def step(self, splats: Splats, dL_dimage: torch.Tensor, stream=None, dL_ddist=None) -> int:
@@ -455,15 +482,16 @@ class Rasterizer:
                      self.records, stream)
         ss_sort_pairs_dev(self.keys, self.vals, self.counters, self.capacity, self.W, self.H,
                           self.tile_offsets, self.workspace, stream)
-        ss_raster_fwd(self.records, self.n, self.vals, self.tile_offsets, self.capacity, self.W,
-                      self.H, self.bg, self.flags, self.image, self.T_final, self.last_contrib,
-                      self.median_depth, self.blend_masks, self.max_weight, self.blend_count,
-                      self.distortion, self.dist_totals, stream, bwd_workspace=self.workspace)
-        ss_raster_bwd(self.records, self.n, self.vals, self.tile_offsets, self.capacity, self.W,
-                      self.H, self.bg, self.flags | SS_RECORDS_CLEARED, self.T_final,
-                      self.last_contrib,
-                      self.blend_masks, dL_dimage, self.grads, self.accum_weight, self.workspace,
-                      stream, self.dist_totals, dL_ddist)
+        ss_raster_fwd_records(self.records, self.n, self.vals, self.tile_offsets, self.capacity,
+                              self.W, self.H, self.bg, self.flags, self.image, self.T_final,
+                              self.last_contrib, self.median_depth, self.blend_masks,
+                              self.max_weight, self.blend_count, self.distortion,
+                              self.dist_totals, stream, bwd_workspace=self.workspace)
+        ss_raster_bwd_records(self.records, self.n, self.vals, self.tile_offsets, self.capacity,
+                              self.W, self.H, self.bg, self.flags | SS_RECORDS_CLEARED,
+                              self.T_final, self.last_contrib, self.blend_masks, dL_dimage,
+                              self.grads, self.accum_weight, self.workspace, stream,
+                              self.dist_totals, dL_ddist)
 
     def check(self, stream=None) -> None:
         """Raise if the last sort reported a device-side problem (capacity

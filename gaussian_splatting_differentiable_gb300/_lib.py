@@ -65,10 +65,14 @@ PROTOTYPES = {
     "ss_sort_pairs": (ctypes.c_int, [P, P, I64, I32, I32, P, P, SZ, P]),
     "ss_sort_pairs_dev": (ctypes.c_int, [P, P, P, I64, I32, I32, P, P, SZ, P]),
     "ss_sort_status": (ctypes.c_int, [P, P]),
-    "ss_raster_fwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P, P, P,
-                                     P, P, P, SZ, P]),
-    "ss_raster_bwd": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P, P,
+    "ss_raster_fwd": (ctypes.c_int, [ctypes.POINTER(SsSplats), P, P, I32, I32, P, U32, P, P, P,
+                                     P, P]),
+    "ss_raster_fwd_records": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P,
+                                             P, P, P, P, P, SZ, P]),
+    "ss_raster_bwd": (ctypes.c_int, [ctypes.POINTER(SsSplats), P, P, I32, I32, P, U32, P, P, P,
                                      ctypes.POINTER(SsGrads), P, P, SZ, P]),
+    "ss_raster_bwd_records": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P, P,
+                                             P, ctypes.POINTER(SsGrads), P, P, SZ, P]),
     "ss_raster_bwd_noalloc": (ctypes.c_int, [P, I32, P, P, I64, I32, I32, P, U32, P, P, P, P,
                                              ctypes.POINTER(SsGrads), P, P]),
     "ss_profile_enable": (None, [I32]),

@@ -66,7 +66,12 @@ WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H) {
     L.sort_end = off;
     L.accum = 256;  // after the status word; the sort's regions are dead by then
     L.bwd_end = align256(L.accum + size_t(n_splats) * 48);  // 48-byte gradient record per splat
-    L.total = L.sort_end > L.bwd_end ? L.sort_end : L.bwd_end;
+    // The backward without the forward's blend masks (or without records)
+    // builds them here, after its gradient records.
+    L.recs = L.bwd_end;
+    L.masks = align256(L.recs + size_t(n_splats) * 64);
+    L.masks_end = align256(L.masks + size_t(n_pairs) * 32);
+    L.total = L.sort_end > L.masks_end ? L.sort_end : L.masks_end;
     return L;
 }
 
@@ -85,7 +90,7 @@ using namespace ss;
 
 extern "C" {
 
-int32_t ss_abi_version(void) { return 7; }
+int32_t ss_abi_version(void) { return 8; }
 
 size_t ss_record_bytes(int32_t n_splats) { return n_splats < 0 ? 0 : size_t(n_splats) * 64; }
 

@@ -566,58 +566,221 @@ __global__ void k_accum_final(const unsigned long long *acc, float *out, int64_t
         out[i] = float(double(acc[i]) * (1.0 / 4294967296.0));
 }
 
+// Records of the splats from the SoA inputs: what the binning writes, bit
+// for bit (record_of), for the backward that takes the splats themselves.
+__global__ void k_make_records(SplatPtrs s, int32_t tiles_x, int32_t tiles_y, SplatRecord *out) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < s.n; i += stride) {
+        const SplatRecord r = record_of(s, uint32_t(i), tiles_x, tiles_y);
+        float4 *dst = reinterpret_cast<float4 *>(out + i);
+        dst[0] = *reinterpret_cast<const float4 *>(&r.geo);
+        dst[1] = *reinterpret_cast<const float4 *>(&r.geo2);
+        dst[2] = *reinterpret_cast<const float4 *>(&r.col);
+        dst[3] = *reinterpret_cast<const float4 *>(&r.box);
+    }
+}
+
+struct MaskParams {
+    const SplatRecord *recs;
+    int32_t n;
+    const uint32_t *vals;
+    const uint32_t *offs;
+    const uint32_t *last;
+    int32_t W, H, tiles_x, tiles;
+    uint32_t *masks;   // [8][stride]
+    int64_t stride;
+    uint32_t *status;  // the workspace's status word
+};
+
+// The forward's blend decisions, re-evaluated from the staged records for a
+// backward given none: a pixel blended list position j of its tile iff
+// j < last_contrib and e2 >= thr (the forward blends every splat it does
+// not skip until it stops, and last_contrib is its last blend), with e2 the
+// same eval_e2 of the same record bits.  One CTA per tile; each warp takes
+// its 8x4 block, box-culls a batch of 256 staged records and evaluates the
+// rest, and writes the masks the backward reads, masks[warp][position].
+// A list longer than the mask rows (offsets[tiles] > stride) is recorded in
+// the status word and its masks are not written past the rows.
+__global__ void __launch_bounds__(256) k_blend_masks(MaskParams p) {
+    __shared__ SplatGeo s_geo[256];
+    __shared__ float2 s_ct[256];    // (C, thr)
+    __shared__ SplatBox s_box[256];
+    __shared__ uint32_t s_wmax[8];
+    const int tile = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tx = tile % p.tiles_x, ty = tile / p.tiles_x;
+    const int bx = tx * kTile + ((warp & 1) << 3), by = ty * kTile + ((warp >> 1) << 2);
+    const int x = bx + (lane & 7), y = by + (lane >> 3);
+    const bool inside = x < p.W && y < p.H;
+    const float px = float(x) + 0.5f, py = float(y) + 0.5f;
+    const float wx0 = float(bx) + 0.5f, wx1 = wx0 + 7.0f;
+    const float wy0 = float(by) + 0.5f, wy1 = wy0 + 3.0f;
+    const uint32_t start = p.offs[tile], len = p.offs[tile + 1] - start;
+    if (tile == 0 && tid == 0 && int64_t(p.offs[p.tiles]) > p.stride)
+        atomicOr(p.status, kDevErrCapacity);
+    const uint32_t n_p = inside ? min(p.last[size_t(y) * p.W + x], len) : 0u;
+    const uint32_t wmax = __reduce_max_sync(0xffffffffu, n_p);
+    if (lane == 0) s_wmax[warp] = wmax;
+    __syncthreads();
+    uint32_t bmax = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) bmax = max(bmax, s_wmax[w]);
+    for (uint32_t base = 0; base < bmax; base += 256) {
+        const int nb = int(min(256u, bmax - base));
+        __syncthreads();   // the previous batch is done everywhere
+        if (tid < nb) {
+            const uint32_t idx = p.vals[start + base + tid];
+            const SplatRecord r = idx < uint32_t(p.n) ? p.recs[idx] : invisible_record();
+            s_geo[tid] = r.geo;
+            s_ct[tid] = make_float2(r.geo2.C, r.geo2.thr);
+            s_box[tid] = r.box;
+        }
+        __syncthreads();
+        if (base >= wmax) continue;   // warp-uniform: no pixel of this block reaches the batch
+        for (int q = 0; q < 8 && q * 32 < nb; ++q) {
+            const int j = q * 32 + lane;
+            bool hit = false;
+            if (j < nb && base + uint32_t(j) < wmax) {
+                const SplatBox b = s_box[j];
+                hit = b.x0 <= wx1 && b.x1 >= wx0 && b.y0 <= wy1 && b.y1 >= wy0;
+            }
+            uint32_t m = __ballot_sync(0xffffffffu, hit), mine = 0;
+            while (m) {
+                const int k = __ffs(m) - 1;
+                m &= m - 1;
+                const int jj = q * 32 + k;
+                float dx, dy;
+                const float e2 = eval_e2(s_geo[jj], s_ct[jj].x, px, py, dx, dy);
+                const uint32_t bm = __ballot_sync(0xffffffffu,
+                                                  base + uint32_t(jj) < n_p && e2 >= s_ct[jj].y);
+                if (lane == k) mine = bm;
+            }
+            if (j < nb) {
+                const int64_t pos = int64_t(start) + base + j;
+                if (pos < p.stride) p.masks[size_t(warp) * size_t(p.stride) + size_t(pos)] = mine;
+            }
+        }
+    }
+}
+
+// The gradient launches shared by both backward entry points: clear the
+// gradient records (unless the forward did), the rasterizer, the
+// conversion to the caller's arrays.
+static ss_status launch_bwd(const BwdParams &p, uint32_t flags, float *accum_weight,
+                            cudaStream_t st, const char *name) {
+    const bool accum = flags & SS_ACCUM_WEIGHT, dist = flags & SS_DISTORTION;
+    ss_status es = ensure_bwd_smem();
+    if (es != SS_OK) return es;
+    int dev = 0, sms = 0;
+    es = current_device(&dev, &sms, name);
+    if (es != SS_OK) return es;
+    const int64_t want = (int64_t(p.n) + 255) / 256;
+    const int zgrid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+    if (!(flags & SS_RECORDS_CLEARED))   // else ss_raster_fwd_records cleared them
+        SS_LAUNCH("k_grad_zero", st,
+                  k_grad_zero<<<zgrid, 256, 0, st>>>(reinterpret_cast<float4 *>(p.scratch),
+                                                     3 * int64_t(p.n)));
+    const int grid = tiles_x(p.W) * tiles_y(p.H);
+    if (accum && dist)
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, true, true><<<grid, 256, kBwdDynSmem, st>>>(p)));
+    else if (dist)
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, true, true><<<grid, 256, kBwdDynSmem, st>>>(p)));
+    else if (accum)
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, true, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
+    else
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, true, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
+    SS_LAUNCH("k_grad_final", st,
+              k_grad_final<<<zgrid, 256, 0, st>>>(p, p.n, accum ? accum_weight : nullptr));
+    return check_launch(name);
+}
+
+// The blend masks of a backward given none (k_blend_masks) into rows of
+// `stride` entries at `masks`.
+static ss_status launch_masks(const SplatRecord *recs, int32_t n, const uint32_t *vals,
+                              const uint32_t *offs, const uint32_t *last, int32_t W, int32_t H,
+                              uint32_t *masks, int64_t stride, void *workspace, cudaStream_t st,
+                              const char *name) {
+    MaskParams m{};
+    m.recs = recs;
+    m.n = n;
+    m.vals = vals;
+    m.offs = offs;
+    m.last = last;
+    m.W = W;
+    m.H = H;
+    m.tiles_x = tiles_x(W);
+    m.tiles = tiles_x(W) * tiles_y(H);
+    m.masks = masks;
+    m.stride = stride;
+    m.status = static_cast<uint32_t *>(workspace);
+    SS_LAUNCH("k_blend_masks", st, k_blend_masks<<<m.tiles, 256, 0, st>>>(m));
+    return check_launch(name);
+}
+
 }  // namespace ss
 
 using namespace ss;
 
-extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
-                                   const uint32_t *vals,
-                                   const uint32_t *tile_offsets, int64_t n_pairs, int32_t W,
-                                   int32_t H, const float *bg, uint32_t flags, const float *T_final,
-                                   const uint32_t *last_contrib, const uint32_t *blend_masks,
-                                   const float *dL_dimage, const float *dist_totals,
-                                   const float *dL_ddist,
-                                   const ss_grads *grads, float *accum_weight, void *workspace,
-                                   size_t workspace_bytes, ss_stream_t stream) {
+extern "C" ss_status ss_raster_bwd_records(const void *records, int32_t n_splats,
+                                           const uint32_t *vals, const uint32_t *tile_offsets,
+                                           int64_t n_pairs, int32_t W, int32_t H, const float *bg,
+                                           uint32_t flags, const float *T_final,
+                                           const uint32_t *last_contrib,
+                                           const uint32_t *blend_masks, const float *dL_dimage,
+                                           const float *dist_totals, const float *dL_ddist,
+                                           const ss_grads *grads, float *accum_weight,
+                                           void *workspace, size_t workspace_bytes,
+                                           ss_stream_t stream) {
     clear_error();
+    const char *name = "ss_raster_bwd_records";
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
-        return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd: image %dx%d outside 1..%d", W, H, kMaxSide);
+        return fail(SS_ERR_UNSUPPORTED, "%s: image %dx%d outside 1..%d", name, W, H, kMaxSide);
     if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION |
                           SS_RECORDS_CLEARED))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: unknown flag bits 0x%x", flags);
+        return fail(SS_ERR_INVALID_ARG, "%s: unknown flag bits 0x%x", name, flags);
     const bool dist = flags & SS_DISTORTION;
     if (dist && (!dist_totals || !dL_ddist))
-        return fail(SS_ERR_INVALID_ARG,
-                    "ss_raster_bwd: SS_DISTORTION set but dist_totals / dL_ddist NULL");
+        return fail(SS_ERR_INVALID_ARG, "%s: SS_DISTORTION set but dist_totals / dL_ddist NULL",
+                    name);
     if (dist && (reinterpret_cast<uintptr_t>(dist_totals) & 15))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: dist_totals not 16-byte aligned");
+        return fail(SS_ERR_INVALID_ARG, "%s: dist_totals not 16-byte aligned", name);
     const int32_t n = n_splats;
-    if (n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: n < 0");
-    if (n > 0 && !records) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: records is NULL");
+    if (n < 0) return fail(SS_ERR_INVALID_ARG, "%s: n < 0", name);
+    if (n > 0 && !records) return fail(SS_ERR_INVALID_ARG, "%s: records is NULL", name);
     if (reinterpret_cast<uintptr_t>(records) & 15)
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: records not 16-byte aligned");
-    if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: vals/offsets NULL");
+        return fail(SS_ERR_INVALID_ARG, "%s: records not 16-byte aligned", name);
+    if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "%s: vals/offsets NULL", name);
     if (!T_final || !last_contrib || !dL_dimage)
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: T_final/last_contrib/dL_dimage NULL");
+        return fail(SS_ERR_INVALID_ARG, "%s: T_final/last_contrib/dL_dimage NULL", name);
     if (n_pairs < 0 || n_pairs > int64_t(0xffffffffu))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: n_pairs outside 0..2^32-1");
-    if (n_pairs > 0 && !blend_masks)
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: blend_masks is NULL");
+        return fail(SS_ERR_INVALID_ARG, "%s: n_pairs outside 0..2^32-1", name);
     if (!grads || (n > 0 && (!grads->dmean2d || !grads->dconic || !grads->dopacity || !grads->drgb)))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: a gradient array is NULL");
+        return fail(SS_ERR_INVALID_ARG, "%s: a gradient array is NULL", name);
     if (dist && n > 0 && !grads->ddepth)
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: SS_DISTORTION set but grads->ddepth NULL");
+        return fail(SS_ERR_INVALID_ARG, "%s: SS_DISTORTION set but grads->ddepth NULL", name);
     const bool accum = flags & SS_ACCUM_WEIGHT;
     if (accum && n > 0 && !accum_weight)
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: SS_ACCUM_WEIGHT set but accum_weight NULL");
-    const WsLayout L = ws_layout(n, 0, W, H);
+        return fail(SS_ERR_INVALID_ARG, "%s: SS_ACCUM_WEIGHT set but accum_weight NULL", name);
+    const bool own_masks = !blend_masks && n_pairs > 0;
+    const WsLayout L = ws_layout(n, own_masks ? n_pairs : 0, W, H);
     if (n > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: workspace NULL or not 256-byte aligned");
-    if (n > 0 && workspace_bytes < L.bwd_end)
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd: workspace %zu bytes < %zu needed",
-                    workspace_bytes, L.bwd_end);
+        return fail(SS_ERR_INVALID_ARG, "%s: workspace NULL or not 256-byte aligned", name);
+    const size_t need = own_masks ? L.masks_end : L.bwd_end;
+    if (n > 0 && workspace_bytes < need)
+        return fail(SS_ERR_INVALID_ARG, "%s: workspace %zu bytes < %zu needed%s", name,
+                    workspace_bytes, need, own_masks ? " (blend masks built here)" : "");
     if (n == 0) return SS_OK;
 
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    if (own_masks) {
+        const ss_status ms = launch_masks(static_cast<const SplatRecord *>(records), n, vals,
+                                          tile_offsets, last_contrib, W, H,
+                                          reinterpret_cast<uint32_t *>(ws + L.masks), n_pairs,
+                                          workspace, st, name);
+        if (ms != SS_OK) return ms;
+        blend_masks = reinterpret_cast<const uint32_t *>(ws + L.masks);
+    }
     BwdParams p{};
     p.recs = static_cast<const SplatRecord *>(records);
     p.n = n;
@@ -640,31 +803,98 @@ extern "C" ss_status ss_raster_bwd(const void *records, int32_t n_splats,
     p.dist_totals = reinterpret_cast<const float4 *>(dist_totals);
     p.dL_ddist = dL_ddist;
     p.accum = nullptr;
-    p.scratch = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + L.accum);
+    p.scratch = reinterpret_cast<float *>(ws + L.accum);
+    return launch_bwd(p, flags, accum_weight, st, name);
+}
+
+extern "C" ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals,
+                                   const uint32_t *tile_offsets, int32_t W, int32_t H,
+                                   const float *bg, uint32_t flags, const float *T_final,
+                                   const uint32_t *last_contrib, const float *dL_dimage,
+                                   const ss_grads *grads, float *accum_weight, void *workspace,
+                                   size_t workspace_bytes, ss_stream_t stream) {
+    clear_error();
+    const char *name = "ss_raster_bwd";
+    if (!splats) return fail(SS_ERR_INVALID_ARG, "%s: splats is NULL", name);
+    if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
+        return fail(SS_ERR_UNSUPPORTED, "%s: image %dx%d outside 1..%d", name, W, H, kMaxSide);
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION |
+                          SS_RECORDS_CLEARED))
+        return fail(SS_ERR_INVALID_ARG, "%s: unknown flag bits 0x%x", name, flags);
+    if (flags & SS_DISTORTION)
+        return fail(SS_ERR_UNSUPPORTED,
+                    "%s: the distortion's gradient needs its totals: use ss_raster_bwd_records",
+                    name);
+    if (flags & SS_RECORDS_CLEARED)
+        return fail(SS_ERR_INVALID_ARG,
+                    "%s: SS_RECORDS_CLEARED belongs to ss_raster_fwd_records' bwd_workspace", name);
+    const int32_t n = splats->n;
+    if (n < 0) return fail(SS_ERR_INVALID_ARG, "%s: n < 0", name);
+    if (n > 0 && (!splats->mean2d || !splats->conic || !splats->opacity || !splats->rgb ||
+                  !splats->depth))
+        return fail(SS_ERR_INVALID_ARG, "%s: a splat array is NULL", name);
+    if (n > 0 && (reinterpret_cast<uintptr_t>(splats->mean2d) & 7))
+        return fail(SS_ERR_INVALID_ARG, "%s: mean2d not 8-byte aligned", name);
+    if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "%s: vals/offsets NULL", name);
+    if (!T_final || !last_contrib || !dL_dimage)
+        return fail(SS_ERR_INVALID_ARG, "%s: T_final/last_contrib/dL_dimage NULL", name);
+    if (!grads || (n > 0 && (!grads->dmean2d || !grads->dconic || !grads->dopacity || !grads->drgb)))
+        return fail(SS_ERR_INVALID_ARG, "%s: a gradient array is NULL", name);
+    const bool accum = flags & SS_ACCUM_WEIGHT;
+    if (accum && n > 0 && !accum_weight)
+        return fail(SS_ERR_INVALID_ARG, "%s: SS_ACCUM_WEIGHT set but accum_weight NULL", name);
+    if (n == 0) return SS_OK;
+    const WsLayout L = ws_layout(n, 0, W, H);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return fail(SS_ERR_INVALID_ARG, "%s: workspace NULL or not 256-byte aligned", name);
+    if (workspace_bytes < L.masks + 32)
+        return fail(SS_ERR_INVALID_ARG, "%s: workspace %zu bytes < %zu + 32 per pair needed", name,
+                    workspace_bytes, L.masks);
+    // Mask rows as long as the workspace allows; the list length is only on
+    // the device (tile_offsets[tiles]): a longer one is reported through
+    // the status word (ss_sort_status: SS_ERR_CAPACITY).
+    const int64_t cap = int64_t((workspace_bytes - L.masks) / 32);
+    const int64_t stride = cap < int64_t(0xffffffffu) ? cap : int64_t(0xffffffffu);
+
     cudaStream_t st = (cudaStream_t)stream;
-    ss_status es = ensure_bwd_smem();
-    if (es != SS_OK) return es;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    SplatRecord *recs = reinterpret_cast<SplatRecord *>(ws + L.recs);
     int dev = 0, sms = 0;
-    es = current_device(&dev, &sms, "ss_raster_bwd: device query");
-    if (es != SS_OK) return es;
+    ss_status s = current_device(&dev, &sms, name);
+    if (s != SS_OK) return s;
+    const SplatPtrs sp{splats->mean2d, splats->conic, splats->opacity, splats->rgb, splats->depth,
+                       n};
     const int64_t want = (int64_t(n) + 255) / 256;
-    const int zgrid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
-    if (!(flags & SS_RECORDS_CLEARED))   // else ss_raster_fwd cleared them
-        SS_LAUNCH("k_grad_zero", st,
-                  k_grad_zero<<<zgrid, 256, 0, st>>>(reinterpret_cast<float4 *>(p.scratch),
-                                                     3 * int64_t(n)));
-    const int grid = tiles_x(W) * tiles_y(H);
-    if (accum && dist)
-        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, true, true><<<grid, 256, kBwdDynSmem, st>>>(p)));
-    else if (dist)
-        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, true, true><<<grid, 256, kBwdDynSmem, st>>>(p)));
-    else if (accum)
-        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, true, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
-    else
-        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, true, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
-    SS_LAUNCH("k_grad_final", st,
-              k_grad_final<<<zgrid, 256, 0, st>>>(p, n, accum ? accum_weight : nullptr));
-    return check_launch("ss_raster_bwd");
+    const int rgrid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+    SS_LAUNCH("k_make_records", st,
+              k_make_records<<<rgrid, 256, 0, st>>>(sp, tiles_x(W), tiles_y(H), recs));
+    s = check_launch(name);
+    if (s != SS_OK) return s;
+    uint32_t *masks = reinterpret_cast<uint32_t *>(ws + L.masks);
+    s = launch_masks(recs, n, vals, tile_offsets, last_contrib, W, H, masks, stride, workspace, st,
+                     name);
+    if (s != SS_OK) return s;
+    BwdParams p{};
+    p.recs = recs;
+    p.n = n;
+    p.vals = vals;
+    p.offs = tile_offsets;
+    p.masks = masks;
+    p.n_pairs = stride;
+    p.W = W;
+    p.H = H;
+    p.tiles_x = tiles_x(W);
+    for (int c = 0; c < 3; ++c) p.bg[c] = bg ? bg[c] : 0.0f;
+    p.T_final = T_final;
+    p.last = last_contrib;
+    p.dL = dL_dimage;
+    p.dmean2d = grads->dmean2d;
+    p.dconic = grads->dconic;
+    p.dopacity = grads->dopacity;
+    p.drgb = grads->drgb;
+    p.ddepth = nullptr;
+    p.scratch = reinterpret_cast<float *>(ws + L.accum);
+    return launch_bwd(p, flags & SS_ACCUM_WEIGHT, accum_weight, st, name);
 }
 
 // ---------------------------------------------------------------------------

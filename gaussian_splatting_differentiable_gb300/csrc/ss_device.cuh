@@ -162,6 +162,17 @@ __device__ __forceinline__ SplatRecord make_record(const SplatPtrs &s, uint32_t 
     return r;
 }
 
+// The record of splat idx computed from the SoA inputs, bit for bit what
+// the binning writes (the culled get the invisible record).
+__device__ __forceinline__ SplatRecord record_of(const SplatPtrs &s, uint32_t idx, int32_t tiles_x,
+                                                 int32_t tiles_y) {
+    int x0, y0, x1, y1;
+    uint32_t dbits;
+    float rx = 0.0f, ry = 0.0f;
+    const int st = splat_tile_rect(s, idx, tiles_x, tiles_y, x0, y0, x1, y1, dbits, rx, ry);
+    return st >= 0 ? make_record(s, idx, rx, ry) : invisible_record();
+}
+
 // 16-byte asynchronous global -> shared copy (cp.async, L2 only).
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));

@@ -63,13 +63,13 @@ struct FwdParams {
 };
 static_assert(sizeof(FwdParams) <= 128, "kernel parameters over 128 bytes run slower");
 
-// A minimum of CTAs a SM only where it measured faster: five for the plain
-// variant (48 registers, ~3 µs at 2M splats), four for the distortion one
-// (62 registers); the statistics and median variants ran slower bounded
-// (0.585 vs 0.567 and 0.517 vs 0.513 ms) and keep the compiler's choice.
-template <bool MEDIAN, bool STATS, bool DIST>
-__global__ void __launch_bounds__(256, (!MEDIAN && !STATS && !DIST) ? 5 : (DIST && !STATS && !MEDIAN) ? 4 : 0)
-k_raster_fwd(FwdParams p) {
+// The forward's body.  SOA: the splats come as the SoA inputs instead of
+// the binning's records -- each batch's records are computed on the fly
+// (record_of: the same bits the binning writes) and stored into shared
+// memory -- and no blend masks are written (the entry point that takes the
+// splats themselves has no mask buffer).
+template <bool MEDIAN, bool STATS, bool DIST, bool SOA>
+__device__ __forceinline__ void raster_fwd(const FwdParams &p, const SplatPtrs &soa) {
     __shared__ SplatGeo s_geo[2][256];
     __shared__ SplatGeo2 s_geo2[2][256];
     __shared__ SplatCol s_col[2][256];
@@ -127,11 +127,25 @@ k_raster_fwd(FwdParams p) {
     uint32_t last = 0;
     bool done = !inside;
 
+    const int nty = (p.H + kTile - 1) / kTile;
+    // Record idx into slot t of buffer b: an asynchronous copy of the
+    // binning's record, or (SOA) the record computed here.
+    auto stage = [&](uint32_t idx, int b, int t) {
+        if (SOA) {
+            const SplatRecord r =
+                idx < uint32_t(soa.n) ? record_of(soa, idx, ntx, nty) : invisible_record();
+            s_geo[b][t] = r.geo;
+            s_geo2[b][t] = r.geo2;
+            s_col[b][t] = r.col;
+            s_box[b][t] = r.box;
+        } else {
+            stage_record_async(p.recs, idx, p.n, s_geo[b], s_geo2[b], s_col[b], s_box[b], t);
+        }
+    };
+
     // Batch b covers list positions [start + 256 b, min(end, start + 256 (b + 1))).
     if (start < end) {
-        if (uint32_t(tid) < end - start)
-            stage_record_async(p.recs, p.vals[start + tid], p.n, s_geo[0], s_geo2[0], s_col[0],
-                               s_box[0], tid);
+        if (uint32_t(tid) < end - start) stage(p.vals[start + tid], 0, tid);
         cp_async_commit();
     }
     uint32_t next_idx = start + 256u + uint32_t(tid) < end ? p.vals[start + 256u + tid] : 0u;
@@ -144,9 +158,7 @@ k_raster_fwd(FwdParams p) {
         // has passed the barrier, so nobody still reads the batch before).
         const uint32_t nbase = base + 256;
         if (nbase < end) {
-            if (nbase + uint32_t(tid) < end)
-                stage_record_async(p.recs, next_idx, p.n, s_geo[buf ^ 1], s_geo2[buf ^ 1],
-                                   s_col[buf ^ 1], s_box[buf ^ 1], tid);
+            if (nbase + uint32_t(tid) < end) stage(next_idx, buf ^ 1, tid);
             cp_async_commit();
             next_idx = nbase + 256u + uint32_t(tid) < end ? p.vals[nbase + 256u + tid] : 0u;
         }
@@ -166,7 +178,8 @@ k_raster_fwd(FwdParams p) {
             if (hit) s_list[warp][cnt + __popc(m & lt)] = uint8_t(j);
             cnt += __popc(m);
         }
-        for (int k = lane; k < nb; k += 32) s_mask[warp][k] = 0u;
+        if (!SOA)
+            for (int k = lane; k < nb; k += 32) s_mask[warp][k] = 0u;
         __syncwarp();
         for (int q = 0; q < cnt; ++q) {
             const int j = s_list[warp][q];
@@ -205,7 +218,7 @@ k_raster_fwd(FwdParams p) {
                 last = base - start + uint32_t(j) + 1u;
             }
             const uint32_t m = __ballot_sync(0xffffffffu, blend);
-            if (lane == 0) s_mask[warp][j] = m;
+            if (!SOA && lane == 0) s_mask[warp][j] = m;
             if (STATS && m) {
                 const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(wblend));
                 if (lane == 0) {
@@ -219,9 +232,11 @@ k_raster_fwd(FwdParams p) {
             // 2M-splat scene, 0.520 vs 0.498 ms with the four dense blobs).
         }
         __syncwarp();
-        uint32_t *gm = p.masks + size_t(warp) * size_t(p.n_pairs) + base;
-        for (int k = lane; k < nb; k += 32)
-            if (base + uint32_t(k) < p.n_pairs) gm[k] = s_mask[warp][k];
+        if (!SOA) {
+            uint32_t *gm = p.masks + size_t(warp) * size_t(p.n_pairs) + base;
+            for (int k = lane; k < nb; k += 32)
+                if (base + uint32_t(k) < p.n_pairs) gm[k] = s_mask[warp][k];
+        }
     }
     cp_async_wait<0>();  // no copy may outlive the CTA
     if (STATS) {
@@ -243,6 +258,23 @@ k_raster_fwd(FwdParams p) {
     }
 }
 
+// A minimum of CTAs a SM only where it measured faster: five for the plain
+// variant (48 registers, ~3 µs at 2M splats), four for the distortion one
+// (62 registers); the statistics and median variants ran slower bounded
+// (0.585 vs 0.567 and 0.517 vs 0.513 ms) and keep the compiler's choice.
+template <bool MEDIAN, bool STATS, bool DIST>
+__global__ void __launch_bounds__(256, (!MEDIAN && !STATS && !DIST) ? 5 : (DIST && !STATS && !MEDIAN) ? 4 : 0)
+k_raster_fwd(FwdParams p) {
+    raster_fwd<MEDIAN, STATS, DIST, false>(p, SplatPtrs{});
+}
+
+// The forward from the SoA splats (ss_raster_fwd): records computed per
+// batch, no blend masks.
+template <bool MEDIAN>
+__global__ void __launch_bounds__(256) k_raster_fwd_splats(FwdParams p, SplatPtrs s) {
+    raster_fwd<MEDIAN, false, false, true>(p, s);
+}
+
 template <bool MEDIAN, bool STATS, bool DIST>
 static void launch_fwd(const FwdParams &p, int grid, cudaStream_t st) {
     SS_LAUNCH("k_raster_fwd", st, (k_raster_fwd<MEDIAN, STATS, DIST><<<grid, 256, 0, st>>>(p)));
@@ -252,49 +284,50 @@ static void launch_fwd(const FwdParams &p, int grid, cudaStream_t st) {
 
 using namespace ss;
 
-extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *vals,
-                                   const uint32_t *tile_offsets, int64_t n_pairs, int32_t W,
-                                   int32_t H, const float *bg, uint32_t flags, float *image,
-                                   float *T_final, uint32_t *last_contrib, float *median_depth,
-                                   uint32_t *blend_masks, float *max_weight,
-                                   uint32_t *blend_count, float *distortion, float *dist_totals,
-                                   void *bwd_workspace, size_t bwd_workspace_bytes,
-                                   ss_stream_t stream) {
+extern "C" ss_status ss_raster_fwd_records(const void *records, int32_t n_splats,
+                                           const uint32_t *vals, const uint32_t *tile_offsets,
+                                           int64_t n_pairs, int32_t W, int32_t H, const float *bg,
+                                           uint32_t flags, float *image, float *T_final,
+                                           uint32_t *last_contrib, float *median_depth,
+                                           uint32_t *blend_masks, float *max_weight,
+                                           uint32_t *blend_count, float *distortion,
+                                           float *dist_totals, void *bwd_workspace,
+                                           size_t bwd_workspace_bytes, ss_stream_t stream) {
     clear_error();
     if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
-        return fail(SS_ERR_UNSUPPORTED, "ss_raster_fwd: image %dx%d outside 1..%d", W, H, kMaxSide);
+        return fail(SS_ERR_UNSUPPORTED, "ss_raster_fwd_records: image %dx%d outside 1..%d", W, H, kMaxSide);
     if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: unknown flag bits 0x%x", flags);
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: unknown flag bits 0x%x", flags);
     const bool dist = flags & SS_DISTORTION;
     if (dist && (!distortion || !dist_totals))
         return fail(SS_ERR_INVALID_ARG,
-                    "ss_raster_fwd: SS_DISTORTION set but distortion / dist_totals NULL");
+                    "ss_raster_fwd_records: SS_DISTORTION set but distortion / dist_totals NULL");
     if (dist && (reinterpret_cast<uintptr_t>(dist_totals) & 15))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: dist_totals not 16-byte aligned");
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: dist_totals not 16-byte aligned");
     const bool stats = flags & SS_WEIGHT_STATS;
     if (stats && n_splats > 0 && (!max_weight || !blend_count))
         return fail(SS_ERR_INVALID_ARG,
-                    "ss_raster_fwd: SS_WEIGHT_STATS set but max_weight / blend_count NULL");
-    if (n_splats < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: n_splats < 0");
-    if (n_splats > 0 && !records) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: records is NULL");
+                    "ss_raster_fwd_records: SS_WEIGHT_STATS set but max_weight / blend_count NULL");
+    if (n_splats < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: n_splats < 0");
+    if (n_splats > 0 && !records) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: records is NULL");
     if (reinterpret_cast<uintptr_t>(records) & 15)
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: records not 16-byte aligned");
-    if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: vals/offsets NULL");
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: records not 16-byte aligned");
+    if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: vals/offsets NULL");
     if (!image || !T_final || !last_contrib)
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: an output is NULL");
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: an output is NULL");
     if (n_pairs < 0 || n_pairs > int64_t(0xffffffffu))
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: n_pairs outside 0..2^32-1");
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: n_pairs outside 0..2^32-1");
     if (n_pairs > 0 && !blend_masks)
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: blend_masks is NULL");
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: blend_masks is NULL");
     const bool median = flags & SS_MEDIAN_DEPTH;
     if (median && !median_depth)
-        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: SS_MEDIAN_DEPTH set but median_depth NULL");
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: SS_MEDIAN_DEPTH set but median_depth NULL");
     if (bwd_workspace) {
         if (reinterpret_cast<uintptr_t>(bwd_workspace) & 255)
-            return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: bwd_workspace not 256-byte aligned");
+            return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: bwd_workspace not 256-byte aligned");
         const size_t need = ws_layout(n_splats, 0, W, H).bwd_end;
         if (bwd_workspace_bytes < need)
-            return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: bwd_workspace %zu bytes < %zu needed",
+            return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd_records: bwd_workspace %zu bytes < %zu needed",
                         bwd_workspace_bytes, need);
     }
     FwdParams p{};
@@ -322,10 +355,10 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
     cudaStream_t st = (cudaStream_t)stream;
     if (stats && n_splats > 0) {
         ss_status s = check_cuda(cudaMemsetAsync(max_weight, 0, size_t(n_splats) * 4, st),
-                                 "ss_raster_fwd: memset");
+                                 "ss_raster_fwd_records: memset");
         if (s == SS_OK)
             s = check_cuda(cudaMemsetAsync(blend_count, 0, size_t(n_splats) * 4, st),
-                           "ss_raster_fwd: memset");
+                           "ss_raster_fwd_records: memset");
         if (s != SS_OK) return s;
     }
     switch ((median ? 4 : 0) | (stats ? 2 : 0) | (dist ? 1 : 0)) {
@@ -338,5 +371,57 @@ extern "C" ss_status ss_raster_fwd(const void *records, int32_t n_splats, const 
         case 6: launch_fwd<true, true, false>(p, grid, st); break;
         default: launch_fwd<true, true, true>(p, grid, st); break;
     }
+    return check_launch("ss_raster_fwd_records");
+}
+
+extern "C" ss_status ss_raster_fwd(const ss_splats *splats, const uint32_t *vals,
+                                   const uint32_t *tile_offsets, int32_t W, int32_t H,
+                                   const float *bg, uint32_t flags, float *image, float *T_final,
+                                   uint32_t *last_contrib, float *median_depth,
+                                   ss_stream_t stream) {
+    clear_error();
+    if (!splats) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: splats is NULL");
+    if (W < 1 || H < 1 || W > kMaxSide || H > kMaxSide)
+        return fail(SS_ERR_UNSUPPORTED, "ss_raster_fwd: image %dx%d outside 1..%d", W, H, kMaxSide);
+    if (flags & ~uint32_t(SS_ACCUM_WEIGHT | SS_MEDIAN_DEPTH | SS_WEIGHT_STATS | SS_DISTORTION |
+                          SS_RECORDS_CLEARED))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: unknown flag bits 0x%x", flags);
+    if (flags & (SS_WEIGHT_STATS | SS_DISTORTION))
+        return fail(SS_ERR_UNSUPPORTED,
+                    "ss_raster_fwd: the weight statistics and the distortion need their output "
+                    "buffers: use ss_raster_fwd_records");
+    const int32_t n = splats->n;
+    if (n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: n < 0");
+    if (n > 0 && (!splats->mean2d || !splats->conic || !splats->opacity || !splats->rgb ||
+                  !splats->depth))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: a splat array is NULL");
+    if (n > 0 && (reinterpret_cast<uintptr_t>(splats->mean2d) & 7))
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: mean2d not 8-byte aligned");
+    if (!vals || !tile_offsets) return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: vals/offsets NULL");
+    if (!image || !T_final || !last_contrib)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: an output is NULL");
+    const bool median = flags & SS_MEDIAN_DEPTH;
+    if (median && !median_depth)
+        return fail(SS_ERR_INVALID_ARG, "ss_raster_fwd: SS_MEDIAN_DEPTH set but median_depth NULL");
+    FwdParams p{};
+    p.recs = nullptr;
+    p.n = n;
+    p.vals = vals;
+    p.offs = tile_offsets;
+    p.W = uint16_t(W);
+    p.H = uint16_t(H);
+    for (int c = 0; c < 3; ++c) p.bg[c] = bg ? bg[c] : 0.0f;
+    p.image = image;
+    p.T_final = T_final;
+    p.last = last_contrib;
+    p.median = median_depth;
+    const SplatPtrs sp{splats->mean2d, splats->conic, splats->opacity, splats->rgb, splats->depth,
+                       n};
+    const int grid = tiles_x(W) * tiles_y(H);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (median)
+        SS_LAUNCH("k_raster_fwd_splats", st, (k_raster_fwd_splats<true><<<grid, 256, 0, st>>>(p, sp)));
+    else
+        SS_LAUNCH("k_raster_fwd_splats", st, (k_raster_fwd_splats<false><<<grid, 256, 0, st>>>(p, sp)));
     return check_launch("ss_raster_fwd");
 }

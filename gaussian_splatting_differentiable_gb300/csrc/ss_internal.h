@@ -59,6 +59,9 @@ struct WsLayout {
     size_t sort_end;
     size_t accum;         // backward per-splat gradient records, 48 bytes each
     size_t bwd_end;
+    size_t recs;          // 64-byte splat records built by the backward from the splats
+    size_t masks;         // uint32 [8][n_pairs] blend masks re-evaluated by the backward
+    size_t masks_end;
     size_t total;
     int ndig;
     int64_t nparts;

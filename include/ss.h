@@ -12,8 +12,15 @@
  *   ss_bin_tiles   tile binning: one (key, value) pair per (splat, touched tile)
  *   ss_pair_count  the one device-to-host read: how many pairs were emitted
  *   ss_sort_pairs  radix sort of the pairs by (tile, depth) + per-tile ranges
- *   ss_raster_fwd  front-to-back compositing per pixel
- *   ss_raster_bwd  back-to-front gradient of the 9 per-splat fields
+ *   ss_raster_fwd  front-to-back compositing per pixel, from the splats
+ *   ss_raster_bwd  back-to-front gradient of the 9 per-splat fields, from the
+ *                  splats, the forward's T_final / last_contrib and dL/dimage
+ *
+ * ss_raster_fwd_records / ss_raster_bwd_records are the same two steps on
+ * the per-splat records ss_bin_tiles writes, with the optional outputs
+ * (weight statistics, distortion) and the forward's blend decisions passed
+ * to the backward (blend_masks), which then need not re-evaluate them: the
+ * form a training step uses.
  *
  * Conventions (every function):
  *   - Memory: the caller owns all memory.  Every pointer is a DEVICE pointer
@@ -61,7 +68,7 @@ typedef enum {
     SS_ERR_DEVICE = 6        /* a device-side check failed (ss_sort_status) */
 } ss_status;
 
-/* flags of ss_raster_fwd / ss_raster_bwd: optional outputs, each compiled
+/* flags of the ss_raster_* calls: optional outputs, each compiled
  * as its own kernel variant so that a disabled output costs no shared memory
  * or registers (the pattern of "从 8.6 KB 到 4.2 KB ...", section 最小改动:
  * optional per-pixel arrays sized by a compile-time constant). */
@@ -75,7 +82,8 @@ enum {
                               gradient, including dL/ddepth (the write-up's distortion
                               option with per-pixel float4 totals, 最小改动) */
     SS_RECORDS_CLEARED = 16u  /* bwd only: the gradient records in the workspace were
-                                 cleared by ss_raster_fwd (its bwd_workspace argument)
+                                 cleared by ss_raster_fwd_records (its bwd_workspace
+                                 argument)
                                  and nothing wrote the workspace since; the backward
                                  then skips its own clearing pass */
 };
@@ -116,9 +124,9 @@ void ss_constants(float out[4]);
 const char *ss_last_error(void);
 
 /* Host: bytes of workspace that ss_sort_pairs (for n_pairs pairs on a W x H
- * image) and ss_raster_bwd (for n_splats splats) need.  One buffer of this
- * size serves both calls, in any order on one stream.  Returns 0 if a size
- * is out of range. */
+ * image), ss_raster_bwd and ss_raster_bwd_records (for n_splats splats and
+ * n_pairs pairs) need.  One buffer of this size serves all of them, in any
+ * order on one stream.  Returns 0 if a size is out of range. */
 size_t ss_workspace_bytes(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H);
 
 /* Tile binning ("Phase 5 step 30b", emit_pairs: tile id computation and an
@@ -201,14 +209,27 @@ ss_status ss_sort_pairs_dev(uint64_t *keys, uint32_t *vals, const uint64_t *d_co
  * SS_ERR_DEVICE or SS_ERR_CAPACITY for the last sort that used `workspace`. */
 ss_status ss_sort_status(const void *workspace, ss_stream_t stream);
 
-/* Forward rasterization ("Phase 5 step 30b", rasterize_f32): one CTA per
- * 16x16 tile, one thread per pixel, the tile's pairs staged in shared memory
- * in batches; each pixel composites its tile's splats front to back (model
- * above).  Outputs (device, W x H each, planar):
+/* Forward rasterization ("Phase 5 step 30b", rasterize_f32) from the splats
+ * themselves: as ss_raster_fwd_records (below), with each batch's records
+ * computed from `splats` (the ones ss_bin_tiles would write, bit for bit)
+ * and no blend masks, weight statistics or distortion (SS_WEIGHT_STATS and
+ * SS_DISTORTION return SS_ERR_UNSUPPORTED; SS_MEDIAN_DEPTH is supported, the
+ * other flags are ignored).
+ *   splats: the splats ss_bin_tiles binned; vals, tile_offsets: the output of
+ *   ss_sort_pairs for the same W, H.  Outputs as ss_raster_fwd_records. */
+ss_status ss_raster_fwd(const ss_splats *splats, const uint32_t *vals, const uint32_t *tile_offsets,
+                        int32_t W, int32_t H, const float *bg, uint32_t flags, float *image,
+                        float *T_final, uint32_t *last_contrib, float *median_depth,
+                        ss_stream_t stream);
+
+/* Forward rasterization ("Phase 5 step 30b", rasterize_f32) on the records of
+ * ss_bin_tiles: one CTA per 16x16 tile, one thread per pixel, the tile's
+ * pairs staged in shared memory in batches; each pixel composites its tile's
+ * splats front to back (model above).  Outputs (device, W x H each, planar):
  *   image[3][H][W]      color + T_final * bg
  *   T_final[H][W]       transmittance after the last blended splat (>= 1e-4)
  *   last_contrib[H][W]  1 + position in the tile's list of the last blended
- *                       splat, 0 if none (what ss_raster_bwd replays from)
+ *                       splat, 0 if none (what the backward replays from)
  *   median_depth[H][W]  only with SS_MEDIAN_DEPTH (else may be NULL): depth
  *                       of the last splat blended while T > 0.5, 0 if none
  *   bg: HOST float[3] background, or NULL for black.
@@ -238,25 +259,52 @@ ss_status ss_sort_status(const void *workspace, ss_stream_t stream);
  *            pair count, or the capacity when the count stayed on the device
  *            (ss_sort_pairs_dev).  The backward must get the same value.
  *   bwd_workspace, bwd_workspace_bytes: optional (NULL: unused).  The
- *            workspace the following ss_raster_bwd gets (256-byte aligned,
+ *            workspace the following ss_raster_bwd_records gets (256-byte aligned,
  *            >= ss_workspace_bytes(n_splats, 0, W, H) bytes): the forward's
  *            CTAs then also clear the backward's per-splat gradient records
  *            in it (a few stores a thread, hidden under the compositing),
- *            and that ss_raster_bwd call, given SS_RECORDS_CLEARED, skips its
+ *            and that ss_raster_bwd_records call, given SS_RECORDS_CLEARED, skips its
  *            separate clearing pass.  No call may write the workspace in
  *            between (ss_sort_pairs uses the same bytes).
  * Pair values >= n_splats are ignored. */
-ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *vals,
-                        const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,
-                        const float *bg, uint32_t flags, float *image, float *T_final,
-                        uint32_t *last_contrib, float *median_depth, uint32_t *blend_masks,
-                        float *max_weight, uint32_t *blend_count, float *distortion,
-                        float *dist_totals, void *bwd_workspace, size_t bwd_workspace_bytes,
-                        ss_stream_t stream);
+ss_status ss_raster_fwd_records(const void *records, int32_t n_splats, const uint32_t *vals,
+                                const uint32_t *tile_offsets, int64_t n_pairs, int32_t W,
+                                int32_t H, const float *bg, uint32_t flags, float *image,
+                                float *T_final, uint32_t *last_contrib, float *median_depth,
+                                uint32_t *blend_masks, float *max_weight, uint32_t *blend_count,
+                                float *distortion, float *dist_totals, void *bwd_workspace,
+                                size_t bwd_workspace_bytes, ss_stream_t stream);
 
-/* Backward rasterization ("从 8.6 KB 到 4.2 KB ...", rasterize_bwd_2d on the
- * 2D screen-space path; "Phase 5 step 30b", rasterize_backwards: the 9-field
- * per-splat gradient).  Each pixel walks its tile's list back to front from
+/* Backward rasterization from the splats themselves ("Phase 5 step 30b",
+ * rasterize_backwards; conclusion: each thread computes its own (pixel,
+ * splat) term and the warp sums them before one atomic): the inputs are
+ * the splats, their sorted pairs and tile ranges, the forward's T_final and
+ * last_contrib and dL/dimage.  The records are built into the workspace
+ * (those ss_bin_tiles would write), the forward's blend decisions are
+ * re-evaluated from them (a pixel blended list position j iff j <
+ * last_contrib and alpha >= 1/255, the forward's own test on the same
+ * float32 values), and then the gradients follow as in
+ * ss_raster_bwd_records.
+ *   flags: SS_ACCUM_WEIGHT as there; SS_DISTORTION returns
+ *   SS_ERR_UNSUPPORTED (its totals are an input of ss_raster_bwd_records);
+ *   SS_RECORDS_CLEARED returns SS_ERR_INVALID_ARG; the rest are ignored.
+ *   grads, accum_weight: as ss_raster_bwd_records (overwritten).
+ *   workspace: 256-byte aligned, at least ss_workspace_bytes(n, n_pairs, W, H)
+ *   bytes for n_pairs = tile_offsets[tiles] (the list length, known here
+ *   only on the device): the blend masks take 32 bytes a pair after the
+ *   records, and a list longer than the workspace holds makes
+ *   ss_sort_status(workspace) return SS_ERR_CAPACITY (the gradients are then
+ *   invalid); bits this call sets add to the status word of the last sort.
+ *   bg: HOST float[3] or NULL (must match the forward call). */
+ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals, const uint32_t *tile_offsets,
+                        int32_t W, int32_t H, const float *bg, uint32_t flags,
+                        const float *T_final, const uint32_t *last_contrib,
+                        const float *dL_dimage, const ss_grads *grads, float *accum_weight,
+                        void *workspace, size_t workspace_bytes, ss_stream_t stream);
+
+/* Backward rasterization on the records of ss_bin_tiles ("从 8.6 KB 到 4.2 KB
+ * ...", rasterize_bwd_2d on the 2D screen-space path; "Phase 5 step 30b",
+ * rasterize_backwards: the 9-field per-splat gradient).  Each pixel walks its tile's list back to front from
  * last_contrib, recovering T before each blended splat as T / (1 - alpha),
  * and adds, for L = sum dL/dimage * image:
  *   dL/drgb += g w,  w = alpha T
@@ -273,8 +321,11 @@ ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *v
  * which all fields follow, then added with four vector reductions per
  * (block, splat) into a per-splat record in the workspace.
  *   records, n_splats: the records ss_bin_tiles wrote for these splats.
- *   T_final, last_contrib, blend_masks: from ss_raster_fwd with the same
- *   inputs (the blend decisions are the forward's, not re-evaluated).
+ *   T_final, last_contrib, blend_masks: from ss_raster_fwd_records with the
+ *   same inputs (the blend decisions are the forward's, not re-evaluated).
+ *   blend_masks may be NULL: the decisions are then re-evaluated as in
+ *   ss_raster_bwd, into the workspace, which must then hold
+ *   ss_workspace_bytes(n_splats, n_pairs, W, H) bytes.
  *   dL_dimage: device float[3][H][W].
  *   dist_totals, dL_ddist: only with SS_DISTORTION (else may be NULL): the
  *   forward's totals and the upstream gradient of its distortion image,
@@ -290,15 +341,16 @@ ss_status ss_raster_fwd(const void *records, int32_t n_splats, const uint32_t *v
  *   workspace: >= ss_workspace_bytes(n, 0, W, H) bytes (48 per splat + 256),
  *   256-byte aligned; required whenever n > 0.  Its gradient records are
  *   cleared here first, unless flags has SS_RECORDS_CLEARED (the forward
- *   cleared them; see ss_raster_fwd's bwd_workspace).
+ *   cleared them; see ss_raster_fwd_records' bwd_workspace).
  *   bg: HOST float[3] or NULL (must match the forward call). */
-ss_status ss_raster_bwd(const void *records, int32_t n_splats, const uint32_t *vals,
-                        const uint32_t *tile_offsets, int64_t n_pairs, int32_t W, int32_t H,
-                        const float *bg, uint32_t flags, const float *T_final,
-                        const uint32_t *last_contrib, const uint32_t *blend_masks,
-                        const float *dL_dimage, const float *dist_totals, const float *dL_ddist,
-                        const ss_grads *grads, float *accum_weight, void *workspace,
-                        size_t workspace_bytes, ss_stream_t stream);
+ss_status ss_raster_bwd_records(const void *records, int32_t n_splats, const uint32_t *vals,
+                                const uint32_t *tile_offsets, int64_t n_pairs, int32_t W,
+                                int32_t H, const float *bg, uint32_t flags, const float *T_final,
+                                const uint32_t *last_contrib, const uint32_t *blend_masks,
+                                const float *dL_dimage, const float *dist_totals,
+                                const float *dL_ddist, const ss_grads *grads,
+                                float *accum_weight, void *workspace, size_t workspace_bytes,
+                                ss_stream_t stream);
 
 /* The backward pass for callers that cannot allocate (the pages have no
  * counterpart: this is a property of the library, not of the method).
@@ -306,13 +358,13 @@ ss_status ss_raster_bwd(const void *records, int32_t n_splats, const uint32_t *v
  * plugin inside an application that owns all device memory through its own
  * pool, or a real-time thread that must not risk the device-wide
  * synchronisation cudaMalloc / cudaFree can cause.  This entry point
- * computes exactly what ss_raster_bwd computes, with the same arguments
+ * computes exactly what ss_raster_bwd_records computes, with the same arguments
  * minus the workspace, and calls no allocator: the accumulated-weight
  * scratch (8 bytes per splat) is a fixed array inside the library,
  * 2,097,152 splats (16 MiB), which every GPU that loads the library holds
  * until the process exits.
- *   - n_splats > 2,097,152 returns SS_ERR_UNSUPPORTED (use ss_raster_bwd).
- *   - SS_DISTORTION returns SS_ERR_UNSUPPORTED (use ss_raster_bwd).
+ *   - n_splats > 2,097,152 returns SS_ERR_UNSUPPORTED (use ss_raster_bwd_records).
+ *   - SS_DISTORTION returns SS_ERR_UNSUPPORTED (use ss_raster_bwd_records).
  *   - SS_RECORDS_CLEARED is accepted and ignored (this call keeps no
  *     gradient records; it always clears its outputs first).
  *   - The first call in a CUDA context on a device, made with that device

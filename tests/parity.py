@@ -123,6 +123,78 @@ def run_gpu(scene, capacity=None, stream=None):
     return out
 
 
+def _outputs(r, out):
+    """numpy copies of a Rasterizer's outputs into out."""
+    torch.cuda.synchronize()
+    out["image"] = r.image.cpu().numpy()
+    out["T_final"] = r.T_final.cpu().numpy()
+    out["last"] = r.last_contrib.cpu().numpy().view(np.uint32)
+    out["median"] = r.median_depth.cpu().numpy() if r.median_depth is not None else None
+    out["dist"] = r.distortion.cpu().numpy() if r.distortion is not None else None
+    for k in GRAD_FIELDS + (DIST_FIELD,):
+        out[k] = r.grads[k].cpu().numpy() if k in r.grads else None
+    out["accum"] = r.accum_weight.cpu().numpy() if r.accum_weight is not None else None
+    out["max_w"] = r.max_weight.cpu().numpy() if r.max_weight is not None else None
+    out["bcount"] = (r.blend_count.cpu().numpy().view(np.uint32)
+                     if r.blend_count is not None else None)
+    return out
+
+
+def run_gpu_splats(scene):
+    """bin -> sort -> ss_raster_fwd -> ss_raster_bwd, the entry points that
+    take the splats themselves: no records and no blend masks are passed
+    (the forward computes each batch's records, the backward rebuilds the
+    records and re-evaluates the blend decisions in its workspace).  The
+    optional outputs these calls have: accumulated weight, median depth."""
+    dev = torch.device("cuda")
+    sp = ss.Splats.from_numpy(scene, dev)
+    flags = flags_of(scene) & (ss.SS_ACCUM_WEIGHT | ss.SS_MEDIAN_DEPTH)
+    r = ss.Rasterizer(scene.W, scene.H, scene.n, max(64, 4 * scene.n), flags, bg=scene.bg,
+                      device=dev)
+    pairs = r.bin_and_sort(sp)
+    out = {"count": pairs, "culled": r.culled}
+    out["keys"] = r.keys[:pairs].cpu().numpy().view(np.uint64).copy()
+    out["vals"] = r.vals[:pairs].cpu().numpy().view(np.uint32).copy()
+    out["keys_binned"], out["vals_binned"] = out["keys"], out["vals"]
+    out["offs"] = r.tile_offsets.cpu().numpy().view(np.uint32).copy()
+    r.image.fill_(float("nan"))
+    ss.ss_raster_fwd(sp, r.vals, r.tile_offsets, scene.W, scene.H, r.bg, flags, r.image,
+                     r.T_final, r.last_contrib, r.median_depth)
+    dL = torch.from_numpy(scene.dL_dimage).to(dev).contiguous()
+    for v in r.grads.values():
+        v.fill_(float("nan"))
+    ss.ss_raster_bwd(sp, r.vals, r.tile_offsets, scene.W, scene.H, r.bg, flags, r.T_final,
+                     r.last_contrib, dL, r.grads, r.accum_weight, r.workspace)
+    out["sort_status"] = ss.ss_sort_status(r.workspace)
+    return _outputs(r, out)
+
+
+def run_gpu_nomask(scene):
+    """The records path with the backward given no blend masks
+    (ss_raster_bwd_records re-evaluates the decisions into its workspace)."""
+    dev = torch.device("cuda")
+    sp = ss.Splats.from_numpy(scene, dev)
+    flags = flags_of(scene)
+    r = ss.Rasterizer(scene.W, scene.H, scene.n, max(64, 4 * scene.n), flags, bg=scene.bg,
+                      device=dev)
+    pairs = r.bin_and_sort(sp)
+    out = {"count": pairs, "culled": r.culled}
+    out["keys"] = r.keys[:pairs].cpu().numpy().view(np.uint64).copy()
+    out["vals"] = r.vals[:pairs].cpu().numpy().view(np.uint32).copy()
+    out["keys_binned"], out["vals_binned"] = out["keys"], out["vals"]
+    out["offs"] = r.tile_offsets.cpu().numpy().view(np.uint32).copy()
+    r.forward(sp)
+    r.blend_masks.fill_(-1)              # the backward must not read them
+    dL = torch.from_numpy(scene.dL_dimage).to(dev).contiguous()
+    dLd = (torch.from_numpy(scene.dL_ddist).to(dev).contiguous()
+           if flags & ss.SS_DISTORTION else None)
+    ss.ss_raster_bwd_records(r.records, r.n, r.vals, r.tile_offsets, r.n_pairs, scene.W, scene.H,
+                             r.bg, flags | ss.SS_RECORDS_CLEARED, r.T_final, r.last_contrib, None,
+                             dL, r.grads, r.accum_weight, r.workspace, None, r.dist_totals, dLd)
+    out["sort_status"] = ss.ss_sort_status(r.workspace)
+    return _outputs(r, out)
+
+
 def _pairs_sorted(keys, vals):
     o = np.lexsort((vals, keys))
     return keys[o], vals[o]
@@ -278,14 +350,21 @@ def _dist_grad(scene):
     return scene.dL_ddist if getattr(scene, "distortion", False) else None
 
 
-def full_parity(scene, capacity=None, knife_cap=None, graph=False, threads=None):
+def full_parity(scene, capacity=None, knife_cap=None, graph=False, threads=None, path=None):
     """Every output of the whole path against the oracle, every pixel and
     every splat.  The oracle runs tile-parallel on the host's cores
     (oracle.forward / oracle.backward with threads > 1: the same per-pixel
     code on disjoint tile sets).  graph=True runs the step the way bench.py
-    times it (run_gpu_graph)."""
+    times it (run_gpu_graph); path="splats" through the entry points that
+    take the splats themselves (run_gpu_splats), path="nomask" with the
+    backward given no blend masks (run_gpu_nomask)."""
     threads = oracle.default_threads() if threads is None else threads
-    gpu = run_gpu_graph(scene) if graph else run_gpu(scene, capacity)
+    if path == "splats":
+        gpu = run_gpu_splats(scene)
+    elif path == "nomask":
+        gpu = run_gpu_nomask(scene)
+    else:
+        gpu = run_gpu_graph(scene) if graph else run_gpu(scene, capacity)
     tl = check_pairs(scene, gpu)
     ofw = oracle.forward(scene, tl["vals"], tl["offs"], alt_capacity=1 << 20, threads=threads)
     f = check_forward(scene, gpu, ofw, knife_cap=knife_cap)

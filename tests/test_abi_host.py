@@ -56,13 +56,16 @@ def test_constants_match_oracle(lib):
     assert buf[1] == np.float32(c["alpha_max"])
     assert buf[2] == np.float32(c["T_eps"])
     assert buf[3] == c["tile"]
-    assert lib.ss_abi_version() == 7
+    assert lib.ss_abi_version() == 8
 
 
 def test_workspace_bytes(lib):
     a = lib.ss_workspace_bytes(2_000_000, 5_000_000, 1237, 822)
     assert a >= 5_000_000 * 12 and a % 256 == 0
     assert lib.ss_workspace_bytes(2_000_000, 0, 1237, 822) >= 2_000_000 * 8
+    # the backward from the splats builds records (64 B a splat) and blend
+    # masks (32 B a pair) after its gradient records (48 B a splat)
+    assert a >= 2_000_000 * (48 + 64) + 5_000_000 * 32
     assert lib.ss_workspace_bytes(0, 0, 1, 1) > 0
     assert lib.ss_workspace_bytes(-1, 0, 16, 16) == 0
     assert lib.ss_workspace_bytes(0, 0, 0, 16) == 0
@@ -94,7 +97,7 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert lib.ss_sort_pairs(0x1000, 0x1000, 10, 16, 16, 0x1000, 0x1000, 16, None) == 1
     assert "workspace" in lib.ss_last_error().decode()
     # forward: unknown flags, NULL outputs, median / stats / distortion flag without buffers
-    F = lambda *a: lib.ss_raster_fwd(*a[:-1], None, 0, a[-1])  # noqa: E731  (no bwd_workspace)
+    F = lambda *a: lib.ss_raster_fwd_records(*a[:-1], None, 0, a[-1])  # noqa: E731  (no bwd_workspace)
     assert F(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 16, 0x1000, 0x1000, 0x1000, None, 0x1000,
              None, None, None, None, None) == 1
     assert F(None, 0, 0x1000, 0x1000, 0, 16, 16, None, 0, None, 0x1000, 0x1000, None, 0x1000,
@@ -114,25 +117,29 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert "aligned" in lib.ss_last_error().decode()
     # backward: NULL gradient array, accum flag without buffer or workspace, distortion inputs
     B = lambda flags, g, ws=None, nbytes=0, acc=None, dt=None, dd=None, rec=0x1000, masks=0x1000: \
-        lib.ss_raster_bwd(rec, 4, 0x1000, 0x1000, 8, 16, 16, None, flags, 0x1000, 0x1000, masks,
-                          0x1000, dt, dd, ctypes.byref(g), acc, ws, nbytes, None)  # noqa: E731
+        lib.ss_raster_bwd_records(rec, 4, 0x1000, 0x1000, 8, 16, 16, None, flags, 0x1000, 0x1000,
+                                  masks, 0x1000, dt, dd, ctypes.byref(g), acc, ws, nbytes,
+                                  None)  # noqa: E731
     g = SsGrads(0x1000, None, 0x1000, 0x1000, None)
     assert B(0, g) == 1
     g = SsGrads(0x1000, 0x1000, 0x1000, 0x1000, None)
     assert B(1, g, ws=0x1000, nbytes=1 << 20) == 1            # accum without buffer
     assert B(1, g, ws=0x1000, nbytes=8, acc=0x1000) == 1      # small workspace
     assert B(0, g, rec=None) == 1
-    assert B(0, g, masks=None) == 1
+    assert B(0, g, masks=None) == 1                          # masks rebuilt: needs a workspace
+    assert B(0, g, masks=None, ws=0x1000, nbytes=1000) == 1
+    assert "blend masks" in lib.ss_last_error().decode()
     assert B(32, g, ws=0x1000, nbytes=1 << 20) == 1           # unknown flag
-    # SS_RECORDS_CLEARED is the backward's; the forward and the static-scratch backward reject it
+    # SS_RECORDS_CLEARED is the backward's: the forward rejects it (the
+    # static-scratch backward accepts and ignores it); unknown bits are rejected
     assert F(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 16, 0x1000, 0x1000, 0x1000, None,
              0x1000, None, None, None, None, None) == 1
-    assert lib.ss_raster_bwd_noalloc(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 16, 0x1000,
+    assert lib.ss_raster_bwd_noalloc(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 32, 0x1000,
                                      0x1000, 0x1000, 0x1000, ctypes.byref(g), None, None) == 1
     # the forward's optional bwd_workspace: 256-byte aligned and large enough for the records
-    Fw = lambda ws, nbytes: lib.ss_raster_fwd(0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 0,  # noqa: E731
-                                              0x1000, 0x1000, 0x1000, None, 0x1000, None, None,
-                                              None, None, ws, nbytes, None)
+    Fw = lambda ws, nbytes: lib.ss_raster_fwd_records(  # noqa: E731
+        0x1000, 5, 0x1000, 0x1000, 10, 16, 16, None, 0, 0x1000, 0x1000, 0x1000, None, 0x1000, None,
+        None, None, None, ws, nbytes, None)
     assert Fw(0x1010, 1 << 20) == 1
     assert "aligned" in lib.ss_last_error().decode()
     assert Fw(0x1000, 8) == 1
@@ -143,6 +150,28 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert "ddepth" in lib.ss_last_error().decode()
     assert lib.ss_raster_bwd_noalloc(0x1000, 4, 0x1000, 0x1000, 8, 16, 16, None, 8, 0x1000,
                                      0x1000, 0x1000, 0x1000, ctypes.byref(g), None, None) == 5
+    # the entry points that take the splats themselves
+    S = ctypes.byref(sp)
+    Fs = lambda flags, img=0x1000, spl=S: lib.ss_raster_fwd(  # noqa: E731
+        spl, 0x1000, 0x1000, 16, 16, None, flags, img, 0x1000, 0x1000, None, None)
+    assert Fs(0, spl=None) == 1
+    assert Fs(0, img=None) == 1
+    assert Fs(2) == 1                                        # median without its buffer
+    assert Fs(4) == 5 and Fs(8) == 5                         # statistics, distortion
+    assert "ss_raster_fwd_records" in lib.ss_last_error().decode()
+    assert Fs(64) == 1                                       # unknown flag
+    Bs = lambda flags, ws=0x1000, nbytes=1 << 20, spl=S, acc=0x1000: lib.ss_raster_bwd(  # noqa: E731
+        spl, 0x1000, 0x1000, 16, 16, None, flags, 0x1000, 0x1000, 0x1000, ctypes.byref(g), acc, ws,
+        nbytes, None)
+    assert Bs(0, spl=None) == 1
+    assert Bs(8) == 5                                        # distortion
+    assert Bs(16) == 1                                       # records-cleared flag
+    assert Bs(1, acc=None) == 1                              # accum without buffer
+    assert Bs(0, ws=0x1010) == 1                             # misaligned workspace
+    assert Bs(0, nbytes=256) == 1                            # no room for records and masks
+    assert "workspace" in lib.ss_last_error().decode()
+    unaligned = SsSplats(0x1004, 0x1000, 0x1000, 0x1000, 0x1000, 4)
+    assert Bs(0, spl=ctypes.byref(unaligned)) == 1
     # pair count / sort status with NULL
     assert lib.ss_pair_count(None, 0, None, None, None) == 1
     assert lib.ss_sort_status(None, None) == 1

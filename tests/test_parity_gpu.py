@@ -46,6 +46,46 @@ def test_workload_full_size_full_parity(P, wl, graph):
     print("workload", wl, "graph" if graph else "sync", r)
 
 
+@pytest.mark.parametrize("wl", [1, 2, 3, 4])
+def test_entry_points_that_take_the_splats(P, wl):
+    """ss_raster_fwd / ss_raster_bwd, given the splats themselves (the
+    forward computes each batch's records; the backward rebuilds the records
+    and re-evaluates the forward's blend decisions in its workspace, then
+    replays transmittance), against the oracle in full."""
+    sc = synth.make_scene(wl)
+    sc.weight_stats = sc.distortion = False
+    cap = P.KNIFE_EDGE_CAP if wl < 4 else P.KNIFE_EDGE_CAP_DENSE
+    r = P.full_parity(sc, knife_cap=cap, path="splats")
+    print("workload", wl, "from the splats", r)
+
+
+@pytest.mark.parametrize("accum,median", [(False, False), (True, True), (False, True)])
+def test_entry_points_that_take_the_splats_flags(P, accum, median):
+    sc = _scene(96, 80, 500, seed=19, wl=2)
+    sc.accum_weight, sc.median_depth = accum, median
+    P.full_parity(sc, path="splats")
+
+
+@pytest.mark.parametrize("wl", [2, 3, 5, 6])
+def test_backward_without_the_forwards_blend_masks(P, wl):
+    """ss_raster_bwd_records given no blend masks re-evaluates the decisions
+    (every variant: workload 5 has the median and the weight statistics,
+    workload 6 the distortion), against the oracle in full."""
+    cap = P.KNIFE_EDGE_CAP if wl < 4 else P.KNIFE_EDGE_CAP_DENSE
+    r = P.full_parity(synth.make_scene(wl), knife_cap=cap, path="nomask")
+    print("workload", wl, "no masks", r)
+
+
+@pytest.mark.parametrize("W,H", [(37, 23), (1, 1), (17, 1), (129, 65)])
+def test_entry_points_that_take_the_splats_on_ragged_images(P, W, H):
+    sc = _scene(W, H, 80, seed=W * 1000 + H + 7)
+    sc.weight_stats = sc.distortion = False
+    sc.mean2d[:, 0] = sc.mean2d[:, 0] * 1.2 - 0.1 * W
+    sc.mean2d[:, 1] = sc.mean2d[:, 1] * 1.2 - 0.1 * H
+    P.full_parity(sc, path="splats")
+    P.full_parity(sc, path="nomask")
+
+
 def test_workload_3_with_distortion(P):
     sc = synth.make_scene(3)
     sc.distortion = True
@@ -397,8 +437,9 @@ def test_sort_modes_against_the_oracle(P, case):
 
 
 def test_forward_clears_the_backward_records(P):
-    """ss_raster_fwd with bwd_workspace clears the backward's gradient records
-    and ss_raster_bwd with SS_RECORDS_CLEARED skips its own clearing pass:
+    """ss_raster_fwd_records with bwd_workspace clears the backward's gradient
+    records and ss_raster_bwd_records with SS_RECORDS_CLEARED skips its own
+    clearing pass:
     the result equals that of a backward that clears them itself (gradients
     to float-atomic ordering, the fixed-point weight bit for bit), although
     the workspace started as non-zero bytes and the sort wrote over the
@@ -418,13 +459,13 @@ def test_forward_clears_the_backward_records(P):
     wa = r.accum_weight.clone()
     args = (r.records, r.n, r.vals, r.tile_offsets, r.n_pairs, sc.W, sc.H, r.bg)
     rest = (r.T_final, r.last_contrib, r.blend_masks, dL, r.grads, r.accum_weight, r.workspace)
-    ss.ss_raster_bwd(*args, r.flags, *rest)      # clears them itself
+    ss.ss_raster_bwd_records(*args, r.flags, *rest)      # clears them itself
     torch.cuda.synchronize()
     assert torch.equal(r.accum_weight, wa)
     for k, v in a.items():
         tol = max(1e-4, 1e-3 * float(v.abs().max()))
         assert float((r.grads[k] - v).abs().max()) <= tol, k
-    ss.ss_raster_bwd(*args, r.flags | ss.SS_RECORDS_CLEARED, *rest)   # stale sums kept
+    ss.ss_raster_bwd_records(*args, r.flags | ss.SS_RECORDS_CLEARED, *rest)   # stale sums kept
     torch.cuda.synchronize()
     assert torch.equal(r.accum_weight, 2 * wa)
 
