@@ -248,6 +248,16 @@ def ss_profile_collect() -> dict:
     return out
 
 
+def ss_debug_bounds_enabled() -> bool:
+    return bool(_L.ss_debug_bounds_enabled())
+
+
+def ss_debug_status(stream=None) -> int:
+    """SS_OK, or SS_ERR_DEVICE if a device-side bounds check failed since the
+    last call (only the SS_DEBUG_BOUNDS build checks; see ss_last_error())."""
+    return int(_L.ss_debug_status(_stream(stream)))
+
+
 def ss_probe_red_f32(buf, rounds: int, stream=None) -> None:
     _check(_L.ss_probe_red_f32(_ptr(buf), buf.numel(), rounds, _stream(stream)),
            "ss_probe_red_f32")

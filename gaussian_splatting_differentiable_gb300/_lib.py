@@ -11,6 +11,9 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libss.so")
+# The same library built with device-side bounds checks (build.py
+# --debug-bounds); SS_LIBRARY=<path> makes load() take it instead.
+DEBUG_LIB_PATH = os.path.join(_HERE, "libss_debug.so")
 
 SS_OK, SS_ERR_INVALID_ARG, SS_ERR_CAPACITY, SS_ERR_CUDA, SS_ERR_TIMEOUT, SS_ERR_UNSUPPORTED, \
     SS_ERR_DEVICE = range(7)
@@ -77,6 +80,8 @@ PROTOTYPES = {
                                              ctypes.POINTER(SsGrads), P, P]),
     "ss_profile_enable": (None, [I32]),
     "ss_profile_collect": (I64, [ctypes.c_char_p, SZ]),
+    "ss_debug_bounds_enabled": (I32, []),
+    "ss_debug_status": (ctypes.c_int, [P]),
     "ss_probe_red_f32": (ctypes.c_int, [P, I64, I32, P]),
     "ss_test_sort_wait_timeout": (ctypes.c_int, [P, SZ, P]),
     "ss_project_fwd": (ctypes.c_int, [ctypes.POINTER(SsSplats3d), ctypes.POINTER(SsCamera), P, P,
@@ -95,7 +100,7 @@ def load(path: str | None = None):
     global _lib
     if _lib is not None and path is None:
         return _lib
-    p = path or LIB_PATH
+    p = path or os.environ.get("SS_LIBRARY") or LIB_PATH
     if not os.path.exists(p):
         raise ImportError("libss.so is not built (%s); run "
                           "`python -c 'import __graft_entry__ as g; g.build()'`" % p)

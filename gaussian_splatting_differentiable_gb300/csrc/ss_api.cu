@@ -152,6 +152,33 @@ ss_status ss_sort_status(const void *workspace, ss_stream_t stream) {
     return SS_OK;
 }
 
+int32_t ss_debug_bounds_enabled(void) {
+#ifdef SS_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+ss_status ss_debug_status(ss_stream_t stream) {
+    clear_error();
+    ss_status st = check_cuda(cudaStreamSynchronize((cudaStream_t)stream),
+                              "ss_debug_status: synchronize");
+    if (st != SS_OK) return st;
+    uint32_t w = 0;
+    cudaError_t (*const readers[4])(uint32_t *) = {debug_word_bin, debug_word_sort,
+                                                   debug_word_fwd, debug_word_bwd};
+    for (int k = 0; k < 4 && st == SS_OK; ++k)
+        st = check_cuda(readers[k](&w), "ss_debug_status: reading a debug word");
+    if (st != SS_OK) return st;
+    if (w)
+        return fail(SS_ERR_DEVICE,
+                    "device bounds checks failed: 0x%x (1 sort destination, 2 sort rank, 4 forward "
+                    "list, 8 backward list, 16 last_contrib past its list, 32 splat index, 64 "
+                    "mask list)", w);
+    return SS_OK;
+}
+
 ss_status ss_probe_red_f32(float *buf, int64_t n, int32_t rounds, ss_stream_t stream) {
     clear_error();
     if (!buf || n < 1 || rounds < 0)

@@ -144,3 +144,7 @@ extern "C" ss_status ss_bin_tiles(const ss_splats *splats, int32_t W, int32_t H,
     SS_LAUNCH("k_emit_pairs", st, k_emit_pairs<<<grid, 256, 0, st>>>(p));
     return check_launch("ss_bin_tiles: k_emit_pairs");
 }
+
+namespace ss {
+cudaError_t debug_word_bin(uint32_t *out) { return read_and_clear_debug_word(out); }
+}  // namespace ss

@@ -218,9 +218,10 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
             dz = 2.0f * fmaf(r.depth, Wa, -Wd);
         }
         const size_t i = r.idx;
+        const bool bad_idx = SS_BAD(slot < nslots && r.idx >= uint32_t(p.n), kDbgBwdSplat);
         const float dmx = kLn2 * (2.0f * r.A * Qx + r.B * Qy);
         const float dmy = kLn2 * (r.B * Qx + 2.0f * r.C * Qy);
-        if (slot >= nslots) {
+        if (slot >= nslots || bad_idx) {
         } else if (AOS) {
             // Four reductions per (warp, splat) into one 48-byte record.
             float *g = p.scratch + kGradRec * i;
@@ -277,14 +278,18 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     const bool inside = x < p.W && y < p.H;
     const float px = float(x) + 0.5f, py = float(y) + 0.5f;
     const float wx0 = float(bx) + 0.5f, wy0 = float(by) + 0.5f;
-    const uint32_t start = p.offs[tile], len = p.offs[tile + 1] - start;
+    uint32_t start = p.offs[tile], len = p.offs[tile + 1] - start;
+    if (SS_BAD(p.offs[tile + 1] < start || int64_t(start) + len > p.n_pairs, kDbgBwdList))
+        start = len = 0u;
     const uint32_t lt = lanemask_lt();
 
     const size_t HW = size_t(p.W) * p.H, pix = size_t(y) * p.W + x;
     uint32_t n_p = 0;
     float T = 1.0f, g0 = 0.0f, g1 = 0.0f, g2 = 0.0f;
     if (inside) {
-        n_p = min(p.last[pix], len);  // a stale last_contrib cannot reach past the tile's pairs
+        n_p = p.last[pix];
+        if (SS_BAD(n_p > len, kDbgBwdLast)) n_p = len;
+        n_p = min(n_p, len);  // a stale last_contrib cannot reach past the tile's pairs
         T = p.T_final[pix];
         g0 = p.dL[pix];
         g1 = p.dL[HW + pix];
@@ -615,7 +620,9 @@ __global__ void __launch_bounds__(256) k_blend_masks(MaskParams p) {
     const float px = float(x) + 0.5f, py = float(y) + 0.5f;
     const float wx0 = float(bx) + 0.5f, wx1 = wx0 + 7.0f;
     const float wy0 = float(by) + 0.5f, wy1 = wy0 + 3.0f;
-    const uint32_t start = p.offs[tile], len = p.offs[tile + 1] - start;
+    uint32_t start = p.offs[tile], len = p.offs[tile + 1] - start;
+    if (SS_BAD(p.offs[tile + 1] < start || int64_t(start) + len > p.stride, kDbgMaskList))
+        start = len = 0u;
     if (tile == 0 && tid == 0 && int64_t(p.offs[p.tiles]) > p.stride)
         atomicOr(p.status, kDevErrCapacity);
     const uint32_t n_p = inside ? min(p.last[size_t(y) * p.W + x], len) : 0u;
@@ -1111,3 +1118,7 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
         SS_LAUNCH("k_accum_final", st, k_accum_final<<<zgrid, 256, 0, st>>>(p.accum, accum_weight, n));
     return check_launch("ss_raster_bwd_noalloc");
 }
+
+namespace ss {
+cudaError_t debug_word_bwd(uint32_t *out) { return read_and_clear_debug_word(out); }
+}  // namespace ss

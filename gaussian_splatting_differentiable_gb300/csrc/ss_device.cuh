@@ -24,6 +24,40 @@ constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kKRel = 1.0f + 1.0f / 1024.0f;
 constexpr float kKAbs = 1.0f / 1024.0f;
 
+// Device-side bounds checks of the SS_DEBUG_BOUNDS build.  A failed check
+// sets its bit in this translation unit's debug word (ss_debug_status reads
+// and clears the words of every unit) and the access it guards is skipped
+// or clamped: nothing traps.  In the normal build SS_BAD(...) is the
+// constant false and its condition is not evaluated.
+enum : unsigned {
+    kDbgSortScatter = 1u,   // a sort pass's destination outside the pairs
+    kDbgSortRank = 2u,      // a sort pass's rank outside its partition
+    kDbgFwdList = 4u,       // a forward tile list outside the pairs
+    kDbgBwdList = 8u,       // a backward tile list outside the pairs
+    kDbgBwdLast = 16u,      // a last_contrib beyond its tile's list
+    kDbgBwdSplat = 32u,     // a gradient record index outside the splats
+    kDbgMaskList = 64u      // a blend-mask tile list outside the mask rows
+};
+#ifdef SS_DEBUG_BOUNDS
+static __device__ unsigned int g_debug_word;
+#define SS_BAD(bad, bit) ((bad) ? (atomicOr(&::ss::g_debug_word, (bit)), true) : false)
+// Host: ORs this unit's debug word into *out and clears it.
+static inline cudaError_t read_and_clear_debug_word(uint32_t *out) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_debug_word, sizeof v);
+    if (e != cudaSuccess) return e;
+    *out |= v;
+    if (v) {
+        const unsigned z = 0;
+        e = cudaMemcpyToSymbol(g_debug_word, &z, sizeof z);
+    }
+    return e;
+}
+#else
+#define SS_BAD(bad, bit) false
+static inline cudaError_t read_and_clear_debug_word(uint32_t *) { return cudaSuccess; }
+#endif
+
 struct SplatPtrs {
     const float *mean2d, *conic, *opacity, *rgb, *depth;
     int32_t n;

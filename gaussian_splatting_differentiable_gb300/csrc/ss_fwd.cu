@@ -93,7 +93,8 @@ __device__ __forceinline__ void raster_fwd(const FwdParams &p, const SplatPtrs &
     const float px = float(x) + 0.5f, py = float(y) + 0.5f;
     const float wx0 = float(bx) + 0.5f, wx1 = wx0 + 7.0f;
     const float wy0 = float(by) + 0.5f, wy1 = wy0 + 3.0f;
-    const uint32_t start = p.offs[tile], end = p.offs[tile + 1];
+    uint32_t start = p.offs[tile], end = p.offs[tile + 1];
+    if (!SOA && SS_BAD(end < start || end > p.n_pairs, kDbgFwdList)) start = end = 0u;
     const uint32_t lt = lanemask_lt();
 
     if (STATS) {
@@ -425,3 +426,7 @@ extern "C" ss_status ss_raster_fwd(const ss_splats *splats, const uint32_t *vals
         SS_LAUNCH("k_raster_fwd_splats", st, (k_raster_fwd_splats<false><<<grid, 256, 0, st>>>(p, sp)));
     return check_launch("ss_raster_fwd");
 }
+
+namespace ss {
+cudaError_t debug_word_fwd(uint32_t *out) { return read_and_clear_debug_word(out); }
+}  // namespace ss

@@ -69,6 +69,13 @@ struct WsLayout {
 
 WsLayout ws_layout(int32_t n_splats, int64_t n_pairs, int32_t W, int32_t H);
 
+// The SS_DEBUG_BOUNDS debug words of the kernel translation units (each
+// ORs its word into *out and clears it; no-ops in the normal build).
+cudaError_t debug_word_bin(uint32_t *out);
+cudaError_t debug_word_sort(uint32_t *out);
+cudaError_t debug_word_fwd(uint32_t *out);
+cudaError_t debug_word_bwd(uint32_t *out);
+
 // Device status bits written by the sort kernels.
 enum : uint32_t { kDevErrTimeout = 1u, kDevErrKeyRange = 2u, kDevErrCapacity = 4u };
 

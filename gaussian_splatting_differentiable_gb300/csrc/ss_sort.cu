@@ -346,6 +346,7 @@ __device__ __forceinline__ void sort_pass_body(const PassParams &p, const KeyMap
             const uint32_t dig = digit(key[j]);
             const uint32_t rank = (j & 1) ? rank2[j >> 1] >> 16 : rank2[j >> 1] & 0xffffu;
             const uint32_t pos = s_lstart[dig] + s_whist[warp][dig] + rank;
+            if (SS_BAD(pos >= uint32_t(kSortPart), kDbgSortRank)) continue;
             s_keys[pos] = key[j];
             if (!PACKED) s_vals[pos] = val[j];
         }
@@ -357,6 +358,7 @@ __device__ __forceinline__ void sort_pass_body(const PassParams &p, const KeyMap
         const uint64_t k = s_keys[i];
         const uint32_t dig = digit(k);
         const uint32_t g = s_gbase[dig] + uint32_t(i) - s_lstart[dig];
+        if (SS_BAD(int64_t(g) >= n, kDbgSortScatter)) continue;
         if (PACKED && !last) {
             wout[g] = k;
         } else if (PACKED) {
@@ -763,3 +765,7 @@ extern "C" ss_status ss_test_sort_wait_timeout(void *workspace, size_t workspace
     SS_LAUNCH("k_sort_pass", st, k_sort_pass<<<1, 256, kSortPart * 12, st>>>(p));
     return check_launch("ss_test_sort_wait_timeout");
 }
+
+namespace ss {
+cudaError_t debug_word_sort(uint32_t *out) { return read_and_clear_debug_word(out); }
+}  // namespace ss

@@ -384,6 +384,21 @@ ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats, const uin
                                 const float *dL_dimage, const ss_grads *grads,
                                 float *accum_weight, ss_stream_t stream);
 
+/* Device-side bounds checks (a build variant, not part of the method).  A
+ * library built with -DSS_DEBUG_BOUNDS (gaussian_splatting_differentiable_gb300/
+ * build.py --debug-bounds, libss_debug.so) checks, in its kernels, that tile
+ * lists lie inside the pairs, that a last_contrib does not reach past its
+ * tile's list, that gradient-record indices lie inside the splats and that
+ * the sort's ranks and destinations lie inside their ranges; a failed check
+ * sets a bit in a device error word and skips or clamps the access it
+ * guards -- nothing traps.
+ * ss_debug_bounds_enabled: 1 in that build, 0 in the normal one.
+ * ss_debug_status: synchronizes `stream`, reads and clears the error word:
+ * SS_OK, or SS_ERR_DEVICE with the failed checks' bits in the message (the
+ * normal build never sets any). */
+int32_t ss_debug_bounds_enabled(void);
+ss_status ss_debug_status(ss_stream_t stream);
+
 /* Per-kernel timing ("从 8.6 KB 到 4.2 KB ...", section 亲手验证: SS_PROFILE=1
  * gives per-kernel segment timings).  Off unless the environment has
  * SS_PROFILE=1 when the library loads or ss_profile_enable(1) is called.
