@@ -266,9 +266,9 @@ def source_sha(paths) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of the kernel and on this workload."""
+def recorded_counters(kernel: str, workload: str):
+    """The committed ncu record of the kernel (profiles/traffic.json), if it
+    was taken on the current source of the kernel and on this workload."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -280,7 +280,42 @@ def recorded_traffic(kernel: str, workload: str):
         return None
     if rec.get("workload_name") != workload:
         return None
-    return rec.get("dram_bytes_per_launch_full")
+    return rec
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu record (None if stale)."""
+    rec = recorded_counters(kernel, workload)
+    return rec.get("dram_bytes_per_launch_full") if rec else None
+
+
+# The backward's method minimum per blended (pixel, splat) pair, in thread
+# instructions: the replay (the exponent from the splat's record: 2 sub,
+# 2 mul, 2 fma; the exponential, o G and the cap: 3; T in front, 1 - alpha,
+# its reciprocal and the product: 3; w = alpha T: 1; dL/dimage . rgb: 3;
+# dL/dalpha: 2; q = dL/dsigma with the cap's select: 2; the suffix colour
+# sum: 1 -- 21) and the pixel's share of the per-splat sums (q times 1, u,
+# v, u^2, uv, v^2 and w times 1, three colour gradients: 10).
+BWD_MIN_INSTR_PER_BLEND = 31
+
+
+def issue_ceiling(blended: int, ms: float, sms: int, sm_mhz: float, inst=None) -> dict:
+    """The backward against its issue ceiling: every blended pair's method
+    minimum on fully used lanes, at one warp instruction a cycle on each of
+    the SMs' four schedulers.  inst: the kernel's warp instructions per
+    launch from an ncu record of the current source (None if stale)."""
+    rate = sms * 4 * sm_mhz * 1e6
+    model = blended * BWD_MIN_INSTR_PER_BLEND / 32.0 / rate
+    out = {"bound": "issue", "blended_px_splat": blended,
+           "min_thread_instructions_per_blend": BWD_MIN_INSTR_PER_BLEND,
+           "peak": "%d SMs x 4 schedulers x %.0f MHz (median SM clock under load), one warp "
+                   "instruction a cycle each" % (sms, sm_mhz),
+           "model_ms": model * 1e3, "frac": model / (ms * 1e-3)}
+    if inst:
+        out["warp_instructions_per_launch"] = inst
+        out["thread_instructions_per_blend"] = 32.0 * inst / max(blended, 1)
+        out["issue_frac_if_every_cycle_issued"] = (inst / rate) / (ms * 1e-3)
+    return out
 
 
 def measured_peaks():
@@ -777,6 +812,10 @@ def run_ours(args, rank: int, world: int, dist):
         "kernels": kernels, "dominant_kernel": dom,
         "roofline": roofline, "roofline_atomic": roofline_atomic,
         "bwd_hbm_atomic_roofline_frac": hbm_atomic_frac,
+        "roofline_issue": issue_ceiling(
+            blended, bwd_ms, torch.cuda.get_device_properties(dev).multi_processor_count,
+            clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0,
+            (recorded_counters("k_raster_bwd", wl.name) or {}).get("inst_executed_per_launch")),
         "kernel_rooflines": kernel_rooflines(
             kernels, args.steps, scene.n, P, HW, cand, active, blended, hbm,
             hbm_src + " (MEASURED_PEAKS.json hbm_gbs)", red_rate, scene.accum_weight,
