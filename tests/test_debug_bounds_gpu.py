@@ -91,5 +91,5 @@ def test_debug_build_reports_a_last_contrib_past_its_list(debug_lib):
 
 
 def test_normal_build_clamps_the_same_input_silently(debug_lib):
-    out = _run(STALE_LAST + "\nassert not ss.ss_debug_bounds_enabled()\n", None)
+    out = _run(textwrap.dedent(STALE_LAST) + "\nassert not ss.ss_debug_bounds_enabled()\n", None)
     assert "status 0" in out, out
