@@ -129,19 +129,27 @@ class ClockSampler:
 # ------------------------------------------------------------------ CPU oracle
 
 def cpu_description() -> dict:
-    """The host's logical CPUs and model name (for the oracle's timings)."""
-    model = None
+    """The host's logical CPUs and CPU (x86: the model name; Arm: the
+    implementer and part numbers /proc/cpuinfo lists)."""
+    fields = {}
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
                 k, _, v = line.partition(":")
-                if k.strip() in ("model name", "Model", "CPU part") and v.strip():
-                    model = v.strip()
-                    break
+                k, v = k.strip(), v.strip()
+                if k in ("model name", "CPU implementer", "CPU part") and v and k not in fields:
+                    fields[k] = v
     except OSError:
         pass
     import platform
-    return {"nproc": os.cpu_count(), "model": model or platform.processor() or platform.machine()}
+    if "model name" in fields:
+        model = fields["model name"]
+    elif "CPU part" in fields:
+        model = "%s, CPU implementer %s, CPU part %s" % (
+            platform.machine(), fields.get("CPU implementer", "?"), fields["CPU part"])
+    else:
+        model = platform.processor() or platform.machine()
+    return {"nproc": os.cpu_count(), "model": model}
 
 
 def oracle_bin_sort(scene):
