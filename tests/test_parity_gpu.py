@@ -528,3 +528,68 @@ def test_maximum_side_length(P, W, H):
     sc = _scene(W, H, 4000, seed=14, wl=3)
     r = P.full_parity(sc)
     assert r["pairs"] > 4000
+
+
+def test_both_forms_of_the_entry_points_agree(P):
+    """ss_raster_fwd (records computed in the kernel from the splats) and
+    ss_raster_fwd_records (the binning's records) give the same image, T and
+    last contributor bit for bit -- the records are the same bits; the two
+    backwards (rebuilt records and re-evaluated decisions against the
+    forward's masks) the same accumulated weight bit for bit (fixed point)
+    and the same gradients up to float-atomic ordering."""
+    import torch
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = synth.make_scene(3)
+    flags = ss.SS_ACCUM_WEIGHT
+    sp = ss.Splats.from_numpy(sc)
+    dL = torch.from_numpy(sc.dL_dimage).cuda()
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, 4 * sc.n, flags, bg=sc.bg)
+    r.bin_and_sort(sp)
+    r.forward(sp)
+    r.backward(sp, dL)
+    torch.cuda.synchronize()
+    ref = {"image": r.image.clone(), "T": r.T_final.clone(), "last": r.last_contrib.clone(),
+           "accum": r.accum_weight.clone(), **{k: v.clone() for k, v in r.grads.items()}}
+    img, T, last = torch.empty_like(r.image), torch.empty_like(r.T_final), \
+        torch.empty_like(r.last_contrib)
+    ss.ss_raster_fwd(sp, r.vals, r.tile_offsets, sc.W, sc.H, r.bg, flags, img, T, last)
+    grads = {k: torch.empty_like(v) for k, v in r.grads.items()}
+    acc = torch.empty_like(r.accum_weight)
+    ss.ss_raster_bwd(sp, r.vals, r.tile_offsets, sc.W, sc.H, r.bg, flags, T, last, dL, grads, acc,
+                     r.workspace)
+    torch.cuda.synchronize()
+    assert ss.ss_sort_status(r.workspace) == ss.SS_OK
+    assert torch.equal(img, ref["image"]) and torch.equal(T, ref["T"])
+    assert torch.equal(last, ref["last"]) and torch.equal(acc, ref["accum"])
+    for k, v in grads.items():
+        tol = max(1e-4, 1e-3 * float(ref[k].abs().max()))
+        assert float((v - ref[k]).abs().max()) <= tol, k
+
+
+def test_backward_from_the_splats_reports_a_workspace_too_small_for_its_masks(P):
+    """ss_raster_bwd learns the pair count only on the device: given a
+    workspace whose mask rows hold fewer pairs than the lists, it writes and
+    reads only inside the rows and reports SS_ERR_CAPACITY through the
+    status word (the gradients are then not valid)."""
+    import torch
+    import gaussian_splatting_differentiable_gb300 as ss
+    sc = synth.make_scene(2)
+    flags = ss.SS_ACCUM_WEIGHT
+    sp = ss.Splats.from_numpy(sc)
+    dL = torch.from_numpy(sc.dL_dimage).cuda()
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, 4 * sc.n, flags, bg=sc.bg)
+    pairs = r.bin_and_sort(sp)
+    ss.ss_raster_fwd(sp, r.vals, r.tile_offsets, sc.W, sc.H, r.bg, flags, r.image, r.T_final,
+                     r.last_contrib)
+    small = ss.ss_workspace_bytes(sc.n, pairs // 2, sc.W, sc.H)
+    ws = torch.empty(small, dtype=torch.uint8, device="cuda")
+    ws[:4].zero_()   # a clean status word (no sort ran on this buffer)
+    ss.ss_raster_bwd(sp, r.vals, r.tile_offsets, sc.W, sc.H, r.bg, flags, r.T_final,
+                     r.last_contrib, dL, r.grads, r.accum_weight, ws)
+    assert ss.ss_sort_status(ws) == ss.SS_ERR_CAPACITY
+    ws2 = torch.empty(ss.ss_workspace_bytes(sc.n, pairs, sc.W, sc.H), dtype=torch.uint8,
+                      device="cuda")
+    ws2[:4].zero_()
+    ss.ss_raster_bwd(sp, r.vals, r.tile_offsets, sc.W, sc.H, r.bg, flags, r.T_final,
+                     r.last_contrib, dL, r.grads, r.accum_weight, ws2)
+    assert ss.ss_sort_status(ws2) == ss.SS_OK
