@@ -499,7 +499,7 @@ constexpr int kBwdDynSmem = 2 * 8 * kSlots * kSlotPad * 4;
 static std::atomic<int> g_bwd_attr_set[64];   // set once per device; any thread
 static ss_status ensure_bwd_smem() {
     int dev = 0;
-    const ss_status ds = current_device(&dev, nullptr, "ss_raster_bwd: cudaGetDevice");
+    const ss_status ds = current_device(&dev, nullptr, "backward: cudaGetDevice");
     if (ds != SS_OK) return ds;
     if (dev >= 0 && dev < 64 && g_bwd_attr_set[dev].load(std::memory_order_acquire)) return SS_OK;
     const void *fns[6] = {(const void *)k_raster_bwd<true, true, false>,
@@ -512,7 +512,7 @@ static ss_status ensure_bwd_smem() {
     for (int f = 0; f < 6 && s == SS_OK; ++f)
         s = check_cuda(cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             kBwdDynSmem),
-                       "ss_raster_bwd: cudaFuncSetAttribute");
+                       "backward: cudaFuncSetAttribute");
     if (s == SS_OK && dev >= 0 && dev < 64) g_bwd_attr_set[dev].store(1, std::memory_order_release);
     return s;
 }
@@ -1043,13 +1043,13 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
         return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: unknown flag bits 0x%x", flags);
     if (flags & SS_DISTORTION)
         return fail(SS_ERR_UNSUPPORTED,
-                    "ss_raster_bwd_noalloc: SS_DISTORTION needs ss_raster_bwd");
+                    "ss_raster_bwd_noalloc: SS_DISTORTION needs ss_raster_bwd_records");
     const int32_t n = n_splats;
     if (n < 0) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: n < 0");
     if (n > kNoAllocMaxSplats)
         return fail(SS_ERR_UNSUPPORTED,
                     "ss_raster_bwd_noalloc: %d splats exceed its fixed scratch of %d splats; "
-                    "use ss_raster_bwd with a workspace",
+                    "use ss_raster_bwd_records with a workspace",
                     n, kNoAllocMaxSplats);
     if (n > 0 && !records) return fail(SS_ERR_INVALID_ARG, "ss_raster_bwd_noalloc: records is NULL");
     if (reinterpret_cast<uintptr_t>(records) & 15)

@@ -43,7 +43,7 @@ inline int tile_bits(int64_t tiles) {
 inline int sort_digits(int64_t tiles) { return (32 + tile_bits(tiles) + 7) / 8; }
 
 // Workspace layout.  The first 256 bytes hold the device status word of the
-// last sort; the rest is shared by ss_sort_pairs and ss_raster_bwd.
+// last sort; the rest is shared by ss_sort_pairs and the backward calls.
 struct WsLayout {
     size_t status_word;   // uint32, offset 0
     size_t hist;          // uint32 [ndig][256] digit counts

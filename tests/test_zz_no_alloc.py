@@ -6,7 +6,7 @@ cause, cannot give the library a workspace.  ss_raster_bwd_noalloc keeps its
 accumulated-weight scratch in a fixed array inside the library instead.
 These tests call it through the C ABI and check, within the tolerances of
 the parity tests:
-  * two calls in a row against ss_raster_bwd and against the oracle, with
+  * two calls in a row against ss_raster_bwd_records and against the oracle, with
     and without the accumulated weight (the second call also shows that the
     array's leftover contents from the first do not leak);
   * a third call on a smaller scene after the larger ones (each call clears
@@ -52,7 +52,7 @@ def _prepared(ss, sc, flags):
     r = ss.Rasterizer(sc.W, sc.H, sc.n, 4 * sc.n, flags, bg=sc.bg)
     r.bin_and_sort(sp)
     r.forward(sp)
-    r.backward(sp, dL)                # ss_raster_bwd, with a workspace
+    r.backward(sp, dL)                # ss_raster_bwd_records, with a workspace
     torch.cuda.synchronize()
     ref = {k: r.grads[k].cpu().numpy().astype(np.float64) for k in FIELDS}
     ref_w = r.accum_weight.cpu().numpy().astype(np.float64) if r.accum_weight is not None else None
