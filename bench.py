@@ -326,6 +326,24 @@ def issue_ceiling(blended: int, ms: float, sms: int, sm_mhz: float, inst=None) -
     return out
 
 
+def smem_ceiling(ms: float, sms: int, sm_mhz: float, rec) -> dict:
+    """The backward's shared-memory traffic against the wavefront peak (one
+    128-byte wavefront a cycle per SM): the design's own shared loads and
+    stores, counted by ncu on the current source (rec: the committed
+    record, None if stale), per launch over the live CUDA-event duration."""
+    out = {"bound": "shared-memory wavefronts (this kernel's own traffic, ncu)",
+           "peak": "%d SMs x one wavefront a cycle x %.0f MHz (median SM clock under load)"
+                   % (sms, sm_mhz)}
+    wf = (rec or {}).get("smem_wavefronts_per_launch")
+    if not wf:
+        out["wavefronts_per_launch"] = None
+        return out
+    rate = sms * sm_mhz * 1e6
+    out.update({"wavefronts_per_launch": wf, "model_ms": wf / rate * 1e3,
+                "frac": (wf / rate) / (ms * 1e-3)})
+    return out
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -824,6 +842,10 @@ def run_ours(args, rank: int, world: int, dist):
             blended, bwd_ms, torch.cuda.get_device_properties(dev).multi_processor_count,
             clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0,
             (recorded_counters("k_raster_bwd", wl.name) or {}).get("inst_executed_per_launch")),
+        "roofline_smem": smem_ceiling(
+            bwd_ms, torch.cuda.get_device_properties(dev).multi_processor_count,
+            clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0,
+            recorded_counters("k_raster_bwd", wl.name)),
         "kernel_rooflines": kernel_rooflines(
             kernels, args.steps, scene.n, P, HW, cand, active, blended, hbm,
             hbm_src + " (MEASURED_PEAKS.json hbm_gbs)", red_rate, scene.accum_weight,

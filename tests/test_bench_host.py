@@ -56,6 +56,20 @@ def test_kernel_rooflines_divide_the_model_by_the_measured_time():
     assert k["alu_blended"]["frac"] == pytest.approx(1e7 * 47 / lanes / 0.6e-3)
 
 
+def test_issue_and_shared_memory_ceilings_use_the_recorded_counters_only():
+    rec = {"inst_executed_per_launch": 4.0e8, "smem_wavefronts_per_launch": 1.0e8}
+    sms, mhz, ms = 100, 1000.0, 0.5
+    i = bench.issue_ceiling(10 ** 7, ms, sms, mhz, rec["inst_executed_per_launch"])
+    assert i["model_ms"] == pytest.approx(1e7 * 31 / 32 / (sms * 4 * mhz * 1e6) * 1e3)
+    assert i["issue_frac_if_every_cycle_issued"] == pytest.approx(4e8 / (sms * 4 * 1e9) / 0.5e-3)
+    m = bench.smem_ceiling(ms, sms, mhz, rec)
+    assert m["model_ms"] == pytest.approx(1e8 / (sms * 1e9) * 1e3)
+    assert m["frac"] == pytest.approx((1e8 / (sms * 1e9)) / (ms * 1e-3))
+    # a record of another source (None) gives no figure
+    assert bench.smem_ceiling(ms, sms, mhz, None)["wavefronts_per_launch"] is None
+    assert "frac" not in bench.smem_ceiling(ms, sms, mhz, None)
+
+
 def test_sort_passes_follow_the_recorded_depth_range():
     import numpy as np
     c = np.zeros(4, np.uint64)
