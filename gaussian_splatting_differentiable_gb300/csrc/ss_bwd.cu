@@ -58,12 +58,15 @@
 
 namespace ss {
 
-// 176 bytes.  Unlike the forward kernel (faster with its parameters packed
+// 168 bytes.  Unlike the forward kernel (faster with its parameters packed
 // into 128 bytes), this one measured 17 % slower in a 128-byte layout: ptxas
 // then spilled under the 3-CTA register cap.
 struct BwdParams {
     const SplatRecord *recs;
     int32_t n;
+    int32_t accum_on;           // add the accumulated weight (SS_ACCUM_WEIGHT): a runtime
+                                // switch, not a template variant -- the variant without it
+                                // spilled under the 3-CTA register cap and ran 9 % slower
     const uint32_t *vals;
     const uint32_t *offs;
     const uint32_t *masks;  // [8][n_pairs] the forward's blend decisions
@@ -145,7 +148,7 @@ struct __align__(16) SlotRec {
     float depth;
 };
 
-template <bool ACCUM, bool AOS, bool DIST>
+template <bool AOS, bool DIST>
 __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int lane, float wx0,
                                             float wy0, const float2 (*qw)[kSlotPad],
                                             const float4 *g, const float *gd1, const SlotRec *rec) {
@@ -233,7 +236,7 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
                     red_add_v2(g + 8, Wb, dz);
                 else
                     atomicAdd(g + 8, Wb);
-                if (ACCUM)
+                if (p.accum_on)
                     atomicAdd(reinterpret_cast<unsigned long long *>(g + 10),
                               (unsigned long long)__float2ull_rn(Wt * 4294967296.0f));
             }
@@ -248,13 +251,13 @@ __device__ __forceinline__ void flush_slots(const BwdParams &p, int nslots, int 
             atomicAdd(p.drgb + 3 * i, Wr);
             atomicAdd(p.drgb + 3 * i + 1, Wg);
             atomicAdd(p.drgb + 3 * i + 2, Wb);
-            if (ACCUM) atomicAdd(p.accum + i, (unsigned long long)__float2ull_rn(Wt * 4294967296.0f));
+            if (p.accum_on) atomicAdd(p.accum + i, (unsigned long long)__float2ull_rn(Wt * 4294967296.0f));
         }
     }
     __syncwarp();
 }
 
-template <bool ACCUM, bool AOS, bool DIST>
+template <bool AOS, bool DIST>
 __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     __shared__ SplatGeo s_geo_[2][256];
     __shared__ SplatGeo2 s_geo2_[2][256];
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
                 //    the others' and records the splat for the flush.
                 const int nrows = nq;
                 if (nslots + nrows > kSlots) {
-                    flush_slots<ACCUM, AOS, DIST>(p, nslots, lane, wx0, wy0, s_qw[warp],
+                    flush_slots<AOS, DIST>(p, nslots, lane, wx0, wy0, s_qw[warp],
                                                   s_g[warp], s_gd1[DIST ? warp : 0],
                                                   s_rec[warp]);
                     nslots = 0;
@@ -488,7 +491,7 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
     }
     cp_async_wait<0>();  // no copy may outlive the CTA
     if (nslots)
-        flush_slots<ACCUM, AOS, DIST>(p, nslots, lane, wx0, wy0, s_qw[warp], s_g[warp],
+        flush_slots<AOS, DIST>(p, nslots, lane, wx0, wy0, s_qw[warp], s_g[warp],
                                       s_gd1[DIST ? warp : 0], s_rec[warp]);
 }
 
@@ -502,14 +505,11 @@ static ss_status ensure_bwd_smem() {
     const ss_status ds = current_device(&dev, nullptr, "backward: cudaGetDevice");
     if (ds != SS_OK) return ds;
     if (dev >= 0 && dev < 64 && g_bwd_attr_set[dev].load(std::memory_order_acquire)) return SS_OK;
-    const void *fns[6] = {(const void *)k_raster_bwd<true, true, false>,
-                          (const void *)k_raster_bwd<false, true, false>,
-                          (const void *)k_raster_bwd<true, false, false>,
-                          (const void *)k_raster_bwd<false, false, false>,
-                          (const void *)k_raster_bwd<true, true, true>,
-                          (const void *)k_raster_bwd<false, true, true>};
+    const void *fns[3] = {(const void *)k_raster_bwd<true, false>,
+                          (const void *)k_raster_bwd<false, false>,
+                          (const void *)k_raster_bwd<true, true>};
     ss_status s = SS_OK;
-    for (int f = 0; f < 6 && s == SS_OK; ++f)
+    for (int f = 0; f < 3 && s == SS_OK; ++f)
         s = check_cuda(cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             kBwdDynSmem),
                        "backward: cudaFuncSetAttribute");
@@ -688,14 +688,12 @@ static ss_status launch_bwd(const BwdParams &p, uint32_t flags, float *accum_wei
                   k_grad_zero<<<zgrid, 256, 0, st>>>(reinterpret_cast<float4 *>(p.scratch),
                                                      3 * int64_t(p.n)));
     const int grid = tiles_x(p.W) * tiles_y(p.H);
-    if (accum && dist)
-        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, true, true><<<grid, 256, kBwdDynSmem, st>>>(p)));
-    else if (dist)
-        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, true, true><<<grid, 256, kBwdDynSmem, st>>>(p)));
-    else if (accum)
-        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, true, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
+    BwdParams q = p;
+    q.accum_on = accum;
+    if (dist)
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, true><<<grid, 256, kBwdDynSmem, st>>>(q)));
     else
-        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, true, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
+        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, false><<<grid, 256, kBwdDynSmem, st>>>(q)));
     SS_LAUNCH("k_grad_final", st,
               k_grad_final<<<zgrid, 256, 0, st>>>(p, p.n, accum ? accum_weight : nullptr));
     return check_launch(name);
@@ -1110,10 +1108,8 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     // k_bwd_zero clears this call's part of the shared array before use.
     SS_LAUNCH("k_bwd_zero", st, k_bwd_zero<<<zgrid, 256, 0, st>>>(p, n, accum));
     const int grid = tiles_x(W) * tiles_y(H);
-    if (accum)
-        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<true, false, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
-    else
-        SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, false, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
+    p.accum_on = accum;
+    SS_LAUNCH("k_raster_bwd", st, (k_raster_bwd<false, false><<<grid, 256, kBwdDynSmem, st>>>(p)));
     if (accum)
         SS_LAUNCH("k_accum_final", st, k_accum_final<<<zgrid, 256, 0, st>>>(p.accum, accum_weight, n));
     return check_launch("ss_raster_bwd_noalloc");
