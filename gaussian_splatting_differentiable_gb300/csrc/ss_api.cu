@@ -1,5 +1,6 @@
 // Shared pieces of the C ABI: error strings, constants, workspace sizing,
 // the pair-count read-back, the sort status read-back and the atomic probe.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -28,6 +29,68 @@ ss_status check_cuda(cudaError_t e, const char *what) {
 }
 
 ss_status check_launch(const char *what) { return check_cuda(cudaGetLastError(), what); }
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, found through the runtime
+// (the library links no driver library, so that it loads where no driver
+// is installed).
+using CtxGetCurrentFn = int (*)(void **);
+using CtxGetIdFn = int (*)(void *, unsigned long long *);
+
+static std::atomic<CtxGetCurrentFn> g_get_current{nullptr};
+static std::atomic<CtxGetIdFn> g_get_id{nullptr};
+
+bool context_id_ready() { return g_get_id.load(std::memory_order_acquire) != nullptr; }
+
+ss_status current_context_id(unsigned long long *id, const char *what) {
+    CtxGetCurrentFn fc = g_get_current.load(std::memory_order_acquire);
+    CtxGetIdFn fi = g_get_id.load(std::memory_order_acquire);
+    if (!fc || !fi) {
+        void *pc = nullptr, *pi = nullptr;
+        cudaDriverEntryPointQueryResult qc = cudaDriverEntryPointSymbolNotFound, qi = qc;
+        ss_status s = check_cuda(
+            cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &pc, 12000, cudaEnableDefault, &qc),
+            what);
+        if (s != SS_OK) return s;
+        s = check_cuda(
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &pi, 12000, cudaEnableDefault, &qi),
+            what);
+        if (s != SS_OK) return s;
+        if (qc != cudaDriverEntryPointSuccess || qi != cudaDriverEntryPointSuccess || !pc || !pi)
+            return fail(SS_ERR_CUDA, "%s: the driver has no cuCtxGetCurrent / cuCtxGetId", what);
+        fc = reinterpret_cast<CtxGetCurrentFn>(pc);
+        fi = reinterpret_cast<CtxGetIdFn>(pi);
+        g_get_current.store(fc, std::memory_order_release);
+        g_get_id.store(fi, std::memory_order_release);
+    }
+    void *ctx = nullptr;
+    if (fc(&ctx) != 0) return fail(SS_ERR_CUDA, "%s: cuCtxGetCurrent failed", what);
+    *id = 0;
+    if (ctx && fi(ctx, id) != 0)
+        return fail(SS_ERR_CUDA, "%s: cuCtxGetId failed", what);
+    return SS_OK;
+}
+
+ss_status ensure_dyn_smem(std::atomic<unsigned long long> *cache, const void *const *fns, int n,
+                          int bytes, const char *what) {
+    int dev = 0;
+    ss_status s = current_device(&dev, nullptr, what);
+    if (s != SS_OK) return s;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    unsigned long long id = 0;
+    s = current_context_id(&id, what);
+    if (s != SS_OK) return s;
+    if (cached && id != 0 && cache[dev].load(std::memory_order_acquire) == id) return SS_OK;
+    for (int f = 0; f < n; ++f) {
+        s = check_cuda(cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            bytes),
+                       what);
+        if (s != SS_OK) return s;
+    }
+    s = current_context_id(&id, what);   // the first CUDA call made the device's context current
+    if (s != SS_OK) return s;
+    if (cached) cache[dev].store(id, std::memory_order_release);
+    return SS_OK;
+}
 
 ss_status current_device(int *dev, int *sms, const char *what) {
     ss_status s = check_cuda(cudaGetDevice(dev), what);

@@ -498,23 +498,13 @@ __global__ void __launch_bounds__(256, 3) k_raster_bwd(BwdParams p) {
 constexpr int kBwdDynSmem = 2 * 8 * kSlots * kSlotPad * 4;
 
 // k_raster_bwd's slot buffers are dynamic shared memory on top of ~25 KB of
-// static arrays: raise its limit once per device.
-static std::atomic<int> g_bwd_attr_set[64];   // set once per device; any thread
+// static arrays: raise its limit once per CUDA context.
+static std::atomic<unsigned long long> g_bwd_smem_ctx[kMaxDevices];
 static ss_status ensure_bwd_smem() {
-    int dev = 0;
-    const ss_status ds = current_device(&dev, nullptr, "backward: cudaGetDevice");
-    if (ds != SS_OK) return ds;
-    if (dev >= 0 && dev < 64 && g_bwd_attr_set[dev].load(std::memory_order_acquire)) return SS_OK;
     const void *fns[3] = {(const void *)k_raster_bwd<true, false>,
                           (const void *)k_raster_bwd<false, false>,
                           (const void *)k_raster_bwd<true, true>};
-    ss_status s = SS_OK;
-    for (int f = 0; f < 3 && s == SS_OK; ++f)
-        s = check_cuda(cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            kBwdDynSmem),
-                       "backward: cudaFuncSetAttribute");
-    if (s == SS_OK && dev >= 0 && dev < 64) g_bwd_attr_set[dev].store(1, std::memory_order_release);
-    return s;
+    return ensure_dyn_smem(g_bwd_smem_ctx, fns, 3, kBwdDynSmem, "backward");
 }
 
 __global__ void k_bwd_zero(BwdParams p, int64_t n, bool accum) {
@@ -935,48 +925,7 @@ struct NoAllocSlot {
     unsigned long long *ptr;
 };
 static std::mutex g_noalloc_mu;
-static NoAllocSlot g_noalloc_slot[64];
-
-// The driver's cuCtxGetCurrent and cuCtxGetId, found through the runtime
-// (the library links no driver library, so that it loads where no driver
-// is installed).
-using CtxGetCurrentFn = int (*)(void **);
-using CtxGetIdFn = int (*)(void *, unsigned long long *);
-
-static std::atomic<CtxGetCurrentFn> g_get_current{nullptr};
-static std::atomic<CtxGetIdFn> g_get_id{nullptr};
-
-// The current context's id in *id (0 if no context is current yet).  The
-// first call resolves the two driver functions.
-static ss_status current_context_id(unsigned long long *id) {
-    CtxGetCurrentFn fc = g_get_current.load(std::memory_order_acquire);
-    CtxGetIdFn fi = g_get_id.load(std::memory_order_acquire);
-    if (!fc || !fi) {
-        void *pc = nullptr, *pi = nullptr;
-        cudaDriverEntryPointQueryResult qc = cudaDriverEntryPointSymbolNotFound, qi = qc;
-        ss_status s = check_cuda(
-            cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &pc, 12000, cudaEnableDefault, &qc),
-            "ss_raster_bwd_noalloc: cudaGetDriverEntryPointByVersion(cuCtxGetCurrent)");
-        if (s != SS_OK) return s;
-        s = check_cuda(
-            cudaGetDriverEntryPointByVersion("cuCtxGetId", &pi, 12000, cudaEnableDefault, &qi),
-            "ss_raster_bwd_noalloc: cudaGetDriverEntryPointByVersion(cuCtxGetId)");
-        if (s != SS_OK) return s;
-        if (qc != cudaDriverEntryPointSuccess || qi != cudaDriverEntryPointSuccess || !pc || !pi)
-            return fail(SS_ERR_CUDA, "ss_raster_bwd_noalloc: the driver has no cuCtxGetCurrent / "
-                                     "cuCtxGetId");
-        fc = reinterpret_cast<CtxGetCurrentFn>(pc);
-        fi = reinterpret_cast<CtxGetIdFn>(pi);
-        g_get_current.store(fc, std::memory_order_release);
-        g_get_id.store(fi, std::memory_order_release);
-    }
-    void *ctx = nullptr;
-    if (fc(&ctx) != 0) return fail(SS_ERR_CUDA, "ss_raster_bwd_noalloc: cuCtxGetCurrent failed");
-    *id = 0;
-    if (ctx && fi(ctx, id) != 0)
-        return fail(SS_ERR_CUDA, "ss_raster_bwd_noalloc: cuCtxGetId failed");
-    return SS_OK;
-}
+static NoAllocSlot g_noalloc_slot[kMaxDevices];
 
 // The array's address in the current context of device dev (cached; see
 // above).  While `stream` is being captured only a cached address is used:
@@ -987,12 +936,12 @@ static ss_status noalloc_scratch(int dev, cudaStream_t stream, unsigned long lon
                              "ss_raster_bwd_noalloc: cudaStreamIsCapturing");
     if (s != SS_OK) return s;
     const bool capturing = cs != cudaStreamCaptureStatusNone;
-    if (capturing && !g_get_id.load(std::memory_order_acquire))
+    if (capturing && !context_id_ready())
         return fail(SS_ERR_UNSUPPORTED,
                     "ss_raster_bwd_noalloc: first call while the stream is being captured; make "
                     "one call on this device before capturing");
     unsigned long long id = 0;
-    s = current_context_id(&id);
+    s = current_context_id(&id, "ss_raster_bwd_noalloc");
     if (s != SS_OK) return s;
     {
         std::lock_guard<std::mutex> lk(g_noalloc_mu);
@@ -1009,7 +958,8 @@ static ss_status noalloc_scratch(int dev, cudaStream_t stream, unsigned long lon
     s = check_cuda(cudaGetSymbolAddress(&ptr, g_noalloc_accum),
                    "ss_raster_bwd_noalloc: cudaGetSymbolAddress");
     if (s != SS_OK) return s;
-    s = current_context_id(&id);   // the lookup made the device's context current if it was not
+    s = current_context_id(&id, "ss_raster_bwd_noalloc");   // the lookup made the device's
+                                                             // context current if it was not
     if (s != SS_OK) return s;
     {
         std::lock_guard<std::mutex> lk(g_noalloc_mu);
@@ -1071,8 +1021,8 @@ extern "C" ss_status ss_raster_bwd_noalloc(const void *records, int32_t n_splats
     int dev = 0, sms = 0;
     ss_status s = check_cuda(cudaGetDevice(&dev), "ss_raster_bwd_noalloc: cudaGetDevice");
     if (s != SS_OK) return s;
-    if (dev < 0 || dev >= 64)
-        return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd_noalloc: device %d >= 64", dev);
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(SS_ERR_UNSUPPORTED, "ss_raster_bwd_noalloc: device %d >= %d", dev, kMaxDevices);
     unsigned long long *scratch = nullptr;
     if (accum) {
         s = noalloc_scratch(dev, (cudaStream_t)stream, &scratch);

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -28,6 +29,21 @@ ss_status check_launch(const char *what);
 ss_status check_cuda(cudaError_t e, const char *what);
 // The current device and its SM count (an error status if either query fails).
 ss_status current_device(int *dev, int *sms, const char *what);
+// The current CUDA context's process-unique id in *id (0 if no context is
+// current yet), through the driver's cuCtxGetCurrent / cuCtxGetId; the first
+// call resolves those two functions.
+ss_status current_context_id(unsigned long long *id, const char *what);
+// True once current_context_id has resolved the driver functions.
+bool context_id_ready();
+// Per-device caches of per-context settings cover devices [0, kMaxDevices).
+constexpr int kMaxDevices = 64;
+// Raises the dynamic shared-memory limit of the kernels fns[0, n) to
+// `bytes`, once per CUDA context: cache[dev] holds the id of the context in
+// which that was done, so a new context on the device (the primary context
+// re-created after cudaDeviceReset, or a driver-API context made current)
+// sets it again.  Devices past kMaxDevices set it on every call.
+ss_status ensure_dyn_smem(std::atomic<unsigned long long> *cache, const void *const *fns, int n,
+                          int bytes, const char *what);
 
 inline int32_t tiles_x(int32_t W) { return (W + kTile - 1) / kTile; }
 inline int32_t tiles_y(int32_t H) { return (H + kTile - 1) / kTile; }

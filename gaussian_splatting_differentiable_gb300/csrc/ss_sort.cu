@@ -591,20 +591,13 @@ __global__ void __launch_bounds__(256) k_sort_ties(uint64_t *dk, uint32_t *dv, u
     }
 }
 
-static std::atomic<int> g_attr_set[64];   // set once per device; any thread
+static std::atomic<unsigned long long> g_pass_smem_ctx[kMaxDevices];
 
 // k_sort_pass needs 48 KB of dynamic shared memory (32 KB when packed) on
-// top of its static arrays: raise its limit once per device.
+// top of its static arrays: raise its limit once per CUDA context.
 static ss_status ensure_pass_smem(int dyn) {
-    int dev = 0;
-    const ss_status ds = current_device(&dev, nullptr, "ss_sort_pairs: cudaGetDevice");
-    if (ds != SS_OK) return ds;
-    if (dev >= 0 && dev < 64 && g_attr_set[dev].load(std::memory_order_acquire)) return SS_OK;
-    ss_status s = check_cuda(
-        cudaFuncSetAttribute(k_sort_pass, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn),
-        "ss_sort_pairs: cudaFuncSetAttribute");
-    if (s == SS_OK && dev >= 0 && dev < 64) g_attr_set[dev].store(1, std::memory_order_release);
-    return s;
+    const void *fn = (const void *)k_sort_pass;
+    return ensure_dyn_smem(g_pass_smem_ctx, &fn, 1, dyn, "ss_sort_pairs");
 }
 
 __global__ void k_set_u32(uint32_t *p, uint32_t v) { *p = v; }

@@ -299,17 +299,10 @@ extern "C" ss_status ss_ssim_loss(const float *img, const float *target, int32_t
     if (workspace_bytes < need)
         return fail(SS_ERR_INVALID_ARG, "ss_ssim_loss: workspace %zu bytes < %zu", workspace_bytes,
                     need);
-    static bool attr_set[64] = {};
-    int dev = 0;
-    ss_status st = check_cuda(cudaGetDevice(&dev), "ss_ssim_loss: cudaGetDevice");
+    static std::atomic<unsigned long long> smem_ctx[kMaxDevices];   // see ensure_dyn_smem
+    const void *fn = (const void *)k_ssim;
+    ss_status st = ensure_dyn_smem(smem_ctx, &fn, 1, int(sizeof(SsimSmem)), "ss_ssim_loss");
     if (st != SS_OK) return st;
-    if (dev < 64 && !attr_set[dev]) {
-        st = check_cuda(cudaFuncSetAttribute(k_ssim, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(sizeof(SsimSmem))),
-                        "ss_ssim_loss: cudaFuncSetAttribute");
-        if (st != SS_OK) return st;
-        attr_set[dev] = true;
-    }
     SsimParams p{};
     p.img = img, p.tgt = target, p.grad = dL_dimg;
     p.partial = static_cast<double2 *>(workspace);
