@@ -51,7 +51,8 @@ def _tolerances(sc, ofw, idx):
     a = np.abs(p[:, None, :] * R[None, :, :]).sum(2) + np.abs(t)      # [n][3]
     z = np.where(ofw["valid"], ofw["depth"], 1.0)
     pc = ofw["pc"]
-    xz, yz = np.abs(pc[:, 0] / pc[:, 2]), np.abs(pc[:, 1] / pc[:, 2])
+    pz = np.where(ofw["valid"], pc[:, 2], 1.0)   # culled splats (z may be 0) are not compared
+    xz, yz = np.abs(pc[:, 0] / pz), np.abs(pc[:, 1] / pz)
     Eu = sc.cam.fx * (a[:, 0] + xz * a[:, 2]) / np.abs(z) + abs(sc.cam.cx)
     Ev = sc.cam.fy * (a[:, 1] + yz * a[:, 2]) / np.abs(z) + abs(sc.cam.cy)
     cov2 = np.where(ofw["valid"][:, None, None], np.nan_to_num(ofw["cov2"]), np.eye(2))
