@@ -35,8 +35,13 @@ METRIC = "rasterize_bwd ms/call and splat-pixel pairs/s at 2M splats 1237×822; 
 UNIT = "splat-px pairs/s"
 WORKLOAD = 4
 L2_FLUSH_BYTES = 256 << 20
-BWD_SOURCES = ("gaussian_splatting_differentiable_gb300/csrc/ss_bwd.cu",
-               "gaussian_splatting_differentiable_gb300/csrc/ss_device.cuh")
+# The backward kernel's source, as the committed ncu counters are tied to it:
+# ss_bwd.cu up to the end of k_raster_bwd (the line defining kBwdDynSmem; the
+# launch code and the other kernels of the file follow it), and the headers
+# it compiles with.
+BWD_SOURCES = (("gaussian_splatting_differentiable_gb300/csrc/ss_bwd.cu", "constexpr int kBwdDynSmem"),
+               ("gaussian_splatting_differentiable_gb300/csrc/ss_device.cuh", None),
+               ("gaussian_splatting_differentiable_gb300/csrc/ss_internal.h", None))
 
 
 def parse():
@@ -266,11 +271,17 @@ def job_value(world: int, units_per_rank: float, ms: float) -> float:
     return world * units_per_rank / (ms * 1e-3)
 
 
-def source_sha(paths) -> str:
+def source_sha(sources) -> str:
+    """Hash of (path, end) pairs: each file up to and including the line
+    that holds `end` (the whole file when end is None)."""
     h = hashlib.sha256()
-    for p in paths:
+    for p, end in sources:
         with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+            data = f.read()
+        if end is not None:
+            i = data.index(end.encode())
+            data = data[:data.index(b"\n", i) + 1]
+        h.update(data)
     return h.hexdigest()[:16]
 
 
@@ -478,6 +489,63 @@ def measure_distortion(ss, dev, flush, steps: int, workload: int = 6, extra_flag
     r.check()
     return {"workload": synth.WORKLOADS[workload].name, "flags": label,
             "ms_per_step": statistics.mean(a.elapsed_time(b) for a, b in ev),
+            "kernels_ms_per_call": {k: v[1] / v[0] for k, v in prof.items()}}
+
+
+def measure_splat_entry_points(ss, dev, flush, steps: int, workload: int = 4) -> dict:
+    """The boundary's entry points that take the splats themselves
+    (ss_raster_fwd: records computed per batch in the kernel, no blend masks;
+    ss_raster_bwd: records rebuilt and blend decisions re-evaluated in its
+    workspace) on the 2M-splat scene, each call timed alone with CUDA events
+    after an L2 flush; per-kernel times from a second, profiled pass."""
+    import torch
+    import synth
+    sc = synth.make_scene(workload)
+    flags = ss.SS_ACCUM_WEIGHT
+    sp = ss.Splats.from_numpy(sc, dev)
+    dL = torch.from_numpy(sc.dL_dimage).to(dev).contiguous()
+    r = ss.Rasterizer(sc.W, sc.H, sc.n, int(2.5 * sc.n), flags, bg=sc.bg, device=dev)
+    r.bin_and_sort(sp)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        ss.ss_raster_fwd(sp, r.vals, r.tile_offsets, sc.W, sc.H, r.bg, flags, r.image,
+                         r.T_final, r.last_contrib, r.median_depth)
+
+    def bwd():
+        ss.ss_raster_bwd(sp, r.vals, r.tile_offsets, sc.W, sc.H, r.bg, flags, r.T_final,
+                         r.last_contrib, dL, r.grads, r.accum_weight, r.workspace)
+
+    for _ in range(3):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    times = {"fwd": [], "bwd": []}
+    for k in range(steps):
+        for name, fn in (("fwd", fwd), ("bwd", bwd)):
+            flush.fill_(float(k))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            times[name].append((e0, e1))
+    torch.cuda.synchronize()
+    ss.ss_profile_collect()
+    ss.ss_profile_enable(True)
+    for k in range(steps):
+        flush.fill_(float(k))
+        fwd()
+        flush.fill_(float(k))
+        bwd()
+    torch.cuda.synchronize()
+    ss.ss_profile_enable(False)
+    prof = ss.ss_profile_collect()
+    st = ss.ss_sort_status(r.workspace)
+    if st != 0:
+        raise RuntimeError("ss_raster_bwd reported status %d" % st)
+    return {"workload": synth.WORKLOADS[workload].name, "flags": "accum_weight",
+            "ss_raster_fwd_ms_per_call": statistics.mean(a.elapsed_time(b) for a, b in times["fwd"]),
+            "ss_raster_bwd_ms_per_call": statistics.mean(a.elapsed_time(b) for a, b in times["bwd"]),
             "kernels_ms_per_call": {k: v[1] / v[0] for k, v in prof.items()}}
 
 
@@ -732,6 +800,8 @@ def run_ours(args, rank: int, world: int, dist):
         next_rows["dense_blobs"] = measure_distortion(
             ss, dev, flush, args.steps, workload=5, extra_flags=ss.SS_MEDIAN_DEPTH,
             label="accum_weight + median depth, 30 % of the splats in four dense blobs")
+        # the boundary's splat-taking forms (not the training step's path)
+        next_rows["b_splat_entry_points"] = measure_splat_entry_points(ss, dev, flush, args.steps)
 
     # --- end to end through the public API with host buffers
     e2e = None

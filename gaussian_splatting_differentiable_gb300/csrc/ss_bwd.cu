@@ -591,15 +591,17 @@ struct MaskParams {
 // backward given none: a pixel blended list position j of its tile iff
 // j < last_contrib and e2 >= thr (the forward blends every splat it does
 // not skip until it stops, and last_contrib is its last blend), with e2 the
-// same eval_e2 of the same record bits.  One CTA per tile; each warp takes
-// its 8x4 block, box-culls a batch of 256 staged records and evaluates the
-// rest, and writes the masks the backward reads, masks[warp][position].
-// A list longer than the mask rows (offsets[tiles] > stride) is recorded in
-// the status word and its masks are not written past the rows.
+// same eval_e2 of the same record bits.  One CTA per tile; batches of 256
+// records are staged front to back with cp.async into two buffers (the next
+// batch copies while this one is evaluated); each warp takes its 8x4 block,
+// box-culls the batch and evaluates the rest, and writes the masks the
+// backward reads, masks[warp][position].  A list longer than the mask rows
+// (offsets[tiles] > stride) is recorded in the status word and its masks are
+// not written past the rows.
 __global__ void __launch_bounds__(256) k_blend_masks(MaskParams p) {
-    __shared__ SplatGeo s_geo[256];
-    __shared__ float2 s_ct[256];    // (C, thr)
-    __shared__ SplatBox s_box[256];
+    __shared__ SplatGeo s_geo[2][256];
+    __shared__ SplatGeo2 s_geo2[2][256];
+    __shared__ SplatBox s_box[2][256];
     __shared__ uint32_t s_wmax[8];
     const int tile = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -622,23 +624,47 @@ __global__ void __launch_bounds__(256) k_blend_masks(MaskParams p) {
     uint32_t bmax = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) bmax = max(bmax, s_wmax[w]);
-    for (uint32_t base = 0; base < bmax; base += 256) {
-        const int nb = int(min(256u, bmax - base));
-        __syncthreads();   // the previous batch is done everywhere
-        if (tid < nb) {
-            const uint32_t idx = p.vals[start + base + tid];
-            const SplatRecord r = idx < uint32_t(p.n) ? p.recs[idx] : invisible_record();
-            s_geo[tid] = r.geo;
-            s_ct[tid] = make_float2(r.geo2.C, r.geo2.thr);
-            s_box[tid] = r.box;
+
+    // Record idx into slot t of buffer b (the invisible record past n).
+    auto stage = [&](uint32_t idx, int b, int t) {
+        if (idx < uint32_t(p.n)) {
+            const SplatRecord *r = p.recs + idx;
+            cp_async16(&s_geo[b][t], &r->geo);
+            cp_async16(&s_geo2[b][t], &r->geo2);
+            cp_async16(&s_box[b][t], &r->box);
+        } else {
+            const SplatRecord r = invisible_record();
+            s_geo[b][t] = r.geo;
+            s_geo2[b][t] = r.geo2;
+            s_box[b][t] = r.box;
         }
-        __syncthreads();
+    };
+    // Batch b covers positions [256 b, min(bmax, 256 (b + 1))) of the list.
+    if (bmax > 0) {
+        if (uint32_t(tid) < bmax) stage(p.vals[start + tid], 0, tid);
+        cp_async_commit();
+    }
+    uint32_t next_idx = 256u + uint32_t(tid) < bmax ? p.vals[start + 256u + tid] : 0u;
+    int buf = 0;
+    for (uint32_t base = 0; base < bmax; base += 256, buf ^= 1) {
+        cp_async_wait<0>();
+        __syncthreads();   // batch staged everywhere; nobody still reads the other buffer
+        const uint32_t nbase = base + 256;
+        if (nbase < bmax) {
+            if (nbase + uint32_t(tid) < bmax) stage(next_idx, buf ^ 1, tid);
+            cp_async_commit();
+            next_idx = nbase + 256u + uint32_t(tid) < bmax ? p.vals[start + nbase + 256u + tid] : 0u;
+        }
+        const int nb = int(min(256u, bmax - base));
         if (base >= wmax) continue;   // warp-uniform: no pixel of this block reaches the batch
+        const SplatGeo *geo = s_geo[buf];
+        const SplatGeo2 *geo2 = s_geo2[buf];
+        const SplatBox *box = s_box[buf];
         for (int q = 0; q < 8 && q * 32 < nb; ++q) {
             const int j = q * 32 + lane;
             bool hit = false;
             if (j < nb && base + uint32_t(j) < wmax) {
-                const SplatBox b = s_box[j];
+                const SplatBox b = box[j];
                 hit = b.x0 <= wx1 && b.x1 >= wx0 && b.y0 <= wy1 && b.y1 >= wy0;
             }
             uint32_t m = __ballot_sync(0xffffffffu, hit), mine = 0;
@@ -647,9 +673,9 @@ __global__ void __launch_bounds__(256) k_blend_masks(MaskParams p) {
                 m &= m - 1;
                 const int jj = q * 32 + k;
                 float dx, dy;
-                const float e2 = eval_e2(s_geo[jj], s_ct[jj].x, px, py, dx, dy);
+                const float e2 = eval_e2(geo[jj], geo2[jj].C, px, py, dx, dy);
                 const uint32_t bm = __ballot_sync(0xffffffffu,
-                                                  base + uint32_t(jj) < n_p && e2 >= s_ct[jj].y);
+                                                  base + uint32_t(jj) < n_p && e2 >= geo2[jj].thr);
                 if (lane == k) mine = bm;
             }
             if (j < nb) {
@@ -658,6 +684,7 @@ __global__ void __launch_bounds__(256) k_blend_masks(MaskParams p) {
             }
         }
     }
+    cp_async_wait<0>();  // no copy may outlive the CTA
 }
 
 // The gradient launches shared by both backward entry points: clear the
