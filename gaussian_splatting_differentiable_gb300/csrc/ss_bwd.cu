@@ -667,16 +667,24 @@ __global__ void __launch_bounds__(256) k_blend_masks(MaskParams p) {
                 const SplatBox b = box[j];
                 hit = b.x0 <= wx1 && b.x1 >= wx0 && b.y0 <= wy1 && b.y1 >= wy0;
             }
+            // The listed entries two at a time (independent evaluations; a
+            // lone last one is evaluated twice): lane k keeps entry k's mask.
             uint32_t m = __ballot_sync(0xffffffffu, hit), mine = 0;
             while (m) {
-                const int k = __ffs(m) - 1;
+                const int k0 = __ffs(m) - 1;
                 m &= m - 1;
-                const int jj = q * 32 + k;
+                const int k1 = m ? __ffs(m) - 1 : k0;
+                m &= m - 1;
+                const int j0 = q * 32 + k0, j1 = q * 32 + k1;
                 float dx, dy;
-                const float e2 = eval_e2(geo[jj], geo2[jj].C, px, py, dx, dy);
-                const uint32_t bm = __ballot_sync(0xffffffffu,
-                                                  base + uint32_t(jj) < n_p && e2 >= geo2[jj].thr);
-                if (lane == k) mine = bm;
+                const float e0 = eval_e2(geo[j0], geo2[j0].C, px, py, dx, dy);
+                const float e1 = eval_e2(geo[j1], geo2[j1].C, px, py, dx, dy);
+                const uint32_t b0 = __ballot_sync(0xffffffffu,
+                                                  base + uint32_t(j0) < n_p && e0 >= geo2[j0].thr);
+                const uint32_t b1 = __ballot_sync(0xffffffffu,
+                                                  base + uint32_t(j1) < n_p && e1 >= geo2[j1].thr);
+                if (lane == k0) mine = b0;
+                if (lane == k1) mine = b1;
             }
             if (j < nb) {
                 const int64_t pos = int64_t(start) + base + j;
