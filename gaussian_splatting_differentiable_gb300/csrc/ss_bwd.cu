@@ -562,8 +562,10 @@ __global__ void k_accum_final(const unsigned long long *acc, float *out, int64_t
 }
 
 // Records of the splats from the SoA inputs: what the binning writes, bit
-// for bit (record_of), for the backward that takes the splats themselves.
-__global__ void k_make_records(SplatPtrs s, int32_t tiles_x, int32_t tiles_y, SplatRecord *out) {
+// for bit (record_of), for the backward that takes the splats themselves;
+// the same pass clears each splat's 48-byte gradient record (clear[3 i ..]).
+__global__ void k_make_records(SplatPtrs s, int32_t tiles_x, int32_t tiles_y, SplatRecord *out,
+                               float4 *clear) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < s.n; i += stride) {
         const SplatRecord r = record_of(s, uint32_t(i), tiles_x, tiles_y);
@@ -572,6 +574,10 @@ __global__ void k_make_records(SplatPtrs s, int32_t tiles_x, int32_t tiles_y, Sp
         dst[1] = *reinterpret_cast<const float4 *>(&r.geo2);
         dst[2] = *reinterpret_cast<const float4 *>(&r.col);
         dst[3] = *reinterpret_cast<const float4 *>(&r.box);
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        clear[3 * i] = z;
+        clear[3 * i + 1] = z;
+        clear[3 * i + 2] = z;
     }
 }
 
@@ -897,7 +903,8 @@ extern "C" ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals
     const int64_t want = (int64_t(n) + 255) / 256;
     const int rgrid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
     SS_LAUNCH("k_make_records", st,
-              k_make_records<<<rgrid, 256, 0, st>>>(sp, tiles_x(W), tiles_y(H), recs));
+              k_make_records<<<rgrid, 256, 0, st>>>(sp, tiles_x(W), tiles_y(H), recs,
+                                                    reinterpret_cast<float4 *>(ws + L.accum)));
     s = check_launch(name);
     if (s != SS_OK) return s;
     uint32_t *masks = reinterpret_cast<uint32_t *>(ws + L.masks);
@@ -924,7 +931,8 @@ extern "C" ss_status ss_raster_bwd(const ss_splats *splats, const uint32_t *vals
     p.drgb = grads->drgb;
     p.ddepth = nullptr;
     p.scratch = reinterpret_cast<float *>(ws + L.accum);
-    return launch_bwd(p, flags & SS_ACCUM_WEIGHT, accum_weight, st, name);
+    // k_make_records cleared the gradient records
+    return launch_bwd(p, (flags & SS_ACCUM_WEIGHT) | SS_RECORDS_CLEARED, accum_weight, st, name);
 }
 
 // ---------------------------------------------------------------------------
