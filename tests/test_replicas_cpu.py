@@ -56,3 +56,24 @@ def test_single_process_is_unchanged():
     import bench
     assert bench.max_over_ranks(1.25, None, "cpu") == 1.25
     assert bench.job_value(1, 500.0, 2.0) == pytest.approx(2.5e5)
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
+    """The launch the harness uses for N > 1 (torch.distributed.run, one
+    process per rank, 127.0.0.1 rendezvous), here for the reference arm on the
+    CPU: rank 0 times the oracle and prints the one JSON line, the other rank
+    exits 0 without output."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--workload", "1", "--steps", "3",
+           "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 3
